@@ -1,0 +1,214 @@
+"""CPU oracle for the batch-invariant mHC pre "H Aggregate" (forward and backward).
+
+TEST INFRASTRUCTURE ONLY.  The arithmetic lives in ``mhc_oracle.c`` (plain C11,
+``-O2 -ffp-contract=off``, no fast math); this module compiles it with the host
+``gcc`` and marshals numpy arrays through ``ctypes``.  Only the tests, the
+package smoke check and the benchmark's CPU-baseline leg may import it; the
+product path never does.  It shares no code with the CUDA library.
+
+BF16 data is carried as ``numpy.uint16`` bit patterns.  Shapes follow the
+"Add batch-invariant h_aggregate kernel" page (Summary): residual ``[T,4,H]``
+BF16, pre ``[T,4]`` FP32, out ``[T,H]`` BF16; the backward adds g ``[T,H]``
+BF16, grad_residual ``[T,4,H]`` BF16 and grad_pre ``[T,4]`` FP32.
+
+Parity status of each function (what pins it, from the oracle pin tests):
+  * bf16_from_float / float_from_bf16: exhaustive round trip, hand tie cases,
+    agreement with torch's CPU conversion.
+  * fwd: hand-worked examples (tree order, no FMA), exact-rational emulation,
+    FP64 error bound, one-hot / zero / symmetry / scaling invariants.
+  * grad_residual: hand-worked double-rounding examples, exact-rational
+    emulation, identity and one-hot invariants.
+  * grad_pre: integer-valued exact sums, FP64 error bound, hand-worked sparse
+    cases that fix every level of the ORDER-256 tree.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mhc_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libmhc_oracle.so")
+
+#: Compiler flags.  ``-ffp-contract=off`` stops GCC from fusing a multiply and
+#: an add into an FMA (GCC's default on aarch64); ISO C11 mode also keeps the
+#: GNU extensions that relax float semantics off.
+CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+          "-Wall", "-Wextra", "-Werror"]
+
+_lock = threading.Lock()
+_default = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def compile_library(src: str, out: str, extra_flags=()) -> str:
+    """Compile an oracle C source into a shared library at ``out`` (atomic replace)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=os.path.dirname(out))
+    os.close(fd)
+    try:
+        subprocess.run(["gcc", *CFLAGS, *extra_flags, "-o", tmp, src], check=True,
+                       capture_output=True, text=True)
+        os.replace(tmp, out)
+    except subprocess.CalledProcessError as e:
+        raise RuntimeError(f"oracle build failed:\n{e.stderr}") from e
+    finally:
+        if os.path.exists(tmp):
+            os.unlink(tmp)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library if it is missing or older than its source."""
+    with _lock:
+        stale = (not os.path.exists(_LIB_PATH)
+                 or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+        if force or stale:
+            compile_library(_SRC, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _as(a, dtype) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    return np.ascontiguousarray(a)
+
+
+def _shape_TH(residual: np.ndarray) -> tuple[int, int]:
+    if residual.ndim != 3 or residual.shape[1] != 4:
+        raise ValueError(f"residual must be [T,4,H], got {residual.shape}")
+    return int(residual.shape[0]), int(residual.shape[2])
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        p = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        lib.oracle_float_from_bf16.argtypes = [ctypes.c_uint16]
+        lib.oracle_float_from_bf16.restype = ctypes.c_float
+        lib.oracle_bf16_from_float.argtypes = [ctypes.c_float]
+        lib.oracle_bf16_from_float.restype = ctypes.c_uint16
+        for name in ("oracle_bf16_from_float_array", "oracle_float_from_bf16_array"):
+            getattr(lib, name).argtypes = [p, p, i64]
+            getattr(lib, name).restype = None
+        lib.oracle_h_aggregate_fwd.argtypes = [p, p, p, i64, i64]
+        lib.oracle_h_aggregate_fwd.restype = None
+        lib.oracle_h_aggregate_bwd_grad_residual.argtypes = [p, p, p, i64, i64]
+        lib.oracle_h_aggregate_bwd_grad_residual.restype = None
+        lib.oracle_h_aggregate_bwd_grad_pre.argtypes = [p, p, p, i64, i64]
+        lib.oracle_h_aggregate_bwd_grad_pre.restype = None
+        lib.oracle_h_aggregate_bwd.argtypes = [p, p, p, p, p, i64, i64]
+        lib.oracle_h_aggregate_bwd.restype = None
+        self.lib = lib
+        self.path = lib_path
+
+    def bf16_from_float(self, x) -> np.ndarray:
+        """Round float32 values to BF16 (RNE); returns uint16 patterns."""
+        x = _as(x, np.float32)
+        y = np.empty(x.shape, dtype=np.uint16)
+        self.lib.oracle_bf16_from_float_array(_ptr(x), _ptr(y), x.size)
+        return y
+
+    def float_from_bf16(self, x) -> np.ndarray:
+        """Widen BF16 patterns (uint16) to float32 exactly."""
+        x = _as(x, np.uint16)
+        y = np.empty(x.shape, dtype=np.float32)
+        self.lib.oracle_float_from_bf16_array(_ptr(x), _ptr(y), x.size)
+        return y
+
+    def fwd(self, residual, pre) -> np.ndarray:
+        """out[t,h] = bf16((pre0*r0 + pre1*r1) + (pre2*r2 + pre3*r3)); uint16 [T,H]."""
+        residual = _as(residual, np.uint16)
+        pre = _as(pre, np.float32)
+        T, H = _shape_TH(residual)
+        if pre.shape != (T, 4):
+            raise ValueError(f"pre must be [{T},4], got {pre.shape}")
+        out = np.empty((T, H), dtype=np.uint16)
+        self.lib.oracle_h_aggregate_fwd(_ptr(residual), _ptr(pre), _ptr(out), T, H)
+        return out
+
+    def grad_residual(self, g, pre) -> np.ndarray:
+        """grad_residual[t,k,h] = bf16(fp32(pre[t,k] * g[t,h])); uint16 [T,4,H]."""
+        g = _as(g, np.uint16)
+        pre = _as(pre, np.float32)
+        T, H = g.shape
+        if pre.shape != (T, 4):
+            raise ValueError(f"pre must be [{T},4], got {pre.shape}")
+        out = np.empty((T, 4, H), dtype=np.uint16)
+        self.lib.oracle_h_aggregate_bwd_grad_residual(_ptr(g), _ptr(pre), _ptr(out), T, H)
+        return out
+
+    def grad_pre(self, g, residual) -> np.ndarray:
+        """grad_pre[t,k] = sum_h g[t,h]*r[t,k,h] in FP32, ORDER-256; float32 [T,4]."""
+        g = _as(g, np.uint16)
+        residual = _as(residual, np.uint16)
+        T, H = _shape_TH(residual)
+        if g.shape != (T, H):
+            raise ValueError(f"g must be [{T},{H}], got {g.shape}")
+        out = np.empty((T, 4), dtype=np.float32)
+        self.lib.oracle_h_aggregate_bwd_grad_pre(_ptr(g), _ptr(residual), _ptr(out), T, H)
+        return out
+
+    def bwd(self, g, residual, pre) -> tuple[np.ndarray, np.ndarray]:
+        """(grad_residual uint16 [T,4,H], grad_pre float32 [T,4])."""
+        g = _as(g, np.uint16)
+        residual = _as(residual, np.uint16)
+        pre = _as(pre, np.float32)
+        T, H = _shape_TH(residual)
+        if g.shape != (T, H) or pre.shape != (T, 4):
+            raise ValueError("shape mismatch between g, residual and pre")
+        gr = np.empty((T, 4, H), dtype=np.uint16)
+        gp = np.empty((T, 4), dtype=np.float32)
+        self.lib.oracle_h_aggregate_bwd(_ptr(g), _ptr(residual), _ptr(pre), _ptr(gr), _ptr(gp),
+                                        T, H)
+        return gr, gp
+
+
+def default() -> Oracle:
+    """The oracle built from ``mhc_oracle.c`` beside this file."""
+    global _default
+    if _default is None:
+        _default = Oracle(build())
+    return _default
+
+
+def bf16_from_float(x):
+    return default().bf16_from_float(x)
+
+
+def float_from_bf16(x):
+    return default().float_from_bf16(x)
+
+
+def fwd(residual, pre):
+    return default().fwd(residual, pre)
+
+
+def grad_residual(g, pre):
+    return default().grad_residual(g, pre)
+
+
+def grad_pre(g, residual):
+    return default().grad_pre(g, residual)
+
+
+def bwd(g, residual, pre):
+    return default().bwd(g, residual, pre)

@@ -1,0 +1,422 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each ``check_*`` function takes an ``oracle.Oracle`` and raises
+``AssertionError`` when the oracle disagrees with a hand-worked value from
+``tests/golden``, an independent library routine, exact rational arithmetic, a
+closed-form error bound or an exact invariant.  ``test_oracle_pins.py`` runs
+them on the real oracle; ``test_oracle_mutants.py`` runs them on copies of the
+oracle with planted mistakes and expects every mistake to be caught.
+
+Sources: "Add batch-invariant h_aggregate kernel" (Summary formula, Batch
+invariance rules) for the forward; the same page's reviewer request for the
+backward, whose formula here is the derivative of the Summary formula.
+"""
+
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+U = 2.0 ** -24  # unit roundoff of binary32
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+
+def golden_rows(name: str):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield line.split()
+
+
+def f32_from_bits(u: int) -> np.float32:
+    return np.array([u], dtype=np.uint32).view(np.float32)[0]
+
+
+def f32_bits(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float32).view(np.uint32)
+
+
+def bf16_widen(u16: np.ndarray) -> np.ndarray:
+    """BF16 patterns -> float32, by shifting into the upper half (independent of the oracle)."""
+    return (np.asarray(u16, dtype=np.uint32) << 16).view(np.float32)
+
+
+def round_rne(x: Fraction, p: int, emin: int = -126, emax: int = 127) -> float:
+    """Round a rational to a binary format with p significant bits, exponent range
+    [emin, emax], ties to even, subnormals kept, overflow to infinity.  The result
+    is returned as a Python float (exact for binary32 and BF16 values)."""
+    if x == 0:
+        return 0.0
+    sign = -1.0 if x < 0 else 1.0
+    a = abs(x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    elif Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, emin)
+    quantum = Fraction(2) ** (e - p + 1)
+    m = a / quantum
+    fl = m.numerator // m.denominator
+    rem = m - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    r = fl * quantum
+    if r >= Fraction(2) ** (emax + 1):
+        return sign * math.inf
+    return sign * float(r)
+
+
+def exact_mul(a: float, b: float) -> float:
+    """One binary32 multiply, rounded to nearest even, by exact rationals."""
+    if a == 0.0 or b == 0.0:
+        return math.copysign(0.0, math.copysign(1.0, a) * math.copysign(1.0, b))
+    return round_rne(Fraction(a) * Fraction(b), 24)
+
+
+def exact_add(a: float, b: float) -> float:
+    """One binary32 add, rounded to nearest even, by exact rationals (IEEE zero signs)."""
+    if math.isinf(a) or math.isinf(b):
+        return a + b
+    s = Fraction(a) + Fraction(b)
+    if s == 0:
+        both_neg = math.copysign(1.0, a) < 0 and math.copysign(1.0, b) < 0
+        return -0.0 if both_neg else 0.0
+    return round_rne(s, 24)
+
+
+def to_bf16_exact(x: float) -> float:
+    if math.isinf(x) or x == 0.0:
+        return x
+    return round_rne(Fraction(x), 8)
+
+
+def bf16_bits_of(x: float) -> int:
+    return int(np.array([x], dtype=np.float32).view(np.uint32)[0] >> 16)
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of BF16 values at |x| (8 significant bits), for finite x."""
+    ax = np.abs(x.astype(np.float64))
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    e = np.maximum(e, -126)
+    return np.ldexp(1.0, (e - 7).astype(np.int64))
+
+
+def random_bf16(rng, shape, scale=1.0) -> np.ndarray:
+    x = (rng.standard_normal(shape) * scale).astype(np.float32)
+    bits = x.view(np.uint32)
+    # truncate-and-round by numpy integer arithmetic on the pattern (test-local RNE)
+    kept = bits >> 16
+    dropped = bits & 0xFFFF
+    up = (dropped > 0x8000) | ((dropped == 0x8000) & ((kept & 1) == 1))
+    return (kept + up).astype(np.uint16)
+
+
+# --------------------------------------------------------------------------
+# BF16 conversion
+# --------------------------------------------------------------------------
+
+def check_bf16_golden(o):
+    for fbits, bbits, *_ in golden_rows("bf16_rounding.txt"):
+        x = f32_from_bits(int(fbits, 16))
+        got = int(o.bf16_from_float(np.array([x], dtype=np.float32))[0])
+        assert got == int(bbits, 16), f"bf16({fbits}) = {got:04X}, expected {bbits}"
+
+
+def check_bf16_roundtrip_exhaustive(o):
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    wide = o.float_from_bf16(pats)
+    assert np.array_equal(f32_bits(wide), pats.astype(np.uint32) << 16)
+    back = o.bf16_from_float(wide)
+    nan = ((pats & 0x7F80) == 0x7F80) & ((pats & 0x007F) != 0)
+    assert np.array_equal(back[~nan], pats[~nan])
+    # NaNs stay NaN (payload not part of the contract)
+    assert np.all(((back[nan] & 0x7F80) == 0x7F80) & ((back[nan] & 0x007F) != 0))
+
+
+def check_bf16_vs_torch(o):
+    import torch
+    rng = np.random.default_rng(7)
+    bits = rng.integers(0, 2 ** 32, size=1 << 20, dtype=np.uint64).astype(np.uint32)
+    # add every pattern near each BF16 rounding boundary in a few binades
+    base = np.arange(0x3F000000, 0x3F000000 + (1 << 18), dtype=np.uint32)
+    edges = np.concatenate([bits, base, base | 0x80000000, np.arange(0, 1 << 16, dtype=np.uint32),
+                            np.array([0x7F7FFFFF, 0x7F7F8000, 0xFF7F8000], dtype=np.uint32)])
+    x = edges.view(np.float32)
+    finite = np.isfinite(x)
+    x = x[finite]
+    ours = o.bf16_from_float(x)
+    ref = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    bad = np.nonzero(ours != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches vs torch, e.g. {x[bad[:4]].view(np.uint32)}"
+
+
+def check_widen_vs_torch(o):
+    import torch
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = o.float_from_bf16(pats)
+    ref = torch.from_numpy(pats.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    finite = np.isfinite(ref)
+    assert np.array_equal(f32_bits(ours)[finite], f32_bits(ref)[finite])
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+
+
+# --------------------------------------------------------------------------
+# forward
+# --------------------------------------------------------------------------
+
+def _fwd_cases():
+    for name, r0, r1, r2, r3, p0, p1, p2, p3, out in golden_rows("fwd_worked_examples.txt"):
+        r = np.array([int(v, 16) for v in (r0, r1, r2, r3)], dtype=np.uint16)
+        pre = np.array([f32_from_bits(int(v, 16)) for v in (p0, p1, p2, p3)], dtype=np.float32)
+        yield name, r, pre, int(out, 16)
+
+
+def check_fwd_golden(o):
+    rng = np.random.default_rng(11)
+    for name, r, pre, expected in _fwd_cases():
+        got = int(o.fwd(r.reshape(1, 4, 1), pre.reshape(1, 4))[0, 0])
+        assert got == expected, f"{name}: {got:04X} != {expected:04X}"
+        # the same element inside a larger ragged batch, at token 2, position 5
+        T, H = 4, 13
+        res = random_bf16(rng, (T, 4, H))
+        pr = rng.random((T, 4), dtype=np.float32)
+        res[2, :, 5] = r
+        pr[2] = pre
+        got = int(o.fwd(res, pr)[2, 5])
+        assert got == expected, f"{name} (embedded): {got:04X} != {expected:04X}"
+
+
+def _fwd_exact(r_u16, pre):
+    r = bf16_widen(r_u16)
+    T, _, H = r.shape
+    out = np.empty((T, H), dtype=np.uint16)
+    for t in range(T):
+        for h in range(H):
+            p = [exact_mul(float(pre[t, k]), float(r[t, k, h])) for k in range(4)]
+            s = exact_add(exact_add(p[0], p[1]), exact_add(p[2], p[3]))
+            out[t, h] = bf16_bits_of(to_bf16_exact(s))
+    return out
+
+
+def check_fwd_exact_rational(o):
+    rng = np.random.default_rng(12)
+    # full-precision values
+    res = random_bf16(rng, (3, 4, 37))
+    pre = rng.random((3, 4), dtype=np.float32)
+    assert np.array_equal(o.fwd(res, pre), _fwd_exact(res, pre))
+    # coarse values: products and sums land on rounding ties often
+    res = random_bf16(rng, (4, 4, 40), scale=4.0)
+    res &= np.uint16(0xFFF0)  # 3 fraction bits
+    pre = (rng.integers(1, 1 << 12, size=(4, 4)) * 2.0 ** -9).astype(np.float32)
+    pre[0, 1] = 1.0 + 2.0 ** -8
+    assert np.array_equal(o.fwd(res, pre), _fwd_exact(res, pre))
+
+
+def check_fwd_fp64_bound(o):
+    rng = np.random.default_rng(13)
+    res = random_bf16(rng, (64, 4, 515))
+    pre = rng.random((64, 4), dtype=np.float32)
+    out = bf16_widen(o.fwd(res, pre)).astype(np.float64)
+    prod = pre.astype(np.float64)[:, :, None] * bf16_widen(res).astype(np.float64)  # exact
+    exact = prod.sum(axis=1)
+    mag = np.abs(prod).sum(axis=1)
+    bound = 0.5 * bf16_ulp(out) + 3.01 * U * mag
+    err = np.abs(out - exact)
+    assert np.all(err <= bound), f"max excess {np.max(err - bound)}"
+
+
+def check_fwd_one_hot(o):
+    rng = np.random.default_rng(14)
+    res = random_bf16(rng, (6, 4, 77))
+    res[res == 0x8000] = 0  # -0 may come out as +0 by IEEE rules
+    for k in range(4):
+        pre = np.zeros((6, 4), dtype=np.float32)
+        pre[:, k] = 1.0
+        out = o.fwd(res, pre)
+        assert np.array_equal(out, res[:, k, :]), f"one-hot k={k}"
+
+
+def check_fwd_zero_pre(o):
+    rng = np.random.default_rng(15)
+    res = random_bf16(rng, (5, 4, 33))
+    out = o.fwd(res, np.zeros((5, 4), dtype=np.float32))
+    assert np.all((out == 0) | (out == 0x8000))
+
+
+def check_fwd_symmetries(o):
+    """The (0+1)+(2+3) tree is unchanged by swapping 0<->1, 2<->3 or the two pairs."""
+    rng = np.random.default_rng(16)
+    res = random_bf16(rng, (8, 4, 301))
+    res &= np.uint16(0xFFF8)
+    pre = (rng.integers(1, 1 << 14, size=(8, 4)) * 2.0 ** -13).astype(np.float32)
+    base = o.fwd(res, pre)
+    for perm in ([1, 0, 2, 3], [0, 1, 3, 2], [2, 3, 0, 1], [3, 2, 1, 0]):
+        assert np.array_equal(o.fwd(res[:, perm, :], pre[:, perm]), base), f"perm {perm}"
+
+
+def check_fwd_scaling(o):
+    rng = np.random.default_rng(17)
+    res = random_bf16(rng, (4, 4, 99))
+    pre = rng.random((4, 4), dtype=np.float32) + 0.5
+    base = bf16_widen(o.fwd(res, pre))
+    for e in (-3, 1, 5):
+        scaled = bf16_widen(o.fwd(res, (pre * np.float32(2.0 ** e)).astype(np.float32)))
+        assert np.array_equal(scaled, base * np.float32(2.0 ** e)), f"scale 2^{e}"
+
+
+def check_fwd_negation(o):
+    rng = np.random.default_rng(18)
+    res = random_bf16(rng, (4, 4, 64))
+    pre = rng.random((4, 4), dtype=np.float32)
+    a = bf16_widen(o.fwd(res, pre))
+    b = bf16_widen(o.fwd(res, -pre))
+    assert np.array_equal(a, -b)
+
+
+def check_fwd_token_independent(o):
+    rng = np.random.default_rng(19)
+    res = random_bf16(rng, (9, 4, 21))
+    pre = rng.random((9, 4), dtype=np.float32)
+    full = o.fwd(res, pre)
+    for t in range(9):
+        assert np.array_equal(o.fwd(res[t:t + 1], pre[t:t + 1])[0], full[t])
+
+
+# --------------------------------------------------------------------------
+# backward: grad_residual
+# --------------------------------------------------------------------------
+
+def check_gr_golden(o):
+    rng = np.random.default_rng(21)
+    for name, pbits, gbits, ebits in golden_rows("grad_residual_worked_examples.txt"):
+        pre_v = f32_from_bits(int(pbits, 16))
+        T, H = 3, 11
+        g = random_bf16(rng, (T, H))
+        pre = rng.random((T, 4), dtype=np.float32)
+        g[1, 7] = int(gbits, 16)
+        pre[1, 2] = pre_v
+        got = int(o.grad_residual(g, pre)[1, 2, 7])
+        assert got == int(ebits, 16), f"{name}: {got:04X} != {ebits}"
+
+
+def check_gr_exact_rational(o):
+    rng = np.random.default_rng(22)
+    g = random_bf16(rng, (3, 29))
+    pre = rng.random((3, 4), dtype=np.float32) * np.float32(3.0)
+    got = o.grad_residual(g, pre)
+    gw = bf16_widen(g)
+    for t in range(3):
+        for k in range(4):
+            for h in range(29):
+                v = to_bf16_exact(exact_mul(float(pre[t, k]), float(gw[t, h])))
+                assert got[t, k, h] == bf16_bits_of(v), (t, k, h)
+
+
+def check_gr_identity_onehot(o):
+    rng = np.random.default_rng(23)
+    g = random_bf16(rng, (5, 40))
+    pre = np.zeros((5, 4), dtype=np.float32)
+    pre[:, 2] = 1.0
+    pre[:, 0] = 4.0
+    pre[:, 3] = 0.5
+    got = o.grad_residual(g, pre)
+    gw = bf16_widen(g)
+    assert np.array_equal(got[:, 2, :], g)
+    assert np.array_equal(bf16_widen(got[:, 0, :]), gw * np.float32(4.0))
+    assert np.array_equal(bf16_widen(got[:, 3, :]), gw * np.float32(0.5))
+    assert np.all(bf16_widen(got[:, 1, :]) == 0.0)
+
+
+# --------------------------------------------------------------------------
+# backward: grad_pre
+# --------------------------------------------------------------------------
+
+def check_gp_golden(o):
+    for name, H, k, carrier, positions, expected in golden_rows("grad_pre_order_cases.txt"):
+        H, k = int(H), int(k)
+        vals = np.zeros(H, dtype=np.uint16)
+        for item in positions.split(","):
+            pos, v = item.split(":")
+            if pos == "*":
+                vals[:] = int(v, 16)
+            else:
+                vals[int(pos)] = int(v, 16)
+        g = np.full((1, H), 0x3F80, dtype=np.uint16)
+        res = np.zeros((1, 4, H), dtype=np.uint16)
+        if carrier == "r":
+            res[0, k] = vals
+        else:
+            g[0] = vals
+            res[0, k] = 0x3F80
+        got = f32_bits(o.grad_pre(g, res))[0]
+        want = np.zeros(4, dtype=np.uint32)
+        want[k] = int(expected, 16)
+        assert np.array_equal(got, want), f"{name}: {[hex(v) for v in got]} != {[hex(v) for v in want]}"
+
+
+def check_gp_integer_exact(o):
+    """Integer-valued g and r with every partial sum below 2^24: any order gives the
+    exact integer sum, which fixes products, lane coverage, padding and rows."""
+    rng = np.random.default_rng(24)
+    for H in (1, 7, 8, 9, 255, 2047, 2048, 2049, 4104, 7168, 9001):
+        T = 3
+        gi = rng.integers(-8, 9, size=(T, H))
+        ri = rng.integers(-8, 9, size=(T, 4, H))
+        g = np.array([bf16_bits_of(float(v)) for v in range(-8, 9)], dtype=np.uint16)[gi + 8]
+        r = np.array([bf16_bits_of(float(v)) for v in range(-8, 9)], dtype=np.uint16)[ri + 8]
+        got = o.grad_pre(g, r)
+        want = np.einsum("th,tkh->tk", gi, ri).astype(np.float64)
+        assert np.array_equal(got.astype(np.float64), want), f"H={H}"
+
+
+def order256_depth(H: int) -> int:
+    """Longest chain of binary32 adds any product goes through in ORDER-256."""
+    C = (H + 7) // 8
+    return 3 + (C + 255) // 256 + 5 + 3
+
+
+def check_gp_fp64_bound(o):
+    rng = np.random.default_rng(25)
+    for H in (8, 1279, 4097, 7168):
+        T = 4
+        g = random_bf16(rng, (T, H))
+        r = random_bf16(rng, (T, 4, H))
+        got = o.grad_pre(g, r).astype(np.float64)
+        q = bf16_widen(g).astype(np.float64)[:, None, :] * bf16_widen(r).astype(np.float64)
+        exact = np.array([[math.fsum(q[t, k]) for k in range(4)] for t in range(T)])
+        mag = np.abs(q).sum(axis=2)
+        bound = 1.01 * order256_depth(H) * U * mag
+        assert np.all(np.abs(got - exact) <= bound), f"H={H}"
+
+
+ALL_CHECKS = [
+    check_bf16_golden,
+    check_bf16_roundtrip_exhaustive,
+    check_bf16_vs_torch,
+    check_widen_vs_torch,
+    check_fwd_golden,
+    check_fwd_exact_rational,
+    check_fwd_fp64_bound,
+    check_fwd_one_hot,
+    check_fwd_zero_pre,
+    check_fwd_symmetries,
+    check_fwd_scaling,
+    check_fwd_negation,
+    check_fwd_token_independent,
+    check_gr_golden,
+    check_gr_exact_rational,
+    check_gr_identity_onehot,
+    check_gp_golden,
+    check_gp_integer_exact,
+    check_gp_fp64_bound,
+]

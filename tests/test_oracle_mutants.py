@@ -1,0 +1,116 @@
+"""Planted mistakes in copies of the CPU oracle must each fail at least one pin.
+
+Every mutant below is a plausible slip (a wrong tree, a dropped term, a wrong
+index, a fused multiply-add, a different rounding) applied to a copy of
+``oracle/mhc_oracle.c`` in a temporary directory.  The copy is compiled with the
+oracle's own flags and run through the pin checks of ``_pins``; the test passes
+when some check rejects it.  This shows the pins constrain the oracle, not just
+agree with it.  Nothing here touches the oracle that the other tests use.
+"""
+
+import os
+
+import pytest
+
+import oracle
+import _pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "mhc_oracle.c")
+
+GROUP_TREE = """    for (int stride = ORDER_GROUP / 2; stride >= 1; stride /= 2) {
+        for (int i = 0; i < stride; ++i) a[i] = a[i] + a[i + stride];
+    }
+    return a[0];"""
+
+GROUPS_TREE = """    for (int stride = ORDER_GROUPS / 2; stride >= 1; stride /= 2) {
+        for (int i = 0; i < stride; ++i) w[i] = w[i] + w[i + stride];
+    }
+    return w[0];"""
+
+CHUNK_TREE = """    float a01 = q[0] + q[1];
+    float a23 = q[2] + q[3];
+    float a45 = q[4] + q[5];
+    float a67 = q[6] + q[7];
+    float a0123 = a01 + a23;
+    float a4567 = a45 + a67;
+    return a0123 + a4567;"""
+
+FWD_TREE = """    float s01 = p0 + p1;
+    float s23 = p2 + p3;
+    float s = s01 + s23;"""
+
+MUTANTS = {
+    # forward
+    "fwd_left_to_right": (FWD_TREE, "    float s = ((p0 + p1) + p2) + p3;"),
+    "fwd_pairs_02_13": (FWD_TREE, "    float s = (p0 + p2) + (p1 + p3);"),
+    "fwd_fma": ("    float s01 = p0 + p1;",
+                "    float s01 = __builtin_fmaf(pre[0], oracle_float_from_bf16(r[0]), p1);"),
+    "fwd_layout_k_major": ("r[k] = residual[(t * 4 + k) * H + h];",
+                           "r[k] = residual[(k * T + t) * H + h];"),
+    "fwd_wrong_pre_component": ("float p0 = pre[0] *", "float p0 = pre[1] *"),
+    "fwd_dropped_term": ("float s23 = p2 + p3;", "float s23 = p2;"),
+    "fwd_flush_subnormal": ("    return oracle_bf16_from_float(s);\n}",
+                            "    return oracle_bf16_from_float((s < 1.17549435e-38f && "
+                            "s > -1.17549435e-38f) ? 0.0f : s);\n}"),
+    # BF16 rounding
+    "bf16_truncate": ("        kept += 1u;", "        kept += 0u;"),
+    "bf16_ties_away": ("(dropped == 0x8000u && (kept & 1u) != 0u)", "(dropped == 0x8000u)"),
+    "bf16_ties_down": ("(dropped == 0x8000u && (kept & 1u) != 0u)", "(0)"),
+    # grad_residual
+    "gr_pre_rounded_first": (
+        "float prod = p * oracle_float_from_bf16(g[t * H + h]);",
+        "float prod = oracle_float_from_bf16(oracle_bf16_from_float(p)) * "
+        "oracle_float_from_bf16(g[t * H + h]);"),
+    "gr_wrong_k": ("float p = pre[t * 4 + k];", "float p = pre[t * 4 + (3 - k)];"),
+    # grad_pre
+    "gp_lanes_128": ("ORDER_LANES = 256", "ORDER_LANES = 128"),
+    "gp_chunk_sequential": (CHUNK_TREE, "    float s = q[0];\n"
+                            "    for (int e = 1; e < ORDER_CHUNK; ++e) s = s + q[e];\n"
+                            "    return s;"),
+    "gp_chunk_stride4": (CHUNK_TREE, "    return ((q[0] + q[4]) + (q[1] + q[5])) + "
+                         "((q[2] + q[6]) + (q[3] + q[7]));"),
+    "gp_group_adjacent_first": (GROUP_TREE, """    for (int stride = 1; stride < ORDER_GROUP; stride *= 2) {
+        for (int i = 0; i + stride < ORDER_GROUP; i += 2 * stride) a[i] = a[i] + a[i + stride];
+    }
+    return a[0];"""),
+    "gp_group_sequential": (GROUP_TREE, """    float s = a[0];
+    for (int i = 1; i < ORDER_GROUP; ++i) s = s + a[i];
+    return s;"""),
+    "gp_groups_sequential": (GROUPS_TREE, """    float s = w[0];
+    for (int i = 1; i < ORDER_GROUPS; ++i) s = s + w[i];
+    return s;"""),
+    "gp_lane_descending": ("for (int64_t c = 0; c < C; ++c) {",
+                           "for (int64_t c = C - 1; c >= 0; --c) {"),
+    "gp_drop_ragged_tail": ("int64_t C = (H + ORDER_CHUNK - 1) / ORDER_CHUNK;",
+                            "int64_t C = H / ORDER_CHUNK;"),
+    "gp_wrong_row": ("residual + (t * 4 + k) * H, H);", "residual + (t * 4 + (k ^ 1)) * H, H);"),
+    "gp_lane_starts_at_first_partial": (
+        "lane[j] = lane[j] + chunk_partial(q);",
+        "lane[j] = (c < ORDER_LANES) ? chunk_partial(q) : lane[j] + chunk_partial(q);"),
+    "gp_fma_products": ("lane[j] = lane[j] + chunk_partial(q);",
+                        "lane[j] = __builtin_fmaf(1.0f + 0x1p-23f, chunk_partial(q), lane[j]);"),
+}
+
+
+def _caught(o) -> list:
+    failures = []
+    for check in _pins.ALL_CHECKS:
+        try:
+            check(o)
+        except AssertionError as e:
+            failures.append(f"{check.__name__}: {str(e)[:80]}")
+    return failures
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.compile_library(str(mutated), str(tmp_path / "libmutant.so"),
+                                 extra_flags=["-Wno-unused-function", "-Wno-unused-variable",
+                                              "-Wno-unused-parameter"])
+    failures = _caught(oracle.Oracle(lib))
+    assert failures, f"mutant {name} passed every pin"
