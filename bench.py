@@ -1,0 +1,581 @@
+"""Benchmark of the batch-invariant mHC pre "H Aggregate" on GB300.
+
+One step = one pass of the whole hot path over one batch: the forward
+(out = bf16((pre0*r0 + pre1*r1) + (pre2*r2 + pre3*r3))) and the fused backward
+(grad_residual, grad_pre) on T=4096 tokens of H=7168, inputs resident in HBM.
+Bytes per step are the algorithmic ones: T*(10H+16) for the forward and
+T*(18H+32) for the backward ("Add batch-invariant h_aggregate kernel",
+Performance: GB/s = T*(10H+16)/time for the forward).
+
+Prints one JSON line on rank 0.  Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Multi-GPU runs (torchrun, one rank per GPU) shard by giving every rank its own
+batch (weak scaling, no data exchange); only the timing uses a collective.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "h_aggregate fwd/bwd HBM GB/s (% of GB300 peak) and µs/call per (T,H)"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+L2_FLUSH_BYTES = 256 << 20
+
+FWD_SWEEP = [("fwd_decode", 2, "decode", [(1, 4096), (8, 4096), (128, 4096),
+                                          (1, 7168), (8, 7168), (128, 7168)]),
+             ("fwd_prefill", 3, "normal", [(1024, 7168), (4096, 7168), (16384, 7168),
+                                           (65536, 7168)])]
+BWD_SWEEP = [("bwd_t4096_h7168", 4, "normal", [(4096, 7168)])]
+
+
+def fwd_bytes(T, H):
+    return T * (10 * H + 16)
+
+
+def bwd_bytes(T, H):
+    return T * (18 * H + 32)
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--T", type=int, default=4096)
+    ap.add_argument("--H", type=int, default=7168)
+    ap.add_argument("--phase", choices=("both", "fwd", "bwd"), default="both",
+                    help="profiling aid: time only one kernel per step")
+    ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target length of the CPU oracle baseline sample")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# environment
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def stored_traffic(kernel: str, digest: str):
+    """DRAM bytes per launch from an ncu capture (profiles/dram_traffic.txt),
+    only if it was taken on this exact library build."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel:
+                lib_digest, T, H = parts[1], parts[2], parts[3]
+                bytes_per_launch = float(parts[4])
+                if lib_digest == digest[:16]:
+                    return bytes_per_launch, int(T), int(H)
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self._reader = threading.Thread(target=self._read, daemon=True)
+        self._reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        if not rows:
+            return None
+        window = [r for r in rows if self.t0 - 0.1 <= r[0] <= self.t1 + 0.3]
+        in_window = len(window)
+        if not window:
+            window = [min(rows, key=lambda r: abs(r[0] - (self.t0 + self.t1) / 2))]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[2]) for _, p in window if num(p[2]) is not None]
+        smax = [num(p[3]) for _, p in window if num(p[3]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for _, p in window for i in range(4)
+                          if p[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": in_window,
+                "power_w_max": max((num(p[4]) or 0.0) for _, p in window)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    from invariant_mhc_aggregate_gb300 import _build, binding
+    from invariant_mhc_aggregate_gb300.inputs import backward_inputs, forward_inputs
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("nccl", device_id=dev)
+        dist = dist_mod
+
+    _build.build()
+    binding.load()
+    digest = _build.source_digest()
+    T, H = args.T, args.H
+    # every rank draws its own batch (weak scaling)
+    g, res, pre = backward_inputs(T, H, "normal", seed=4 + rank, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    grad_res = torch.empty((T, 4, H), dtype=torch.bfloat16, device=dev)
+    grad_pre = torch.empty((T, 4), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    do_fwd = args.phase in ("both", "fwd")
+    do_bwd = args.phase in ("both", "bwd")
+
+    def step():
+        if do_fwd:
+            binding.mhc_h_aggregate_fwd(res, pre, out, stream)
+        if do_bwd:
+            binding.mhc_h_aggregate_bwd(g, res, pre, grad_res, grad_pre, stream)
+
+    for _ in range(max(args.warmup, 0)):
+        if not args.no_flush:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.5)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark_start()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        if not args.no_flush:
+            flush.zero_()
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        if do_fwd:
+            binding.mhc_h_aggregate_fwd(res, pre, out, stream)
+        e1.record(stream)
+        if do_bwd:
+            binding.mhc_h_aggregate_bwd(g, res, pre, grad_res, grad_pre, stream)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    sampler.mark_end()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    step_ms_local = (sum(fwd_ms) + sum(bwd_ms)) / K
+    step_ms = step_ms_local
+    if dist is not None:
+        t = torch.tensor([step_ms_local], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+
+    bytes_step = (fwd_bytes(T, H) if do_fwd else 0) + (bwd_bytes(T, H) if do_bwd else 0)
+    value = bytes_step * world / (step_ms * 1e-3) / 1e9
+
+    peak, peak_kind = measured_peaks()
+    fwd_us = 1e3 * statistics.fmean(fwd_ms) if do_fwd else None
+    bwd_us = 1e3 * statistics.fmean(bwd_ms) if do_bwd else None
+    per_kernel = {}
+    if do_fwd:
+        a = fwd_bytes(T, H) / (fwd_us * 1e-6) / 1e9
+        per_kernel["h_agg_fwd_vec16"] = {"us_mean": round(fwd_us, 3),
+                                         "us_p50": round(1e3 * statistics.median(fwd_ms), 3),
+                                         "GBps": round(a, 1), "frac": round(a / peak, 4),
+                                         "bytes": fwd_bytes(T, H)}
+    if do_bwd:
+        a = bwd_bytes(T, H) / (bwd_us * 1e-6) / 1e9
+        per_kernel["h_agg_bwd_vec16"] = {"us_mean": round(bwd_us, 3),
+                                         "us_p50": round(1e3 * statistics.median(bwd_ms), 3),
+                                         "GBps": round(a, 1), "frac": round(a / peak, 4),
+                                         "bytes": bwd_bytes(T, H)}
+    dom = max(per_kernel, key=lambda k: per_kernel[k]["us_mean"])
+    dk = per_kernel[dom]
+    traffic = stored_traffic(dom, digest)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": dk["GBps"], "peak": peak,
+                "peak_kind": f"of {peak_kind}", "unit": "GB/s", "frac": dk["frac"],
+                "traffic": None, "algorithmic_bytes": dk["bytes"]}
+    if traffic is not None:
+        tb, tT, tH = traffic
+        roofline["traffic"] = round(tb * (T / tT) * (H / tH))
+        roofline["traffic_note"] = f"ncu dram bytes at T={tT},H={tH}, scaled by tokens" \
+            if (tT, tH) != (T, H) else "ncu dram bytes, same workload"
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"h_aggregate fwd+bwd, T={T}, H={H}" if args.phase == "both"
+                   else f"h_aggregate {args.phase} only, T={T}, H={H}",
+                   "T": T, "H": H, "tokens_per_rank": T,
+                   "values": "residual, g ~ N(0,1) rounded to bf16; pre ~ U(0,1); seed 4+rank",
+                   "storage": "bf16 residual/out/g/grad_residual, f32 pre/grad_pre",
+                   "l2": ("flushed before every step (256 MiB write, outside the timed events); "
+                          "inputs 294 MB > L2") if not args.no_flush else "not flushed",
+                   "timing": "CUDA events on the launching stream around each kernel",
+                   "bytes_per_step": bytes_step},
+        "gpu_launches": K * (int(do_fwd) + int(do_bwd)),
+        "roofline": roofline,
+        "per_kernel": per_kernel,
+        "wall_s_timed_region": round(wall, 3),
+        "library": {"so": os.path.relpath(_build.LIB_PATH, ROOT), "digest": digest[:16]},
+    }
+    if clocks is not None:
+        line["clocks"] = clocks
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_measure(args, torch, binding, g, res, pre, dev, stream, world, dist)
+
+    if not args.no_sweep and rank == 0:
+        line["sweep"] = sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak)
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(g, res, pre, T, H, args.cpu_seconds)
+
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def e2e_measure(args, torch, binding, g, res, pre, dev, stream, world, dist):
+    """The step through the public API with host buffers: pinned host -> device
+    copies of the step's inputs, forward, backward, device -> pinned host copies
+    of its results, all inside the timed region."""
+    T, H = args.T, args.H
+    hg = g.cpu().pin_memory()
+    hr = res.cpu().pin_memory()
+    hp = pre.cpu().pin_memory()
+    ho = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    hgr = torch.empty((T, 4, H), dtype=torch.bfloat16).pin_memory()
+    hgp = torch.empty((T, 4), dtype=torch.float32).pin_memory()
+    dg, dr, dp = torch.empty_like(g), torch.empty_like(res), torch.empty_like(pre)
+    do = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    dgr = torch.empty((T, 4, H), dtype=torch.bfloat16, device=dev)
+    dgp = torch.empty((T, 4), dtype=torch.float32, device=dev)
+
+    def e2e_step():
+        dr.copy_(hr, non_blocking=True)
+        dp.copy_(hp, non_blocking=True)
+        dg.copy_(hg, non_blocking=True)
+        binding.mhc_h_aggregate_fwd(dr, dp, do, stream)
+        binding.mhc_h_aggregate_bwd(dg, dr, dp, dgr, dgp, stream)
+        ho.copy_(do, non_blocking=True)
+        hgr.copy_(dgr, non_blocking=True)
+        hgp.copy_(dgp, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    n = max(5, min(args.steps, 50))
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert torch.equal(hgp, dgp.cpu()) and torch.equal(ho.view(torch.int16), do.cpu().view(torch.int16))
+    h2d = hr.numel() * 2 + hp.numel() * 4 + hg.numel() * 2
+    d2h = ho.numel() * 2 + hgr.numel() * 2 + hgp.numel() * 4
+    value = (fwd_bytes(T, H) + bwd_bytes(T, H)) * world / (ms * 1e-3) / 1e9
+    return {"value": round(value, 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "note": "pinned host buffers; copies, forward and backward in one stream"}
+
+
+def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
+    """us/call per (T,H): CUDA-graph replay of one call, L2 flushed before each
+    sample, 7 rounds x (10 warm-up + 100 samples); p20/p50/p80 of round medians."""
+    results = []
+    stream = torch.cuda.Stream(dev)
+
+    def time_graph(graph):
+        meds = []
+        for _ in range(7):
+            samples = []
+            for i in range(110):
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                graph.replay()
+                e1.record()
+                e1.synchronize()
+                if i >= 10:
+                    samples.append(e0.elapsed_time(e1) * 1e3)
+            meds.append(statistics.median(samples))
+        meds.sort()
+        q = np.quantile(np.array(meds), [0.2, 0.5, 0.8])
+        return [round(float(x), 3) for x in q]
+
+    for name, seed, recipe, shapes in FWD_SWEEP:
+        for T, H in shapes:
+            r, p = forward_inputs(T, H, recipe, seed, device=dev)
+            o = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+            binding.mhc_h_aggregate_fwd(r, p, o)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                binding.mhc_h_aggregate_fwd(r, p, o)
+            us = time_graph(graph)
+            gbs = fwd_bytes(T, H) / (us[1] * 1e-6) / 1e9
+            results.append({"workload": name, "dir": "fwd", "T": T, "H": H,
+                            "us_p20_p50_p80": us, "GBps_p50": round(gbs, 1),
+                            "frac_of_measured": round(gbs / peak, 4),
+                            "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)})
+            del r, p, o, graph
+    for name, seed, recipe, shapes in BWD_SWEEP:
+        for T, H in shapes:
+            g, r, p = backward_inputs(T, H, recipe, seed, device=dev)
+            gr = torch.empty((T, 4, H), dtype=torch.bfloat16, device=dev)
+            gp = torch.empty((T, 4), dtype=torch.float32, device=dev)
+            binding.mhc_h_aggregate_bwd(g, r, p, gr, gp)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                binding.mhc_h_aggregate_bwd(g, r, p, gr, gp)
+            us = time_graph(graph)
+            gbs = bwd_bytes(T, H) / (us[1] * 1e-6) / 1e9
+            results.append({"workload": name, "dir": "bwd", "T": T, "H": H,
+                            "us_p20_p50_p80": us, "GBps_p50": round(gbs, 1),
+                            "frac_of_measured": round(gbs / peak, 4),
+                            "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)})
+            del g, r, p, gr, gp, graph
+    torch.cuda.synchronize()
+    return results
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_pass(o, g_u16, r_u16, pre_f32, threads: int):
+    """Forward and backward of the oracle over all tokens given, tokens split
+    into contiguous blocks over `threads` host threads (ctypes releases the GIL;
+    tokens are independent, so the results do not depend on the split)."""
+    T, _, H = r_u16.shape
+    out = np.empty((T, H), dtype=np.uint16)
+    gr = np.empty((T, 4, H), dtype=np.uint16)
+    gp = np.empty((T, 4), dtype=np.float32)
+    bounds = np.linspace(0, T, threads + 1).astype(int)
+
+    def work(a, b):
+        if b <= a:
+            return
+        o.lib.oracle_h_aggregate_fwd(r_u16[a:b].ctypes.data, pre_f32[a:b].ctypes.data,
+                                     out[a:b].ctypes.data, b - a, H)
+        o.lib.oracle_h_aggregate_bwd(g_u16[a:b].ctypes.data, r_u16[a:b].ctypes.data,
+                                     pre_f32[a:b].ctypes.data, gr[a:b].ctypes.data,
+                                     gp[a:b].ctypes.data, b - a, H)
+
+    ths = [threading.Thread(target=work, args=(int(bounds[i]), int(bounds[i + 1])))
+           for i in range(threads)]
+    for t in ths:
+        t.start()
+    for t in ths:
+        t.join()
+    return out, gr, gp
+
+
+def _host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(g, res, pre, T, H, seconds):
+    """The CPU oracle, as it stands, on the host cores over a bounded sample of
+    the same workload (whole tokens), sized to about `seconds` of work."""
+    import oracle
+    o = oracle.default()
+    threads = _host_threads()
+    probe = 64
+    gu = g[:probe].contiguous().cpu().view(__import__("torch").int16).numpy().view(np.uint16)
+    ru = res[:probe].contiguous().cpu().view(__import__("torch").int16).numpy().view(np.uint16)
+    pf = pre[:probe].contiguous().cpu().numpy()
+    t0 = time.perf_counter()
+    _oracle_pass(o, gu, ru, pf, threads)
+    dt = time.perf_counter() - t0
+    per_token = dt / probe
+    n_tok = int(min(T, max(probe, seconds / max(per_token, 1e-9))))
+    reps = max(1, int(seconds / max(per_token * n_tok, 1e-9)))
+    import torch
+    gu = g[:n_tok].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    ru = res[:n_tok].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    pf = pre[:n_tok].contiguous().cpu().numpy()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        _oracle_pass(o, gu, ru, pf, threads)
+    dt = time.perf_counter() - t0
+    bytes_done = reps * (fwd_bytes(n_tok, H) + bwd_bytes(n_tok, H))
+    return {"value": round(bytes_done / dt / 1e9, 3), "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": f"{reps} x {n_tok} of {T} tokens (H={H}), forward + backward, "
+                      f"{dt:.1f} s on {threads} host threads"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle on the host cores, on the same metric
+    and workload, each step a bounded sample (256 whole tokens) of the batch."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    import oracle
+    from invariant_mhc_aggregate_gb300.inputs import backward_inputs
+    T, H = args.T, args.H
+    n_tok = min(T, 256)
+    g, res, pre = backward_inputs(n_tok, H, "normal", seed=4, device="cpu")
+    gu = g.view(torch.int16).numpy().view(np.uint16)
+    ru = res.view(torch.int16).numpy().view(np.uint16)
+    pf = pre.numpy()
+    o = oracle.default()
+    threads = _host_threads()
+    for _ in range(max(args.warmup, 0)):
+        _oracle_pass(o, gu, ru, pf, threads)
+    K = args.steps
+    t0 = time.perf_counter()
+    for _ in range(K):
+        _oracle_pass(o, gu, ru, pf, threads)
+    dt = time.perf_counter() - t0
+    bytes_step = fwd_bytes(n_tok, H) + bwd_bytes(n_tok, H)
+    value = bytes_step * K / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * dt / K, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"h_aggregate fwd+bwd, T={T}, H={H}", "T": T, "H": H,
+                   "sample_tokens_per_step": n_tok,
+                   "values": "residual, g ~ N(0,1) rounded to bf16; pre ~ U(0,1); seed 4"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{n_tok} of {T} tokens per step, forward + backward"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

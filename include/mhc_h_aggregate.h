@@ -1,0 +1,131 @@
+/*
+ * mhc_h_aggregate.h -- C ABI of the batch-invariant mHC pre "H Aggregate"
+ * library for GB300 (sm_103a).
+ *
+ * The operation ("Add batch-invariant h_aggregate kernel", RL-Kernel pull
+ * request 366, Summary):
+ *
+ *   residual  [T,4,H]  BF16      pre  [T,4]  FP32      out  [T,H]  BF16
+ *   out[t,h] = bf16( (pre[t,0]*r[t,0,h] + pre[t,1]*r[t,1,h])
+ *                  + (pre[t,2]*r[t,2,h] + pre[t,3]*r[t,3,h]) )
+ *
+ * with every product and sum one FP32 round-to-nearest-even operation (no
+ * fused multiply-add), the fixed (0 + 1) + (2 + 3) tree, and BF16
+ * round-to-nearest-even only at the output (same page, Batch invariance).
+ *
+ * Its backward (asked for by the reviewer on that page; the page gives no
+ * formula, so this is the exact derivative of the one above):
+ *
+ *   grad_residual[t,k,h] = bf16( fp32(pre[t,k] * g[t,h]) )
+ *   grad_pre[t,k]        = sum over h of g[t,h] * r[t,k,h]      (FP32)
+ *
+ * grad_pre is summed in ORDER-256, which depends on H only:
+ *   1. q_h = g[t,h] * r[t,k,h] in FP32 (exact: both factors are BF16);
+ *   2. chunk c = elements 8c .. 8c+7 (+0.0 past H), partial
+ *      ((q0+q1)+(q2+q3)) + ((q4+q5)+(q6+q7));
+ *   3. lane j (0..255) starts at +0.0 and adds the partials of chunks
+ *      j, j+256, j+512, ... in increasing order;
+ *   4. each group of 32 lanes folds with strides 16, 8, 4, 2, 1
+ *      (lane i < stride: a_i = a_i + a_(i+stride));
+ *   5. the 8 group results fold with strides 4, 2, 1; the first is grad_pre.
+ *
+ * Determinism contract.  Every output byte depends only on the input bytes of
+ * its own token and on H.  Calls on any split of the batch along T, with any
+ * pointer alignment, on any stream, give byte-identical results, and repeated
+ * calls give identical bytes.  NaN payloads are outside the contract.
+ *
+ * Layout.  Dense row-major: residual[t][k][h] at element (t*4 + k)*H + h;
+ * pre[t][k] at t*4 + k; out and g at t*H + h; grad_residual like residual;
+ * grad_pre like pre.  BF16 buffers are 2-byte aligned, FP32 buffers 4-byte
+ * aligned.  Any such alignment is accepted; 16-byte-aligned buffers with
+ * H % 8 == 0 take the 16-byte vector path, others a narrower path with
+ * identical results.
+ *
+ * Pointers and ownership.  Every data pointer is a DEVICE pointer (or managed
+ * memory) allocated and owned by the caller.  The library allocates nothing,
+ * keeps no state between calls except a per-thread copy of the last CUDA
+ * error code, and never synchronises: each call enqueues kernels on `stream`
+ * (NULL = the legacy default stream) and returns.  Calls are safe from several
+ * host threads at once.
+ *
+ * Errors.  T == 0 returns MHC_OK without launching.  T < 0, H <= 0, a NULL
+ * pointer, a misaligned pointer, a size whose byte count overflows int64, or
+ * an output that overlaps an input or another output returns
+ * MHC_ERR_INVALID_ARG without launching.  A failed launch returns
+ * MHC_ERR_CUDA; the CUDA error code is then available from
+ * mhc_h_aggregate_last_cuda_error() on the same thread.  Faults during
+ * execution surface, as usual in CUDA, at the caller's next synchronisation.
+ */
+#ifndef MHC_H_AGGREGATE_H
+#define MHC_H_AGGREGATE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t (declared here so that the header does not
+ * need the CUDA headers). */
+struct CUstream_st;
+typedef struct CUstream_st* mhc_stream_t;
+
+typedef enum mhc_status {
+    MHC_OK = 0,
+    MHC_ERR_INVALID_ARG = 1,
+    MHC_ERR_UNSUPPORTED = 2,
+    MHC_ERR_CUDA = 3
+} mhc_status_t;
+
+/* Kernel path a call takes (returned by the *_path queries). */
+typedef enum mhc_path {
+    MHC_PATH_NONE = -1,   /* the call would be rejected or launches nothing */
+    MHC_PATH_VEC16 = 0,   /* 16-byte loads/stores: H % 8 == 0, buffers 16-byte aligned */
+    MHC_PATH_PAIR = 1,    /* 4-byte loads/stores: H even, buffers 4-byte aligned */
+    MHC_PATH_ELEMENT = 2  /* 2-byte loads/stores: any H and alignment */
+} mhc_path_t;
+
+/* Version of this ABI; changes when a declaration here changes. */
+int32_t mhc_h_aggregate_abi_version(void);
+
+/* Forward ("Add batch-invariant h_aggregate kernel", Summary and Batch
+ * invariance).
+ *   residual  in   BF16 [T,4,H]
+ *   pre       in   FP32 [T,4]
+ *   out       out  BF16 [T,H]; every element is written exactly once.
+ */
+mhc_status_t mhc_h_aggregate_fwd(const void* residual, const float* pre, void* out,
+                                 int64_t T, int64_t H, mhc_stream_t stream);
+
+/* Backward (same page, reviewer request; formula above): one fused pass.
+ *   grad_out       in   BF16 [T,H]    g, the gradient of out
+ *   residual       in   BF16 [T,4,H]
+ *   pre            in   FP32 [T,4]
+ *   grad_residual  out  BF16 [T,4,H]
+ *   grad_pre       out  FP32 [T,4]   ORDER-256 sums
+ */
+mhc_status_t mhc_h_aggregate_bwd(const void* grad_out, const void* residual, const float* pre,
+                                 void* grad_residual, float* grad_pre,
+                                 int64_t T, int64_t H, mhc_stream_t stream);
+
+/* The kernel path mhc_h_aggregate_fwd / _bwd would take for these arguments
+ * (no launch, no CUDA call).  MHC_PATH_NONE when the call would be rejected or
+ * when T == 0. */
+mhc_path_t mhc_h_aggregate_fwd_path(const void* residual, const float* pre, const void* out,
+                                    int64_t T, int64_t H);
+mhc_path_t mhc_h_aggregate_bwd_path(const void* grad_out, const void* residual,
+                                    const float* pre, const void* grad_residual,
+                                    const float* grad_pre, int64_t T, int64_t H);
+
+/* Static text for a status code. */
+const char* mhc_status_string(mhc_status_t status);
+
+/* The cudaError_t value behind the last MHC_ERR_CUDA returned on the calling
+ * thread (0 when there was none). */
+int32_t mhc_h_aggregate_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHC_H_AGGREGATE_H */

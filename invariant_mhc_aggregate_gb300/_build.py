@@ -1,0 +1,91 @@
+"""Compile the sm_103a library ``libmhc_h_aggregate.so`` in-tree with nvcc.
+
+The library is one translation unit (``csrc/mhc_h_aggregate.cu``) exporting
+the C ABI of ``include/mhc_h_aggregate.h``.  It is rebuilt when its sources or
+flags change (a stamp file beside it records their hash).
+"""
+
+from __future__ import annotations
+
+import hashlib
+import os
+import shutil
+import subprocess
+import tempfile
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+LIB_DIR = os.path.join(PKG, "lib")
+LIB_NAME = "libmhc_h_aggregate.so"
+LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
+SOURCES = [os.path.join(CSRC, "mhc_h_aggregate.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, "fastdiv.cuh"), os.path.join(INCLUDE, "mhc_h_aggregate.h")]
+
+ARCH = "sm_103a"
+
+#: nvcc flags.  No fast math anywhere: the kernels promise IEEE round-to-nearest
+#: binary32 products and sums, and subnormals kept.  ``--fmad=false`` keeps
+#: nvcc from contracting a multiply and an add (the kernels use __fmul_rn /
+#: __fadd_rn, which are never contracted, so this guards any code added later).
+NVCC_FLAGS = [
+    "-gencode", "arch=compute_103a,code=sm_103a",
+    "-O3", "-lineinfo", "-std=c++17",
+    "--fmad=false", "-ftz=false", "-prec-div=true", "-prec-sqrt=true",
+    "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
+    "-shared",
+]
+
+
+def nvcc_path() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found (set NVCC or put the CUDA toolkit on PATH)")
+
+
+def _digest(extra_flags) -> str:
+    h = hashlib.sha256()
+    for p in DEPS:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(NVCC_FLAGS + list(extra_flags)).encode())
+    return h.hexdigest()
+
+
+def source_digest() -> str:
+    """Hash of the library's sources and flags (identifies a kernel build)."""
+    return _digest(())
+
+
+def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
+    """Build the library if its sources or flags changed; return its path."""
+    digest = _digest(extra_flags)
+    stamp = LIB_PATH + ".stamp"
+    if not force and os.path.exists(LIB_PATH) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == digest:
+                return LIB_PATH
+    os.makedirs(LIB_DIR, exist_ok=True)
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=LIB_DIR)
+    os.close(fd)
+    cmd = [nvcc_path(), *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-I", CSRC, "-o", tmp, *SOURCES]
+    try:
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError(f"nvcc failed ({' '.join(cmd)}):\n{res.stderr}")
+        if verbose and res.stderr:
+            print(res.stderr)
+        os.replace(tmp, LIB_PATH)
+    finally:
+        if os.path.exists(tmp):
+            os.unlink(tmp)
+    with open(stamp, "w") as f:
+        f.write(digest + "\n")
+    return LIB_PATH
+
+
+if __name__ == "__main__":
+    import sys
+    print(build(force="--force" in sys.argv, verbose=True))

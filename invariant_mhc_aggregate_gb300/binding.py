@@ -1,0 +1,208 @@
+"""Python binding of the C ABI in ``include/mhc_h_aggregate.h`` (ctypes).
+
+Argument marshalling only: every step of the operation runs in the sm_103a
+kernels of ``libmhc_h_aggregate.so``.  There is no CPU or PyTorch fallback; if
+the library has not been built, loading it raises.
+
+The function names match the C entry points.  Tensor arguments must be CUDA
+tensors, contiguous, with the dtypes and shapes of the header; T and H are
+read from ``residual``.  Calls are asynchronous on ``stream`` (default: the
+current PyTorch stream of the tensors' device).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+MHC_OK = 0
+MHC_ERR_INVALID_ARG = 1
+MHC_ERR_UNSUPPORTED = 2
+MHC_ERR_CUDA = 3
+
+MHC_PATH_NONE = -1
+MHC_PATH_VEC16 = 0
+MHC_PATH_PAIR = 1
+MHC_PATH_ELEMENT = 2
+PATH_NAMES = {MHC_PATH_NONE: "none", MHC_PATH_VEC16: "vec16", MHC_PATH_PAIR: "pair",
+              MHC_PATH_ELEMENT: "element"}
+
+#: Every symbol the header declares, in declaration order.
+EXPORTS = (
+    "mhc_h_aggregate_abi_version",
+    "mhc_h_aggregate_fwd",
+    "mhc_h_aggregate_bwd",
+    "mhc_h_aggregate_fwd_path",
+    "mhc_h_aggregate_bwd_path",
+    "mhc_status_string",
+    "mhc_h_aggregate_last_cuda_error",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MhcError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        lib = load()
+        text = lib.mhc_status_string(status).decode()
+        if status == MHC_ERR_CUDA:
+            text += f" (cudaError {lib.mhc_h_aggregate_last_cuda_error()})"
+        super().__init__(f"{what}: {text}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        path = path or _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        p = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        i32 = ctypes.c_int32
+        lib.mhc_h_aggregate_abi_version.argtypes = []
+        lib.mhc_h_aggregate_abi_version.restype = i32
+        lib.mhc_h_aggregate_fwd.argtypes = [p, p, p, i64, i64, p]
+        lib.mhc_h_aggregate_fwd.restype = i32
+        lib.mhc_h_aggregate_bwd.argtypes = [p, p, p, p, p, i64, i64, p]
+        lib.mhc_h_aggregate_bwd.restype = i32
+        lib.mhc_h_aggregate_fwd_path.argtypes = [p, p, p, i64, i64]
+        lib.mhc_h_aggregate_fwd_path.restype = i32
+        lib.mhc_h_aggregate_bwd_path.argtypes = [p, p, p, p, p, i64, i64]
+        lib.mhc_h_aggregate_bwd_path.restype = i32
+        lib.mhc_status_string.argtypes = [i32]
+        lib.mhc_status_string.restype = ctypes.c_char_p
+        lib.mhc_h_aggregate_last_cuda_error.argtypes = []
+        lib.mhc_h_aggregate_last_cuda_error.restype = i32
+        if path == _build.LIB_PATH:
+            _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------------------
+# raw entry points: integer addresses, sizes and a stream handle
+# ---------------------------------------------------------------------------
+
+def fwd_raw(residual: int, pre: int, out: int, T: int, H: int, stream: int = 0) -> int:
+    return load().mhc_h_aggregate_fwd(residual, pre, out, T, H, stream)
+
+
+def bwd_raw(grad_out: int, residual: int, pre: int, grad_residual: int, grad_pre: int,
+            T: int, H: int, stream: int = 0) -> int:
+    return load().mhc_h_aggregate_bwd(grad_out, residual, pre, grad_residual, grad_pre, T, H,
+                                      stream)
+
+
+def fwd_path_raw(residual: int, pre: int, out: int, T: int, H: int) -> int:
+    return load().mhc_h_aggregate_fwd_path(residual, pre, out, T, H)
+
+
+def bwd_path_raw(grad_out: int, residual: int, pre: int, grad_residual: int, grad_pre: int,
+                 T: int, H: int) -> int:
+    return load().mhc_h_aggregate_bwd_path(grad_out, residual, pre, grad_residual, grad_pre, T, H)
+
+
+# ---------------------------------------------------------------------------
+# tensor entry points
+# ---------------------------------------------------------------------------
+
+def _check(t: torch.Tensor, name: str, dtype, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor, got {t.device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return int(stream.cuda_stream)
+    return int(stream)
+
+
+def _TH(residual: torch.Tensor) -> tuple[int, int]:
+    if residual.dim() != 3 or residual.shape[1] != 4:
+        raise ValueError(f"residual must be [T,4,H], got {tuple(residual.shape)}")
+    return int(residual.shape[0]), int(residual.shape[2])
+
+
+def mhc_h_aggregate_fwd(residual: torch.Tensor, pre: torch.Tensor, out: torch.Tensor,
+                        stream=None) -> None:
+    """out[t,h] = bf16((pre0*r0 + pre1*r1) + (pre2*r2 + pre3*r3)), written into ``out``."""
+    T, H = _TH(residual)
+    _check(residual, "residual", torch.bfloat16, (T, 4, H))
+    _check(pre, "pre", torch.float32, (T, 4))
+    _check(out, "out", torch.bfloat16, (T, H))
+    st = fwd_raw(residual.data_ptr(), pre.data_ptr(), out.data_ptr(), T, H,
+                 _stream_handle(stream, residual.device))
+    if st != MHC_OK:
+        raise MhcError(st, "mhc_h_aggregate_fwd")
+
+
+def mhc_h_aggregate_bwd(grad_out: torch.Tensor, residual: torch.Tensor, pre: torch.Tensor,
+                        grad_residual: torch.Tensor, grad_pre: torch.Tensor,
+                        stream=None) -> None:
+    """grad_residual = bf16(pre*g), grad_pre = ORDER-256 sums of g*r; written in place."""
+    T, H = _TH(residual)
+    _check(grad_out, "grad_out", torch.bfloat16, (T, H))
+    _check(residual, "residual", torch.bfloat16, (T, 4, H))
+    _check(pre, "pre", torch.float32, (T, 4))
+    _check(grad_residual, "grad_residual", torch.bfloat16, (T, 4, H))
+    _check(grad_pre, "grad_pre", torch.float32, (T, 4))
+    st = bwd_raw(grad_out.data_ptr(), residual.data_ptr(), pre.data_ptr(),
+                 grad_residual.data_ptr(), grad_pre.data_ptr(), T, H,
+                 _stream_handle(stream, residual.device))
+    if st != MHC_OK:
+        raise MhcError(st, "mhc_h_aggregate_bwd")
+
+
+def mhc_h_aggregate_fwd_path(residual: torch.Tensor, pre: torch.Tensor, out: torch.Tensor) -> int:
+    T, H = _TH(residual)
+    return fwd_path_raw(residual.data_ptr(), pre.data_ptr(), out.data_ptr(), T, H)
+
+
+def mhc_h_aggregate_bwd_path(grad_out, residual, pre, grad_residual, grad_pre) -> int:
+    T, H = _TH(residual)
+    return bwd_path_raw(grad_out.data_ptr(), residual.data_ptr(), pre.data_ptr(),
+                        grad_residual.data_ptr(), grad_pre.data_ptr(), T, H)
+
+
+def h_aggregate(residual: torch.Tensor, pre: torch.Tensor, stream=None) -> torch.Tensor:
+    """Allocate ``out`` [T,H] BF16 and run the forward."""
+    T, H = _TH(residual)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=residual.device)
+    mhc_h_aggregate_fwd(residual, pre, out, stream)
+    return out
+
+
+def h_aggregate_backward(grad_out: torch.Tensor, residual: torch.Tensor, pre: torch.Tensor,
+                         stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Allocate and return (grad_residual [T,4,H] BF16, grad_pre [T,4] FP32)."""
+    T, H = _TH(residual)
+    grad_residual = torch.empty((T, 4, H), dtype=torch.bfloat16, device=residual.device)
+    grad_pre = torch.empty((T, 4), dtype=torch.float32, device=residual.device)
+    mhc_h_aggregate_bwd(grad_out, residual, pre, grad_residual, grad_pre, stream)
+    return grad_residual, grad_pre

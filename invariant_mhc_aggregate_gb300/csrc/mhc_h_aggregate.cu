@@ -1,0 +1,583 @@
+// Batch-invariant mHC pre "H Aggregate" for GB300 (sm_103a): forward and
+// fused backward kernels behind the C ABI declared in mhc_h_aggregate.h.
+//
+// Source: "Add batch-invariant h_aggregate kernel" (RL-Kernel pull request
+// 366).  Summary: residual [T,4,H] BF16, pre [T,4] FP32, out [T,H] BF16,
+//   out = bf16((pre0*r0 + pre1*r1) + (pre2*r2 + pre3*r3)).
+// Batch invariance: one writer per output, no atomics, FP32 __fmul_rn /
+// __fadd_rn, the fixed (0 + 1) + (2 + 3) tree, BF16 only at the boundaries.
+// The backward answers that page's reviewer request; its formula is the exact
+// derivative of the Summary formula and its grad_pre order (ORDER-256) is
+// defined in mhc_h_aggregate.h.
+//
+// Design (GB300, HBM-bound: about 0.7 FP32 operations per byte moved):
+//  * Forward: a flat grid over 16-byte chunks of the output (8 BF16 values).
+//    A thread loads the four residual chunks that feed its output chunk with
+//    16-byte streaming loads and the token's pre as one 16-byte load, and
+//    stores one 16-byte chunk.  Large calls give each thread UNROLL chunks,
+//    all loads issued before any arithmetic, to keep enough bytes in flight
+//    per SM; small (decode) calls give each thread one chunk so that the
+//    work spreads over as many SMs as possible.  The arithmetic of an element
+//    never depends on the grid, the block or T.
+//  * Backward: one 256-thread block per token (grid-stride over tokens).
+//    Thread j is lane j of ORDER-256: it streams the chunks c = j, j+256, ...
+//    of g and the four residual rows, writes grad_residual for them, and
+//    accumulates the chunk partials of grad_pre in increasing c.  Lanes fold
+//    with warp shuffles (strides 16..1) and the 8 warps through shared memory
+//    (strides 4, 2, 1).  No atomics, no cross-block traffic.
+//  * Narrower paths (H not a multiple of 8, or buffers not 16-byte aligned)
+//    run the same per-element arithmetic and the same grad_pre tree with 4- or
+//    2-byte accesses, so every path gives the same bytes.
+//  * No tensor cores: nothing here is a contraction.
+//  * Built without fast math, with --fmad=false and -ftz=false; the
+//    intrinsics below already forbid contraction and flushing.
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "mhc_h_aggregate.h"
+#include "fastdiv.cuh"
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+
+// --------------------------------------------------------------------------
+// memory access helpers
+// --------------------------------------------------------------------------
+
+// 16-byte load of data read exactly once: read-only path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// 16-byte store of data written exactly once: streaming (evict-first).
+__device__ __forceinline__ void st_stream16(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :
+                 : "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_stream4(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream4(void* p, uint32_t v) {
+    asm volatile("st.global.cs.u32 [%0], %1;" : : "l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint16_t ld_stream2(const void* p) {
+    uint16_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream2(void* p, uint16_t v) {
+    asm volatile("st.global.cs.u16 [%0], %1;" : : "l"(p), "h"(v) : "memory");
+}
+
+// pre[t] is read by every thread of the token: keep it in L1.
+__device__ __forceinline__ float4 ld_pre16(const float* p) {
+    return __ldg(reinterpret_cast<const float4*>(p));
+}
+
+__device__ __forceinline__ float4 ld_pre4x(const float* p) {
+    return make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
+}
+
+// --------------------------------------------------------------------------
+// BF16 <-> FP32 (widening is exact: the BF16 pattern is the upper half)
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_one(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+// Two FP32 values -> two BF16 values (round to nearest even), lo in bits 0..15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint16_t to_bf16(float x) {
+    __nv_bfloat16 v = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t*>(&v);
+}
+
+// --------------------------------------------------------------------------
+// the forward element: four RN products, the (0 + 1) + (2 + 3) tree
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ float h_agg(const float4 p, float r0, float r1, float r2, float r3) {
+    const float p0 = __fmul_rn(p.x, r0);
+    const float p1 = __fmul_rn(p.y, r1);
+    const float p2 = __fmul_rn(p.z, r2);
+    const float p3 = __fmul_rn(p.w, r3);
+    return __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3));
+}
+
+// Two adjacent elements held as BF16 pairs in one 32-bit word per k.
+__device__ __forceinline__ uint32_t h_agg_pair(const float4 p, uint32_t w0, uint32_t w1,
+                                               uint32_t w2, uint32_t w3) {
+    const float lo = h_agg(p, bf16_lo(w0), bf16_lo(w1), bf16_lo(w2), bf16_lo(w3));
+    const float hi = h_agg(p, bf16_hi(w0), bf16_hi(w1), bf16_hi(w2), bf16_hi(w3));
+    return pack_bf16x2(lo, hi);
+}
+
+__device__ __forceinline__ uint4 h_agg_chunk(const float4 p, const uint4 r0, const uint4 r1,
+                                             const uint4 r2, const uint4 r3) {
+    uint4 o;
+    o.x = h_agg_pair(p, r0.x, r1.x, r2.x, r3.x);
+    o.y = h_agg_pair(p, r0.y, r1.y, r2.y, r3.y);
+    o.z = h_agg_pair(p, r0.z, r1.z, r2.z, r3.z);
+    o.w = h_agg_pair(p, r0.w, r1.w, r2.w, r3.w);
+    return o;
+}
+
+// --------------------------------------------------------------------------
+// forward kernels
+// --------------------------------------------------------------------------
+
+// 16-byte path.  Chunk i of the output (i = t*C + c, C = H/8) is out4[i]; its
+// residual chunks are res4[t*4C + k*C + c] = res4[i + 3tC + kC].
+template <int BLOCK, int UNROLL, bool PRE_VEC>
+__global__ void __launch_bounds__(BLOCK)
+h_agg_fwd_vec16_kernel(const uint4* __restrict__ res4, const float* __restrict__ pre,
+                       uint4* __restrict__ out4, uint32_t n_chunks, uint32_t C,
+                       FastDivU32 divC) {
+    const uint32_t first = blockIdx.x * uint32_t(BLOCK * UNROLL) + threadIdx.x;
+    uint4 r[UNROLL][4];
+    float4 p[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+        const uint32_t i = first + uint32_t(u * BLOCK);
+        if (i < n_chunks) {
+            const uint32_t t = fastdiv_u32(i, divC);
+            const uint4* src = res4 + (uint64_t(i) + 3ull * uint64_t(t) * C);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) r[u][k] = ld_stream16(src + uint64_t(k) * C);
+            p[u] = PRE_VEC ? ld_pre16(pre + 4ull * t) : ld_pre4x(pre + 4ull * t);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+        const uint32_t i = first + uint32_t(u * BLOCK);
+        if (i < n_chunks) st_stream16(out4 + i, h_agg_chunk(p[u], r[u][0], r[u][1], r[u][2], r[u][3]));
+    }
+}
+
+// 4-byte path (H even): pair i = t*P + c, P = H/2.
+__global__ void __launch_bounds__(256)
+h_agg_fwd_pair_kernel(const uint32_t* __restrict__ res2, const float* __restrict__ pre,
+                      uint32_t* __restrict__ out2, uint64_t n_pairs, uint64_t P) {
+    const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+    for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_pairs; i += stride) {
+        const uint64_t t = i / P;
+        const uint32_t* src = res2 + (i + 3 * t * P);
+        const uint32_t w0 = ld_stream4(src);
+        const uint32_t w1 = ld_stream4(src + P);
+        const uint32_t w2 = ld_stream4(src + 2 * P);
+        const uint32_t w3 = ld_stream4(src + 3 * P);
+        st_stream4(out2 + i, h_agg_pair(ld_pre4x(pre + 4 * t), w0, w1, w2, w3));
+    }
+}
+
+// 2-byte path (any H, any 2-byte alignment): element i = t*H + h.
+__global__ void __launch_bounds__(256)
+h_agg_fwd_element_kernel(const uint16_t* __restrict__ res, const float* __restrict__ pre,
+                         uint16_t* __restrict__ out, uint64_t n, uint64_t H) {
+    const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+    for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const uint64_t t = i / H;
+        const uint16_t* src = res + (i + 3 * t * H);
+        const float r0 = bf16_one(ld_stream2(src));
+        const float r1 = bf16_one(ld_stream2(src + H));
+        const float r2 = bf16_one(ld_stream2(src + 2 * H));
+        const float r3 = bf16_one(ld_stream2(src + 3 * H));
+        st_stream2(out + i, to_bf16(h_agg(ld_pre4x(pre + 4 * t), r0, r1, r2, r3)));
+    }
+}
+
+// --------------------------------------------------------------------------
+// backward
+// --------------------------------------------------------------------------
+
+constexpr int kLanes = 256;   // ORDER-256 lanes == threads of a backward block
+constexpr int kWarps = kLanes / 32;
+// Chunks a backward thread keeps in registers per pass, and the blocks per SM
+// the register budget is sized for (launch shape only; the sums do not depend
+// on either).
+#ifndef MHC_BWD_BATCH
+#define MHC_BWD_BATCH 2
+#endif
+#ifndef MHC_BWD_MIN_BLOCKS
+#define MHC_BWD_MIN_BLOCKS 3
+#endif
+constexpr int kBwdBatch = MHC_BWD_BATCH;
+constexpr int kBwdMinBlocks = MHC_BWD_MIN_BLOCKS;
+
+// grad_residual for two adjacent elements: bf16(RN(pre_k * g)).
+__device__ __forceinline__ uint32_t scale_pair(float pk, uint32_t gw) {
+    return pack_bf16x2(__fmul_rn(pk, bf16_lo(gw)), __fmul_rn(pk, bf16_hi(gw)));
+}
+
+__device__ __forceinline__ uint4 scale_chunk(float pk, const uint4 g) {
+    return make_uint4(scale_pair(pk, g.x), scale_pair(pk, g.y), scale_pair(pk, g.z),
+                      scale_pair(pk, g.w));
+}
+
+// ((q0+q1)+(q2+q3)) + ((q4+q5)+(q6+q7)) of q_e = g_e * r_e (exact products).
+__device__ __forceinline__ float chunk_partial(const uint4 g, const uint4 r) {
+    const float q0 = __fmul_rn(bf16_lo(g.x), bf16_lo(r.x));
+    const float q1 = __fmul_rn(bf16_hi(g.x), bf16_hi(r.x));
+    const float q2 = __fmul_rn(bf16_lo(g.y), bf16_lo(r.y));
+    const float q3 = __fmul_rn(bf16_hi(g.y), bf16_hi(r.y));
+    const float q4 = __fmul_rn(bf16_lo(g.z), bf16_lo(r.z));
+    const float q5 = __fmul_rn(bf16_hi(g.z), bf16_hi(r.z));
+    const float q6 = __fmul_rn(bf16_lo(g.w), bf16_lo(r.w));
+    const float q7 = __fmul_rn(bf16_hi(g.w), bf16_hi(r.w));
+    return __fadd_rn(__fadd_rn(__fadd_rn(q0, q1), __fadd_rn(q2, q3)),
+                     __fadd_rn(__fadd_rn(q4, q5), __fadd_rn(q6, q7)));
+}
+
+__device__ __forceinline__ float chunk_partial8(const float q[8]) {
+    return __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
+                     __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
+}
+
+// Steps 4 and 5 of ORDER-256: fold the 256 lane values acc[k] of this block
+// and write grad_pre[t, 0..3].  Must be called by all 256 threads.
+__device__ __forceinline__ void fold_lanes_and_store(float acc[4], float (*red)[4],
+                                                     float* __restrict__ grad_pre_t) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+        for (int s = 16; s >= 1; s >>= 1) acc[k] = __fadd_rn(acc[k], __shfl_xor_sync(0xffffffffu, acc[k], s));
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) red[warp][k] = acc[k];
+    }
+    __syncthreads();
+    if (threadIdx.x < 4) {
+        const int k = threadIdx.x;
+        float w[kWarps];
+#pragma unroll
+        for (int i = 0; i < kWarps; ++i) w[i] = red[i][k];
+#pragma unroll
+        for (int s = kWarps / 2; s >= 1; s >>= 1) {
+#pragma unroll
+            for (int i = 0; i < s; ++i) w[i] = __fadd_rn(w[i], w[i + s]);
+        }
+        grad_pre_t[k] = w[0];
+    }
+    __syncthreads();  // red[] is reused by the next token of this block
+}
+
+// 16-byte path: H % 8 == 0, g / residual / grad_residual 16-byte aligned.
+// A thread holds up to BATCH chunks in registers per pass over its lane.
+template <int BATCH, int MIN_BLOCKS, bool PRE_VEC>
+__global__ void __launch_bounds__(kLanes, MIN_BLOCKS)
+h_agg_bwd_vec16_kernel(const uint4* __restrict__ g4, const uint4* __restrict__ res4,
+                       const float* __restrict__ pre, uint4* __restrict__ gres4,
+                       float* __restrict__ grad_pre, uint64_t T, uint32_t C) {
+    __shared__ float red[kWarps][4];
+    const uint32_t j = threadIdx.x;
+    for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        const float4 p = PRE_VEC ? ld_pre16(pre + 4 * t) : ld_pre4x(pre + 4 * t);
+        const uint4* gt = g4 + t * C;
+        const uint4* rt = res4 + 4 * t * C;
+        uint4* grt = gres4 + 4 * t * C;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (uint32_t c0 = j; c0 < C; c0 += uint32_t(kLanes * BATCH)) {
+            uint4 gv[BATCH];
+            uint4 rv[BATCH][4];
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const uint32_t c = c0 + uint32_t(b * kLanes);
+                if (c < C) {
+                    gv[b] = ld_stream16(gt + c);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) rv[b][k] = ld_stream16(rt + uint64_t(k) * C + c);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const uint32_t c = c0 + uint32_t(b * kLanes);
+                if (c < C) {
+                    st_stream16(grt + c, scale_chunk(p.x, gv[b]));
+                    st_stream16(grt + uint64_t(C) + c, scale_chunk(p.y, gv[b]));
+                    st_stream16(grt + 2 * uint64_t(C) + c, scale_chunk(p.z, gv[b]));
+                    st_stream16(grt + 3 * uint64_t(C) + c, scale_chunk(p.w, gv[b]));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) acc[k] = __fadd_rn(acc[k], chunk_partial(gv[b], rv[b][k]));
+                }
+            }
+        }
+        fold_lanes_and_store(acc, red, grad_pre + 4 * t);
+    }
+}
+
+// 2-byte path: any H and any 2-byte alignment; same lanes, chunks and tree,
+// with positions past H contributing +0.0.
+__global__ void __launch_bounds__(kLanes)
+h_agg_bwd_element_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ res,
+                         const float* __restrict__ pre, uint16_t* __restrict__ gres,
+                         float* __restrict__ grad_pre, uint64_t T, uint64_t H) {
+    __shared__ float red[kWarps][4];
+    const uint64_t C = (H + 7) / 8;
+    for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        const float4 p = ld_pre4x(pre + 4 * t);
+        const float pk[4] = {p.x, p.y, p.z, p.w};
+        const uint16_t* gt = g + t * H;
+        const uint16_t* rt = res + 4 * t * H;
+        uint16_t* grt = gres + 4 * t * H;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (uint64_t c = threadIdx.x; c < C; c += kLanes) {
+            float gf[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint64_t h = 8 * c + e;
+                gf[e] = (h < H) ? bf16_one(ld_stream2(gt + h)) : 0.0f;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float q[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint64_t h = 8 * c + e;
+                    if (h < H) {
+                        q[e] = __fmul_rn(gf[e], bf16_one(ld_stream2(rt + uint64_t(k) * H + h)));
+                        st_stream2(grt + uint64_t(k) * H + h, to_bf16(__fmul_rn(pk[k], gf[e])));
+                    } else {
+                        q[e] = 0.0f;
+                    }
+                }
+                acc[k] = __fadd_rn(acc[k], chunk_partial8(q));
+            }
+        }
+        fold_lanes_and_store(acc, red, grad_pre + 4 * t);
+    }
+}
+
+// --------------------------------------------------------------------------
+// host side: validation, path choice, launch
+// --------------------------------------------------------------------------
+
+thread_local int32_t g_last_cuda_error = 0;
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+inline Range range_of(const void* p, uint64_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + uintptr_t(bytes)};
+}
+
+inline bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Byte counts of [T,4,H] BF16 etc., or false when they overflow int64.
+inline bool sizes_ok(int64_t T, int64_t H) {
+    if (T < 0 || H <= 0) return false;
+    if (T == 0) return true;
+    const int64_t lim = INT64_MAX / 8;  // residual bytes = 8 * T * H
+    return H <= lim / T;
+}
+
+// SM count of the current device, used only to size grids (never the arithmetic).
+int num_sms() {
+    static std::atomic<int> cached{0};
+    int n = cached.load(std::memory_order_relaxed);
+    if (n == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            n = 152;
+        }
+        cached.store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+mhc_status_t finish_launch() {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        g_last_cuda_error = int32_t(e);
+        return MHC_ERR_CUDA;
+    }
+    return MHC_OK;
+}
+
+mhc_path_t fwd_path(const void* residual, const float* pre, const void* out, int64_t T, int64_t H) {
+    if (!sizes_ok(T, H) || T == 0) return MHC_PATH_NONE;
+    if (!residual || !pre || !out) return MHC_PATH_NONE;
+    if (!aligned(residual, 2) || !aligned(out, 2) || !aligned(pre, 4)) return MHC_PATH_NONE;
+    const uint64_t res_bytes = uint64_t(T) * 8 * uint64_t(H);
+    const Range ro = range_of(out, uint64_t(T) * 2 * uint64_t(H));
+    if (overlap(ro, range_of(residual, res_bytes)) || overlap(ro, range_of(pre, uint64_t(T) * 16)))
+        return MHC_PATH_NONE;
+    if (H % 8 == 0 && aligned(residual, 16) && aligned(out, 16)) return MHC_PATH_VEC16;
+    if (H % 2 == 0 && aligned(residual, 4) && aligned(out, 4)) return MHC_PATH_PAIR;
+    return MHC_PATH_ELEMENT;
+}
+
+mhc_path_t bwd_path(const void* g, const void* residual, const float* pre, const void* gres,
+                    const float* gpre, int64_t T, int64_t H) {
+    if (!sizes_ok(T, H) || T == 0) return MHC_PATH_NONE;
+    if (!g || !residual || !pre || !gres || !gpre) return MHC_PATH_NONE;
+    if (!aligned(g, 2) || !aligned(residual, 2) || !aligned(gres, 2) || !aligned(pre, 4) ||
+        !aligned(gpre, 4))
+        return MHC_PATH_NONE;
+    const uint64_t TH = uint64_t(T) * uint64_t(H);
+    const Range rgr = range_of(gres, TH * 8);
+    const Range rgp = range_of(gpre, uint64_t(T) * 16);
+    const Range ins[3] = {range_of(g, TH * 2), range_of(residual, TH * 8), range_of(pre, uint64_t(T) * 16)};
+    if (overlap(rgr, rgp)) return MHC_PATH_NONE;
+    for (const Range& in : ins)
+        if (overlap(rgr, in) || overlap(rgp, in)) return MHC_PATH_NONE;
+    if (H % 8 == 0 && aligned(g, 16) && aligned(residual, 16) && aligned(gres, 16)) return MHC_PATH_VEC16;
+    return MHC_PATH_ELEMENT;
+}
+
+template <int BLOCK, int UNROLL>
+void launch_fwd_vec16(const void* residual, const float* pre, void* out, uint32_t n_chunks,
+                      uint32_t C, bool pre_vec, cudaStream_t stream) {
+    const uint32_t per_block = uint32_t(BLOCK * UNROLL);
+    const uint32_t blocks = uint32_t((uint64_t(n_chunks) + per_block - 1) / per_block);
+    const FastDivU32 divC = make_fastdiv_u32(C);
+    const uint4* r = static_cast<const uint4*>(residual);
+    uint4* o = static_cast<uint4*>(out);
+    if (pre_vec)
+        h_agg_fwd_vec16_kernel<BLOCK, UNROLL, true><<<blocks, BLOCK, 0, stream>>>(r, pre, o, n_chunks, C, divC);
+    else
+        h_agg_fwd_vec16_kernel<BLOCK, UNROLL, false><<<blocks, BLOCK, 0, stream>>>(r, pre, o, n_chunks, C, divC);
+}
+
+inline uint32_t grid_for(uint64_t items, uint32_t per_block, uint64_t cap) {
+    uint64_t b = (items + per_block - 1) / per_block;
+    if (b > cap) b = cap;
+    if (b < 1) b = 1;
+    return uint32_t(b);
+}
+
+}  // namespace
+
+// --------------------------------------------------------------------------
+// C ABI
+// --------------------------------------------------------------------------
+
+extern "C" {
+
+int32_t mhc_h_aggregate_abi_version(void) { return kAbiVersion; }
+
+const char* mhc_status_string(mhc_status_t status) {
+    switch (status) {
+        case MHC_OK: return "MHC_OK";
+        case MHC_ERR_INVALID_ARG: return "MHC_ERR_INVALID_ARG: bad size, null, misaligned or overlapping buffer";
+        case MHC_ERR_UNSUPPORTED: return "MHC_ERR_UNSUPPORTED";
+        case MHC_ERR_CUDA: return "MHC_ERR_CUDA: kernel launch failed (see mhc_h_aggregate_last_cuda_error)";
+    }
+    return "unknown mhc_status_t";
+}
+
+int32_t mhc_h_aggregate_last_cuda_error(void) { return g_last_cuda_error; }
+
+mhc_path_t mhc_h_aggregate_fwd_path(const void* residual, const float* pre, const void* out,
+                                    int64_t T, int64_t H) {
+    return fwd_path(residual, pre, out, T, H);
+}
+
+mhc_path_t mhc_h_aggregate_bwd_path(const void* grad_out, const void* residual, const float* pre,
+                                    const void* grad_residual, const float* grad_pre, int64_t T,
+                                    int64_t H) {
+    return bwd_path(grad_out, residual, pre, grad_residual, grad_pre, T, H);
+}
+
+mhc_status_t mhc_h_aggregate_fwd(const void* residual, const float* pre, void* out, int64_t T,
+                                 int64_t H, mhc_stream_t stream_) {
+    if (!sizes_ok(T, H)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    const mhc_path_t path = fwd_path(residual, pre, out, T, H);
+    if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const bool pre_vec = aligned(pre, 16);
+    const uint64_t cap = uint64_t(num_sms()) * 64;
+
+    if (path == MHC_PATH_VEC16) {
+        // Chunk indices are 32-bit: a call with 2^31 chunks or more runs as
+        // several launches over consecutive token ranges.  Tokens are
+        // independent, so the bytes are the same as one launch.
+        const uint64_t C = uint64_t(H) / 8;
+        const uint64_t max_tokens = 0x7FFFFFFFull / C;
+        if (max_tokens == 0) return MHC_ERR_UNSUPPORTED;  // H >= 2^34
+        for (uint64_t t0 = 0; t0 < uint64_t(T); t0 += max_tokens) {
+            const uint64_t nt = (uint64_t(T) - t0 < max_tokens) ? uint64_t(T) - t0 : max_tokens;
+            const uint32_t n_chunks = uint32_t(nt * C);
+            const void* r = static_cast<const char*>(residual) + t0 * 8 * uint64_t(H);
+            const float* p = pre + 4 * t0;
+            void* o = static_cast<char*>(out) + t0 * 2 * uint64_t(H);
+            // Decode-sized calls: one chunk per thread, 128-thread blocks, to
+            // reach as many SMs as possible.  Larger calls: 4 chunks per thread.
+            if (n_chunks <= uint32_t(num_sms()) * 512u)
+                launch_fwd_vec16<128, 1>(r, p, o, n_chunks, uint32_t(C), pre_vec, stream);
+            else
+                launch_fwd_vec16<256, 4>(r, p, o, n_chunks, uint32_t(C), pre_vec, stream);
+        }
+    } else if (path == MHC_PATH_PAIR) {
+        const uint64_t P = uint64_t(H) / 2;
+        const uint64_t n = uint64_t(T) * P;
+        h_agg_fwd_pair_kernel<<<grid_for(n, 256, cap * 16), 256, 0, stream>>>(
+            static_cast<const uint32_t*>(residual), pre, static_cast<uint32_t*>(out), n, P);
+    } else {
+        const uint64_t n = uint64_t(T) * uint64_t(H);
+        h_agg_fwd_element_kernel<<<grid_for(n, 256, cap * 16), 256, 0, stream>>>(
+            static_cast<const uint16_t*>(residual), pre, static_cast<uint16_t*>(out), n, uint64_t(H));
+    }
+    return finish_launch();
+}
+
+mhc_status_t mhc_h_aggregate_bwd(const void* grad_out, const void* residual, const float* pre,
+                                 void* grad_residual, float* grad_pre, int64_t T, int64_t H,
+                                 mhc_stream_t stream_) {
+    if (!sizes_ok(T, H)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    const mhc_path_t path = bwd_path(grad_out, residual, pre, grad_residual, grad_pre, T, H);
+    if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const uint32_t blocks = grid_for(uint64_t(T), 1, uint64_t(num_sms()) * 256);
+
+    if (path == MHC_PATH_VEC16 && uint64_t(H) / 8 <= 0xFFFFFFFFull) {
+        const uint32_t C = uint32_t(H / 8);
+        const uint4* g4 = static_cast<const uint4*>(grad_out);
+        const uint4* r4 = static_cast<const uint4*>(residual);
+        uint4* gr4 = static_cast<uint4*>(grad_residual);
+        if (aligned(pre, 16))
+            h_agg_bwd_vec16_kernel<kBwdBatch, kBwdMinBlocks, true><<<blocks, kLanes, 0, stream>>>(
+                g4, r4, pre, gr4, grad_pre, uint64_t(T), C);
+        else
+            h_agg_bwd_vec16_kernel<kBwdBatch, kBwdMinBlocks, false><<<blocks, kLanes, 0, stream>>>(
+                g4, r4, pre, gr4, grad_pre, uint64_t(T), C);
+    } else {
+        h_agg_bwd_element_kernel<<<blocks, kLanes, 0, stream>>>(
+            static_cast<const uint16_t*>(grad_out), static_cast<const uint16_t*>(residual), pre,
+            static_cast<uint16_t*>(grad_residual), grad_pre, uint64_t(T), uint64_t(H));
+    }
+    return finish_launch();
+}
+
+}  // extern "C"

@@ -1,0 +1,200 @@
+"""The C-ABI library on the host: it builds, loads, exports what the header
+declares, picks paths and rejects bad arguments without touching a GPU."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from invariant_mhc_aggregate_gb300 import _build, binding
+
+HEADER = os.path.join(_build.INCLUDE, "mhc_h_aggregate.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return binding.load()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(mhc_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_binding_exports():
+    assert tuple(header_functions()) == binding.EXPORTS
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_exported_symbols_are_c_linkage():
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    names = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in header_functions():
+        assert name in names, f"{name} not exported with C linkage"
+
+
+def test_abi_version(lib):
+    assert lib.mhc_h_aggregate_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for s in range(4):
+        assert lib.mhc_status_string(s).decode().startswith("MHC_")
+    assert b"unknown" in lib.mhc_status_string(99)
+
+
+# --- path selection: pure host logic on addresses that are never dereferenced
+
+A = 1 << 40          # a 256-byte aligned fake device address
+GAP = 1 << 34        # keeps fake buffers apart
+
+
+def fpath(r_off=0, p_off=0, o_off=0, T=4, H=4096):
+    return binding.fwd_path_raw(A + r_off, A + GAP + p_off, A + 2 * GAP + o_off, T, H)
+
+
+def bpath(g_off=0, r_off=0, p_off=0, gr_off=0, gp_off=0, T=4, H=4096):
+    return binding.bwd_path_raw(A + g_off, A + GAP + r_off, A + 2 * GAP + p_off,
+                                A + 3 * GAP + gr_off, A + 4 * GAP + gp_off, T, H)
+
+
+def test_fwd_path_choice(lib):
+    assert fpath() == binding.MHC_PATH_VEC16
+    assert fpath(p_off=4) == binding.MHC_PATH_VEC16          # pre only needs 4 bytes
+    assert fpath(r_off=4) == binding.MHC_PATH_PAIR
+    assert fpath(o_off=8) == binding.MHC_PATH_PAIR
+    assert fpath(r_off=2) == binding.MHC_PATH_ELEMENT
+    assert fpath(H=2050) == binding.MHC_PATH_PAIR
+    assert fpath(H=1279) == binding.MHC_PATH_ELEMENT
+    assert fpath(H=4097) == binding.MHC_PATH_ELEMENT
+    assert fpath(r_off=1) == binding.MHC_PATH_NONE           # not BF16 aligned
+    assert fpath(p_off=2) == binding.MHC_PATH_NONE           # not FP32 aligned
+    assert fpath(T=0) == binding.MHC_PATH_NONE
+    assert fpath(T=-1) == binding.MHC_PATH_NONE
+    assert fpath(H=0) == binding.MHC_PATH_NONE
+
+
+def test_bwd_path_choice(lib):
+    assert bpath() == binding.MHC_PATH_VEC16
+    assert bpath(p_off=4, gp_off=4) == binding.MHC_PATH_VEC16
+    assert bpath(g_off=2) == binding.MHC_PATH_ELEMENT
+    assert bpath(gr_off=4) == binding.MHC_PATH_ELEMENT
+    assert bpath(H=2050) == binding.MHC_PATH_ELEMENT
+    assert bpath(H=13) == binding.MHC_PATH_ELEMENT
+    assert bpath(gp_off=2) == binding.MHC_PATH_NONE
+    assert bpath(T=0) == binding.MHC_PATH_NONE
+
+
+def test_fwd_rejects_overlap(lib):
+    T, H = 4, 64
+    # out starts inside residual
+    assert binding.fwd_path_raw(A, A + GAP, A + 16, T, H) == binding.MHC_PATH_NONE
+    # out overlaps pre
+    assert binding.fwd_path_raw(A, A + GAP, A + GAP + 32, T, H) == binding.MHC_PATH_NONE
+    # out right after residual is fine
+    assert binding.fwd_path_raw(A, A + GAP, A + T * 4 * H * 2, T, H) == binding.MHC_PATH_VEC16
+
+
+def test_bwd_rejects_overlap(lib):
+    T, H = 4, 64
+    g, r, p = A, A + GAP, A + 2 * GAP
+    assert binding.bwd_path_raw(g, r, p, r, A + 3 * GAP, T, H) == binding.MHC_PATH_NONE
+    assert binding.bwd_path_raw(g, r, p, A + 3 * GAP, A + 3 * GAP + 64, T, H) == binding.MHC_PATH_NONE
+    assert binding.bwd_path_raw(g, r, p, A + 3 * GAP, g, T, H) == binding.MHC_PATH_NONE
+
+
+# --- entry points: rejected calls return before any CUDA call
+
+def test_fwd_invalid_arguments(lib):
+    ok = dict(residual=A, pre=A + GAP, out=A + 2 * GAP)
+    assert binding.fwd_raw(ok["residual"], ok["pre"], ok["out"], -1, 8) == binding.MHC_ERR_INVALID_ARG
+    assert binding.fwd_raw(ok["residual"], ok["pre"], ok["out"], 1, 0) == binding.MHC_ERR_INVALID_ARG
+    assert binding.fwd_raw(0, ok["pre"], ok["out"], 1, 8) == binding.MHC_ERR_INVALID_ARG
+    assert binding.fwd_raw(ok["residual"], 0, ok["out"], 1, 8) == binding.MHC_ERR_INVALID_ARG
+    assert binding.fwd_raw(ok["residual"], ok["pre"], 0, 1, 8) == binding.MHC_ERR_INVALID_ARG
+    assert binding.fwd_raw(ok["residual"] + 1, ok["pre"], ok["out"], 1, 8) == binding.MHC_ERR_INVALID_ARG
+    assert binding.fwd_raw(ok["residual"], ok["pre"], ok["residual"], 1, 8) == binding.MHC_ERR_INVALID_ARG
+    # byte count of residual overflows int64
+    assert binding.fwd_raw(ok["residual"], ok["pre"], ok["out"], 1 << 32, 1 << 29) == binding.MHC_ERR_INVALID_ARG
+
+
+def test_bwd_invalid_arguments(lib):
+    args = [A, A + GAP, A + 2 * GAP, A + 3 * GAP, A + 4 * GAP]
+    assert binding.bwd_raw(*args, -5, 8) == binding.MHC_ERR_INVALID_ARG
+    assert binding.bwd_raw(*args, 1, -8) == binding.MHC_ERR_INVALID_ARG
+    for i in range(5):
+        bad = list(args)
+        bad[i] = 0
+        assert binding.bwd_raw(*bad, 2, 8) == binding.MHC_ERR_INVALID_ARG, i
+    bad = list(args)
+    bad[4] += 2
+    assert binding.bwd_raw(*bad, 2, 8) == binding.MHC_ERR_INVALID_ARG
+
+
+def test_zero_tokens_is_a_noop(lib):
+    # T == 0 succeeds without a launch, even with NULL pointers
+    assert binding.fwd_raw(0, 0, 0, 0, 4096) == binding.MHC_OK
+    assert binding.bwd_raw(0, 0, 0, 0, 0, 0, 4096) == binding.MHC_OK
+    assert lib.mhc_h_aggregate_last_cuda_error() == 0
+
+
+# --- build settings
+
+def test_build_has_no_fast_math():
+    flags = " ".join(_build.NVCC_FLAGS)
+    assert "use_fast_math" not in flags
+    assert "--fmad=false" in flags and "-ftz=false" in flags
+    assert "arch=compute_103a,code=sm_103a" in flags
+
+
+def test_kernels_use_rn_intrinsics_only():
+    src = open(_build.SOURCES[0]).read()
+    code = re.sub(r"//.*", "", src)
+    assert "__fmaf" not in code and "fmaf(" not in code and "__fma_rn" not in code
+    # one writer per output element: no device atomics or reductions
+    assert not re.search(r"\batomic[A-Z]\w*\(|\bred\.|\batom\.", code)
+
+
+def test_fastdiv_exhaustive_sample(tmp_path):
+    """The launch-time divider in csrc/fastdiv.cuh, compiled as host C++."""
+    prog = tmp_path / "fd.cpp"
+    prog.write_text(r'''
+#include "fastdiv.cuh"
+#include <cstdio>
+#include <cstdint>
+int main() {
+    uint64_t bad = 0, n_checked = 0;
+    const uint32_t ds[] = {1u, 2u, 3u, 7u, 8u, 160u, 255u, 256u, 257u, 512u, 513u, 896u,
+                           1279u, 2050u, 4097u, 7168u, 65535u, 65536u, 1000003u,
+                           0x7FFFFFFFu, 0x80000000u, 0x80000001u, 0xFFFFFFFEu, 0xFFFFFFFFu};
+    for (uint32_t d : ds) {
+        FastDivU32 f = make_fastdiv_u32(d);
+        uint64_t x = 0x9E3779B97F4A7C15ull;
+        for (int i = 0; i < 200000; ++i) {
+            x ^= x << 13; x ^= x >> 7; x ^= x << 17;
+            uint32_t n = uint32_t(x);
+            if (i < 4096) n = uint32_t(i);
+            if (i >= 4096 && i < 8192) n = 0xFFFFFFFFu - uint32_t(i - 4096);
+            if (i >= 8192 && i < 12288) n = uint32_t(uint64_t(d) * uint32_t(i - 8192) + (i & 1 ? d - 1 : 0));
+            ++n_checked;
+            if (fastdiv_u32(n, f) != n / d) { if (bad < 5) printf("d=%u n=%u\n", d, n); ++bad; }
+        }
+    }
+    printf("checked %llu bad %llu\n", (unsigned long long)n_checked, (unsigned long long)bad);
+    return bad != 0;
+}
+''')
+    exe = tmp_path / "fd"
+    subprocess.run(["g++", "-std=c++17", "-O2", "-I", _build.CSRC, "-o", str(exe), str(prog)],
+                   check=True)
+    res = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert res.returncode == 0, res.stdout
