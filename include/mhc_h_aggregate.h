@@ -37,9 +37,10 @@
  * Layout.  Dense row-major: residual[t][k][h] at element (t*4 + k)*H + h;
  * pre[t][k] at t*4 + k; out and g at t*H + h; grad_residual like residual;
  * grad_pre like pre.  BF16 buffers are 2-byte aligned, FP32 buffers 4-byte
- * aligned.  Any such alignment is accepted; 16-byte-aligned buffers with
- * H % 8 == 0 take the 16-byte vector path, others a narrower path with
- * identical results.
+ * aligned.  Any such alignment is accepted: 32-byte-aligned BF16 buffers
+ * with H % 16 == 0 take the 32-byte vector path, 16-byte-aligned ones with
+ * H % 8 == 0 the 16-byte path, others a narrower path; all give identical
+ * results.
  *
  * Pointers and ownership.  Every data pointer is a DEVICE pointer (or managed
  * memory) allocated and owned by the caller.  The library allocates nothing,
@@ -51,7 +52,8 @@
  * Errors.  T == 0 returns MHC_OK without launching.  T < 0, H <= 0, a NULL
  * pointer, a misaligned pointer, a size whose byte count overflows int64, or
  * an output that overlaps an input or another output returns
- * MHC_ERR_INVALID_ARG without launching.  A failed launch returns
+ * MHC_ERR_INVALID_ARG without launching; H / 8 >= 2^31 on a vector path
+ * returns MHC_ERR_UNSUPPORTED.  A failed launch returns
  * MHC_ERR_CUDA; the CUDA error code is then available from
  * mhc_h_aggregate_last_cuda_error() on the same thread.  Faults during
  * execution surface, as usual in CUDA, at the caller's next synchronisation.
@@ -81,8 +83,9 @@ typedef enum mhc_status {
 typedef enum mhc_path {
     MHC_PATH_NONE = -1,   /* the call would be rejected or launches nothing */
     MHC_PATH_VEC16 = 0,   /* 16-byte loads/stores: H % 8 == 0, buffers 16-byte aligned */
-    MHC_PATH_PAIR = 1,    /* 4-byte loads/stores: H even, buffers 4-byte aligned */
-    MHC_PATH_ELEMENT = 2  /* 2-byte loads/stores: any H and alignment */
+    MHC_PATH_PAIR = 1,    /* 4-byte loads/stores: H even, buffers 4-byte aligned (forward only) */
+    MHC_PATH_ELEMENT = 2, /* 2-byte loads/stores: any H and alignment */
+    MHC_PATH_VEC32 = 3    /* 32-byte loads/stores: H % 16 == 0, buffers 32-byte aligned */
 } mhc_path_t;
 
 /* Version of this ABI; changes when a declaration here changes. */

@@ -29,8 +29,9 @@ MHC_PATH_NONE = -1
 MHC_PATH_VEC16 = 0
 MHC_PATH_PAIR = 1
 MHC_PATH_ELEMENT = 2
+MHC_PATH_VEC32 = 3
 PATH_NAMES = {MHC_PATH_NONE: "none", MHC_PATH_VEC16: "vec16", MHC_PATH_PAIR: "pair",
-              MHC_PATH_ELEMENT: "element"}
+              MHC_PATH_ELEMENT: "element", MHC_PATH_VEC32: "vec32"}
 
 #: Every symbol the header declares, in declaration order.
 EXPORTS = (

@@ -11,20 +11,25 @@
 // defined in mhc_h_aggregate.h.
 //
 // Design (GB300, HBM-bound: about 0.7 FP32 operations per byte moved):
-//  * Forward: a flat grid over 16-byte chunks of the output (8 BF16 values).
-//    A thread loads the four residual chunks that feed its output chunk with
-//    16-byte streaming loads and the token's pre as one 16-byte load, and
-//    stores one 16-byte chunk.  Large calls give each thread UNROLL chunks,
-//    all loads issued before any arithmetic, to keep enough bytes in flight
-//    per SM; small (decode) calls give each thread one chunk so that the
-//    work spreads over as many SMs as possible.  The arithmetic of an element
-//    never depends on the grid, the block or T.
-//  * Backward: one 256-thread block per token (grid-stride over tokens).
-//    Thread j is lane j of ORDER-256: it streams the chunks c = j, j+256, ...
-//    of g and the four residual rows, writes grad_residual for them, and
-//    accumulates the chunk partials of grad_pre in increasing c.  Lanes fold
-//    with warp shuffles (strides 16..1) and the 8 warps through shared memory
-//    (strides 4, 2, 1).  No atomics, no cross-block traffic.
+//  * Vector paths move NW 32-bit words per access: NW = 8 uses the 256-bit
+//    (32-byte) global loads and stores that sm_100-class GPUs added
+//    (ld/st .v8.b32), NW = 4 the 16-byte ones.  One access covers 2*NW BF16
+//    values, i.e. NW/4 "chunks" of 8 values.
+//  * Forward: a flat grid over output vectors.  A thread loads the four
+//    residual vectors feeding its output vector with streaming loads and the
+//    token's pre as one 16-byte load, and stores one vector.  Large calls
+//    give each thread UNROLL vectors, all loads issued before any arithmetic,
+//    to keep enough bytes in flight per SM; decode-sized calls give each
+//    thread one vector so the work spreads over as many SMs as possible.  The
+//    arithmetic of an element never depends on the grid, the block or T.
+//  * Backward: one block per token (grid-stride over tokens) whose threads
+//    own the 256 lanes of ORDER-256, NW/4 lanes each: thread j holds the
+//    chunks of lanes (NW/4)*j .. (NW/4)*j + NW/4 - 1, which are adjacent, so
+//    one vector access serves all of them.  It streams g and the four residual
+//    rows, writes grad_residual, and adds the chunk partials of each lane in
+//    increasing chunk order.  Groups of 32 lanes fold with warp shuffles (and
+//    one in-thread add when a thread holds two lanes), the 8 groups through
+//    shared memory.  No atomics, no cross-block traffic.
 //  * Narrower paths (H not a multiple of 8, or buffers not 16-byte aligned)
 //    run the same per-element arithmetic and the same grad_pre tree with 4- or
 //    2-byte accesses, so every path gives the same bytes.
@@ -49,20 +54,52 @@ constexpr int kAbiVersion = 1;
 // memory access helpers
 // --------------------------------------------------------------------------
 
-// 16-byte load of data read exactly once: read-only path, no L1 allocation.
-__device__ __forceinline__ uint4 ld_stream16(const void* p) {
-    uint4 v;
+template <int NW>
+struct Words {
+    uint32_t w[NW];
+};
+
+// Vector load of data read exactly once: read-only path, no L1 allocation.
+template <int NW>
+__device__ __forceinline__ Words<NW> ld_stream(const void* p);
+
+template <>
+__device__ __forceinline__ Words<4> ld_stream<4>(const void* p) {
+    Words<4> v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
                  : "l"(p));
     return v;
 }
 
-// 16-byte store of data written exactly once: streaming (evict-first).
-__device__ __forceinline__ void st_stream16(void* p, uint4 v) {
+template <>
+__device__ __forceinline__ Words<8> ld_stream<8>(const void* p) {
+    Words<8> v;
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]),
+                   "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
+                 : "l"(p));
+    return v;
+}
+
+// Vector store of data written exactly once: streaming (evict-first).
+template <int NW>
+__device__ __forceinline__ void st_stream(void* p, const Words<NW>& v);
+
+template <>
+__device__ __forceinline__ void st_stream<4>(void* p, const Words<4>& v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};"
                  :
-                 : "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
+                 : "memory");
+}
+
+template <>
+__device__ __forceinline__ void st_stream<8>(void* p, const Words<8>& v) {
+    asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :
+                 : "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]),
+                   "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
                  : "memory");
 }
 
@@ -93,6 +130,11 @@ __device__ __forceinline__ float4 ld_pre16(const float* p) {
 
 __device__ __forceinline__ float4 ld_pre4x(const float* p) {
     return make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
+}
+
+template <bool PRE_VEC>
+__device__ __forceinline__ float4 ld_pre(const float* p) {
+    return PRE_VEC ? ld_pre16(p) : ld_pre4x(p);
 }
 
 // --------------------------------------------------------------------------
@@ -134,13 +176,11 @@ __device__ __forceinline__ uint32_t h_agg_pair(const float4 p, uint32_t w0, uint
     return pack_bf16x2(lo, hi);
 }
 
-__device__ __forceinline__ uint4 h_agg_chunk(const float4 p, const uint4 r0, const uint4 r1,
-                                             const uint4 r2, const uint4 r3) {
-    uint4 o;
-    o.x = h_agg_pair(p, r0.x, r1.x, r2.x, r3.x);
-    o.y = h_agg_pair(p, r0.y, r1.y, r2.y, r3.y);
-    o.z = h_agg_pair(p, r0.z, r1.z, r2.z, r3.z);
-    o.w = h_agg_pair(p, r0.w, r1.w, r2.w, r3.w);
+template <int NW>
+__device__ __forceinline__ Words<NW> h_agg_vec(const float4 p, const Words<NW> (&r)[4]) {
+    Words<NW> o;
+#pragma unroll
+    for (int e = 0; e < NW; ++e) o.w[e] = h_agg_pair(p, r[0].w[e], r[1].w[e], r[2].w[e], r[3].w[e]);
     return o;
 }
 
@@ -148,31 +188,31 @@ __device__ __forceinline__ uint4 h_agg_chunk(const float4 p, const uint4 r0, con
 // forward kernels
 // --------------------------------------------------------------------------
 
-// 16-byte path.  Chunk i of the output (i = t*C + c, C = H/8) is out4[i]; its
-// residual chunks are res4[t*4C + k*C + c] = res4[i + 3tC + kC].
-template <int BLOCK, int UNROLL, bool PRE_VEC>
+// Vector path.  Output vector i (i = t*V + v, V = H / (2*NW) vectors per row)
+// is out[i]; the residual vector of row k is res[t*4V + k*V + v] =
+// res[i + 3tV + kV].
+template <int NW, int BLOCK, int UNROLL, bool PRE_VEC>
 __global__ void __launch_bounds__(BLOCK)
-h_agg_fwd_vec16_kernel(const uint4* __restrict__ res4, const float* __restrict__ pre,
-                       uint4* __restrict__ out4, uint32_t n_chunks, uint32_t C,
-                       FastDivU32 divC) {
+h_agg_fwd_vec_kernel(const Words<NW>* __restrict__ res, const float* __restrict__ pre,
+                     Words<NW>* __restrict__ out, uint32_t n_vec, uint32_t V, FastDivU32 divV) {
     const uint32_t first = blockIdx.x * uint32_t(BLOCK * UNROLL) + threadIdx.x;
-    uint4 r[UNROLL][4];
+    Words<NW> r[UNROLL][4];
     float4 p[UNROLL];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
         const uint32_t i = first + uint32_t(u * BLOCK);
-        if (i < n_chunks) {
-            const uint32_t t = fastdiv_u32(i, divC);
-            const uint4* src = res4 + (uint64_t(i) + 3ull * uint64_t(t) * C);
+        if (i < n_vec) {
+            const uint32_t t = fastdiv_u32(i, divV);
+            const Words<NW>* src = res + (uint64_t(i) + 3ull * uint64_t(t) * V);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) r[u][k] = ld_stream16(src + uint64_t(k) * C);
-            p[u] = PRE_VEC ? ld_pre16(pre + 4ull * t) : ld_pre4x(pre + 4ull * t);
+            for (int k = 0; k < 4; ++k) r[u][k] = ld_stream<NW>(src + uint64_t(k) * V);
+            p[u] = ld_pre<PRE_VEC>(pre + 4ull * t);
         }
     }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
         const uint32_t i = first + uint32_t(u * BLOCK);
-        if (i < n_chunks) st_stream16(out4 + i, h_agg_chunk(p[u], r[u][0], r[u][1], r[u][2], r[u][3]));
+        if (i < n_vec) st_stream<NW>(out + i, h_agg_vec<NW>(p[u], r[u]));
     }
 }
 
@@ -212,40 +252,34 @@ h_agg_fwd_element_kernel(const uint16_t* __restrict__ res, const float* __restri
 // backward
 // --------------------------------------------------------------------------
 
-constexpr int kLanes = 256;   // ORDER-256 lanes == threads of a backward block
-constexpr int kWarps = kLanes / 32;
-// Chunks a backward thread keeps in registers per pass, and the blocks per SM
-// the register budget is sized for (launch shape only; the sums do not depend
-// on either).
-#ifndef MHC_BWD_BATCH
-#define MHC_BWD_BATCH 2
-#endif
-#ifndef MHC_BWD_MIN_BLOCKS
-#define MHC_BWD_MIN_BLOCKS 3
-#endif
-constexpr int kBwdBatch = MHC_BWD_BATCH;
-constexpr int kBwdMinBlocks = MHC_BWD_MIN_BLOCKS;
+constexpr int kLanes = 256;   // lanes of ORDER-256
+constexpr int kGroups = 8;    // groups of 32 lanes
 
 // grad_residual for two adjacent elements: bf16(RN(pre_k * g)).
 __device__ __forceinline__ uint32_t scale_pair(float pk, uint32_t gw) {
     return pack_bf16x2(__fmul_rn(pk, bf16_lo(gw)), __fmul_rn(pk, bf16_hi(gw)));
 }
 
-__device__ __forceinline__ uint4 scale_chunk(float pk, const uint4 g) {
-    return make_uint4(scale_pair(pk, g.x), scale_pair(pk, g.y), scale_pair(pk, g.z),
-                      scale_pair(pk, g.w));
+template <int NW>
+__device__ __forceinline__ Words<NW> scale_vec(float pk, const Words<NW>& g) {
+    Words<NW> o;
+#pragma unroll
+    for (int e = 0; e < NW; ++e) o.w[e] = scale_pair(pk, g.w[e]);
+    return o;
 }
 
-// ((q0+q1)+(q2+q3)) + ((q4+q5)+(q6+q7)) of q_e = g_e * r_e (exact products).
-__device__ __forceinline__ float chunk_partial(const uint4 g, const uint4 r) {
-    const float q0 = __fmul_rn(bf16_lo(g.x), bf16_lo(r.x));
-    const float q1 = __fmul_rn(bf16_hi(g.x), bf16_hi(r.x));
-    const float q2 = __fmul_rn(bf16_lo(g.y), bf16_lo(r.y));
-    const float q3 = __fmul_rn(bf16_hi(g.y), bf16_hi(r.y));
-    const float q4 = __fmul_rn(bf16_lo(g.z), bf16_lo(r.z));
-    const float q5 = __fmul_rn(bf16_hi(g.z), bf16_hi(r.z));
-    const float q6 = __fmul_rn(bf16_lo(g.w), bf16_lo(r.w));
-    const float q7 = __fmul_rn(bf16_hi(g.w), bf16_hi(r.w));
+// ((q0+q1)+(q2+q3)) + ((q4+q5)+(q6+q7)) of q_e = g_e * r_e (exact products)
+// for the chunk held in words w0 .. w0+3 of g and r.
+template <int NW>
+__device__ __forceinline__ float chunk_partial(const Words<NW>& g, const Words<NW>& r, int w0) {
+    const float q0 = __fmul_rn(bf16_lo(g.w[w0 + 0]), bf16_lo(r.w[w0 + 0]));
+    const float q1 = __fmul_rn(bf16_hi(g.w[w0 + 0]), bf16_hi(r.w[w0 + 0]));
+    const float q2 = __fmul_rn(bf16_lo(g.w[w0 + 1]), bf16_lo(r.w[w0 + 1]));
+    const float q3 = __fmul_rn(bf16_hi(g.w[w0 + 1]), bf16_hi(r.w[w0 + 1]));
+    const float q4 = __fmul_rn(bf16_lo(g.w[w0 + 2]), bf16_lo(r.w[w0 + 2]));
+    const float q5 = __fmul_rn(bf16_hi(g.w[w0 + 2]), bf16_hi(r.w[w0 + 2]));
+    const float q6 = __fmul_rn(bf16_lo(g.w[w0 + 3]), bf16_lo(r.w[w0 + 3]));
+    const float q7 = __fmul_rn(bf16_hi(g.w[w0 + 3]), bf16_hi(r.w[w0 + 3]));
     return __fadd_rn(__fadd_rn(__fadd_rn(q0, q1), __fadd_rn(q2, q3)),
                      __fadd_rn(__fadd_rn(q4, q5), __fadd_rn(q6, q7)));
 }
@@ -255,29 +289,38 @@ __device__ __forceinline__ float chunk_partial8(const float q[8]) {
                      __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
 }
 
-// Steps 4 and 5 of ORDER-256: fold the 256 lane values acc[k] of this block
-// and write grad_pre[t, 0..3].  Must be called by all 256 threads.
-__device__ __forceinline__ void fold_lanes_and_store(float acc[4], float (*red)[4],
+// Steps 4 and 5 of ORDER-256 for a block of 256/LPT threads, thread j holding
+// lanes LPT*j + l (l < LPT) in acc[l][k].  A group of 32 lanes is 32/LPT
+// adjacent threads: lane strides 16 .. LPT are thread strides 16/LPT .. 1
+// (xor shuffles), lane stride 1 (when LPT == 2) is the add of a thread's own
+// two lanes.  The 8 group values then fold with strides 4, 2, 1 in shared
+// memory, and grad_pre[t, 0..3] is written.  All threads of the block call it.
+template <int LPT>
+__device__ __forceinline__ void fold_lanes_and_store(float (&acc)[LPT][4], float (*red)[4],
                                                      float* __restrict__ grad_pre_t) {
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
+    constexpr int kThreadsPerGroup = 32 / LPT;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
 #pragma unroll
-        for (int s = 16; s >= 1; s >>= 1) acc[k] = __fadd_rn(acc[k], __shfl_xor_sync(0xffffffffu, acc[k], s));
-    }
-    if (lane == 0) {
+        for (int s = kThreadsPerGroup / 2; s >= 1; s >>= 1) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) red[warp][k] = acc[k];
+            for (int l = 0; l < LPT; ++l)
+                acc[l][k] = __fadd_rn(acc[l][k], __shfl_xor_sync(0xffffffffu, acc[l][k], s));
+        }
+        if (LPT == 2) acc[0][k] = __fadd_rn(acc[0][k], acc[LPT - 1][k]);
+    }
+    if ((threadIdx.x % kThreadsPerGroup) == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) red[threadIdx.x / kThreadsPerGroup][k] = acc[0][k];
     }
     __syncthreads();
     if (threadIdx.x < 4) {
         const int k = threadIdx.x;
-        float w[kWarps];
+        float w[kGroups];
 #pragma unroll
-        for (int i = 0; i < kWarps; ++i) w[i] = red[i][k];
+        for (int i = 0; i < kGroups; ++i) w[i] = red[i][k];
 #pragma unroll
-        for (int s = kWarps / 2; s >= 1; s >>= 1) {
+        for (int s = kGroups / 2; s >= 1; s >>= 1) {
 #pragma unroll
             for (int i = 0; i < s; ++i) w[i] = __fadd_rn(w[i], w[i + s]);
         }
@@ -286,57 +329,69 @@ __device__ __forceinline__ void fold_lanes_and_store(float acc[4], float (*red)[
     __syncthreads();  // red[] is reused by the next token of this block
 }
 
-// 16-byte path: H % 8 == 0, g / residual / grad_residual 16-byte aligned.
-// A thread holds up to BATCH chunks in registers per pass over its lane.
-template <int BATCH, int MIN_BLOCKS, bool PRE_VEC>
-__global__ void __launch_bounds__(kLanes, MIN_BLOCKS)
-h_agg_bwd_vec16_kernel(const uint4* __restrict__ g4, const uint4* __restrict__ res4,
-                       const float* __restrict__ pre, uint4* __restrict__ gres4,
-                       float* __restrict__ grad_pre, uint64_t T, uint32_t C) {
-    __shared__ float red[kWarps][4];
+// Vector path: H % (2*NW) == 0 and g / residual / grad_residual aligned to
+// 4*NW bytes.  V = H / (2*NW) vectors per row; thread j handles vectors
+// j, j + B, j + 2B, ... (B = 256/LPT threads), i.e. for lane LPT*j + l the
+// chunks LPT*(j + mB) + l = (LPT*j + l) + 256m: exactly that lane's chunks,
+// in increasing order.  Up to BATCH vectors per thread are held in registers
+// per pass.
+template <int NW, int BATCH, int MIN_BLOCKS, bool PRE_VEC>
+__global__ void __launch_bounds__(kLanes / (NW / 4), MIN_BLOCKS)
+h_agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict__ res,
+                     const float* __restrict__ pre, Words<NW>* __restrict__ gres,
+                     float* __restrict__ grad_pre, uint64_t T, uint32_t V) {
+    constexpr int LPT = NW / 4;
+    constexpr uint32_t B = kLanes / LPT;
+    __shared__ float red[kGroups][4];
     const uint32_t j = threadIdx.x;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        const float4 p = PRE_VEC ? ld_pre16(pre + 4 * t) : ld_pre4x(pre + 4 * t);
-        const uint4* gt = g4 + t * C;
-        const uint4* rt = res4 + 4 * t * C;
-        uint4* grt = gres4 + 4 * t * C;
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (uint32_t c0 = j; c0 < C; c0 += uint32_t(kLanes * BATCH)) {
-            uint4 gv[BATCH];
-            uint4 rv[BATCH][4];
+        const float4 p4 = ld_pre<PRE_VEC>(pre + 4 * t);
+        const float pk[4] = {p4.x, p4.y, p4.z, p4.w};
+        const Words<NW>* gt = g + t * V;
+        const Words<NW>* rt = res + 4 * t * V;
+        Words<NW>* grt = gres + 4 * t * V;
+        float acc[LPT][4];
+#pragma unroll
+        for (int l = 0; l < LPT; ++l)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[l][k] = 0.0f;
+        for (uint32_t v0 = j; v0 < V; v0 += B * BATCH) {
+            Words<NW> gv[BATCH];
+            Words<NW> rv[BATCH][4];
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) {
-                const uint32_t c = c0 + uint32_t(b * kLanes);
-                if (c < C) {
-                    gv[b] = ld_stream16(gt + c);
+                const uint32_t v = v0 + uint32_t(b) * B;
+                if (v < V) {
+                    gv[b] = ld_stream<NW>(gt + v);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) rv[b][k] = ld_stream16(rt + uint64_t(k) * C + c);
+                    for (int k = 0; k < 4; ++k) rv[b][k] = ld_stream<NW>(rt + uint64_t(k) * V + v);
                 }
             }
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) {
-                const uint32_t c = c0 + uint32_t(b * kLanes);
-                if (c < C) {
-                    st_stream16(grt + c, scale_chunk(p.x, gv[b]));
-                    st_stream16(grt + uint64_t(C) + c, scale_chunk(p.y, gv[b]));
-                    st_stream16(grt + 2 * uint64_t(C) + c, scale_chunk(p.z, gv[b]));
-                    st_stream16(grt + 3 * uint64_t(C) + c, scale_chunk(p.w, gv[b]));
+                const uint32_t v = v0 + uint32_t(b) * B;
+                if (v < V) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) acc[k] = __fadd_rn(acc[k], chunk_partial(gv[b], rv[b][k]));
+                    for (int k = 0; k < 4; ++k) {
+                        st_stream<NW>(grt + uint64_t(k) * V + v, scale_vec<NW>(pk[k], gv[b]));
+#pragma unroll
+                        for (int l = 0; l < LPT; ++l)
+                            acc[l][k] = __fadd_rn(acc[l][k], chunk_partial<NW>(gv[b], rv[b][k], 4 * l));
+                    }
                 }
             }
         }
-        fold_lanes_and_store(acc, red, grad_pre + 4 * t);
+        fold_lanes_and_store<LPT>(acc, red, grad_pre + 4 * t);
     }
 }
 
 // 2-byte path: any H and any 2-byte alignment; same lanes, chunks and tree,
-// with positions past H contributing +0.0.
+// with positions past H contributing +0.0.  256 threads, one lane each.
 __global__ void __launch_bounds__(kLanes)
 h_agg_bwd_element_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ res,
                          const float* __restrict__ pre, uint16_t* __restrict__ gres,
                          float* __restrict__ grad_pre, uint64_t T, uint64_t H) {
-    __shared__ float red[kWarps][4];
+    __shared__ float red[kGroups][4];
     const uint64_t C = (H + 7) / 8;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
         const float4 p = ld_pre4x(pre + 4 * t);
@@ -344,7 +399,7 @@ h_agg_bwd_element_kernel(const uint16_t* __restrict__ g, const uint16_t* __restr
         const uint16_t* gt = g + t * H;
         const uint16_t* rt = res + 4 * t * H;
         uint16_t* grt = gres + 4 * t * H;
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float acc[1][4] = {{0.0f, 0.0f, 0.0f, 0.0f}};
         for (uint64_t c = threadIdx.x; c < C; c += kLanes) {
             float gf[8];
 #pragma unroll
@@ -365,10 +420,10 @@ h_agg_bwd_element_kernel(const uint16_t* __restrict__ g, const uint16_t* __restr
                         q[e] = 0.0f;
                     }
                 }
-                acc[k] = __fadd_rn(acc[k], chunk_partial8(q));
+                acc[0][k] = __fadd_rn(acc[0][k], chunk_partial8(q));
             }
         }
-        fold_lanes_and_store(acc, red, grad_pre + 4 * t);
+        fold_lanes_and_store<1>(acc, red, grad_pre + 4 * t);
     }
 }
 
@@ -431,6 +486,7 @@ mhc_path_t fwd_path(const void* residual, const float* pre, const void* out, int
     const Range ro = range_of(out, uint64_t(T) * 2 * uint64_t(H));
     if (overlap(ro, range_of(residual, res_bytes)) || overlap(ro, range_of(pre, uint64_t(T) * 16)))
         return MHC_PATH_NONE;
+    if (H % 16 == 0 && aligned(residual, 32) && aligned(out, 32)) return MHC_PATH_VEC32;
     if (H % 8 == 0 && aligned(residual, 16) && aligned(out, 16)) return MHC_PATH_VEC16;
     if (H % 2 == 0 && aligned(residual, 4) && aligned(out, 4)) return MHC_PATH_PAIR;
     return MHC_PATH_ELEMENT;
@@ -450,22 +506,9 @@ mhc_path_t bwd_path(const void* g, const void* residual, const float* pre, const
     if (overlap(rgr, rgp)) return MHC_PATH_NONE;
     for (const Range& in : ins)
         if (overlap(rgr, in) || overlap(rgp, in)) return MHC_PATH_NONE;
+    if (H % 16 == 0 && aligned(g, 32) && aligned(residual, 32) && aligned(gres, 32)) return MHC_PATH_VEC32;
     if (H % 8 == 0 && aligned(g, 16) && aligned(residual, 16) && aligned(gres, 16)) return MHC_PATH_VEC16;
     return MHC_PATH_ELEMENT;
-}
-
-template <int BLOCK, int UNROLL>
-void launch_fwd_vec16(const void* residual, const float* pre, void* out, uint32_t n_chunks,
-                      uint32_t C, bool pre_vec, cudaStream_t stream) {
-    const uint32_t per_block = uint32_t(BLOCK * UNROLL);
-    const uint32_t blocks = uint32_t((uint64_t(n_chunks) + per_block - 1) / per_block);
-    const FastDivU32 divC = make_fastdiv_u32(C);
-    const uint4* r = static_cast<const uint4*>(residual);
-    uint4* o = static_cast<uint4*>(out);
-    if (pre_vec)
-        h_agg_fwd_vec16_kernel<BLOCK, UNROLL, true><<<blocks, BLOCK, 0, stream>>>(r, pre, o, n_chunks, C, divC);
-    else
-        h_agg_fwd_vec16_kernel<BLOCK, UNROLL, false><<<blocks, BLOCK, 0, stream>>>(r, pre, o, n_chunks, C, divC);
 }
 
 inline uint32_t grid_for(uint64_t items, uint32_t per_block, uint64_t cap) {
@@ -473,6 +516,79 @@ inline uint32_t grid_for(uint64_t items, uint32_t per_block, uint64_t cap) {
     if (b > cap) b = cap;
     if (b < 1) b = 1;
     return uint32_t(b);
+}
+
+template <int NW, int BLOCK, int UNROLL>
+void launch_fwd_vec(const void* residual, const float* pre, void* out, uint32_t n_vec, uint32_t V,
+                    bool pre_vec, cudaStream_t stream) {
+    const uint32_t per_block = uint32_t(BLOCK * UNROLL);
+    const uint32_t blocks = uint32_t((uint64_t(n_vec) + per_block - 1) / per_block);
+    const FastDivU32 divV = make_fastdiv_u32(V);
+    const Words<NW>* r = static_cast<const Words<NW>*>(residual);
+    Words<NW>* o = static_cast<Words<NW>*>(out);
+    if (pre_vec)
+        h_agg_fwd_vec_kernel<NW, BLOCK, UNROLL, true><<<blocks, BLOCK, 0, stream>>>(r, pre, o, n_vec, V, divV);
+    else
+        h_agg_fwd_vec_kernel<NW, BLOCK, UNROLL, false><<<blocks, BLOCK, 0, stream>>>(r, pre, o, n_vec, V, divV);
+}
+
+// Launch shapes of the vector forward (launch-time only; results do not
+// depend on them).  Large calls: 256 threads, 64 bytes of output each
+// (2 vectors of 32 bytes or 4 of 16); calls of at most 8 KiB of output per
+// SM: 128 threads x 1 vector, to spread a decode-sized call over more SMs.
+template <int NW>
+void fwd_vec(const void* residual, const float* pre, void* out, uint64_t T, uint64_t H,
+             bool pre_vec, cudaStream_t stream) {
+    constexpr uint64_t kElemsPerVec = 2 * NW;
+    const uint64_t V = H / kElemsPerVec;
+    // Vector indices are 32-bit: a call with 2^31 vectors or more runs as
+    // several launches over consecutive token ranges.  Tokens are
+    // independent, so the bytes are the same as one launch.
+    const uint64_t max_tokens = 0x7FFFFFFFull / V;
+    const uint64_t small_limit = uint64_t(num_sms()) * (8192 / (4 * NW));
+    for (uint64_t t0 = 0; t0 < T; t0 += max_tokens) {
+        const uint64_t nt = (T - t0 < max_tokens) ? T - t0 : max_tokens;
+        const uint32_t n_vec = uint32_t(nt * V);
+        const void* r = static_cast<const char*>(residual) + t0 * 8 * H;
+        const float* p = pre + 4 * t0;
+        void* o = static_cast<char*>(out) + t0 * 2 * H;
+        if (n_vec <= small_limit)
+            launch_fwd_vec<NW, 128, 1>(r, p, o, n_vec, uint32_t(V), pre_vec, stream);
+        else
+            launch_fwd_vec<NW, 256, 16 / NW>(r, p, o, n_vec, uint32_t(V), pre_vec, stream);
+    }
+}
+
+// Backward vector launch shapes: 32-byte vectors with 128 threads (2 lanes
+// each), 4 vectors per pass, register budget for 2 blocks per SM; 16-byte
+// vectors with 256 threads, 2 per pass, 3 blocks per SM.
+template <int NW>
+struct BwdShape;
+template <>
+struct BwdShape<8> {
+    static constexpr int kBatch = 4, kMinBlocks = 2;
+};
+template <>
+struct BwdShape<4> {
+    static constexpr int kBatch = 2, kMinBlocks = 3;
+};
+
+template <int NW>
+void bwd_vec(const void* g, const void* residual, const float* pre, void* gres, float* gpre,
+             uint64_t T, uint64_t H, cudaStream_t stream) {
+    constexpr int kThreads = kLanes / (NW / 4);
+    constexpr int kBatch = BwdShape<NW>::kBatch, kMinBlocks = BwdShape<NW>::kMinBlocks;
+    const uint32_t V = uint32_t(H / (2 * NW));
+    const uint32_t blocks = grid_for(T, 1, uint64_t(num_sms()) * 256);
+    const Words<NW>* gv = static_cast<const Words<NW>*>(g);
+    const Words<NW>* rv = static_cast<const Words<NW>*>(residual);
+    Words<NW>* grv = static_cast<Words<NW>*>(gres);
+    if (aligned(pre, 16))
+        h_agg_bwd_vec_kernel<NW, kBatch, kMinBlocks, true><<<blocks, kThreads, 0, stream>>>(
+            gv, rv, pre, grv, gpre, T, V);
+    else
+        h_agg_bwd_vec_kernel<NW, kBatch, kMinBlocks, false><<<blocks, kThreads, 0, stream>>>(
+            gv, rv, pre, grv, gpre, T, V);
 }
 
 }  // namespace
@@ -489,7 +605,7 @@ const char* mhc_status_string(mhc_status_t status) {
     switch (status) {
         case MHC_OK: return "MHC_OK";
         case MHC_ERR_INVALID_ARG: return "MHC_ERR_INVALID_ARG: bad size, null, misaligned or overlapping buffer";
-        case MHC_ERR_UNSUPPORTED: return "MHC_ERR_UNSUPPORTED";
+        case MHC_ERR_UNSUPPORTED: return "MHC_ERR_UNSUPPORTED: H too large for the 32-bit row index";
         case MHC_ERR_CUDA: return "MHC_ERR_CUDA: kernel launch failed (see mhc_h_aggregate_last_cuda_error)";
     }
     return "unknown mhc_status_t";
@@ -516,36 +632,22 @@ mhc_status_t mhc_h_aggregate_fwd(const void* residual, const float* pre, void* o
     if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     const bool pre_vec = aligned(pre, 16);
-    const uint64_t cap = uint64_t(num_sms()) * 64;
+    const uint64_t cap = uint64_t(num_sms()) * 1024;
+    if ((path == MHC_PATH_VEC32 || path == MHC_PATH_VEC16) && uint64_t(H) / 8 > 0x7FFFFFFFull)
+        return MHC_ERR_UNSUPPORTED;
 
-    if (path == MHC_PATH_VEC16) {
-        // Chunk indices are 32-bit: a call with 2^31 chunks or more runs as
-        // several launches over consecutive token ranges.  Tokens are
-        // independent, so the bytes are the same as one launch.
-        const uint64_t C = uint64_t(H) / 8;
-        const uint64_t max_tokens = 0x7FFFFFFFull / C;
-        if (max_tokens == 0) return MHC_ERR_UNSUPPORTED;  // H >= 2^34
-        for (uint64_t t0 = 0; t0 < uint64_t(T); t0 += max_tokens) {
-            const uint64_t nt = (uint64_t(T) - t0 < max_tokens) ? uint64_t(T) - t0 : max_tokens;
-            const uint32_t n_chunks = uint32_t(nt * C);
-            const void* r = static_cast<const char*>(residual) + t0 * 8 * uint64_t(H);
-            const float* p = pre + 4 * t0;
-            void* o = static_cast<char*>(out) + t0 * 2 * uint64_t(H);
-            // Decode-sized calls: one chunk per thread, 128-thread blocks, to
-            // reach as many SMs as possible.  Larger calls: 4 chunks per thread.
-            if (n_chunks <= uint32_t(num_sms()) * 512u)
-                launch_fwd_vec16<128, 1>(r, p, o, n_chunks, uint32_t(C), pre_vec, stream);
-            else
-                launch_fwd_vec16<256, 4>(r, p, o, n_chunks, uint32_t(C), pre_vec, stream);
-        }
+    if (path == MHC_PATH_VEC32) {
+        fwd_vec<8>(residual, pre, out, uint64_t(T), uint64_t(H), pre_vec, stream);
+    } else if (path == MHC_PATH_VEC16) {
+        fwd_vec<4>(residual, pre, out, uint64_t(T), uint64_t(H), pre_vec, stream);
     } else if (path == MHC_PATH_PAIR) {
         const uint64_t P = uint64_t(H) / 2;
         const uint64_t n = uint64_t(T) * P;
-        h_agg_fwd_pair_kernel<<<grid_for(n, 256, cap * 16), 256, 0, stream>>>(
+        h_agg_fwd_pair_kernel<<<grid_for(n, 256, cap), 256, 0, stream>>>(
             static_cast<const uint32_t*>(residual), pre, static_cast<uint32_t*>(out), n, P);
     } else {
         const uint64_t n = uint64_t(T) * uint64_t(H);
-        h_agg_fwd_element_kernel<<<grid_for(n, 256, cap * 16), 256, 0, stream>>>(
+        h_agg_fwd_element_kernel<<<grid_for(n, 256, cap), 256, 0, stream>>>(
             static_cast<const uint16_t*>(residual), pre, static_cast<uint16_t*>(out), n, uint64_t(H));
     }
     return finish_launch();
@@ -559,20 +661,15 @@ mhc_status_t mhc_h_aggregate_bwd(const void* grad_out, const void* residual, con
     const mhc_path_t path = bwd_path(grad_out, residual, pre, grad_residual, grad_pre, T, H);
     if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    const uint32_t blocks = grid_for(uint64_t(T), 1, uint64_t(num_sms()) * 256);
+    if ((path == MHC_PATH_VEC32 || path == MHC_PATH_VEC16) && uint64_t(H) / 8 > 0xFFFFFFFFull)
+        return MHC_ERR_UNSUPPORTED;
 
-    if (path == MHC_PATH_VEC16 && uint64_t(H) / 8 <= 0xFFFFFFFFull) {
-        const uint32_t C = uint32_t(H / 8);
-        const uint4* g4 = static_cast<const uint4*>(grad_out);
-        const uint4* r4 = static_cast<const uint4*>(residual);
-        uint4* gr4 = static_cast<uint4*>(grad_residual);
-        if (aligned(pre, 16))
-            h_agg_bwd_vec16_kernel<kBwdBatch, kBwdMinBlocks, true><<<blocks, kLanes, 0, stream>>>(
-                g4, r4, pre, gr4, grad_pre, uint64_t(T), C);
-        else
-            h_agg_bwd_vec16_kernel<kBwdBatch, kBwdMinBlocks, false><<<blocks, kLanes, 0, stream>>>(
-                g4, r4, pre, gr4, grad_pre, uint64_t(T), C);
+    if (path == MHC_PATH_VEC32) {
+        bwd_vec<8>(grad_out, residual, pre, grad_residual, grad_pre, uint64_t(T), uint64_t(H), stream);
+    } else if (path == MHC_PATH_VEC16) {
+        bwd_vec<4>(grad_out, residual, pre, grad_residual, grad_pre, uint64_t(T), uint64_t(H), stream);
     } else {
+        const uint32_t blocks = grid_for(uint64_t(T), 1, uint64_t(num_sms()) * 256);
         h_agg_bwd_element_kernel<<<blocks, kLanes, 0, stream>>>(
             static_cast<const uint16_t*>(grad_out), static_cast<const uint16_t*>(residual), pre,
             static_cast<uint16_t*>(grad_residual), grad_pre, uint64_t(T), uint64_t(H));

@@ -57,14 +57,44 @@ class DevBuf:
                     and np.all(host[self.start + self.nbytes:] == CANARY))
 
 
+def _align_of(offset: int) -> int:
+    """Alignment of a DevBuf placed at `offset` bytes past a 256-byte boundary."""
+    if offset == 0:
+        return 256
+    return offset & -offset
+
+
+def expected_fwd_path(H: int, offsets) -> int:
+    a = min(_align_of(offsets[0]), _align_of(offsets[2]))
+    if H % 16 == 0 and a >= 32:
+        return binding.MHC_PATH_VEC32
+    if H % 8 == 0 and a >= 16:
+        return binding.MHC_PATH_VEC16
+    if H % 2 == 0 and a >= 4:
+        return binding.MHC_PATH_PAIR
+    return binding.MHC_PATH_ELEMENT
+
+
+def expected_bwd_path(H: int, offsets) -> int:
+    a = min(_align_of(offsets[0]), _align_of(offsets[1]), _align_of(offsets[3]))
+    if H % 16 == 0 and a >= 32:
+        return binding.MHC_PATH_VEC32
+    if H % 8 == 0 and a >= 16:
+        return binding.MHC_PATH_VEC16
+    return binding.MHC_PATH_ELEMENT
+
+
 def stream_handle() -> int:
     return int(torch.cuda.current_stream().cuda_stream)
 
 
 def run_fwd(residual: torch.Tensor, pre: torch.Tensor, offsets=(0, 0, 0), check_guards=True,
-            expect_path=None) -> np.ndarray:
-    """Forward through the C ABI with residual / pre / out at the given byte offsets."""
+            expect_path="auto") -> np.ndarray:
+    """Forward through the C ABI with residual / pre / out at the given byte offsets;
+    checks that the library picks the path the alignment calls for."""
     T, _, H = residual.shape
+    if expect_path == "auto":
+        expect_path = expected_fwd_path(H, offsets)
     r = DevBuf.of(residual, offsets[0])
     p = DevBuf.of(pre, offsets[1])
     o = DevBuf(T * H * 2, offsets[2])
@@ -79,8 +109,10 @@ def run_fwd(residual: torch.Tensor, pre: torch.Tensor, offsets=(0, 0, 0), check_
 
 
 def run_bwd(g: torch.Tensor, residual: torch.Tensor, pre: torch.Tensor,
-            offsets=(0, 0, 0, 0, 0), check_guards=True, expect_path=None):
+            offsets=(0, 0, 0, 0, 0), check_guards=True, expect_path="auto"):
     T, _, H = residual.shape
+    if expect_path == "auto":
+        expect_path = expected_bwd_path(H, offsets)
     gb = DevBuf.of(g, offsets[0])
     r = DevBuf.of(residual, offsets[1])
     p = DevBuf.of(pre, offsets[2])

@@ -68,8 +68,11 @@ def bpath(g_off=0, r_off=0, p_off=0, gr_off=0, gp_off=0, T=4, H=4096):
 
 
 def test_fwd_path_choice(lib):
-    assert fpath() == binding.MHC_PATH_VEC16
-    assert fpath(p_off=4) == binding.MHC_PATH_VEC16          # pre only needs 4 bytes
+    assert fpath() == binding.MHC_PATH_VEC32
+    assert fpath(p_off=4) == binding.MHC_PATH_VEC32          # pre only needs 4 bytes
+    assert fpath(r_off=16) == binding.MHC_PATH_VEC16
+    assert fpath(o_off=16) == binding.MHC_PATH_VEC16
+    assert fpath(H=4104) == binding.MHC_PATH_VEC16           # H % 16 == 8
     assert fpath(r_off=4) == binding.MHC_PATH_PAIR
     assert fpath(o_off=8) == binding.MHC_PATH_PAIR
     assert fpath(r_off=2) == binding.MHC_PATH_ELEMENT
@@ -84,8 +87,11 @@ def test_fwd_path_choice(lib):
 
 
 def test_bwd_path_choice(lib):
-    assert bpath() == binding.MHC_PATH_VEC16
-    assert bpath(p_off=4, gp_off=4) == binding.MHC_PATH_VEC16
+    assert bpath() == binding.MHC_PATH_VEC32
+    assert bpath(p_off=4, gp_off=4) == binding.MHC_PATH_VEC32
+    assert bpath(g_off=16) == binding.MHC_PATH_VEC16
+    assert bpath(gr_off=16) == binding.MHC_PATH_VEC16
+    assert bpath(H=4104) == binding.MHC_PATH_VEC16
     assert bpath(g_off=2) == binding.MHC_PATH_ELEMENT
     assert bpath(gr_off=4) == binding.MHC_PATH_ELEMENT
     assert bpath(H=2050) == binding.MHC_PATH_ELEMENT
@@ -101,7 +107,7 @@ def test_fwd_rejects_overlap(lib):
     # out overlaps pre
     assert binding.fwd_path_raw(A, A + GAP, A + GAP + 32, T, H) == binding.MHC_PATH_NONE
     # out right after residual is fine
-    assert binding.fwd_path_raw(A, A + GAP, A + T * 4 * H * 2, T, H) == binding.MHC_PATH_VEC16
+    assert binding.fwd_path_raw(A, A + GAP, A + T * 4 * H * 2, T, H) == binding.MHC_PATH_VEC32
 
 
 def test_bwd_rejects_overlap(lib):

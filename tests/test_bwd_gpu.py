@@ -21,7 +21,7 @@ from invariant_mhc_aggregate_gb300.inputs import backward_inputs, workload
 
 pytestmark = pytest.mark.gpu
 
-VEC16, ELEMENT = binding.MHC_PATH_VEC16, binding.MHC_PATH_ELEMENT
+VEC32, VEC16, ELEMENT = binding.MHC_PATH_VEC32, binding.MHC_PATH_VEC16, binding.MHC_PATH_ELEMENT
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -111,14 +111,13 @@ def test_shapes_bit_exact(T, H):
     assert_bytes_equal(gp, want_gp, f"grad_pre T={T} H={H}")
 
 
-@pytest.mark.parametrize("T,H", [(7, 2048), (3, 7168), (2, 4104)])
+@pytest.mark.parametrize("T,H", [(7, 2048), (3, 7168), (2, 4104), (2, 24), (1, 4112)])
 def test_paths_agree(T, H):
     g, res, pre = backward_inputs(T, H, "decode", 16)
     want_gr, want_gp = oracle_bwd(g, res, pre)
-    for offsets, path in (((0, 0, 0, 0, 0), VEC16), ((0, 0, 4, 0, 4), VEC16),
-                          ((2, 0, 0, 0, 0), ELEMENT), ((0, 4, 0, 0, 0), ELEMENT),
-                          ((0, 0, 0, 8, 0), ELEMENT)):
-        gr, gp = run_bwd(g, res, pre, offsets=offsets, expect_path=path)
+    for offsets in ((0, 0, 0, 0, 0), (0, 0, 4, 0, 4), (16, 0, 0, 0, 0), (0, 16, 0, 16, 0),
+                    (2, 0, 0, 0, 0), (0, 4, 0, 0, 0), (0, 0, 0, 8, 0)):
+        gr, gp = run_bwd(g, res, pre, offsets=offsets)
         assert_bytes_equal(gr, want_gr, f"grad_residual offsets={offsets}")
         assert_bytes_equal(gp, want_gp, f"grad_pre offsets={offsets}")
 
@@ -148,7 +147,7 @@ def test_order_cases_on_gpu():
         want[k] = int(expected, 16)
         offsets_list = [(2, 0, 0, 0, 0)]
         if H % 8 == 0:
-            offsets_list.append((0, 0, 0, 0, 0))
+            offsets_list += [(0, 0, 0, 0, 0), (16, 16, 0, 16, 0)]
         for offsets in offsets_list:
             _, gp = run_bwd(gt, rt, torch.from_numpy(pre), offsets=offsets)
             assert np.array_equal(gp.view(np.uint32)[0], want), (name, offsets)
@@ -166,7 +165,7 @@ def test_grad_residual_worked_examples_on_gpu():
         g[t, 5] = int(gbits, 16)
     gt = torch.from_numpy(g.view(np.int16).copy()).view(torch.bfloat16)
     rt = torch.from_numpy(res.view(np.int16).copy()).view(torch.bfloat16)
-    for offsets in ((0, 0, 0, 0, 0), (2, 0, 0, 2, 0)):
+    for offsets in ((0, 0, 0, 0, 0), (16, 16, 0, 16, 0), (2, 0, 0, 2, 0)):
         gr, gp = run_bwd(gt, rt, torch.from_numpy(pre), offsets=offsets)
         for t, (name, pbits, gbits, ebits) in enumerate(rows):
             assert int(gr[t, 1, 5]) == int(ebits, 16), (name, offsets)

@@ -13,13 +13,15 @@ import torch
 
 import oracle
 import _pins
-from _gpu import DevBuf, assert_bytes_equal, lib, run_fwd, sha, stream_handle, u16, f32
+from _gpu import (DevBuf, assert_bytes_equal, expected_fwd_path, lib, run_fwd, sha,
+                  stream_handle, u16, f32)
 from invariant_mhc_aggregate_gb300 import binding
 from invariant_mhc_aggregate_gb300.inputs import forward_inputs, workload
 
 pytestmark = pytest.mark.gpu
 
-VEC16, PAIR, ELEMENT = binding.MHC_PATH_VEC16, binding.MHC_PATH_PAIR, binding.MHC_PATH_ELEMENT
+VEC32, VEC16 = binding.MHC_PATH_VEC32, binding.MHC_PATH_VEC16
+PAIR, ELEMENT = binding.MHC_PATH_PAIR, binding.MHC_PATH_ELEMENT
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -37,7 +39,7 @@ def test_t129_bit_exact_and_split_invariant():
     w = workload("fwd_t129_h4096")
     (T, H), = w.shapes
     res, pre = forward_inputs(T, H, w.recipe, w.seed)
-    full = run_fwd(res, pre, expect_path=VEC16)
+    full = run_fwd(res, pre, expect_path=VEC32)
     assert_bytes_equal(full, oracle_fwd(res, pre), "T=129 vs oracle")
     # 129 one-token calls (a different launch shape) give the same bytes
     r_d, p_d = res.cuda(), pre.cuda()
@@ -77,7 +79,7 @@ def test_ragged_bit_exact(T, H):
 def test_decode_bit_exact(T, H):
     w = workload("fwd_decode")
     res, pre = forward_inputs(T, H, w.recipe, w.seed)
-    got = run_fwd(res, pre, expect_path=VEC16)
+    got = run_fwd(res, pre, expect_path=VEC32)
     assert_bytes_equal(got, oracle_fwd(res, pre), f"decode T={T} H={H}")
 
 
@@ -120,7 +122,8 @@ def test_prefill_t65536_sampled_tokens():
 # --- hand-worked elements through every path
 
 @pytest.mark.parametrize("H,offsets,path", [
-    (8, (0, 0, 0), VEC16), (8, (4, 0, 4), PAIR), (9, (0, 0, 0), ELEMENT), (8, (2, 4, 0), ELEMENT)])
+    (16, (0, 0, 0), VEC32), (8, (0, 0, 0), VEC16), (16, (16, 0, 0), VEC16), (8, (4, 0, 4), PAIR),
+    (9, (0, 0, 0), ELEMENT), (8, (2, 4, 0), ELEMENT)])
 def test_worked_examples_on_gpu(H, offsets, path):
     cases = list(_pins._fwd_cases())
     T = len(cases)
@@ -140,14 +143,17 @@ def test_worked_examples_on_gpu(H, offsets, path):
 
 # --- all paths give the same bytes
 
-@pytest.mark.parametrize("T,H", [(37, 1024), (5, 8), (300, 7168), (1, 4104)])
+@pytest.mark.parametrize("T,H", [(37, 1024), (5, 8), (300, 7168), (1, 4104), (3, 2050)])
 def test_paths_agree(T, H):
     res, pre = forward_inputs(T, H, "decode", 9)
     want = oracle_fwd(res, pre)
-    for offsets, path in (((0, 0, 0), VEC16), ((0, 4, 0), VEC16), ((4, 0, 0), PAIR),
-                          ((0, 0, 8), PAIR), ((2, 0, 0), ELEMENT), ((0, 0, 6), ELEMENT)):
-        got = run_fwd(res, pre, offsets=offsets, expect_path=path)
+    seen = set()
+    for offsets in ((0, 0, 0), (0, 4, 0), (16, 0, 0), (0, 0, 16), (4, 0, 0), (0, 0, 8),
+                    (2, 0, 0), (0, 0, 6)):
+        seen.add(expected_fwd_path(H, offsets))
+        got = run_fwd(res, pre, offsets=offsets)
         assert_bytes_equal(got, want, f"T={T} H={H} offsets={offsets}")
+    assert ELEMENT in seen
 
 
 # --- edge cases
@@ -182,7 +188,7 @@ def test_special_values():
     pre[5] = np.float32(1e-40)                        # subnormal pre
     res_t = torch.from_numpy(res.view(np.int16).copy()).view(torch.bfloat16)
     pre_t = torch.from_numpy(pre)
-    for offsets in ((0, 0, 0), (4, 0, 4), (2, 0, 2)):
+    for offsets in ((0, 0, 0), (16, 0, 16), (4, 0, 4), (2, 0, 2)):
         got = run_fwd(res_t, pre_t, offsets=offsets)
         assert_bytes_equal(got, oracle.fwd(res, pre), f"special values offsets={offsets}")
 
