@@ -86,6 +86,16 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest value of x over all ranks (the step time every rank waits for)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -195,6 +205,7 @@ def run_ours(args):
     import torch
     from invariant_mhc_aggregate_gb300 import _build, binding
     from invariant_mhc_aggregate_gb300.inputs import backward_inputs, forward_inputs
+    from invariant_mhc_aggregate_gb300.sharding import token_range
 
     world, rank, local = dist_env()
     if not torch.cuda.is_available():
@@ -211,7 +222,11 @@ def run_ours(args):
     binding.load()
     digest = _build.source_digest()
     T, H = args.T, args.H
-    # every rank draws its own batch (weak scaling)
+    # Weak scaling: rank r owns tokens token_range(world*T, r, world) of a global
+    # batch of world*T tokens and draws them with its own seed; no data moves
+    # between ranks.
+    t_start, t_stop = token_range(world * T, rank, world)
+    assert t_stop - t_start == T
     g, res, pre = backward_inputs(T, H, "normal", seed=4 + rank, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     grad_res = torch.empty((T, 4, H), dtype=torch.bfloat16, device=dev)
@@ -265,11 +280,7 @@ def run_ours(args):
     fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     step_ms_local = (sum(fwd_ms) + sum(bwd_ms)) / K
-    step_ms = step_ms_local
-    if dist is not None:
-        t = torch.tensor([step_ms_local], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms_local, dist, dev)
 
     bytes_step = (fwd_bytes(T, H) if do_fwd else 0) + (bwd_bytes(T, H) if do_bwd else 0)
     value = bytes_step * world / (step_ms * 1e-3) / 1e9
@@ -311,7 +322,7 @@ def run_ours(args):
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"h_aggregate fwd+bwd, T={T}, H={H}" if args.phase == "both"
                    else f"h_aggregate {args.phase} only, T={T}, H={H}",
-                   "T": T, "H": H, "tokens_per_rank": T,
+                   "T": T, "H": H, "tokens_per_rank": T, "global_tokens": world * T,
                    "values": "residual, g ~ N(0,1) rounded to bf16; pre ~ U(0,1); seed 4+rank",
                    "storage": "bf16 residual/out/g/grad_residual, f32 pre/grad_pre",
                    "l2": ("flushed before every step (256 MiB write, outside the timed events)"
@@ -385,11 +396,7 @@ def e2e_measure(args, torch, binding, g, res, pre, dev, stream, world, dist):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / n
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / n, dist, dev)
     assert torch.equal(hgp, dgp.cpu()) and torch.equal(ho.view(torch.int16), do.cpu().view(torch.int16))
     h2d = hr.numel() * 2 + hp.numel() * 4 + hg.numel() * 2
     d2h = ho.numel() * 2 + hgr.numel() * 2 + hgp.numel() * 4
