@@ -9,4 +9,4 @@ by :mod:`invariant_mhc_aggregate_gb300.binding`, which raises if it has not
 been built (``invariant_mhc_aggregate_gb300._build.build()``).
 """
 
-__all__ = ["binding", "inputs"]
+__all__ = ["autograd", "binding", "inputs", "sharding"]

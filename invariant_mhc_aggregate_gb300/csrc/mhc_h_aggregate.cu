@@ -559,36 +559,45 @@ void fwd_vec(const void* residual, const float* pre, void* out, uint64_t T, uint
     }
 }
 
-// Backward vector launch shapes: 32-byte vectors with 128 threads (2 lanes
-// each), 4 vectors per pass, register budget for 2 blocks per SM; 16-byte
-// vectors with 256 threads, 2 per pass, 3 blocks per SM.
-template <int NW>
-struct BwdShape;
-template <>
-struct BwdShape<8> {
-    static constexpr int kBatch = 4, kMinBlocks = 2;
-};
-template <>
-struct BwdShape<4> {
-    static constexpr int kBatch = 2, kMinBlocks = 3;
-};
-
-template <int NW>
-void bwd_vec(const void* g, const void* residual, const float* pre, void* gres, float* gpre,
-             uint64_t T, uint64_t H, cudaStream_t stream) {
+// Backward vector launch shapes (launch-time only; the sums do not depend on
+// them).  A block holds one token; its threads keep BATCH vectors each in
+// registers per pass, and the register budget is sized for MIN_BLOCKS blocks
+// per SM.  The batch is chosen from the vectors per thread so that a row is
+// covered in one pass where possible and each SM keeps roughly 160 KB of loads
+// in flight: 32-byte vectors (128 threads) use batch 1 / 2 / 4 with 6 / 3 / 2
+// blocks per SM for up to 1 / 2 / more vectors per thread; 16-byte vectors
+// (256 threads) use batch 2 with 3 blocks per SM.
+template <int NW, int BATCH, int MIN_BLOCKS>
+void launch_bwd_vec(const void* g, const void* residual, const float* pre, void* gres, float* gpre,
+                    uint64_t T, uint32_t V, cudaStream_t stream) {
     constexpr int kThreads = kLanes / (NW / 4);
-    constexpr int kBatch = BwdShape<NW>::kBatch, kMinBlocks = BwdShape<NW>::kMinBlocks;
-    const uint32_t V = uint32_t(H / (2 * NW));
     const uint32_t blocks = grid_for(T, 1, uint64_t(num_sms()) * 256);
     const Words<NW>* gv = static_cast<const Words<NW>*>(g);
     const Words<NW>* rv = static_cast<const Words<NW>*>(residual);
     Words<NW>* grv = static_cast<Words<NW>*>(gres);
     if (aligned(pre, 16))
-        h_agg_bwd_vec_kernel<NW, kBatch, kMinBlocks, true><<<blocks, kThreads, 0, stream>>>(
+        h_agg_bwd_vec_kernel<NW, BATCH, MIN_BLOCKS, true><<<blocks, kThreads, 0, stream>>>(
             gv, rv, pre, grv, gpre, T, V);
     else
-        h_agg_bwd_vec_kernel<NW, kBatch, kMinBlocks, false><<<blocks, kThreads, 0, stream>>>(
+        h_agg_bwd_vec_kernel<NW, BATCH, MIN_BLOCKS, false><<<blocks, kThreads, 0, stream>>>(
             gv, rv, pre, grv, gpre, T, V);
+}
+
+void bwd_vec32(const void* g, const void* residual, const float* pre, void* gres, float* gpre,
+               uint64_t T, uint64_t H, cudaStream_t stream) {
+    const uint32_t V = uint32_t(H / 16);
+    const uint32_t per_thread = (V + 127) / 128;
+    if (per_thread <= 1)
+        launch_bwd_vec<8, 1, 6>(g, residual, pre, gres, gpre, T, V, stream);
+    else if (per_thread == 2)
+        launch_bwd_vec<8, 2, 3>(g, residual, pre, gres, gpre, T, V, stream);
+    else
+        launch_bwd_vec<8, 4, 2>(g, residual, pre, gres, gpre, T, V, stream);
+}
+
+void bwd_vec16(const void* g, const void* residual, const float* pre, void* gres, float* gpre,
+               uint64_t T, uint64_t H, cudaStream_t stream) {
+    launch_bwd_vec<4, 2, 3>(g, residual, pre, gres, gpre, T, uint32_t(H / 8), stream);
 }
 
 }  // namespace
@@ -665,9 +674,9 @@ mhc_status_t mhc_h_aggregate_bwd(const void* grad_out, const void* residual, con
         return MHC_ERR_UNSUPPORTED;
 
     if (path == MHC_PATH_VEC32) {
-        bwd_vec<8>(grad_out, residual, pre, grad_residual, grad_pre, uint64_t(T), uint64_t(H), stream);
+        bwd_vec32(grad_out, residual, pre, grad_residual, grad_pre, uint64_t(T), uint64_t(H), stream);
     } else if (path == MHC_PATH_VEC16) {
-        bwd_vec<4>(grad_out, residual, pre, grad_residual, grad_pre, uint64_t(T), uint64_t(H), stream);
+        bwd_vec16(grad_out, residual, pre, grad_residual, grad_pre, uint64_t(T), uint64_t(H), stream);
     } else {
         const uint32_t blocks = grid_for(uint64_t(T), 1, uint64_t(num_sms()) * 256);
         h_agg_bwd_element_kernel<<<blocks, kLanes, 0, stream>>>(

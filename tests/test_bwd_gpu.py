@@ -100,9 +100,10 @@ def test_repeat_100_calls_byte_identical():
 
 # --- shapes and paths
 
-@pytest.mark.parametrize("T,H", [(1, 1), (2, 7), (3, 8), (1, 13), (5, 255), (3, 1279),
-                                 (1, 2048), (2, 2050), (1, 4097), (2, 4104), (9, 7168),
-                                 (1, 16392), (2, 65536)])
+@pytest.mark.parametrize("T,H", [(1, 1), (2, 7), (3, 8), (1, 13), (4, 16), (5, 255), (3, 1279),
+                                 (1, 2048), (2, 2050), (2, 2064), (2, 3072), (3, 4096),
+                                 (1, 4097), (2, 4104), (2, 4112), (9, 7168), (1, 16392),
+                                 (2, 65536)])
 def test_shapes_bit_exact(T, H):
     g, res, pre = backward_inputs(T, H, "ragged", 15)
     gr, gp = run_bwd(g, res, pre)
