@@ -57,8 +57,8 @@ def bwd_bytes(T, H):
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=8000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--T", type=int, default=4096)
     ap.add_argument("--H", type=int, default=7168)
@@ -249,17 +249,41 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
         time.sleep(0.5)
+    # The timed region: K steps back to back, CUDA events only at its two ends
+    # (an event between two kernels would stop the second from becoming
+    # resident while the first drains).
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     sampler.mark_start()
     wall0 = time.perf_counter()
-    for i in range(K):
+    e_start.record(stream)
+    for _ in range(K):
+        if args.flush:
+            flush.zero_()
+        step()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    sampler.mark_end()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    region_ms = e_start.elapsed_time(e_end)
+    if args.flush:
+        region_ms = None  # the flushes are inside; use the per-kernel pass below
+
+    # Per-kernel pass (for the roofline): the same steps with an event pair
+    # around every kernel, on the launching stream.
+    K2 = min(K, 500)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K2)]
+    for i in range(K2):
         if args.flush:
             flush.zero_()
         e0, e1, e2 = ev[i]
@@ -271,15 +295,9 @@ def run_ours(args):
             binding.mhc_h_aggregate_bwd(g, res, pre, grad_res, grad_pre, stream)
         e2.record(stream)
     torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    sampler.mark_end()
-    if dist is not None:
-        dist.barrier()
-    clocks = sampler.stop() if rank == 0 else None
-
-    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    step_ms_local = (sum(fwd_ms) + sum(bwd_ms)) / K
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K2)]
+    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K2)]
+    step_ms_local = region_ms / K if region_ms is not None else (sum(fwd_ms) + sum(bwd_ms)) / K2
     step_ms = max_over_ranks(step_ms_local, dist, dev)
 
     bytes_step = (fwd_bytes(T, H) if do_fwd else 0) + (bwd_bytes(T, H) if do_bwd else 0)
@@ -329,7 +347,9 @@ def run_ours(args):
                           if args.flush else
                           "not flushed: the step reads 294 MB of inputs (> 126 MB L2) in token "
                           "order, so no kernel finds its inputs in L2"),
-                   "timing": "CUDA events on the launching stream around each kernel",
+                   "timing": ("CUDA events on the launching stream at the two ends of the K-step "
+                              "region; per-kernel times (per_kernel, roofline) from a second pass "
+                              "of min(K, 500) steps with events around every kernel"),
                    "bytes_per_step": bytes_step},
         "gpu_launches": K * (int(do_fwd) + int(do_bwd)),
         "roofline": roofline,
@@ -407,47 +427,59 @@ def e2e_measure(args, torch, binding, g, res, pre, dev, stream, world, dist):
 
 
 def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
-    """us/call per (T,H) by CUDA-graph replay of one call.  "cold": L2 flushed
-    by a 256 MiB write before each sample (the pages' cold-L2 method; the
-    flush leaves dirty lines that the timed call must write back).  "steady":
-    back-to-back replays without a flush, only where the call's inputs exceed
-    L2.  7 rounds x (10 warm-up + 100 samples); p20/p50/p80 of round medians."""
+    """us/call per (T,H).
+
+    "cold": CUDA-graph replay of one call with L2 flushed by a 256 MiB write
+    before each sample (the pages' cold-L2 method; the flush leaves dirty lines
+    that the timed call has to write back); 7 rounds x (10 warm-up + 100
+    samples), p20/p50/p80 of the round medians.
+    "steady": 400 calls back to back, rotating over enough buffer sets that no
+    call finds its inputs in L2 (at least 3x L2 in total), events only at the
+    two ends; shapes whose sets would not reach that in 8 sets are skipped.
+    """
     results = []
     stream = torch.cuda.Stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 
-    def time_graph(graph, cold):
+    def time_graph(graph):
         meds = []
         for _ in range(7):
             samples = []
             for i in range(110):
-                if cold:
-                    flush.zero_()
+                flush.zero_()
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record()
                 graph.replay()
                 e1.record()
-                if cold:
-                    e1.synchronize()
+                e1.synchronize()
                 samples.append((e0, e1))
-            torch.cuda.synchronize()
             ts = [a.elapsed_time(b) * 1e3 for a, b in samples[10:]]
             meds.append(statistics.median(ts))
         q = np.quantile(np.array(meds), [0.2, 0.5, 0.8])
         return [round(float(x), 3) for x in q]
 
-    def record(name, direction, T, H, graph, nbytes, in_bytes):
-        entry = {"workload": name, "dir": direction, "T": T, "H": H}
-        for mode in ("cold", "steady"):
-            if mode == "steady" and in_bytes <= l2:
-                continue
-            us = time_graph(graph, mode == "cold")
-            gbs = nbytes / (us[1] * 1e-6) / 1e9
-            entry[mode] = {"us_p20_p50_p80": us, "GBps_p50": round(gbs, 1),
-                           "frac_of_measured": round(gbs / peak, 4),
-                           "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)}
-        results.append(entry)
+    def time_steady(call, sets, n=400):
+        for i in range(2 * len(sets)):
+            call(*sets[i % len(sets)])
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n):
+            call(*sets[i % len(sets)])
+        e1.record()
+        torch.cuda.synchronize()
+        return round(e0.elapsed_time(e1) * 1e3 / n, 3)
+
+    def entry_for(us, nbytes):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"GBps": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
+                "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)}
+
+    def n_sets(set_bytes):
+        n = max(2, -(-3 * l2 // set_bytes))
+        return n if n <= 8 else None
 
     for name, seed, recipe, shapes in FWD_SWEEP:
         for T, H in shapes:
@@ -458,8 +490,21 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
                 binding.mhc_h_aggregate_fwd(r, p, o)
-            record(name, "fwd", T, H, graph, fwd_bytes(T, H), T * (8 * H + 16))
-            del r, p, o, graph
+            nbytes = fwd_bytes(T, H)
+            us = time_graph(graph)
+            entry = {"workload": name, "dir": "fwd", "T": T, "H": H,
+                     "cold": {"us_p20_p50_p80": us, **entry_for(us[1], nbytes)}}
+            del graph
+            ns = n_sets(nbytes)
+            if ns is not None:
+                sets = [(r, p, o)] + [(torch.empty_like(r).copy_(r), p.clone(), torch.empty_like(o))
+                                      for _ in range(ns - 1)]
+                us_s = time_steady(lambda a, b, c: binding.mhc_h_aggregate_fwd(a, b, c), sets)
+                entry["steady"] = {"us": us_s, "sets": ns, **entry_for(us_s, nbytes)}
+                del sets
+            results.append(entry)
+            del r, p, o
+            torch.cuda.empty_cache()
     for name, seed, recipe, shapes in BWD_SWEEP:
         for T, H in shapes:
             g, r, p = backward_inputs(T, H, recipe, seed, device=dev)
@@ -470,8 +515,21 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
                 binding.mhc_h_aggregate_bwd(g, r, p, gr, gp)
-            record(name, "bwd", T, H, graph, bwd_bytes(T, H), T * (10 * H + 16))
-            del g, r, p, gr, gp, graph
+            nbytes = bwd_bytes(T, H)
+            us = time_graph(graph)
+            entry = {"workload": name, "dir": "bwd", "T": T, "H": H,
+                     "cold": {"us_p20_p50_p80": us, **entry_for(us[1], nbytes)}}
+            del graph
+            ns = n_sets(nbytes)
+            if ns is not None:
+                sets = [(g, r, p, gr, gp)] + [(g.clone(), r.clone(), p.clone(), torch.empty_like(gr),
+                                               torch.empty_like(gp)) for _ in range(ns - 1)]
+                us_s = time_steady(lambda a, b, c, d, e: binding.mhc_h_aggregate_bwd(a, b, c, d, e), sets)
+                entry["steady"] = {"us": us_s, "sets": ns, **entry_for(us_s, nbytes)}
+                del sets
+            results.append(entry)
+            del g, r, p, gr, gp
+            torch.cuda.empty_cache()
     torch.cuda.synchronize()
     return results
 

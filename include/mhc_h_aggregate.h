@@ -47,7 +47,10 @@
  * keeps no state between calls except a per-thread copy of the last CUDA
  * error code, and never synchronises: each call enqueues kernels on `stream`
  * (NULL = the legacy default stream) and returns.  Calls are safe from several
- * host threads at once.
+ * host threads at once.  Kernels are launched with programmatic stream
+ * serialization: they may become resident while the previous kernel in the
+ * stream finishes, but touch no memory until it has completed, so stream order
+ * is kept for every producer and consumer of the buffers.
  *
  * Errors.  T == 0 returns MHC_OK without launching.  T < 0, H <= 0, a NULL
  * pointer, a misaligned pointer, a size whose byte count overflows int64, or
@@ -124,7 +127,7 @@ mhc_path_t mhc_h_aggregate_bwd_path(const void* grad_out, const void* residual,
 const char* mhc_status_string(mhc_status_t status);
 
 /* The cudaError_t value behind the last MHC_ERR_CUDA returned on the calling
- * thread (0 when there was none). */
+ * thread; a call that launches successfully resets it to 0. */
 int32_t mhc_h_aggregate_last_cuda_error(void);
 
 #ifdef __cplusplus

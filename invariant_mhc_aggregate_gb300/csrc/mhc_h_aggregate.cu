@@ -137,6 +137,18 @@ __device__ __forceinline__ float4 ld_pre(const float* p) {
     return PRE_VEC ? ld_pre16(p) : ld_pre4x(p);
 }
 
+// Programmatic dependent launch.  Every kernel here is launched so that it may
+// become resident while the previous kernel in its stream is still finishing
+// (its blocks then wait here, in hardware, until that kernel has completed and
+// its memory is visible), and lets the next kernel do the same.  Nothing is
+// read or written before the wait, so a producer of any input, or a reader of
+// any output, earlier in the stream is always respected.  Outside such a
+// launch both instructions do nothing.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 // --------------------------------------------------------------------------
 // BF16 <-> FP32 (widening is exact: the BF16 pattern is the upper half)
 // --------------------------------------------------------------------------
@@ -195,6 +207,7 @@ template <int NW, int BLOCK, int UNROLL, bool PRE_VEC>
 __global__ void __launch_bounds__(BLOCK)
 h_agg_fwd_vec_kernel(const Words<NW>* __restrict__ res, const float* __restrict__ pre,
                      Words<NW>* __restrict__ out, uint32_t n_vec, uint32_t V, FastDivU32 divV) {
+    pdl_enter();
     const uint32_t first = blockIdx.x * uint32_t(BLOCK * UNROLL) + threadIdx.x;
     Words<NW> r[UNROLL][4];
     float4 p[UNROLL];
@@ -220,6 +233,7 @@ h_agg_fwd_vec_kernel(const Words<NW>* __restrict__ res, const float* __restrict_
 __global__ void __launch_bounds__(256)
 h_agg_fwd_pair_kernel(const uint32_t* __restrict__ res2, const float* __restrict__ pre,
                       uint32_t* __restrict__ out2, uint64_t n_pairs, uint64_t P) {
+    pdl_enter();
     const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
     for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_pairs; i += stride) {
         const uint64_t t = i / P;
@@ -236,6 +250,7 @@ h_agg_fwd_pair_kernel(const uint32_t* __restrict__ res2, const float* __restrict
 __global__ void __launch_bounds__(256)
 h_agg_fwd_element_kernel(const uint16_t* __restrict__ res, const float* __restrict__ pre,
                          uint16_t* __restrict__ out, uint64_t n, uint64_t H) {
+    pdl_enter();
     const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
     for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
         const uint64_t t = i / H;
@@ -340,6 +355,7 @@ __global__ void __launch_bounds__(kLanes / (NW / 4), MIN_BLOCKS)
 h_agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict__ res,
                      const float* __restrict__ pre, Words<NW>* __restrict__ gres,
                      float* __restrict__ grad_pre, uint64_t T, uint32_t V) {
+    pdl_enter();
     constexpr int LPT = NW / 4;
     constexpr uint32_t B = kLanes / LPT;
     __shared__ float red[kGroups][4];
@@ -391,6 +407,7 @@ __global__ void __launch_bounds__(kLanes)
 h_agg_bwd_element_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ res,
                          const float* __restrict__ pre, uint16_t* __restrict__ gres,
                          float* __restrict__ grad_pre, uint64_t T, uint64_t H) {
+    pdl_enter();
     __shared__ float red[kGroups][4];
     const uint64_t C = (H + 7) / 8;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
@@ -469,13 +486,14 @@ int num_sms() {
     return n;
 }
 
+// Status of the launches since begin_launches(): a failed cudaLaunchKernelEx
+// is recorded by launch(), anything else by cudaGetLastError().
+void begin_launches() { g_last_cuda_error = 0; }
+
 mhc_status_t finish_launch() {
     const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) {
-        g_last_cuda_error = int32_t(e);
-        return MHC_ERR_CUDA;
-    }
-    return MHC_OK;
+    if (e != cudaSuccess) g_last_cuda_error = int32_t(e);
+    return g_last_cuda_error != 0 ? MHC_ERR_CUDA : MHC_OK;
 }
 
 mhc_path_t fwd_path(const void* residual, const float* pre, const void* out, int64_t T, int64_t H) {
@@ -511,6 +529,24 @@ mhc_path_t bwd_path(const void* g, const void* residual, const float* pre, const
     return MHC_PATH_ELEMENT;
 }
 
+// Launch with programmatic stream serialization (see pdl_enter).
+template <typename... Params, typename... Args>
+void launch(void (*kernel)(Params...), uint32_t grid, uint32_t block, cudaStream_t stream,
+            Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+    if (e != cudaSuccess) g_last_cuda_error = int32_t(e);
+}
+
 inline uint32_t grid_for(uint64_t items, uint32_t per_block, uint64_t cap) {
     uint64_t b = (items + per_block - 1) / per_block;
     if (b > cap) b = cap;
@@ -527,9 +563,9 @@ void launch_fwd_vec(const void* residual, const float* pre, void* out, uint32_t 
     const Words<NW>* r = static_cast<const Words<NW>*>(residual);
     Words<NW>* o = static_cast<Words<NW>*>(out);
     if (pre_vec)
-        h_agg_fwd_vec_kernel<NW, BLOCK, UNROLL, true><<<blocks, BLOCK, 0, stream>>>(r, pre, o, n_vec, V, divV);
+        launch(h_agg_fwd_vec_kernel<NW, BLOCK, UNROLL, true>, blocks, BLOCK, stream, r, pre, o, n_vec, V, divV);
     else
-        h_agg_fwd_vec_kernel<NW, BLOCK, UNROLL, false><<<blocks, BLOCK, 0, stream>>>(r, pre, o, n_vec, V, divV);
+        launch(h_agg_fwd_vec_kernel<NW, BLOCK, UNROLL, false>, blocks, BLOCK, stream, r, pre, o, n_vec, V, divV);
 }
 
 // Launch shapes of the vector forward (launch-time only; results do not
@@ -576,11 +612,11 @@ void launch_bwd_vec(const void* g, const void* residual, const float* pre, void*
     const Words<NW>* rv = static_cast<const Words<NW>*>(residual);
     Words<NW>* grv = static_cast<Words<NW>*>(gres);
     if (aligned(pre, 16))
-        h_agg_bwd_vec_kernel<NW, BATCH, MIN_BLOCKS, true><<<blocks, kThreads, 0, stream>>>(
-            gv, rv, pre, grv, gpre, T, V);
+        launch(h_agg_bwd_vec_kernel<NW, BATCH, MIN_BLOCKS, true>, blocks, kThreads, stream, gv, rv, pre, grv,
+               gpre, T, V);
     else
-        h_agg_bwd_vec_kernel<NW, BATCH, MIN_BLOCKS, false><<<blocks, kThreads, 0, stream>>>(
-            gv, rv, pre, grv, gpre, T, V);
+        launch(h_agg_bwd_vec_kernel<NW, BATCH, MIN_BLOCKS, false>, blocks, kThreads, stream, gv, rv, pre, grv,
+               gpre, T, V);
 }
 
 void bwd_vec32(const void* g, const void* residual, const float* pre, void* gres, float* gpre,
@@ -640,6 +676,7 @@ mhc_status_t mhc_h_aggregate_fwd(const void* residual, const float* pre, void* o
     const mhc_path_t path = fwd_path(residual, pre, out, T, H);
     if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    begin_launches();
     const bool pre_vec = aligned(pre, 16);
     const uint64_t cap = uint64_t(num_sms()) * 1024;
     if ((path == MHC_PATH_VEC32 || path == MHC_PATH_VEC16) && uint64_t(H) / 8 > 0x7FFFFFFFull)
@@ -652,12 +689,12 @@ mhc_status_t mhc_h_aggregate_fwd(const void* residual, const float* pre, void* o
     } else if (path == MHC_PATH_PAIR) {
         const uint64_t P = uint64_t(H) / 2;
         const uint64_t n = uint64_t(T) * P;
-        h_agg_fwd_pair_kernel<<<grid_for(n, 256, cap), 256, 0, stream>>>(
-            static_cast<const uint32_t*>(residual), pre, static_cast<uint32_t*>(out), n, P);
+        launch(h_agg_fwd_pair_kernel, grid_for(n, 256, cap), 256, stream,
+               static_cast<const uint32_t*>(residual), pre, static_cast<uint32_t*>(out), n, P);
     } else {
         const uint64_t n = uint64_t(T) * uint64_t(H);
-        h_agg_fwd_element_kernel<<<grid_for(n, 256, cap), 256, 0, stream>>>(
-            static_cast<const uint16_t*>(residual), pre, static_cast<uint16_t*>(out), n, uint64_t(H));
+        launch(h_agg_fwd_element_kernel, grid_for(n, 256, cap), 256, stream,
+               static_cast<const uint16_t*>(residual), pre, static_cast<uint16_t*>(out), n, uint64_t(H));
     }
     return finish_launch();
 }
@@ -672,6 +709,7 @@ mhc_status_t mhc_h_aggregate_bwd(const void* grad_out, const void* residual, con
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if ((path == MHC_PATH_VEC32 || path == MHC_PATH_VEC16) && uint64_t(H) / 8 > 0xFFFFFFFFull)
         return MHC_ERR_UNSUPPORTED;
+    begin_launches();
 
     if (path == MHC_PATH_VEC32) {
         bwd_vec32(grad_out, residual, pre, grad_residual, grad_pre, uint64_t(T), uint64_t(H), stream);
@@ -679,9 +717,9 @@ mhc_status_t mhc_h_aggregate_bwd(const void* grad_out, const void* residual, con
         bwd_vec16(grad_out, residual, pre, grad_residual, grad_pre, uint64_t(T), uint64_t(H), stream);
     } else {
         const uint32_t blocks = grid_for(uint64_t(T), 1, uint64_t(num_sms()) * 256);
-        h_agg_bwd_element_kernel<<<blocks, kLanes, 0, stream>>>(
-            static_cast<const uint16_t*>(grad_out), static_cast<const uint16_t*>(residual), pre,
-            static_cast<uint16_t*>(grad_residual), grad_pre, uint64_t(T), uint64_t(H));
+        launch(h_agg_bwd_element_kernel, blocks, kLanes, stream, static_cast<const uint16_t*>(grad_out),
+               static_cast<const uint16_t*>(residual), pre, static_cast<uint16_t*>(grad_residual), grad_pre,
+               uint64_t(T), uint64_t(H));
     }
     return finish_launch();
 }
