@@ -20,6 +20,12 @@ Parity status of each function (what pins it, from the oracle pin tests):
     emulation, identity and one-hot invariants.
   * grad_pre: integer-valued exact sums, FP64 error bound, hand-worked sparse
     cases that fix every level of the ORDER-256 tree.
+  * f16_from_float / float_from_f16: exhaustive round trip, hand ties and
+    edges, agreement with torch's CPU conversion.
+  * aggregate_fwd / aggregate_bwd (stream count n in {1,2,4,8}, BF16 or FP16
+    storage; a reading beyond the pages): hand-worked tree-order cases for n = 2
+    and 8, equality with fwd/bwd at n = 4 BF16, exact-rational emulation,
+    integer-valued exact sums, one-hot invariants.
 """
 
 from __future__ import annotations
@@ -95,6 +101,9 @@ def _shape_TH(residual: np.ndarray) -> tuple[int, int]:
     return int(residual.shape[0]), int(residual.shape[2])
 
 
+_DTYPES = {"bf16": 0, "f16": 1}
+
+
 class Oracle:
     """ctypes view of one compiled oracle library."""
 
@@ -117,6 +126,13 @@ class Oracle:
         lib.oracle_h_aggregate_bwd_grad_pre.restype = None
         lib.oracle_h_aggregate_bwd.argtypes = [p, p, p, p, p, i64, i64]
         lib.oracle_h_aggregate_bwd.restype = None
+        for name in ("oracle_f16_from_float_array", "oracle_float_from_f16_array"):
+            getattr(lib, name).argtypes = [p, p, i64]
+            getattr(lib, name).restype = None
+        lib.oracle_aggregate_fwd.argtypes = [p, p, p, i64, i64, i64, ctypes.c_int]
+        lib.oracle_aggregate_fwd.restype = ctypes.c_int
+        lib.oracle_aggregate_bwd.argtypes = [p, p, p, p, p, i64, i64, i64, ctypes.c_int]
+        lib.oracle_aggregate_bwd.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -133,6 +149,49 @@ class Oracle:
         y = np.empty(x.shape, dtype=np.float32)
         self.lib.oracle_float_from_bf16_array(_ptr(x), _ptr(y), x.size)
         return y
+
+    def f16_from_float(self, x) -> np.ndarray:
+        """Round float32 values to IEEE binary16 (RNE); returns uint16 patterns."""
+        x = _as(x, np.float32)
+        y = np.empty(x.shape, dtype=np.uint16)
+        self.lib.oracle_f16_from_float_array(_ptr(x), _ptr(y), x.size)
+        return y
+
+    def float_from_f16(self, x) -> np.ndarray:
+        """Widen IEEE binary16 patterns (uint16) to float32 exactly."""
+        x = _as(x, np.uint16)
+        y = np.empty(x.shape, dtype=np.float32)
+        self.lib.oracle_float_from_f16_array(_ptr(x), _ptr(y), x.size)
+        return y
+
+    def aggregate_fwd(self, residual, pre, dtype: str = "bf16") -> np.ndarray:
+        """General stream count n (residual [T,n,H], pre [T,n]) and storage dtype
+        ("bf16" or "f16"): out = cvt(balanced pairwise tree of pre_k * r_k)."""
+        residual = _as(residual, np.uint16)
+        pre = _as(pre, np.float32)
+        T, n, H = residual.shape
+        if pre.shape != (T, n):
+            raise ValueError(f"pre must be [{T},{n}], got {pre.shape}")
+        out = np.empty((T, H), dtype=np.uint16)
+        if self.lib.oracle_aggregate_fwd(_ptr(residual), _ptr(pre), _ptr(out), T, n, H,
+                                         _DTYPES[dtype]) != 0:
+            raise ValueError(f"unsupported n={n} or dtype={dtype}")
+        return out
+
+    def aggregate_bwd(self, g, residual, pre, dtype: str = "bf16") -> tuple[np.ndarray, np.ndarray]:
+        """(grad_residual uint16 [T,n,H], grad_pre float32 [T,n]) for stream count n."""
+        g = _as(g, np.uint16)
+        residual = _as(residual, np.uint16)
+        pre = _as(pre, np.float32)
+        T, n, H = residual.shape
+        if g.shape != (T, H) or pre.shape != (T, n):
+            raise ValueError("shape mismatch between g, residual and pre")
+        gr = np.empty((T, n, H), dtype=np.uint16)
+        gp = np.empty((T, n), dtype=np.float32)
+        if self.lib.oracle_aggregate_bwd(_ptr(g), _ptr(residual), _ptr(pre), _ptr(gr), _ptr(gp),
+                                         T, n, H, _DTYPES[dtype]) != 0:
+            raise ValueError(f"unsupported n={n} or dtype={dtype}")
+        return gr, gp
 
     def fwd(self, residual, pre) -> np.ndarray:
         """out[t,h] = bf16((pre0*r0 + pre1*r1) + (pre2*r2 + pre3*r3)); uint16 [T,H]."""
@@ -212,3 +271,19 @@ def grad_pre(g, residual):
 
 def bwd(g, residual, pre):
     return default().bwd(g, residual, pre)
+
+
+def f16_from_float(x):
+    return default().f16_from_float(x)
+
+
+def float_from_f16(x):
+    return default().float_from_f16(x)
+
+
+def aggregate_fwd(residual, pre, dtype="bf16"):
+    return default().aggregate_fwd(residual, pre, dtype)
+
+
+def aggregate_bwd(g, residual, pre, dtype="bf16"):
+    return default().aggregate_bwd(g, residual, pre, dtype)

@@ -199,8 +199,12 @@ static float groups_tree(float w[ORDER_GROUPS]) {
     return w[0];
 }
 
-/* grad_pre[t,k] for one token and one k: g_row is g[t,:], r_row is r[t,k,:]. */
-static float oracle_grad_pre_token(const uint16_t* g_row, const uint16_t* r_row, int64_t H) {
+static float widen(uint16_t v, int dtype);
+
+/* grad_pre[t,k] for one token and one k: g_row is g[t,:], r_row is r[t,k,:],
+ * stored as BF16 (dtype 0) or binary16 (dtype 1).  The product of two BF16 or
+ * two binary16 values is exact in binary32. */
+static float grad_pre_row(const uint16_t* g_row, const uint16_t* r_row, int64_t H, int dtype) {
     float lane[ORDER_LANES];
     for (int j = 0; j < ORDER_LANES; ++j) lane[j] = 0.0f;
 
@@ -209,8 +213,7 @@ static float oracle_grad_pre_token(const uint16_t* g_row, const uint16_t* r_row,
         float q[ORDER_CHUNK];
         for (int e = 0; e < ORDER_CHUNK; ++e) {
             int64_t h = c * ORDER_CHUNK + e;
-            q[e] = (h < H) ? oracle_float_from_bf16(g_row[h]) * oracle_float_from_bf16(r_row[h])
-                           : 0.0f;
+            q[e] = (h < H) ? widen(g_row[h], dtype) * widen(r_row[h], dtype) : 0.0f;
         }
         int j = (int)(c % ORDER_LANES);
         lane[j] = lane[j] + chunk_partial(q);
@@ -219,6 +222,10 @@ static float oracle_grad_pre_token(const uint16_t* g_row, const uint16_t* r_row,
     float w[ORDER_GROUPS];
     for (int grp = 0; grp < ORDER_GROUPS; ++grp) w[grp] = group_tree(lane + grp * ORDER_GROUP);
     return groups_tree(w);
+}
+
+static float oracle_grad_pre_token(const uint16_t* g_row, const uint16_t* r_row, int64_t H) {
+    return grad_pre_row(g_row, r_row, H, 0);
 }
 
 void oracle_h_aggregate_bwd_grad_pre(const uint16_t* g, const uint16_t* residual,
@@ -235,4 +242,143 @@ void oracle_h_aggregate_bwd(const uint16_t* g, const uint16_t* residual, const f
                             uint16_t* grad_residual, float* grad_pre, int64_t T, int64_t H) {
     oracle_h_aggregate_bwd_grad_residual(g, pre, grad_residual, T, H);
     oracle_h_aggregate_bwd_grad_pre(g, residual, grad_pre, T, H);
+}
+
+/* ----------------------------------------------------------------------- */
+/* General stream count n and FP16 storage                                   */
+/* ----------------------------------------------------------------------- */
+
+/* The pages fix n = 4 streams and BF16 storage.  The general form used here
+ * (a reading, not on the pages) keeps every rule of the Batch invariance
+ * section: for n in {1, 2, 4, 8}
+ *     out[t,h] = cvt( tree_n( pre[t,k] * r[t,k,h] ) )
+ * where tree_n is the balanced pairwise tree of binary32 sums (n = 2:
+ * p0 + p1; n = 4: (p0 + p1) + (p2 + p3); n = 8: ((p0+p1)+(p2+p3)) +
+ * ((p4+p5)+(p6+p7))), cvt is round-to-nearest-even into the storage format,
+ * and the backward is the derivative with the same roundings and ORDER-256.
+ * Storage is BF16 (dtype 0) or IEEE binary16 (dtype 1). */
+
+/* IEEE binary16 -> binary32, exact: normal, subnormal, zero, inf and NaN
+ * patterns are rebuilt field by field. */
+float oracle_float_from_f16(uint16_t h) {
+    uint32_t sign = (uint32_t)(h >> 15) << 31;
+    uint32_t exponent = (h >> 10) & 0x1Fu;
+    uint32_t fraction = h & 0x3FFu;
+    uint32_t u;
+    if (exponent == 0x1Fu) {
+        u = sign | 0x7F800000u | (fraction << 13);              /* inf or NaN */
+    } else if (exponent != 0u) {
+        u = sign | ((exponent + 112u) << 23) | (fraction << 13); /* normal: bias 15 -> 127 */
+    } else if (fraction == 0u) {
+        u = sign;                                                 /* signed zero */
+    } else {
+        /* subnormal: fraction * 2^-24, normalised into binary32 */
+        uint32_t e = 113u;  /* exponent field of 2^-14 */
+        while ((fraction & 0x400u) == 0u) {
+            fraction <<= 1;
+            e -= 1u;
+        }
+        u = sign | (e << 23) | ((fraction & 0x3FFu) << 13);
+    }
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* binary32 -> IEEE binary16, round to nearest, ties to even.  Written from
+ * the definition.  A normal binary32 x is m * 2^(e-23) with a 24-bit
+ * significand m.  Its binary16 quantum is 2^(e-10) in the normal range
+ * (e >= -14) and 2^-24 below it, so the low `shift` bits of m fall under the
+ * quantum: they decide the rounding (above half: up; exactly half: up only to
+ * an even count).  A carry can step into the next binade, and results of
+ * 65520 (= 2^16 - 2^4) or more become infinity.  Binary32 subnormals are far
+ * below 2^-25 and become signed zeros. */
+uint16_t oracle_f16_from_float(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    uint32_t exponent = (u >> 23) & 0xFFu;
+    uint32_t fraction = u & 0x7FFFFFu;
+    if (exponent == 0xFFu) {
+        if (fraction != 0u) return (uint16_t)(sign | 0x7E00u | (fraction >> 13)); /* quiet NaN */
+        return (uint16_t)(sign | 0x7C00u);                                        /* inf */
+    }
+    if (exponent == 0u) return sign;
+    int e = (int)exponent - 127;
+    if (e >= 16) return (uint16_t)(sign | 0x7C00u);
+    if (e <= -26) return sign;                   /* |x| < 2^-25: below half the smallest subnormal */
+    uint32_t m = fraction | 0x800000u;
+    int subnormal = e < -14;
+    int shift = subnormal ? (-1 - e) : 13;       /* 14..24 for subnormal results */
+    uint32_t kept = m >> shift;
+    uint32_t rem = m & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    if (rem > half || (rem == half && (kept & 1u) != 0u)) kept += 1u;
+    if (subnormal) return (uint16_t)(sign | kept);  /* a carry to 0x400 is the smallest normal */
+    int biased = e + 15;
+    if (kept == 0x800u) {                        /* rounded up into the next binade */
+        kept = 0x400u;
+        biased += 1;
+    }
+    if (biased >= 31) return (uint16_t)(sign | 0x7C00u);
+    return (uint16_t)(sign | ((uint32_t)biased << 10) | (kept & 0x3FFu));
+}
+
+void oracle_f16_from_float_array(const float* x, uint16_t* y, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_f16_from_float(x[i]);
+}
+
+void oracle_float_from_f16_array(const uint16_t* x, float* y, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_float_from_f16(x[i]);
+}
+
+static float widen(uint16_t v, int dtype) {
+    return dtype == 0 ? oracle_float_from_bf16(v) : oracle_float_from_f16(v);
+}
+
+static uint16_t narrow(float x, int dtype) {
+    return dtype == 0 ? oracle_bf16_from_float(x) : oracle_f16_from_float(x);
+}
+
+/* tree_n: level by level, element i of the next level is the sum of elements
+ * 2i and 2i+1 of this one, until one value is left. */
+static float pairwise_tree(float p[8], int n) {
+    for (int width = n; width > 1; width /= 2) {
+        for (int i = 0; i < width / 2; ++i) p[i] = p[2 * i] + p[2 * i + 1];
+    }
+    return p[0];
+}
+
+static int valid_streams(int64_t n) { return n == 1 || n == 2 || n == 4 || n == 8; }
+
+/* Returns 0, or -1 for an unsupported n or dtype (nothing written). */
+int oracle_aggregate_fwd(const uint16_t* residual, const float* pre, uint16_t* out,
+                         int64_t T, int64_t n, int64_t H, int dtype) {
+    if (!valid_streams(n) || (dtype != 0 && dtype != 1)) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            float p[8];
+            for (int64_t k = 0; k < n; ++k)
+                p[k] = pre[t * n + k] * widen(residual[(t * n + k) * H + h], dtype);
+            out[t * H + h] = narrow(pairwise_tree(p, (int)n), dtype);
+        }
+    }
+    return 0;
+}
+
+int oracle_aggregate_bwd(const uint16_t* g, const uint16_t* residual, const float* pre,
+                         uint16_t* grad_residual, float* grad_pre,
+                         int64_t T, int64_t n, int64_t H, int dtype) {
+    if (!valid_streams(n) || (dtype != 0 && dtype != 1)) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t k = 0; k < n; ++k) {
+            float p = pre[t * n + k];
+            for (int64_t h = 0; h < H; ++h) {
+                float prod = p * widen(g[t * H + h], dtype);
+                grad_residual[(t * n + k) * H + h] = narrow(prod, dtype);
+            }
+            grad_pre[t * n + k] = grad_pre_row(g + t * H, residual + (t * n + k) * H, H, dtype);
+        }
+    }
+    return 0;
 }

@@ -420,3 +420,215 @@ ALL_CHECKS = [
     check_gp_integer_exact,
     check_gp_fp64_bound,
 ]
+
+
+# --------------------------------------------------------------------------
+# FP16 storage and the general stream count (a reading beyond the pages)
+# --------------------------------------------------------------------------
+
+def f16_widen(u16: np.ndarray) -> np.ndarray:
+    """binary16 patterns -> float32 through numpy's own float16 (independent of the oracle)."""
+    return np.asarray(u16, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def to_f16_exact(x: float) -> float:
+    if math.isinf(x) or x == 0.0:
+        return x
+    return round_rne(Fraction(x), 11, emin=-14, emax=15)
+
+
+def f16_bits_of(x: float) -> int:
+    return int(np.array([x], dtype=np.float16).view(np.uint16)[0])
+
+
+STORAGE = {
+    "bf16": (bf16_widen, to_bf16_exact, bf16_bits_of),
+    "f16": (f16_widen, to_f16_exact, f16_bits_of),
+}
+
+
+def random_f16(rng, shape, scale=1.0) -> np.ndarray:
+    return (rng.standard_normal(shape) * scale).astype(np.float16).view(np.uint16)
+
+
+def random_storage(rng, shape, dtype, scale=1.0):
+    return random_bf16(rng, shape, scale) if dtype == "bf16" else random_f16(rng, shape, scale)
+
+
+def check_f16_golden(o):
+    for fbits, hbits, *_ in golden_rows("f16_rounding.txt"):
+        x = f32_from_bits(int(fbits, 16))
+        got = int(o.f16_from_float(np.array([x], dtype=np.float32))[0])
+        assert got == int(hbits, 16), f"f16({fbits}) = {got:04X}, expected {hbits}"
+
+
+def check_f16_roundtrip_exhaustive(o):
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    wide = o.float_from_f16(pats)
+    ref = pats.view(np.float16).astype(np.float32)
+    finite = np.isfinite(ref)
+    assert np.array_equal(f32_bits(wide)[finite], f32_bits(ref)[finite])
+    assert np.array_equal(np.isnan(wide), np.isnan(ref))
+    back = o.f16_from_float(wide)
+    nan = ((pats & 0x7C00) == 0x7C00) & ((pats & 0x03FF) != 0)
+    assert np.array_equal(back[~nan], pats[~nan])
+    assert np.all(((back[nan] & 0x7C00) == 0x7C00) & ((back[nan] & 0x03FF) != 0))
+
+
+def check_f16_vs_torch(o):
+    import torch
+    rng = np.random.default_rng(8)
+    bits = rng.integers(0, 2 ** 32, size=1 << 20, dtype=np.uint64).astype(np.uint32)
+    base = np.arange(0x33000000, 0x33000000 + (1 << 18), dtype=np.uint32)        # subnormal range
+    near_one = np.arange(0x3F7E0000, 0x3F7E0000 + (1 << 18), dtype=np.uint32)
+    near_max = np.arange(0x477F0000, 0x477F0000 + (1 << 17), dtype=np.uint32)
+    x = np.concatenate([bits, base, near_one, near_max, near_max | 0x80000000]).view(np.float32)
+    x = x[np.isfinite(x)]
+    ours = o.f16_from_float(x)
+    ref = torch.from_numpy(x.copy()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    bad = np.nonzero(ours != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches vs torch, e.g. {x[bad[:4]].view(np.uint32)}"
+
+
+def _hc_cases():
+    for row in golden_rows("fwd_hc_worked_examples.txt"):
+        name, dtype, n = row[0], row[1], int(row[2])
+        r = np.array([int(v, 16) for v in row[3:3 + n]], dtype=np.uint16)
+        pre = np.array([f32_from_bits(int(v, 16)) for v in row[3 + n:3 + 2 * n]], dtype=np.float32)
+        yield name, dtype, n, r, pre, int(row[3 + 2 * n], 16)
+
+
+def check_agg_golden(o):
+    rng = np.random.default_rng(51)
+    for name, dtype, n, r, pre, expected in _hc_cases():
+        got = int(o.aggregate_fwd(r.reshape(1, n, 1), pre.reshape(1, n), dtype)[0, 0])
+        assert got == expected, f"{name}: {got:04X} != {expected:04X}"
+        T, H = 3, 11
+        res = random_storage(rng, (T, n, H), dtype)
+        pr = rng.random((T, n), dtype=np.float32)
+        res[1, :, 4] = r
+        pr[1] = pre
+        got = int(o.aggregate_fwd(res, pr, dtype)[1, 4])
+        assert got == expected, f"{name} (embedded): {got:04X} != {expected:04X}"
+
+
+def check_agg_n4_bf16_is_the_pages_op(o):
+    rng = np.random.default_rng(52)
+    res = random_bf16(rng, (5, 4, 77))
+    pre = rng.random((5, 4), dtype=np.float32)
+    g = random_bf16(rng, (5, 77))
+    assert np.array_equal(o.aggregate_fwd(res, pre, "bf16"), o.fwd(res, pre))
+    gr1, gp1 = o.aggregate_bwd(g, res, pre, "bf16")
+    gr2, gp2 = o.bwd(g, res, pre)
+    assert np.array_equal(gr1, gr2) and np.array_equal(f32_bits(gp1), f32_bits(gp2))
+
+
+def _agg_exact(r_u16, pre, dtype):
+    widen, rnd, bits = STORAGE[dtype]
+    r = widen(r_u16)
+    T, n, H = r.shape
+    out = np.empty((T, H), dtype=np.uint16)
+    for t in range(T):
+        for h in range(H):
+            p = [exact_mul(float(pre[t, k]), float(r[t, k, h])) for k in range(n)]
+            while len(p) > 1:
+                p = [exact_add(p[2 * i], p[2 * i + 1]) for i in range(len(p) // 2)]
+            out[t, h] = bits(rnd(p[0]))
+    return out
+
+
+def check_agg_exact_rational(o):
+    rng = np.random.default_rng(53)
+    for dtype in ("bf16", "f16"):
+        for n in (1, 2, 4, 8):
+            res = random_storage(rng, (2, n, 13), dtype, scale=3.0)
+            pre = rng.random((2, n), dtype=np.float32) * np.float32(2.0)
+            assert np.array_equal(o.aggregate_fwd(res, pre, dtype), _agg_exact(res, pre, dtype)), (dtype, n)
+        # coarse values: ties in the final rounding are frequent
+        res = random_storage(rng, (3, 8, 16), dtype, scale=4.0)
+        res &= np.uint16(0xFFF0 if dtype == "bf16" else 0xFF80)
+        pre = (rng.integers(1, 1 << 12, size=(3, 8)) * 2.0 ** -9).astype(np.float32)
+        assert np.array_equal(o.aggregate_fwd(res, pre, dtype), _agg_exact(res, pre, dtype)), dtype
+
+
+def check_agg_one_hot(o):
+    rng = np.random.default_rng(54)
+    for dtype in ("bf16", "f16"):
+        for n in (1, 2, 8):
+            res = random_storage(rng, (4, n, 33), dtype)
+            res[res == 0x8000] = 0
+            for k in range(n):
+                pre = np.zeros((4, n), dtype=np.float32)
+                pre[:, k] = 1.0
+                assert np.array_equal(o.aggregate_fwd(res, pre, dtype), res[:, k, :]), (dtype, n, k)
+
+
+def check_agg_grad_residual_exact(o):
+    rng = np.random.default_rng(55)
+    for dtype in ("bf16", "f16"):
+        widen, rnd, bits = STORAGE[dtype]
+        for n in (1, 2, 8):
+            g = random_storage(rng, (2, 9), dtype)
+            res = random_storage(rng, (2, n, 9), dtype)
+            pre = rng.random((2, n), dtype=np.float32) * np.float32(3.0)
+            gr, _ = o.aggregate_bwd(g, res, pre, dtype)
+            gw = widen(g)
+            for t in range(2):
+                for k in range(n):
+                    for h in range(9):
+                        want = bits(rnd(exact_mul(float(pre[t, k]), float(gw[t, h]))))
+                        assert gr[t, k, h] == want, (dtype, n, t, k, h)
+
+
+def check_agg_grad_pre_integer_exact(o):
+    rng = np.random.default_rng(56)
+    for dtype in ("bf16", "f16"):
+        _, _, bits = STORAGE[dtype]
+        lut = np.array([bits(float(v)) for v in range(-8, 9)], dtype=np.uint16)
+        for n, H in ((1, 9), (2, 2049), (8, 4104), (8, 13)):
+            gi = rng.integers(-8, 9, size=(2, H))
+            ri = rng.integers(-8, 9, size=(2, n, H))
+            _, gp = o.aggregate_bwd(lut[gi + 8], lut[ri + 8], np.ones((2, n), dtype=np.float32), dtype)
+            assert np.array_equal(gp.astype(np.float64), np.einsum("th,tkh->tk", gi, ri).astype(np.float64)), (dtype, n, H)
+
+
+def check_agg_grad_pre_order_f16(o):
+    """The ORDER-256 golden cases with FP16 storage (1 = 0x3C00, 2^-24 = 0x0001,
+    -0 = 0x8000), in an n = 8 layout."""
+    remap = {0x3F80: 0x3C00, 0x3380: 0x0001, 0x8000: 0x8000}
+    for name, H, k, carrier, positions, expected in golden_rows("grad_pre_order_cases.txt"):
+        H, k = int(H), int(k)
+        vals = np.zeros(H, dtype=np.uint16)
+        for item in positions.split(","):
+            pos, v = item.split(":")
+            if pos == "*":
+                vals[:] = remap[int(v, 16)]
+            else:
+                vals[int(pos)] = remap[int(v, 16)]
+        n = 8
+        g = np.full((1, H), 0x3C00, dtype=np.uint16)
+        res = np.zeros((1, n, H), dtype=np.uint16)
+        kk = k + 4
+        if carrier == "r":
+            res[0, kk] = vals
+        else:
+            g[0] = vals
+            res[0, kk] = 0x3C00
+        _, gp = o.aggregate_bwd(g, res, np.ones((1, n), dtype=np.float32), "f16")
+        want = np.zeros(n, dtype=np.uint32)
+        want[kk] = int(expected, 16)
+        assert np.array_equal(f32_bits(gp)[0], want), name
+
+
+ALL_CHECKS += [
+    check_f16_golden,
+    check_f16_roundtrip_exhaustive,
+    check_f16_vs_torch,
+    check_agg_golden,
+    check_agg_n4_bf16_is_the_pages_op,
+    check_agg_exact_rational,
+    check_agg_one_hot,
+    check_agg_grad_residual_exact,
+    check_agg_grad_pre_integer_exact,
+    check_agg_grad_pre_order_f16,
+]

@@ -89,6 +89,21 @@ MUTANTS = {
         "lane[j] = (c < ORDER_LANES) ? chunk_partial(q) : lane[j] + chunk_partial(q);"),
     "gp_fma_products": ("lane[j] = lane[j] + chunk_partial(q);",
                         "lane[j] = __builtin_fmaf(1.0f + 0x1p-23f, chunk_partial(q), lane[j]);"),
+    # FP16 storage and the general stream count
+    "f16_truncate": ("    if (rem > half || (rem == half && (kept & 1u) != 0u)) kept += 1u;\n",
+                     "    (void)half;\n"),
+    "f16_ties_away": ("(rem == half && (kept & 1u) != 0u)", "(rem == half)"),
+    "f16_flush_subnormal_results": ("if (subnormal) return (uint16_t)(sign | kept);",
+                                    "if (subnormal) return sign;"),
+    "f16_saturate_instead_of_inf": ("    if (biased >= 31) return (uint16_t)(sign | 0x7C00u);",
+                                    "    if (biased >= 31) return (uint16_t)(sign | 0x7BFFu);"),
+    "f16_widen_subnormal_off_by_one": ("            e -= 1u;\n        }", "            e -= 2u;\n        }"),
+    "hc_tree_sequential": ("        for (int i = 0; i < width / 2; ++i) p[i] = p[2 * i] + p[2 * i + 1];\n    }\n    return p[0];",
+                           "    }\n    for (int i = 1; i < n; ++i) p[0] = p[0] + p[i];\n    return p[0];"),
+    "hc_tree_stride_pairs": ("p[i] = p[2 * i] + p[2 * i + 1];", "p[i] = p[i] + p[i + width / 2];"),
+    "hc_wrong_pre_stride": ("p[k] = pre[t * n + k] * widen(", "p[k] = pre[t * 4 + (k & 3)] * widen("),
+    "hc_grad_pre_wrong_row": ("grad_pre_row(g + t * H, residual + (t * n + k) * H, H, dtype)",
+                              "grad_pre_row(g + t * H, residual + (t * n + (k ^ 1)) * H, H, dtype)"),
 }
 
 
