@@ -19,6 +19,14 @@
  *   grad_residual[t,k,h] = bf16( fp32(pre[t,k] * g[t,h]) )
  *   grad_pre[t,k]        = sum over h of g[t,h] * r[t,k,h]      (FP32)
  *
+ * General form (this library's widening, not on the pages; the calls named
+ * mhc_aggregate_*): n streams, n in {1, 2, 4, 8}, residual [T,n,H], pre [T,n],
+ * out[t,h] = cvt(tree_n(pre[t,k] * r[t,k,h])), tree_n the balanced pairwise
+ * tree of FP32 sums (n = 2: p0+p1; n = 4: the (0+1)+(2+3) above; n = 8:
+ * ((p0+p1)+(p2+p3)) + ((p4+p5)+(p6+p7))), with storage BF16 or IEEE binary16
+ * (cvt rounds to nearest even, overflow to infinity, subnormals kept); the
+ * backward has the same form per stream k.
+ *
  * grad_pre is summed in ORDER-256, which depends on H only:
  *   1. q_h = g[t,h] * r[t,k,h] in FP32 (exact: both factors are BF16);
  *   2. chunk c = elements 8c .. 8c+7 (+0.0 past H), partial
@@ -122,6 +130,44 @@ mhc_path_t mhc_h_aggregate_fwd_path(const void* residual, const float* pre, cons
 mhc_path_t mhc_h_aggregate_bwd_path(const void* grad_out, const void* residual,
                                     const float* pre, const void* grad_residual,
                                     const float* grad_pre, int64_t T, int64_t H);
+
+/* Storage type of residual, out, g and grad_residual (pre and grad_pre are
+ * always FP32). */
+typedef enum mhc_dtype {
+    MHC_DTYPE_BF16 = 0,
+    MHC_DTYPE_F16 = 1   /* IEEE binary16 */
+} mhc_dtype_t;
+
+/* General forward: n streams (n in {1, 2, 4, 8}; others return
+ * MHC_ERR_UNSUPPORTED), BF16 or FP16 storage.  The pages' op is n = 4 with
+ * BF16, which is exactly mhc_h_aggregate_fwd.  The paper has only n = 4 / BF16;
+ * the tree for other n and the FP16 rounding are this library's reading.
+ *   residual  in   [T,n,H] dtype
+ *   pre       in   FP32 [T,n]
+ *   out       out  [T,H] dtype
+ */
+mhc_status_t mhc_aggregate_fwd(const void* residual, const float* pre, void* out, int64_t T,
+                               int32_t n, int64_t H, mhc_dtype_t dtype, mhc_stream_t stream);
+
+/* General backward, same n and dtype rules; n = 4 with BF16 is exactly
+ * mhc_h_aggregate_bwd.
+ *   grad_out       in   [T,H] dtype
+ *   residual       in   [T,n,H] dtype
+ *   pre            in   FP32 [T,n]
+ *   grad_residual  out  [T,n,H] dtype: cvt(fp32(pre[t,k] * g[t,h]))
+ *   grad_pre       out  FP32 [T,n]: ORDER-256 sums of g * r[t,k]
+ */
+mhc_status_t mhc_aggregate_bwd(const void* grad_out, const void* residual, const float* pre,
+                               void* grad_residual, float* grad_pre, int64_t T, int32_t n,
+                               int64_t H, mhc_dtype_t dtype, mhc_stream_t stream);
+
+/* Kernel path of the general calls (no launch, no CUDA call); the storage type
+ * does not change the path. */
+mhc_path_t mhc_aggregate_fwd_path(const void* residual, const float* pre, const void* out,
+                                  int64_t T, int32_t n, int64_t H);
+mhc_path_t mhc_aggregate_bwd_path(const void* grad_out, const void* residual, const float* pre,
+                                  const void* grad_residual, const float* grad_pre, int64_t T,
+                                  int32_t n, int64_t H);
 
 /* Static text for a status code. */
 const char* mhc_status_string(mhc_status_t status);

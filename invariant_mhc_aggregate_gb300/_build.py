@@ -1,7 +1,8 @@
 """Compile the sm_103a library ``libmhc_h_aggregate.so`` in-tree with nvcc.
 
-The library is one translation unit (``csrc/mhc_h_aggregate.cu``) exporting
-the C ABI of ``include/mhc_h_aggregate.h``.  It is rebuilt when its sources or
+The library exports the C ABI of ``include/mhc_h_aggregate.h`` from
+``csrc/mhc_h_aggregate.cu``; the kernels (``csrc/mhc_device.cuh``) are
+instantiated per storage type in ``csrc/mhc_launch_*.cu``, compiled in parallel.  It is rebuilt when its sources or
 flags change (a stamp file beside it records their hash).
 """
 
@@ -20,8 +21,10 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_NAME = "libmhc_h_aggregate.so"
 LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
-SOURCES = [os.path.join(CSRC, "mhc_h_aggregate.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "fastdiv.cuh"), os.path.join(INCLUDE, "mhc_h_aggregate.h")]
+SOURCES = [os.path.join(CSRC, f) for f in
+           ("mhc_h_aggregate.cu", "mhc_launch_bf16.cu", "mhc_launch_f16.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fastdiv.cuh", "mhc_device.cuh", "mhc_launch.cuh")] \
+    + [os.path.join(INCLUDE, "mhc_h_aggregate.h")]
 
 ARCH = "sm_103a"
 
@@ -34,7 +37,6 @@ NVCC_FLAGS = [
     "-O3", "-lineinfo", "-std=c++17",
     "--fmad=false", "-ftz=false", "-prec-div=true", "-prec-sqrt=true",
     "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-    "-shared",
 ]
 
 
@@ -68,19 +70,29 @@ def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
             if f.read().strip() == digest:
                 return LIB_PATH
     os.makedirs(LIB_DIR, exist_ok=True)
-    fd, tmp = tempfile.mkstemp(suffix=".so", dir=LIB_DIR)
-    os.close(fd)
-    cmd = [nvcc_path(), *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-I", CSRC, "-o", tmp, *SOURCES]
-    try:
+    nvcc = nvcc_path()
+    with tempfile.TemporaryDirectory(dir=LIB_DIR) as work:
+        # one translation unit per process, in parallel
+        procs = []
+        objs = []
+        for src in SOURCES:
+            obj = os.path.join(work, os.path.basename(src) + ".o")
+            cmd = [nvcc, *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-I", CSRC, "-c", "-o", obj, src]
+            procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                                                text=True)))
+            objs.append(obj)
+        for cmd, proc in procs:
+            out, err = proc.communicate()
+            if proc.returncode != 0:
+                raise RuntimeError(f"nvcc failed ({' '.join(cmd)}):\n{err}")
+            if verbose and err:
+                print(err)
+        tmp = os.path.join(work, LIB_NAME)
+        cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-o", tmp, *objs]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
-            raise RuntimeError(f"nvcc failed ({' '.join(cmd)}):\n{res.stderr}")
-        if verbose and res.stderr:
-            print(res.stderr)
+            raise RuntimeError(f"link failed ({' '.join(cmd)}):\n{res.stderr}")
         os.replace(tmp, LIB_PATH)
-    finally:
-        if os.path.exists(tmp):
-            os.unlink(tmp)
     with open(stamp, "w") as f:
         f.write(digest + "\n")
     return LIB_PATH

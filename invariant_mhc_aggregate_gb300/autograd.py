@@ -11,8 +11,10 @@ allocates the outputs and tracks the graph.
     residual.grad  # bf16 [T,4,H] = bf16(fp32(pre * g))
     pre.grad       # fp32 [T,4]   = ORDER-256 sums of g * residual
 
-Inputs may have any leading batch shape: ``residual [..., 4, H]`` and
-``pre [..., 4]`` are flattened to tokens and the results reshaped back.
+Inputs may have any leading batch shape: ``residual [..., n, H]`` and
+``pre [..., n]`` are flattened to tokens and the results reshaped back.  The
+pages' op has n = 4 streams and BF16 storage; n in {1, 2, 8} and FP16 storage
+run the library's general form (balanced pairwise tree, same roundings).
 """
 
 from __future__ import annotations
@@ -25,15 +27,15 @@ from . import binding
 class HAggregate(torch.autograd.Function):
     @staticmethod
     def forward(ctx, residual: torch.Tensor, pre: torch.Tensor) -> torch.Tensor:
-        if residual.dtype != torch.bfloat16 or pre.dtype != torch.float32:
-            raise TypeError("h_aggregate expects residual bf16 [...,4,H] and pre fp32 [...,4]")
-        if residual.shape[:-1] != pre.shape or residual.shape[-2] != 4:
+        if residual.dtype not in (torch.bfloat16, torch.float16) or pre.dtype != torch.float32:
+            raise TypeError("h_aggregate expects residual bf16/f16 [...,n,H] and pre fp32 [...,n]")
+        if residual.dim() < 2 or residual.shape[:-1] != pre.shape:
             raise ValueError(f"shape mismatch: residual {tuple(residual.shape)}, pre {tuple(pre.shape)}")
         lead = residual.shape[:-2]
-        H = residual.shape[-1]
-        r = residual.reshape(-1, 4, H).contiguous()
-        p = pre.reshape(-1, 4).contiguous()
-        out = binding.h_aggregate(r, p)
+        n, H = residual.shape[-2], residual.shape[-1]
+        r = residual.reshape(-1, n, H).contiguous()
+        p = pre.reshape(-1, n).contiguous()
+        out = binding.aggregate(r, p)
         ctx.save_for_backward(r, p)
         ctx.lead = lead
         return out.reshape(*lead, H)
@@ -41,13 +43,13 @@ class HAggregate(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad_out: torch.Tensor):
         r, p = ctx.saved_tensors
-        H = r.shape[-1]
-        if grad_out.dtype != torch.bfloat16:
-            raise TypeError(f"the gradient of the bf16 output must be bf16, got {grad_out.dtype}")
+        n, H = r.shape[-2], r.shape[-1]
+        if grad_out.dtype != r.dtype:
+            raise TypeError(f"the output gradient must be {r.dtype}, got {grad_out.dtype}")
         g = grad_out.reshape(-1, H).contiguous()
-        grad_residual, grad_pre = binding.h_aggregate_backward(g, r, p)
-        gr = grad_residual.reshape(*ctx.lead, 4, H) if ctx.needs_input_grad[0] else None
-        gp = grad_pre.reshape(*ctx.lead, 4) if ctx.needs_input_grad[1] else None
+        grad_residual, grad_pre = binding.aggregate_backward(g, r, p)
+        gr = grad_residual.reshape(*ctx.lead, n, H) if ctx.needs_input_grad[0] else None
+        gp = grad_pre.reshape(*ctx.lead, n) if ctx.needs_input_grad[1] else None
         return gr, gp
 
 

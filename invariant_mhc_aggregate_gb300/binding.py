@@ -33,6 +33,9 @@ MHC_PATH_VEC32 = 3
 PATH_NAMES = {MHC_PATH_NONE: "none", MHC_PATH_VEC16: "vec16", MHC_PATH_PAIR: "pair",
               MHC_PATH_ELEMENT: "element", MHC_PATH_VEC32: "vec32"}
 
+MHC_DTYPE_BF16 = 0
+MHC_DTYPE_F16 = 1
+
 #: Every symbol the header declares, in declaration order.
 EXPORTS = (
     "mhc_h_aggregate_abi_version",
@@ -40,6 +43,10 @@ EXPORTS = (
     "mhc_h_aggregate_bwd",
     "mhc_h_aggregate_fwd_path",
     "mhc_h_aggregate_bwd_path",
+    "mhc_aggregate_fwd",
+    "mhc_aggregate_bwd",
+    "mhc_aggregate_fwd_path",
+    "mhc_aggregate_bwd_path",
     "mhc_status_string",
     "mhc_h_aggregate_last_cuda_error",
 )
@@ -87,6 +94,14 @@ def load(path: str | None = None):
         lib.mhc_h_aggregate_fwd_path.restype = i32
         lib.mhc_h_aggregate_bwd_path.argtypes = [p, p, p, p, p, i64, i64]
         lib.mhc_h_aggregate_bwd_path.restype = i32
+        lib.mhc_aggregate_fwd.argtypes = [p, p, p, i64, i32, i64, i32, p]
+        lib.mhc_aggregate_fwd.restype = i32
+        lib.mhc_aggregate_bwd.argtypes = [p, p, p, p, p, i64, i32, i64, i32, p]
+        lib.mhc_aggregate_bwd.restype = i32
+        lib.mhc_aggregate_fwd_path.argtypes = [p, p, p, i64, i32, i64]
+        lib.mhc_aggregate_fwd_path.restype = i32
+        lib.mhc_aggregate_bwd_path.argtypes = [p, p, p, p, p, i64, i32, i64]
+        lib.mhc_aggregate_bwd_path.restype = i32
         lib.mhc_status_string.argtypes = [i32]
         lib.mhc_status_string.restype = ctypes.c_char_p
         lib.mhc_h_aggregate_last_cuda_error.argtypes = []
@@ -119,9 +134,31 @@ def bwd_path_raw(grad_out: int, residual: int, pre: int, grad_residual: int, gra
     return load().mhc_h_aggregate_bwd_path(grad_out, residual, pre, grad_residual, grad_pre, T, H)
 
 
+def agg_fwd_raw(residual: int, pre: int, out: int, T: int, n: int, H: int, dtype: int,
+                stream: int = 0) -> int:
+    return load().mhc_aggregate_fwd(residual, pre, out, T, n, H, dtype, stream)
+
+
+def agg_bwd_raw(grad_out: int, residual: int, pre: int, grad_residual: int, grad_pre: int,
+                T: int, n: int, H: int, dtype: int, stream: int = 0) -> int:
+    return load().mhc_aggregate_bwd(grad_out, residual, pre, grad_residual, grad_pre, T, n, H,
+                                    dtype, stream)
+
+
+def agg_fwd_path_raw(residual: int, pre: int, out: int, T: int, n: int, H: int) -> int:
+    return load().mhc_aggregate_fwd_path(residual, pre, out, T, n, H)
+
+
+def agg_bwd_path_raw(grad_out: int, residual: int, pre: int, grad_residual: int, grad_pre: int,
+                     T: int, n: int, H: int) -> int:
+    return load().mhc_aggregate_bwd_path(grad_out, residual, pre, grad_residual, grad_pre, T, n, H)
+
+
 # ---------------------------------------------------------------------------
 # tensor entry points
 # ---------------------------------------------------------------------------
+
+_TORCH_DTYPES = {torch.bfloat16: MHC_DTYPE_BF16, torch.float16: MHC_DTYPE_F16}
 
 def _check(t: torch.Tensor, name: str, dtype, shape):
     if not isinstance(t, torch.Tensor):
@@ -189,6 +226,67 @@ def mhc_h_aggregate_bwd_path(grad_out, residual, pre, grad_residual, grad_pre) -
     T, H = _TH(residual)
     return bwd_path_raw(grad_out.data_ptr(), residual.data_ptr(), pre.data_ptr(),
                         grad_residual.data_ptr(), grad_pre.data_ptr(), T, H)
+
+
+def _TnH(residual: torch.Tensor) -> tuple[int, int, int]:
+    if residual.dim() != 3:
+        raise ValueError(f"residual must be [T,n,H], got {tuple(residual.shape)}")
+    return int(residual.shape[0]), int(residual.shape[1]), int(residual.shape[2])
+
+
+def _storage(t: torch.Tensor, name: str) -> int:
+    if t.dtype not in _TORCH_DTYPES:
+        raise TypeError(f"{name} must be bfloat16 or float16, got {t.dtype}")
+    return _TORCH_DTYPES[t.dtype]
+
+
+def mhc_aggregate_fwd(residual: torch.Tensor, pre: torch.Tensor, out: torch.Tensor,
+                      stream=None) -> None:
+    """General forward: residual [T,n,H] (bf16 or f16), pre [T,n] fp32 -> out [T,H]."""
+    T, n, H = _TnH(residual)
+    dt = _storage(residual, "residual")
+    _check(residual, "residual", residual.dtype, (T, n, H))
+    _check(pre, "pre", torch.float32, (T, n))
+    _check(out, "out", residual.dtype, (T, H))
+    st = agg_fwd_raw(residual.data_ptr(), pre.data_ptr(), out.data_ptr(), T, n, H, dt,
+                     _stream_handle(stream, residual.device))
+    if st != MHC_OK:
+        raise MhcError(st, "mhc_aggregate_fwd")
+
+
+def mhc_aggregate_bwd(grad_out: torch.Tensor, residual: torch.Tensor, pre: torch.Tensor,
+                      grad_residual: torch.Tensor, grad_pre: torch.Tensor, stream=None) -> None:
+    """General backward for n streams and bf16 / f16 storage, written in place."""
+    T, n, H = _TnH(residual)
+    dt = _storage(residual, "residual")
+    _check(grad_out, "grad_out", residual.dtype, (T, H))
+    _check(residual, "residual", residual.dtype, (T, n, H))
+    _check(pre, "pre", torch.float32, (T, n))
+    _check(grad_residual, "grad_residual", residual.dtype, (T, n, H))
+    _check(grad_pre, "grad_pre", torch.float32, (T, n))
+    st = agg_bwd_raw(grad_out.data_ptr(), residual.data_ptr(), pre.data_ptr(),
+                     grad_residual.data_ptr(), grad_pre.data_ptr(), T, n, H, dt,
+                     _stream_handle(stream, residual.device))
+    if st != MHC_OK:
+        raise MhcError(st, "mhc_aggregate_bwd")
+
+
+def aggregate(residual: torch.Tensor, pre: torch.Tensor, stream=None) -> torch.Tensor:
+    """Allocate ``out`` [T,H] and run the general forward."""
+    T, n, H = _TnH(residual)
+    out = torch.empty((T, H), dtype=residual.dtype, device=residual.device)
+    mhc_aggregate_fwd(residual, pre, out, stream)
+    return out
+
+
+def aggregate_backward(grad_out: torch.Tensor, residual: torch.Tensor, pre: torch.Tensor,
+                       stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Allocate and return (grad_residual [T,n,H], grad_pre [T,n] fp32)."""
+    T, n, H = _TnH(residual)
+    grad_residual = torch.empty((T, n, H), dtype=residual.dtype, device=residual.device)
+    grad_pre = torch.empty((T, n), dtype=torch.float32, device=residual.device)
+    mhc_aggregate_bwd(grad_out, residual, pre, grad_residual, grad_pre, stream)
+    return grad_residual, grad_pre
 
 
 def h_aggregate(residual: torch.Tensor, pre: torch.Tensor, stream=None) -> torch.Tensor:

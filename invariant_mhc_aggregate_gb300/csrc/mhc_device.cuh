@@ -1,0 +1,500 @@
+// Device code of the mHC "H Aggregate" library for GB300 (sm_103a): the
+// forward and fused backward kernels, templated on the stream count N, the
+// storage type DT and the access width.
+//
+// Source: "Add batch-invariant h_aggregate kernel" (RL-Kernel pull request
+// 366).  Summary: residual [T,4,H] BF16, pre [T,4] FP32, out [T,H] BF16,
+//   out = bf16((pre0*r0 + pre1*r1) + (pre2*r2 + pre3*r3)).
+// Batch invariance: one writer per output, no atomics, FP32 __fmul_rn /
+// __fadd_rn, the fixed (0 + 1) + (2 + 3) tree, BF16 only at the boundaries.
+// The backward answers that page's reviewer request; its formula is the exact
+// derivative of the Summary formula and its grad_pre order (ORDER-256) is
+// defined in mhc_h_aggregate.h.  N = 4 with BF16 storage is the pages' op;
+// N in {1, 2, 8} (balanced pairwise tree) and FP16 storage are this library's
+// widening of it, keeping every rule above.
+//
+// Design (GB300, HBM-bound: about 0.7 FP32 operations per byte moved):
+//  * Vector paths move NW 32-bit words per access: NW = 8 uses the 256-bit
+//    (32-byte) global loads and stores that sm_100-class GPUs added
+//    (ld/st .v8.b32), NW = 4 the 16-byte ones.  One access covers 2*NW
+//    stored values, i.e. NW/4 "chunks" of 8 values.
+//  * Forward: a flat grid over output vectors.  A thread loads the N residual
+//    vectors feeding its output vector with streaming loads and the token's
+//    pre, and stores one vector.  Large calls give each thread UNROLL
+//    vectors, all loads issued before any arithmetic, to keep enough bytes
+//    in flight per SM; decode-sized calls give each thread one vector so the
+//    work spreads over as many SMs as possible.  The arithmetic of an element
+//    never depends on the grid, the block or T.
+//  * Backward: one block per token (grid-stride over tokens) whose threads
+//    own the 256 lanes of ORDER-256, NW/4 lanes each: thread j holds the
+//    chunks of lanes (NW/4)*j .. (NW/4)*j + NW/4 - 1, which are adjacent, so
+//    one vector access serves all of them.  It streams g and the N residual
+//    rows, writes grad_residual, and adds the chunk partials of each lane in
+//    increasing chunk order.  Groups of 32 lanes fold with warp shuffles (and
+//    one in-thread add when a thread holds two lanes), the 8 groups through
+//    shared memory.  No atomics, no cross-block traffic.
+//  * Narrower paths (H not a multiple of 8, or buffers not 16-byte aligned)
+//    run the same per-element arithmetic and the same grad_pre tree with 4- or
+//    2-byte accesses, so every path gives the same bytes.
+//  * Every kernel is launched with programmatic stream serialization and
+//    waits for its predecessor before touching memory (pdl_enter).
+//  * No tensor cores: nothing here is a contraction.
+//  * Built without fast math, with --fmad=false and -ftz=false; the
+//    intrinsics below already forbid contraction and flushing.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "fastdiv.cuh"
+
+namespace mhc {
+
+constexpr int kBF16 = 0;
+constexpr int kF16 = 1;
+
+// --------------------------------------------------------------------------
+// memory access helpers
+// --------------------------------------------------------------------------
+
+template <int NW>
+struct Words {
+    uint32_t w[NW];
+};
+
+// Vector load of data read exactly once: read-only path, no L1 allocation.
+template <int NW>
+__device__ __forceinline__ Words<NW> ld_stream(const void* p);
+
+template <>
+__device__ __forceinline__ Words<4> ld_stream<4>(const void* p) {
+    Words<4> v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+    return v;
+}
+
+template <>
+__device__ __forceinline__ Words<8> ld_stream<8>(const void* p) {
+    Words<8> v;
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]),
+                   "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
+                 : "l"(p));
+    return v;
+}
+
+// Vector store of data written exactly once: streaming (evict-first).
+template <int NW>
+__device__ __forceinline__ void st_stream(void* p, const Words<NW>& v);
+
+template <>
+__device__ __forceinline__ void st_stream<4>(void* p, const Words<4>& v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :
+                 : "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
+                 : "memory");
+}
+
+template <>
+__device__ __forceinline__ void st_stream<8>(void* p, const Words<8>& v) {
+    asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :
+                 : "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]),
+                   "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_stream4(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream4(void* p, uint32_t v) {
+    asm volatile("st.global.cs.u32 [%0], %1;" : : "l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint16_t ld_stream2(const void* p) {
+    uint16_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream2(void* p, uint16_t v) {
+    asm volatile("st.global.cs.u16 [%0], %1;" : : "l"(p), "h"(v) : "memory");
+}
+
+// The N pre values of a token (read by all of the token's threads: keep them
+// in L1).  pre_vec: the token's pre is aligned to min(16, 4N) bytes, so it is
+// read with float2 / float4 loads.
+template <int N>
+__device__ __forceinline__ void ld_pre(const float* p, bool pre_vec, float (&out)[N]) {
+    if (N == 1) {
+        out[0] = __ldg(p);
+    } else if (pre_vec && N == 2) {
+        const float2 v = __ldg(reinterpret_cast<const float2*>(p));
+        out[0] = v.x;
+        out[N - 1] = v.y;
+    } else if (pre_vec) {
+#pragma unroll
+        for (int i = 0; i < N / 4; ++i) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(p) + i);
+            out[4 * i + 0] = v.x;
+            out[4 * i + 1] = v.y;
+            out[4 * i + 2] = v.z;
+            out[4 * i + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < N; ++k) out[k] = __ldg(p + k);
+    }
+}
+
+// Programmatic dependent launch.  Every kernel here is launched so that it may
+// become resident while the previous kernel in its stream is still finishing
+// (its blocks then wait here, in hardware, until that kernel has completed and
+// its memory is visible), and lets the next kernel do the same.  Nothing is
+// read or written before the wait, so a producer of any input, or a reader of
+// any output, earlier in the stream is always respected.  Outside such a
+// launch both instructions do nothing.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
+// --------------------------------------------------------------------------
+// storage <-> FP32: BF16 widening is exact (the pattern is the upper half of
+// the binary32 one), binary16 widening is exact too (cvt.f32.f16); narrowing
+// rounds to nearest even in both.
+// --------------------------------------------------------------------------
+
+template <int DT>
+struct Elem;
+
+template <>
+struct Elem<kBF16> {
+    static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+    static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+    static __device__ __forceinline__ float one(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    static __device__ __forceinline__ uint16_t cvt(float x) {
+        __nv_bfloat16 v = __float2bfloat16_rn(x);
+        return *reinterpret_cast<uint16_t*>(&v);
+    }
+};
+
+template <>
+struct Elem<kF16> {
+    static __device__ __forceinline__ float lo(uint32_t w) {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+    }
+    static __device__ __forceinline__ float hi(uint32_t w) {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+    }
+    static __device__ __forceinline__ float one(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    static __device__ __forceinline__ uint16_t cvt(float x) { return __half_as_ushort(__float2half_rn(x)); }
+};
+
+// --------------------------------------------------------------------------
+// the forward element: N RN products and the balanced pairwise tree of RN
+// sums (N = 4: (p0 + p1) + (p2 + p3))
+// --------------------------------------------------------------------------
+
+template <int N>
+__device__ __forceinline__ float tree_sum(float (&p)[N]) {
+#pragma unroll
+    for (int width = N; width > 1; width /= 2) {
+#pragma unroll
+        for (int i = 0; i < width / 2; ++i) p[i] = __fadd_rn(p[2 * i], p[2 * i + 1]);
+    }
+    return p[0];
+}
+
+// Two adjacent elements held as a pair in word `e` of each of the N inputs.
+template <int N, int DT>
+__device__ __forceinline__ uint32_t agg_pair(const float (&pre)[N], const uint32_t (&w)[N]) {
+    float lo[N], hi[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+        lo[k] = __fmul_rn(pre[k], Elem<DT>::lo(w[k]));
+        hi[k] = __fmul_rn(pre[k], Elem<DT>::hi(w[k]));
+    }
+    return Elem<DT>::pack(tree_sum<N>(lo), tree_sum<N>(hi));
+}
+
+// --------------------------------------------------------------------------
+// forward kernels
+// --------------------------------------------------------------------------
+
+// Vector path.  Output vector i (i = t*V + v, V = H / (2*NW) vectors per row)
+// is out[i]; the residual vector of row k is res[t*N*V + k*V + v] =
+// res[i + (N-1)tV + kV].
+template <int N, int DT, int NW, int BLOCK, int UNROLL>
+__global__ void __launch_bounds__(BLOCK)
+agg_fwd_vec_kernel(const Words<NW>* __restrict__ res, const float* __restrict__ pre,
+                   Words<NW>* __restrict__ out, uint32_t n_vec, uint32_t V, FastDivU32 divV,
+                   bool pre_vec) {
+    pdl_enter();
+    const uint32_t first = blockIdx.x * uint32_t(BLOCK * UNROLL) + threadIdx.x;
+    Words<NW> r[UNROLL][N];
+    float p[UNROLL][N];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+        const uint32_t i = first + uint32_t(u * BLOCK);
+        if (i < n_vec) {
+            const uint32_t t = fastdiv_u32(i, divV);
+            const Words<NW>* src = res + (uint64_t(i) + uint64_t(N - 1) * uint64_t(t) * V);
+#pragma unroll
+            for (int k = 0; k < N; ++k) r[u][k] = ld_stream<NW>(src + uint64_t(k) * V);
+            ld_pre<N>(pre + uint64_t(N) * t, pre_vec, p[u]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+        const uint32_t i = first + uint32_t(u * BLOCK);
+        if (i < n_vec) {
+            Words<NW> o;
+#pragma unroll
+            for (int e = 0; e < NW; ++e) {
+                uint32_t w[N];
+#pragma unroll
+                for (int k = 0; k < N; ++k) w[k] = r[u][k].w[e];
+                o.w[e] = agg_pair<N, DT>(p[u], w);
+            }
+            st_stream<NW>(out + i, o);
+        }
+    }
+}
+
+// 4-byte path (H even): pair i = t*P + c, P = H/2.
+template <int N, int DT>
+__global__ void __launch_bounds__(256)
+agg_fwd_pair_kernel(const uint32_t* __restrict__ res2, const float* __restrict__ pre,
+                    uint32_t* __restrict__ out2, uint64_t n_pairs, uint64_t P) {
+    pdl_enter();
+    const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+    for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_pairs; i += stride) {
+        const uint64_t t = i / P;
+        const uint32_t* src = res2 + (i + uint64_t(N - 1) * t * P);
+        uint32_t w[N];
+#pragma unroll
+        for (int k = 0; k < N; ++k) w[k] = ld_stream4(src + uint64_t(k) * P);
+        float p[N];
+        ld_pre<N>(pre + uint64_t(N) * t, false, p);
+        st_stream4(out2 + i, agg_pair<N, DT>(p, w));
+    }
+}
+
+// 2-byte path (any H, any 2-byte alignment): element i = t*H + h.
+template <int N, int DT>
+__global__ void __launch_bounds__(256)
+agg_fwd_element_kernel(const uint16_t* __restrict__ res, const float* __restrict__ pre,
+                       uint16_t* __restrict__ out, uint64_t n, uint64_t H) {
+    pdl_enter();
+    const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+    for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const uint64_t t = i / H;
+        const uint16_t* src = res + (i + uint64_t(N - 1) * t * H);
+        float p[N], q[N];
+        ld_pre<N>(pre + uint64_t(N) * t, false, p);
+#pragma unroll
+        for (int k = 0; k < N; ++k) q[k] = __fmul_rn(p[k], Elem<DT>::one(ld_stream2(src + uint64_t(k) * H)));
+        st_stream2(out + i, Elem<DT>::cvt(tree_sum<N>(q)));
+    }
+}
+
+// --------------------------------------------------------------------------
+// backward
+// --------------------------------------------------------------------------
+
+constexpr int kLanes = 256;   // lanes of ORDER-256
+constexpr int kGroups = 8;    // groups of 32 lanes
+
+// grad_residual for two adjacent elements: cvt(RN(pre_k * g)).
+template <int DT>
+__device__ __forceinline__ uint32_t scale_pair(float pk, uint32_t gw) {
+    return Elem<DT>::pack(__fmul_rn(pk, Elem<DT>::lo(gw)), __fmul_rn(pk, Elem<DT>::hi(gw)));
+}
+
+template <int DT, int NW>
+__device__ __forceinline__ Words<NW> scale_vec(float pk, const Words<NW>& g) {
+    Words<NW> o;
+#pragma unroll
+    for (int e = 0; e < NW; ++e) o.w[e] = scale_pair<DT>(pk, g.w[e]);
+    return o;
+}
+
+// ((q0+q1)+(q2+q3)) + ((q4+q5)+(q6+q7)) of q_e = g_e * r_e (exact products)
+// for the chunk held in words w0 .. w0+3 of g and r.
+template <int DT, int NW>
+__device__ __forceinline__ float chunk_partial(const Words<NW>& g, const Words<NW>& r, int w0) {
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        q[2 * i] = __fmul_rn(Elem<DT>::lo(g.w[w0 + i]), Elem<DT>::lo(r.w[w0 + i]));
+        q[2 * i + 1] = __fmul_rn(Elem<DT>::hi(g.w[w0 + i]), Elem<DT>::hi(r.w[w0 + i]));
+    }
+    return __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
+                     __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
+}
+
+__device__ __forceinline__ float chunk_partial8(const float q[8]) {
+    return __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
+                     __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
+}
+
+// Steps 4 and 5 of ORDER-256 for a block of 256/LPT threads, thread j holding
+// lanes LPT*j + l (l < LPT) in acc[l][k].  A group of 32 lanes is 32/LPT
+// adjacent threads: lane strides 16 .. LPT are thread strides 16/LPT .. 1
+// (xor shuffles), lane stride 1 (when LPT == 2) is the add of a thread's own
+// two lanes.  The 8 group values then fold with strides 4, 2, 1 in shared
+// memory, and grad_pre[t, 0..N-1] is written.  All threads of the block call it.
+template <int N, int LPT>
+__device__ __forceinline__ void fold_lanes_and_store(float (&acc)[LPT][N], float (*red)[N],
+                                                     float* __restrict__ grad_pre_t) {
+    constexpr int kThreadsPerGroup = 32 / LPT;
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+#pragma unroll
+        for (int s = kThreadsPerGroup / 2; s >= 1; s >>= 1) {
+#pragma unroll
+            for (int l = 0; l < LPT; ++l)
+                acc[l][k] = __fadd_rn(acc[l][k], __shfl_xor_sync(0xffffffffu, acc[l][k], s));
+        }
+        if (LPT == 2) acc[0][k] = __fadd_rn(acc[0][k], acc[LPT - 1][k]);
+    }
+    if ((threadIdx.x % kThreadsPerGroup) == 0) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) red[threadIdx.x / kThreadsPerGroup][k] = acc[0][k];
+    }
+    __syncthreads();
+    if (threadIdx.x < N) {
+        const int k = threadIdx.x;
+        float w[kGroups];
+#pragma unroll
+        for (int i = 0; i < kGroups; ++i) w[i] = red[i][k];
+#pragma unroll
+        for (int s = kGroups / 2; s >= 1; s >>= 1) {
+#pragma unroll
+            for (int i = 0; i < s; ++i) w[i] = __fadd_rn(w[i], w[i + s]);
+        }
+        grad_pre_t[k] = w[0];
+    }
+    __syncthreads();  // red[] is reused by the next token of this block
+}
+
+// Vector path: H % (2*NW) == 0 and g / residual / grad_residual aligned to
+// 4*NW bytes.  V = H / (2*NW) vectors per row; thread j handles vectors
+// j, j + B, j + 2B, ... (B = 256/LPT threads), i.e. for lane LPT*j + l the
+// chunks LPT*(j + mB) + l = (LPT*j + l) + 256m: exactly that lane's chunks,
+// in increasing order.  Up to BATCH vectors per thread are held in registers
+// per pass.
+template <int N, int DT, int NW, int BATCH, int MIN_BLOCKS>
+__global__ void __launch_bounds__(kLanes / (NW / 4), MIN_BLOCKS)
+agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict__ res,
+                   const float* __restrict__ pre, Words<NW>* __restrict__ gres,
+                   float* __restrict__ grad_pre, uint64_t T, uint32_t V, bool pre_vec) {
+    constexpr int LPT = NW / 4;
+    constexpr uint32_t B = kLanes / LPT;
+    __shared__ float red[kGroups][N];
+    pdl_enter();
+    const uint32_t j = threadIdx.x;
+    for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        float pk[N];
+        ld_pre<N>(pre + uint64_t(N) * t, pre_vec, pk);
+        const Words<NW>* gt = g + t * V;
+        const Words<NW>* rt = res + uint64_t(N) * t * V;
+        Words<NW>* grt = gres + uint64_t(N) * t * V;
+        float acc[LPT][N];
+#pragma unroll
+        for (int l = 0; l < LPT; ++l)
+#pragma unroll
+            for (int k = 0; k < N; ++k) acc[l][k] = 0.0f;
+        for (uint32_t v0 = j; v0 < V; v0 += B * BATCH) {
+            Words<NW> gv[BATCH];
+            Words<NW> rv[BATCH][N];
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const uint32_t v = v0 + uint32_t(b) * B;
+                if (v < V) {
+                    gv[b] = ld_stream<NW>(gt + v);
+#pragma unroll
+                    for (int k = 0; k < N; ++k) rv[b][k] = ld_stream<NW>(rt + uint64_t(k) * V + v);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const uint32_t v = v0 + uint32_t(b) * B;
+                if (v < V) {
+#pragma unroll
+                    for (int k = 0; k < N; ++k) {
+                        st_stream<NW>(grt + uint64_t(k) * V + v, scale_vec<DT, NW>(pk[k], gv[b]));
+#pragma unroll
+                        for (int l = 0; l < LPT; ++l)
+                            acc[l][k] = __fadd_rn(acc[l][k], chunk_partial<DT, NW>(gv[b], rv[b][k], 4 * l));
+                    }
+                }
+            }
+        }
+        fold_lanes_and_store<N, LPT>(acc, red, grad_pre + uint64_t(N) * t);
+    }
+}
+
+// 2-byte path: any H and any 2-byte alignment; same lanes, chunks and tree,
+// with positions past H contributing +0.0.  256 threads, one lane each.
+template <int N, int DT>
+__global__ void __launch_bounds__(kLanes)
+agg_bwd_element_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ res,
+                       const float* __restrict__ pre, uint16_t* __restrict__ gres,
+                       float* __restrict__ grad_pre, uint64_t T, uint64_t H) {
+    __shared__ float red[kGroups][N];
+    pdl_enter();
+    const uint64_t C = (H + 7) / 8;
+    for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        float pk[N];
+        ld_pre<N>(pre + uint64_t(N) * t, false, pk);
+        const uint16_t* gt = g + t * H;
+        const uint16_t* rt = res + uint64_t(N) * t * H;
+        uint16_t* grt = gres + uint64_t(N) * t * H;
+        float acc[1][N];
+#pragma unroll
+        for (int k = 0; k < N; ++k) acc[0][k] = 0.0f;
+        for (uint64_t c = threadIdx.x; c < C; c += kLanes) {
+            float gf[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint64_t h = 8 * c + e;
+                gf[e] = (h < H) ? Elem<DT>::one(ld_stream2(gt + h)) : 0.0f;
+            }
+#pragma unroll
+            for (int k = 0; k < N; ++k) {
+                float q[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint64_t h = 8 * c + e;
+                    if (h < H) {
+                        q[e] = __fmul_rn(gf[e], Elem<DT>::one(ld_stream2(rt + uint64_t(k) * H + h)));
+                        st_stream2(grt + uint64_t(k) * H + h, Elem<DT>::cvt(__fmul_rn(pk[k], gf[e])));
+                    } else {
+                        q[e] = 0.0f;
+                    }
+                }
+                acc[0][k] = __fadd_rn(acc[0][k], chunk_partial8(q));
+            }
+        }
+        fold_lanes_and_store<N, 1>(acc, red, grad_pre + uint64_t(N) * t);
+    }
+}
+
+}  // namespace mhc

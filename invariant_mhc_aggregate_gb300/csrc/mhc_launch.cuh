@@ -1,0 +1,218 @@
+// Host-side launch layer: picks the launch shape for a validated call and
+// launches the kernels of mhc_device.cuh with programmatic stream
+// serialization.  Launch shapes never change results.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mhc_device.cuh"
+
+namespace mhc {
+
+// Kernel path codes (the values of mhc_path_t).
+constexpr int kPathVec16 = 0;
+constexpr int kPathPair = 1;
+constexpr int kPathElement = 2;
+constexpr int kPathVec32 = 3;
+
+struct FwdCall {
+    const void* residual;
+    const float* pre;
+    void* out;
+    uint64_t T, H;
+    int n;            // streams: 1, 2, 4 or 8
+    int path;         // kPath*
+    bool pre_vec;     // pre aligned to min(16, 4n) bytes
+    int num_sms;
+    cudaStream_t stream;
+};
+
+struct BwdCall {
+    const void* g;
+    const void* residual;
+    const float* pre;
+    void* gres;
+    float* gpre;
+    uint64_t T, H;
+    int n;
+    int path;
+    bool pre_vec;
+    int num_sms;
+    cudaStream_t stream;
+};
+
+cudaError_t fwd_bf16(const FwdCall& c);
+cudaError_t fwd_f16(const FwdCall& c);
+cudaError_t bwd_bf16(const BwdCall& c);
+cudaError_t bwd_f16(const BwdCall& c);
+
+// Launch with programmatic stream serialization (see pdl_enter).
+template <typename... Params, typename... Args>
+cudaError_t launch(void (*kernel)(Params...), uint32_t grid, uint32_t block, cudaStream_t stream,
+                   Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
+inline uint32_t grid_for(uint64_t items, uint32_t per_block, uint64_t cap) {
+    uint64_t b = (items + per_block - 1) / per_block;
+    if (b > cap) b = cap;
+    if (b < 1) b = 1;
+    return uint32_t(b);
+}
+
+// ---------------------------------------------------------------------------
+// forward
+// ---------------------------------------------------------------------------
+
+template <int N, int DT, int NW, int BLOCK, int UNROLL>
+cudaError_t launch_fwd_vec(const void* residual, const float* pre, void* out, uint32_t n_vec,
+                           uint32_t V, bool pre_vec, cudaStream_t stream) {
+    const uint32_t per_block = uint32_t(BLOCK * UNROLL);
+    const uint32_t blocks = uint32_t((uint64_t(n_vec) + per_block - 1) / per_block);
+    return launch(agg_fwd_vec_kernel<N, DT, NW, BLOCK, UNROLL>, blocks, BLOCK, stream,
+                  static_cast<const Words<NW>*>(residual), pre, static_cast<Words<NW>*>(out), n_vec,
+                  V, make_fastdiv_u32(V), pre_vec);
+}
+
+// Large calls: 256 threads holding about 64 bytes of residual loads per
+// stream pair (UNROLL = 64 / (N * NW) vectors, at least 1); calls of at most
+// 8 KiB of output per SM: 128 threads x 1 vector, to spread a decode-sized
+// call over more SMs.  Vector indices are 32-bit: a call with 2^31 vectors or
+// more runs as several launches over consecutive token ranges (tokens are
+// independent, so the bytes are the same as one launch).
+template <int N, int DT, int NW>
+cudaError_t fwd_vec(const FwdCall& c) {
+    constexpr int kUnroll = (64 / (N * NW)) > 0 ? (64 / (N * NW)) : 1;
+    const uint64_t V = c.H / (2 * NW);
+    const uint64_t max_tokens = 0x7FFFFFFFull / V;
+    const uint64_t small_limit = uint64_t(c.num_sms) * (8192 / (4 * NW));
+    for (uint64_t t0 = 0; t0 < c.T; t0 += max_tokens) {
+        const uint64_t nt = (c.T - t0 < max_tokens) ? c.T - t0 : max_tokens;
+        const uint32_t n_vec = uint32_t(nt * V);
+        const void* r = static_cast<const char*>(c.residual) + t0 * 2 * N * c.H;
+        const float* p = c.pre + uint64_t(N) * t0;
+        void* o = static_cast<char*>(c.out) + t0 * 2 * c.H;
+        const cudaError_t e =
+            n_vec <= small_limit
+                ? launch_fwd_vec<N, DT, NW, 128, 1>(r, p, o, n_vec, uint32_t(V), c.pre_vec, c.stream)
+                : launch_fwd_vec<N, DT, NW, 256, kUnroll>(r, p, o, n_vec, uint32_t(V), c.pre_vec, c.stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+template <int N, int DT>
+cudaError_t fwd_n(const FwdCall& c) {
+    const uint64_t cap = uint64_t(c.num_sms) * 1024;
+    switch (c.path) {
+        case kPathVec32: return fwd_vec<N, DT, 8>(c);
+        case kPathVec16: return fwd_vec<N, DT, 4>(c);
+        case kPathPair: {
+            const uint64_t P = c.H / 2;
+            const uint64_t n = c.T * P;
+            return launch(agg_fwd_pair_kernel<N, DT>, grid_for(n, 256, cap), 256, c.stream,
+                          static_cast<const uint32_t*>(c.residual), c.pre, static_cast<uint32_t*>(c.out), n, P);
+        }
+        default: {
+            const uint64_t n = c.T * c.H;
+            return launch(agg_fwd_element_kernel<N, DT>, grid_for(n, 256, cap), 256, c.stream,
+                          static_cast<const uint16_t*>(c.residual), c.pre, static_cast<uint16_t*>(c.out), n, c.H);
+        }
+    }
+}
+
+template <int DT>
+cudaError_t fwd_dispatch(const FwdCall& c) {
+    switch (c.n) {
+        case 1: return fwd_n<1, DT>(c);
+        case 2: return fwd_n<2, DT>(c);
+        case 4: return fwd_n<4, DT>(c);
+        default: return fwd_n<8, DT>(c);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// backward
+// ---------------------------------------------------------------------------
+
+template <int N, int DT, int NW, int BATCH, int MIN_BLOCKS>
+cudaError_t launch_bwd_vec(const BwdCall& c, uint32_t V) {
+    constexpr int kThreads = kLanes / (NW / 4);
+    const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
+    return launch(agg_bwd_vec_kernel<N, DT, NW, BATCH, MIN_BLOCKS>, blocks, kThreads, c.stream,
+                  static_cast<const Words<NW>*>(c.g), static_cast<const Words<NW>*>(c.residual), c.pre,
+                  static_cast<Words<NW>*>(c.gres), c.gpre, c.T, V, c.pre_vec);
+}
+
+// Backward vector launch shapes.  A block holds one token; its threads keep
+// BATCH vectors each (g and N residual rows) in registers per pass, with the
+// register budget sized for MIN_BLOCKS blocks per SM, so that each SM keeps
+// roughly 160 KB of loads in flight.  For the pages' N = 4 with 32-byte
+// vectors (128 threads) the batch follows the vectors per thread so that a
+// row is covered in one pass: batch 1 / 2 / 4 with 6 / 3 / 2 blocks per SM
+// for up to 1 / 2 / more vectors per thread.
+template <int N, int DT>
+cudaError_t bwd_vec32(const BwdCall& c) {
+    const uint32_t V = uint32_t(c.H / 16);
+    if constexpr (N == 4) {
+        const uint32_t per_thread = (V + 127) / 128;
+        if (per_thread <= 1) return launch_bwd_vec<N, DT, 8, 1, 6>(c, V);
+        if (per_thread == 2) return launch_bwd_vec<N, DT, 8, 2, 3>(c, V);
+        return launch_bwd_vec<N, DT, 8, 4, 2>(c, V);
+    } else if constexpr (N == 1) {
+        return launch_bwd_vec<N, DT, 8, 4, 4>(c, V);
+    } else if constexpr (N == 2) {
+        return launch_bwd_vec<N, DT, 8, 4, 3>(c, V);
+    } else {
+        return launch_bwd_vec<N, DT, 8, 2, 2>(c, V);
+    }
+}
+
+template <int N, int DT>
+cudaError_t bwd_vec16(const BwdCall& c) {
+    const uint32_t V = uint32_t(c.H / 8);
+    if constexpr (N == 1) {
+        return launch_bwd_vec<N, DT, 4, 4, 3>(c, V);
+    } else if constexpr (N == 8) {
+        return launch_bwd_vec<N, DT, 4, 1, 2>(c, V);
+    } else {
+        return launch_bwd_vec<N, DT, 4, 2, 3>(c, V);
+    }
+}
+
+template <int N, int DT>
+cudaError_t bwd_n(const BwdCall& c) {
+    switch (c.path) {
+        case kPathVec32: return bwd_vec32<N, DT>(c);
+        case kPathVec16: return bwd_vec16<N, DT>(c);
+        default: {
+            const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
+            return launch(agg_bwd_element_kernel<N, DT>, blocks, kLanes, c.stream,
+                          static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.residual), c.pre,
+                          static_cast<uint16_t*>(c.gres), c.gpre, c.T, c.H);
+        }
+    }
+}
+
+template <int DT>
+cudaError_t bwd_dispatch(const BwdCall& c) {
+    switch (c.n) {
+        case 1: return bwd_n<1, DT>(c);
+        case 2: return bwd_n<2, DT>(c);
+        case 4: return bwd_n<4, DT>(c);
+        default: return bwd_n<8, DT>(c);
+    }
+}
+
+}  // namespace mhc

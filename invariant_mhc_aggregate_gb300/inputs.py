@@ -76,44 +76,47 @@ def _generator(device, seed: int) -> torch.Generator:
 
 
 def forward_inputs(T: int, H: int, recipe: str = "normal", seed: int = 0,
-                   device="cpu") -> tuple[torch.Tensor, torch.Tensor]:
-    """(residual bf16 [T,4,H], pre fp32 [T,4]) drawn on ``device``."""
+                   device="cpu", n: int = 4,
+                   dtype=torch.bfloat16) -> tuple[torch.Tensor, torch.Tensor]:
+    """(residual [T,n,H] in `dtype`, pre fp32 [T,n]) drawn on ``device``."""
     gen = _generator(device, seed)
-    return _draw_forward(T, H, recipe, gen, device)
+    return _draw_forward(T, H, recipe, gen, device, n, dtype)
 
 
 def backward_inputs(T: int, H: int, recipe: str = "normal", seed: int = 4,
-                    device="cpu") -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """(g bf16 [T,H], residual bf16 [T,4,H], pre fp32 [T,4]) drawn on ``device``."""
+                    device="cpu", n: int = 4,
+                    dtype=torch.bfloat16) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(g [T,H], residual [T,n,H], pre fp32 [T,n]) drawn on ``device``; g and the
+    residual in `dtype` (bfloat16 or float16, rounded to nearest even)."""
     gen = _generator(device, seed)
-    residual, pre = _draw_forward(T, H, recipe, gen, device)
+    residual, pre = _draw_forward(T, H, recipe, gen, device, n, dtype)
     g = torch.randn((T, H), generator=gen, device=device, dtype=torch.float32)
-    return g.to(torch.bfloat16), residual, pre
+    return g.to(dtype), residual, pre
 
 
-def _draw_forward(T, H, recipe, gen, device):
+def _draw_forward(T, H, recipe, gen, device, n=4, dtype=torch.bfloat16):
     if recipe not in RECIPES:
         raise ValueError(f"unknown recipe {recipe!r}; expected one of {RECIPES}")
     f32 = torch.float32
-    r = torch.randn((T, 4, H), generator=gen, device=device, dtype=f32)
+    r = torch.randn((T, n, H), generator=gen, device=device, dtype=f32)
     if recipe == "decode":
         r.mul_(2.0)
-        outlier = torch.rand((T, 4, H), generator=gen, device=device, dtype=f32) < 0.01
+        outlier = torch.rand((T, n, H), generator=gen, device=device, dtype=f32) < 0.01
         r = torch.where(outlier, r * 100.0, r)
-        pre = torch.sigmoid(torch.randn((T, 4), generator=gen, device=device, dtype=f32))
+        pre = torch.sigmoid(torch.randn((T, n), generator=gen, device=device, dtype=f32))
     else:
-        pre = torch.rand((T, 4), generator=gen, device=device, dtype=f32)
+        pre = torch.rand((T, n), generator=gen, device=device, dtype=f32)
         if recipe == "ragged":
-            u = torch.rand((T, 4), generator=gen, device=device, dtype=f32)
+            u = torch.rand((T, n), generator=gen, device=device, dtype=f32)
             pre = torch.where(u < 0.05, torch.zeros_like(pre), pre)
             pre = torch.where((u >= 0.05) & (u < 0.10), torch.ones_like(pre), pre)
-    residual = r.to(torch.bfloat16)
+    residual = r.to(dtype)
     del r
     return residual.contiguous(), pre.contiguous()
 
 
 def as_u16(x: torch.Tensor):
-    """BF16 tensor -> numpy uint16 bit patterns (host copy)."""
+    """BF16 / FP16 tensor -> numpy uint16 bit patterns (host copy)."""
     return x.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")
 
 

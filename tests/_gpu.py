@@ -154,3 +154,42 @@ def assert_bytes_equal(got: np.ndarray, want: np.ndarray, what: str):
         idx = tuple(int(b[0]) for b in bad)
         raise AssertionError(f"{what}: {n} elements differ, first at {idx}: "
                              f"got {got[idx]!r} want {want[idx]!r}")
+
+
+DTYPE_CODE = {torch.bfloat16: binding.MHC_DTYPE_BF16, torch.float16: binding.MHC_DTYPE_F16}
+DTYPE_NAME = {torch.bfloat16: "bf16", torch.float16: "f16"}
+
+
+def run_agg_fwd(residual: torch.Tensor, pre: torch.Tensor, offsets=(0, 0, 0), check_guards=True):
+    """General forward (stream count from residual.shape[1], storage from its dtype)
+    through the C ABI with buffers at the given byte offsets."""
+    T, n, H = residual.shape
+    r = DevBuf.of(residual, offsets[0])
+    p = DevBuf.of(pre, offsets[1])
+    o = DevBuf(T * H * 2, offsets[2])
+    assert binding.agg_fwd_path_raw(r.ptr, p.ptr, o.ptr, T, n, H) == expected_fwd_path(H, offsets)
+    st = binding.agg_fwd_raw(r.ptr, p.ptr, o.ptr, T, n, H, DTYPE_CODE[residual.dtype], stream_handle())
+    assert st == binding.MHC_OK, st
+    torch.cuda.synchronize()
+    if check_guards:
+        assert o.guards_ok(), "forward wrote outside out"
+    return o.get(np.uint16, (T, H))
+
+
+def run_agg_bwd(g: torch.Tensor, residual: torch.Tensor, pre: torch.Tensor,
+                offsets=(0, 0, 0, 0, 0), check_guards=True):
+    T, n, H = residual.shape
+    gb = DevBuf.of(g, offsets[0])
+    r = DevBuf.of(residual, offsets[1])
+    p = DevBuf.of(pre, offsets[2])
+    gr = DevBuf(T * n * H * 2, offsets[3])
+    gp = DevBuf(T * n * 4, offsets[4])
+    assert binding.agg_bwd_path_raw(gb.ptr, r.ptr, p.ptr, gr.ptr, gp.ptr, T, n, H) == \
+        expected_bwd_path(H, offsets)
+    st = binding.agg_bwd_raw(gb.ptr, r.ptr, p.ptr, gr.ptr, gp.ptr, T, n, H,
+                             DTYPE_CODE[residual.dtype], stream_handle())
+    assert st == binding.MHC_OK, st
+    torch.cuda.synchronize()
+    if check_guards:
+        assert gr.guards_ok() and gp.guards_ok(), "backward wrote outside its outputs"
+    return gr.get(np.uint16, (T, n, H)), gp.get(np.float32, (T, n))

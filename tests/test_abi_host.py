@@ -43,7 +43,7 @@ def test_exported_symbols_are_c_linkage():
 
 
 def test_abi_version(lib):
-    assert lib.mhc_h_aggregate_abi_version() == 1
+    assert lib.mhc_h_aggregate_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -163,7 +163,7 @@ def test_build_has_no_fast_math():
 
 
 def test_kernels_use_rn_intrinsics_only():
-    src = open(_build.SOURCES[0]).read()
+    src = "".join(open(p).read() for p in _build.DEPS if p.startswith(_build.CSRC))
     code = re.sub(r"//.*", "", src)
     assert "__fmaf" not in code and "fmaf(" not in code and "__fma_rn" not in code
     # one writer per output element: no device atomics or reductions
@@ -204,3 +204,46 @@ int main() {
                    check=True)
     res = subprocess.run([str(exe)], capture_output=True, text=True)
     assert res.returncode == 0, res.stdout
+
+
+# --- the general entry points (stream count n, storage dtype)
+
+def test_general_path_choice(lib):
+    def gpath(n, H=4096, r_off=0, o_off=0, T=4):
+        return binding.agg_fwd_path_raw(A + r_off, A + GAP, A + 2 * GAP + o_off, T, n, H)
+    for n in (1, 2, 4, 8):
+        assert gpath(n) == binding.MHC_PATH_VEC32
+        assert gpath(n, r_off=16) == binding.MHC_PATH_VEC16
+        assert gpath(n, H=2050) == binding.MHC_PATH_PAIR
+        assert gpath(n, H=1279) == binding.MHC_PATH_ELEMENT
+    for n in (0, 3, 5, 16, -1):
+        assert gpath(n) == binding.MHC_PATH_NONE
+    # n = 4 is the pages' op
+    assert gpath(4) == binding.fwd_path_raw(A, A + GAP, A + 2 * GAP, 4, 4096)
+    # an output that ends where an n = 8 residual would still be: overlap depends on n
+    T, H = 2, 64
+    out_at = A + T * 4 * H * 2
+    assert binding.agg_fwd_path_raw(A, A + GAP, out_at, T, 4, H) != binding.MHC_PATH_NONE
+    assert binding.agg_fwd_path_raw(A, A + GAP, out_at, T, 8, H) == binding.MHC_PATH_NONE
+
+
+def test_general_bwd_path_choice(lib):
+    for n in (1, 2, 4, 8):
+        assert binding.agg_bwd_path_raw(A, A + GAP, A + 2 * GAP, A + 3 * GAP, A + 4 * GAP, 4, n,
+                                        4096) == binding.MHC_PATH_VEC32
+    assert binding.agg_bwd_path_raw(A, A + GAP, A + 2 * GAP, A + 3 * GAP, A + 4 * GAP, 4, 6,
+                                    4096) == binding.MHC_PATH_NONE
+
+
+def test_general_invalid_arguments(lib):
+    args = (A, A + GAP, A + 2 * GAP)
+    assert binding.agg_fwd_raw(*args, 4, 3, 64, binding.MHC_DTYPE_BF16) == binding.MHC_ERR_UNSUPPORTED
+    assert binding.agg_fwd_raw(*args, 4, 4, 64, 7) == binding.MHC_ERR_INVALID_ARG
+    assert binding.agg_fwd_raw(*args, -1, 2, 64, binding.MHC_DTYPE_F16) == binding.MHC_ERR_INVALID_ARG
+    assert binding.agg_fwd_raw(*args, 0, 8, 64, binding.MHC_DTYPE_F16) == binding.MHC_OK
+    bargs = (A, A + GAP, A + 2 * GAP, A + 3 * GAP, A + 4 * GAP)
+    assert binding.agg_bwd_raw(*bargs, 4, 0, 64, binding.MHC_DTYPE_BF16) == binding.MHC_ERR_UNSUPPORTED
+    assert binding.agg_bwd_raw(*bargs, 4, 2, 64, 2) == binding.MHC_ERR_INVALID_ARG
+    assert binding.agg_bwd_raw(*bargs, 0, 1, 64, binding.MHC_DTYPE_BF16) == binding.MHC_OK
+    # byte count of an n = 8 residual overflows int64
+    assert binding.agg_fwd_raw(*args, 1 << 31, 8, 1 << 29, binding.MHC_DTYPE_BF16) == binding.MHC_ERR_INVALID_ARG
