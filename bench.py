@@ -475,6 +475,17 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
         n = max(2, -(-3 * l2 // set_bytes))
         return n if n <= 8 else None
 
+    # The floor of the cold method: a graph holding one trivial kernel.
+    z = torch.zeros(1, device=dev)
+    floor_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(floor_graph, stream=stream):
+        z.add_(1.0)
+    results.append({"workload": "launch_floor", "dir": "none",
+                    "note": "one trivial kernel timed by the cold method (graph replay after a "
+                            "256 MiB write flush, CUDA events)",
+                    "cold": {"us_p20_p50_p80": time_graph(floor_graph)}})
+    del floor_graph
+
     for name, seed, recipe, shapes in FWD_SWEEP:
         for T, H in shapes:
             r, p = forward_inputs(T, H, recipe, seed, device=dev)
