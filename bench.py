@@ -507,6 +507,15 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
                 us_s = time_steady(lambda a, b, c: binding.mhc_h_aggregate_fwd(a, b, c), sets)
                 entry["steady"] = {"us": us_s, "sets": ns, **entry_for(us_s, nbytes)}
                 del sets
+            elif T <= 128:
+                # decode-sized: back-to-back calls over 16 buffer sets that stay in L2
+                # (as a decode step's inputs, just written by the previous layer, would)
+                sets = [(r, p, o)] + [(torch.empty_like(r).copy_(r), p.clone(), torch.empty_like(o))
+                                      for _ in range(15)]
+                us_w = time_steady(lambda a, b, c: binding.mhc_h_aggregate_fwd(a, b, c), sets)
+                entry["warm"] = {"us": us_w, "sets": 16, "note": "back-to-back, inputs L2-resident",
+                                 **entry_for(us_w, nbytes)}
+                del sets
             results.append(entry)
             del r, p, o
             torch.cuda.empty_cache()
