@@ -620,7 +620,43 @@ def check_agg_grad_pre_order_f16(o):
         assert np.array_equal(f32_bits(gp)[0], want), name
 
 
+def check_fwd_fp64_emulation(o):
+    """FP64 brute force on tiny shapes: each binary32 operation computed in FP64
+    and rounded once to binary32 is correctly rounded (53 >= 2*24 + 2, so the
+    double rounding is innocuous), and the final BF16 rounding is numpy's own
+    RNE on the pattern; every element must match."""
+    rng = np.random.default_rng(57)
+    for T, H in ((1, 1), (2, 7), (3, 64)):
+        res = random_bf16(rng, (T, 4, H), scale=2.0)
+        pre = rng.random((T, 4), dtype=np.float32)
+        r = bf16_widen(res).astype(np.float64)
+        p = pre.astype(np.float64)
+        f32 = lambda x: np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+        prod = [f32(p[:, k, None] * r[:, k, :]) for k in range(4)]
+        s = f32(f32(prod[0] + prod[1]) + f32(prod[2] + prod[3])).astype(np.float32)
+        bits = s.view(np.uint32)
+        kept = bits >> 16
+        dropped = bits & 0xFFFF
+        up = (dropped > 0x8000) | ((dropped == 0x8000) & ((kept & 1) == 1))
+        want = (kept + up).astype(np.uint16)
+        assert np.array_equal(o.fwd(res, pre), want), (T, H)
+
+
+def check_gr_fp64_emulation(o):
+    rng = np.random.default_rng(58)
+    g = random_bf16(rng, (3, 33), scale=3.0)
+    pre = rng.random((3, 4), dtype=np.float32) * np.float32(5.0)
+    prod = (pre.astype(np.float64)[:, :, None] * bf16_widen(g).astype(np.float64)[:, None, :]).astype(np.float32)
+    bits = prod.view(np.uint32)
+    kept = bits >> 16
+    dropped = bits & 0xFFFF
+    up = (dropped > 0x8000) | ((dropped == 0x8000) & ((kept & 1) == 1))
+    assert np.array_equal(o.grad_residual(g, pre), (kept + up).astype(np.uint16))
+
+
 ALL_CHECKS += [
+    check_fwd_fp64_emulation,
+    check_gr_fp64_emulation,
     check_f16_golden,
     check_f16_roundtrip_exhaustive,
     check_f16_vs_torch,
