@@ -590,26 +590,26 @@ def _host_threads() -> int:
 def cpu_baseline(g, res, pre, T, H, seconds):
     """The CPU oracle, as it stands, on the host cores over a bounded sample of
     the same workload (whole tokens), sized to about `seconds` of work."""
+    import torch
     import oracle
+
+    def host(n_tok):
+        return (g[:n_tok].contiguous().cpu().view(torch.int16).numpy().view(np.uint16),
+                res[:n_tok].contiguous().cpu().view(torch.int16).numpy().view(np.uint16),
+                pre[:n_tok].contiguous().cpu().numpy())
+
     o = oracle.default()
     threads = _host_threads()
-    probe = 64
-    gu = g[:probe].contiguous().cpu().view(__import__("torch").int16).numpy().view(np.uint16)
-    ru = res[:probe].contiguous().cpu().view(__import__("torch").int16).numpy().view(np.uint16)
-    pf = pre[:probe].contiguous().cpu().numpy()
+    probe = min(T, 64)
     t0 = time.perf_counter()
-    _oracle_pass(o, gu, ru, pf, threads)
-    dt = time.perf_counter() - t0
-    per_token = dt / probe
+    _oracle_pass(o, *host(probe), threads)
+    per_token = (time.perf_counter() - t0) / probe
     n_tok = int(min(T, max(probe, seconds / max(per_token, 1e-9))))
     reps = max(1, int(seconds / max(per_token * n_tok, 1e-9)))
-    import torch
-    gu = g[:n_tok].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
-    ru = res[:n_tok].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
-    pf = pre[:n_tok].contiguous().cpu().numpy()
+    sample = host(n_tok)
     t0 = time.perf_counter()
     for _ in range(reps):
-        _oracle_pass(o, gu, ru, pf, threads)
+        _oracle_pass(o, *sample, threads)
     dt = time.perf_counter() - t0
     bytes_done = reps * (fwd_bytes(n_tok, H) + bwd_bytes(n_tok, H))
     return {"value": round(bytes_done / dt / 1e9, 3), "unit": UNIT, "cores": threads,
