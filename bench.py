@@ -427,9 +427,12 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
     before each sample (the pages' cold-L2 method; the flush leaves dirty lines
     that the timed call has to write back); 7 rounds x (10 warm-up + 100
     samples), p20/p50/p80 of the round medians.
-    "steady": 400 calls back to back, rotating over enough buffer sets that no
-    call finds its inputs in L2 (at least 3x L2 in total), events only at the
-    two ends; shapes whose sets would not reach that in 8 sets are skipped.
+    "steady": about 400 calls back to back (a CUDA graph of at least 16
+    calls, replayed), rotating over enough buffer sets that no call finds its
+    inputs in L2 (at least 3x L2 in total), events only at the two ends;
+    shapes whose sets would not reach that in 8 sets get a "warm" entry
+    instead (16 sets that stay in L2, as a decode step's freshly written
+    inputs would).
     """
     results = []
     stream = torch.cuda.Stream(dev)
@@ -454,17 +457,30 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
         return [round(float(x), 3) for x in q]
 
     def time_steady(call, sets, n=400):
-        for i in range(2 * len(sets)):
-            call(*sets[i % len(sets)])
+        """Per-call time of back-to-back calls rotating over `sets`, from a CUDA
+        graph of at least 16 calls (so the host's launch cost is out of the
+        measurement and consecutive kernels keep their programmatic overlap),
+        replayed until about n calls ran; events only at the two ends."""
+        per_graph = max(16, len(sets))
+        for i in range(len(sets)):
+            call(*sets[i])
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(per_graph):
+                call(*sets[i % len(sets)])
+        reps = max(2, n // per_graph)
+        graph.replay()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
-        for i in range(n):
-            call(*sets[i % len(sets)])
+        for _ in range(reps):
+            graph.replay()
         e1.record()
         torch.cuda.synchronize()
-        return round(e0.elapsed_time(e1) * 1e3 / n, 3)
+        del graph
+        return round(e0.elapsed_time(e1) * 1e3 / (reps * per_graph), 3)
 
     def entry_for(us, nbytes):
         gbs = nbytes / (us * 1e-6) / 1e9
@@ -544,6 +560,25 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
             results.append(entry)
             del g, r, p, gr, gp
             torch.cuda.empty_cache()
+    # the general form (stream count n, FP16 storage), steady state only
+    for n, dtype in ((8, torch.bfloat16), (2, torch.bfloat16), (4, torch.float16)):
+        T, H = 4096, 7168
+        name = f"general_n{n}_{'bf16' if dtype == torch.bfloat16 else 'f16'}"
+        g, r, p = backward_inputs(T, H, "normal", 4, device=dev, n=n, dtype=dtype)
+        fb = T * (2 * (n + 1) * H + 4 * n)
+        bb = T * (2 * (2 * n + 1) * H + 8 * n)
+        sets = [(g, r, p)] + [(g.clone(), r.clone(), p.clone()) for _ in range(max(1, n_sets(fb) or 2) - 1)]
+        fsets = [(rr, pp, torch.empty((T, H), dtype=dtype, device=dev)) for _, rr, pp in sets]
+        us_f = time_steady(lambda a, b, c: binding.mhc_aggregate_fwd(a, b, c), fsets)
+        bsets = [(gg, rr, pp, torch.empty_like(rr), torch.empty((T, n), dtype=torch.float32, device=dev))
+                 for gg, rr, pp in sets]
+        us_b = time_steady(lambda a, b, c, d, e: binding.mhc_aggregate_bwd(a, b, c, d, e), bsets)
+        results.append({"workload": name, "dir": "fwd", "T": T, "H": H, "n": n,
+                        "steady": {"us": us_f, "sets": len(sets), **entry_for(us_f, fb)}})
+        results.append({"workload": name, "dir": "bwd", "T": T, "H": H, "n": n,
+                        "steady": {"us": us_b, "sets": len(sets), **entry_for(us_b, bb)}})
+        del g, r, p, sets, fsets, bsets
+        torch.cuda.empty_cache()
     torch.cuda.synchronize()
     return results
 
