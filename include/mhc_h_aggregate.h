@@ -94,7 +94,7 @@ typedef enum mhc_status {
 typedef enum mhc_path {
     MHC_PATH_NONE = -1,   /* the call would be rejected or launches nothing */
     MHC_PATH_VEC16 = 0,   /* 16-byte loads/stores: H % 8 == 0, buffers 16-byte aligned */
-    MHC_PATH_PAIR = 1,    /* 4-byte loads/stores: H even, buffers 4-byte aligned (forward only) */
+    MHC_PATH_PAIR = 1,    /* 4-byte loads/stores: H even, buffers 4-byte aligned */
     MHC_PATH_ELEMENT = 2, /* 2-byte loads/stores: any H and alignment */
     MHC_PATH_VEC32 = 3    /* 32-byte loads/stores: H % 16 == 0, buffers 32-byte aligned */
 } mhc_path_t;

@@ -35,7 +35,9 @@
 //    shared memory.  No atomics, no cross-block traffic.
 //  * Narrower paths (H not a multiple of 8, or buffers not 16-byte aligned)
 //    run the same per-element arithmetic and the same grad_pre tree with 4- or
-//    2-byte accesses, so every path gives the same bytes.
+//    2-byte coalesced accesses (the backward stages row segments in shared
+//    memory so that each lane still sees its own 8-value chunks), so every
+//    path gives the same bytes.
 //  * Every kernel is launched with programmatic stream serialization and
 //    waits for its predecessor before touching memory (pdl_enter).
 //  * No tensor cores: nothing here is a contraction.
@@ -277,40 +279,74 @@ agg_fwd_vec_kernel(const Words<NW>* __restrict__ res, const float* __restrict__ 
     }
 }
 
-// 4-byte path (H even): pair i = t*P + c, P = H/2.
+// Narrow forward paths: a 2-D grid of (row segment, token) blocks, grid-stride
+// over tokens.  A block of 256 threads covers 2048 units of one output row
+// (unit = a 4-byte pair of values when H is even and the buffers are 4-byte
+// aligned, else one 2-byte value); thread j takes units e*256 + j (e < 8), so
+// consecutive threads touch consecutive units (coalesced), and all its loads
+// are issued before any arithmetic.  The token's pre is loaded once.
+constexpr int kNarrowBlock = 256;
+constexpr int kNarrowPerThread = 8;
+constexpr int kNarrowSeg = kNarrowBlock * kNarrowPerThread;
+
+// 4-byte path: P = H/2 pairs per row.
 template <int N, int DT>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kNarrowBlock)
 agg_fwd_pair_kernel(const uint32_t* __restrict__ res2, const float* __restrict__ pre,
-                    uint32_t* __restrict__ out2, uint64_t n_pairs, uint64_t P) {
+                    uint32_t* __restrict__ out2, uint64_t T, uint64_t P) {
     pdl_enter();
-    const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
-    for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_pairs; i += stride) {
-        const uint64_t t = i / P;
-        const uint32_t* src = res2 + (i + uint64_t(N - 1) * t * P);
-        uint32_t w[N];
-#pragma unroll
-        for (int k = 0; k < N; ++k) w[k] = ld_stream4(src + uint64_t(k) * P);
+    const uint64_t base = uint64_t(blockIdx.x) * kNarrowSeg + threadIdx.x;
+    for (uint64_t t = blockIdx.y; t < T; t += gridDim.y) {
         float p[N];
         ld_pre<N>(pre + uint64_t(N) * t, false, p);
-        st_stream4(out2 + i, agg_pair<N, DT>(p, w));
+        const uint32_t* src = res2 + uint64_t(N) * t * P;
+        uint32_t w[kNarrowPerThread][N];
+#pragma unroll
+        for (int e = 0; e < kNarrowPerThread; ++e) {
+            const uint64_t c = base + uint64_t(e) * kNarrowBlock;
+            if (c < P) {
+#pragma unroll
+                for (int k = 0; k < N; ++k) w[e][k] = ld_stream4(src + uint64_t(k) * P + c);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < kNarrowPerThread; ++e) {
+            const uint64_t c = base + uint64_t(e) * kNarrowBlock;
+            if (c < P) st_stream4(out2 + t * P + c, agg_pair<N, DT>(p, w[e]));
+        }
     }
 }
 
-// 2-byte path (any H, any 2-byte alignment): element i = t*H + h.
+// 2-byte path: any H and any 2-byte alignment.
 template <int N, int DT>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kNarrowBlock)
 agg_fwd_element_kernel(const uint16_t* __restrict__ res, const float* __restrict__ pre,
-                       uint16_t* __restrict__ out, uint64_t n, uint64_t H) {
+                       uint16_t* __restrict__ out, uint64_t T, uint64_t H) {
     pdl_enter();
-    const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
-    for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
-        const uint64_t t = i / H;
-        const uint16_t* src = res + (i + uint64_t(N - 1) * t * H);
-        float p[N], q[N];
+    const uint64_t base = uint64_t(blockIdx.x) * kNarrowSeg + threadIdx.x;
+    for (uint64_t t = blockIdx.y; t < T; t += gridDim.y) {
+        float p[N];
         ld_pre<N>(pre + uint64_t(N) * t, false, p);
+        const uint16_t* src = res + uint64_t(N) * t * H;
+        uint16_t v[kNarrowPerThread][N];
 #pragma unroll
-        for (int k = 0; k < N; ++k) q[k] = __fmul_rn(p[k], Elem<DT>::one(ld_stream2(src + uint64_t(k) * H)));
-        st_stream2(out + i, Elem<DT>::cvt(tree_sum<N>(q)));
+        for (int e = 0; e < kNarrowPerThread; ++e) {
+            const uint64_t h = base + uint64_t(e) * kNarrowBlock;
+            if (h < H) {
+#pragma unroll
+                for (int k = 0; k < N; ++k) v[e][k] = ld_stream2(src + uint64_t(k) * H + h);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < kNarrowPerThread; ++e) {
+            const uint64_t h = base + uint64_t(e) * kNarrowBlock;
+            if (h < H) {
+                float q[N];
+#pragma unroll
+                for (int k = 0; k < N; ++k) q[k] = __fmul_rn(p[k], Elem<DT>::one(v[e][k]));
+                st_stream2(out + t * H + h, Elem<DT>::cvt(tree_sum<N>(q)));
+            }
+        }
     }
 }
 
@@ -345,11 +381,6 @@ __device__ __forceinline__ float chunk_partial(const Words<NW>& g, const Words<N
         q[2 * i] = __fmul_rn(Elem<DT>::lo(g.w[w0 + i]), Elem<DT>::lo(r.w[w0 + i]));
         q[2 * i + 1] = __fmul_rn(Elem<DT>::hi(g.w[w0 + i]), Elem<DT>::hi(r.w[w0 + i]));
     }
-    return __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
-                     __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
-}
-
-__device__ __forceinline__ float chunk_partial8(const float q[8]) {
     return __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
                      __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
 }
@@ -451,16 +482,29 @@ agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict_
     }
 }
 
-// 2-byte path: any H and any 2-byte alignment; same lanes, chunks and tree,
-// with positions past H contributing +0.0.  256 threads, one lane each.
-template <int N, int DT>
+// Narrow backward paths: any H; same lanes, chunks and tree.  256 threads,
+// one lane each.  A token's rows are processed in segments of 2048 values =
+// 256 chunks, so segment m holds exactly chunk 256m + j of lane j.  Each
+// segment of g and of the N residual rows is loaded with coalesced accesses
+// into shared memory (values past H are +0), lane j reads its chunk there,
+// adds its partial and writes its grad_residual chunk back in place, and the
+// segment's grad_residual rows are then stored with coalesced accesses.
+// PAIRS: 4-byte accesses (H even, buffers 4-byte aligned); else 2-byte.
+template <int N, int DT, bool PAIRS>
 __global__ void __launch_bounds__(kLanes)
-agg_bwd_element_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ res,
-                       const float* __restrict__ pre, uint16_t* __restrict__ gres,
-                       float* __restrict__ grad_pre, uint64_t T, uint64_t H) {
+agg_bwd_staged_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ res,
+                      const float* __restrict__ pre, uint16_t* __restrict__ gres,
+                      float* __restrict__ grad_pre, uint64_t T, uint64_t H) {
+    constexpr int kSeg = 8 * kLanes;                 // values per segment
+    constexpr int kUnit = PAIRS ? 2 : 1;             // values per access
+    constexpr int kPer = kSeg / (kUnit * kLanes);    // accesses per thread per row
     __shared__ float red[kGroups][N];
+    __shared__ __align__(16) uint16_t sg[kSeg];
+    __shared__ __align__(16) uint16_t sr[N][kSeg];
     pdl_enter();
+    const uint32_t j = threadIdx.x;
     const uint64_t C = (H + 7) / 8;
+    const uint64_t U = H / kUnit;                    // units per row
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
         float pk[N];
         ld_pre<N>(pre + uint64_t(N) * t, false, pk);
@@ -470,28 +514,56 @@ agg_bwd_element_kernel(const uint16_t* __restrict__ g, const uint16_t* __restric
         float acc[1][N];
 #pragma unroll
         for (int k = 0; k < N; ++k) acc[0][k] = 0.0f;
-        for (uint64_t c = threadIdx.x; c < C; c += kLanes) {
-            float gf[8];
+        for (uint64_t base = 0; base < H; base += kSeg) {
+            const uint64_t ubase = base / kUnit;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint64_t h = 8 * c + e;
-                gf[e] = (h < H) ? Elem<DT>::one(ld_stream2(gt + h)) : 0.0f;
+            for (int e = 0; e < kPer; ++e) {
+                const uint32_t s = e * kLanes + j;   // unit index within the segment
+                const uint64_t u = ubase + s;
+                if (PAIRS) {
+                    reinterpret_cast<uint32_t*>(sg)[s] =
+                        (u < U) ? ld_stream4(reinterpret_cast<const uint32_t*>(gt) + u) : 0u;
+#pragma unroll
+                    for (int k = 0; k < N; ++k)
+                        reinterpret_cast<uint32_t*>(sr[k])[s] =
+                            (u < U) ? ld_stream4(reinterpret_cast<const uint32_t*>(rt + uint64_t(k) * H) + u) : 0u;
+                } else {
+                    sg[s] = (u < U) ? ld_stream2(gt + u) : uint16_t(0);
+#pragma unroll
+                    for (int k = 0; k < N; ++k)
+                        sr[k][s] = (u < U) ? ld_stream2(rt + uint64_t(k) * H + u) : uint16_t(0);
+                }
             }
+            __syncthreads();
+            if (base / 8 + j < C) {
+                Words<4> gv;
+                *reinterpret_cast<uint4*>(gv.w) = *reinterpret_cast<const uint4*>(sg + 8 * j);
 #pragma unroll
-            for (int k = 0; k < N; ++k) {
-                float q[8];
+                for (int k = 0; k < N; ++k) {
+                    Words<4> rv;
+                    *reinterpret_cast<uint4*>(rv.w) = *reinterpret_cast<const uint4*>(&sr[k][8 * j]);
+                    acc[0][k] = __fadd_rn(acc[0][k], chunk_partial<DT, 4>(gv, rv, 0));
+                    const Words<4> o = scale_vec<DT, 4>(pk[k], gv);
+                    *reinterpret_cast<uint4*>(&sr[k][8 * j]) = *reinterpret_cast<const uint4*>(o.w);
+                }
+            }
+            __syncthreads();
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint64_t h = 8 * c + e;
-                    if (h < H) {
-                        q[e] = __fmul_rn(gf[e], Elem<DT>::one(ld_stream2(rt + uint64_t(k) * H + h)));
-                        st_stream2(grt + uint64_t(k) * H + h, Elem<DT>::cvt(__fmul_rn(pk[k], gf[e])));
-                    } else {
-                        q[e] = 0.0f;
+            for (int e = 0; e < kPer; ++e) {
+                const uint32_t s = e * kLanes + j;
+                const uint64_t u = ubase + s;
+                if (u < U) {
+#pragma unroll
+                    for (int k = 0; k < N; ++k) {
+                        if (PAIRS)
+                            st_stream4(reinterpret_cast<uint32_t*>(grt + uint64_t(k) * H) + u,
+                                       reinterpret_cast<const uint32_t*>(sr[k])[s]);
+                        else
+                            st_stream2(grt + uint64_t(k) * H + u, sr[k][s]);
                     }
                 }
-                acc[0][k] = __fadd_rn(acc[0][k], chunk_partial8(q));
             }
+            __syncthreads();  // the next segment overwrites the staging buffers
         }
         fold_lanes_and_store<N, 1>(acc, red, grad_pre + uint64_t(N) * t);
     }

@@ -92,6 +92,7 @@ mhc_path_t bwd_path(const void* g, const void* residual, const float* pre, const
         if (overlap(rgr, in) || overlap(rgp, in)) return MHC_PATH_NONE;
     if (H % 16 == 0 && aligned(g, 32) && aligned(residual, 32) && aligned(gres, 32)) return MHC_PATH_VEC32;
     if (H % 8 == 0 && aligned(g, 16) && aligned(residual, 16) && aligned(gres, 16)) return MHC_PATH_VEC16;
+    if (H % 2 == 0 && aligned(g, 4) && aligned(residual, 4) && aligned(gres, 4)) return MHC_PATH_PAIR;
     return MHC_PATH_ELEMENT;
 }
 

@@ -112,23 +112,42 @@ cudaError_t fwd_vec(const FwdCall& c) {
     return cudaSuccess;
 }
 
+// Narrow forward paths: one block per (2048-unit row segment, token), with
+// at most 65535 token rows of blocks (grid-stride over the rest).
+inline dim3 narrow_grid(uint64_t units_per_row, uint64_t T) {
+    const uint64_t segs = (units_per_row + kNarrowSeg - 1) / kNarrowSeg;
+    return dim3(uint32_t(segs), uint32_t(T < 65535 ? T : 65535));
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch2d(void (*kernel)(Params...), dim3 grid, uint32_t block, cudaStream_t stream,
+                     Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 template <int N, int DT>
 cudaError_t fwd_n(const FwdCall& c) {
-    const uint64_t cap = uint64_t(c.num_sms) * 1024;
     switch (c.path) {
         case kPathVec32: return fwd_vec<N, DT, 8>(c);
         case kPathVec16: return fwd_vec<N, DT, 4>(c);
         case kPathPair: {
             const uint64_t P = c.H / 2;
-            const uint64_t n = c.T * P;
-            return launch(agg_fwd_pair_kernel<N, DT>, grid_for(n, 256, cap), 256, c.stream,
-                          static_cast<const uint32_t*>(c.residual), c.pre, static_cast<uint32_t*>(c.out), n, P);
+            return launch2d(agg_fwd_pair_kernel<N, DT>, narrow_grid(P, c.T), kNarrowBlock, c.stream,
+                            static_cast<const uint32_t*>(c.residual), c.pre, static_cast<uint32_t*>(c.out), c.T, P);
         }
-        default: {
-            const uint64_t n = c.T * c.H;
-            return launch(agg_fwd_element_kernel<N, DT>, grid_for(n, 256, cap), 256, c.stream,
-                          static_cast<const uint16_t*>(c.residual), c.pre, static_cast<uint16_t*>(c.out), n, c.H);
-        }
+        default:
+            return launch2d(agg_fwd_element_kernel<N, DT>, narrow_grid(c.H, c.T), kNarrowBlock, c.stream,
+                            static_cast<const uint16_t*>(c.residual), c.pre, static_cast<uint16_t*>(c.out), c.T, c.H);
     }
 }
 
@@ -196,9 +215,15 @@ cudaError_t bwd_n(const BwdCall& c) {
     switch (c.path) {
         case kPathVec32: return bwd_vec32<N, DT>(c);
         case kPathVec16: return bwd_vec16<N, DT>(c);
+        case kPathPair: {
+            const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
+            return launch(agg_bwd_staged_kernel<N, DT, true>, blocks, kLanes, c.stream,
+                          static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.residual), c.pre,
+                          static_cast<uint16_t*>(c.gres), c.gpre, c.T, c.H);
+        }
         default: {
             const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
-            return launch(agg_bwd_element_kernel<N, DT>, blocks, kLanes, c.stream,
+            return launch(agg_bwd_staged_kernel<N, DT, false>, blocks, kLanes, c.stream,
                           static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.residual), c.pre,
                           static_cast<uint16_t*>(c.gres), c.gpre, c.T, c.H);
         }

@@ -81,6 +81,8 @@ def expected_bwd_path(H: int, offsets) -> int:
         return binding.MHC_PATH_VEC32
     if H % 8 == 0 and a >= 16:
         return binding.MHC_PATH_VEC16
+    if H % 2 == 0 and a >= 4:
+        return binding.MHC_PATH_PAIR
     return binding.MHC_PATH_ELEMENT
 
 

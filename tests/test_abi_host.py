@@ -93,8 +93,9 @@ def test_bwd_path_choice(lib):
     assert bpath(gr_off=16) == binding.MHC_PATH_VEC16
     assert bpath(H=4104) == binding.MHC_PATH_VEC16
     assert bpath(g_off=2) == binding.MHC_PATH_ELEMENT
-    assert bpath(gr_off=4) == binding.MHC_PATH_ELEMENT
-    assert bpath(H=2050) == binding.MHC_PATH_ELEMENT
+    assert bpath(gr_off=4) == binding.MHC_PATH_PAIR
+    assert bpath(H=2050) == binding.MHC_PATH_PAIR
+    assert bpath(H=2050, r_off=2) == binding.MHC_PATH_ELEMENT
     assert bpath(H=13) == binding.MHC_PATH_ELEMENT
     assert bpath(gp_off=2) == binding.MHC_PATH_NONE
     assert bpath(T=0) == binding.MHC_PATH_NONE
