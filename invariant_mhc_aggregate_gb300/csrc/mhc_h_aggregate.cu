@@ -132,7 +132,8 @@ mhc_status_t aggregate_bwd(const void* grad_out, const void* residual, const flo
     if (T == 0) return MHC_OK;
     const mhc_path_t path = bwd_path(grad_out, residual, pre, grad_residual, grad_pre, T, n, H);
     if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
-    if ((path == MHC_PATH_VEC32 || path == MHC_PATH_VEC16) && uint64_t(H) / 8 > 0xFFFFFFFFull)
+    // vector indices within a row are 32-bit (with headroom for the per-pass stride)
+    if ((path == MHC_PATH_VEC32 || path == MHC_PATH_VEC16) && uint64_t(H) / 8 > 0x7FFFFFFFull)
         return MHC_ERR_UNSUPPORTED;
     const mhc::BwdCall c{grad_out, residual, pre, grad_residual, grad_pre, uint64_t(T), uint64_t(H),
                          int(n), int(path), pre_vectorizable(pre, n), num_sms(),
