@@ -108,7 +108,7 @@ def measured_peaks():
 
 def stored_traffic(kernel: str, digest: str):
     """DRAM bytes per launch from an ncu capture (profiles/dram_traffic.txt),
-    only if it was taken on this exact library build."""
+    only if it was taken on these exact kernels (same kernel digest)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -220,7 +220,7 @@ def run_ours(args):
 
     _build.build()
     binding.load()
-    digest = _build.source_digest()
+    digest = _build.kernel_digest()
     T, H = args.T, args.H
     # Weak scaling: rank r owns tokens token_range(world*T, r, world) of a global
     # batch of world*T tokens and draws them with its own seed; no data moves
@@ -355,7 +355,8 @@ def run_ours(args):
         "roofline": roofline,
         "per_kernel": per_kernel,
         "wall_s_timed_region": round(wall, 3),
-        "library": {"so": os.path.relpath(_build.LIB_PATH, ROOT), "digest": digest[:16]},
+        "library": {"so": os.path.relpath(_build.LIB_PATH, ROOT),
+                    "digest": _build.source_digest()[:16], "kernel_digest": digest[:16]},
     }
     if clocks is not None:
         line["clocks"] = clocks

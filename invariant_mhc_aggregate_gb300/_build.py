@@ -57,8 +57,24 @@ def _digest(extra_flags) -> str:
 
 
 def source_digest() -> str:
-    """Hash of the library's sources and flags (identifies a kernel build)."""
+    """Hash of the library's sources and flags (identifies a library build)."""
     return _digest(())
+
+
+KERNEL_FILES = [os.path.join(CSRC, f) for f in
+                ("mhc_device.cuh", "fastdiv.cuh", "mhc_launch.cuh", "mhc_launch_bf16.cu",
+                 "mhc_launch_f16.cu")]
+
+
+def kernel_digest() -> str:
+    """Hash of what decides the kernels' memory traffic: the device code, the
+    launch shapes and the flags (not the host-side validation)."""
+    h = hashlib.sha256()
+    for p in KERNEL_FILES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(NVCC_FLAGS).encode())
+    return h.hexdigest()
 
 
 def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
