@@ -561,6 +561,24 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
             results.append(entry)
             del g, r, p, gr, gp
             torch.cuda.empty_cache()
+    # the narrow paths (H even but not a multiple of 8: 4-byte; H odd: 2-byte), steady state
+    for H in (7166, 7167):
+        T = 4096
+        g, r, p = backward_inputs(T, H, "normal", 4, device=dev)
+        sets = [(g, r, p), (g.clone(), r.clone(), p.clone())]
+        fsets = [(rr, pp, torch.empty((T, H), dtype=torch.bfloat16, device=dev)) for _, rr, pp in sets]
+        bsets = [(gg, rr, pp, torch.empty_like(rr), torch.empty_like(pp)) for gg, rr, pp in sets]
+        fpath = binding.PATH_NAMES[binding.mhc_h_aggregate_fwd_path(*fsets[0])]
+        bpath = binding.PATH_NAMES[binding.mhc_h_aggregate_bwd_path(*bsets[0])]
+        us_f = time_steady(lambda a, b, c: binding.mhc_h_aggregate_fwd(a, b, c), fsets)
+        us_b = time_steady(lambda a, b, c, d, e: binding.mhc_h_aggregate_bwd(a, b, c, d, e), bsets)
+        results.append({"workload": f"narrow_h{H}", "dir": "fwd", "T": T, "H": H, "path": fpath,
+                        "steady": {"us": us_f, "sets": 2, **entry_for(us_f, fwd_bytes(T, H))}})
+        results.append({"workload": f"narrow_h{H}", "dir": "bwd", "T": T, "H": H, "path": bpath,
+                        "steady": {"us": us_b, "sets": 2, **entry_for(us_b, bwd_bytes(T, H))}})
+        del g, r, p, sets, fsets, bsets
+        torch.cuda.empty_cache()
+
     # the general form (stream count n, FP16 storage), steady state only
     for n, dtype in ((8, torch.bfloat16), (2, torch.bfloat16), (4, torch.float16)):
         T, H = 4096, 7168
