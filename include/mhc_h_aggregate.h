@@ -74,6 +74,14 @@
 
 #include <stdint.h>
 
+/* The library is built with hidden symbol visibility; only the declarations
+ * below are exported. */
+#if defined(__GNUC__) || defined(__clang__)
+#define MHC_API __attribute__((visibility("default")))
+#else
+#define MHC_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -100,7 +108,7 @@ typedef enum mhc_path {
 } mhc_path_t;
 
 /* Version of this ABI; changes when a declaration here changes. */
-int32_t mhc_h_aggregate_abi_version(void);
+MHC_API int32_t mhc_h_aggregate_abi_version(void);
 
 /* Forward ("Add batch-invariant h_aggregate kernel", Summary and Batch
  * invariance).
@@ -108,7 +116,7 @@ int32_t mhc_h_aggregate_abi_version(void);
  *   pre       in   FP32 [T,4]
  *   out       out  BF16 [T,H]; every element is written exactly once.
  */
-mhc_status_t mhc_h_aggregate_fwd(const void* residual, const float* pre, void* out,
+MHC_API mhc_status_t mhc_h_aggregate_fwd(const void* residual, const float* pre, void* out,
                                  int64_t T, int64_t H, mhc_stream_t stream);
 
 /* Backward (same page, reviewer request; formula above): one fused pass.
@@ -118,16 +126,16 @@ mhc_status_t mhc_h_aggregate_fwd(const void* residual, const float* pre, void* o
  *   grad_residual  out  BF16 [T,4,H]
  *   grad_pre       out  FP32 [T,4]   ORDER-256 sums
  */
-mhc_status_t mhc_h_aggregate_bwd(const void* grad_out, const void* residual, const float* pre,
+MHC_API mhc_status_t mhc_h_aggregate_bwd(const void* grad_out, const void* residual, const float* pre,
                                  void* grad_residual, float* grad_pre,
                                  int64_t T, int64_t H, mhc_stream_t stream);
 
 /* The kernel path mhc_h_aggregate_fwd / _bwd would take for these arguments
  * (no launch, no CUDA call).  MHC_PATH_NONE when the call would be rejected or
  * when T == 0. */
-mhc_path_t mhc_h_aggregate_fwd_path(const void* residual, const float* pre, const void* out,
+MHC_API mhc_path_t mhc_h_aggregate_fwd_path(const void* residual, const float* pre, const void* out,
                                     int64_t T, int64_t H);
-mhc_path_t mhc_h_aggregate_bwd_path(const void* grad_out, const void* residual,
+MHC_API mhc_path_t mhc_h_aggregate_bwd_path(const void* grad_out, const void* residual,
                                     const float* pre, const void* grad_residual,
                                     const float* grad_pre, int64_t T, int64_t H);
 
@@ -146,7 +154,7 @@ typedef enum mhc_dtype {
  *   pre       in   FP32 [T,n]
  *   out       out  [T,H] dtype
  */
-mhc_status_t mhc_aggregate_fwd(const void* residual, const float* pre, void* out, int64_t T,
+MHC_API mhc_status_t mhc_aggregate_fwd(const void* residual, const float* pre, void* out, int64_t T,
                                int32_t n, int64_t H, mhc_dtype_t dtype, mhc_stream_t stream);
 
 /* General backward, same n and dtype rules; n = 4 with BF16 is exactly
@@ -157,24 +165,24 @@ mhc_status_t mhc_aggregate_fwd(const void* residual, const float* pre, void* out
  *   grad_residual  out  [T,n,H] dtype: cvt(fp32(pre[t,k] * g[t,h]))
  *   grad_pre       out  FP32 [T,n]: ORDER-256 sums of g * r[t,k]
  */
-mhc_status_t mhc_aggregate_bwd(const void* grad_out, const void* residual, const float* pre,
+MHC_API mhc_status_t mhc_aggregate_bwd(const void* grad_out, const void* residual, const float* pre,
                                void* grad_residual, float* grad_pre, int64_t T, int32_t n,
                                int64_t H, mhc_dtype_t dtype, mhc_stream_t stream);
 
 /* Kernel path of the general calls (no launch, no CUDA call); the storage type
  * does not change the path. */
-mhc_path_t mhc_aggregate_fwd_path(const void* residual, const float* pre, const void* out,
+MHC_API mhc_path_t mhc_aggregate_fwd_path(const void* residual, const float* pre, const void* out,
                                   int64_t T, int32_t n, int64_t H);
-mhc_path_t mhc_aggregate_bwd_path(const void* grad_out, const void* residual, const float* pre,
+MHC_API mhc_path_t mhc_aggregate_bwd_path(const void* grad_out, const void* residual, const float* pre,
                                   const void* grad_residual, const float* grad_pre, int64_t T,
                                   int32_t n, int64_t H);
 
 /* Static text for a status code. */
-const char* mhc_status_string(mhc_status_t status);
+MHC_API const char* mhc_status_string(mhc_status_t status);
 
 /* The cudaError_t value behind the last MHC_ERR_CUDA returned on the calling
  * thread; a call that launches successfully resets it to 0. */
-int32_t mhc_h_aggregate_last_cuda_error(void);
+MHC_API int32_t mhc_h_aggregate_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

@@ -36,7 +36,7 @@ NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
     "--fmad=false", "-ftz=false", "-prec-div=true", "-prec-sqrt=true",
-    "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
+    "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "-Xcompiler", "-fvisibility=hidden",
 ]
 
 
@@ -73,7 +73,16 @@ def kernel_digest() -> str:
     for p in KERNEL_FILES:
         with open(p, "rb") as f:
             h.update(f.read())
-    h.update(" ".join(NVCC_FLAGS).encode())
+    device_flags = []
+    skip = False
+    for flag in NVCC_FLAGS:            # host-compiler flags do not touch the kernels
+        if skip:
+            skip = False
+        elif flag == "-Xcompiler":
+            skip = True
+        else:
+            device_flags.append(flag)
+    h.update(" ".join(device_flags).encode())
     return h.hexdigest()
 
 

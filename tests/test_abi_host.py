@@ -22,7 +22,7 @@ def lib():
 def header_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(mhc_\w+)\s*\(", text, flags=re.M)
+    return re.findall(r"^\s*(?:MHC_API\s+)?(?:const\s+)?\w+\*?\s+\*?(mhc_\w+)\s*\(", text, flags=re.M)
 
 
 def test_header_declares_the_binding_exports():
@@ -40,6 +40,13 @@ def test_exported_symbols_are_c_linkage():
     names = {line.split()[-1] for line in out.splitlines() if line.strip()}
     for name in header_functions():
         assert name in names, f"{name} not exported with C linkage"
+
+
+def test_only_the_c_abi_is_exported():
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    names = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert names == set(header_functions()), sorted(names - set(header_functions()))[:10]
 
 
 def test_abi_version(lib):
