@@ -26,6 +26,15 @@ Parity status of each function (what pins it, from the oracle pin tests):
     storage; a reading beyond the pages): hand-worked tree-order cases for n = 2
     and 8, equality with fwd/bwd at n = 4 BF16, exact-rational emulation,
     integer-valued exact sums, one-hot invariants.
+  * exp32 / sigmoid32 (the fixed binary32 sequence that defines the sigmoid of
+    the fused pre coefficients): hand-worked values, exact-rational emulation of
+    every step, error bounds against FP64 e^x and sigmoid on a dense sample,
+    exact special values, symmetry and monotonicity.
+  * pre_sigmoid / aggregate_sigmoid_fwd / aggregate_sigmoid_bwd /
+    sigmoid_param_grad (the "perf: fuse mHC coefficient backward epilogue"
+    page's pre coefficients, a reading): FP64 bounds, exact special cases
+    (z = 0, integer-valued sums), hand-worked token-order cases and an
+    independent recursive builder of ORDER-256 over tokens.
 """
 
 from __future__ import annotations
@@ -133,6 +142,19 @@ class Oracle:
         lib.oracle_aggregate_fwd.restype = ctypes.c_int
         lib.oracle_aggregate_bwd.argtypes = [p, p, p, p, p, i64, i64, i64, ctypes.c_int]
         lib.oracle_aggregate_bwd.restype = ctypes.c_int
+        lib.oracle_exp32_array.argtypes = [p, p, i64]
+        lib.oracle_exp32_array.restype = None
+        lib.oracle_sigmoid32_array.argtypes = [p, p, p, i64]
+        lib.oracle_sigmoid32_array.restype = None
+        lib.oracle_pre_sigmoid.argtypes = [p, p, p, p, i64, i64]
+        lib.oracle_pre_sigmoid.restype = ctypes.c_int
+        lib.oracle_aggregate_sigmoid_fwd.argtypes = [p, p, p, p, p, i64, i64, i64, ctypes.c_int]
+        lib.oracle_aggregate_sigmoid_fwd.restype = ctypes.c_int
+        lib.oracle_aggregate_sigmoid_bwd.argtypes = [p, p, p, p, p, p, p, p, i64, i64, i64,
+                                                     ctypes.c_int]
+        lib.oracle_aggregate_sigmoid_bwd.restype = ctypes.c_int
+        lib.oracle_sigmoid_param_grad.argtypes = [p, p, p, p, i64, i64]
+        lib.oracle_sigmoid_param_grad.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -192,6 +214,84 @@ class Oracle:
                                          T, n, H, _DTYPES[dtype]) != 0:
             raise ValueError(f"unsupported n={n} or dtype={dtype}")
         return gr, gp
+
+    # -- the pre coefficients from the mix (sigmoid), fused into the aggregate --
+
+    def exp32(self, x) -> np.ndarray:
+        """The library's binary32 e^x (Cody-Waite reduction, degree-7 Taylor)."""
+        x = _as(x, np.float32)
+        y = np.empty(x.shape, dtype=np.float32)
+        self.lib.oracle_exp32_array(_ptr(x), _ptr(y), x.size)
+        return y
+
+    def sigmoid32(self, z) -> tuple[np.ndarray, np.ndarray]:
+        """(sigmoid(z), sigmoid'(z)) as defined by the binary32 sequence."""
+        z = _as(z, np.float32)
+        s = np.empty(z.shape, dtype=np.float32)
+        ds = np.empty(z.shape, dtype=np.float32)
+        self.lib.oracle_sigmoid32_array(_ptr(z), _ptr(s), _ptr(ds), z.size)
+        return s, ds
+
+    @staticmethod
+    def _coeffs(mix, alpha, b):
+        mix = _as(mix, np.float32)
+        alpha = _as(np.asarray(alpha, dtype=np.float32).reshape(1), np.float32)
+        b = _as(b, np.float32)
+        if mix.ndim != 2 or b.shape != (mix.shape[1],):
+            raise ValueError(f"mix must be [T,n] and b [n], got {mix.shape} and {b.shape}")
+        return mix, alpha, b
+
+    def pre_sigmoid(self, mix, alpha, b) -> np.ndarray:
+        """pre[t,k] = sigmoid(alpha * mix[t,k] + b[k]); float32 [T,n]."""
+        mix, alpha, b = self._coeffs(mix, alpha, b)
+        T, n = mix.shape
+        pre = np.empty((T, n), dtype=np.float32)
+        if self.lib.oracle_pre_sigmoid(_ptr(mix), _ptr(alpha), _ptr(b), _ptr(pre), T, n) != 0:
+            raise ValueError(f"unsupported n={n}")
+        return pre
+
+    def aggregate_sigmoid_fwd(self, residual, mix, alpha, b, dtype: str = "bf16") -> np.ndarray:
+        """out = aggregate(residual, sigmoid(alpha * mix + b)); uint16 [T,H]."""
+        residual = _as(residual, np.uint16)
+        mix, alpha, b = self._coeffs(mix, alpha, b)
+        T, n, H = residual.shape
+        if mix.shape != (T, n):
+            raise ValueError(f"mix must be [{T},{n}], got {mix.shape}")
+        out = np.empty((T, H), dtype=np.uint16)
+        if self.lib.oracle_aggregate_sigmoid_fwd(_ptr(residual), _ptr(mix), _ptr(alpha), _ptr(b),
+                                                 _ptr(out), T, n, H, _DTYPES[dtype]) != 0:
+            raise ValueError(f"unsupported n={n} or dtype={dtype}")
+        return out
+
+    def aggregate_sigmoid_bwd(self, g, residual, mix, alpha, b, dtype: str = "bf16"):
+        """(grad_residual uint16 [T,n,H], grad_z float32 [T,n], grad_mix float32 [T,n])."""
+        g = _as(g, np.uint16)
+        residual = _as(residual, np.uint16)
+        mix, alpha, b = self._coeffs(mix, alpha, b)
+        T, n, H = residual.shape
+        if g.shape != (T, H) or mix.shape != (T, n):
+            raise ValueError("shape mismatch between g, residual and mix")
+        gr = np.empty((T, n, H), dtype=np.uint16)
+        gz = np.empty((T, n), dtype=np.float32)
+        gm = np.empty((T, n), dtype=np.float32)
+        if self.lib.oracle_aggregate_sigmoid_bwd(_ptr(g), _ptr(residual), _ptr(mix), _ptr(alpha),
+                                                 _ptr(b), _ptr(gr), _ptr(gz), _ptr(gm), T, n, H,
+                                                 _DTYPES[dtype]) != 0:
+            raise ValueError(f"unsupported n={n} or dtype={dtype}")
+        return gr, gz, gm
+
+    def sigmoid_param_grad(self, grad_z, mix) -> tuple[np.ndarray, np.float32]:
+        """(grad_b float32 [n], grad_alpha float32): sums over tokens in ORDER-256."""
+        grad_z = _as(grad_z, np.float32)
+        mix = _as(mix, np.float32)
+        if grad_z.ndim != 2 or grad_z.shape != mix.shape:
+            raise ValueError("grad_z and mix must both be [T,n]")
+        T, n = grad_z.shape
+        gb = np.empty(n, dtype=np.float32)
+        ga = np.empty(1, dtype=np.float32)
+        if self.lib.oracle_sigmoid_param_grad(_ptr(grad_z), _ptr(mix), _ptr(gb), _ptr(ga), T, n) != 0:
+            raise ValueError(f"unsupported n={n}")
+        return gb, ga[0]
 
     def fwd(self, residual, pre) -> np.ndarray:
         """out[t,h] = bf16((pre0*r0 + pre1*r1) + (pre2*r2 + pre3*r3)); uint16 [T,H]."""
@@ -287,3 +387,19 @@ def aggregate_fwd(residual, pre, dtype="bf16"):
 
 def aggregate_bwd(g, residual, pre, dtype="bf16"):
     return default().aggregate_bwd(g, residual, pre, dtype)
+
+
+def pre_sigmoid(mix, alpha, b):
+    return default().pre_sigmoid(mix, alpha, b)
+
+
+def aggregate_sigmoid_fwd(residual, mix, alpha, b, dtype="bf16"):
+    return default().aggregate_sigmoid_fwd(residual, mix, alpha, b, dtype)
+
+
+def aggregate_sigmoid_bwd(g, residual, mix, alpha, b, dtype="bf16"):
+    return default().aggregate_sigmoid_bwd(g, residual, mix, alpha, b, dtype)
+
+
+def sigmoid_param_grad(grad_z, mix):
+    return default().sigmoid_param_grad(grad_z, mix)

@@ -43,6 +43,7 @@
  */
 #include <float.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #if !defined(FLT_EVAL_METHOD) || FLT_EVAL_METHOD != 0
@@ -381,4 +382,237 @@ int oracle_aggregate_bwd(const uint16_t* g, const uint16_t* residual, const floa
         }
     }
     return 0;
+}
+
+/* ----------------------------------------------------------------------- */
+/* The pre coefficients from the mix, fused into the aggregate               */
+/* ----------------------------------------------------------------------- */
+
+/* Source: "perf: fuse mHC coefficient backward epilogue" (Liger-Kernel pull
+ * request 1402), Summary: the coefficient backward ends in the derivatives of
+ * the pre / post sigmoids, grad_mix, and FP32 gradients of the bias b (24
+ * columns for HC = 4) and of three scalar alphas; Risks and Limitations: the
+ * grad_b / alpha reductions run in a fixed, deterministic order instead of
+ * eager PyTorch's.  The page prints no formula.  The reading used here, for
+ * the pre part only (the post and residual-mixing parts feed other stages):
+ *
+ *     z[t,k]   = alpha * mix[t,k] + b[k]        RN multiply, then RN add
+ *     pre[t,k] = sigmoid(z[t,k]) = 1 / (1 + e^(-z[t,k]))
+ *     out      = the aggregate of residual with that pre (as above)
+ *
+ * and its derivative, with grad_pre[t,k] the ORDER-256 value of the plain
+ * backward:
+ *
+ *     grad_z[t,k]   = grad_pre[t,k] * sigmoid'(z[t,k])
+ *     grad_mix[t,k] = alpha * grad_z[t,k]
+ *     grad_b[k]     = sum over t of grad_z[t,k]
+ *     grad_alpha    = sum over t of tree_n( grad_z[t,k] * mix[t,k] )
+ *
+ * (24 columns = n pre + n post + n*n residual-mixing columns at n = 4, one
+ * alpha per group, which is what the page's counts say).  The two sums over
+ * t use ORDER-256 with tokens in place of h (see oracle_sigmoid_param_grad).
+ *
+ * The page fixes no evaluation of the sigmoid.  To keep every result a fixed
+ * function of its inputs on any device, it is defined here as the sequence of
+ * binary32 RN operations below (exp32, then sigmoid32), which both this
+ * oracle and the CUDA library carry out step for step.
+ */
+
+/* Round to the nearest integer, ties to even (|y| < 2^30). */
+static float round_half_even(float y) {
+    int32_t n = (int32_t)y;                 /* toward zero; exact for |y| < 2^31 */
+    float frac = y - (float)n;              /* exact: the dropped fraction */
+    if (frac > 0.5f || (frac == 0.5f && (n & 1))) n += 1;
+    else if (frac < -0.5f || (frac == -0.5f && (n & 1))) n -= 1;
+    return (float)n;
+}
+
+/* 2^e as a binary32 value, for -126 <= e <= 127 (built from its fields). */
+static float pow2_f32(int32_t e) {
+    uint32_t u = (uint32_t)(e + 127) << 23;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* e^x in binary32, defined as this fixed sequence of RN operations:
+ *   1. Argument reduction of Cody and Waite (W. J. Cody and W. Waite,
+ *      "Software Manual for the Elementary Functions", 1980): x = k ln2 + r
+ *      with k = round_half_even(x * log2e) and r = (x - k*L1) - k*L2, where
+ *      L1 + L2 is ln 2 split so that L1 has 15 significant bits (k*L1 is then
+ *      exact for |k| < 2^9).
+ *   2. e^r by its Taylor polynomial of degree 7, sum of r^i / i!, evaluated by
+ *      Horner's rule from the highest term: q = c7; q = c_i + r*q for
+ *      i = 6 .. 0, with c_i = RN(1 / i!).
+ *   3. e^x = (q * 2^(k1)) * 2^(k - k1) with k1 = k / 2 rounded toward zero:
+ *      the first product is exact, the second rounds once (also into the
+ *      subnormal range).
+ * NaN gives NaN, x > 89 gives +inf and x < -104 gives +0 (the correctly
+ * rounded values there).  Error: within 1.2 ulp of e^x on [-104, 0]. */
+static const float EXP_LOG2E = 0x1.715476p+0f;     /* RN(log2 e) */
+static const float EXP_L1 = 0x1.62e4p-1f;          /* ln 2, high part (15 bits) */
+static const float EXP_L2 = 0x1.7f7d1cp-20f;       /* RN(ln 2 - L1) */
+
+float oracle_exp32(float x) {
+    if (x != x) return x;
+    if (x > 89.0f) {
+        uint32_t inf = 0x7F800000u;
+        float f;
+        memcpy(&f, &inf, sizeof f);
+        return f;
+    }
+    if (x < -104.0f) return 0.0f;
+    float k = round_half_even(x * EXP_LOG2E);
+    float hi = k * EXP_L1;
+    float lo = k * EXP_L2;
+    float r = (x - hi) - lo;
+    const float c[8] = {1.0f, 1.0f, 1.0f / 2.0f, 1.0f / 6.0f, 1.0f / 24.0f, 1.0f / 120.0f,
+                        1.0f / 720.0f, 1.0f / 5040.0f};
+    float q = c[7];
+    for (int i = 6; i >= 0; --i) q = c[i] + r * q;
+    int32_t ki = (int32_t)k;
+    int32_t k1 = ki / 2;
+    float partial = q * pow2_f32(k1);
+    return partial * pow2_f32(ki - k1);
+}
+
+/* sigmoid(z) and 1 - sigmoid(z), both from e = e^(-|z|) in (0, 1]:
+ *   d = 1 + e;  for z >= 0: sigmoid = 1/d, 1 - sigmoid = e/d;
+ *               for z <  0: sigmoid = e/d, 1 - sigmoid = 1/d.
+ * No term overflows, the small one of the two is never formed by
+ * cancellation, and sigmoid(-z) is bit for bit 1 - sigmoid(z) as computed
+ * here.  sigmoid'(z) = sigmoid * (1 - sigmoid), one RN product. */
+static void sigmoid32(float z, float* s, float* one_minus_s) {
+    float a = (z < 0.0f) ? -z : z;
+    float e = oracle_exp32(-a);
+    float d = 1.0f + e;
+    float big = 1.0f / d;
+    float small = e / d;
+    if (z >= 0.0f) {
+        *s = big;
+        *one_minus_s = small;
+    } else {
+        *s = small;
+        *one_minus_s = big;
+    }
+}
+
+float oracle_sigmoid32(float z) {
+    float s, t;
+    sigmoid32(z, &s, &t);
+    return s;
+}
+
+float oracle_sigmoid32_grad(float z) {
+    float s, t;
+    sigmoid32(z, &s, &t);
+    return s * t;
+}
+
+static float pre_activation(float alpha, float mix, float b) {
+    float scaled = alpha * mix;
+    return scaled + b;
+}
+
+/* pre[t,k] = sigmoid(alpha * mix[t,k] + b[k]); mix and pre are [T,n], b is
+ * [n], alpha one value.  Returns 0, or -1 for an unsupported n. */
+int oracle_pre_sigmoid(const float* mix, const float* alpha, const float* b, float* pre,
+                       int64_t T, int64_t n) {
+    if (!valid_streams(n)) return -1;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t k = 0; k < n; ++k)
+            pre[t * n + k] = oracle_sigmoid32(pre_activation(alpha[0], mix[t * n + k], b[k]));
+    return 0;
+}
+
+/* out = aggregate(residual, sigmoid(alpha * mix + b)). */
+int oracle_aggregate_sigmoid_fwd(const uint16_t* residual, const float* mix, const float* alpha,
+                                 const float* b, uint16_t* out, int64_t T, int64_t n, int64_t H,
+                                 int dtype) {
+    if (!valid_streams(n) || (dtype != 0 && dtype != 1)) return -1;
+    float* pre = (float*)malloc(sizeof(float) * (size_t)(T * n + 1));
+    if (!pre) return -2;
+    oracle_pre_sigmoid(mix, alpha, b, pre, T, n);
+    int rc = oracle_aggregate_fwd(residual, pre, out, T, n, H, dtype);
+    free(pre);
+    return rc;
+}
+
+/* grad_residual as in oracle_aggregate_bwd with pre = sigmoid(z), and
+ * grad_z[t,k] = grad_pre[t,k] * sigmoid'(z[t,k]), grad_mix = alpha * grad_z. */
+int oracle_aggregate_sigmoid_bwd(const uint16_t* g, const uint16_t* residual, const float* mix,
+                                 const float* alpha, const float* b, uint16_t* grad_residual,
+                                 float* grad_z, float* grad_mix, int64_t T, int64_t n, int64_t H,
+                                 int dtype) {
+    if (!valid_streams(n) || (dtype != 0 && dtype != 1)) return -1;
+    float* pre = (float*)malloc(sizeof(float) * (size_t)(T * n + 1));
+    float* grad_pre = (float*)malloc(sizeof(float) * (size_t)(T * n + 1));
+    if (!pre || !grad_pre) {
+        free(pre);
+        free(grad_pre);
+        return -2;
+    }
+    oracle_pre_sigmoid(mix, alpha, b, pre, T, n);
+    int rc = oracle_aggregate_bwd(g, residual, pre, grad_residual, grad_pre, T, n, H, dtype);
+    for (int64_t i = 0; rc == 0 && i < T * n; ++i) {
+        float z = pre_activation(alpha[0], mix[i], b[i % n]);
+        grad_z[i] = grad_pre[i] * oracle_sigmoid32_grad(z);
+        grad_mix[i] = alpha[0] * grad_z[i];
+    }
+    free(pre);
+    free(grad_pre);
+    return rc;
+}
+
+/* Sum of x_0 .. x_(T-1) (x_t = x[t * stride]) in ORDER-256 with tokens in
+ * place of h: chunks of 8 consecutive tokens (+0 past T) summed by the chunk
+ * tree, lane j adding the partials of chunks j, j + 256, ... in increasing
+ * order from +0, then the group and cross-group trees. */
+static float order256_over_tokens(const float* x, int64_t stride, int64_t T) {
+    float acc[ORDER_LANES];
+    for (int j = 0; j < ORDER_LANES; ++j) acc[j] = 0.0f;
+    int64_t chunks = (T + ORDER_CHUNK - 1) / ORDER_CHUNK;
+    for (int64_t chunk = 0; chunk < chunks; ++chunk) {
+        float v[ORDER_CHUNK];
+        for (int e = 0; e < ORDER_CHUNK; ++e) {
+            int64_t t = chunk * ORDER_CHUNK + e;
+            v[e] = (t < T) ? x[t * stride] : 0.0f;
+        }
+        int lane = (int)(chunk % ORDER_LANES);
+        acc[lane] = acc[lane] + chunk_partial(v);
+    }
+    float w[ORDER_GROUPS];
+    for (int grp = 0; grp < ORDER_GROUPS; ++grp) w[grp] = group_tree(acc + grp * ORDER_GROUP);
+    return groups_tree(w);
+}
+
+/* grad_b[k] = sum_t grad_z[t,k] and grad_alpha[0] = sum_t tree_n(grad_z[t,k] *
+ * mix[t,k]), both over tokens in ORDER-256.  Returns 0, -1 for an unsupported
+ * n, -2 when out of memory. */
+int oracle_sigmoid_param_grad(const float* grad_z, const float* mix, float* grad_b,
+                              float* grad_alpha, int64_t T, int64_t n) {
+    if (!valid_streams(n)) return -1;
+    for (int64_t k = 0; k < n; ++k) grad_b[k] = order256_over_tokens(grad_z + k, n, T);
+    float* per_token = (float*)malloc(sizeof(float) * (size_t)(T + 1));
+    if (!per_token) return -2;
+    for (int64_t t = 0; t < T; ++t) {
+        float p[8];
+        for (int64_t k = 0; k < n; ++k) p[k] = grad_z[t * n + k] * mix[t * n + k];
+        per_token[t] = pairwise_tree(p, (int)n);
+    }
+    grad_alpha[0] = order256_over_tokens(per_token, 1, T);
+    free(per_token);
+    return 0;
+}
+
+void oracle_exp32_array(const float* x, float* y, int64_t count) {
+    for (int64_t i = 0; i < count; ++i) y[i] = oracle_exp32(x[i]);
+}
+
+/* s[i] = sigmoid(z[i]), ds[i] = sigmoid'(z[i]). */
+void oracle_sigmoid32_array(const float* z, float* s, float* ds, int64_t count) {
+    for (int64_t i = 0; i < count; ++i) {
+        s[i] = oracle_sigmoid32(z[i]);
+        ds[i] = oracle_sigmoid32_grad(z[i]);
+    }
 }

@@ -668,3 +668,346 @@ ALL_CHECKS += [
     check_agg_grad_pre_integer_exact,
     check_agg_grad_pre_order_f16,
 ]
+
+
+# --------------------------------------------------------------------------
+# the fused pre coefficients: pre = sigmoid(alpha * mix + b)
+#
+# Source: "perf: fuse mHC coefficient backward epilogue" (Liger-Kernel pull
+# request 1402), Summary (pre / post sigmoid derivatives, grad_mix, grad_b and
+# alpha gradients) and Risks and Limitations (deterministic order of the
+# grad_b / alpha reductions).  The formulas are a reading; the binary32
+# sigmoid is a definition of this library (exp32, sigmoid32 in the oracle).
+# --------------------------------------------------------------------------
+
+def f32_ulp(x) -> np.ndarray:
+    """Spacing of binary32 at |x| (x given in FP64), never below the subnormal step."""
+    a = np.abs(np.asarray(x, dtype=np.float64)).astype(np.float32)
+    return np.maximum(np.spacing(a).astype(np.float64), 2.0 ** -149)
+
+
+def dense_floats(lo_bits: int, hi_bits: int, step: int) -> np.ndarray:
+    """Every step-th binary32 pattern in [lo_bits, hi_bits)."""
+    return np.arange(lo_bits, hi_bits, step, dtype=np.uint64).astype(np.uint32).view(np.float32)
+
+
+def sigmoid64(z) -> np.ndarray:
+    """sigmoid in FP64 without overflow (accurate to a few FP64 ulps)."""
+    z = np.asarray(z, dtype=np.float64)
+    e = np.exp(-np.abs(z))
+    return np.where(z >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def check_exp32_fp64_bound(o):
+    """exp32 against FP64 e^x: within 1.2 binary32 ulps on [-104, 88.7] and
+    correctly rounded on at least 99% of a dense sample (a dropped term, a
+    one-part ln 2 or a wrong reduction breaks one of the two)."""
+    neg = dense_floats(0x80000000, 0xC2D00000, 997)            # -0 .. -104
+    pos = dense_floats(0x00000000, 0x42B17000, 1009)           # 0 .. 88.72
+    edges = np.float32([-0.0, 0.0, -104.0, -87.33655, -0.34657359, -0.34657362,
+                        -0.6931472, 0.6931472, 88.7, 88.72])
+    x = np.concatenate([neg, pos, edges])
+    y = o.exp32(x).astype(np.float64)
+    ex = np.exp(x.astype(np.float64))
+    err = np.abs(y - ex) / f32_ulp(ex)
+    assert err.max() <= 1.2, f"max error {err.max():.3f} ulp at x={x[err.argmax()]}"
+    exact = (y == ex.astype(np.float32).astype(np.float64)).mean()
+    assert exact >= 0.99, f"only {exact:.4f} correctly rounded"
+
+
+def _exp32_exact(x: float) -> float:
+    """The defining step sequence of exp32, each binary32 operation done in
+    exact rationals and rounded once (round_rne); x finite in [-104, 89]."""
+    f32 = lambda v: round_rne(Fraction(v), 24)
+    mul = lambda a, b: f32(Fraction(a) * Fraction(b))
+    add = lambda a, b: f32(Fraction(a) + Fraction(b))
+    log2e, l1, l2 = (float(f32_from_bits(u)) for u in (0x3FB8AA3B, 0x3F317200, 0x35BFBE8E))
+    y = Fraction(mul(x, log2e))
+    k = math.floor(y)
+    if y - k > Fraction(1, 2) or (y - k == Fraction(1, 2) and k % 2 == 1):
+        k += 1
+    r = add(add(x, -mul(k, l1)), -mul(k, l2))
+    c = [f32(Fraction(1, math.factorial(i))) for i in range(8)]
+    q = c[7]
+    for i in range(6, -1, -1):
+        q = add(c[i], mul(r, q))
+    k1 = int(k / 2)
+    return f32(Fraction(f32(Fraction(q) * Fraction(2) ** k1)) * Fraction(2) ** (k - k1))
+
+
+def check_exp32_exact_rational(o):
+    """exp32 equals its step sequence done in exact rationals, including inputs
+    where x * log2e rounds to exactly half an integer (the reduction's tie,
+    broken to even) and results deep in the subnormal range."""
+    log2e = f32_from_bits(0x3FB8AA3B)
+    halves = np.arange(-149.5, 128.0, 1.0)
+    x0 = (halves / np.float64(log2e)).astype(np.float32)
+    cand = x0.view(np.int32)[:, None] + np.arange(-4, 5, dtype=np.int32)[None, :]
+    cand = cand.astype(np.int32).view(np.float32)
+    hit = (cand * log2e).astype(np.float32) == halves.astype(np.float32)[:, None]
+    ties = cand[hit & (cand >= -104) & (cand <= 88.5)]
+    assert ties.size > 100, f"only {ties.size} tie inputs found"
+    rng = np.random.default_rng(90)
+    xs = np.concatenate([np.float32(ties), np.float32([-103.9, -100.0, -88.0, -0.75, 3.0, 88.5]),
+                         rng.uniform(-104, 88, 100).astype(np.float32)])
+    got = o.exp32(xs)
+    for x, g in zip(xs, got):
+        assert float(g) == _exp32_exact(float(x)), f"x={x!r}: {g!r} vs {_exp32_exact(float(x))!r}"
+
+
+def check_exp32_special(o):
+    x = np.float32([0.0, -0.0, np.inf, -np.inf, np.nan, -104.5, 89.5, 1e30, -1e30])
+    y = o.exp32(x)
+    assert f32_bits(y[:2]).tolist() == [0x3F800000, 0x3F800000]
+    assert y[2] == np.inf and f32_bits(y[3]) == 0 and np.isnan(y[4])
+    assert f32_bits(y[5]) == 0 and y[6] == np.inf and y[7] == np.inf and f32_bits(y[8]) == 0
+
+
+def check_sigmoid_golden(o):
+    rows = list(golden_rows("sigmoid_worked_examples.txt"))
+    z = np.array([f32_from_bits(int(r[1], 16)) for r in rows], dtype=np.float32)
+    s, ds = o.sigmoid32(z)
+    for (name, _, ws, wd), a, b in zip(rows, f32_bits(s), f32_bits(ds)):
+        assert (int(a), int(b)) == (int(ws, 16), int(wd, 16)), f"{name}: {hex(a)} {hex(b)}"
+
+
+def check_sigmoid_fp64_bound(o):
+    """sigmoid within 2.5 ulps and sigmoid' within 4.5 ulps of FP64, for both
+    signs of z on a dense sample of [-128, 128]."""
+    zp = dense_floats(0x00000000, 0x43000000, 1013)
+    z = np.concatenate([zp, -zp])
+    s, ds = o.sigmoid32(z)
+    S = sigmoid64(z)
+    D = S * sigmoid64(-z.astype(np.float64))
+    es = np.abs(s.astype(np.float64) - S) / f32_ulp(S)
+    ed = np.abs(ds.astype(np.float64) - D) / f32_ulp(D)
+    assert es.max() <= 2.5, f"sigmoid {es.max():.3f} ulp at z={z[es.argmax()]}"
+    assert ed.max() <= 4.5, f"sigmoid' {ed.max():.3f} ulp at z={z[ed.argmax()]}"
+
+
+def check_sigmoid_invariants(o):
+    """sigmoid(z) + sigmoid(-z) is 1 within 2^-23 (the rounding of d = 1 + e
+    moves (1 + e)/d off 1 by at most 2^-24, the two quotients add at most
+    3 * 2^-26), sigmoid' is even (bit for bit), sigmoid is non-decreasing in z
+    and lies in [0, 1]."""
+    rng = np.random.default_rng(91)
+    z = np.sort(np.concatenate([rng.standard_normal(20000).astype(np.float32) * np.float32(8.0),
+                                dense_floats(0x3F000000, 0x41A00000, 40009)]))
+    s, ds = o.sigmoid32(z)
+    sn, dsn = o.sigmoid32(-z)
+    assert np.all(np.abs(s.astype(np.float64) + sn.astype(np.float64) - 1.0) <= 2.0 ** -23)
+    assert np.array_equal(f32_bits(ds), f32_bits(dsn))
+    assert np.all(np.diff(s.astype(np.float64)) >= 0.0)
+    assert np.all((s >= 0.0) & (s <= 1.0))
+
+
+def _coeff_inputs(rng, T, n):
+    mix = (rng.standard_normal((T, n)) * 2.0).astype(np.float32)
+    alpha = np.float32(rng.uniform(0.2, 3.0))
+    b = rng.standard_normal(n).astype(np.float32)
+    return mix, alpha, b
+
+
+def check_pre_sigmoid_wiring(o):
+    """pre = sigmoid(RN(RN(alpha*mix) + b[k])) with the [T,n] layout (the
+    pre-activation by numpy binary32 arithmetic), and within the FP64 bound of
+    the exact sigmoid(alpha*mix + b)."""
+    rng = np.random.default_rng(92)
+    for n in (1, 2, 4, 8):
+        T = 37
+        mix, alpha, b = _coeff_inputs(rng, T, n)
+        z = (alpha * mix).astype(np.float32) + b[None, :]
+        want, _ = o.sigmoid32(z.astype(np.float32))
+        got = o.pre_sigmoid(mix, alpha, b)
+        assert np.array_equal(f32_bits(got), f32_bits(want)), n
+        z64 = np.float64(alpha) * mix.astype(np.float64) + b.astype(np.float64)[None, :]
+        S = sigmoid64(z64)
+        dz = 2.02 * U * (np.abs(np.float64(alpha) * mix) + np.abs(b.astype(np.float64))[None, :])
+        bound = 2.5 * f32_ulp(S) + S * (1.0 - S) * dz * 1.01
+        assert np.all(np.abs(got.astype(np.float64) - S) <= bound), n
+
+
+def check_agg_sigmoid_fwd_half(o):
+    """mix = 0 and b = 0 give z = 0 and pre = 0.5 exactly, so the fused forward
+    is the aggregate with pre = 0.5, emulated in exact rationals."""
+    rng = np.random.default_rng(93)
+    for dtype in ("bf16", "f16"):
+        for n in (1, 2, 4, 8):
+            T, H = 3, 19
+            r = random_storage(rng, (T, n, H), dtype, scale=2.0)
+            got = o.aggregate_sigmoid_fwd(r, np.zeros((T, n), np.float32), np.float32(1.7),
+                                          np.zeros(n, np.float32), dtype)
+            want = _agg_exact(r, np.full((T, n), 0.5, dtype=np.float32), dtype)
+            assert np.array_equal(got, want), (dtype, n)
+
+
+def check_agg_sigmoid_fwd_composition(o):
+    rng = np.random.default_rng(94)
+    for dtype, n, T, H in (("bf16", 4, 5, 33), ("f16", 8, 3, 17), ("bf16", 1, 4, 9)):
+        r = random_storage(rng, (T, n, H), dtype)
+        mix, alpha, b = _coeff_inputs(rng, T, n)
+        got = o.aggregate_sigmoid_fwd(r, mix, alpha, b, dtype)
+        assert np.array_equal(got, o.aggregate_fwd(r, o.pre_sigmoid(mix, alpha, b), dtype))
+
+
+def check_agg_sigmoid_bwd_half(o):
+    """z = 0: sigmoid' = 1/4 exactly, so with integer-valued g and r, grad_z is
+    the exact integer sum / 4, grad_mix = RN(alpha * grad_z), and
+    grad_residual = g / 2 exactly."""
+    rng = np.random.default_rng(95)
+    lut = np.array([bf16_bits_of(float(v)) for v in range(-8, 9)], dtype=np.uint16)
+    half = np.array([bf16_bits_of(v / 2.0) for v in range(-8, 9)], dtype=np.uint16)
+    for n in (1, 2, 4, 8):
+        T, H = 3, 2053
+        gi = rng.integers(-8, 9, size=(T, H))
+        ri = rng.integers(-8, 9, size=(T, n, H))
+        alpha = np.float32(1.3)
+        gr, gz, gm = o.aggregate_sigmoid_bwd(lut[gi + 8], lut[ri + 8], np.zeros((T, n), np.float32),
+                                             alpha, np.zeros(n, np.float32))
+        exact = np.einsum("th,tkh->tk", gi, ri).astype(np.float64) / 4.0
+        assert np.array_equal(gz.astype(np.float64), exact), n
+        assert np.array_equal(f32_bits(gm), f32_bits(alpha * exact.astype(np.float32))), n
+        assert np.array_equal(gr, np.broadcast_to(half[gi + 8][:, None, :], (T, n, H))), n
+
+
+def check_agg_sigmoid_bwd_composition(o):
+    """grad_residual and grad_pre are the plain backward's at pre = sigmoid(z);
+    grad_z = RN(grad_pre * sigmoid'(z)); grad_mix = RN(alpha * grad_z)."""
+    rng = np.random.default_rng(96)
+    for dtype, n, T, H in (("bf16", 4, 4, 40), ("f16", 2, 3, 21), ("bf16", 8, 2, 16)):
+        g = random_storage(rng, (T, H), dtype)
+        r = random_storage(rng, (T, n, H), dtype)
+        mix, alpha, b = _coeff_inputs(rng, T, n)
+        gr, gz, gm = o.aggregate_sigmoid_bwd(g, r, mix, alpha, b, dtype)
+        pre = o.pre_sigmoid(mix, alpha, b)
+        gr2, gp = o.aggregate_bwd(g, r, pre, dtype)
+        z = (alpha * mix).astype(np.float32) + b[None, :]
+        _, ds = o.sigmoid32(z.astype(np.float32))
+        assert np.array_equal(gr, gr2)
+        assert np.array_equal(f32_bits(gz), f32_bits(gp * ds))
+        assert np.array_equal(f32_bits(gm), f32_bits(alpha * gz))
+
+
+def order256_reference(x) -> np.float32:
+    """ORDER-256 over a sequence, written as an explicit expression tree and
+    evaluated recursively in numpy binary32: chunk = adjacent-pair tree over 8
+    values (+0 past the end), lane j = +0 then its chunks j, j+256, ... in
+    increasing order, each group of 32 lanes and then the 8 groups folded by
+    halving (element i with element i + half)."""
+    x = np.asarray(x, dtype=np.float32)
+    n_chunks = -(-len(x) // 8)
+
+    def leaf(i):
+        return x[i] if i < len(x) else np.float32(0.0)
+
+    def adjacent_pairs(nodes):
+        if len(nodes) == 1:
+            return nodes[0]
+        return adjacent_pairs([nodes[2 * i] + nodes[2 * i + 1] for i in range(len(nodes) // 2)])
+
+    def halving(nodes):
+        if len(nodes) == 1:
+            return nodes[0]
+        h = len(nodes) // 2
+        return halving([nodes[i] + nodes[i + h] for i in range(h)])
+
+    def lane(j, c):
+        # value of lane j after all of its chunks below c
+        if c < 0:
+            return np.float32(0.0)
+        return lane(j, c - 256) + adjacent_pairs([leaf(8 * c + e) for e in range(8)])
+
+    def lane_value(j):
+        last = j + 256 * ((n_chunks - 1 - j) // 256) if j < n_chunks else -1
+        return lane(j, last)
+
+    groups = [halving([lane_value(32 * w + i) for i in range(32)]) for w in range(8)]
+    return halving(groups)
+
+
+def check_param_grad_recursive_builder(o):
+    """grad_b and grad_alpha equal the recursive ORDER-256 builder over tokens,
+    bit for bit, on random data (T from 1 to past 2048 tokens, so that lanes
+    hold several chunks and the last chunk is ragged)."""
+    rng = np.random.default_rng(97)
+    for T in (1, 5, 8, 13, 300, 2049, 2100):
+        for n in (1, 4):
+            gz = rng.standard_normal((T, n)).astype(np.float32)
+            mix = rng.standard_normal((T, n)).astype(np.float32)
+            gb, ga = o.sigmoid_param_grad(gz, mix)
+            for k in range(n):
+                assert f32_bits(gb[k]) == f32_bits(order256_reference(gz[:, k])), (T, n, k)
+            prod = gz * mix
+            per_token = prod[:, 0] if n == 1 else (prod[:, 0] + prod[:, 1]) + (prod[:, 2] + prod[:, 3])
+            assert f32_bits(ga) == f32_bits(order256_reference(per_token)), (T, n)
+
+
+def check_param_grad_integer_exact(o):
+    rng = np.random.default_rng(98)
+    for T in (1, 7, 8, 9, 2047, 2048, 2049, 4104):
+        for n in (1, 2, 4, 8):
+            gzi = rng.integers(-8, 9, size=(T, n))
+            mi = rng.integers(-8, 9, size=(T, n))
+            gb, ga = o.sigmoid_param_grad(gzi.astype(np.float32), mi.astype(np.float32))
+            assert np.array_equal(gb.astype(np.float64), gzi.sum(axis=0).astype(np.float64)), (T, n)
+            assert float(ga) == float((gzi * mi).sum()), (T, n)
+
+
+def check_param_grad_order_golden(o):
+    """The ORDER-256 golden cases with tokens in place of h: the listed values
+    sit in column k of grad_z (mix = 1) and must give the listed grad_b[k]; at
+    n = 1 the same cases give grad_alpha."""
+    vals_of = {0x3F80: 1.0, 0x3380: 2.0 ** -24, 0x8000: -0.0}
+    for name, H, k, _carrier, positions, expected in golden_rows("grad_pre_order_cases.txt"):
+        T, k = int(H), int(k)
+        col = np.zeros(T, dtype=np.float32)
+        for item in positions.split(","):
+            pos, v = item.split(":")
+            if pos == "*":
+                col[:] = vals_of[int(v, 16)]
+            else:
+                col[int(pos)] = vals_of[int(v, 16)]
+        gz = np.zeros((T, 4), dtype=np.float32)
+        gz[:, k] = col
+        gb, _ = o.sigmoid_param_grad(gz, np.ones((T, 4), dtype=np.float32))
+        want = np.zeros(4, dtype=np.uint32)
+        want[k] = int(expected, 16)
+        assert np.array_equal(f32_bits(gb), want), name
+        _, ga = o.sigmoid_param_grad(col[:, None].copy(), np.ones((T, 1), dtype=np.float32))
+        assert int(f32_bits(ga)) == int(expected, 16), name
+
+
+def check_param_grad_fp64_bound(o):
+    rng = np.random.default_rng(99)
+    for T in (3, 1000, 4096):
+        n = 4
+        gz = rng.standard_normal((T, n)).astype(np.float32)
+        mix = rng.standard_normal((T, n)).astype(np.float32)
+        gb, ga = o.sigmoid_param_grad(gz, mix)
+        g64 = gz.astype(np.float64)
+        depth = order256_depth(T)
+        for k in range(n):
+            exact = math.fsum(g64[:, k])
+            assert abs(float(gb[k]) - exact) <= 1.01 * depth * U * np.abs(g64[:, k]).sum(), (T, k)
+        prod = g64 * mix.astype(np.float64)
+        exact = math.fsum(prod.ravel())
+        assert abs(float(ga) - exact) <= 1.01 * (depth + 3) * U * np.abs(prod).sum(), T
+
+
+ALL_CHECKS += [
+    check_exp32_fp64_bound,
+    check_exp32_exact_rational,
+    check_exp32_special,
+    check_sigmoid_golden,
+    check_sigmoid_fp64_bound,
+    check_sigmoid_invariants,
+    check_pre_sigmoid_wiring,
+    check_agg_sigmoid_fwd_half,
+    check_agg_sigmoid_fwd_composition,
+    check_agg_sigmoid_bwd_half,
+    check_agg_sigmoid_bwd_composition,
+    check_param_grad_recursive_builder,
+    check_param_grad_integer_exact,
+    check_param_grad_order_golden,
+    check_param_grad_fp64_bound,
+]

@@ -102,6 +102,32 @@ MUTANTS = {
                            "    }\n    for (int i = 1; i < n; ++i) p[0] = p[0] + p[i];\n    return p[0];"),
     "hc_tree_stride_pairs": ("p[i] = p[2 * i] + p[2 * i + 1];", "p[i] = p[i] + p[i + width / 2];"),
     "hc_wrong_pre_stride": ("p[k] = pre[t * n + k] * widen(", "p[k] = pre[t * 4 + (k & 3)] * widen("),
+    # the fused pre coefficients (sigmoid of alpha * mix + b)
+    "exp_one_part_ln2": ("float r = (x - hi) - lo;", "float r = x - hi;"),
+    "exp_k_truncated": ("float k = round_half_even(x * EXP_LOG2E);",
+                        "float k = (float)(int32_t)(x * EXP_LOG2E);"),
+    "exp_ties_away": ("(frac == 0.5f && (n & 1))", "(frac == 0.5f)"),
+    "exp_negative_ties_away": ("(frac == -0.5f && (n & 1))", "(frac == -0.5f)"),
+    "exp_dropped_taylor_term": ("float q = c[7];", "float q = 0.0f;"),
+    "exp_wrong_coefficient": ("1.0f / 6.0f", "1.0f / 5.0f"),
+    "exp_unsplit_scale": ("int32_t k1 = ki / 2;", "int32_t k1 = ki;"),
+    "exp_overflow_guard_early": ("    if (x > 89.0f) {", "    if (x > 88.0f) {"),
+    "exp_underflow_guard_early": ("if (x < -104.0f) return 0.0f;", "if (x < -87.0f) return 0.0f;"),
+    "sigmoid_branch_swapped": ("    if (z >= 0.0f) {\n        *s = big;", "    if (z < 0.0f) {\n        *s = big;"),
+    "sigmoid_grad_by_cancellation": ("    return s * t;", "    return s * (1.0f - s);"),
+    "sigmoid_one_formula": ("    float a = (z < 0.0f) ? -z : z;", "    float a = z;"),
+    "preact_fma": ("    return scaled + b;", "    return __builtin_fmaf(alpha, mix, b) + 0.0f * scaled;"),
+    "preact_bias_first_column": ("pre_activation(alpha[0], mix[t * n + k], b[k])",
+                                 "pre_activation(alpha[0], mix[t * n + k], b[0])"),
+    "bwd_grad_z_uses_sigmoid": ("grad_pre[i] * oracle_sigmoid32_grad(z)", "grad_pre[i] * oracle_sigmoid32(z)"),
+    "bwd_grad_mix_unscaled": ("grad_mix[i] = alpha[0] * grad_z[i];", "grad_mix[i] = grad_z[i];"),
+    "bwd_bias_index": ("pre_activation(alpha[0], mix[i], b[i % n])", "pre_activation(alpha[0], mix[i], b[i / n % n])"),
+    "param_alpha_without_mix": ("p[k] = grad_z[t * n + k] * mix[t * n + k];", "p[k] = grad_z[t * n + k];"),
+    "param_tokens_descending": ("for (int64_t chunk = 0; chunk < chunks; ++chunk) {",
+                                "for (int64_t chunk = chunks - 1; chunk >= 0; --chunk) {"),
+    "param_drop_ragged_tail": ("int64_t chunks = (T + ORDER_CHUNK - 1) / ORDER_CHUNK;",
+                               "int64_t chunks = T / ORDER_CHUNK;"),
+    "param_lanes_128": ("int lane = (int)(chunk % ORDER_LANES);", "int lane = (int)(chunk % 128);"),
     "hc_grad_pre_wrong_row": ("grad_pre_row(g + t * H, residual + (t * n + k) * H, H, dtype)",
                               "grad_pre_row(g + t * H, residual + (t * n + (k ^ 1)) * H, H, dtype)"),
 }
