@@ -598,6 +598,37 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
                         "steady": {"us": us_b, "sets": len(sets), **entry_for(us_b, bb)}})
         del g, r, p, sets, fsets, bsets
         torch.cuda.empty_cache()
+
+    # pre computed in the kernels from the mix (sigmoid of alpha * mix + b), n = 4 BF16,
+    # steady state; and the reduction of grad_b / grad_alpha over the tokens
+    from invariant_mhc_aggregate_gb300.inputs import coeff_inputs
+    T, H = 4096, 7168
+    g, r, _ = backward_inputs(T, H, "normal", 4, device=dev)
+    mix, alpha, b = coeff_inputs(T, 4, "normal", 5, device=dev)
+    fb = T * (10 * H + 16)
+    bb = T * (18 * H + 48)
+    ns = n_sets(fb) or 2
+    sets = [(g, r, mix)] + [(g.clone(), r.clone(), mix.clone()) for _ in range(ns - 1)]
+    fsets = [(rr, mm, alpha, b, torch.empty((T, H), dtype=torch.bfloat16, device=dev))
+             for _, rr, mm in sets]
+    us_f = time_steady(lambda *a: binding.mhc_aggregate_sigmoid_fwd(*a), fsets)
+    bsets = [(gg, rr, mm, alpha, b, torch.empty_like(rr), torch.empty_like(mm), torch.empty_like(mm))
+             for gg, rr, mm in sets]
+    us_b = time_steady(lambda *a: binding.mhc_aggregate_sigmoid_bwd(*a), bsets)
+    psets = [(bs[6], bs[2], torch.empty(4, device=dev), torch.empty(1, device=dev)) for bs in bsets]
+    us_p = time_steady(lambda *a: binding.mhc_sigmoid_param_grad(*a), psets)
+    results.append({"workload": "sigmoid_coeffs_n4_bf16", "dir": "fwd", "T": T, "H": H,
+                    "note": "pre = sigmoid(alpha*mix + b) computed in the kernel; bytes T*(10H+16)",
+                    "steady": {"us": us_f, "sets": ns, **entry_for(us_f, fb)}})
+    results.append({"workload": "sigmoid_coeffs_n4_bf16", "dir": "bwd", "T": T, "H": H,
+                    "note": "grad_residual, grad_z, grad_mix; bytes T*(18H+48)",
+                    "steady": {"us": us_b, "sets": ns, **entry_for(us_b, bb)}})
+    results.append({"workload": "sigmoid_param_grad_n4", "dir": "bwd", "T": T,
+                    "note": "grad_b and grad_alpha summed over the tokens (one block); "
+                            "bytes T*32, latency-bound",
+                    "steady": {"us": us_p, "sets": ns}})
+    del g, r, mix, sets, fsets, bsets, psets
+    torch.cuda.empty_cache()
     torch.cuda.synchronize()
     return results
 

@@ -177,6 +177,92 @@ MHC_API mhc_path_t mhc_aggregate_bwd_path(const void* grad_out, const void* resi
                                   const void* grad_residual, const float* grad_pre, int64_t T,
                                   int32_t n, int64_t H);
 
+/* ---- The pre coefficients computed from the mix --------------------------
+ *
+ * Source: "perf: fuse mHC coefficient backward epilogue" (Liger-Kernel pull
+ * request 1402), Summary: the mHC coefficient backward ends in the
+ * derivatives of the pre / post sigmoids, grad_mix, and the gradients of the
+ * bias b and of scalar alphas; Risks and Limitations: those two reductions run
+ * in a fixed, deterministic order.  The page prints no formula.  This
+ * library's reading, for the pre coefficients only:
+ *
+ *   z[t,k]   = alpha * mix[t,k] + b[k]       (FP32: RN multiply, then RN add)
+ *   pre[t,k] = sigmoid(z[t,k])
+ *   out      = the general forward above with that pre
+ *
+ *   grad_z[t,k]   = grad_pre[t,k] * sigmoid'(z[t,k])   (grad_pre: ORDER-256)
+ *   grad_mix[t,k] = alpha * grad_z[t,k]
+ *   grad_b[k]     = sum over t of grad_z[t,k]
+ *   grad_alpha    = sum over t of tree_n(grad_z[t,k] * mix[t,k])
+ *
+ * The last two are summed over tokens in ORDER-256 with t in place of h
+ * (chunks of 8 tokens, +0 past T), so they depend on T and on every token,
+ * but on nothing else.
+ *
+ * The sigmoid is this library's fixed binary32 sequence, so that results are
+ * a function of the input bits alone: e = exp32(-|z|) with exp32 the
+ * argument reduction of Cody and Waite (x = k ln2 + r, k = the integer
+ * nearest RN(x * RN(log2 e)), ties to even, r = (x - k*L1) - k*L2 with
+ * L1 = 0x1.62e4p-1, L2 = 0x1.7f7d1cp-20), the degree-7 Taylor polynomial of
+ * e^r in Horner form with coefficients RN(1/i!), and the scaling
+ * (q * 2^(k/2)) * 2^(k - k/2) (k/2 rounded toward zero); x < -104 gives +0.
+ * Then d = 1 + e; for z >= 0 sigmoid = 1/d and 1 - sigmoid = e/d, for z < 0
+ * the two swap; sigmoid' = sigmoid * (1 - sigmoid).  Every step is one RN
+ * binary32 operation.  sigmoid is within 2.5 ulp and sigmoid' within 4.5 ulp
+ * of the exact values.
+ *
+ * alpha is a DEVICE pointer to one FP32 value and b a DEVICE pointer to n
+ * FP32 values; neither may overlap an output.  Other rules as above.
+ */
+
+/* pre[t,k] = sigmoid(alpha * mix[t,k] + b[k]) on its own (the same bits as
+ * the fused calls compute internally).
+ *   mix  in   FP32 [T,n]
+ *   pre  out  FP32 [T,n]
+ */
+MHC_API mhc_status_t mhc_pre_sigmoid(const float* mix, const float* alpha, const float* b,
+                                     float* pre, int64_t T, int32_t n, mhc_stream_t stream);
+
+/* Fused forward: out = mhc_aggregate_fwd(residual, sigmoid(alpha * mix + b)),
+ * byte for byte, in one kernel (no pre buffer).
+ *   residual  in   [T,n,H] dtype
+ *   mix       in   FP32 [T,n]
+ *   out       out  [T,H] dtype
+ * Takes the kernel path mhc_aggregate_fwd_path(residual, mix, out, T, n, H).
+ */
+MHC_API mhc_status_t mhc_aggregate_sigmoid_fwd(const void* residual, const float* mix,
+                                               const float* alpha, const float* b, void* out,
+                                               int64_t T, int32_t n, int64_t H, mhc_dtype_t dtype,
+                                               mhc_stream_t stream);
+
+/* Fused backward, one kernel.
+ *   grad_out       in   [T,H] dtype
+ *   residual       in   [T,n,H] dtype
+ *   mix            in   FP32 [T,n]
+ *   grad_residual  out  [T,n,H] dtype: as mhc_aggregate_bwd with pre = sigmoid(z)
+ *   grad_z         out  FP32 [T,n]: grad_pre * sigmoid'(z)
+ *   grad_mix       out  FP32 [T,n]: alpha * grad_z
+ * Takes the kernel path mhc_aggregate_bwd_path(grad_out, residual, mix,
+ * grad_residual, grad_z, T, n, H).
+ */
+MHC_API mhc_status_t mhc_aggregate_sigmoid_bwd(const void* grad_out, const void* residual,
+                                               const float* mix, const float* alpha,
+                                               const float* b, void* grad_residual, float* grad_z,
+                                               float* grad_mix, int64_t T, int32_t n, int64_t H,
+                                               mhc_dtype_t dtype, mhc_stream_t stream);
+
+/* The gradients of b and alpha from the fused backward's grad_z.
+ *   grad_z      in   FP32 [T,n]
+ *   mix         in   FP32 [T,n]
+ *   grad_b      out  FP32 [n]
+ *   grad_alpha  out  FP32 [1]
+ * T == 0 writes +0 to every output (one launch); grad_z and mix may then be
+ * NULL.  One kernel, one block.
+ */
+MHC_API mhc_status_t mhc_sigmoid_param_grad(const float* grad_z, const float* mix, float* grad_b,
+                                            float* grad_alpha, int64_t T, int32_t n,
+                                            mhc_stream_t stream);
+
 /* Static text for a status code. */
 MHC_API const char* mhc_status_string(mhc_status_t status);
 

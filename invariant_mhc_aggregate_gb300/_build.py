@@ -1,9 +1,10 @@
 """Compile the sm_103a library ``libmhc_h_aggregate.so`` in-tree with nvcc.
 
 The library exports the C ABI of ``include/mhc_h_aggregate.h`` from
-``csrc/mhc_h_aggregate.cu``; the kernels (``csrc/mhc_device.cuh``) are
-instantiated per storage type in ``csrc/mhc_launch_*.cu``, compiled in parallel.  It is rebuilt when its sources or
-flags change (a stamp file beside it records their hash).
+``csrc/mhc_h_aggregate.cu``; the kernels (``csrc/mhc_device.cuh``,
+``csrc/mhc_coeffs.cuh``) are instantiated per storage type and coefficient
+source in ``csrc/mhc_launch_*.cu``, compiled in parallel.  It is rebuilt when
+its sources or flags change (a stamp file beside it records their hash).
 """
 
 from __future__ import annotations
@@ -22,8 +23,10 @@ LIB_DIR = os.path.join(PKG, "lib")
 LIB_NAME = "libmhc_h_aggregate.so"
 LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
 SOURCES = [os.path.join(CSRC, f) for f in
-           ("mhc_h_aggregate.cu", "mhc_launch_bf16.cu", "mhc_launch_f16.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fastdiv.cuh", "mhc_device.cuh", "mhc_launch.cuh")] \
+           ("mhc_h_aggregate.cu", "mhc_launch_bf16.cu", "mhc_launch_f16.cu",
+            "mhc_launch_sigmoid_bf16.cu", "mhc_launch_sigmoid_f16.cu", "mhc_launch_coeffs.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in
+                  ("fastdiv.cuh", "mhc_coeffs.cuh", "mhc_device.cuh", "mhc_launch.cuh")] \
     + [os.path.join(INCLUDE, "mhc_h_aggregate.h")]
 
 ARCH = "sm_103a"
@@ -62,8 +65,9 @@ def source_digest() -> str:
 
 
 KERNEL_FILES = [os.path.join(CSRC, f) for f in
-                ("mhc_device.cuh", "fastdiv.cuh", "mhc_launch.cuh", "mhc_launch_bf16.cu",
-                 "mhc_launch_f16.cu")]
+                ("mhc_device.cuh", "mhc_coeffs.cuh", "fastdiv.cuh", "mhc_launch.cuh",
+                 "mhc_launch_bf16.cu", "mhc_launch_f16.cu", "mhc_launch_sigmoid_bf16.cu",
+                 "mhc_launch_sigmoid_f16.cu", "mhc_launch_coeffs.cu")]
 
 
 def kernel_digest() -> str:

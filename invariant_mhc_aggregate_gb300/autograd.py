@@ -56,3 +56,53 @@ class HAggregate(torch.autograd.Function):
 def h_aggregate(residual: torch.Tensor, pre: torch.Tensor) -> torch.Tensor:
     """Differentiable batch-invariant H Aggregate (see the module docstring)."""
     return HAggregate.apply(residual, pre)
+
+
+class HAggregateSigmoid(torch.autograd.Function):
+    """out = aggregate(residual, sigmoid(alpha * mix + b)), with the pre
+    coefficients computed inside the kernels ("perf: fuse mHC coefficient
+    backward epilogue", Summary: the pre sigmoid's derivative, grad_mix and the
+    gradients of b and alpha).  The backward is one fused kernel for
+    grad_residual, grad_z and grad_mix, and one kernel summing grad_b and
+    grad_alpha over tokens in a fixed order."""
+
+    @staticmethod
+    def forward(ctx, residual, mix, alpha, b):
+        if residual.dtype not in (torch.bfloat16, torch.float16) or mix.dtype != torch.float32:
+            raise TypeError("expects residual bf16/f16 [...,n,H] and mix fp32 [...,n]")
+        if residual.dim() < 2 or residual.shape[:-1] != mix.shape:
+            raise ValueError(f"shape mismatch: residual {tuple(residual.shape)}, mix {tuple(mix.shape)}")
+        lead = residual.shape[:-2]
+        n, H = residual.shape[-2], residual.shape[-1]
+        r = residual.reshape(-1, n, H).contiguous()
+        m = mix.reshape(-1, n).contiguous()
+        a = alpha.reshape(1).contiguous()
+        bb = b.contiguous()
+        out = binding.aggregate_sigmoid(r, m, a, bb)
+        ctx.save_for_backward(r, m, a, bb)
+        ctx.lead = lead
+        ctx.alpha_shape = alpha.shape
+        return out.reshape(*lead, H)
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        r, m, a, bb = ctx.saved_tensors
+        n, H = r.shape[-2], r.shape[-1]
+        if grad_out.dtype != r.dtype:
+            raise TypeError(f"the output gradient must be {r.dtype}, got {grad_out.dtype}")
+        g = grad_out.reshape(-1, H).contiguous()
+        grad_residual, grad_z, grad_mix = binding.aggregate_sigmoid_backward(g, r, m, a, bb)
+        grad_alpha = grad_b = None
+        if ctx.needs_input_grad[2] or ctx.needs_input_grad[3]:
+            grad_b, grad_alpha = binding.sigmoid_param_grad(grad_z, m)
+            grad_alpha = grad_alpha.reshape(ctx.alpha_shape)
+        gr = grad_residual.reshape(*ctx.lead, n, H) if ctx.needs_input_grad[0] else None
+        gm = grad_mix.reshape(*ctx.lead, n) if ctx.needs_input_grad[1] else None
+        return (gr, gm, grad_alpha if ctx.needs_input_grad[2] else None,
+                grad_b if ctx.needs_input_grad[3] else None)
+
+
+def h_aggregate_sigmoid(residual: torch.Tensor, mix: torch.Tensor, alpha: torch.Tensor,
+                        b: torch.Tensor) -> torch.Tensor:
+    """Differentiable aggregate with pre = sigmoid(alpha * mix + b) computed in the kernel."""
+    return HAggregateSigmoid.apply(residual, mix, alpha, b)

@@ -47,6 +47,10 @@ EXPORTS = (
     "mhc_aggregate_bwd",
     "mhc_aggregate_fwd_path",
     "mhc_aggregate_bwd_path",
+    "mhc_pre_sigmoid",
+    "mhc_aggregate_sigmoid_fwd",
+    "mhc_aggregate_sigmoid_bwd",
+    "mhc_sigmoid_param_grad",
     "mhc_status_string",
     "mhc_h_aggregate_last_cuda_error",
 )
@@ -102,6 +106,14 @@ def load(path: str | None = None):
         lib.mhc_aggregate_fwd_path.restype = i32
         lib.mhc_aggregate_bwd_path.argtypes = [p, p, p, p, p, i64, i32, i64]
         lib.mhc_aggregate_bwd_path.restype = i32
+        lib.mhc_pre_sigmoid.argtypes = [p, p, p, p, i64, i32, p]
+        lib.mhc_pre_sigmoid.restype = i32
+        lib.mhc_aggregate_sigmoid_fwd.argtypes = [p, p, p, p, p, i64, i32, i64, i32, p]
+        lib.mhc_aggregate_sigmoid_fwd.restype = i32
+        lib.mhc_aggregate_sigmoid_bwd.argtypes = [p, p, p, p, p, p, p, p, i64, i32, i64, i32, p]
+        lib.mhc_aggregate_sigmoid_bwd.restype = i32
+        lib.mhc_sigmoid_param_grad.argtypes = [p, p, p, p, i64, i32, p]
+        lib.mhc_sigmoid_param_grad.restype = i32
         lib.mhc_status_string.argtypes = [i32]
         lib.mhc_status_string.restype = ctypes.c_char_p
         lib.mhc_h_aggregate_last_cuda_error.argtypes = []
@@ -152,6 +164,27 @@ def agg_fwd_path_raw(residual: int, pre: int, out: int, T: int, n: int, H: int) 
 def agg_bwd_path_raw(grad_out: int, residual: int, pre: int, grad_residual: int, grad_pre: int,
                      T: int, n: int, H: int) -> int:
     return load().mhc_aggregate_bwd_path(grad_out, residual, pre, grad_residual, grad_pre, T, n, H)
+
+
+def pre_sigmoid_raw(mix: int, alpha: int, b: int, pre: int, T: int, n: int, stream: int = 0) -> int:
+    return load().mhc_pre_sigmoid(mix, alpha, b, pre, T, n, stream)
+
+
+def agg_sigmoid_fwd_raw(residual: int, mix: int, alpha: int, b: int, out: int, T: int, n: int,
+                        H: int, dtype: int, stream: int = 0) -> int:
+    return load().mhc_aggregate_sigmoid_fwd(residual, mix, alpha, b, out, T, n, H, dtype, stream)
+
+
+def agg_sigmoid_bwd_raw(grad_out: int, residual: int, mix: int, alpha: int, b: int,
+                        grad_residual: int, grad_z: int, grad_mix: int, T: int, n: int, H: int,
+                        dtype: int, stream: int = 0) -> int:
+    return load().mhc_aggregate_sigmoid_bwd(grad_out, residual, mix, alpha, b, grad_residual,
+                                            grad_z, grad_mix, T, n, H, dtype, stream)
+
+
+def sigmoid_param_grad_raw(grad_z: int, mix: int, grad_b: int, grad_alpha: int, T: int, n: int,
+                           stream: int = 0) -> int:
+    return load().mhc_sigmoid_param_grad(grad_z, mix, grad_b, grad_alpha, T, n, stream)
 
 
 # ---------------------------------------------------------------------------
@@ -305,3 +338,121 @@ def h_aggregate_backward(grad_out: torch.Tensor, residual: torch.Tensor, pre: to
     grad_pre = torch.empty((T, 4), dtype=torch.float32, device=residual.device)
     mhc_h_aggregate_bwd(grad_out, residual, pre, grad_residual, grad_pre, stream)
     return grad_residual, grad_pre
+
+
+# ---------------------------------------------------------------------------
+# the pre coefficients computed from the mix: pre = sigmoid(alpha * mix + b)
+# ---------------------------------------------------------------------------
+
+def _coeff_params(alpha: torch.Tensor, b: torch.Tensor, n: int, device) -> None:
+    _check(b, "b", torch.float32, (n,))
+    if not isinstance(alpha, torch.Tensor) or alpha.numel() != 1:
+        raise ValueError("alpha must be a one-element tensor")
+    _check(alpha, "alpha", torch.float32, tuple(alpha.shape))
+    if alpha.device != device or b.device != device:
+        raise ValueError("alpha and b must be on the device of the other tensors")
+
+
+def mhc_pre_sigmoid(mix: torch.Tensor, alpha: torch.Tensor, b: torch.Tensor, pre: torch.Tensor,
+                    stream=None) -> None:
+    """pre[t,k] = sigmoid(alpha * mix[t,k] + b[k]) (the library's binary32 sigmoid)."""
+    if mix.dim() != 2:
+        raise ValueError(f"mix must be [T,n], got {tuple(mix.shape)}")
+    T, n = int(mix.shape[0]), int(mix.shape[1])
+    _check(mix, "mix", torch.float32, (T, n))
+    _check(pre, "pre", torch.float32, (T, n))
+    _coeff_params(alpha, b, n, mix.device)
+    st = pre_sigmoid_raw(mix.data_ptr(), alpha.data_ptr(), b.data_ptr(), pre.data_ptr(), T, n,
+                         _stream_handle(stream, mix.device))
+    if st != MHC_OK:
+        raise MhcError(st, "mhc_pre_sigmoid")
+
+
+def mhc_aggregate_sigmoid_fwd(residual: torch.Tensor, mix: torch.Tensor, alpha: torch.Tensor,
+                              b: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """out = aggregate(residual, sigmoid(alpha * mix + b)) in one kernel."""
+    T, n, H = _TnH(residual)
+    dt = _storage(residual, "residual")
+    _check(residual, "residual", residual.dtype, (T, n, H))
+    _check(mix, "mix", torch.float32, (T, n))
+    _check(out, "out", residual.dtype, (T, H))
+    _coeff_params(alpha, b, n, residual.device)
+    st = agg_sigmoid_fwd_raw(residual.data_ptr(), mix.data_ptr(), alpha.data_ptr(), b.data_ptr(),
+                             out.data_ptr(), T, n, H, dt, _stream_handle(stream, residual.device))
+    if st != MHC_OK:
+        raise MhcError(st, "mhc_aggregate_sigmoid_fwd")
+
+
+def mhc_aggregate_sigmoid_bwd(grad_out: torch.Tensor, residual: torch.Tensor, mix: torch.Tensor,
+                              alpha: torch.Tensor, b: torch.Tensor, grad_residual: torch.Tensor,
+                              grad_z: torch.Tensor, grad_mix: torch.Tensor, stream=None) -> None:
+    """Fused backward: grad_residual, grad_z = grad_pre * sigmoid'(z), grad_mix = alpha * grad_z."""
+    T, n, H = _TnH(residual)
+    dt = _storage(residual, "residual")
+    _check(grad_out, "grad_out", residual.dtype, (T, H))
+    _check(residual, "residual", residual.dtype, (T, n, H))
+    _check(mix, "mix", torch.float32, (T, n))
+    _check(grad_residual, "grad_residual", residual.dtype, (T, n, H))
+    _check(grad_z, "grad_z", torch.float32, (T, n))
+    _check(grad_mix, "grad_mix", torch.float32, (T, n))
+    _coeff_params(alpha, b, n, residual.device)
+    st = agg_sigmoid_bwd_raw(grad_out.data_ptr(), residual.data_ptr(), mix.data_ptr(),
+                             alpha.data_ptr(), b.data_ptr(), grad_residual.data_ptr(),
+                             grad_z.data_ptr(), grad_mix.data_ptr(), T, n, H, dt,
+                             _stream_handle(stream, residual.device))
+    if st != MHC_OK:
+        raise MhcError(st, "mhc_aggregate_sigmoid_bwd")
+
+
+def mhc_sigmoid_param_grad(grad_z: torch.Tensor, mix: torch.Tensor, grad_b: torch.Tensor,
+                           grad_alpha: torch.Tensor, stream=None) -> None:
+    """grad_b [n] and grad_alpha [1]: sums over tokens in ORDER-256."""
+    if grad_z.dim() != 2:
+        raise ValueError(f"grad_z must be [T,n], got {tuple(grad_z.shape)}")
+    T, n = int(grad_z.shape[0]), int(grad_z.shape[1])
+    _check(grad_z, "grad_z", torch.float32, (T, n))
+    _check(mix, "mix", torch.float32, (T, n))
+    _check(grad_b, "grad_b", torch.float32, (n,))
+    if grad_alpha.numel() != 1:
+        raise ValueError("grad_alpha must be a one-element tensor")
+    _check(grad_alpha, "grad_alpha", torch.float32, tuple(grad_alpha.shape))
+    st = sigmoid_param_grad_raw(grad_z.data_ptr(), mix.data_ptr(), grad_b.data_ptr(),
+                                grad_alpha.data_ptr(), T, n, _stream_handle(stream, grad_z.device))
+    if st != MHC_OK:
+        raise MhcError(st, "mhc_sigmoid_param_grad")
+
+
+def pre_sigmoid(mix: torch.Tensor, alpha: torch.Tensor, b: torch.Tensor, stream=None) -> torch.Tensor:
+    pre = torch.empty_like(mix)
+    mhc_pre_sigmoid(mix, alpha, b, pre, stream)
+    return pre
+
+
+def aggregate_sigmoid(residual: torch.Tensor, mix: torch.Tensor, alpha: torch.Tensor,
+                      b: torch.Tensor, stream=None) -> torch.Tensor:
+    """Allocate ``out`` [T,H] and run the fused forward."""
+    T, n, H = _TnH(residual)
+    out = torch.empty((T, H), dtype=residual.dtype, device=residual.device)
+    mhc_aggregate_sigmoid_fwd(residual, mix, alpha, b, out, stream)
+    return out
+
+
+def aggregate_sigmoid_backward(grad_out: torch.Tensor, residual: torch.Tensor, mix: torch.Tensor,
+                               alpha: torch.Tensor, b: torch.Tensor, stream=None):
+    """Allocate and return (grad_residual [T,n,H], grad_z [T,n], grad_mix [T,n])."""
+    T, n, H = _TnH(residual)
+    grad_residual = torch.empty((T, n, H), dtype=residual.dtype, device=residual.device)
+    grad_z = torch.empty((T, n), dtype=torch.float32, device=residual.device)
+    grad_mix = torch.empty((T, n), dtype=torch.float32, device=residual.device)
+    mhc_aggregate_sigmoid_bwd(grad_out, residual, mix, alpha, b, grad_residual, grad_z, grad_mix,
+                              stream)
+    return grad_residual, grad_z, grad_mix
+
+
+def sigmoid_param_grad(grad_z: torch.Tensor, mix: torch.Tensor, stream=None):
+    """Allocate and return (grad_b [n], grad_alpha [1])."""
+    n = int(grad_z.shape[1])
+    grad_b = torch.empty((n,), dtype=torch.float32, device=grad_z.device)
+    grad_alpha = torch.empty((1,), dtype=torch.float32, device=grad_z.device)
+    mhc_sigmoid_param_grad(grad_z, mix, grad_b, grad_alpha, stream)
+    return grad_b, grad_alpha

@@ -51,6 +51,7 @@
 #include <stdint.h>
 
 #include "fastdiv.cuh"
+#include "mhc_coeffs.cuh"
 
 namespace mhc {
 
@@ -128,32 +129,6 @@ __device__ __forceinline__ uint16_t ld_stream2(const void* p) {
 
 __device__ __forceinline__ void st_stream2(void* p, uint16_t v) {
     asm volatile("st.global.cs.u16 [%0], %1;" : : "l"(p), "h"(v) : "memory");
-}
-
-// The N pre values of a token (read by all of the token's threads: keep them
-// in L1).  pre_vec: the token's pre is aligned to min(16, 4N) bytes, so it is
-// read with float2 / float4 loads.
-template <int N>
-__device__ __forceinline__ void ld_pre(const float* p, bool pre_vec, float (&out)[N]) {
-    if (N == 1) {
-        out[0] = __ldg(p);
-    } else if (pre_vec && N == 2) {
-        const float2 v = __ldg(reinterpret_cast<const float2*>(p));
-        out[0] = v.x;
-        out[N - 1] = v.y;
-    } else if (pre_vec) {
-#pragma unroll
-        for (int i = 0; i < N / 4; ++i) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(p) + i);
-            out[4 * i + 0] = v.x;
-            out[4 * i + 1] = v.y;
-            out[4 * i + 2] = v.z;
-            out[4 * i + 3] = v.w;
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < N; ++k) out[k] = __ldg(p + k);
-    }
 }
 
 // Programmatic dependent launch.  Every kernel here is launched so that it may
@@ -242,11 +217,10 @@ __device__ __forceinline__ uint32_t agg_pair(const float (&pre)[N], const uint32
 // Vector path.  Output vector i (i = t*V + v, V = H / (2*NW) vectors per row)
 // is out[i]; the residual vector of row k is res[t*N*V + k*V + v] =
 // res[i + (N-1)tV + kV].
-template <int N, int DT, int NW, int BLOCK, int UNROLL>
+template <int N, int DT, int NW, int BLOCK, int UNROLL, class Coeffs>
 __global__ void __launch_bounds__(BLOCK)
-agg_fwd_vec_kernel(const Words<NW>* __restrict__ res, const float* __restrict__ pre,
-                   Words<NW>* __restrict__ out, uint32_t n_vec, uint32_t V, FastDivU32 divV,
-                   bool pre_vec) {
+agg_fwd_vec_kernel(const Words<NW>* __restrict__ res, Coeffs coeffs, Words<NW>* __restrict__ out,
+                   uint32_t n_vec, uint32_t V, FastDivU32 divV) {
     pdl_enter();
     const uint32_t first = blockIdx.x * uint32_t(BLOCK * UNROLL) + threadIdx.x;
     Words<NW> r[UNROLL][N];
@@ -259,13 +233,14 @@ agg_fwd_vec_kernel(const Words<NW>* __restrict__ res, const float* __restrict__ 
             const Words<NW>* src = res + (uint64_t(i) + uint64_t(N - 1) * uint64_t(t) * V);
 #pragma unroll
             for (int k = 0; k < N; ++k) r[u][k] = ld_stream<NW>(src + uint64_t(k) * V);
-            ld_pre<N>(pre + uint64_t(N) * t, pre_vec, p[u]);
+            coeffs.template load<N>(t, p[u]);
         }
     }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
         const uint32_t i = first + uint32_t(u * BLOCK);
         if (i < n_vec) {
+            coeffs.template to_pre<N>(p[u]);
             Words<NW> o;
 #pragma unroll
             for (int e = 0; e < NW; ++e) {
@@ -290,15 +265,15 @@ constexpr int kNarrowPerThread = 8;
 constexpr int kNarrowSeg = kNarrowBlock * kNarrowPerThread;
 
 // 4-byte path: P = H/2 pairs per row.
-template <int N, int DT>
+template <int N, int DT, class Coeffs>
 __global__ void __launch_bounds__(kNarrowBlock)
-agg_fwd_pair_kernel(const uint32_t* __restrict__ res2, const float* __restrict__ pre,
-                    uint32_t* __restrict__ out2, uint64_t T, uint64_t P) {
+agg_fwd_pair_kernel(const uint32_t* __restrict__ res2, Coeffs coeffs, uint32_t* __restrict__ out2,
+                    uint64_t T, uint64_t P) {
     pdl_enter();
     const uint64_t base = uint64_t(blockIdx.x) * kNarrowSeg + threadIdx.x;
     for (uint64_t t = blockIdx.y; t < T; t += gridDim.y) {
         float p[N];
-        ld_pre<N>(pre + uint64_t(N) * t, false, p);
+        coeffs.template load<N>(t, p);
         const uint32_t* src = res2 + uint64_t(N) * t * P;
         uint32_t w[kNarrowPerThread][N];
 #pragma unroll
@@ -309,6 +284,7 @@ agg_fwd_pair_kernel(const uint32_t* __restrict__ res2, const float* __restrict__
                 for (int k = 0; k < N; ++k) w[e][k] = ld_stream4(src + uint64_t(k) * P + c);
             }
         }
+        coeffs.template to_pre<N>(p);
 #pragma unroll
         for (int e = 0; e < kNarrowPerThread; ++e) {
             const uint64_t c = base + uint64_t(e) * kNarrowBlock;
@@ -318,15 +294,15 @@ agg_fwd_pair_kernel(const uint32_t* __restrict__ res2, const float* __restrict__
 }
 
 // 2-byte path: any H and any 2-byte alignment.
-template <int N, int DT>
+template <int N, int DT, class Coeffs>
 __global__ void __launch_bounds__(kNarrowBlock)
-agg_fwd_element_kernel(const uint16_t* __restrict__ res, const float* __restrict__ pre,
-                       uint16_t* __restrict__ out, uint64_t T, uint64_t H) {
+agg_fwd_element_kernel(const uint16_t* __restrict__ res, Coeffs coeffs, uint16_t* __restrict__ out,
+                       uint64_t T, uint64_t H) {
     pdl_enter();
     const uint64_t base = uint64_t(blockIdx.x) * kNarrowSeg + threadIdx.x;
     for (uint64_t t = blockIdx.y; t < T; t += gridDim.y) {
         float p[N];
-        ld_pre<N>(pre + uint64_t(N) * t, false, p);
+        coeffs.template load<N>(t, p);
         const uint16_t* src = res + uint64_t(N) * t * H;
         uint16_t v[kNarrowPerThread][N];
 #pragma unroll
@@ -337,6 +313,7 @@ agg_fwd_element_kernel(const uint16_t* __restrict__ res, const float* __restrict
                 for (int k = 0; k < N; ++k) v[e][k] = ld_stream2(src + uint64_t(k) * H + h);
             }
         }
+        coeffs.template to_pre<N>(p);
 #pragma unroll
         for (int e = 0; e < kNarrowPerThread; ++e) {
             const uint64_t h = base + uint64_t(e) * kNarrowBlock;
@@ -390,10 +367,11 @@ __device__ __forceinline__ float chunk_partial(const Words<NW>& g, const Words<N
 // adjacent threads: lane strides 16 .. LPT are thread strides 16/LPT .. 1
 // (xor shuffles), lane stride 1 (when LPT == 2) is the add of a thread's own
 // two lanes.  The 8 group values then fold with strides 4, 2, 1 in shared
-// memory, and grad_pre[t, 0..N-1] is written.  All threads of the block call it.
-template <int N, int LPT>
+// memory, and grad_pre[t, 0..N-1] goes to the coefficient source (which
+// stores it, or the gradients derived from it).  All threads of the block call it.
+template <int N, int LPT, class Coeffs>
 __device__ __forceinline__ void fold_lanes_and_store(float (&acc)[LPT][N], float (*red)[N],
-                                                     float* __restrict__ grad_pre_t) {
+                                                     const Coeffs& coeffs, uint64_t t) {
     constexpr int kThreadsPerGroup = 32 / LPT;
 #pragma unroll
     for (int k = 0; k < N; ++k) {
@@ -420,7 +398,7 @@ __device__ __forceinline__ void fold_lanes_and_store(float (&acc)[LPT][N], float
 #pragma unroll
             for (int i = 0; i < s; ++i) w[i] = __fadd_rn(w[i], w[i + s]);
         }
-        grad_pre_t[k] = w[0];
+        coeffs.template store_grad<N>(t, k, w[0]);
     }
     __syncthreads();  // red[] is reused by the next token of this block
 }
@@ -431,11 +409,10 @@ __device__ __forceinline__ void fold_lanes_and_store(float (&acc)[LPT][N], float
 // chunks LPT*(j + mB) + l = (LPT*j + l) + 256m: exactly that lane's chunks,
 // in increasing order.  Up to BATCH vectors per thread are held in registers
 // per pass.
-template <int N, int DT, int NW, int BATCH, int MIN_BLOCKS>
+template <int N, int DT, int NW, int BATCH, int MIN_BLOCKS, class Coeffs>
 __global__ void __launch_bounds__(kLanes / (NW / 4), MIN_BLOCKS)
 agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict__ res,
-                   const float* __restrict__ pre, Words<NW>* __restrict__ gres,
-                   float* __restrict__ grad_pre, uint64_t T, uint32_t V, bool pre_vec) {
+                   Coeffs coeffs, Words<NW>* __restrict__ gres, uint64_t T, uint32_t V) {
     constexpr int LPT = NW / 4;
     constexpr uint32_t B = kLanes / LPT;
     __shared__ float red[kGroups][N];
@@ -443,7 +420,8 @@ agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict_
     const uint32_t j = threadIdx.x;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
         float pk[N];
-        ld_pre<N>(pre + uint64_t(N) * t, pre_vec, pk);
+        coeffs.template load<N>(t, pk);
+        bool pk_ready = false;
         const Words<NW>* gt = g + t * V;
         const Words<NW>* rt = res + uint64_t(N) * t * V;
         Words<NW>* grt = gres + uint64_t(N) * t * V;
@@ -464,6 +442,10 @@ agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict_
                     for (int k = 0; k < N; ++k) rv[b][k] = ld_stream<NW>(rt + uint64_t(k) * V + v);
                 }
             }
+            if (!pk_ready) {
+                coeffs.template to_pre<N>(pk);
+                pk_ready = true;
+            }
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) {
                 const uint32_t v = v0 + uint32_t(b) * B;
@@ -478,7 +460,7 @@ agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict_
                 }
             }
         }
-        fold_lanes_and_store<N, LPT>(acc, red, grad_pre + uint64_t(N) * t);
+        fold_lanes_and_store<N, LPT>(acc, red, coeffs, t);
     }
 }
 
@@ -490,11 +472,10 @@ agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict_
 // adds its partial and writes its grad_residual chunk back in place, and the
 // segment's grad_residual rows are then stored with coalesced accesses.
 // PAIRS: 4-byte accesses (H even, buffers 4-byte aligned); else 2-byte.
-template <int N, int DT, bool PAIRS>
+template <int N, int DT, bool PAIRS, class Coeffs>
 __global__ void __launch_bounds__(kLanes)
 agg_bwd_staged_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ res,
-                      const float* __restrict__ pre, uint16_t* __restrict__ gres,
-                      float* __restrict__ grad_pre, uint64_t T, uint64_t H) {
+                      Coeffs coeffs, uint16_t* __restrict__ gres, uint64_t T, uint64_t H) {
     constexpr int kSeg = 8 * kLanes;                 // values per segment
     constexpr int kUnit = PAIRS ? 2 : 1;             // values per access
     constexpr int kPer = kSeg / (kUnit * kLanes);    // accesses per thread per row
@@ -507,7 +488,8 @@ agg_bwd_staged_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict
     const uint64_t U = H / kUnit;                    // units per row
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
         float pk[N];
-        ld_pre<N>(pre + uint64_t(N) * t, false, pk);
+        coeffs.template load<N>(t, pk);
+        bool pk_ready = false;
         const uint16_t* gt = g + t * H;
         const uint16_t* rt = res + uint64_t(N) * t * H;
         uint16_t* grt = gres + uint64_t(N) * t * H;
@@ -535,6 +517,10 @@ agg_bwd_staged_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict
                 }
             }
             __syncthreads();
+            if (!pk_ready) {
+                coeffs.template to_pre<N>(pk);
+                pk_ready = true;
+            }
             if (base / 8 + j < C) {
                 Words<4> gv;
                 *reinterpret_cast<uint4*>(gv.w) = *reinterpret_cast<const uint4*>(sg + 8 * j);
@@ -565,7 +551,130 @@ agg_bwd_staged_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict
             }
             __syncthreads();  // the next segment overwrites the staging buffers
         }
-        fold_lanes_and_store<N, 1>(acc, red, grad_pre + uint64_t(N) * t);
+        fold_lanes_and_store<N, 1>(acc, red, coeffs, t);
+    }
+}
+
+// --------------------------------------------------------------------------
+// the pre coefficients on their own, and the gradients of alpha and b
+// --------------------------------------------------------------------------
+
+// pre[i] = sigmoid(alpha * mix[i] + b[i mod N]) over the T*N values (flat,
+// grid-stride; the same binary32 sequence as the fused kernels).
+constexpr int kCoeffBlock = 256;
+
+template <int N>
+__global__ void __launch_bounds__(kCoeffBlock)
+pre_sigmoid_kernel(const float* __restrict__ mix, const float* __restrict__ alpha,
+                   const float* __restrict__ b, float* __restrict__ pre, uint64_t count) {
+    pdl_enter();
+    const float a = __ldg(alpha);
+    const uint64_t stride = uint64_t(gridDim.x) * kCoeffBlock;
+    for (uint64_t i = uint64_t(blockIdx.x) * kCoeffBlock + threadIdx.x; i < count; i += stride) {
+        float s, one_minus;
+        sigmoid32(pre_activation(a, __ldg(mix + i), __ldg(b + (i % N))), s, one_minus);
+        pre[i] = s;
+    }
+}
+
+// grad_b[k] = sum over t of grad_z[t,k] and grad_alpha = sum over t of
+// tree_N(grad_z[t,k] * mix[t,k]), both in ORDER-256 with tokens in place of h:
+// chunk c = tokens 8c .. 8c+7 (+0 past T) summed by the chunk tree; lane j
+// adds the partials of chunks j, j + 256, ... in increasing order from +0;
+// groups of 32 lanes fold with strides 16 .. 1, the 8 groups with 4, 2, 1.
+//
+// One block of P = param_threads<N>() threads (a reduction over T has no
+// per-token parallelism left to give other blocks without a cross-block
+// exchange).  Each round, thread i computes the partials of chunk c0 + i
+// (holding 16N loaded values, hence fewer threads for larger N) into shared
+// memory; lane j (thread j < 256) then adds the partials of its chunks
+// c0 + j, c0 + 256 + j, ... < c0 + P, in that order.
+template <int N>
+__host__ __device__ constexpr int param_threads() { return N <= 2 ? 1024 : 2048 / N; }
+
+template <int N>
+__global__ void __launch_bounds__(param_threads<N>())
+sigmoid_param_grad_kernel(const float* __restrict__ grad_z, const float* __restrict__ mix,
+                          float* __restrict__ grad_b, float* __restrict__ grad_alpha, uint64_t T,
+                          bool vec) {
+    constexpr int kParamThreads = param_threads<N>();
+    constexpr int M = N + 1;   // grad_b[0 .. N-1], grad_alpha
+    __shared__ float part[kParamThreads][M];
+    __shared__ float red[kGroups][M];
+    pdl_enter();
+    const uint32_t i = threadIdx.x;
+    const uint64_t C = (T + 7) / 8;
+    float acc[M];
+#pragma unroll
+    for (int k = 0; k < M; ++k) acc[k] = 0.0f;
+    for (uint64_t c0 = 0; c0 < C; c0 += kParamThreads) {
+        const uint64_t c = c0 + i;
+        if (c < C) {
+            float gz[8][N], m[8][N];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint64_t t = 8 * c + e;
+                if (t < T) {
+                    ld_row<N>(grad_z + uint64_t(N) * t, vec, gz[e]);
+                    ld_row<N>(mix + uint64_t(N) * t, vec, m[e]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < N; ++k) gz[e][k] = m[e][k] = 0.0f;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < N; ++k) {
+                float q[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q[e] = gz[e][k];
+                part[i][k] = tree_sum<8>(q);
+            }
+            float qa[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float prod[N];
+#pragma unroll
+                for (int k = 0; k < N; ++k) prod[k] = __fmul_rn(gz[e][k], m[e][k]);
+                qa[e] = tree_sum<N>(prod);
+            }
+            part[i][N] = tree_sum<8>(qa);
+        }
+        __syncthreads();
+        if (i < kLanes) {
+#pragma unroll
+            for (int h = 0; h < kParamThreads / kLanes; ++h) {
+                if (c0 + uint64_t(h) * kLanes + i < C) {
+#pragma unroll
+                    for (int k = 0; k < M; ++k) acc[k] = __fadd_rn(acc[k], part[h * kLanes + i][k]);
+                }
+            }
+        }
+        __syncthreads();   // part[] is refilled by the next round
+    }
+    if (i < kLanes) {      // warps 0 .. 7 are the 8 groups of 32 lanes
+#pragma unroll
+        for (int k = 0; k < M; ++k) {
+#pragma unroll
+            for (int s = 16; s >= 1; s >>= 1)
+                acc[k] = __fadd_rn(acc[k], __shfl_xor_sync(0xffffffffu, acc[k], s));
+        }
+        if ((i % 32) == 0) {
+#pragma unroll
+            for (int k = 0; k < M; ++k) red[i / 32][k] = acc[k];
+        }
+    }
+    __syncthreads();
+    if (i < uint32_t(M)) {
+        float w[kGroups];
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) w[g] = red[g][i];
+#pragma unroll
+        for (int s = kGroups / 2; s >= 1; s >>= 1) {
+#pragma unroll
+            for (int g = 0; g < s; ++g) w[g] = __fadd_rn(w[g], w[g + s]);
+        }
+        if (i < uint32_t(N)) grad_b[i] = w[0];
+        else grad_alpha[0] = w[0];
     }
 }
 

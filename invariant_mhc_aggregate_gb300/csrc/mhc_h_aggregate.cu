@@ -15,7 +15,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 
 thread_local int32_t g_last_cuda_error = 0;
 
@@ -118,9 +118,10 @@ mhc_status_t aggregate_fwd(const void* residual, const float* pre, void* out, in
     if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
     if ((path == MHC_PATH_VEC32 || path == MHC_PATH_VEC16) && uint64_t(H) / 8 > 0x7FFFFFFFull)
         return MHC_ERR_UNSUPPORTED;
-    const mhc::FwdCall c{residual, pre, out, uint64_t(T), uint64_t(H), int(n), int(path),
-                         pre_vectorizable(pre, n), num_sms(), reinterpret_cast<cudaStream_t>(stream)};
-    return finish(dtype == MHC_DTYPE_BF16 ? mhc::fwd_bf16(c) : mhc::fwd_f16(c));
+    const mhc::FwdCall c{residual, out, uint64_t(T), uint64_t(H), int(n), int(path), num_sms(),
+                         reinterpret_cast<cudaStream_t>(stream)};
+    const mhc::PlainCoeffs k{pre, nullptr, pre_vectorizable(pre, n)};
+    return finish(dtype == MHC_DTYPE_BF16 ? mhc::fwd_bf16(c, k) : mhc::fwd_f16(c, k));
 }
 
 mhc_status_t aggregate_bwd(const void* grad_out, const void* residual, const float* pre,
@@ -135,10 +136,105 @@ mhc_status_t aggregate_bwd(const void* grad_out, const void* residual, const flo
     // vector indices within a row are 32-bit (with headroom for the per-pass stride)
     if ((path == MHC_PATH_VEC32 || path == MHC_PATH_VEC16) && uint64_t(H) / 8 > 0x7FFFFFFFull)
         return MHC_ERR_UNSUPPORTED;
-    const mhc::BwdCall c{grad_out, residual, pre, grad_residual, grad_pre, uint64_t(T), uint64_t(H),
-                         int(n), int(path), pre_vectorizable(pre, n), num_sms(),
+    const mhc::BwdCall c{grad_out, residual, grad_residual, uint64_t(T), uint64_t(H), int(n),
+                         int(path), num_sms(), reinterpret_cast<cudaStream_t>(stream)};
+    const mhc::PlainCoeffs k{pre, grad_pre, pre_vectorizable(pre, n)};
+    return finish(dtype == MHC_DTYPE_BF16 ? mhc::bwd_bf16(c, k) : mhc::bwd_f16(c, k));
+}
+
+// ---- the pre coefficients computed from the mix (sigmoid) ----------------
+
+// alpha (one float) and b (n floats) are 4-byte aligned and overlap none of
+// the outputs.
+bool params_ok(const float* alpha, const float* b, int64_t n, const Range* outs, int n_outs) {
+    if (!alpha || !b || !aligned(alpha, 4) || !aligned(b, 4)) return false;
+    const Range ra = range_of(alpha, 4), rb = range_of(b, uint64_t(4) * uint64_t(n));
+    for (int i = 0; i < n_outs; ++i)
+        if (overlap(outs[i], ra) || overlap(outs[i], rb)) return false;
+    return true;
+}
+
+mhc_status_t aggregate_sigmoid_fwd(const void* residual, const float* mix, const float* alpha,
+                                   const float* b, void* out, int64_t T, int64_t n, int64_t H,
+                                   int32_t dtype, mhc_stream_t stream) {
+    if (!dtype_ok(dtype)) return MHC_ERR_INVALID_ARG;
+    if (!streams_ok(n)) return MHC_ERR_UNSUPPORTED;
+    if (!sizes_ok(T, n, H)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    const mhc_path_t path = fwd_path(residual, mix, out, T, n, H);
+    if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
+    const Range ro = range_of(out, uint64_t(T) * 2 * uint64_t(H));
+    if (!params_ok(alpha, b, n, &ro, 1)) return MHC_ERR_INVALID_ARG;
+    if ((path == MHC_PATH_VEC32 || path == MHC_PATH_VEC16) && uint64_t(H) / 8 > 0x7FFFFFFFull)
+        return MHC_ERR_UNSUPPORTED;
+    const mhc::FwdCall c{residual, out, uint64_t(T), uint64_t(H), int(n), int(path), num_sms(),
                          reinterpret_cast<cudaStream_t>(stream)};
-    return finish(dtype == MHC_DTYPE_BF16 ? mhc::bwd_bf16(c) : mhc::bwd_f16(c));
+    const mhc::SigmoidCoeffs k{mix, alpha, b, nullptr, nullptr, pre_vectorizable(mix, n)};
+    return finish(dtype == MHC_DTYPE_BF16 ? mhc::fwd_bf16(c, k) : mhc::fwd_f16(c, k));
+}
+
+mhc_status_t aggregate_sigmoid_bwd(const void* grad_out, const void* residual, const float* mix,
+                                   const float* alpha, const float* b, void* grad_residual,
+                                   float* grad_z, float* grad_mix, int64_t T, int64_t n, int64_t H,
+                                   int32_t dtype, mhc_stream_t stream) {
+    if (!dtype_ok(dtype)) return MHC_ERR_INVALID_ARG;
+    if (!streams_ok(n)) return MHC_ERR_UNSUPPORTED;
+    if (!sizes_ok(T, n, H)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    // grad_z stands in for grad_pre in the path check (same shape and rules)
+    const mhc_path_t path = bwd_path(grad_out, residual, mix, grad_residual, grad_z, T, n, H);
+    if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
+    if (!grad_mix || !aligned(grad_mix, 4)) return MHC_ERR_INVALID_ARG;
+    const uint64_t TH = uint64_t(T) * uint64_t(H);
+    const Range outs[3] = {range_of(grad_residual, TH * 2 * uint64_t(n)),
+                           range_of(grad_z, uint64_t(T) * 4 * uint64_t(n)),
+                           range_of(grad_mix, uint64_t(T) * 4 * uint64_t(n))};
+    const Range ins[3] = {range_of(grad_out, TH * 2), range_of(residual, TH * 2 * uint64_t(n)),
+                          range_of(mix, uint64_t(T) * 4 * uint64_t(n))};
+    for (const Range& in : ins)
+        if (overlap(outs[2], in)) return MHC_ERR_INVALID_ARG;
+    if (overlap(outs[2], outs[0]) || overlap(outs[2], outs[1])) return MHC_ERR_INVALID_ARG;
+    if (!params_ok(alpha, b, n, outs, 3)) return MHC_ERR_INVALID_ARG;
+    if ((path == MHC_PATH_VEC32 || path == MHC_PATH_VEC16) && uint64_t(H) / 8 > 0x7FFFFFFFull)
+        return MHC_ERR_UNSUPPORTED;
+    const mhc::BwdCall c{grad_out, residual, grad_residual, uint64_t(T), uint64_t(H), int(n),
+                         int(path), num_sms(), reinterpret_cast<cudaStream_t>(stream)};
+    const mhc::SigmoidCoeffs k{mix, alpha, b, grad_z, grad_mix, pre_vectorizable(mix, n)};
+    return finish(dtype == MHC_DTYPE_BF16 ? mhc::bwd_bf16(c, k) : mhc::bwd_f16(c, k));
+}
+
+mhc_status_t pre_sigmoid(const float* mix, const float* alpha, const float* b, float* pre,
+                         int64_t T, int64_t n, mhc_stream_t stream) {
+    if (!streams_ok(n)) return MHC_ERR_UNSUPPORTED;
+    if (T < 0 || T > INT64_MAX / (4 * n)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    if (!mix || !pre || !aligned(mix, 4) || !aligned(pre, 4)) return MHC_ERR_INVALID_ARG;
+    const Range rp = range_of(pre, uint64_t(T) * 4 * uint64_t(n));
+    if (overlap(rp, range_of(mix, uint64_t(T) * 4 * uint64_t(n)))) return MHC_ERR_INVALID_ARG;
+    if (!params_ok(alpha, b, n, &rp, 1)) return MHC_ERR_INVALID_ARG;
+    return finish(mhc::pre_sigmoid(mix, alpha, b, pre, uint64_t(T), int(n), num_sms(),
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mhc_status_t sigmoid_param_grad(const float* grad_z, const float* mix, float* grad_b,
+                                float* grad_alpha, int64_t T, int64_t n, mhc_stream_t stream) {
+    if (!streams_ok(n)) return MHC_ERR_UNSUPPORTED;
+    if (T < 0 || T > INT64_MAX / (4 * n)) return MHC_ERR_INVALID_ARG;
+    if (!grad_b || !grad_alpha || !aligned(grad_b, 4) || !aligned(grad_alpha, 4))
+        return MHC_ERR_INVALID_ARG;
+    if (T > 0 && (!grad_z || !mix || !aligned(grad_z, 4) || !aligned(mix, 4)))
+        return MHC_ERR_INVALID_ARG;
+    const Range rb = range_of(grad_b, uint64_t(4) * uint64_t(n)), ra = range_of(grad_alpha, 4);
+    if (overlap(rb, ra)) return MHC_ERR_INVALID_ARG;
+    if (T > 0) {
+        const Range rz = range_of(grad_z, uint64_t(T) * 4 * uint64_t(n));
+        const Range rm = range_of(mix, uint64_t(T) * 4 * uint64_t(n));
+        if (overlap(rb, rz) || overlap(rb, rm) || overlap(ra, rz) || overlap(ra, rm))
+            return MHC_ERR_INVALID_ARG;
+    }
+    const bool vec = T > 0 && pre_vectorizable(grad_z, n) && pre_vectorizable(mix, n);
+    return finish(mhc::sigmoid_param_grad(grad_z, mix, grad_b, grad_alpha, uint64_t(T), int(n), vec,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -209,6 +305,30 @@ mhc_path_t mhc_aggregate_bwd_path(const void* grad_out, const void* residual, co
                                   const void* grad_residual, const float* grad_pre, int64_t T,
                                   int32_t n, int64_t H) {
     return bwd_path(grad_out, residual, pre, grad_residual, grad_pre, T, n, H);
+}
+
+mhc_status_t mhc_pre_sigmoid(const float* mix, const float* alpha, const float* b, float* pre,
+                             int64_t T, int32_t n, mhc_stream_t stream) {
+    return pre_sigmoid(mix, alpha, b, pre, T, n, stream);
+}
+
+mhc_status_t mhc_aggregate_sigmoid_fwd(const void* residual, const float* mix, const float* alpha,
+                                       const float* b, void* out, int64_t T, int32_t n, int64_t H,
+                                       mhc_dtype_t dtype, mhc_stream_t stream) {
+    return aggregate_sigmoid_fwd(residual, mix, alpha, b, out, T, n, H, int32_t(dtype), stream);
+}
+
+mhc_status_t mhc_aggregate_sigmoid_bwd(const void* grad_out, const void* residual, const float* mix,
+                                       const float* alpha, const float* b, void* grad_residual,
+                                       float* grad_z, float* grad_mix, int64_t T, int32_t n,
+                                       int64_t H, mhc_dtype_t dtype, mhc_stream_t stream) {
+    return aggregate_sigmoid_bwd(grad_out, residual, mix, alpha, b, grad_residual, grad_z, grad_mix,
+                                 T, n, H, int32_t(dtype), stream);
+}
+
+mhc_status_t mhc_sigmoid_param_grad(const float* grad_z, const float* mix, float* grad_b,
+                                    float* grad_alpha, int64_t T, int32_t n, mhc_stream_t stream) {
+    return sigmoid_param_grad(grad_z, mix, grad_b, grad_alpha, T, n, stream);
 }
 
 }  // extern "C"

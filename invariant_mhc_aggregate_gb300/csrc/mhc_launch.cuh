@@ -16,14 +16,15 @@ constexpr int kPathPair = 1;
 constexpr int kPathElement = 2;
 constexpr int kPathVec32 = 3;
 
+// The per-token coefficients (pre, or the mix they are computed from) and the
+// per-token coefficient gradients travel in a PlainCoeffs / SigmoidCoeffs
+// value (mhc_coeffs.cuh) next to these.
 struct FwdCall {
     const void* residual;
-    const float* pre;
     void* out;
     uint64_t T, H;
     int n;            // streams: 1, 2, 4 or 8
     int path;         // kPath*
-    bool pre_vec;     // pre aligned to min(16, 4n) bytes
     int num_sms;
     cudaStream_t stream;
 };
@@ -31,21 +32,29 @@ struct FwdCall {
 struct BwdCall {
     const void* g;
     const void* residual;
-    const float* pre;
     void* gres;
-    float* gpre;
     uint64_t T, H;
     int n;
     int path;
-    bool pre_vec;
     int num_sms;
     cudaStream_t stream;
 };
 
-cudaError_t fwd_bf16(const FwdCall& c);
-cudaError_t fwd_f16(const FwdCall& c);
-cudaError_t bwd_bf16(const BwdCall& c);
-cudaError_t bwd_f16(const BwdCall& c);
+// One translation unit per storage type and coefficient source.
+cudaError_t fwd_bf16(const FwdCall& c, const PlainCoeffs& k);
+cudaError_t fwd_f16(const FwdCall& c, const PlainCoeffs& k);
+cudaError_t bwd_bf16(const BwdCall& c, const PlainCoeffs& k);
+cudaError_t bwd_f16(const BwdCall& c, const PlainCoeffs& k);
+cudaError_t fwd_bf16(const FwdCall& c, const SigmoidCoeffs& k);
+cudaError_t fwd_f16(const FwdCall& c, const SigmoidCoeffs& k);
+cudaError_t bwd_bf16(const BwdCall& c, const SigmoidCoeffs& k);
+cudaError_t bwd_f16(const BwdCall& c, const SigmoidCoeffs& k);
+
+// The coefficient kernels of their own (mhc_launch_coeffs.cu).
+cudaError_t pre_sigmoid(const float* mix, const float* alpha, const float* b, float* pre,
+                        uint64_t T, int n, int num_sms, cudaStream_t stream);
+cudaError_t sigmoid_param_grad(const float* grad_z, const float* mix, float* grad_b,
+                               float* grad_alpha, uint64_t T, int n, bool vec, cudaStream_t stream);
 
 // Launch with programmatic stream serialization (see pdl_enter).
 template <typename... Params, typename... Args>
@@ -75,14 +84,14 @@ inline uint32_t grid_for(uint64_t items, uint32_t per_block, uint64_t cap) {
 // forward
 // ---------------------------------------------------------------------------
 
-template <int N, int DT, int NW, int BLOCK, int UNROLL>
-cudaError_t launch_fwd_vec(const void* residual, const float* pre, void* out, uint32_t n_vec,
-                           uint32_t V, bool pre_vec, cudaStream_t stream) {
+template <int N, int DT, int NW, int BLOCK, int UNROLL, class Coeffs>
+cudaError_t launch_fwd_vec(const void* residual, const Coeffs& k, void* out, uint32_t n_vec,
+                           uint32_t V, cudaStream_t stream) {
     const uint32_t per_block = uint32_t(BLOCK * UNROLL);
     const uint32_t blocks = uint32_t((uint64_t(n_vec) + per_block - 1) / per_block);
-    return launch(agg_fwd_vec_kernel<N, DT, NW, BLOCK, UNROLL>, blocks, BLOCK, stream,
-                  static_cast<const Words<NW>*>(residual), pre, static_cast<Words<NW>*>(out), n_vec,
-                  V, make_fastdiv_u32(V), pre_vec);
+    return launch(agg_fwd_vec_kernel<N, DT, NW, BLOCK, UNROLL, Coeffs>, blocks, BLOCK, stream,
+                  static_cast<const Words<NW>*>(residual), k, static_cast<Words<NW>*>(out), n_vec,
+                  V, make_fastdiv_u32(V));
 }
 
 // Large calls: 256 threads holding about 64 bytes of residual loads per
@@ -91,8 +100,8 @@ cudaError_t launch_fwd_vec(const void* residual, const float* pre, void* out, ui
 // call over more SMs.  Vector indices are 32-bit: a call with 2^31 vectors or
 // more runs as several launches over consecutive token ranges (tokens are
 // independent, so the bytes are the same as one launch).
-template <int N, int DT, int NW>
-cudaError_t fwd_vec(const FwdCall& c) {
+template <int N, int DT, int NW, class Coeffs>
+cudaError_t fwd_vec(const FwdCall& c, const Coeffs& coeffs) {
     constexpr int kUnroll = (64 / (N * NW)) > 0 ? (64 / (N * NW)) : 1;
     const uint64_t V = c.H / (2 * NW);
     const uint64_t max_tokens = 0x7FFFFFFFull / V;
@@ -101,12 +110,12 @@ cudaError_t fwd_vec(const FwdCall& c) {
         const uint64_t nt = (c.T - t0 < max_tokens) ? c.T - t0 : max_tokens;
         const uint32_t n_vec = uint32_t(nt * V);
         const void* r = static_cast<const char*>(c.residual) + t0 * 2 * N * c.H;
-        const float* p = c.pre + uint64_t(N) * t0;
+        const Coeffs k = coeffs.shifted(N * t0);
         void* o = static_cast<char*>(c.out) + t0 * 2 * c.H;
         const cudaError_t e =
             n_vec <= small_limit
-                ? launch_fwd_vec<N, DT, NW, 128, 1>(r, p, o, n_vec, uint32_t(V), c.pre_vec, c.stream)
-                : launch_fwd_vec<N, DT, NW, 256, kUnroll>(r, p, o, n_vec, uint32_t(V), c.pre_vec, c.stream);
+                ? launch_fwd_vec<N, DT, NW, 128, 1>(r, k, o, n_vec, uint32_t(V), c.stream)
+                : launch_fwd_vec<N, DT, NW, 256, kUnroll>(r, k, o, n_vec, uint32_t(V), c.stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -135,29 +144,29 @@ cudaError_t launch2d(void (*kernel)(Params...), dim3 grid, uint32_t block, cudaS
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
 }
 
-template <int N, int DT>
-cudaError_t fwd_n(const FwdCall& c) {
+template <int N, int DT, class Coeffs>
+cudaError_t fwd_n(const FwdCall& c, const Coeffs& k) {
     switch (c.path) {
-        case kPathVec32: return fwd_vec<N, DT, 8>(c);
-        case kPathVec16: return fwd_vec<N, DT, 4>(c);
+        case kPathVec32: return fwd_vec<N, DT, 8>(c, k);
+        case kPathVec16: return fwd_vec<N, DT, 4>(c, k);
         case kPathPair: {
             const uint64_t P = c.H / 2;
-            return launch2d(agg_fwd_pair_kernel<N, DT>, narrow_grid(P, c.T), kNarrowBlock, c.stream,
-                            static_cast<const uint32_t*>(c.residual), c.pre, static_cast<uint32_t*>(c.out), c.T, P);
+            return launch2d(agg_fwd_pair_kernel<N, DT, Coeffs>, narrow_grid(P, c.T), kNarrowBlock, c.stream,
+                            static_cast<const uint32_t*>(c.residual), k, static_cast<uint32_t*>(c.out), c.T, P);
         }
         default:
-            return launch2d(agg_fwd_element_kernel<N, DT>, narrow_grid(c.H, c.T), kNarrowBlock, c.stream,
-                            static_cast<const uint16_t*>(c.residual), c.pre, static_cast<uint16_t*>(c.out), c.T, c.H);
+            return launch2d(agg_fwd_element_kernel<N, DT, Coeffs>, narrow_grid(c.H, c.T), kNarrowBlock, c.stream,
+                            static_cast<const uint16_t*>(c.residual), k, static_cast<uint16_t*>(c.out), c.T, c.H);
     }
 }
 
-template <int DT>
-cudaError_t fwd_dispatch(const FwdCall& c) {
+template <int DT, class Coeffs>
+cudaError_t fwd_dispatch(const FwdCall& c, const Coeffs& k) {
     switch (c.n) {
-        case 1: return fwd_n<1, DT>(c);
-        case 2: return fwd_n<2, DT>(c);
-        case 4: return fwd_n<4, DT>(c);
-        default: return fwd_n<8, DT>(c);
+        case 1: return fwd_n<1, DT>(c, k);
+        case 2: return fwd_n<2, DT>(c, k);
+        case 4: return fwd_n<4, DT>(c, k);
+        default: return fwd_n<8, DT>(c, k);
     }
 }
 
@@ -165,13 +174,13 @@ cudaError_t fwd_dispatch(const FwdCall& c) {
 // backward
 // ---------------------------------------------------------------------------
 
-template <int N, int DT, int NW, int BATCH, int MIN_BLOCKS>
-cudaError_t launch_bwd_vec(const BwdCall& c, uint32_t V) {
+template <int N, int DT, int NW, int BATCH, int MIN_BLOCKS, class Coeffs>
+cudaError_t launch_bwd_vec(const BwdCall& c, const Coeffs& k, uint32_t V) {
     constexpr int kThreads = kLanes / (NW / 4);
     const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
-    return launch(agg_bwd_vec_kernel<N, DT, NW, BATCH, MIN_BLOCKS>, blocks, kThreads, c.stream,
-                  static_cast<const Words<NW>*>(c.g), static_cast<const Words<NW>*>(c.residual), c.pre,
-                  static_cast<Words<NW>*>(c.gres), c.gpre, c.T, V, c.pre_vec);
+    return launch(agg_bwd_vec_kernel<N, DT, NW, BATCH, MIN_BLOCKS, Coeffs>, blocks, kThreads, c.stream,
+                  static_cast<const Words<NW>*>(c.g), static_cast<const Words<NW>*>(c.residual), k,
+                  static_cast<Words<NW>*>(c.gres), c.T, V);
 }
 
 // Backward vector launch shapes.  A block holds one token; its threads keep
@@ -181,62 +190,62 @@ cudaError_t launch_bwd_vec(const BwdCall& c, uint32_t V) {
 // vectors (128 threads) the batch follows the vectors per thread so that a
 // row is covered in one pass: batch 1 / 2 / 4 with 6 / 3 / 2 blocks per SM
 // for up to 1 / 2 / more vectors per thread.
-template <int N, int DT>
-cudaError_t bwd_vec32(const BwdCall& c) {
+template <int N, int DT, class Coeffs>
+cudaError_t bwd_vec32(const BwdCall& c, const Coeffs& k) {
     const uint32_t V = uint32_t(c.H / 16);
     if constexpr (N == 4) {
         const uint32_t per_thread = (V + 127) / 128;
-        if (per_thread <= 1) return launch_bwd_vec<N, DT, 8, 1, 6>(c, V);
-        if (per_thread == 2) return launch_bwd_vec<N, DT, 8, 2, 3>(c, V);
-        return launch_bwd_vec<N, DT, 8, 4, 2>(c, V);
+        if (per_thread <= 1) return launch_bwd_vec<N, DT, 8, 1, 6>(c, k, V);
+        if (per_thread == 2) return launch_bwd_vec<N, DT, 8, 2, 3>(c, k, V);
+        return launch_bwd_vec<N, DT, 8, 4, 2>(c, k, V);
     } else if constexpr (N == 1) {
-        return launch_bwd_vec<N, DT, 8, 4, 4>(c, V);
+        return launch_bwd_vec<N, DT, 8, 4, 4>(c, k, V);
     } else if constexpr (N == 2) {
-        return launch_bwd_vec<N, DT, 8, 4, 3>(c, V);
+        return launch_bwd_vec<N, DT, 8, 4, 3>(c, k, V);
     } else {
-        return launch_bwd_vec<N, DT, 8, 2, 2>(c, V);
+        return launch_bwd_vec<N, DT, 8, 2, 2>(c, k, V);
     }
 }
 
-template <int N, int DT>
-cudaError_t bwd_vec16(const BwdCall& c) {
+template <int N, int DT, class Coeffs>
+cudaError_t bwd_vec16(const BwdCall& c, const Coeffs& k) {
     const uint32_t V = uint32_t(c.H / 8);
     if constexpr (N == 1) {
-        return launch_bwd_vec<N, DT, 4, 4, 3>(c, V);
+        return launch_bwd_vec<N, DT, 4, 4, 3>(c, k, V);
     } else if constexpr (N == 8) {
-        return launch_bwd_vec<N, DT, 4, 1, 2>(c, V);
+        return launch_bwd_vec<N, DT, 4, 1, 2>(c, k, V);
     } else {
-        return launch_bwd_vec<N, DT, 4, 2, 3>(c, V);
+        return launch_bwd_vec<N, DT, 4, 2, 3>(c, k, V);
     }
 }
 
-template <int N, int DT>
-cudaError_t bwd_n(const BwdCall& c) {
+template <int N, int DT, class Coeffs>
+cudaError_t bwd_n(const BwdCall& c, const Coeffs& k) {
     switch (c.path) {
-        case kPathVec32: return bwd_vec32<N, DT>(c);
-        case kPathVec16: return bwd_vec16<N, DT>(c);
+        case kPathVec32: return bwd_vec32<N, DT>(c, k);
+        case kPathVec16: return bwd_vec16<N, DT>(c, k);
         case kPathPair: {
             const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
-            return launch(agg_bwd_staged_kernel<N, DT, true>, blocks, kLanes, c.stream,
-                          static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.residual), c.pre,
-                          static_cast<uint16_t*>(c.gres), c.gpre, c.T, c.H);
+            return launch(agg_bwd_staged_kernel<N, DT, true, Coeffs>, blocks, kLanes, c.stream,
+                          static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.residual), k,
+                          static_cast<uint16_t*>(c.gres), c.T, c.H);
         }
         default: {
             const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
-            return launch(agg_bwd_staged_kernel<N, DT, false>, blocks, kLanes, c.stream,
-                          static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.residual), c.pre,
-                          static_cast<uint16_t*>(c.gres), c.gpre, c.T, c.H);
+            return launch(agg_bwd_staged_kernel<N, DT, false, Coeffs>, blocks, kLanes, c.stream,
+                          static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.residual), k,
+                          static_cast<uint16_t*>(c.gres), c.T, c.H);
         }
     }
 }
 
-template <int DT>
-cudaError_t bwd_dispatch(const BwdCall& c) {
+template <int DT, class Coeffs>
+cudaError_t bwd_dispatch(const BwdCall& c, const Coeffs& k) {
     switch (c.n) {
-        case 1: return bwd_n<1, DT>(c);
-        case 2: return bwd_n<2, DT>(c);
-        case 4: return bwd_n<4, DT>(c);
-        default: return bwd_n<8, DT>(c);
+        case 1: return bwd_n<1, DT>(c, k);
+        case 2: return bwd_n<2, DT>(c, k);
+        case 4: return bwd_n<4, DT>(c, k);
+        default: return bwd_n<8, DT>(c, k);
     }
 }
 

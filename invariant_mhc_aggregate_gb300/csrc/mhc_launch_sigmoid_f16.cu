@@ -1,0 +1,8 @@
+// Instantiates the launch layer for binary16 storage with pre computed in the
+// kernels from the mix.
+#include "mhc_launch.cuh"
+
+namespace mhc {
+cudaError_t fwd_f16(const FwdCall& c, const SigmoidCoeffs& k) { return fwd_dispatch<kF16>(c, k); }
+cudaError_t bwd_f16(const BwdCall& c, const SigmoidCoeffs& k) { return bwd_dispatch<kF16>(c, k); }
+}  // namespace mhc

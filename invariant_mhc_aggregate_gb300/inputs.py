@@ -19,6 +19,16 @@ recipe          values
 backward ``g``  g ~ N(0,1) rounded to BF16, drawn after residual and pre
 ==============  =====================================================================
 
+For the pre coefficients computed from the mix (``coeff_inputs``): ``mix``
+``[T,n]`` FP32, ``alpha`` ``[1]`` and ``b`` ``[n]``:
+
+==============  =====================================================================
+``normal``      mix ~ N(0,1); alpha ~ U(0.5, 2); b ~ 0.5*N(0,1)
+``wide``        mix ~ 16*N(0,1), then 5% of entries set to exactly 0.0 and 2% to
+                +-100 (sigmoid saturates, 1 - sigmoid underflows toward the
+                subnormal range); alpha and b as ``normal``
+==============  =====================================================================
+
 Every draw comes from one ``torch.Generator`` seeded with the workload's seed,
 in a fixed order (residual, pre, masks, g), so a (recipe, T, H, seed, device)
 tuple always gives the same bytes on a given PyTorch build.
@@ -31,6 +41,7 @@ from dataclasses import dataclass
 import torch
 
 RECIPES = ("normal", "ragged", "decode")
+COEFF_RECIPES = ("normal", "wide")
 
 
 @dataclass(frozen=True)
@@ -92,6 +103,26 @@ def backward_inputs(T: int, H: int, recipe: str = "normal", seed: int = 4,
     residual, pre = _draw_forward(T, H, recipe, gen, device, n, dtype)
     g = torch.randn((T, H), generator=gen, device=device, dtype=torch.float32)
     return g.to(dtype), residual, pre
+
+
+def coeff_inputs(T: int, n: int = 4, recipe: str = "normal", seed: int = 5,
+                 device="cpu") -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(mix fp32 [T,n], alpha fp32 [1], b fp32 [n]) drawn on ``device``."""
+    if recipe not in COEFF_RECIPES:
+        raise ValueError(f"unknown recipe {recipe!r}; expected one of {COEFF_RECIPES}")
+    gen = _generator(device, seed)
+    f32 = torch.float32
+    mix = torch.randn((T, n), generator=gen, device=device, dtype=f32)
+    alpha = 0.5 + 1.5 * torch.rand((1,), generator=gen, device=device, dtype=f32)
+    b = 0.5 * torch.randn((n,), generator=gen, device=device, dtype=f32)
+    if recipe == "wide":
+        mix.mul_(16.0)
+        u = torch.rand((T, n), generator=gen, device=device, dtype=f32)
+        sign = torch.where(torch.rand((T, n), generator=gen, device=device, dtype=f32) < 0.5,
+                           -1.0, 1.0)
+        mix = torch.where(u < 0.05, torch.zeros_like(mix), mix)
+        mix = torch.where((u >= 0.05) & (u < 0.07), 100.0 * sign, mix)
+    return mix.contiguous(), alpha, b
 
 
 def _draw_forward(T, H, recipe, gen, device, n=4, dtype=torch.bfloat16):

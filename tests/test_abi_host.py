@@ -50,7 +50,7 @@ def test_only_the_c_abi_is_exported():
 
 
 def test_abi_version(lib):
-    assert lib.mhc_h_aggregate_abi_version() == 2
+    assert lib.mhc_h_aggregate_abi_version() == 3
 
 
 def test_status_strings(lib):
@@ -255,3 +255,73 @@ def test_general_invalid_arguments(lib):
     assert binding.agg_bwd_raw(*bargs, 0, 1, 64, binding.MHC_DTYPE_BF16) == binding.MHC_OK
     # byte count of an n = 8 residual overflows int64
     assert binding.agg_fwd_raw(*args, 1 << 31, 8, 1 << 29, binding.MHC_DTYPE_BF16) == binding.MHC_ERR_INVALID_ARG
+
+
+# --- the pre coefficients computed from the mix (sigmoid): rejected calls
+
+def test_pre_sigmoid_invalid_arguments(lib):
+    mix, alpha, b, pre = A, A + GAP, A + 2 * GAP, A + 3 * GAP
+    assert binding.pre_sigmoid_raw(mix, alpha, b, pre, 4, 3) == binding.MHC_ERR_UNSUPPORTED
+    assert binding.pre_sigmoid_raw(mix, alpha, b, pre, -1, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.pre_sigmoid_raw(0, 0, 0, 0, 0, 4) == binding.MHC_OK
+    assert binding.pre_sigmoid_raw(0, alpha, b, pre, 4, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.pre_sigmoid_raw(mix, 0, b, pre, 4, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.pre_sigmoid_raw(mix, alpha, 0, pre, 4, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.pre_sigmoid_raw(mix, alpha, b + 2, pre, 4, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.pre_sigmoid_raw(mix, alpha, b, mix + 16, 4, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.pre_sigmoid_raw(mix, alpha, pre + 8, pre, 4, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.pre_sigmoid_raw(mix, pre + 60, b, pre, 4, 4) == binding.MHC_ERR_INVALID_ARG
+
+
+def test_aggregate_sigmoid_fwd_invalid_arguments(lib):
+    r, mix, alpha, b, out = A, A + GAP, A + 2 * GAP, A + 3 * GAP, A + 4 * GAP
+    bf16 = binding.MHC_DTYPE_BF16
+    assert binding.agg_sigmoid_fwd_raw(r, mix, alpha, b, out, 4, 4, 64, 7) == binding.MHC_ERR_INVALID_ARG
+    assert binding.agg_sigmoid_fwd_raw(r, mix, alpha, b, out, 4, 3, 64, bf16) == binding.MHC_ERR_UNSUPPORTED
+    assert binding.agg_sigmoid_fwd_raw(0, 0, 0, 0, 0, 0, 4, 64, bf16) == binding.MHC_OK
+    assert binding.agg_sigmoid_fwd_raw(r, mix, 0, b, out, 4, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG
+    assert binding.agg_sigmoid_fwd_raw(r, mix, alpha, 0, out, 4, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG
+    assert binding.agg_sigmoid_fwd_raw(r, mix, alpha, b + 1, out, 4, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG
+    assert binding.agg_sigmoid_fwd_raw(r, mix, out + 64, b, out, 4, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG
+    assert binding.agg_sigmoid_fwd_raw(r, mix, alpha, out + 4, out, 4, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG
+    assert binding.agg_sigmoid_fwd_raw(r, out, alpha, b, out, 4, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG
+
+
+def test_aggregate_sigmoid_bwd_invalid_arguments(lib):
+    g, r, mix, alpha, b = A, A + GAP, A + 2 * GAP, A + 3 * GAP, A + 4 * GAP
+    gr, gz, gm = A + 5 * GAP, A + 6 * GAP, A + 7 * GAP
+    bf16 = binding.MHC_DTYPE_BF16
+
+    def call(**kw):
+        a = dict(g=g, r=r, mix=mix, alpha=alpha, b=b, gr=gr, gz=gz, gm=gm, T=4, n=4, H=64, dt=bf16)
+        a.update(kw)
+        return binding.agg_sigmoid_bwd_raw(a["g"], a["r"], a["mix"], a["alpha"], a["b"], a["gr"],
+                                           a["gz"], a["gm"], a["T"], a["n"], a["H"], a["dt"])
+
+    assert call(n=6) == binding.MHC_ERR_UNSUPPORTED
+    assert call(dt=5) == binding.MHC_ERR_INVALID_ARG
+    assert call(T=0, g=0, r=0, mix=0, alpha=0, b=0, gr=0, gz=0, gm=0) == binding.MHC_OK
+    for name in ("g", "r", "mix", "alpha", "b", "gr", "gz", "gm"):
+        assert call(**{name: 0}) == binding.MHC_ERR_INVALID_ARG, name
+    assert call(gm=gm + 2) == binding.MHC_ERR_INVALID_ARG
+    assert call(gm=gz + 32) == binding.MHC_ERR_INVALID_ARG        # grad_mix overlaps grad_z
+    assert call(gm=mix) == binding.MHC_ERR_INVALID_ARG            # grad_mix overlaps mix
+    assert call(gm=gr + 128) == binding.MHC_ERR_INVALID_ARG       # grad_mix overlaps grad_residual
+    assert call(gz=mix + 16) == binding.MHC_ERR_INVALID_ARG       # grad_z overlaps mix
+    assert call(b=gz + 8) == binding.MHC_ERR_INVALID_ARG          # b overlaps grad_z
+    assert call(alpha=gm) == binding.MHC_ERR_INVALID_ARG          # alpha overlaps grad_mix
+    assert call(alpha=gr + 2 * 64) == binding.MHC_ERR_INVALID_ARG  # alpha inside grad_residual
+
+
+def test_sigmoid_param_grad_invalid_arguments(lib):
+    gz, mix, gb, ga = A, A + GAP, A + 2 * GAP, A + 3 * GAP
+    assert binding.sigmoid_param_grad_raw(gz, mix, gb, ga, 8, 5) == binding.MHC_ERR_UNSUPPORTED
+    assert binding.sigmoid_param_grad_raw(gz, mix, gb, ga, -1, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.sigmoid_param_grad_raw(gz, mix, 0, ga, 8, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.sigmoid_param_grad_raw(gz, mix, gb, 0, 8, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.sigmoid_param_grad_raw(0, mix, gb, ga, 8, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.sigmoid_param_grad_raw(gz, 0, gb, ga, 8, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.sigmoid_param_grad_raw(gz, mix, gb, gb + 12, 8, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.sigmoid_param_grad_raw(gz, mix, gz + 64, ga, 8, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.sigmoid_param_grad_raw(gz, mix, gb, mix + 4, 8, 4) == binding.MHC_ERR_INVALID_ARG
+    assert binding.sigmoid_param_grad_raw(gz, mix, gb + 2, ga, 8, 4) == binding.MHC_ERR_INVALID_ARG
