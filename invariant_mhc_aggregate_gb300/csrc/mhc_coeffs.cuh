@@ -102,10 +102,18 @@ __device__ __forceinline__ void ld_row(const float* p, bool vec, float (&out)[N]
     }
 }
 
+// A kernel either has each thread load (and, for the sigmoid, compute) the
+// coefficients it needs (kBlockTable false: load() then to_pre()), or has a
+// few threads compute each token's values once into shared memory for the
+// whole block (kBlockTable true: mix_at() early, pre_from() later), which is
+// what the sigmoid wants: its binary32 evaluation costs about 70
+// instructions per value, too many to repeat in every thread of a token.
 struct PlainCoeffs {
     const float* pre;   // [T,n]
     float* grad_pre;    // [T,n] (backward only)
     bool vec;           // pre aligned to min(16, 4n) bytes
+
+    static constexpr bool kBlockTable = false;
 
     // The same source for the tokens from t0 on (offset = n * t0 values).
     __host__ __device__ PlainCoeffs shifted(uint64_t offset) const {
@@ -135,6 +143,18 @@ struct SigmoidCoeffs {
     float* grad_z;      // [T,n] (backward only)
     float* grad_mix;    // [T,n] (backward only)
     bool vec;           // mix aligned to min(16, 4n) bytes
+
+    static constexpr bool kBlockTable = true;
+
+    // mix value idx = n*t + k of the [T,n] mix (issued early: the kernels
+    // fetch it before their bulk loads and turn it into pre afterwards) ...
+    __device__ __forceinline__ float mix_at(uint64_t idx) const { return __ldg(mix + idx); }
+    // ... and pre for that value.
+    __device__ __forceinline__ float pre_from(float m, int k) const {
+        float s, one_minus;
+        sigmoid32(pre_activation(__ldg(alpha), m, __ldg(b + k)), s, one_minus);
+        return s;
+    }
 
     __host__ __device__ SigmoidCoeffs shifted(uint64_t offset) const {
         return SigmoidCoeffs{mix + offset, alpha, b, grad_z ? grad_z + offset : nullptr,

@@ -225,22 +225,52 @@ agg_fwd_vec_kernel(const Words<NW>* __restrict__ res, Coeffs coeffs, Words<NW>* 
     const uint32_t first = blockIdx.x * uint32_t(BLOCK * UNROLL) + threadIdx.x;
     Words<NW> r[UNROLL][N];
     float p[UNROLL][N];
+    uint32_t tok[UNROLL];
+    // kBlockTable: the block's tokens t0 .. and count = N * (number of them);
+    // each thread fetches its first mix value before the residual loads.
+    uint32_t t0 = 0, count = 0;
+    float m0 = 0.0f;
+    if constexpr (Coeffs::kBlockTable) {
+        const uint32_t b0 = blockIdx.x * uint32_t(BLOCK * UNROLL);
+        const uint32_t b1 = min(b0 + uint32_t(BLOCK * UNROLL), n_vec) - 1;
+        t0 = fastdiv_u32(b0, divV);
+        count = (fastdiv_u32(b1, divV) - t0 + 1) * uint32_t(N);
+        if (threadIdx.x < count) m0 = coeffs.mix_at(uint64_t(t0) * N + threadIdx.x);
+    }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
         const uint32_t i = first + uint32_t(u * BLOCK);
         if (i < n_vec) {
             const uint32_t t = fastdiv_u32(i, divV);
+            tok[u] = t;
             const Words<NW>* src = res + (uint64_t(i) + uint64_t(N - 1) * uint64_t(t) * V);
 #pragma unroll
             for (int k = 0; k < N; ++k) r[u][k] = ld_stream<NW>(src + uint64_t(k) * V);
-            coeffs.template load<N>(t, p[u]);
+            if constexpr (!Coeffs::kBlockTable) coeffs.template load<N>(t, p[u]);
+        }
+    }
+    if constexpr (Coeffs::kBlockTable) {
+        // The coefficients of the (at most BLOCK*UNROLL + 1) tokens the block
+        // touches, each computed once, while the residual loads are in flight.
+        __shared__ float table[(BLOCK * UNROLL + 1) * N];
+        for (uint32_t j = threadIdx.x; j < count; j += BLOCK) {
+            const float m = (j == threadIdx.x) ? m0 : coeffs.mix_at(uint64_t(t0) * N + j);
+            table[j] = coeffs.pre_from(m, int(j % N));
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            if (first + uint32_t(u * BLOCK) < n_vec) {
+#pragma unroll
+                for (int k = 0; k < N; ++k) p[u][k] = table[(tok[u] - t0) * N + k];
+            }
         }
     }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
         const uint32_t i = first + uint32_t(u * BLOCK);
         if (i < n_vec) {
-            coeffs.template to_pre<N>(p[u]);
+            if constexpr (!Coeffs::kBlockTable) coeffs.template to_pre<N>(p[u]);
             Words<NW> o;
 #pragma unroll
             for (int e = 0; e < NW; ++e) {
@@ -264,16 +294,39 @@ constexpr int kNarrowBlock = 256;
 constexpr int kNarrowPerThread = 8;
 constexpr int kNarrowSeg = kNarrowBlock * kNarrowPerThread;
 
+// Token t's pre in p, for a block whose threads all run the same token loop,
+// once the token's loads are issued.  With a block table, threads 0..N-1
+// compute the N values into table[parity] and the block reads them after a
+// barrier (the two halves alternate, so one barrier per token suffices);
+// otherwise every thread finishes what load() fetched.
+template <int N, class Coeffs>
+__device__ __forceinline__ void token_pre(const Coeffs& coeffs, uint64_t t, float (&p)[N],
+                                          float (*table)[N], int& parity) {
+    if constexpr (Coeffs::kBlockTable) {
+        if (threadIdx.x < N)
+            table[parity][threadIdx.x] =
+                coeffs.pre_from(coeffs.mix_at(uint64_t(N) * t + threadIdx.x), int(threadIdx.x));
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < N; ++k) p[k] = table[parity][k];
+        parity ^= 1;
+    } else {
+        coeffs.template to_pre<N>(p);
+    }
+}
+
 // 4-byte path: P = H/2 pairs per row.
 template <int N, int DT, class Coeffs>
 __global__ void __launch_bounds__(kNarrowBlock)
 agg_fwd_pair_kernel(const uint32_t* __restrict__ res2, Coeffs coeffs, uint32_t* __restrict__ out2,
                     uint64_t T, uint64_t P) {
+    __shared__ float table[2][N];   // kBlockTable: the token's pre, by loop parity
     pdl_enter();
     const uint64_t base = uint64_t(blockIdx.x) * kNarrowSeg + threadIdx.x;
+    int parity = 0;
     for (uint64_t t = blockIdx.y; t < T; t += gridDim.y) {
         float p[N];
-        coeffs.template load<N>(t, p);
+        if constexpr (!Coeffs::kBlockTable) coeffs.template load<N>(t, p);
         const uint32_t* src = res2 + uint64_t(N) * t * P;
         uint32_t w[kNarrowPerThread][N];
 #pragma unroll
@@ -284,7 +337,7 @@ agg_fwd_pair_kernel(const uint32_t* __restrict__ res2, Coeffs coeffs, uint32_t* 
                 for (int k = 0; k < N; ++k) w[e][k] = ld_stream4(src + uint64_t(k) * P + c);
             }
         }
-        coeffs.template to_pre<N>(p);
+        token_pre<N>(coeffs, t, p, table, parity);
 #pragma unroll
         for (int e = 0; e < kNarrowPerThread; ++e) {
             const uint64_t c = base + uint64_t(e) * kNarrowBlock;
@@ -298,11 +351,13 @@ template <int N, int DT, class Coeffs>
 __global__ void __launch_bounds__(kNarrowBlock)
 agg_fwd_element_kernel(const uint16_t* __restrict__ res, Coeffs coeffs, uint16_t* __restrict__ out,
                        uint64_t T, uint64_t H) {
+    __shared__ float table[2][N];
     pdl_enter();
     const uint64_t base = uint64_t(blockIdx.x) * kNarrowSeg + threadIdx.x;
+    int parity = 0;
     for (uint64_t t = blockIdx.y; t < T; t += gridDim.y) {
         float p[N];
-        coeffs.template load<N>(t, p);
+        if constexpr (!Coeffs::kBlockTable) coeffs.template load<N>(t, p);
         const uint16_t* src = res + uint64_t(N) * t * H;
         uint16_t v[kNarrowPerThread][N];
 #pragma unroll
@@ -313,7 +368,7 @@ agg_fwd_element_kernel(const uint16_t* __restrict__ res, Coeffs coeffs, uint16_t
                 for (int k = 0; k < N; ++k) v[e][k] = ld_stream2(src + uint64_t(k) * H + h);
             }
         }
-        coeffs.template to_pre<N>(p);
+        token_pre<N>(coeffs, t, p, table, parity);
 #pragma unroll
         for (int e = 0; e < kNarrowPerThread; ++e) {
             const uint64_t h = base + uint64_t(e) * kNarrowBlock;
@@ -416,11 +471,17 @@ agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict_
     constexpr int LPT = NW / 4;
     constexpr uint32_t B = kLanes / LPT;
     __shared__ float red[kGroups][N];
+    __shared__ float table[N];   // kBlockTable: the token's pre
     pdl_enter();
     const uint32_t j = threadIdx.x;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
         float pk[N];
-        coeffs.template load<N>(t, pk);
+        float m_own = 0.0f;   // kBlockTable: thread j < N fetches mix[t, j] first
+        if constexpr (Coeffs::kBlockTable) {
+            if (j < N) m_own = coeffs.mix_at(uint64_t(N) * t + j);
+        } else {
+            coeffs.template load<N>(t, pk);
+        }
         bool pk_ready = false;
         const Words<NW>* gt = g + t * V;
         const Words<NW>* rt = res + uint64_t(N) * t * V;
@@ -430,7 +491,11 @@ agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict_
         for (int l = 0; l < LPT; ++l)
 #pragma unroll
             for (int k = 0; k < N; ++k) acc[l][k] = 0.0f;
-        for (uint32_t v0 = j; v0 < V; v0 += B * BATCH) {
+        // With a block table the first pass runs in every thread (its loads
+        // are guarded), so that all of them meet the barrier that publishes
+        // the table; the fold's barriers keep the table until the next token.
+        for (uint32_t v0 = j; Coeffs::kBlockTable ? (v0 < V || !pk_ready) : (v0 < V);
+             v0 += B * BATCH) {
             Words<NW> gv[BATCH];
             Words<NW> rv[BATCH][N];
 #pragma unroll
@@ -443,7 +508,14 @@ agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict_
                 }
             }
             if (!pk_ready) {
-                coeffs.template to_pre<N>(pk);
+                if constexpr (Coeffs::kBlockTable) {
+                    if (j < N) table[j] = coeffs.pre_from(m_own, int(j));
+                    __syncthreads();
+#pragma unroll
+                    for (int k = 0; k < N; ++k) pk[k] = table[k];
+                } else {
+                    coeffs.template to_pre<N>(pk);
+                }
                 pk_ready = true;
             }
 #pragma unroll
@@ -480,6 +552,7 @@ agg_bwd_staged_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict
     constexpr int kUnit = PAIRS ? 2 : 1;             // values per access
     constexpr int kPer = kSeg / (kUnit * kLanes);    // accesses per thread per row
     __shared__ float red[kGroups][N];
+    __shared__ float table[N];   // kBlockTable: the token's pre
     __shared__ __align__(16) uint16_t sg[kSeg];
     __shared__ __align__(16) uint16_t sr[N][kSeg];
     pdl_enter();
@@ -488,7 +561,12 @@ agg_bwd_staged_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict
     const uint64_t U = H / kUnit;                    // units per row
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
         float pk[N];
-        coeffs.template load<N>(t, pk);
+        float m_own = 0.0f;   // kBlockTable: thread j < N fetches mix[t, j] first
+        if constexpr (Coeffs::kBlockTable) {
+            if (j < N) m_own = coeffs.mix_at(uint64_t(N) * t + j);
+        } else {
+            coeffs.template load<N>(t, pk);
+        }
         bool pk_ready = false;
         const uint16_t* gt = g + t * H;
         const uint16_t* rt = res + uint64_t(N) * t * H;
@@ -516,9 +594,17 @@ agg_bwd_staged_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict
                         sr[k][s] = (u < U) ? ld_stream2(rt + uint64_t(k) * H + u) : uint16_t(0);
                 }
             }
+            if constexpr (Coeffs::kBlockTable) {
+                if (!pk_ready && j < N) table[j] = coeffs.pre_from(m_own, int(j));
+            }
             __syncthreads();
             if (!pk_ready) {
-                coeffs.template to_pre<N>(pk);
+                if constexpr (Coeffs::kBlockTable) {
+#pragma unroll
+                    for (int k = 0; k < N; ++k) pk[k] = table[k];
+                } else {
+                    coeffs.template to_pre<N>(pk);
+                }
                 pk_ready = true;
             }
             if (base / 8 + j < C) {
@@ -577,104 +663,140 @@ pre_sigmoid_kernel(const float* __restrict__ mix, const float* __restrict__ alph
     }
 }
 
+// Thread-block cluster helpers (inline PTX): this CTA's rank in its cluster,
+// the cluster-wide barrier (release / acquire: shared-memory writes made
+// before it, to any CTA of the cluster, are visible after it), and a store
+// into another CTA's shared memory.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_cluster(const float* local, uint32_t rank, float v) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" : : "r"(remote), "f"(v) : "memory");
+}
+
 // grad_b[k] = sum over t of grad_z[t,k] and grad_alpha = sum over t of
 // tree_N(grad_z[t,k] * mix[t,k]), both in ORDER-256 with tokens in place of h:
 // chunk c = tokens 8c .. 8c+7 (+0 past T) summed by the chunk tree; lane j
 // adds the partials of chunks j, j + 256, ... in increasing order from +0;
 // groups of 32 lanes fold with strides 16 .. 1, the 8 groups with 4, 2, 1.
 //
-// One block of P = param_threads<N>() threads (a reduction over T has no
-// per-token parallelism left to give other blocks without a cross-block
-// exchange).  Each round, thread i computes the partials of chunk c0 + i
-// (holding 16N loaded values, hence fewer threads for larger N) into shared
-// memory; lane j (thread j < 256) then adds the partials of its chunks
-// c0 + j, c0 + 256 + j, ... < c0 + P, in that order.
-template <int N>
-__host__ __device__ constexpr int param_threads() { return N <= 2 ? 1024 : 2048 / N; }
+// One cluster of 8 CTAs, CTA w owning the lanes 32w .. 32w+31 of group w: its
+// chunks are 256m + 32w + i (i < 32), i.e. the 256 consecutive tokens
+// 8(256m + 32w) .. + 255 of every "m-block" m.  Each round, warp q of the CTA
+// takes m-block m0 + q: lane l loads tokens 32e + l (e < 8) of it (32
+// consecutive rows per warp load), and xor shuffles over 8 lanes build the
+// chunk trees, leaving chunk 4e + l/8 in lane l (l % 8 == 0); the partials
+// go to shared memory, and warp 0, lane i, adds those of chunk i for the
+// round's m-blocks in increasing m.  Warp 0 then folds the group with xor
+// shuffles, lane 0 stores the group value into CTA 0's shared memory, and
+// after a cluster barrier CTA 0 folds the 8 group values and writes the
+// result.  No global scratch, no atomics; the exchange uses two hardware
+// cluster barriers (all 8 CTAs are resident together by construction).
+constexpr int kParamClusterCtas = kGroups;   // 8
+constexpr int kParamWarps = 8;
+constexpr int kParamThreads = 32 * kParamWarps;
 
 template <int N>
-__global__ void __launch_bounds__(param_threads<N>())
+__global__ void __launch_bounds__(kParamThreads)
 sigmoid_param_grad_kernel(const float* __restrict__ grad_z, const float* __restrict__ mix,
                           float* __restrict__ grad_b, float* __restrict__ grad_alpha, uint64_t T,
                           bool vec) {
-    constexpr int kParamThreads = param_threads<N>();
     constexpr int M = N + 1;   // grad_b[0 .. N-1], grad_alpha
-    __shared__ float part[kParamThreads][M];
-    __shared__ float red[kGroups][M];
+    __shared__ float part[kParamWarps][32][M];
+    __shared__ float groups[kParamClusterCtas][M];   // used in CTA 0
     pdl_enter();
-    const uint32_t i = threadIdx.x;
-    const uint64_t C = (T + 7) / 8;
+    const uint32_t w = cluster_rank();
+    const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint64_t n_mblocks = ((T + 7) / 8 + 255) / 256;
     float acc[M];
 #pragma unroll
     for (int k = 0; k < M; ++k) acc[k] = 0.0f;
-    for (uint64_t c0 = 0; c0 < C; c0 += kParamThreads) {
-        const uint64_t c = c0 + i;
-        if (c < C) {
-            float gz[8][N], m[8][N];
+    for (uint64_t m0 = 0; m0 < n_mblocks; m0 += kParamWarps) {
+        const uint64_t m = m0 + warp;
+        const uint64_t tbase = 8 * (256 * m + 32 * uint64_t(w));
+        float gz[8][N], mx[8][N];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint64_t t = 8 * c + e;
-                if (t < T) {
-                    ld_row<N>(grad_z + uint64_t(N) * t, vec, gz[e]);
-                    ld_row<N>(mix + uint64_t(N) * t, vec, m[e]);
-                } else {
+        for (int e = 0; e < 8; ++e) {
+            const uint64_t t = tbase + 32 * e + lane;
+            if (m < n_mblocks && t < T) {
+                ld_row<N>(grad_z + uint64_t(N) * t, vec, gz[e]);
+                ld_row<N>(mix + uint64_t(N) * t, vec, mx[e]);
+            } else {
 #pragma unroll
-                    for (int k = 0; k < N; ++k) gz[e][k] = m[e][k] = 0.0f;
-                }
+                for (int k = 0; k < N; ++k) gz[e][k] = mx[e][k] = 0.0f;
             }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float v[M];
+            float prod[N];
 #pragma unroll
             for (int k = 0; k < N; ++k) {
-                float q[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) q[e] = gz[e][k];
-                part[i][k] = tree_sum<8>(q);
+                v[k] = gz[e][k];
+                prod[k] = __fmul_rn(gz[e][k], mx[e][k]);
             }
-            float qa[8];
+            v[N] = tree_sum<N>(prod);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                float prod[N];
+            for (int sh = 1; sh <= 4; sh <<= 1) {
 #pragma unroll
-                for (int k = 0; k < N; ++k) prod[k] = __fmul_rn(gz[e][k], m[e][k]);
-                qa[e] = tree_sum<N>(prod);
+                for (int k = 0; k < M; ++k) v[k] = __fadd_rn(v[k], __shfl_xor_sync(0xffffffffu, v[k], sh));
             }
-            part[i][N] = tree_sum<8>(qa);
+            if ((lane % 8) == 0) {
+#pragma unroll
+                for (int k = 0; k < M; ++k) part[warp][4 * e + lane / 8][k] = v[k];
+            }
         }
         __syncthreads();
-        if (i < kLanes) {
+        if (warp == 0) {
 #pragma unroll
-            for (int h = 0; h < kParamThreads / kLanes; ++h) {
-                if (c0 + uint64_t(h) * kLanes + i < C) {
+            for (int q = 0; q < kParamWarps; ++q) {
+                if (m0 + q < n_mblocks) {
 #pragma unroll
-                    for (int k = 0; k < M; ++k) acc[k] = __fadd_rn(acc[k], part[h * kLanes + i][k]);
+                    for (int k = 0; k < M; ++k) acc[k] = __fadd_rn(acc[k], part[q][lane][k]);
                 }
             }
         }
         __syncthreads();   // part[] is refilled by the next round
     }
-    if (i < kLanes) {      // warps 0 .. 7 are the 8 groups of 32 lanes
+    // every CTA of the cluster is running (and CTA 0's shared memory live)
+    // before any of them writes into CTA 0's shared memory
+    cluster_barrier();
+    if (warp == 0) {
 #pragma unroll
         for (int k = 0; k < M; ++k) {
 #pragma unroll
-            for (int s = 16; s >= 1; s >>= 1)
-                acc[k] = __fadd_rn(acc[k], __shfl_xor_sync(0xffffffffu, acc[k], s));
+            for (int sh = 16; sh >= 1; sh >>= 1)
+                acc[k] = __fadd_rn(acc[k], __shfl_xor_sync(0xffffffffu, acc[k], sh));
         }
-        if ((i % 32) == 0) {
+        if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < M; ++k) red[i / 32][k] = acc[k];
+            for (int k = 0; k < M; ++k) st_shared_cluster(&groups[w][k], 0, acc[k]);
         }
     }
-    __syncthreads();
-    if (i < uint32_t(M)) {
-        float w[kGroups];
+    cluster_barrier();
+    if (w == 0 && threadIdx.x < uint32_t(M)) {
+        const uint32_t k = threadIdx.x;
+        float g[kParamClusterCtas];
 #pragma unroll
-        for (int g = 0; g < kGroups; ++g) w[g] = red[g][i];
+        for (int i = 0; i < kParamClusterCtas; ++i) g[i] = groups[i][k];
 #pragma unroll
-        for (int s = kGroups / 2; s >= 1; s >>= 1) {
+        for (int s2 = kParamClusterCtas / 2; s2 >= 1; s2 >>= 1) {
 #pragma unroll
-            for (int g = 0; g < s; ++g) w[g] = __fadd_rn(w[g], w[g + s]);
+            for (int i = 0; i < s2; ++i) g[i] = __fadd_rn(g[i], g[i + s2]);
         }
-        if (i < uint32_t(N)) grad_b[i] = w[0];
-        else grad_alpha[0] = w[0];
+        if (k < uint32_t(N)) grad_b[k] = g[0];
+        else grad_alpha[0] = g[0];
     }
 }
 

@@ -22,11 +22,27 @@ cudaError_t pre_sigmoid(const float* mix, const float* alpha, const float* b, fl
     }
 }
 
+// One cluster of 8 CTAs (see sigmoid_param_grad_kernel), with programmatic
+// stream serialization like every launch here.
 template <int N>
 static cudaError_t param_grad_n(const float* grad_z, const float* mix, float* grad_b,
                                 float* grad_alpha, uint64_t T, bool vec, cudaStream_t stream) {
-    return launch(sigmoid_param_grad_kernel<N>, 1, param_threads<N>(), stream, grad_z, mix, grad_b,
-                  grad_alpha, T, vec);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kParamClusterCtas);
+    cfg.blockDim = dim3(kParamThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kParamClusterCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, sigmoid_param_grad_kernel<N>, grad_z, mix, grad_b, grad_alpha,
+                              T, vec);
 }
 
 cudaError_t sigmoid_param_grad(const float* grad_z, const float* mix, float* grad_b,
