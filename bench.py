@@ -624,7 +624,7 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
                     "note": "grad_residual, grad_z, grad_mix; bytes T*(18H+48)",
                     "steady": {"us": us_b, "sets": ns, **entry_for(us_b, bb)}})
     results.append({"workload": "sigmoid_param_grad_n4", "dir": "bwd", "T": T,
-                    "note": "grad_b and grad_alpha summed over the tokens (one block); "
+                    "note": "grad_b and grad_alpha summed over the tokens (one cluster of 8 CTAs); "
                             "bytes T*32, latency-bound",
                     "steady": {"us": us_p, "sets": ns}})
     del g, r, mix, sets, fsets, bsets, psets

@@ -26,7 +26,8 @@ def test_split_launch_beyond_2e31_vectors():
     2^31 vectors or more into launches over consecutive token ranges.  With
     n = 1, H = 16384 and the 16-byte path, T = 2^20 tokens make exactly 2^31
     vectors: the second launch holds the last token.  (34 GB residual + 34 GB
-    out on the device.)"""
+    out on the device.)  Checked for pre given and for pre computed from the
+    mix."""
     T, H = 1 << 20, 16384
     dev = torch.device("cuda")
     buf_r = torch.empty(T * H + 8, dtype=torch.bfloat16, device=dev)
@@ -48,6 +49,17 @@ def test_split_launch_beyond_2e31_vectors():
     for t in (0, 1, boundary - 1, boundary, T - 1):
         want = oracle.aggregate_fwd(u16(res[t:t + 1]), f32(pre[t:t + 1]), "bf16")
         assert_bytes_equal(u16(out[t:t + 1]), want, f"token {t}")
+    # the same split with pre computed from the mix: the second launch's mix
+    # rows start at the boundary token
+    mix = torch.randn((T, 1), generator=gen, device=dev) * 3
+    alpha = torch.full((1,), 1.25, device=dev)
+    b = torch.full((1,), -0.5, device=dev)
+    binding.mhc_aggregate_sigmoid_fwd(res, mix, alpha, b, out)
+    torch.cuda.synchronize()
+    for t in (0, boundary - 1, boundary, boundary + 1, T - 1):
+        want = oracle.aggregate_sigmoid_fwd(u16(res[t:t + 1]), f32(mix[t:t + 1]), np.float32(1.25),
+                                            np.float32([-0.5]), "bf16")
+        assert_bytes_equal(u16(out[t:t + 1]), want, f"sigmoid coefficients, token {t}")
     del buf_r, buf_o, res, out, flat
     torch.cuda.empty_cache()
 
