@@ -26,7 +26,8 @@ SOURCES = [os.path.join(CSRC, f) for f in
            ("mhc_h_aggregate.cu", "mhc_launch_bf16.cu", "mhc_launch_f16.cu",
             "mhc_launch_sigmoid_bf16.cu", "mhc_launch_sigmoid_f16.cu", "mhc_launch_coeffs.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in
-                  ("fastdiv.cuh", "mhc_coeffs.cuh", "mhc_device.cuh", "mhc_launch.cuh")] \
+                  ("fastdiv.cuh", "mhc_coeffs.cuh", "mhc_device.cuh", "mhc_shift.cuh",
+                   "mhc_launch.cuh")] \
     + [os.path.join(INCLUDE, "mhc_h_aggregate.h")]
 
 ARCH = "sm_103a"
@@ -65,7 +66,7 @@ def source_digest() -> str:
 
 
 KERNEL_FILES = [os.path.join(CSRC, f) for f in
-                ("mhc_device.cuh", "mhc_coeffs.cuh", "fastdiv.cuh", "mhc_launch.cuh",
+                ("mhc_device.cuh", "mhc_coeffs.cuh", "mhc_shift.cuh", "fastdiv.cuh", "mhc_launch.cuh",
                  "mhc_launch_bf16.cu", "mhc_launch_f16.cu", "mhc_launch_sigmoid_bf16.cu",
                  "mhc_launch_sigmoid_f16.cu", "mhc_launch_coeffs.cu")]
 

@@ -30,8 +30,9 @@ MHC_PATH_VEC16 = 0
 MHC_PATH_PAIR = 1
 MHC_PATH_ELEMENT = 2
 MHC_PATH_VEC32 = 3
+MHC_PATH_SHIFT16 = 4
 PATH_NAMES = {MHC_PATH_NONE: "none", MHC_PATH_VEC16: "vec16", MHC_PATH_PAIR: "pair",
-              MHC_PATH_ELEMENT: "element", MHC_PATH_VEC32: "vec32"}
+              MHC_PATH_ELEMENT: "element", MHC_PATH_VEC32: "vec32", MHC_PATH_SHIFT16: "shift16"}
 
 MHC_DTYPE_BF16 = 0
 MHC_DTYPE_F16 = 1

@@ -129,6 +129,11 @@ struct PlainCoeffs {
     // its other loads (nothing to do here).
     template <int N>
     __device__ __forceinline__ void to_pre(float (&)[N]) const {}
+    // Token t's pre in every lane of a warp (all 32 lanes call it).
+    template <int N>
+    __device__ __forceinline__ void warp_pre(uint64_t t, float (&p)[N]) const {
+        ld_row<N>(pre + uint64_t(N) * t, vec, p);
+    }
     // Called by the thread that holds grad_pre[t,k].
     template <int N>
     __device__ __forceinline__ void store_grad(uint64_t t, int k, float gp) const {
@@ -154,6 +159,16 @@ struct SigmoidCoeffs {
         float s, one_minus;
         sigmoid32(pre_activation(__ldg(alpha), m, __ldg(b + k)), s, one_minus);
         return s;
+    }
+    // Token t's pre in every lane of a warp (all 32 lanes call it): lanes
+    // 0 .. N-1 evaluate one sigmoid each, shuffles broadcast them.
+    template <int N>
+    __device__ __forceinline__ void warp_pre(uint64_t t, float (&p)[N]) const {
+        const uint32_t lane = threadIdx.x & 31u;
+        float mine = 0.0f;
+        if (lane < uint32_t(N)) mine = pre_from(mix_at(uint64_t(N) * t + lane), int(lane));
+#pragma unroll
+        for (int k = 0; k < N; ++k) p[k] = __shfl_sync(0xffffffffu, mine, k);
     }
 
     __host__ __device__ SigmoidCoeffs shifted(uint64_t offset) const {

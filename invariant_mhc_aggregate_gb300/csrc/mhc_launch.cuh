@@ -15,6 +15,7 @@ constexpr int kPathVec16 = 0;
 constexpr int kPathPair = 1;
 constexpr int kPathElement = 2;
 constexpr int kPathVec32 = 3;
+constexpr int kPathShift16 = 4;
 
 // The per-token coefficients (pre, or the mix they are computed from) and the
 // per-token coefficient gradients travel in a PlainCoeffs / SigmoidCoeffs
@@ -149,6 +150,26 @@ cudaError_t fwd_n(const FwdCall& c, const Coeffs& k) {
     switch (c.path) {
         case kPathVec32: return fwd_vec<N, DT, 8>(c, k);
         case kPathVec16: return fwd_vec<N, DT, 4>(c, k);
+        case kPathShift16: {
+            // a row's output vectors in nseg equal segments: up to 8 warps x 31 x 2
+            // vectors each (U = 2), or, for rows of fewer than 496 vectors, one
+            // segment of ceil(vectors / 31) warps (U = 1); blocks of 32 x warps threads
+            const uint64_t vecs = shift_row_vectors(c.H);
+            const uint32_t tokens = uint32_t(c.T < 65535 ? c.T : 65535);
+            const auto* r = static_cast<const uint16_t*>(c.residual);
+            auto* o = static_cast<uint16_t*>(c.out);
+            constexpr uint64_t kRun2 = 2 * kShiftWarpVectors;
+            if (vecs >= 8 * kRun2) {
+                const uint64_t nseg = (vecs + 8 * kRun2 - 1) / (8 * kRun2);
+                const uint64_t per_seg = (vecs + nseg - 1) / nseg;
+                const uint32_t warps = uint32_t((per_seg + kRun2 - 1) / kRun2);
+                return launch2d(agg_fwd_shift_kernel<N, DT, 2, Coeffs>, dim3(uint32_t(nseg), tokens),
+                                32 * warps, c.stream, r, k, o, c.T, c.H);
+            }
+            const uint32_t warps = uint32_t((vecs + kShiftWarpVectors - 1) / kShiftWarpVectors);
+            return launch2d(agg_fwd_shift_kernel<N, DT, 1, Coeffs>, dim3(1, tokens), 32 * warps, c.stream,
+                            r, k, o, c.T, c.H);
+        }
         case kPathPair: {
             const uint64_t P = c.H / 2;
             return launch2d(agg_fwd_pair_kernel<N, DT, Coeffs>, narrow_grid(P, c.T), kNarrowBlock, c.stream,
@@ -224,6 +245,12 @@ cudaError_t bwd_n(const BwdCall& c, const Coeffs& k) {
     switch (c.path) {
         case kPathVec32: return bwd_vec32<N, DT>(c, k);
         case kPathVec16: return bwd_vec16<N, DT>(c, k);
+        case kPathShift16: {
+            const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
+            return launch(agg_bwd_shift_kernel<N, DT, Coeffs>, blocks, kShiftBwdThreads, c.stream,
+                          static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.residual), k,
+                          static_cast<uint16_t*>(c.gres), c.T, c.H);
+        }
         case kPathPair: {
             const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
             return launch(agg_bwd_staged_kernel<N, DT, true, Coeffs>, blocks, kLanes, c.stream,

@@ -64,6 +64,11 @@ def _align_of(offset: int) -> int:
     return offset & -offset
 
 
+#: rows of at least this many values that neither a vector path nor the 4-byte
+#: pair path takes use the realigned 16-byte path
+SHIFT_MIN_H = 64
+
+
 def expected_fwd_path(H: int, offsets) -> int:
     a = min(_align_of(offsets[0]), _align_of(offsets[2]))
     if H % 16 == 0 and a >= 32:
@@ -72,6 +77,8 @@ def expected_fwd_path(H: int, offsets) -> int:
         return binding.MHC_PATH_VEC16
     if H % 2 == 0 and a >= 4:
         return binding.MHC_PATH_PAIR
+    if H >= SHIFT_MIN_H:
+        return binding.MHC_PATH_SHIFT16
     return binding.MHC_PATH_ELEMENT
 
 
@@ -83,6 +90,8 @@ def expected_bwd_path(H: int, offsets) -> int:
         return binding.MHC_PATH_VEC16
     if H % 2 == 0 and a >= 4:
         return binding.MHC_PATH_PAIR
+    if H >= SHIFT_MIN_H:
+        return binding.MHC_PATH_SHIFT16
     return binding.MHC_PATH_ELEMENT
 
 

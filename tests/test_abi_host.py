@@ -82,10 +82,14 @@ def test_fwd_path_choice(lib):
     assert fpath(H=4104) == binding.MHC_PATH_VEC16           # H % 16 == 8
     assert fpath(r_off=4) == binding.MHC_PATH_PAIR
     assert fpath(o_off=8) == binding.MHC_PATH_PAIR
-    assert fpath(r_off=2) == binding.MHC_PATH_ELEMENT
+    assert fpath(r_off=2) == binding.MHC_PATH_SHIFT16         # 2-byte aligned, H >= 64: realigned
     assert fpath(H=2050) == binding.MHC_PATH_PAIR
-    assert fpath(H=1279) == binding.MHC_PATH_ELEMENT
-    assert fpath(H=4097) == binding.MHC_PATH_ELEMENT
+    assert fpath(H=1279) == binding.MHC_PATH_SHIFT16          # odd H >= 64: realigned
+    assert fpath(H=4097) == binding.MHC_PATH_SHIFT16
+    assert fpath(H=64, r_off=2) == binding.MHC_PATH_SHIFT16
+    assert fpath(H=62) == binding.MHC_PATH_PAIR
+    assert fpath(H=56, r_off=2) == binding.MHC_PATH_ELEMENT   # shorter rows: 2-byte path
+    assert fpath(H=63) == binding.MHC_PATH_ELEMENT
     assert fpath(r_off=1) == binding.MHC_PATH_NONE           # not BF16 aligned
     assert fpath(p_off=2) == binding.MHC_PATH_NONE           # not FP32 aligned
     assert fpath(T=0) == binding.MHC_PATH_NONE
@@ -99,10 +103,13 @@ def test_bwd_path_choice(lib):
     assert bpath(g_off=16) == binding.MHC_PATH_VEC16
     assert bpath(gr_off=16) == binding.MHC_PATH_VEC16
     assert bpath(H=4104) == binding.MHC_PATH_VEC16
-    assert bpath(g_off=2) == binding.MHC_PATH_ELEMENT
+    assert bpath(g_off=2) == binding.MHC_PATH_SHIFT16
     assert bpath(gr_off=4) == binding.MHC_PATH_PAIR
     assert bpath(H=2050) == binding.MHC_PATH_PAIR
-    assert bpath(H=2050, r_off=2) == binding.MHC_PATH_ELEMENT
+    assert bpath(H=2050, r_off=2) == binding.MHC_PATH_SHIFT16
+    assert bpath(H=1279) == binding.MHC_PATH_SHIFT16
+    assert bpath(H=50) == binding.MHC_PATH_PAIR
+    assert bpath(H=50, r_off=2) == binding.MHC_PATH_ELEMENT
     assert bpath(H=13) == binding.MHC_PATH_ELEMENT
     assert bpath(gp_off=2) == binding.MHC_PATH_NONE
     assert bpath(T=0) == binding.MHC_PATH_NONE
@@ -223,7 +230,9 @@ def test_general_path_choice(lib):
         assert gpath(n) == binding.MHC_PATH_VEC32
         assert gpath(n, r_off=16) == binding.MHC_PATH_VEC16
         assert gpath(n, H=2050) == binding.MHC_PATH_PAIR
-        assert gpath(n, H=1279) == binding.MHC_PATH_ELEMENT
+        assert gpath(n, H=1279) == binding.MHC_PATH_SHIFT16
+        assert gpath(n, H=34) == binding.MHC_PATH_PAIR
+        assert gpath(n, H=33) == binding.MHC_PATH_ELEMENT
     for n in (0, 3, 5, 16, -1):
         assert gpath(n) == binding.MHC_PATH_NONE
     # n = 4 is the pages' op

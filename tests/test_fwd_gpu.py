@@ -22,6 +22,7 @@ pytestmark = pytest.mark.gpu
 
 VEC32, VEC16 = binding.MHC_PATH_VEC32, binding.MHC_PATH_VEC16
 PAIR, ELEMENT = binding.MHC_PATH_PAIR, binding.MHC_PATH_ELEMENT
+SHIFT16 = binding.MHC_PATH_SHIFT16
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -62,15 +63,18 @@ def test_t129_repeat_100_calls_byte_identical():
     assert len(digests) == 1
 
 
-# --- workload fwd_ragged: odd-H element path and ragged shapes, seed 1
+# --- workload fwd_ragged: odd H and ragged shapes (realigned 16-byte path), seed 1
 
 @pytest.mark.parametrize("T,H", workload("fwd_ragged").shapes)
 def test_ragged_bit_exact(T, H):
     w = workload("fwd_ragged")
     res, pre = forward_inputs(T, H, w.recipe, w.seed)
-    path = PAIR if H % 2 == 0 else ELEMENT
-    got = run_fwd(res, pre, expect_path=path)
-    assert_bytes_equal(got, oracle_fwd(res, pre), f"ragged T={T} H={H}")
+    want = oracle_fwd(res, pre)
+    for offsets in ((0, 0, 0), (2, 4, 2), (6, 0, 14), (4, 8, 10)):
+        got = run_fwd(res, pre, offsets=offsets)
+        assert_bytes_equal(got, want, f"ragged T={T} H={H} offsets={offsets}")
+    if H % 2:
+        assert expected_fwd_path(H, (0, 0, 0)) == SHIFT16   # odd H: 16-byte, realigned
 
 
 # --- workload fwd_decode: decode-sized shapes, seed 2
@@ -123,7 +127,8 @@ def test_prefill_t65536_sampled_tokens():
 
 @pytest.mark.parametrize("H,offsets,path", [
     (16, (0, 0, 0), VEC32), (8, (0, 0, 0), VEC16), (16, (16, 0, 0), VEC16), (8, (4, 0, 4), PAIR),
-    (9, (0, 0, 0), ELEMENT), (8, (2, 4, 0), ELEMENT)])
+    (9, (0, 0, 0), ELEMENT), (8, (2, 4, 0), ELEMENT), (67, (0, 0, 0), SHIFT16),
+    (72, (2, 0, 4), SHIFT16), (80, (2, 4, 0), SHIFT16), (64, (14, 0, 6), SHIFT16)])
 def test_worked_examples_on_gpu(H, offsets, path):
     cases = list(_pins._fwd_cases())
     T = len(cases)
@@ -153,7 +158,7 @@ def test_paths_agree(T, H):
         seen.add(expected_fwd_path(H, offsets))
         got = run_fwd(res, pre, offsets=offsets)
         assert_bytes_equal(got, want, f"T={T} H={H} offsets={offsets}")
-    assert ELEMENT in seen
+    assert seen & {ELEMENT, SHIFT16}
 
 
 # --- edge cases
