@@ -34,10 +34,12 @@
 //    one in-thread add when a thread holds two lanes), the 8 groups through
 //    shared memory.  No atomics, no cross-block traffic.
 //  * Narrower paths (H not a multiple of 8, or buffers not 16-byte aligned)
-//    run the same per-element arithmetic and the same grad_pre tree with 4- or
-//    2-byte coalesced accesses (the backward stages row segments in shared
-//    memory so that each lane still sees its own 8-value chunks), so every
-//    path gives the same bytes.
+//    run the same per-element arithmetic and the same grad_pre tree: even H
+//    with 4-byte-aligned buffers with 4-byte coalesced accesses (the backward
+//    stages row segments in shared memory so that each lane still sees its
+//    own 8-value chunks), other rows of H >= 64 (odd H) with aligned 16-byte
+//    accesses realigned in registers (mhc_shift.cuh), and short rows with
+//    2-byte accesses.  Every path gives the same bytes.
 //  * Every kernel is launched with programmatic stream serialization and
 //    waits for its predecessor before touching memory (pdl_enter).
 //  * No tensor cores: nothing here is a contraction.
