@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import hashlib
 import os
+import re
 import shutil
 import subprocess
 import tempfile
@@ -71,13 +72,22 @@ KERNEL_FILES = [os.path.join(CSRC, f) for f in
                  "mhc_launch_sigmoid_f16.cu", "mhc_launch_coeffs.cu")]
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace runs collapsed (string
+    literals in these files hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_digest() -> str:
     """Hash of what decides the kernels' memory traffic: the device code, the
-    launch shapes and the flags (not the host-side validation)."""
+    launch shapes and the flags (not the host-side validation, and not the
+    comments)."""
     h = hashlib.sha256()
     for p in KERNEL_FILES:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p) as f:
+            h.update(_code_only(f.read()).encode())
     device_flags = []
     skip = False
     for flag in NVCC_FLAGS:            # host-compiler flags do not touch the kernels

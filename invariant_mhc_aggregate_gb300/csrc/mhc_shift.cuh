@@ -1,6 +1,6 @@
-// The realigned ("shifted") 16-byte paths, for rows that are not 16-byte
-// aligned: H not a multiple of 8 (odd H included) or buffers only 2- or
-// 4-byte aligned.
+// The realigned ("shifted") 16-byte paths, for rows of H >= 64 that neither
+// a vector path nor the 4-byte pair path can take: odd H, or buffers only
+// 2-byte aligned.
 //
 // A row of 2-byte values that starts `phase` values past a 16-byte boundary
 // (phase = (address / 2) mod 8) is covered by the 16-byte-aligned vectors
@@ -18,7 +18,9 @@
 // the at most 7 + 7 values at the row's two ends are computed and stored
 // one by one.  Loads stay inside the buffer (a vector not wholly inside it,
 // only at the buffer's ends, is read value by value), and no store leaves the
-// row.  No shared-memory staging and no block barrier in the main loops.
+// row.  The data is not staged through shared memory; the only block
+// barriers publish a token's sigmoid coefficients (when pre is computed from
+// the mix) and fold the backward's lane sums, once per token.
 //
 // The kernels run the same per-element arithmetic, the same per-lane
 // ORDER-256 chunks and the same fold as every other path, so the bytes are
