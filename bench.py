@@ -46,6 +46,15 @@ FWD_SWEEP = [("fwd_decode", 2, "decode", [(1, 4096), (8, 4096), (128, 4096),
 BWD_SWEEP = [("bwd_t4096_h7168", 4, "normal", [(4096, 7168)])]
 
 
+#: the kernel each path of the forward / backward runs
+KERNEL_OF_PATH = {
+    "fwd": {"vec32": "agg_fwd_vec_kernel", "vec16": "agg_fwd_vec_kernel", "pair": "agg_fwd_pair_kernel",
+            "element": "agg_fwd_element_kernel", "shift16": "agg_fwd_shift_kernel"},
+    "bwd": {"vec32": "agg_bwd_vec_kernel", "vec16": "agg_bwd_vec_kernel", "pair": "agg_bwd_staged_kernel",
+            "element": "agg_bwd_staged_kernel", "shift16": "agg_bwd_shift_kernel"},
+}
+
+
 def fwd_bytes(T, H):
     return T * (10 * H + 16)
 
@@ -311,13 +320,13 @@ def run_ours(args):
     bwd_path = binding.PATH_NAMES[binding.mhc_h_aggregate_bwd_path(g, res, pre, grad_res, grad_pre)]
     if do_fwd:
         a = fwd_bytes(T, H) / (fwd_us * 1e-6) / 1e9
-        per_kernel["agg_fwd_vec_kernel"] = {"path": fwd_path,"us_mean": round(fwd_us, 3),
+        per_kernel[KERNEL_OF_PATH["fwd"][fwd_path]] = {"path": fwd_path,"us_mean": round(fwd_us, 3),
                                          "us_p50": round(1e3 * statistics.median(fwd_ms), 3),
                                          "GBps": round(a, 1), "frac": round(a / peak, 4),
                                          "bytes": fwd_bytes(T, H)}
     if do_bwd:
         a = bwd_bytes(T, H) / (bwd_us * 1e-6) / 1e9
-        per_kernel["agg_bwd_vec_kernel"] = {"path": bwd_path,"us_mean": round(bwd_us, 3),
+        per_kernel[KERNEL_OF_PATH["bwd"][bwd_path]] = {"path": bwd_path,"us_mean": round(bwd_us, 3),
                                          "us_p50": round(1e3 * statistics.median(bwd_ms), 3),
                                          "GBps": round(a, 1), "frac": round(a / peak, 4),
                                          "bytes": bwd_bytes(T, H)}

@@ -107,8 +107,8 @@ typedef enum mhc_path {
     MHC_PATH_ELEMENT = 2, /* 2-byte loads/stores: any H and alignment */
     MHC_PATH_VEC32 = 3,   /* 32-byte loads/stores: H % 16 == 0, buffers 32-byte aligned */
     MHC_PATH_SHIFT16 = 4  /* 16-byte loads/stores at each row's own alignment, realigned in
-                             registers: H >= 64 that neither a vector path nor the PAIR path
-                             takes (odd H, or buffers only 2-byte aligned) */
+                             registers: 64 <= H < 2^30 that neither a vector path nor the
+                             PAIR path takes (odd H, or buffers only 2-byte aligned) */
 } mhc_path_t;
 
 /* Version of this ABI; changes when a declaration here changes. */

@@ -38,6 +38,7 @@ inline bool streams_ok(int64_t n) { return n == 1 || n == 2 || n == 4 || n == 8;
 // or buffers only 2-byte aligned) take the realigned 16-byte path when they
 // hold at least this many values, else the 2-byte element path.
 constexpr int64_t kShiftMinH = 64;
+constexpr int64_t kShiftMaxH = int64_t(1) << 30;   // row positions are 32-bit there
 
 inline bool dtype_ok(int32_t d) { return d == MHC_DTYPE_BF16 || d == MHC_DTYPE_F16; }
 
@@ -77,7 +78,7 @@ mhc_path_t fwd_path(const void* residual, const float* pre, const void* out, int
     if (H % 16 == 0 && aligned(residual, 32) && aligned(out, 32)) return MHC_PATH_VEC32;
     if (H % 8 == 0 && aligned(residual, 16) && aligned(out, 16)) return MHC_PATH_VEC16;
     if (H % 2 == 0 && aligned(residual, 4) && aligned(out, 4)) return MHC_PATH_PAIR;
-    if (H >= kShiftMinH) return MHC_PATH_SHIFT16;
+    if (H >= kShiftMinH && H < kShiftMaxH) return MHC_PATH_SHIFT16;
     return MHC_PATH_ELEMENT;
 }
 
@@ -99,7 +100,7 @@ mhc_path_t bwd_path(const void* g, const void* residual, const float* pre, const
     if (H % 16 == 0 && aligned(g, 32) && aligned(residual, 32) && aligned(gres, 32)) return MHC_PATH_VEC32;
     if (H % 8 == 0 && aligned(g, 16) && aligned(residual, 16) && aligned(gres, 16)) return MHC_PATH_VEC16;
     if (H % 2 == 0 && aligned(g, 4) && aligned(residual, 4) && aligned(gres, 4)) return MHC_PATH_PAIR;
-    if (H >= kShiftMinH) return MHC_PATH_SHIFT16;
+    if (H >= kShiftMinH && H < kShiftMaxH) return MHC_PATH_SHIFT16;
     return MHC_PATH_ELEMENT;
 }
 

@@ -72,10 +72,11 @@ struct Span {
     uintptr_t lo, hi;
 };
 
-// The 16 bytes at a (16-byte aligned) that lie inside `buf`, value by value
-// (only the buffer's first and last vectors get here: kept out of line).
-static __device__ __noinline__ Vec16 load_vec_clipped(uintptr_t a, Span buf) {
+// The 16 bytes at p (16-byte aligned) that lie inside `buf`, value by value
+// (only vectors at the buffer's two ends get here: kept out of line).
+static __device__ __noinline__ Vec16 load_vec_clipped(const uint16_t* p, Span buf) {
     Vec16 v = {{0u, 0u, 0u, 0u}};
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const uintptr_t e = a + uintptr_t(2 * i);
@@ -85,20 +86,33 @@ static __device__ __noinline__ Vec16 load_vec_clipped(uintptr_t a, Span buf) {
     return v;
 }
 
-// Vector m of a row (values 8m - phase .. + 7), from inside `buf` only.
-__device__ __forceinline__ Vec16 load_row_vec(const uint16_t* row, int phase, int64_t m, Span buf) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(row) + uintptr_t(2 * (8 * m - phase));
-    if (a >= buf.lo && a + 16 <= buf.hi) return ld_stream<4>(reinterpret_cast<const void*>(a));
-    return load_vec_clipped(a, buf);
-}
-
 __device__ __forceinline__ Vec16 zero16() { return Vec16{{0u, 0u, 0u, 0u}}; }
 
-// Vector m of a row if it holds any of the row's values 0 .. H-1, else zeros.
-__device__ __forceinline__ Vec16 load_if_in_row(const uint16_t* row, int phase, int64_t m, uint64_t H,
-                                                Span buf) {
-    const int64_t first = 8 * m - phase;
-    return (first < int64_t(H) && first > -8) ? load_row_vec(row, phase, m, buf) : zero16();
+// A row as the realigned kernels read it: its aligned vector 0 (which starts
+// `phase` values before the row), and whether all the vectors that hold a
+// row value lie inside the buffer (true for every row but possibly the
+// buffer's first and last), in which case its loads need no buffer check.
+// Row positions are 32-bit (the path takes H < 2^30).
+struct RowRef {
+    const uint16_t* v0;
+    int phase;
+    bool interior;
+};
+
+__device__ __forceinline__ RowRef row_ref(const uint16_t* row, int H, Span buf) {
+    const int phase = row_phase(row);
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(row) - uintptr_t(2 * phase);
+    const uintptr_t hi = lo + uintptr_t(16) * uintptr_t((H + phase + 7) / 8);
+    return RowRef{reinterpret_cast<const uint16_t*>(lo), phase, lo >= buf.lo && hi <= buf.hi};
+}
+
+// Vector m of a row (values 8m - phase .. 8m - phase + 7) if it holds any of
+// the row's values 0 .. H-1, else zeros.
+__device__ __forceinline__ Vec16 load_vec(const RowRef& r, int m, int H, Span buf) {
+    const int first = 8 * m - r.phase;
+    if (first >= H || first <= -8) return zero16();
+    const uint16_t* p = r.v0 + 8 * m;
+    return r.interior ? ld_stream<4>(p) : load_vec_clipped(p, buf);
 }
 
 // The window of (own, the next lane's own) at offset d.
@@ -131,36 +145,35 @@ agg_fwd_shift_kernel(const uint16_t* __restrict__ res, Coeffs coeffs, uint16_t* 
     __shared__ float table[2][N];
     pdl_enter();
     const Span rbuf{reinterpret_cast<uintptr_t>(res), reinterpret_cast<uintptr_t>(res + T * N * H)};
+    const int Hi = int(H);
     const uint32_t lane = threadIdx.x & 31u;
-    const int64_t wbase = int64_t(blockIdx.x) * (blockDim.x / 32) * kShiftWarpVectors * U +
-                          int64_t(threadIdx.x >> 5) * kShiftWarpVectors * U;
+    const int wbase = int(blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)) * kShiftWarpVectors * U;
     int parity = 0;
     for (uint64_t t = blockIdx.y; t < T; t += gridDim.y) {
         uint16_t* orow = out + t * H;
         const int po = row_phase(orow);
         float p[N];
         if constexpr (!Coeffs::kBlockTable) coeffs.template load<N>(t, p);
-        const uint16_t* rrow[N];
-        int rph[N];
+        int d[N];
         Vec16 own[U][N];
 #pragma unroll
         for (int k = 0; k < N; ++k) {
-            rrow[k] = res + (uint64_t(N) * t + k) * H;
-            rph[k] = row_phase(rrow[k]);
-            const int sh = (rph[k] >= po) ? 0 : -1;   // residual vector m + sh holds out vector m's start
+            const RowRef rr = row_ref(res + (uint64_t(N) * t + k) * H, Hi, rbuf);
+            const int sh = (rr.phase >= po) ? 0 : -1;   // residual vector m + sh holds out vector m's start
+            d[k] = (rr.phase - po) & 7;                  // ... at this offset
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                own[u][k] = load_if_in_row(rrow[k], rph[k], wbase + u * kShiftWarpVectors + lane + sh, H, rbuf);
+                own[u][k] = load_vec(rr, wbase + u * kShiftWarpVectors + int(lane) + sh, Hi, rbuf);
         }
         token_pre<N>(coeffs, t, p, table, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             Vec16 x[N];
 #pragma unroll
-            for (int k = 0; k < N; ++k) x[k] = window_next(own[u][k], (rph[k] - po) & 7);
-            const int64_t m = wbase + u * kShiftWarpVectors + lane;
-            const int64_t e0 = 8 * m - po;   // row value in lane 0 of output vector m
-            if (lane < uint32_t(kShiftWarpVectors) && e0 < int64_t(H) && e0 + 8 > 0) {
+            for (int k = 0; k < N; ++k) x[k] = window_next(own[u][k], d[k]);
+            const int m = wbase + u * kShiftWarpVectors + int(lane);
+            const int e0 = 8 * m - po;   // row value in lane 0 of output vector m
+            if (lane < uint32_t(kShiftWarpVectors) && e0 < Hi && e0 + 8 > 0) {
                 Vec16 o;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -169,12 +182,12 @@ agg_fwd_shift_kernel(const uint16_t* __restrict__ res, Coeffs coeffs, uint16_t* 
                     for (int k = 0; k < N; ++k) w[k] = x[k].w[e];
                     o.w[e] = agg_pair<N, DT>(p, w);
                 }
-                if (e0 >= 0 && e0 + 8 <= int64_t(H)) {
+                if (e0 >= 0 && e0 + 8 <= Hi) {
                     st_stream<4>(orow + e0, o);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        if (e0 + i >= 0 && e0 + i < int64_t(H)) st_stream2(orow + e0 + i, half_of(o, i));
+                        if (e0 + i >= 0 && e0 + i < Hi) st_stream2(orow + e0 + i, half_of(o, i));
                 }
             }
         }
@@ -209,22 +222,23 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
     pdl_enter();
     const Span gbuf{reinterpret_cast<uintptr_t>(g), reinterpret_cast<uintptr_t>(g + T * H)};
     const Span rbuf{reinterpret_cast<uintptr_t>(res), reinterpret_cast<uintptr_t>(res + T * N * H)};
+    const int Hi = int(H);
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-    const int64_t L = int64_t(warp) * kShiftWarpVectors + lane;    // ORDER-256 lane (if < 256, lane < 31)
+    const int L = int(warp) * kShiftWarpVectors + int(lane);   // ORDER-256 lane (if < 256, lane < 31)
     const bool works = lane < uint32_t(kShiftWarpVectors) && L < kLanes;
     const bool loads = L <= kLanes;   // the working lanes and the next-vector lane of each warp
-    const int64_t C = int64_t((H + 7) / 8);
+    const int C = (Hi + 7) / 8;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
         const uint16_t* grow = g + t * H;
-        const int gph = row_phase(grow);
-        const uint16_t* rrow[N];
+        const RowRef gref = row_ref(grow, Hi, gbuf);
+        const int gph = gref.phase;
+        RowRef rref[N];
         uint16_t* orow[N];
-        int rph[N], oph[N], osh[N], od[N];
+        int oph[N], osh[N], od[N];
 #pragma unroll
         for (int k = 0; k < N; ++k) {
-            rrow[k] = res + (uint64_t(N) * t + k) * H;
+            rref[k] = row_ref(res + (uint64_t(N) * t + k) * H, Hi, rbuf);
             orow[k] = gres + (uint64_t(N) * t + k) * H;
-            rph[k] = row_phase(rrow[k]);
             oph[k] = row_phase(orow[k]);
             osh[k] = (gph >= oph[k]) ? 0 : 1;    // this window gives grad_residual vector c + osh
             od[k] = (gph - oph[k]) & 7;          // at this offset
@@ -241,15 +255,14 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
 #pragma unroll
         for (int k = 0; k < N; ++k) acc[k] = 0.0f;
         // every thread runs the same number of steps (shuffles); chunks past C are empty
-        for (int64_t i0 = 0; i0 * kLanes < C || !pk_ready; i0 += B) {
+        for (int i0 = 0; i0 * kLanes < C || !pk_ready; i0 += B) {
             Vec16 gv[B], rv[B][N];
 #pragma unroll
             for (int b = 0; b < B; ++b) {
-                const int64_t c = L + kLanes * (i0 + b);
-                gv[b] = loads ? load_if_in_row(grow, gph, c, H, gbuf) : zero16();
+                const int c = L + kLanes * (i0 + b);
+                gv[b] = loads ? load_vec(gref, c, Hi, gbuf) : zero16();
 #pragma unroll
-                for (int k = 0; k < N; ++k)
-                    rv[b][k] = loads ? load_if_in_row(rrow[k], rph[k], c, H, rbuf) : zero16();
+                for (int k = 0; k < N; ++k) rv[b][k] = loads ? load_vec(rref[k], c, Hi, rbuf) : zero16();
             }
             if (!pk_ready) {
                 if constexpr (Coeffs::kBlockTable) {
@@ -264,7 +277,7 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
             }
 #pragma unroll
             for (int b = 0; b < B; ++b) {
-                const int64_t c = L + kLanes * (i0 + b);
+                const int c = L + kLanes * (i0 + b);
                 const bool live = works && c < C;
                 // g realigned to the chunk (values 8c .. 8c+7), +0 past H
                 Vec16 gn;
@@ -273,11 +286,11 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
                 Vec16 gc = window8(gv[b], gn, gph);
                 Vec16 rc[N];
 #pragma unroll
-                for (int k = 0; k < N; ++k) rc[k] = window_next(rv[b][k], rph[k]);
-                if (8 * c + 8 > int64_t(H)) {
+                for (int k = 0; k < N; ++k) rc[k] = window_next(rv[b][k], rref[k].phase);
+                if (8 * c + 8 > Hi) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        if (8 * c + e >= int64_t(H)) {
+                        if (8 * c + e >= Hi) {
                             const uint32_t keep = (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
                             gc.w[e >> 1] &= keep;
 #pragma unroll
@@ -293,9 +306,8 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
 #pragma unroll
                 for (int k = 0; k < N; ++k) {
                     const Vec16 gw = window8(gv[b], gn, od[k]);
-                    const int64_t m = c + osh[k];
-                    const int64_t e0 = 8 * m - oph[k];
-                    if (works && e0 >= 0 && e0 + 8 <= int64_t(H))
+                    const int e0 = 8 * (c + osh[k]) - oph[k];
+                    if (works && e0 >= 0 && e0 + 8 <= Hi)
                         st_stream<4>(orow[k] + e0, scale_vec<DT, 4>(pk[k], gw));
                 }
             }

@@ -77,7 +77,7 @@ def expected_fwd_path(H: int, offsets) -> int:
         return binding.MHC_PATH_VEC16
     if H % 2 == 0 and a >= 4:
         return binding.MHC_PATH_PAIR
-    if H >= SHIFT_MIN_H:
+    if SHIFT_MIN_H <= H < 2 ** 30:
         return binding.MHC_PATH_SHIFT16
     return binding.MHC_PATH_ELEMENT
 
@@ -90,7 +90,7 @@ def expected_bwd_path(H: int, offsets) -> int:
         return binding.MHC_PATH_VEC16
     if H % 2 == 0 and a >= 4:
         return binding.MHC_PATH_PAIR
-    if H >= SHIFT_MIN_H:
+    if SHIFT_MIN_H <= H < 2 ** 30:
         return binding.MHC_PATH_SHIFT16
     return binding.MHC_PATH_ELEMENT
 

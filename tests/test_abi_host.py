@@ -90,6 +90,10 @@ def test_fwd_path_choice(lib):
     assert fpath(H=62) == binding.MHC_PATH_PAIR
     assert fpath(H=56, r_off=2) == binding.MHC_PATH_ELEMENT   # shorter rows: 2-byte path
     assert fpath(H=63) == binding.MHC_PATH_ELEMENT
+    # the realigned path keeps row positions in 32 bits (H < 2^30); one token
+    # so that the fake buffers stay apart
+    assert fpath(H=(1 << 30) - 1, T=1) == binding.MHC_PATH_SHIFT16
+    assert fpath(H=(1 << 30) + 1, T=1) == binding.MHC_PATH_ELEMENT
     assert fpath(r_off=1) == binding.MHC_PATH_NONE           # not BF16 aligned
     assert fpath(p_off=2) == binding.MHC_PATH_NONE           # not FP32 aligned
     assert fpath(T=0) == binding.MHC_PATH_NONE
