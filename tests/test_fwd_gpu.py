@@ -220,3 +220,18 @@ def test_rejected_call_writes_nothing():
         binding.mhc_h_aggregate_fwd(res, pre, overlapping)
     torch.cuda.synchronize()
     assert torch.equal(res.view(torch.int16), before.view(torch.int16))
+
+
+# --- the page's third check: against a plain PyTorch computation within its tolerance
+
+@pytest.mark.parametrize("T,H", [(1, 4096), (8, 4096), (128, 7168), (1024, 7168), (3, 1279)])
+def test_matches_plain_pytorch_within_page_tolerance(T, H):
+    """"Add batch-invariant h_aggregate kernel", Correctness, check 3: the
+    result matches a PyTorch reference within atol=5e-2, rtol=1e-2.  The
+    reference here is plain PyTorch in FP32 on the CPU, rounded to BF16 once."""
+    res, pre = forward_inputs(T, H, "normal", 77)
+    out = binding.h_aggregate(res.cuda(), pre.cuda()).cpu().float()
+    r = res.float()
+    ref = ((pre[:, 0:1] * r[:, 0] + pre[:, 1:2] * r[:, 1]) +
+           (pre[:, 2:3] * r[:, 2] + pre[:, 3:4] * r[:, 3])).to(torch.bfloat16).float()
+    assert torch.allclose(out, ref, atol=5e-2, rtol=1e-2)
