@@ -154,11 +154,18 @@ struct SigmoidCoeffs {
     // mix value idx = n*t + k of the [T,n] mix (issued early: the kernels
     // fetch it before their bulk loads and turn it into pre afterwards) ...
     __device__ __forceinline__ float mix_at(uint64_t idx) const { return __ldg(mix + idx); }
-    // ... and pre for that value.
+    // ... and pre for that value ...
     __device__ __forceinline__ float pre_from(float m, int k) const {
         float s, one_minus;
         sigmoid32(pre_activation(__ldg(alpha), m, __ldg(b + k)), s, one_minus);
         return s;
+    }
+    // ... or pre and sigmoid' = RN(sigmoid * (1 - sigmoid)) for it (the
+    // backward keeps the slope for its epilogue).
+    __device__ __forceinline__ void pre_and_slope(float m, int k, float& s, float& slope) const {
+        float one_minus;
+        sigmoid32(pre_activation(__ldg(alpha), m, __ldg(b + k)), s, one_minus);
+        slope = __fmul_rn(s, one_minus);
     }
     // Token t's pre in every lane of a warp (all 32 lanes call it): lanes
     // 0 .. N-1 evaluate one sigmoid each, shuffles broadcast them.
@@ -193,12 +200,17 @@ struct SigmoidCoeffs {
     template <int N>
     __device__ __forceinline__ void store_grad(uint64_t t, int k, float gp) const {
         const uint64_t i = uint64_t(N) * t + k;
-        const float a = __ldg(alpha);
-        float s, one_minus;
-        sigmoid32(pre_activation(a, __ldg(mix + i), __ldg(b + k)), s, one_minus);
-        const float gz = __fmul_rn(gp, __fmul_rn(s, one_minus));
+        float s, slope;
+        pre_and_slope(__ldg(mix + i), k, s, slope);
+        store_grad_slope<N>(t, k, gp, slope);
+    }
+    // The same with sigmoid'(z[t,k]) already at hand.
+    template <int N>
+    __device__ __forceinline__ void store_grad_slope(uint64_t t, int k, float gp, float slope) const {
+        const uint64_t i = uint64_t(N) * t + k;
+        const float gz = __fmul_rn(gp, slope);
         grad_z[i] = gz;
-        grad_mix[i] = __fmul_rn(a, gz);
+        grad_mix[i] = __fmul_rn(__ldg(alpha), gz);
     }
 };
 

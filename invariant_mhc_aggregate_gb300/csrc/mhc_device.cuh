@@ -228,16 +228,20 @@ agg_fwd_vec_kernel(const Words<NW>* __restrict__ res, Coeffs coeffs, Words<NW>* 
     Words<NW> r[UNROLL][N];
     float p[UNROLL][N];
     uint32_t tok[UNROLL];
-    // kBlockTable: the block's tokens t0 .. and count = N * (number of them);
-    // each thread fetches its first mix value before the residual loads.
-    uint32_t t0 = 0, count = 0;
-    float m0 = 0.0f;
+    // kBlockTable: the coefficients of the (at most BLOCK*UNROLL + 1) tokens
+    // the block touches, each computed once, by the first threads, before
+    // their residual loads (the sigmoid's temporaries and the loaded vectors
+    // are then never live together, which keeps the register count, and so
+    // the occupancy, of the plain kernel).
+    __shared__ float table[Coeffs::kBlockTable ? (BLOCK * UNROLL + 1) * N : 1];
+    uint32_t t0 = 0;
     if constexpr (Coeffs::kBlockTable) {
         const uint32_t b0 = blockIdx.x * uint32_t(BLOCK * UNROLL);
         const uint32_t b1 = min(b0 + uint32_t(BLOCK * UNROLL), n_vec) - 1;
         t0 = fastdiv_u32(b0, divV);
-        count = (fastdiv_u32(b1, divV) - t0 + 1) * uint32_t(N);
-        if (threadIdx.x < count) m0 = coeffs.mix_at(uint64_t(t0) * N + threadIdx.x);
+        const uint32_t count = (fastdiv_u32(b1, divV) - t0 + 1) * uint32_t(N);
+        for (uint32_t j = threadIdx.x; j < count; j += BLOCK)
+            table[j] = coeffs.pre_from(coeffs.mix_at(uint64_t(t0) * N + j), int(j % N));
     }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
@@ -252,13 +256,6 @@ agg_fwd_vec_kernel(const Words<NW>* __restrict__ res, Coeffs coeffs, Words<NW>* 
         }
     }
     if constexpr (Coeffs::kBlockTable) {
-        // The coefficients of the (at most BLOCK*UNROLL + 1) tokens the block
-        // touches, each computed once, while the residual loads are in flight.
-        __shared__ float table[(BLOCK * UNROLL + 1) * N];
-        for (uint32_t j = threadIdx.x; j < count; j += BLOCK) {
-            const float m = (j == threadIdx.x) ? m0 : coeffs.mix_at(uint64_t(t0) * N + j);
-            table[j] = coeffs.pre_from(m, int(j % N));
-        }
         __syncthreads();
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
@@ -428,7 +425,8 @@ __device__ __forceinline__ float chunk_partial(const Words<NW>& g, const Words<N
 // stores it, or the gradients derived from it).  All threads of the block call it.
 template <int N, int LPT, class Coeffs>
 __device__ __forceinline__ void fold_lanes_and_store(float (&acc)[LPT][N], float (*red)[N],
-                                                     const Coeffs& coeffs, uint64_t t) {
+                                                     const Coeffs& coeffs, uint64_t t,
+                                                     const float* slope) {
     constexpr int kThreadsPerGroup = 32 / LPT;
 #pragma unroll
     for (int k = 0; k < N; ++k) {
@@ -455,9 +453,13 @@ __device__ __forceinline__ void fold_lanes_and_store(float (&acc)[LPT][N], float
 #pragma unroll
             for (int i = 0; i < s; ++i) w[i] = __fadd_rn(w[i], w[i + s]);
         }
-        coeffs.template store_grad<N>(t, k, w[0]);
+        if constexpr (Coeffs::kBlockTable) {
+            coeffs.template store_grad_slope<N>(t, k, w[0], slope[k]);
+        } else {
+            coeffs.template store_grad<N>(t, k, w[0]);
+        }
     }
-    __syncthreads();  // red[] is reused by the next token of this block
+    __syncthreads();  // red[] (and the slope table) are reused by the next token of this block
 }
 
 // Vector path: H % (2*NW) == 0 and g / residual / grad_residual aligned to
@@ -473,7 +475,8 @@ agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict_
     constexpr int LPT = NW / 4;
     constexpr uint32_t B = kLanes / LPT;
     __shared__ float red[kGroups][N];
-    __shared__ float table[N];   // kBlockTable: the token's pre
+    __shared__ float table[N];   // kBlockTable: the token's pre ...
+    __shared__ float slope[N];   // ... and sigmoid' (for the epilogue)
     pdl_enter();
     const uint32_t j = threadIdx.x;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
@@ -511,7 +514,7 @@ agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict_
             }
             if (!pk_ready) {
                 if constexpr (Coeffs::kBlockTable) {
-                    if (j < N) table[j] = coeffs.pre_from(m_own, int(j));
+                    if (j < N) coeffs.pre_and_slope(m_own, int(j), table[j], slope[j]);
                     __syncthreads();
 #pragma unroll
                     for (int k = 0; k < N; ++k) pk[k] = table[k];
@@ -534,7 +537,7 @@ agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict_
                 }
             }
         }
-        fold_lanes_and_store<N, LPT>(acc, red, coeffs, t);
+        fold_lanes_and_store<N, LPT>(acc, red, coeffs, t, slope);
     }
 }
 
@@ -554,7 +557,8 @@ agg_bwd_staged_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict
     constexpr int kUnit = PAIRS ? 2 : 1;             // values per access
     constexpr int kPer = kSeg / (kUnit * kLanes);    // accesses per thread per row
     __shared__ float red[kGroups][N];
-    __shared__ float table[N];   // kBlockTable: the token's pre
+    __shared__ float table[N];   // kBlockTable: the token's pre ...
+    __shared__ float slope[N];   // ... and sigmoid' (for the epilogue)
     __shared__ __align__(16) uint16_t sg[kSeg];
     __shared__ __align__(16) uint16_t sr[N][kSeg];
     pdl_enter();
@@ -597,7 +601,7 @@ agg_bwd_staged_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict
                 }
             }
             if constexpr (Coeffs::kBlockTable) {
-                if (!pk_ready && j < N) table[j] = coeffs.pre_from(m_own, int(j));
+                if (!pk_ready && j < N) coeffs.pre_and_slope(m_own, int(j), table[j], slope[j]);
             }
             __syncthreads();
             if (!pk_ready) {
@@ -639,7 +643,7 @@ agg_bwd_staged_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict
             }
             __syncthreads();  // the next segment overwrites the staging buffers
         }
-        fold_lanes_and_store<N, 1>(acc, red, coeffs, t);
+        fold_lanes_and_store<N, 1>(acc, red, coeffs, t, slope);
     }
 }
 

@@ -218,7 +218,8 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
     constexpr int B = shift_bwd_batch<N>();
     __shared__ float lanes_acc[kLanes][N];
     __shared__ float red[kGroups][N];
-    __shared__ float table[N];
+    __shared__ float table[N];    // kBlockTable: the token's pre ...
+    __shared__ float slope[N];    // ... and sigmoid' (for the epilogue)
     pdl_enter();
     const Span gbuf{reinterpret_cast<uintptr_t>(g), reinterpret_cast<uintptr_t>(g + T * H)};
     const Span rbuf{reinterpret_cast<uintptr_t>(res), reinterpret_cast<uintptr_t>(res + T * N * H)};
@@ -266,7 +267,8 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
             }
             if (!pk_ready) {
                 if constexpr (Coeffs::kBlockTable) {
-                    if (threadIdx.x < N) table[threadIdx.x] = coeffs.pre_from(m_own, int(threadIdx.x));
+                    if (threadIdx.x < N)
+                        coeffs.pre_and_slope(m_own, int(threadIdx.x), table[threadIdx.x], slope[threadIdx.x]);
                     __syncthreads();
 #pragma unroll
                     for (int k = 0; k < N; ++k) pk[k] = table[k];
@@ -362,7 +364,11 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
 #pragma unroll
                 for (int i = 0; i < sft; ++i) w[i] = __fadd_rn(w[i], w[i + sft]);
             }
-            coeffs.template store_grad<N>(t, k, w[0]);
+            if constexpr (Coeffs::kBlockTable) {
+                coeffs.template store_grad_slope<N>(t, k, w[0], slope[k]);
+            } else {
+                coeffs.template store_grad<N>(t, k, w[0]);
+            }
         }
         __syncthreads();   // lanes_acc, red and table are reused by the next token
     }
