@@ -395,3 +395,65 @@ def test_fused_calls_capture_in_a_graph():
     e_gb, e_ga = binding.sigmoid_param_grad(e_gz, md)
     for x, y in ((out, e_out), (gr, e_gr), (gz, e_gz), (gm, e_gm), (gb, e_gb), (ga, e_ga)):
         assert sha(x) == sha(y)
+
+
+def test_four_way_report_with_sigmoid_coefficients():
+    """The reviewer's four checks for the aggregate with pre computed from the
+    mix: forward and gradient accuracy against FP64 (with bounds from the
+    binary32 steps), forward and gradient invariance under a batch split and
+    repeats."""
+    T, H, n = 128, 7168, 4
+    g, res, _ = backward_inputs(T, H, "normal", 210)
+    mix, alpha, b = coeff_inputs(T, n, "normal", 211)
+    gd, rd, md, ad, bd = (x.cuda() for x in (g, res, mix, alpha, b))
+    out = binding.aggregate_sigmoid(rd, md, ad, bd)
+    gr, gz, gm = binding.aggregate_sigmoid_backward(gd, rd, md, ad, bd)
+    gb, ga = binding.sigmoid_param_grad(gz, md)
+    torch.cuda.synchronize()
+    U = 2.0 ** -24
+    a64 = float(alpha.item())
+    z64 = a64 * f32(mix).astype(np.float64) + f32(b).astype(np.float64)[None, :]
+    s64 = _pins.sigmoid64(z64)
+    ds64 = s64 * _pins.sigmoid64(-z64)
+    dz = 2.02 * U * (np.abs(a64 * f32(mix).astype(np.float64)) + np.abs(f32(b)).astype(np.float64)[None, :])
+    rw = _pins.bf16_widen(u16(res)).astype(np.float64)
+    gw = _pins.bf16_widen(u16(g)).astype(np.float64)
+    # forward: exact sum of sigmoid(z_k) * r_k; bound = half a BF16 ulp + the
+    # tree's rounding + each pre_k's error (2.5 ulp of the sigmoid, plus the
+    # rounding of z carried through the slope)
+    exact = np.einsum("tk,tkh->th", s64, rw)
+    pre_err = 2.5 * _pins.f32_ulp(s64) + ds64 * dz
+    o64 = _pins.bf16_widen(u16(out)).astype(np.float64)
+    bound = (0.5 * _pins.bf16_ulp(o64) + 3.01 * U * np.einsum("tk,tkh->th", s64, np.abs(rw))
+             + np.einsum("tk,tkh->th", pre_err, np.abs(rw)))
+    fwd_ratio = float(np.max(np.abs(o64 - exact) / bound))
+    # gradients: grad_mix = alpha * sigmoid'(z) * sum_h g r, relative to the
+    # magnitude sum |alpha sigmoid' g r| (cancellation makes a plain relative
+    # error meaningless), within 1e-3
+    q = np.einsum("th,tkh->tk", gw, rw)
+    qa = np.einsum("th,tkh->tk", np.abs(gw), np.abs(rw))
+    exact_gm = a64 * ds64 * q
+    scale = np.maximum(np.abs(exact_gm), np.abs(a64) * ds64 * qa)
+    gm_err = float(np.max(np.abs(f32(gm).astype(np.float64) - exact_gm) / scale))
+    exact_gz = ds64 * q
+    gb_exact = exact_gz.sum(axis=0)
+    gb_scale = np.abs(exact_gz).sum(axis=0) + 1e-30
+    gb_err = float(np.max(np.abs(f32(gb).astype(np.float64) - gb_exact) / gb_scale))
+    ga_exact = float((exact_gz * f32(mix).astype(np.float64)).sum())
+    ga_err = abs(float(ga.item()) - ga_exact) / float(np.abs(exact_gz * f32(mix)).sum())
+    # invariance: the batch split into halves, and a repeat
+    h0 = T // 2
+    part0 = binding.aggregate_sigmoid(rd[:h0].contiguous(), md[:h0].contiguous(), ad, bd)
+    p_gr, p_gz, p_gm = binding.aggregate_sigmoid_backward(gd[h0:].contiguous(), rd[h0:].contiguous(),
+                                                          md[h0:].contiguous(), ad, bd)
+    fwd_inv = torch.equal(part0.view(torch.int16), out[:h0].view(torch.int16)) and \
+        sha(binding.aggregate_sigmoid(rd, md, ad, bd)) == sha(out)
+    grad_inv = torch.equal(p_gr.view(torch.int16), gr[h0:].view(torch.int16)) and \
+        torch.equal(p_gz.view(torch.int32), gz[h0:].view(torch.int32)) and \
+        torch.equal(p_gm.view(torch.int32), gm[h0:].view(torch.int32))
+    report = {"forward_accuracy (error / bound)": fwd_ratio, "gradient_accuracy grad_mix": gm_err,
+              "gradient_accuracy grad_b": gb_err, "gradient_accuracy grad_alpha": ga_err,
+              "forward_invariance": fwd_inv, "gradient_invariance": grad_inv}
+    print(report)
+    assert fwd_ratio <= 1.0 and gm_err <= 1e-3 and gb_err <= 1e-3 and ga_err <= 1e-3, report
+    assert fwd_inv and grad_inv, report
