@@ -47,9 +47,10 @@
  * grad_pre like pre.  BF16 buffers are 2-byte aligned, FP32 buffers 4-byte
  * aligned.  Any such alignment is accepted: 32-byte-aligned BF16 buffers
  * with H % 16 == 0 take the 32-byte vector path, 16-byte-aligned ones with
- * H % 8 == 0 the 16-byte path, even H with 4-byte-aligned buffers the 4-byte
- * path, other rows of H >= 64 (odd H included) the realigned 16-byte path and
- * the rest the 2-byte path; all give identical results.
+ * H % 8 == 0 the 16-byte path; other rows of 64 <= H < 2^30 take the
+ * realigned 16-byte path (the forward takes the 4-byte path instead when H is
+ * even and the buffers 4-byte aligned), shorter rows the 4- or 2-byte path;
+ * all give identical results.
  *
  * Pointers and ownership.  Every data pointer is a DEVICE pointer (or managed
  * memory) allocated and owned by the caller.  The library allocates nothing,
@@ -103,12 +104,14 @@ typedef enum mhc_status {
 typedef enum mhc_path {
     MHC_PATH_NONE = -1,   /* the call would be rejected or launches nothing */
     MHC_PATH_VEC16 = 0,   /* 16-byte loads/stores: H % 8 == 0, buffers 16-byte aligned */
-    MHC_PATH_PAIR = 1,    /* 4-byte loads/stores: H even, buffers 4-byte aligned */
+    MHC_PATH_PAIR = 1,    /* 4-byte loads/stores: H even, buffers 4-byte aligned (the
+                             backward takes it only for H < 64) */
     MHC_PATH_ELEMENT = 2, /* 2-byte loads/stores: any H and alignment */
     MHC_PATH_VEC32 = 3,   /* 32-byte loads/stores: H % 16 == 0, buffers 32-byte aligned */
     MHC_PATH_SHIFT16 = 4  /* 16-byte loads/stores at each row's own alignment, realigned in
-                             registers: 64 <= H < 2^30 that neither a vector path nor the
-                             PAIR path takes (odd H, or buffers only 2-byte aligned) */
+                             registers, for 64 <= H < 2^30 when no vector path applies
+                             (the forward leaves even H with 4-byte-aligned buffers to
+                             the PAIR path) */
 } mhc_path_t;
 
 /* Version of this ABI; changes when a declaration here changes. */

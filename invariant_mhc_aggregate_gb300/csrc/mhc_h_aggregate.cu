@@ -34,9 +34,10 @@ inline bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
 inline bool streams_ok(int64_t n) { return n == 1 || n == 2 || n == 4 || n == 8; }
 
-// Rows that can take neither a vector path nor the 4-byte pair path (odd H,
-// or buffers only 2-byte aligned) take the realigned 16-byte path when they
-// hold at least this many values, else the 2-byte element path.
+// Rows that no vector path can take use the realigned 16-byte path when they
+// hold at least kShiftMinH values (the forward keeps the faster 4-byte pair
+// path for even H with 4-byte-aligned buffers); shorter rows the 4- or
+// 2-byte paths.
 constexpr int64_t kShiftMinH = 64;
 constexpr int64_t kShiftMaxH = int64_t(1) << 30;   // row positions are 32-bit there
 
@@ -99,8 +100,10 @@ mhc_path_t bwd_path(const void* g, const void* residual, const float* pre, const
         if (overlap(rgr, in) || overlap(rgp, in)) return MHC_PATH_NONE;
     if (H % 16 == 0 && aligned(g, 32) && aligned(residual, 32) && aligned(gres, 32)) return MHC_PATH_VEC32;
     if (H % 8 == 0 && aligned(g, 16) && aligned(residual, 16) && aligned(gres, 16)) return MHC_PATH_VEC16;
-    if (H % 2 == 0 && aligned(g, 4) && aligned(residual, 4) && aligned(gres, 4)) return MHC_PATH_PAIR;
+    // the realigned backward is faster than the staged 4-byte one, so it also
+    // takes even H
     if (H >= kShiftMinH && H < kShiftMaxH) return MHC_PATH_SHIFT16;
+    if (H % 2 == 0 && aligned(g, 4) && aligned(residual, 4) && aligned(gres, 4)) return MHC_PATH_PAIR;
     return MHC_PATH_ELEMENT;
 }
 

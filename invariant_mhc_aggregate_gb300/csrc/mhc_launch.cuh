@@ -247,7 +247,7 @@ cudaError_t bwd_n(const BwdCall& c, const Coeffs& k) {
         case kPathVec16: return bwd_vec16<N, DT>(c, k);
         case kPathShift16: {
             const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
-            return launch(agg_bwd_shift_kernel<N, DT, Coeffs>, blocks, kShiftBwdThreads, c.stream,
+            return launch(agg_bwd_shift_kernel<N, DT, Coeffs>, blocks, kLanes, c.stream,
                           static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.residual), k,
                           static_cast<uint16_t*>(c.gres), c.T, c.H);
         }

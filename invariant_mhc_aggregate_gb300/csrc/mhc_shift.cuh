@@ -9,18 +9,24 @@
 // (vector m, vector m + 1) shifted by d values: funnel shifts of 32-bit words,
 // with d the same in every thread of a row (no divergence).
 //
-// Each warp works on 32 consecutive vectors of a row per step: every lane
-// loads one with an aligned 16-byte load (streaming), takes its neighbour's
-// with warp shuffles, and lanes 0..30 use the window; lane 31 only supplies
-// the neighbour of lane 30 (and is lane 0 of the next warp's step, so its
-// vector is read twice: 1/31 of the loads, usually from L2).  Outputs are
-// written with aligned 16-byte stores when the whole vector lies in the row;
-// the at most 7 + 7 values at the row's two ends are computed and stored
-// one by one.  Loads stay inside the buffer (a vector not wholly inside it,
-// only at the buffer's ends, is read value by value), and no store leaves the
-// row.  The data is not staged through shared memory; the only block
-// barriers publish a token's sigmoid coefficients (when pre is computed from
-// the mix) and fold the backward's lane sums, once per token.
+// The forward works on 32 consecutive vectors of a row per warp and step:
+// every lane loads one (streaming), takes its neighbour's with warp
+// shuffles, and lanes 0..30 use the window; lane 31 only supplies lane 30's
+// neighbour (and is lane 0 of the next run, so 1/31 of the vectors are read
+// twice, mostly from L2).  The backward keeps ORDER-256's one-lane-per-thread
+// layout: each lane loads both aligned vectors of its chunk's windows with
+// L1-allocating loads, the second being the next lane's first, so a warp's
+// second load instruction finds its lines in L1 (or in flight there).
+// Measured at H = 7167: shuffles are faster for the forward (46 against
+// 55 us), paired loads for the backward (87 against 97 us; the shuffle
+// version also needed a 9-warp block and a shared-memory fold).
+// Outputs are written with aligned 16-byte stores when the whole vector lies
+// in the row; the at most 7 + 7 values at the row's two ends are computed and
+// stored one by one.  Loads stay inside the buffer (a vector not wholly
+// inside it, only at the buffer's ends, is read value by value), and no store
+// leaves the row.  The data is not staged through shared memory; the only
+// block barriers publish a token's sigmoid coefficients (when pre is computed
+// from the mix) and fold the backward's lane sums, once per token.
 //
 // The kernels run the same per-element arithmetic, the same per-lane
 // ORDER-256 chunks and the same fold as every other path, so the bytes are
@@ -106,13 +112,27 @@ __device__ __forceinline__ RowRef row_ref(const uint16_t* row, int H, Span buf) 
     return RowRef{reinterpret_cast<const uint16_t*>(lo), phase, lo >= buf.lo && hi <= buf.hi};
 }
 
+// 16 bytes through the read-only path, allocating in L1 (the next lane loads
+// the same vector as the second half of its window).
+__device__ __forceinline__ Vec16 ld_shared_line(const void* p) {
+    Vec16 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+    return v;
+}
+
 // Vector m of a row (values 8m - phase .. 8m - phase + 7) if it holds any of
-// the row's values 0 .. H-1, else zeros.
+// the row's values 0 .. H-1, else zeros: streaming (L1 = false: the forward,
+// which passes vectors between lanes with shuffles) or L1-allocating (L1 =
+// true: the backward, whose lanes load both vectors of their windows).
+template <bool L1>
 __device__ __forceinline__ Vec16 load_vec(const RowRef& r, int m, int H, Span buf) {
     const int first = 8 * m - r.phase;
     if (first >= H || first <= -8) return zero16();
     const uint16_t* p = r.v0 + 8 * m;
-    return r.interior ? ld_stream<4>(p) : load_vec_clipped(p, buf);
+    if (!r.interior) return load_vec_clipped(p, buf);
+    return L1 ? ld_shared_line(p) : ld_stream<4>(p);
 }
 
 // The window of (own, the next lane's own) at offset d.
@@ -163,7 +183,7 @@ agg_fwd_shift_kernel(const uint16_t* __restrict__ res, Coeffs coeffs, uint16_t* 
             d[k] = (rr.phase - po) & 7;                  // ... at this offset
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                own[u][k] = load_vec(rr, wbase + u * kShiftWarpVectors + int(lane) + sh, Hi, rbuf);
+                own[u][k] = load_vec<false>(rr, wbase + u * kShiftWarpVectors + int(lane) + sh, Hi, rbuf);
         }
         token_pre<N>(coeffs, t, p, table, parity);
 #pragma unroll
@@ -195,28 +215,22 @@ agg_fwd_shift_kernel(const uint16_t* __restrict__ res, Coeffs coeffs, uint16_t* 
 }
 
 // --------------------------------------------------------------------------
-// backward: one block per token (grid-stride), 9 warps.  ORDER-256 lane L is
-// held by lane L mod 31 of warp L / 31 (lanes 248 .. 255 by warp 8), so that
-// each warp's working lanes hold consecutive chunks: in step i, lane l of
-// warp w takes chunk c = 31w + l + 256i, and its lane 31 loads chunk
-// 31w + 31 + 256i for lane 30's window.  The per-lane sums (each lane adds
-// its chunks in increasing order) go through shared memory at the end of the
-// token, where warp g folds group g (lanes 32g .. 32g+31) with the usual xor
-// shuffles and the 8 group values fold as everywhere else.
+// backward: one block of 256 threads per token (grid-stride); thread j is
+// ORDER-256 lane j and takes chunks j, j + 256, ... in increasing order, as
+// in every other path.  For chunk c it loads the two aligned vectors of g
+// and of each residual row that cover values 8c .. 8c+7 and realigns them;
+// g's pair also gives the grad_residual vector c + osh_k of each output row
+// k (at that row's offset).  The fold is the common one.
 // --------------------------------------------------------------------------
 
-constexpr int kShiftBwdWarps = 9;
-constexpr int kShiftBwdThreads = 32 * kShiftBwdWarps;
-
 template <int N>
-__host__ __device__ constexpr int shift_bwd_batch() { return N >= 8 ? 1 : 2; }
+__host__ __device__ constexpr int shift_bwd_batch() { return N >= 4 ? 1 : 2; }
 
 template <int N, int DT, class Coeffs>
-__global__ void __launch_bounds__(kShiftBwdThreads)
+__global__ void __launch_bounds__(kLanes)
 agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ res,
                      Coeffs coeffs, uint16_t* __restrict__ gres, uint64_t T, uint64_t H) {
     constexpr int B = shift_bwd_batch<N>();
-    __shared__ float lanes_acc[kLanes][N];
     __shared__ float red[kGroups][N];
     __shared__ float table[N];    // kBlockTable: the token's pre ...
     __shared__ float slope[N];    // ... and sigmoid' (for the epilogue)
@@ -224,10 +238,7 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
     const Span gbuf{reinterpret_cast<uintptr_t>(g), reinterpret_cast<uintptr_t>(g + T * H)};
     const Span rbuf{reinterpret_cast<uintptr_t>(res), reinterpret_cast<uintptr_t>(res + T * N * H)};
     const int Hi = int(H);
-    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-    const int L = int(warp) * kShiftWarpVectors + int(lane);   // ORDER-256 lane (if < 256, lane < 31)
-    const bool works = lane < uint32_t(kShiftWarpVectors) && L < kLanes;
-    const bool loads = L <= kLanes;   // the working lanes and the next-vector lane of each warp
+    const int j = int(threadIdx.x);
     const int C = (Hi + 7) / 8;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
         const uint16_t* grow = g + t * H;
@@ -241,34 +252,38 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
             rref[k] = row_ref(res + (uint64_t(N) * t + k) * H, Hi, rbuf);
             orow[k] = gres + (uint64_t(N) * t + k) * H;
             oph[k] = row_phase(orow[k]);
-            osh[k] = (gph >= oph[k]) ? 0 : 1;    // this window gives grad_residual vector c + osh
+            osh[k] = (gph >= oph[k]) ? 0 : 1;    // g's window gives grad_residual vector c + osh
             od[k] = (gph - oph[k]) & 7;          // at this offset
         }
         float pk[N];
         float m_own = 0.0f;
         if constexpr (Coeffs::kBlockTable) {
-            if (threadIdx.x < N) m_own = coeffs.mix_at(uint64_t(N) * t + threadIdx.x);
+            if (j < N) m_own = coeffs.mix_at(uint64_t(N) * t + j);
         } else {
             coeffs.template load<N>(t, pk);
         }
         bool pk_ready = false;
-        float acc[N];
+        float acc[1][N];
 #pragma unroll
-        for (int k = 0; k < N; ++k) acc[k] = 0.0f;
-        // every thread runs the same number of steps (shuffles); chunks past C are empty
-        for (int i0 = 0; i0 * kLanes < C || !pk_ready; i0 += B) {
-            Vec16 gv[B], rv[B][N];
+        for (int k = 0; k < N; ++k) acc[0][k] = 0.0f;
+        // with a block table the first pass runs in every thread (its loads are
+        // guarded) so that all of them meet the barrier that publishes it
+        for (int i0 = 0; i0 * kLanes + j < C || !pk_ready; i0 += B) {
+            Vec16 glo[B], ghi[B], rlo[B][N], rhi[B][N];
 #pragma unroll
             for (int b = 0; b < B; ++b) {
-                const int c = L + kLanes * (i0 + b);
-                gv[b] = loads ? load_vec(gref, c, Hi, gbuf) : zero16();
+                const int c = j + kLanes * (i0 + b);
+                glo[b] = load_vec<true>(gref, c, Hi, gbuf);
+                ghi[b] = load_vec<true>(gref, c + 1, Hi, gbuf);
 #pragma unroll
-                for (int k = 0; k < N; ++k) rv[b][k] = loads ? load_vec(rref[k], c, Hi, rbuf) : zero16();
+                for (int k = 0; k < N; ++k) {
+                    rlo[b][k] = load_vec<true>(rref[k], c, Hi, rbuf);
+                    rhi[b][k] = load_vec<true>(rref[k], c + 1, Hi, rbuf);
+                }
             }
             if (!pk_ready) {
                 if constexpr (Coeffs::kBlockTable) {
-                    if (threadIdx.x < N)
-                        coeffs.pre_and_slope(m_own, int(threadIdx.x), table[threadIdx.x], slope[threadIdx.x]);
+                    if (j < N) coeffs.pre_and_slope(m_own, j, table[j], slope[j]);
                     __syncthreads();
 #pragma unroll
                     for (int k = 0; k < N; ++k) pk[k] = table[k];
@@ -279,16 +294,13 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
             }
 #pragma unroll
             for (int b = 0; b < B; ++b) {
-                const int c = L + kLanes * (i0 + b);
-                const bool live = works && c < C;
-                // g realigned to the chunk (values 8c .. 8c+7), +0 past H
-                Vec16 gn;
-#pragma unroll
-                for (int w = 0; w < 4; ++w) gn.w[w] = __shfl_down_sync(0xffffffffu, gv[b].w[w], 1);
-                Vec16 gc = window8(gv[b], gn, gph);
+                const int c = j + kLanes * (i0 + b);
+                if (c >= C) continue;
+                // g and the residual rows realigned to the chunk (values 8c .. 8c+7), +0 past H
+                Vec16 gc = window8(glo[b], ghi[b], gph);
                 Vec16 rc[N];
 #pragma unroll
-                for (int k = 0; k < N; ++k) rc[k] = window_next(rv[b][k], rref[k].phase);
+                for (int k = 0; k < N; ++k) rc[k] = window8(rlo[b][k], rhi[b][k], rref[k].phase);
                 if (8 * c + 8 > Hi) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
@@ -300,77 +312,36 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
                         }
                     }
                 }
-                if (live) {
 #pragma unroll
-                    for (int k = 0; k < N; ++k) acc[k] = __fadd_rn(acc[k], chunk_partial<DT, 4>(gc, rc[k], 0));
-                }
+                for (int k = 0; k < N; ++k) acc[0][k] = __fadd_rn(acc[0][k], chunk_partial<DT, 4>(gc, rc[k], 0));
                 // grad_residual vectors from g's window at each output row's offset
 #pragma unroll
                 for (int k = 0; k < N; ++k) {
-                    const Vec16 gw = window8(gv[b], gn, od[k]);
                     const int e0 = 8 * (c + osh[k]) - oph[k];
-                    if (works && e0 >= 0 && e0 + 8 <= Hi)
-                        st_stream<4>(orow[k] + e0, scale_vec<DT, 4>(pk[k], gw));
+                    if (e0 >= 0 && e0 + 8 <= Hi)
+                        st_stream<4>(orow[k] + e0, scale_vec<DT, 4>(pk[k], window8(glo[b], ghi[b], od[k])));
                 }
             }
         }
-        // the fold: lane sums to shared memory (then as in every other path);
-        // and the values of each grad_residual row that lie in no whole vector
-        // ([0, head) and [tail, H), at most 7 + 7), one by one
-        if (works) {
-#pragma unroll
-            for (int k = 0; k < N; ++k) lanes_acc[L][k] = acc[k];
-        }
-        __syncthreads();
-        if (threadIdx.x < 16 * N) {   // threads 16k .. 16k+15 take row k
-            const int k = int(threadIdx.x) / 16, s16 = int(threadIdx.x) % 16;
+        // the grad_residual values of each row that lie in no whole vector
+        // ([0, head) and [tail, H), at most 7 + 7), one by one: threads
+        // 16k .. 16k+15 take row k
+        if (threadIdx.x < 16 * N) {
+            const int k = j / 16, s16 = j % 16;
             float pkk = pk[0];   // pk[k] by selects (no dynamic register indexing)
 #pragma unroll
             for (int kk = 1; kk < N; ++kk)
                 if (kk == k) pkk = pk[kk];
             uint16_t* row = gres + (uint64_t(N) * t + k) * H;
             const int ph = row_phase(row);
-            const int64_t head = (8 - ph) & 7;
-            int64_t tail = ((int64_t(H) + ph) / 8) * 8 - ph;
+            const int head = (8 - ph) & 7;
+            int tail = ((Hi + ph) / 8) * 8 - ph;
             if (tail < head) tail = head;
-            const int64_t h = (s16 < 8) ? int64_t(s16) : tail + s16 - 8;
-            const bool mine = (s16 < 8) ? (h < head && h < int64_t(H)) : (h < int64_t(H));
-            if (mine)
+            const int h = (s16 < 8) ? s16 : tail + s16 - 8;
+            if ((s16 < 8) ? (h < head && h < Hi) : (h < Hi))
                 st_stream2(row + h, Elem<DT>::cvt(__fmul_rn(pkk, Elem<DT>::one(ld_stream2(grow + h)))));
         }
-        if (warp < uint32_t(kGroups)) {
-            float a[1][N];
-#pragma unroll
-            for (int k = 0; k < N; ++k) a[0][k] = lanes_acc[threadIdx.x][k];
-#pragma unroll
-            for (int k = 0; k < N; ++k) {
-#pragma unroll
-                for (int sft = 16; sft >= 1; sft >>= 1)
-                    a[0][k] = __fadd_rn(a[0][k], __shfl_xor_sync(0xffffffffu, a[0][k], sft));
-            }
-            if (lane == 0) {
-#pragma unroll
-                for (int k = 0; k < N; ++k) red[warp][k] = a[0][k];
-            }
-        }
-        __syncthreads();
-        if (threadIdx.x < N) {
-            const int k = threadIdx.x;
-            float w[kGroups];
-#pragma unroll
-            for (int i = 0; i < kGroups; ++i) w[i] = red[i][k];
-#pragma unroll
-            for (int sft = kGroups / 2; sft >= 1; sft >>= 1) {
-#pragma unroll
-                for (int i = 0; i < sft; ++i) w[i] = __fadd_rn(w[i], w[i + sft]);
-            }
-            if constexpr (Coeffs::kBlockTable) {
-                coeffs.template store_grad_slope<N>(t, k, w[0], slope[k]);
-            } else {
-                coeffs.template store_grad<N>(t, k, w[0]);
-            }
-        }
-        __syncthreads();   // lanes_acc, red and table are reused by the next token
+        fold_lanes_and_store<N, 1>(acc, red, coeffs, t, slope);
     }
 }
 

@@ -83,15 +83,16 @@ def expected_fwd_path(H: int, offsets) -> int:
 
 
 def expected_bwd_path(H: int, offsets) -> int:
+    """The backward prefers the realigned path to the 4-byte pair path."""
     a = min(_align_of(offsets[0]), _align_of(offsets[1]), _align_of(offsets[3]))
     if H % 16 == 0 and a >= 32:
         return binding.MHC_PATH_VEC32
     if H % 8 == 0 and a >= 16:
         return binding.MHC_PATH_VEC16
-    if H % 2 == 0 and a >= 4:
-        return binding.MHC_PATH_PAIR
     if SHIFT_MIN_H <= H < 2 ** 30:
         return binding.MHC_PATH_SHIFT16
+    if H % 2 == 0 and a >= 4:
+        return binding.MHC_PATH_PAIR
     return binding.MHC_PATH_ELEMENT
 
 

@@ -108,8 +108,8 @@ def test_bwd_path_choice(lib):
     assert bpath(gr_off=16) == binding.MHC_PATH_VEC16
     assert bpath(H=4104) == binding.MHC_PATH_VEC16
     assert bpath(g_off=2) == binding.MHC_PATH_SHIFT16
-    assert bpath(gr_off=4) == binding.MHC_PATH_PAIR
-    assert bpath(H=2050) == binding.MHC_PATH_PAIR
+    assert bpath(gr_off=4) == binding.MHC_PATH_SHIFT16          # the backward prefers the realigned path
+    assert bpath(H=2050) == binding.MHC_PATH_SHIFT16
     assert bpath(H=2050, r_off=2) == binding.MHC_PATH_SHIFT16
     assert bpath(H=1279) == binding.MHC_PATH_SHIFT16
     assert bpath(H=50) == binding.MHC_PATH_PAIR
