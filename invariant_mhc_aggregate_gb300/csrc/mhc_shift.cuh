@@ -1,6 +1,7 @@
-// The realigned ("shifted") 16-byte paths, for rows of H >= 64 that neither
-// a vector path nor the 4-byte pair path can take: odd H, or buffers only
-// 2-byte aligned.
+// The realigned ("shifted") 16-byte paths, for rows of 64 <= H < 2^30 that
+// no vector path can take (H not a multiple of 8, odd H included, or buffers
+// not 16-byte aligned).  The forward leaves even H with 4-byte-aligned
+// buffers to the 4-byte pair kernel, which is faster there.
 //
 // A row of 2-byte values that starts `phase` values past a 16-byte boundary
 // (phase = (address / 2) mod 8) is covered by the 16-byte-aligned vectors
@@ -114,7 +115,7 @@ __device__ __forceinline__ RowRef row_ref(const uint16_t* row, int H, Span buf) 
 
 // 16 bytes through the read-only path, allocating in L1 (the next lane loads
 // the same vector as the second half of its window).
-__device__ __forceinline__ Vec16 ld_shared_line(const void* p) {
+__device__ __forceinline__ Vec16 ld_l1_line(const void* p) {
     Vec16 v;
     asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
@@ -132,7 +133,7 @@ __device__ __forceinline__ Vec16 load_vec(const RowRef& r, int m, int H, Span bu
     if (first >= H || first <= -8) return zero16();
     const uint16_t* p = r.v0 + 8 * m;
     if (!r.interior) return load_vec_clipped(p, buf);
-    return L1 ? ld_shared_line(p) : ld_stream<4>(p);
+    return L1 ? ld_l1_line(p) : ld_stream<4>(p);
 }
 
 // The window of (own, the next lane's own) at offset d.
