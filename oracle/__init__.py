@@ -35,6 +35,9 @@ Parity status of each function (what pins it, from the oracle pin tests):
     page's pre coefficients, a reading): FP64 bounds, exact special cases
     (z = 0, integer-valued sums), hand-worked token-order cases and an
     independent recursive builder of ORDER-256 over tokens.
+  * post_fwd / post_bwd (mHC post, a reading not on the pages): hand-worked
+    tree-order cases, exact-rational emulation, identity and zero special
+    cases, integer-valued exact sums for grad_res and grad_post, FP64 bounds.
 """
 
 from __future__ import annotations
@@ -155,6 +158,10 @@ class Oracle:
         lib.oracle_aggregate_sigmoid_bwd.restype = ctypes.c_int
         lib.oracle_sigmoid_param_grad.argtypes = [p, p, p, p, i64, i64]
         lib.oracle_sigmoid_param_grad.restype = ctypes.c_int
+        lib.oracle_post_fwd.argtypes = [p, p, p, p, p, i64, i64, i64, ctypes.c_int]
+        lib.oracle_post_fwd.restype = ctypes.c_int
+        lib.oracle_post_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i64, i64, i64, ctypes.c_int]
+        lib.oracle_post_bwd.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -293,6 +300,43 @@ class Oracle:
             raise ValueError(f"unsupported n={n}")
         return gb, ga[0]
 
+    # -- mHC post (a reading: the layer output expanded onto the n streams) --
+
+    @staticmethod
+    def _post_args(x, y, post, res):
+        x = _as(x, np.uint16)
+        y = _as(y, np.uint16)
+        post = _as(post, np.float32)
+        res = _as(res, np.float32)
+        T, n, H = x.shape
+        if y.shape != (T, H) or post.shape != (T, n) or res.shape != (T, n, n):
+            raise ValueError("shapes: x [T,n,H], y [T,H], post [T,n], res [T,n,n]")
+        return x, y, post, res, T, n, H
+
+    def post_fwd(self, x, y, post, res, dtype: str = "bf16") -> np.ndarray:
+        """out[t,k,h] = cvt(tree_n(res[t,k,j] * x[t,j,h]) + post[t,k] * y[t,h]); [T,n,H]."""
+        x, y, post, res, T, n, H = self._post_args(x, y, post, res)
+        out = np.empty((T, n, H), dtype=np.uint16)
+        if self.lib.oracle_post_fwd(_ptr(x), _ptr(y), _ptr(post), _ptr(res), _ptr(out), T, n, H,
+                                    _DTYPES[dtype]) != 0:
+            raise ValueError(f"unsupported n={n} or dtype={dtype}")
+        return out
+
+    def post_bwd(self, g, x, y, post, res, dtype: str = "bf16"):
+        """(grad_x [T,n,H], grad_y [T,H], grad_post float32 [T,n], grad_res float32 [T,n,n])."""
+        x, y, post, res, T, n, H = self._post_args(x, y, post, res)
+        g = _as(g, np.uint16)
+        if g.shape != (T, n, H):
+            raise ValueError(f"g must be [{T},{n},{H}]")
+        gx = np.empty((T, n, H), dtype=np.uint16)
+        gy = np.empty((T, H), dtype=np.uint16)
+        gp = np.empty((T, n), dtype=np.float32)
+        gr = np.empty((T, n, n), dtype=np.float32)
+        if self.lib.oracle_post_bwd(_ptr(g), _ptr(x), _ptr(y), _ptr(post), _ptr(res), _ptr(gx),
+                                    _ptr(gy), _ptr(gp), _ptr(gr), T, n, H, _DTYPES[dtype]) != 0:
+            raise ValueError(f"unsupported n={n} or dtype={dtype}")
+        return gx, gy, gp, gr
+
     def fwd(self, residual, pre) -> np.ndarray:
         """out[t,h] = bf16((pre0*r0 + pre1*r1) + (pre2*r2 + pre3*r3)); uint16 [T,H]."""
         residual = _as(residual, np.uint16)
@@ -403,3 +447,11 @@ def aggregate_sigmoid_bwd(g, residual, mix, alpha, b, dtype="bf16"):
 
 def sigmoid_param_grad(grad_z, mix):
     return default().sigmoid_param_grad(grad_z, mix)
+
+
+def post_fwd(x, y, post, res, dtype="bf16"):
+    return default().post_fwd(x, y, post, res, dtype)
+
+
+def post_bwd(g, x, y, post, res, dtype="bf16"):
+    return default().post_bwd(g, x, y, post, res, dtype)

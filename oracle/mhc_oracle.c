@@ -616,3 +616,77 @@ void oracle_sigmoid32_array(const float* z, float* s, float* ds, int64_t count) 
         ds[i] = oracle_sigmoid32_grad(z[i]);
     }
 }
+
+/* ----------------------------------------------------------------------- */
+/* mHC post: the layer output expanded back onto the n residual streams      */
+/* ----------------------------------------------------------------------- */
+
+/* Source: "Add batch-invariant h_aggregate kernel", Summary, names the stage
+ * ("MHC Post") without defining it; "perf: fuse mHC coefficient backward
+ * epilogue", Summary, names its post coefficients (post sigmoid) and the
+ * residual-mixing coefficients (the n*n columns) and the "pre/post-residual
+ * kernels".  Reading used here (the hyper-connection update; not on the
+ * pages), with the pages' rules for the pre aggregate:
+ *
+ *   out[t,k,h] = cvt( tree_n( res[t,k,j] * x[t,j,h] ) + post[t,k] * y[t,h] )
+ *
+ * x [T,n,H] the n residual streams, y [T,H] the layer output, post [T,n] and
+ * res [T,n,n] FP32 (row k: output stream k; column j: input stream j), out
+ * [T,n,H]; every product and sum one RN binary32 operation, the n mixing
+ * terms in the balanced pairwise tree, then the post term added last; cvt
+ * rounds to the storage type.  The backward is the derivative with the same
+ * roundings:
+ *
+ *   grad_x[t,j,h]   = cvt( tree_n over k of res[t,k,j] * g[t,k,h] )
+ *   grad_y[t,h]     = cvt( tree_n over k of post[t,k] * g[t,k,h] )
+ *   grad_res[t,k,j] = sum over h of g[t,k,h] * x[t,j,h]    (ORDER-256)
+ *   grad_post[t,k]  = sum over h of g[t,k,h] * y[t,h]      (ORDER-256)
+ */
+
+static uint16_t post_element(const uint16_t* x, const uint16_t* y, const float* post,
+                             const float* res, int64_t t, int64_t k, int64_t h, int64_t n,
+                             int64_t H, int dtype) {
+    float p[8];
+    for (int64_t j = 0; j < n; ++j)
+        p[j] = res[(t * n + k) * n + j] * widen(x[(t * n + j) * H + h], dtype);
+    float mixed = pairwise_tree(p, (int)n);
+    float lifted = post[t * n + k] * widen(y[t * H + h], dtype);
+    return narrow(mixed + lifted, dtype);
+}
+
+/* Returns 0, or -1 for an unsupported n or dtype (nothing written). */
+int oracle_post_fwd(const uint16_t* x, const uint16_t* y, const float* post, const float* res,
+                    uint16_t* out, int64_t T, int64_t n, int64_t H, int dtype) {
+    if (!valid_streams(n) || (dtype != 0 && dtype != 1)) return -1;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t k = 0; k < n; ++k)
+            for (int64_t h = 0; h < H; ++h)
+                out[(t * n + k) * H + h] = post_element(x, y, post, res, t, k, h, n, H, dtype);
+    return 0;
+}
+
+int oracle_post_bwd(const uint16_t* g, const uint16_t* x, const uint16_t* y, const float* post,
+                    const float* res, uint16_t* grad_x, uint16_t* grad_y, float* grad_post,
+                    float* grad_res, int64_t T, int64_t n, int64_t H, int dtype) {
+    if (!valid_streams(n) || (dtype != 0 && dtype != 1)) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            for (int64_t j = 0; j < n; ++j) {
+                float q[8];
+                for (int64_t k = 0; k < n; ++k)
+                    q[k] = res[(t * n + k) * n + j] * widen(g[(t * n + k) * H + h], dtype);
+                grad_x[(t * n + j) * H + h] = narrow(pairwise_tree(q, (int)n), dtype);
+            }
+            float q[8];
+            for (int64_t k = 0; k < n; ++k) q[k] = post[t * n + k] * widen(g[(t * n + k) * H + h], dtype);
+            grad_y[t * H + h] = narrow(pairwise_tree(q, (int)n), dtype);
+        }
+        for (int64_t k = 0; k < n; ++k) {
+            const uint16_t* g_row = g + (t * n + k) * H;
+            grad_post[t * n + k] = grad_pre_row(g_row, y + t * H, H, dtype);
+            for (int64_t j = 0; j < n; ++j)
+                grad_res[(t * n + k) * n + j] = grad_pre_row(g_row, x + (t * n + j) * H, H, dtype);
+        }
+    }
+    return 0;
+}

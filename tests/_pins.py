@@ -1011,3 +1011,153 @@ ALL_CHECKS += [
     check_param_grad_order_golden,
     check_param_grad_fp64_bound,
 ]
+
+
+# --------------------------------------------------------------------------
+# mHC post (a reading; the pages name "MHC Post" but print no formula)
+# --------------------------------------------------------------------------
+
+def check_post_golden(o):
+    for name, res_s, post_s, x_s, y_s, want in golden_rows("post_worked_examples.txt"):
+        res_row = np.array([f32_from_bits(int(v, 16)) for v in res_s.split(",")], dtype=np.float32)
+        n = len(res_row)
+        res = np.zeros((1, n, n), dtype=np.float32)
+        res[0, 0] = res_row
+        res[0, 1:] = 0.5
+        post = np.full((1, n), 0.25, dtype=np.float32)
+        post[0, 0] = f32_from_bits(int(post_s, 16))
+        x = np.array([[int(v, 16) for v in x_s.split(",")]], dtype=np.uint16).reshape(1, n, 1)
+        y = np.array([[int(y_s, 16)]], dtype=np.uint16)
+        got = o.post_fwd(x, y, post, res)
+        assert int(got[0, 0, 0]) == int(want, 16), f"{name}: {hex(int(got[0, 0, 0]))}"
+
+
+def _post_exact(x_u16, y_u16, post, res, dtype):
+    widen, rnd, bits = STORAGE[dtype]
+    x = widen(x_u16)
+    y = widen(y_u16)
+    T, n, H = x.shape
+    out = np.empty((T, n, H), dtype=np.uint16)
+    for t in range(T):
+        for k in range(n):
+            for h in range(H):
+                p = [exact_mul(float(res[t, k, j]), float(x[t, j, h])) for j in range(n)]
+                while len(p) > 1:
+                    p = [exact_add(p[2 * i], p[2 * i + 1]) for i in range(len(p) // 2)]
+                s = exact_add(p[0], exact_mul(float(post[t, k]), float(y[t, h])))
+                out[t, k, h] = bits(rnd(s))
+    return out
+
+
+def check_post_exact_rational(o):
+    rng = np.random.default_rng(301)
+    for dtype in ("bf16", "f16"):
+        for n in (1, 2, 4, 8):
+            T, H = 2, 5
+            x = random_storage(rng, (T, n, H), dtype, scale=2.0)
+            y = random_storage(rng, (T, H), dtype, scale=2.0)
+            post = rng.random((T, n), dtype=np.float32) * np.float32(2.0)
+            res = rng.random((T, n, n), dtype=np.float32)
+            assert np.array_equal(o.post_fwd(x, y, post, res, dtype), _post_exact(x, y, post, res, dtype)), (dtype, n)
+
+
+def check_post_identity_and_zero(o):
+    """res = I and post = 0 return x (numerically); x = 0 returns cvt(RN(post * y))."""
+    rng = np.random.default_rng(302)
+    for n in (1, 2, 4, 8):
+        T, H = 3, 33
+        x = random_bf16(rng, (T, n, H))
+        y = random_bf16(rng, (T, H))
+        res = np.broadcast_to(np.eye(n, dtype=np.float32), (T, n, n)).copy()
+        out = o.post_fwd(x, y, np.zeros((T, n), np.float32), res)
+        assert np.array_equal(bf16_widen(out), bf16_widen(x)), n
+        post = rng.random((T, n), dtype=np.float32)
+        out0 = o.post_fwd(np.zeros_like(x), y, post, rng.random((T, n, n), dtype=np.float32))
+        want = (post[:, :, None] * bf16_widen(y)[:, None, :]).astype(np.float32)
+        assert np.array_equal(bf16_widen(out0), bf16_widen(o.bf16_from_float(want))), n
+
+
+def check_post_fp64_bound(o):
+    rng = np.random.default_rng(303)
+    T, H, n = 4, 300, 4
+    x = random_bf16(rng, (T, n, H))
+    y = random_bf16(rng, (T, H))
+    post = rng.random((T, n), dtype=np.float32)
+    res = rng.random((T, n, n), dtype=np.float32)
+    terms = res.astype(np.float64)[:, :, :, None] * bf16_widen(x).astype(np.float64)[:, None, :, :]
+    lift = post.astype(np.float64)[:, :, None] * bf16_widen(y).astype(np.float64)[:, None, :]
+    exact = terms.sum(axis=2) + lift
+    mag = np.abs(terms).sum(axis=2) + np.abs(lift)
+    got = bf16_widen(o.post_fwd(x, y, post, res)).astype(np.float64)
+    assert np.all(np.abs(got - exact) <= 0.5 * bf16_ulp(got) + 4.01 * U * mag)
+
+
+def check_post_bwd_exact(o):
+    """Integer-valued g, x, y: grad_res and grad_post are exact integer sums in any
+    order; res = I gives grad_x = g and post = e_0 gives grad_y = g[:, 0]."""
+    rng = np.random.default_rng(304)
+    lut = np.array([bf16_bits_of(float(v)) for v in range(-8, 9)], dtype=np.uint16)
+    for n in (1, 2, 4, 8):
+        T, H = 2, 2053
+        gi = rng.integers(-8, 9, size=(T, n, H))
+        xi = rng.integers(-8, 9, size=(T, n, H))
+        yi = rng.integers(-8, 9, size=(T, H))
+        post = np.zeros((T, n), np.float32)
+        post[:, 0] = 1.0
+        res = np.broadcast_to(np.eye(n, dtype=np.float32), (T, n, n)).copy()
+        gx, gy, gp, gr = o.post_bwd(lut[gi + 8], lut[xi + 8], lut[yi + 8], post, res)
+        assert np.array_equal(gp.astype(np.float64), np.einsum("tkh,th->tk", gi, yi).astype(np.float64)), n
+        assert np.array_equal(gr.astype(np.float64), np.einsum("tkh,tjh->tkj", gi, xi).astype(np.float64)), n
+        assert np.array_equal(bf16_widen(gx), bf16_widen(lut[gi + 8])), n
+        assert np.array_equal(bf16_widen(gy), bf16_widen(lut[gi[:, 0] + 8])), n
+
+
+def check_post_bwd_tree_golden(o):
+    """grad_x and grad_y take the mixing tree over k: the 'mix_tree_pairs' column
+    [1+2^-8, 0, 2^-24, 2^-24] gives 0x3F81 (left to right would give 0x3F80)."""
+    n, H = 4, 1
+    col = np.array([f32_from_bits(0x3F808000), 0.0, 2.0 ** -24, 2.0 ** -24], dtype=np.float32)
+    res = np.zeros((1, n, n), dtype=np.float32)
+    res[0, :, 2] = col                        # column j = 2: res[k, 2] for k = 0..3
+    post = col[None, :].copy()
+    g = np.full((1, n, H), 0x3F80, dtype=np.uint16)
+    x = np.full((1, n, H), 0x3F80, dtype=np.uint16)
+    y = np.full((1, H), 0x3F80, dtype=np.uint16)
+    gx, gy, _, _ = o.post_bwd(g, x, y, post, res)
+    assert int(gx[0, 2, 0]) == 0x3F81 and int(gy[0, 0]) == 0x3F81, (hex(int(gx[0, 2, 0])), hex(int(gy[0, 0])))
+
+
+def check_post_bwd_order_golden(o):
+    """grad_post is summed in ORDER-256: the golden cases, with the values in
+    row k of g and y = 1."""
+    for name, H, k, carrier, positions, expected in golden_rows("grad_pre_order_cases.txt"):
+        H, k = int(H), int(k)
+        vals = np.zeros(H, dtype=np.uint16)
+        for item in positions.split(","):
+            pos, v = item.split(":")
+            if pos == "*":
+                vals[:] = int(v, 16)
+            else:
+                vals[int(pos)] = int(v, 16)
+        n = 4
+        g = np.zeros((1, n, H), dtype=np.uint16)
+        g[0, k] = vals
+        x = np.zeros((1, n, H), dtype=np.uint16)
+        y = np.full((1, H), 0x3F80, dtype=np.uint16)
+        _, _, gp, gr = o.post_bwd(g, x, y, np.ones((1, n), np.float32), np.ones((1, n, n), np.float32))
+        assert int(f32_bits(gp)[0, k]) == int(expected, 16), name
+        # the same sums for grad_res with x = 1 in row j = 3
+        x[0, 3] = 0x3F80
+        _, _, _, gr = o.post_bwd(g, x, y, np.ones((1, n), np.float32), np.ones((1, n, n), np.float32))
+        assert int(f32_bits(gr)[0, k, 3]) == int(expected, 16), name
+
+
+ALL_CHECKS += [
+    check_post_golden,
+    check_post_exact_rational,
+    check_post_identity_and_zero,
+    check_post_fp64_bound,
+    check_post_bwd_exact,
+    check_post_bwd_tree_golden,
+    check_post_bwd_order_golden,
+]

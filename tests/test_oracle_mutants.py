@@ -128,6 +128,22 @@ MUTANTS = {
     "param_drop_ragged_tail": ("int64_t chunks = (T + ORDER_CHUNK - 1) / ORDER_CHUNK;",
                                "int64_t chunks = T / ORDER_CHUNK;"),
     "param_lanes_128": ("int lane = (int)(chunk % ORDER_LANES);", "int lane = (int)(chunk % 128);"),
+    # mHC post
+    "post_term_inside_tree": ("    float mixed = pairwise_tree(p, (int)n);\n    float lifted = post[t * n + k] * widen(y[t * H + h], dtype);",
+                              "    float lifted = post[t * n + k] * widen(y[t * H + h], dtype);\n"
+                              "    p[n - 1] = p[n - 1] + lifted; lifted = 0.0f;\n"
+                              "    float mixed = pairwise_tree(p, (int)n);"),
+    "post_wrong_post_index": ("float lifted = post[t * n + k] *", "float lifted = post[t * n + (k ^ (n > 1))] *"),
+    "post_res_transposed": ("p[j] = res[(t * n + k) * n + j] * widen(x[(t * n + j) * H + h], dtype);",
+                            "p[j] = res[(t * n + j) * n + k] * widen(x[(t * n + j) * H + h], dtype);"),
+    "post_bwd_grad_x_untransposed": ("q[k] = res[(t * n + k) * n + j] * widen(g[(t * n + k) * H + h], dtype);",
+                                     "q[k] = res[(t * n + j) * n + k] * widen(g[(t * n + k) * H + h], dtype);"),
+    "post_bwd_grad_y_without_post": ("for (int64_t k = 0; k < n; ++k) q[k] = post[t * n + k] * widen(",
+                                     "for (int64_t k = 0; k < n; ++k) q[k] = 1.0f * widen("),
+    "post_bwd_grad_post_against_x": ("grad_post[t * n + k] = grad_pre_row(g_row, y + t * H, H, dtype);",
+                                     "grad_post[t * n + k] = grad_pre_row(g_row, x + (t * n + k) * H, H, dtype);"),
+    "post_bwd_grad_res_wrong_row": ("grad_res[(t * n + k) * n + j] = grad_pre_row(g_row, x + (t * n + j) * H, H, dtype);",
+                                    "grad_res[(t * n + k) * n + j] = grad_pre_row(g_row, x + (t * n + k) * H, H, dtype);"),
     "hc_grad_pre_wrong_row": ("grad_pre_row(g + t * H, residual + (t * n + k) * H, H, dtype)",
                               "grad_pre_row(g + t * H, residual + (t * n + (k ^ 1)) * H, H, dtype)"),
 }
