@@ -638,6 +638,33 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
                     "steady": {"us": us_p, "sets": ns}})
     del g, r, mix, sets, fsets, bsets, psets
     torch.cuda.empty_cache()
+
+    # the mHC post (the layer output expanded back onto the n streams), steady state
+    from invariant_mhc_aggregate_gb300.inputs import post_inputs
+    for n in (4, 8):
+        T, H = 4096, 7168
+        x, y, post, res, g = post_inputs(T, H, n, "normal", 6, device=dev, with_grad=True)
+        fb = T * (2 * (2 * n + 1) * H + 4 * n + 4 * n * n)
+        bb = T * (2 * (3 * n + 2) * H + 8 * n + 8 * n * n)
+        ns = n_sets(fb) or 2
+        sets = [(g, x, y, post, res)] + [tuple(t.clone() for t in (g, x, y, post, res))
+                                         for _ in range(ns - 1)]
+        fsets = [(xx, yy, pp, rr, torch.empty_like(xx)) for _, xx, yy, pp, rr in sets]
+        fpath = binding.PATH_NAMES[binding.post_fwd_path_raw(*(t.data_ptr() for t in fsets[0]), T, n, H)]
+        us_f = time_steady(lambda *a: binding.mhc_post_fwd(*a), fsets)
+        del fsets
+        bsets = [(gg, xx, yy, pp, rr, torch.empty_like(xx), torch.empty_like(yy), torch.empty_like(pp),
+                  torch.empty_like(rr)) for gg, xx, yy, pp, rr in sets]
+        bpath = binding.PATH_NAMES[binding.post_bwd_path_raw(*(t.data_ptr() for t in bsets[0]), T, n, H)]
+        us_b = time_steady(lambda *a: binding.mhc_post_bwd(*a), bsets)
+        results.append({"workload": f"post_n{n}_bf16", "dir": "fwd", "T": T, "H": H, "n": n, "path": fpath,
+                        "note": "out = tree(res*x) + post*y; bytes T*(2(2n+1)H + 4n + 4n^2)",
+                        "steady": {"us": us_f, "sets": ns, **entry_for(us_f, fb)}})
+        results.append({"workload": f"post_n{n}_bf16", "dir": "bwd", "T": T, "H": H, "n": n, "path": bpath,
+                        "note": "grad_x, grad_y, grad_post, grad_res; bytes T*(2(3n+2)H + 8n + 8n^2)",
+                        "steady": {"us": us_b, "sets": ns, **entry_for(us_b, bb)}})
+        del x, y, post, res, g, sets, bsets
+        torch.cuda.empty_cache()
     torch.cuda.synchronize()
     return results
 

@@ -270,6 +270,50 @@ MHC_API mhc_status_t mhc_sigmoid_param_grad(const float* grad_z, const float* mi
                                             float* grad_alpha, int64_t T, int32_t n,
                                             mhc_stream_t stream);
 
+/* ---- mHC post: the layer output expanded back onto the n streams ----------
+ *
+ * "Add batch-invariant h_aggregate kernel", Summary, names this stage ("MHC
+ * Post") without defining it; "perf: fuse mHC coefficient backward epilogue",
+ * Summary, names its post coefficients and the n*n residual-mixing
+ * coefficients.  This library's reading (the hyper-connection update), with
+ * the rules of the aggregate above:
+ *
+ *   out[t,k,h] = cvt( tree_n( res[t,k,j] * x[t,j,h] ) + post[t,k] * y[t,h] )
+ *
+ * every product and sum one RN binary32 operation, the n mixing terms in the
+ * balanced pairwise tree, the post term added last.  Its backward:
+ *
+ *   grad_x[t,j,h]   = cvt( tree_n over k of res[t,k,j] * g[t,k,h] )
+ *   grad_y[t,h]     = cvt( tree_n over k of post[t,k] * g[t,k,h] )
+ *   grad_res[t,k,j] = sum over h of g[t,k,h] * x[t,j,h]    (ORDER-256)
+ *   grad_post[t,k]  = sum over h of g[t,k,h] * y[t,h]      (ORDER-256)
+ *
+ *   x, out, g, grad_x   [T,n,H] dtype      y, grad_y   [T,H] dtype
+ *   post, grad_post     FP32 [T,n]         res, grad_res  FP32 [T,n,n]
+ *                                           (row k = output stream k)
+ * n in {1, 2, 4, 8}; the other rules (errors, ownership, determinism,
+ * alignment) as for the aggregate.  Paths: the forward takes 32- or 16-byte
+ * vectors (H % 16 / H % 8 == 0 and the 2-byte buffers 32- / 16-byte aligned),
+ * the backward 16-byte vectors, both else the 2-byte path.
+ */
+MHC_API mhc_status_t mhc_post_fwd(const void* x, const void* y, const float* post, const float* res,
+                                  void* out, int64_t T, int32_t n, int64_t H, mhc_dtype_t dtype,
+                                  mhc_stream_t stream);
+
+MHC_API mhc_status_t mhc_post_bwd(const void* grad_out, const void* x, const void* y,
+                                  const float* post, const float* res, void* grad_x, void* grad_y,
+                                  float* grad_post, float* grad_res, int64_t T, int32_t n,
+                                  int64_t H, mhc_dtype_t dtype, mhc_stream_t stream);
+
+/* Kernel path of the two calls (no launch, no CUDA call). */
+MHC_API mhc_path_t mhc_post_fwd_path(const void* x, const void* y, const float* post,
+                                     const float* res, const void* out, int64_t T, int32_t n,
+                                     int64_t H);
+MHC_API mhc_path_t mhc_post_bwd_path(const void* grad_out, const void* x, const void* y,
+                                     const float* post, const float* res, const void* grad_x,
+                                     const void* grad_y, const float* grad_post,
+                                     const float* grad_res, int64_t T, int32_t n, int64_t H);
+
 /* Static text for a status code. */
 MHC_API const char* mhc_status_string(mhc_status_t status);
 

@@ -106,3 +106,52 @@ def h_aggregate_sigmoid(residual: torch.Tensor, mix: torch.Tensor, alpha: torch.
                         b: torch.Tensor) -> torch.Tensor:
     """Differentiable aggregate with pre = sigmoid(alpha * mix + b) computed in the kernel."""
     return HAggregateSigmoid.apply(residual, mix, alpha, b)
+
+
+class MhcPost(torch.autograd.Function):
+    """out[..., k, :] = tree_n(res[..., k, j] * x[..., j, :]) + post[..., k] * y —
+    the layer output y expanded back onto the n streams (the library's reading
+    of the "MHC Post" stage named in "Add batch-invariant h_aggregate kernel",
+    Summary).  Forward and backward are one kernel each; the backward gives
+    all four gradients, grad_post and grad_res summed over H in ORDER-256."""
+
+    @staticmethod
+    def forward(ctx, x, y, post, res):
+        if x.dtype not in (torch.bfloat16, torch.float16) or y.dtype != x.dtype:
+            raise TypeError("expects x [...,n,H] and y [...,H] of one type, bf16 or f16")
+        if post.dtype != torch.float32 or res.dtype != torch.float32:
+            raise TypeError("expects post [...,n] and res [...,n,n] fp32")
+        if x.dim() < 2:
+            raise ValueError(f"x must be [...,n,H], got {tuple(x.shape)}")
+        lead = x.shape[:-2]
+        n, H = x.shape[-2], x.shape[-1]
+        if y.shape != (*lead, H) or post.shape != (*lead, n) or res.shape != (*lead, n, n):
+            raise ValueError(f"shape mismatch: x {tuple(x.shape)}, y {tuple(y.shape)}, "
+                             f"post {tuple(post.shape)}, res {tuple(res.shape)}")
+        xx = x.reshape(-1, n, H).contiguous()
+        yy = y.reshape(-1, H).contiguous()
+        pp = post.reshape(-1, n).contiguous()
+        rr = res.reshape(-1, n, n).contiguous()
+        out = binding.post(xx, yy, pp, rr)
+        ctx.save_for_backward(xx, yy, pp, rr)
+        ctx.lead = lead
+        return out.reshape(*lead, n, H)
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        xx, yy, pp, rr = ctx.saved_tensors
+        n, H = xx.shape[-2], xx.shape[-1]
+        if grad_out.dtype != xx.dtype:
+            raise TypeError(f"the output gradient must be {xx.dtype}, got {grad_out.dtype}")
+        g = grad_out.reshape(-1, n, H).contiguous()
+        gx, gy, gp, gr = binding.post_backward(g, xx, yy, pp, rr)
+        lead = ctx.lead
+        return (gx.reshape(*lead, n, H) if ctx.needs_input_grad[0] else None,
+                gy.reshape(*lead, H) if ctx.needs_input_grad[1] else None,
+                gp.reshape(*lead, n) if ctx.needs_input_grad[2] else None,
+                gr.reshape(*lead, n, n) if ctx.needs_input_grad[3] else None)
+
+
+def mhc_post(x: torch.Tensor, y: torch.Tensor, post: torch.Tensor, res: torch.Tensor) -> torch.Tensor:
+    """Differentiable mHC post (see MhcPost)."""
+    return MhcPost.apply(x, y, post, res)

@@ -52,6 +52,10 @@ EXPORTS = (
     "mhc_aggregate_sigmoid_fwd",
     "mhc_aggregate_sigmoid_bwd",
     "mhc_sigmoid_param_grad",
+    "mhc_post_fwd",
+    "mhc_post_bwd",
+    "mhc_post_fwd_path",
+    "mhc_post_bwd_path",
     "mhc_status_string",
     "mhc_h_aggregate_last_cuda_error",
 )
@@ -115,6 +119,14 @@ def load(path: str | None = None):
         lib.mhc_aggregate_sigmoid_bwd.restype = i32
         lib.mhc_sigmoid_param_grad.argtypes = [p, p, p, p, i64, i32, p]
         lib.mhc_sigmoid_param_grad.restype = i32
+        lib.mhc_post_fwd.argtypes = [p, p, p, p, p, i64, i32, i64, i32, p]
+        lib.mhc_post_fwd.restype = i32
+        lib.mhc_post_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i64, i32, i64, i32, p]
+        lib.mhc_post_bwd.restype = i32
+        lib.mhc_post_fwd_path.argtypes = [p, p, p, p, p, i64, i32, i64]
+        lib.mhc_post_fwd_path.restype = i32
+        lib.mhc_post_bwd_path.argtypes = [p, p, p, p, p, p, p, p, p, i64, i32, i64]
+        lib.mhc_post_bwd_path.restype = i32
         lib.mhc_status_string.argtypes = [i32]
         lib.mhc_status_string.restype = ctypes.c_char_p
         lib.mhc_h_aggregate_last_cuda_error.argtypes = []
@@ -186,6 +198,28 @@ def agg_sigmoid_bwd_raw(grad_out: int, residual: int, mix: int, alpha: int, b: i
 def sigmoid_param_grad_raw(grad_z: int, mix: int, grad_b: int, grad_alpha: int, T: int, n: int,
                            stream: int = 0) -> int:
     return load().mhc_sigmoid_param_grad(grad_z, mix, grad_b, grad_alpha, T, n, stream)
+
+
+def post_fwd_raw(x: int, y: int, post: int, res: int, out: int, T: int, n: int, H: int, dtype: int,
+                 stream: int = 0) -> int:
+    return load().mhc_post_fwd(x, y, post, res, out, T, n, H, dtype, stream)
+
+
+def post_bwd_raw(grad_out: int, x: int, y: int, post: int, res: int, grad_x: int, grad_y: int,
+                 grad_post: int, grad_res: int, T: int, n: int, H: int, dtype: int,
+                 stream: int = 0) -> int:
+    return load().mhc_post_bwd(grad_out, x, y, post, res, grad_x, grad_y, grad_post, grad_res,
+                               T, n, H, dtype, stream)
+
+
+def post_fwd_path_raw(x: int, y: int, post: int, res: int, out: int, T: int, n: int, H: int) -> int:
+    return load().mhc_post_fwd_path(x, y, post, res, out, T, n, H)
+
+
+def post_bwd_path_raw(grad_out: int, x: int, y: int, post: int, res: int, grad_x: int, grad_y: int,
+                      grad_post: int, grad_res: int, T: int, n: int, H: int) -> int:
+    return load().mhc_post_bwd_path(grad_out, x, y, post, res, grad_x, grad_y, grad_post,
+                                    grad_res, T, n, H)
 
 
 # ---------------------------------------------------------------------------
@@ -457,3 +491,65 @@ def sigmoid_param_grad(grad_z: torch.Tensor, mix: torch.Tensor, stream=None):
     grad_alpha = torch.empty((1,), dtype=torch.float32, device=grad_z.device)
     mhc_sigmoid_param_grad(grad_z, mix, grad_b, grad_alpha, stream)
     return grad_b, grad_alpha
+
+
+# ---------------------------------------------------------------------------
+# mHC post: out[t,k] = tree_n(res[t,k,j] * x[t,j]) + post[t,k] * y[t]
+# ---------------------------------------------------------------------------
+
+def _post_shapes(x: torch.Tensor, y: torch.Tensor, post: torch.Tensor, res: torch.Tensor):
+    T, n, H = _TnH(x)
+    dt = _storage(x, "x")
+    _check(x, "x", x.dtype, (T, n, H))
+    _check(y, "y", x.dtype, (T, H))
+    _check(post, "post", torch.float32, (T, n))
+    _check(res, "res", torch.float32, (T, n, n))
+    return T, n, H, dt
+
+
+def mhc_post_fwd(x: torch.Tensor, y: torch.Tensor, post: torch.Tensor, res: torch.Tensor,
+                 out: torch.Tensor, stream=None) -> None:
+    """out [T,n,H] = the n streams mixed by res plus post times the layer output y."""
+    T, n, H, dt = _post_shapes(x, y, post, res)
+    _check(out, "out", x.dtype, (T, n, H))
+    st = post_fwd_raw(x.data_ptr(), y.data_ptr(), post.data_ptr(), res.data_ptr(), out.data_ptr(),
+                      T, n, H, dt, _stream_handle(stream, x.device))
+    if st != MHC_OK:
+        raise MhcError(st, "mhc_post_fwd")
+
+
+def mhc_post_bwd(grad_out: torch.Tensor, x: torch.Tensor, y: torch.Tensor, post: torch.Tensor,
+                 res: torch.Tensor, grad_x: torch.Tensor, grad_y: torch.Tensor,
+                 grad_post: torch.Tensor, grad_res: torch.Tensor, stream=None) -> None:
+    """Fused backward: grad_x, grad_y, and grad_post / grad_res summed over H in ORDER-256."""
+    T, n, H, dt = _post_shapes(x, y, post, res)
+    _check(grad_out, "grad_out", x.dtype, (T, n, H))
+    _check(grad_x, "grad_x", x.dtype, (T, n, H))
+    _check(grad_y, "grad_y", x.dtype, (T, H))
+    _check(grad_post, "grad_post", torch.float32, (T, n))
+    _check(grad_res, "grad_res", torch.float32, (T, n, n))
+    st = post_bwd_raw(grad_out.data_ptr(), x.data_ptr(), y.data_ptr(), post.data_ptr(),
+                      res.data_ptr(), grad_x.data_ptr(), grad_y.data_ptr(), grad_post.data_ptr(),
+                      grad_res.data_ptr(), T, n, H, dt, _stream_handle(stream, x.device))
+    if st != MHC_OK:
+        raise MhcError(st, "mhc_post_bwd")
+
+
+def post(x: torch.Tensor, y: torch.Tensor, post_coeffs: torch.Tensor, res: torch.Tensor,
+         stream=None) -> torch.Tensor:
+    """Allocate ``out`` [T,n,H] and run the post forward."""
+    out = torch.empty_like(x)
+    mhc_post_fwd(x, y, post_coeffs, res, out, stream)
+    return out
+
+
+def post_backward(grad_out: torch.Tensor, x: torch.Tensor, y: torch.Tensor,
+                  post_coeffs: torch.Tensor, res: torch.Tensor, stream=None):
+    """Allocate and return (grad_x [T,n,H], grad_y [T,H], grad_post [T,n], grad_res [T,n,n])."""
+    T, n, H = _TnH(x)
+    grad_x = torch.empty_like(x)
+    grad_y = torch.empty((T, H), dtype=x.dtype, device=x.device)
+    grad_post = torch.empty((T, n), dtype=torch.float32, device=x.device)
+    grad_res = torch.empty((T, n, n), dtype=torch.float32, device=x.device)
+    mhc_post_bwd(grad_out, x, y, post_coeffs, res, grad_x, grad_y, grad_post, grad_res, stream)
+    return grad_x, grad_y, grad_post, grad_res

@@ -809,3 +809,4 @@ sigmoid_param_grad_kernel(const float* __restrict__ grad_z, const float* __restr
 }  // namespace mhc
 
 #include "mhc_shift.cuh"
+#include "mhc_post.cuh"

@@ -15,7 +15,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 3;
+constexpr int kAbiVersion = 4;
 
 thread_local int32_t g_last_cuda_error = 0;
 
@@ -248,6 +248,91 @@ mhc_status_t sigmoid_param_grad(const float* grad_z, const float* mix, float* gr
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// ---- mHC post ---------------------------------------------------------------
+
+// Disjointness of a set of output ranges from each other and from the inputs.
+bool disjoint(const Range* outs, int n_outs, const Range* ins, int n_ins) {
+    for (int a = 0; a < n_outs; ++a) {
+        for (int b = a + 1; b < n_outs; ++b)
+            if (overlap(outs[a], outs[b])) return false;
+        for (int i = 0; i < n_ins; ++i)
+            if (overlap(outs[a], ins[i])) return false;
+    }
+    return true;
+}
+
+mhc_path_t post_fwd_path(const void* x, const void* y, const float* post, const float* res,
+                         const void* out, int64_t T, int64_t n, int64_t H) {
+    if (!streams_ok(n) || !sizes_ok(T, n, H) || T == 0) return MHC_PATH_NONE;
+    if (!x || !y || !post || !res || !out) return MHC_PATH_NONE;
+    if (!aligned(x, 2) || !aligned(y, 2) || !aligned(out, 2) || !aligned(post, 4) || !aligned(res, 4))
+        return MHC_PATH_NONE;
+    const uint64_t TH = uint64_t(T) * uint64_t(H), nu = uint64_t(n);
+    const Range outs[1] = {range_of(out, TH * 2 * nu)};
+    const Range ins[4] = {range_of(x, TH * 2 * nu), range_of(y, TH * 2),
+                          range_of(post, uint64_t(T) * 4 * nu), range_of(res, uint64_t(T) * 4 * nu * nu)};
+    if (!disjoint(outs, 1, ins, 4)) return MHC_PATH_NONE;
+    if (H % 16 == 0 && aligned(x, 32) && aligned(y, 32) && aligned(out, 32)) return MHC_PATH_VEC32;
+    if (H % 8 == 0 && aligned(x, 16) && aligned(y, 16) && aligned(out, 16)) return MHC_PATH_VEC16;
+    return MHC_PATH_ELEMENT;
+}
+
+mhc_path_t post_bwd_path(const void* g, const void* x, const void* y, const float* post,
+                         const float* res, const void* grad_x, const void* grad_y,
+                         const float* grad_post, const float* grad_res, int64_t T, int64_t n,
+                         int64_t H) {
+    if (!streams_ok(n) || !sizes_ok(T, n, H) || T == 0) return MHC_PATH_NONE;
+    if (!g || !x || !y || !post || !res || !grad_x || !grad_y || !grad_post || !grad_res)
+        return MHC_PATH_NONE;
+    if (!aligned(g, 2) || !aligned(x, 2) || !aligned(y, 2) || !aligned(grad_x, 2) ||
+        !aligned(grad_y, 2) || !aligned(post, 4) || !aligned(res, 4) || !aligned(grad_post, 4) ||
+        !aligned(grad_res, 4))
+        return MHC_PATH_NONE;
+    const uint64_t TH = uint64_t(T) * uint64_t(H), nu = uint64_t(n);
+    const Range outs[4] = {range_of(grad_x, TH * 2 * nu), range_of(grad_y, TH * 2),
+                           range_of(grad_post, uint64_t(T) * 4 * nu),
+                           range_of(grad_res, uint64_t(T) * 4 * nu * nu)};
+    const Range ins[5] = {range_of(g, TH * 2 * nu), range_of(x, TH * 2 * nu), range_of(y, TH * 2),
+                          range_of(post, uint64_t(T) * 4 * nu), range_of(res, uint64_t(T) * 4 * nu * nu)};
+    if (!disjoint(outs, 4, ins, 5)) return MHC_PATH_NONE;
+    if (H % 8 == 0 && aligned(g, 16) && aligned(x, 16) && aligned(y, 16) && aligned(grad_x, 16) &&
+        aligned(grad_y, 16))
+        return MHC_PATH_VEC16;
+    return MHC_PATH_ELEMENT;
+}
+
+mhc_status_t post_fwd(const void* x, const void* y, const float* post, const float* res, void* out,
+                      int64_t T, int64_t n, int64_t H, int32_t dtype, mhc_stream_t stream) {
+    if (!dtype_ok(dtype)) return MHC_ERR_INVALID_ARG;
+    if (!streams_ok(n)) return MHC_ERR_UNSUPPORTED;
+    if (!sizes_ok(T, n, H)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    const mhc_path_t path = post_fwd_path(x, y, post, res, out, T, n, H);
+    if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
+    if ((path == MHC_PATH_VEC32 || path == MHC_PATH_VEC16) && uint64_t(H) / 8 > 0x7FFFFFFFull)
+        return MHC_ERR_UNSUPPORTED;
+    const mhc::PostFwdCall c{x, y, post, res, out, uint64_t(T), uint64_t(H), int(n), int(path),
+                             num_sms(), reinterpret_cast<cudaStream_t>(stream)};
+    return finish(mhc::post_fwd(c, dtype == MHC_DTYPE_BF16 ? mhc::kBF16 : mhc::kF16));
+}
+
+mhc_status_t post_bwd(const void* g, const void* x, const void* y, const float* post, const float* res,
+                      void* grad_x, void* grad_y, float* grad_post, float* grad_res, int64_t T,
+                      int64_t n, int64_t H, int32_t dtype, mhc_stream_t stream) {
+    if (!dtype_ok(dtype)) return MHC_ERR_INVALID_ARG;
+    if (!streams_ok(n)) return MHC_ERR_UNSUPPORTED;
+    if (!sizes_ok(T, n, H)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    const mhc_path_t path =
+        post_bwd_path(g, x, y, post, res, grad_x, grad_y, grad_post, grad_res, T, n, H);
+    if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
+    if (path == MHC_PATH_VEC16 && uint64_t(H) / 8 > 0x7FFFFFFFull) return MHC_ERR_UNSUPPORTED;
+    const mhc::PostBwdCall c{g, x, y, post, res, grad_x, grad_y, grad_post, grad_res, uint64_t(T),
+                             uint64_t(H), int(n), int(path), num_sms(),
+                             reinterpret_cast<cudaStream_t>(stream)};
+    return finish(mhc::post_bwd(c, dtype == MHC_DTYPE_BF16 ? mhc::kBF16 : mhc::kF16));
+}
+
 }  // namespace
 
 // --------------------------------------------------------------------------
@@ -340,6 +425,32 @@ mhc_status_t mhc_aggregate_sigmoid_bwd(const void* grad_out, const void* residua
 mhc_status_t mhc_sigmoid_param_grad(const float* grad_z, const float* mix, float* grad_b,
                                     float* grad_alpha, int64_t T, int32_t n, mhc_stream_t stream) {
     return sigmoid_param_grad(grad_z, mix, grad_b, grad_alpha, T, n, stream);
+}
+
+mhc_status_t mhc_post_fwd(const void* x, const void* y, const float* post, const float* res,
+                          void* out, int64_t T, int32_t n, int64_t H, mhc_dtype_t dtype,
+                          mhc_stream_t stream) {
+    return post_fwd(x, y, post, res, out, T, n, H, int32_t(dtype), stream);
+}
+
+mhc_status_t mhc_post_bwd(const void* grad_out, const void* x, const void* y, const float* post,
+                          const float* res, void* grad_x, void* grad_y, float* grad_post,
+                          float* grad_res, int64_t T, int32_t n, int64_t H, mhc_dtype_t dtype,
+                          mhc_stream_t stream) {
+    return post_bwd(grad_out, x, y, post, res, grad_x, grad_y, grad_post, grad_res, T, n, H,
+                    int32_t(dtype), stream);
+}
+
+mhc_path_t mhc_post_fwd_path(const void* x, const void* y, const float* post, const float* res,
+                             const void* out, int64_t T, int32_t n, int64_t H) {
+    return post_fwd_path(x, y, post, res, out, T, n, H);
+}
+
+mhc_path_t mhc_post_bwd_path(const void* grad_out, const void* x, const void* y, const float* post,
+                             const float* res, const void* grad_x, const void* grad_y,
+                             const float* grad_post, const float* grad_res, int64_t T, int32_t n,
+                             int64_t H) {
+    return post_bwd_path(grad_out, x, y, post, res, grad_x, grad_y, grad_post, grad_res, T, n, H);
 }
 
 }  // extern "C"

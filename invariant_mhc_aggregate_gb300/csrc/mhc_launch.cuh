@@ -51,6 +51,40 @@ cudaError_t fwd_f16(const FwdCall& c, const SigmoidCoeffs& k);
 cudaError_t bwd_bf16(const BwdCall& c, const SigmoidCoeffs& k);
 cudaError_t bwd_f16(const BwdCall& c, const SigmoidCoeffs& k);
 
+// mHC post (mhc_post.cuh, launched from mhc_launch_post.cu).
+struct PostFwdCall {
+    const void* x;
+    const void* y;
+    const float* post;
+    const float* res;
+    void* out;
+    uint64_t T, H;
+    int n;
+    int path;
+    int num_sms;
+    cudaStream_t stream;
+};
+
+struct PostBwdCall {
+    const void* g;
+    const void* x;
+    const void* y;
+    const float* post;
+    const float* res;
+    void* grad_x;
+    void* grad_y;
+    float* grad_post;
+    float* grad_res;
+    uint64_t T, H;
+    int n;
+    int path;
+    int num_sms;
+    cudaStream_t stream;
+};
+
+cudaError_t post_fwd(const PostFwdCall& c, int dtype);
+cudaError_t post_bwd(const PostBwdCall& c, int dtype);
+
 // The coefficient kernels of their own (mhc_launch_coeffs.cu).
 cudaError_t pre_sigmoid(const float* mix, const float* alpha, const float* b, float* pre,
                         uint64_t T, int n, int num_sms, cudaStream_t stream);

@@ -29,6 +29,18 @@ For the pre coefficients computed from the mix (``coeff_inputs``): ``mix``
                 subnormal range); alpha and b as ``normal``
 ==============  =====================================================================
 
+For the mHC post (``post_inputs``): ``x`` ``[T,n,H]`` (the streams), ``y``
+``[T,H]`` (the layer output), ``post`` ``[T,n]`` and ``res`` ``[T,n,n]`` FP32,
+and for the backward ``g`` ``[T,n,H]``:
+
+==============  =====================================================================
+``normal``      x, y, g ~ N(0,1) rounded to the storage type; post ~ 2*U(0,1); each
+                row of res = exp(N(0,1)) divided by its row sum (rows of positive
+                mixing weights near a unit sum)
+``ragged``      as ``normal``; then 10% of tokens get res = the identity and 5% of
+                post entries exactly 0.0
+==============  =====================================================================
+
 Every draw comes from one ``torch.Generator`` seeded with the workload's seed,
 in a fixed order (residual, pre, masks, g), so a (recipe, T, H, seed, device)
 tuple always gives the same bytes on a given PyTorch build.
@@ -123,6 +135,34 @@ def coeff_inputs(T: int, n: int = 4, recipe: str = "normal", seed: int = 5,
         mix = torch.where(u < 0.05, torch.zeros_like(mix), mix)
         mix = torch.where((u >= 0.05) & (u < 0.07), 100.0 * sign, mix)
     return mix.contiguous(), alpha, b
+
+
+POST_RECIPES = ("normal", "ragged")
+
+
+def post_inputs(T: int, H: int, n: int = 4, recipe: str = "normal", seed: int = 6,
+                device="cpu", dtype=torch.bfloat16, with_grad: bool = False):
+    """(x [T,n,H], y [T,H], post fp32 [T,n], res fp32 [T,n,n]) drawn on ``device``,
+    then g [T,n,H] when ``with_grad``; x, y and g in `dtype`."""
+    if recipe not in POST_RECIPES:
+        raise ValueError(f"unknown recipe {recipe!r}; expected one of {POST_RECIPES}")
+    gen = _generator(device, seed)
+    f32 = torch.float32
+    x = torch.randn((T, n, H), generator=gen, device=device, dtype=f32).to(dtype)
+    y = torch.randn((T, H), generator=gen, device=device, dtype=f32).to(dtype)
+    post = 2.0 * torch.rand((T, n), generator=gen, device=device, dtype=f32)
+    w = torch.exp(torch.randn((T, n, n), generator=gen, device=device, dtype=f32))
+    res = w / w.sum(dim=-1, keepdim=True)
+    if recipe == "ragged":
+        ident = torch.rand((T,), generator=gen, device=device, dtype=f32) < 0.10
+        eye = torch.eye(n, device=device, dtype=f32).expand(T, n, n)
+        res = torch.where(ident[:, None, None], eye, res)
+        zero = torch.rand((T, n), generator=gen, device=device, dtype=f32) < 0.05
+        post = torch.where(zero, torch.zeros_like(post), post)
+    out = [x.contiguous(), y.contiguous(), post.contiguous(), res.contiguous()]
+    if with_grad:
+        out.append(torch.randn((T, n, H), generator=gen, device=device, dtype=f32).to(dtype))
+    return tuple(out)
 
 
 def _draw_forward(T, H, recipe, gen, device, n=4, dtype=torch.bfloat16):

@@ -9,6 +9,8 @@ Families (one step = forward then backward):
   plain     mhc_aggregate_fwd / mhc_aggregate_bwd (pre given)
   sigmoid   mhc_aggregate_sigmoid_fwd / mhc_aggregate_sigmoid_bwd, then
             mhc_sigmoid_param_grad (pre computed from the mix)
+  post      mhc_post_fwd / mhc_post_bwd (the layer output expanded onto the
+            n streams)
 
 The buffers are PyTorch allocations (512-byte aligned), so the path follows
 from H: H % 16 == 0 the 32-byte path, H % 8 == 0 the 16-byte path, even H
@@ -25,7 +27,7 @@ import argparse
 import torch
 
 from . import _build, binding
-from .inputs import backward_inputs, coeff_inputs
+from .inputs import backward_inputs, coeff_inputs, post_inputs
 
 
 def _shifted(t: torch.Tensor, offset: int) -> torch.Tensor:
@@ -39,9 +41,44 @@ def _shifted(t: torch.Tensor, offset: int) -> torch.Tensor:
     return view
 
 
+def _time(step, steps: int) -> float:
+    step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / steps
+
+
+def _post(args, dev, dtype) -> None:
+    T, H, n = args.T, args.H, args.n
+    x, y, post, res, g = post_inputs(T, H, n, "normal", 6, device=dev, dtype=dtype, with_grad=True)
+    x, y, g = (_shifted(t, args.offset) for t in (x, y, g))
+    out = _shifted(torch.empty_like(x), args.offset)
+    gx = _shifted(torch.empty_like(x), args.offset)
+    gy = _shifted(torch.empty_like(y), args.offset)
+    gp, gr = torch.empty_like(post), torch.empty_like(res)
+    paths = (binding.PATH_NAMES[binding.post_fwd_path_raw(x.data_ptr(), y.data_ptr(), post.data_ptr(),
+                                                           res.data_ptr(), out.data_ptr(), T, n, H)],
+             binding.PATH_NAMES[binding.post_bwd_path_raw(*(t.data_ptr() for t in (g, x, y, post, res, gx,
+                                                                                  gy, gp, gr)), T, n, H)])
+
+    def step():
+        binding.mhc_post_fwd(x, y, post, res, out)
+        binding.mhc_post_bwd(g, x, y, post, res, gx, gy, gp, gr)
+
+    us = _time(step, args.steps)
+    print(f"post T={T} H={H} n={n} {args.dtype} offset={args.offset} paths fwd/bwd={paths[0]}/"
+          f"{paths[1]}: {us:.1f} us per step")
+
+
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--family", choices=("plain", "sigmoid"), default="plain")
+    ap.add_argument("--family", choices=("plain", "sigmoid", "post"), default="plain")
     ap.add_argument("--T", type=int, default=4096)
     ap.add_argument("--H", type=int, default=7168)
     ap.add_argument("--n", type=int, default=4)
@@ -55,6 +92,9 @@ def main(argv=None) -> None:
     dev = torch.device("cuda", 0)
     dtype = torch.bfloat16 if args.dtype == "bf16" else torch.float16
     T, H, n = args.T, args.H, args.n
+    if args.family == "post":
+        _post(args, dev, dtype)
+        return
     g, res, pre = backward_inputs(T, H, "normal", 4, device=dev, n=n, dtype=dtype)
     g, res = _shifted(g, args.offset), _shifted(res, args.offset)
     out = _shifted(torch.empty((T, H), dtype=dtype, device=dev), args.offset)

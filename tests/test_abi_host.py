@@ -50,7 +50,7 @@ def test_only_the_c_abi_is_exported():
 
 
 def test_abi_version(lib):
-    assert lib.mhc_h_aggregate_abi_version() == 3
+    assert lib.mhc_h_aggregate_abi_version() == 4
 
 
 def test_status_strings(lib):
@@ -338,3 +338,87 @@ def test_sigmoid_param_grad_invalid_arguments(lib):
     assert binding.sigmoid_param_grad_raw(gz, mix, gz + 64, ga, 8, 4) == binding.MHC_ERR_INVALID_ARG
     assert binding.sigmoid_param_grad_raw(gz, mix, gb, mix + 4, 8, 4) == binding.MHC_ERR_INVALID_ARG
     assert binding.sigmoid_param_grad_raw(gz, mix, gb + 2, ga, 8, 4) == binding.MHC_ERR_INVALID_ARG
+
+
+# --- mHC post: path choice and rejected calls
+
+def post_fpath(x_off=0, y_off=0, p_off=0, r_off=0, o_off=0, T=4, n=4, H=4096):
+    return binding.post_fwd_path_raw(A + x_off, A + GAP + y_off, A + 2 * GAP + p_off,
+                                     A + 3 * GAP + r_off, A + 4 * GAP + o_off, T, n, H)
+
+
+def post_bpath(offs=(0,) * 9, T=4, n=4, H=4096):
+    return binding.post_bwd_path_raw(*(A + i * GAP + o for i, o in enumerate(offs)), T, n, H)
+
+
+def test_post_fwd_path_choice(lib):
+    assert post_fpath() == binding.MHC_PATH_VEC32
+    assert post_fpath(p_off=4, r_off=4) == binding.MHC_PATH_VEC32     # coefficients need 4 bytes
+    assert post_fpath(y_off=16) == binding.MHC_PATH_VEC16
+    assert post_fpath(o_off=16) == binding.MHC_PATH_VEC16
+    assert post_fpath(H=4104) == binding.MHC_PATH_VEC16
+    assert post_fpath(x_off=8) == binding.MHC_PATH_ELEMENT
+    assert post_fpath(H=4100) == binding.MHC_PATH_ELEMENT
+    assert post_fpath(H=1279, n=8) == binding.MHC_PATH_ELEMENT
+    assert post_fpath(x_off=1) == binding.MHC_PATH_NONE
+    assert post_fpath(r_off=2) == binding.MHC_PATH_NONE
+    assert post_fpath(n=3) == binding.MHC_PATH_NONE
+    assert post_fpath(T=0) == binding.MHC_PATH_NONE
+
+
+def test_post_bwd_path_choice(lib):
+    assert post_bpath() == binding.MHC_PATH_VEC16
+    assert post_bpath(H=4104) == binding.MHC_PATH_VEC16
+    for i in range(5):   # any 2-byte buffer off 16 bytes: the 2-byte path
+        offs = [0] * 9
+        offs[i if i < 3 else i + 2] = 8
+        assert post_bpath(tuple(offs)) == binding.MHC_PATH_ELEMENT, i
+    assert post_bpath(H=4100) == binding.MHC_PATH_ELEMENT
+    assert post_bpath((0, 0, 0, 0, 0, 0, 0, 2, 0)) == binding.MHC_PATH_NONE
+    assert post_bpath(T=0) == binding.MHC_PATH_NONE
+
+
+def test_post_rejects_overlap(lib):
+    T, n, H = 4, 4, 64
+    x, y, p, r, o = A, A + GAP, A + 2 * GAP, A + 3 * GAP, A + 4 * GAP
+    assert binding.post_fwd_path_raw(x, y, p, r, x + 64, T, n, H) == binding.MHC_PATH_NONE
+    assert binding.post_fwd_path_raw(x, y, p, r, y, T, n, H) == binding.MHC_PATH_NONE
+    assert binding.post_fwd_path_raw(x, y, p, o + 256, o, T, n, H) == binding.MHC_PATH_NONE
+    assert binding.post_fwd_path_raw(x, y, p, r, x + T * n * H * 2, T, n, H) == binding.MHC_PATH_VEC32
+    bufs = [A + i * GAP for i in range(9)]
+    # every output against every other buffer
+    for out in range(5, 9):
+        for other in range(9):
+            if other == out:
+                continue
+            b = list(bufs)
+            b[out] = b[other] + 16
+            assert binding.post_bwd_path_raw(*b, T, n, H) == binding.MHC_PATH_NONE, (out, other)
+
+
+def test_post_invalid_arguments(lib):
+    bf16 = binding.MHC_DTYPE_BF16
+    f = [A + i * GAP for i in range(5)]
+    assert binding.post_fwd_raw(*f, 4, 3, 64, bf16) == binding.MHC_ERR_UNSUPPORTED
+    assert binding.post_fwd_raw(*f, 4, 4, 64, 9) == binding.MHC_ERR_INVALID_ARG
+    assert binding.post_fwd_raw(*f, -1, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG
+    assert binding.post_fwd_raw(*f, 4, 4, 0, bf16) == binding.MHC_ERR_INVALID_ARG
+    assert binding.post_fwd_raw(0, 0, 0, 0, 0, 0, 4, 64, bf16) == binding.MHC_OK
+    for i in range(5):
+        bad = list(f)
+        bad[i] = 0
+        assert binding.post_fwd_raw(*bad, 4, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG, i
+    b = [A + i * GAP for i in range(9)]
+    assert binding.post_bwd_raw(*b, 4, 5, 64, bf16) == binding.MHC_ERR_UNSUPPORTED
+    assert binding.post_bwd_raw(*b, 4, 4, 64, -1) == binding.MHC_ERR_INVALID_ARG
+    assert binding.post_bwd_raw(*([0] * 9), 0, 2, 64, binding.MHC_DTYPE_F16) == binding.MHC_OK
+    for i in range(9):
+        bad = list(b)
+        bad[i] = 0
+        assert binding.post_bwd_raw(*bad, 4, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG, i
+    bad = list(b)
+    bad[8] += 2      # grad_res not FP32 aligned
+    assert binding.post_bwd_raw(*bad, 4, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG
+    # byte count of an n = 8 x overflows int64
+    assert binding.post_fwd_raw(*f, 1 << 31, 8, 1 << 29, bf16) == binding.MHC_ERR_INVALID_ARG
+    assert lib.mhc_h_aggregate_last_cuda_error() == 0

@@ -1,0 +1,255 @@
+"""The mHC post on the GPU, against the CPU oracle byte for byte through the C ABI.
+
+Source: "Add batch-invariant h_aggregate kernel", Summary, names the stage
+("MHC Post"); "perf: fuse mHC coefficient backward epilogue", Summary, names
+its post and residual-mixing coefficients.  The formula is the library's
+reading (the hyper-connection update, see the oracle):
+    out[t,k,h]      = cvt(tree_n(res[t,k,j] * x[t,j,h]) + post[t,k] * y[t,h])
+    grad_x[t,j,h]   = cvt(tree_n over k of res[t,k,j] * g[t,k,h])
+    grad_y[t,h]     = cvt(tree_n over k of post[t,k] * g[t,k,h])
+    grad_res, grad_post: sums over h in ORDER-256.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _gpu import (DTYPE_CODE, DTYPE_NAME, DevBuf, _align_of, assert_bytes_equal, f32, lib, sha,
+                  stream_handle, u16)
+from invariant_mhc_aggregate_gb300 import binding
+from invariant_mhc_aggregate_gb300.autograd import mhc_post
+from invariant_mhc_aggregate_gb300.inputs import post_inputs
+
+pytestmark = pytest.mark.gpu
+
+NS = (1, 2, 4, 8)
+DTYPES = (torch.bfloat16, torch.float16)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    return lib()
+
+
+def _ids(v):
+    return DTYPE_NAME.get(v, str(v))
+
+
+def expected_post_fwd_path(H, offsets):
+    """offsets: x, y, post, res, out."""
+    a = min(_align_of(offsets[0]), _align_of(offsets[1]), _align_of(offsets[4]))
+    if H % 16 == 0 and a >= 32:
+        return binding.MHC_PATH_VEC32
+    if H % 8 == 0 and a >= 16:
+        return binding.MHC_PATH_VEC16
+    return binding.MHC_PATH_ELEMENT
+
+
+def expected_post_bwd_path(H, offsets):
+    """offsets: g, x, y, post, res, grad_x, grad_y, grad_post, grad_res."""
+    a = min(_align_of(offsets[i]) for i in (0, 1, 2, 5, 6))
+    if H % 8 == 0 and a >= 16:
+        return binding.MHC_PATH_VEC16
+    return binding.MHC_PATH_ELEMENT
+
+
+def run_post_fwd(x, y, post, res, offsets=(0,) * 5):
+    T, n, H = x.shape
+    bx, by = DevBuf.of(x, offsets[0]), DevBuf.of(y, offsets[1])
+    bp, br = DevBuf.of(post, offsets[2]), DevBuf.of(res, offsets[3])
+    bo = DevBuf(T * n * H * 2, offsets[4])
+    assert binding.post_fwd_path_raw(bx.ptr, by.ptr, bp.ptr, br.ptr, bo.ptr, T, n, H) == \
+        expected_post_fwd_path(H, offsets)
+    st = binding.post_fwd_raw(bx.ptr, by.ptr, bp.ptr, br.ptr, bo.ptr, T, n, H, DTYPE_CODE[x.dtype],
+                              stream_handle())
+    assert st == binding.MHC_OK, st
+    torch.cuda.synchronize()
+    assert bo.guards_ok(), "post forward wrote outside out"
+    return bo.get(np.uint16, (T, n, H))
+
+
+def run_post_bwd(g, x, y, post, res, offsets=(0,) * 9):
+    T, n, H = x.shape
+    ins = [DevBuf.of(t, o) for t, o in zip((g, x, y, post, res), offsets[:5])]
+    outs = [DevBuf(T * n * H * 2, offsets[5]), DevBuf(T * H * 2, offsets[6]),
+            DevBuf(T * n * 4, offsets[7]), DevBuf(T * n * n * 4, offsets[8])]
+    ptrs = [b.ptr for b in ins + outs]
+    assert binding.post_bwd_path_raw(*ptrs, T, n, H) == expected_post_bwd_path(H, offsets)
+    st = binding.post_bwd_raw(*ptrs, T, n, H, DTYPE_CODE[x.dtype], stream_handle())
+    assert st == binding.MHC_OK, st
+    torch.cuda.synchronize()
+    assert all(b.guards_ok() for b in outs), "post backward wrote outside its outputs"
+    return (outs[0].get(np.uint16, (T, n, H)), outs[1].get(np.uint16, (T, H)),
+            outs[2].get(np.float32, (T, n)), outs[3].get(np.float32, (T, n, n)))
+
+
+# (T, H, offsets of x, y, post, res, out): each forward path, rows spanning
+# several blocks and ragged tails, tokens straddling blocks of the flat grid
+FWD_CASES = [
+    (5, 4096, (0, 0, 0, 0, 0)),        # 32-byte vectors
+    (3, 7168, (0, 0, 4, 4, 0)),        # 32-byte, a block spans two tokens
+    (7, 4104, (0, 0, 0, 0, 0)),        # H % 16 == 8: 16-byte vectors
+    (4, 4096, (16, 0, 0, 0, 0)),       # x 16-byte aligned: 16-byte vectors
+    (3, 4100, (0, 0, 0, 0, 0)),        # H % 8 != 0: 2-byte path
+    (2, 1279, (0, 2, 0, 0, 6)),        # odd H, 2-byte aligned buffers
+    (9, 8, (0, 0, 0, 0, 0)),           # one 16-byte vector a row
+    (3, 1, (0, 0, 0, 0, 0)),           # one value a row
+    (1, 2048 + 16, (0, 0, 0, 0, 0)),   # a single token
+]
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=_ids)
+@pytest.mark.parametrize("n", NS)
+@pytest.mark.parametrize("T,H,offsets", FWD_CASES)
+def test_post_fwd_all_paths(T, H, offsets, n, dtype):
+    x, y, post, res = post_inputs(T, H, n, "normal", 300 + T + H, dtype=dtype)
+    got = run_post_fwd(x, y, post, res, offsets)
+    want = oracle.post_fwd(u16(x), u16(y), f32(post), f32(res), DTYPE_NAME[dtype])
+    assert_bytes_equal(got, want, "out")
+
+
+# (T, H, offsets of g, x, y, post, res, grad_x, grad_y, grad_post, grad_res)
+BWD_CASES = [
+    (5, 4096, (0,) * 9),                               # 16-byte chunks, 2 a lane
+    (3, 7168, (0, 0, 0, 4, 4, 0, 0, 4, 4)),            # 3.5 chunks a lane
+    (7, 4104, (0,) * 9),
+    (2, 1024, (0,) * 9),                               # fewer chunks than lanes
+    (4, 4096, (0, 0, 0, 0, 0, 0, 8, 0, 0)),            # grad_y off 16 bytes: 2-byte path
+    (3, 4100, (0,) * 9),                               # ragged last chunk
+    (2, 1279, (2, 0, 6, 0, 0, 2, 0, 0, 0)),
+    (9, 8, (0,) * 9),
+    (3, 1, (0,) * 9),
+    (1, 2048 * 8 + 8, (0,) * 9),                       # long row: 8+ chunks a lane
+]
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=_ids)
+@pytest.mark.parametrize("n", NS)
+@pytest.mark.parametrize("T,H,offsets", BWD_CASES)
+def test_post_bwd_all_paths(T, H, offsets, n, dtype):
+    x, y, post, res, g = post_inputs(T, H, n, "normal", 400 + T + H, dtype=dtype, with_grad=True)
+    got = run_post_bwd(g, x, y, post, res, offsets)
+    want = oracle.post_bwd(u16(g), u16(x), u16(y), f32(post), f32(res), DTYPE_NAME[dtype])
+    for a, b, what in zip(got, want, ("grad_x", "grad_y", "grad_post", "grad_res")):
+        assert_bytes_equal(a, b, what)
+
+
+@pytest.mark.parametrize("n", NS)
+def test_post_ragged_recipe(n):
+    """Identity mixing rows and zero post coefficients."""
+    T, H = 40, 2048
+    x, y, post, res, g = post_inputs(T, H, n, "ragged", 500 + n, with_grad=True)
+    xd, yd, pd, rd, gd = (t.cuda() for t in (x, y, post, res, g))
+    out = binding.post(xd, yd, pd, rd)
+    gx, gy, gp, gr = binding.post_backward(gd, xd, yd, pd, rd)
+    torch.cuda.synchronize()
+    o = oracle.default()
+    assert_bytes_equal(u16(out), o.post_fwd(u16(x), u16(y), f32(post), f32(res)), "out")
+    want = o.post_bwd(u16(g), u16(x), u16(y), f32(post), f32(res))
+    for a, b, what in zip((u16(gx), u16(gy), f32(gp), f32(gr)), want,
+                          ("grad_x", "grad_y", "grad_post", "grad_res")):
+        assert_bytes_equal(a, b, what)
+
+
+def test_post_full_size_against_oracle():
+    """T = 4096, H = 7168, n = 4, BF16 (the benchmark's shape), every output
+    against the oracle, in the launch configuration the benchmark uses (torch
+    allocations, the current stream)."""
+    T, H, n = 4096, 7168, 4
+    x, y, post, res, g = post_inputs(T, H, n, "normal", 6, with_grad=True)
+    xd, yd, pd, rd, gd = (t.cuda() for t in (x, y, post, res, g))
+    out = binding.post(xd, yd, pd, rd)
+    gx, gy, gp, gr = binding.post_backward(gd, xd, yd, pd, rd)
+    torch.cuda.synchronize()
+    o = oracle.default()
+    assert_bytes_equal(u16(out), o.post_fwd(u16(x), u16(y), f32(post), f32(res)), "out")
+    want = o.post_bwd(u16(g), u16(x), u16(y), f32(post), f32(res))
+    for a, b, what in zip((u16(gx), u16(gy), f32(gp), f32(gr)), want,
+                          ("grad_x", "grad_y", "grad_post", "grad_res")):
+        assert_bytes_equal(a, b, what)
+
+
+@pytest.mark.parametrize("n", (1, 4, 8))
+def test_post_batch_split_invariance(n):
+    """Every token's outputs are the same bytes whatever batch it is run in."""
+    T, H = 64, 4096
+    x, y, post, res, g = post_inputs(T, H, n, "normal", 600 + n, with_grad=True)
+    xd, yd, pd, rd, gd = (t.cuda() for t in (x, y, post, res, g))
+    full = binding.post(xd, yd, pd, rd)
+    fgrads = binding.post_backward(gd, xd, yd, pd, rd)
+    for chunk in (1, 7, 64):
+        for t0 in range(0, T, chunk):
+            sl = slice(t0, min(T, t0 + chunk))
+            args = [t[sl].contiguous() for t in (xd, yd, pd, rd)]
+            part = binding.post(*args)
+            assert sha(part) == sha(full[sl]), (chunk, t0)
+            pgrads = binding.post_backward(gd[sl].contiguous(), *args)
+            for p, f in zip(pgrads, fgrads):
+                assert sha(p) == sha(f[sl]), (chunk, t0)
+
+
+def test_post_repeat_calls_identical():
+    T, H, n = 256, 7168, 4
+    x, y, post, res, g = (t.cuda() for t in post_inputs(T, H, n, "normal", 700, with_grad=True))
+    first = [sha(binding.post(x, y, post, res))] + [sha(t) for t in binding.post_backward(g, x, y, post, res)]
+    for _ in range(3):
+        again = [sha(binding.post(x, y, post, res))] + [sha(t) for t in binding.post_backward(g, x, y, post, res)]
+        assert again == first
+
+
+def test_post_autograd_gradients_match_oracle():
+    T, H, n = 2 * 17, 2048, 4
+    x, y, post, res, g = post_inputs(T, H, n, "normal", 800, with_grad=True)
+    xd = x.cuda().reshape(2, 17, n, H).requires_grad_(True)
+    yd = y.cuda().reshape(2, 17, H).requires_grad_(True)
+    pd = post.cuda().reshape(2, 17, n).requires_grad_(True)
+    rd = res.cuda().reshape(2, 17, n, n).requires_grad_(True)
+    out = mhc_post(xd, yd, pd, rd)
+    assert out.shape == (2, 17, n, H)
+    out.backward(g.cuda().reshape(2, 17, n, H))
+    o = oracle.default()
+    assert_bytes_equal(u16(out.detach().reshape(T, n, H)),
+                       o.post_fwd(u16(x), u16(y), f32(post), f32(res)), "out")
+    wgx, wgy, wgp, wgr = o.post_bwd(u16(g), u16(x), u16(y), f32(post), f32(res))
+    assert_bytes_equal(u16(xd.grad.reshape(T, n, H)), wgx, "x.grad")
+    assert_bytes_equal(u16(yd.grad.reshape(T, H)), wgy, "y.grad")
+    assert_bytes_equal(f32(pd.grad.reshape(T, n)), wgp, "post.grad")
+    assert_bytes_equal(f32(rd.grad.reshape(T, n, n)), wgr, "res.grad")
+
+
+def test_post_identity_on_gpu():
+    """res = I and post = 0 give out = x exactly; post = 1 and x = 0 give
+    out = y exactly (the oracle's special cases, through the kernels)."""
+    T, H, n = 16, 4096, 4
+    x, y, post, res = post_inputs(T, H, n, "normal", 900)
+    xd, yd = x.cuda(), y.cuda()
+    eye = torch.eye(n, device="cuda").expand(T, n, n).contiguous()
+    out = binding.post(xd, yd, torch.zeros(T, n, device="cuda"), eye)
+    assert sha(out) == sha(xd)
+    out = binding.post(torch.zeros_like(xd), yd, torch.ones(T, n, device="cuda"), eye)
+    assert sha(out) == sha(yd[:, None, :].expand(T, n, H).contiguous())
+
+
+def test_post_calls_capture_in_a_graph():
+    T, H, n = 128, 4096, 4
+    x, y, post, res, g = (t.cuda() for t in post_inputs(T, H, n, "normal", 950, with_grad=True))
+    out = torch.empty_like(x)
+    gx, gy = torch.empty_like(x), torch.empty_like(y)
+    gp, gr = torch.empty_like(post), torch.empty_like(res)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        binding.mhc_post_fwd(x, y, post, res, out)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=s):
+            binding.mhc_post_fwd(x, y, post, res, out)
+            binding.mhc_post_bwd(g, x, y, post, res, gx, gy, gp, gr)
+    for t in (out, gx, gy, gp, gr):
+        t.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    e = [binding.post(x, y, post, res)] + list(binding.post_backward(g, x, y, post, res))
+    for a, b in zip((out, gx, gy, gp, gr), e):
+        assert sha(a) == sha(b)
