@@ -292,9 +292,9 @@ MHC_API mhc_status_t mhc_sigmoid_param_grad(const float* grad_z, const float* mi
  *   post, grad_post     FP32 [T,n]         res, grad_res  FP32 [T,n,n]
  *                                           (row k = output stream k)
  * n in {1, 2, 4, 8}; the other rules (errors, ownership, determinism,
- * alignment) as for the aggregate.  Paths: the forward takes 32- or 16-byte
- * vectors (H % 16 / H % 8 == 0 and the 2-byte buffers 32- / 16-byte aligned),
- * the backward 16-byte vectors, both else the 2-byte path.
+ * alignment) as for the aggregate.  Paths: both calls take 16-byte vectors
+ * (MHC_PATH_VEC16) when H % 8 == 0 and every 2-byte buffer is 16-byte
+ * aligned, else the 2-byte path (MHC_PATH_ELEMENT).
  */
 MHC_API mhc_status_t mhc_post_fwd(const void* x, const void* y, const float* post, const float* res,
                                   void* out, int64_t T, int32_t n, int64_t H, mhc_dtype_t dtype,
@@ -320,6 +320,15 @@ MHC_API const char* mhc_status_string(mhc_status_t status);
 /* The cudaError_t value behind the last MHC_ERR_CUDA returned on the calling
  * thread; a call that launches successfully resets it to 0. */
 MHC_API int32_t mhc_h_aggregate_last_cuda_error(void);
+
+/* Kernels that stream their inputs through shared memory with bulk copies
+ * (the mHC post backward on its 16-byte path) bound every wait for a copy or
+ * for a free stage (1 s of the GPU's global timer); a wait that runs out is
+ * recorded, the kernel still runs to its end (its outputs are then not to be
+ * trusted), and no wait can hang the GPU.  This returns 1 if a wait ran out
+ * on the current device since the previous call, else 0, and clears the
+ * record; -1 if a CUDA call fails.  It synchronizes the device. */
+MHC_API int64_t mhc_h_aggregate_wait_timeouts(void);
 
 #ifdef __cplusplus
 }

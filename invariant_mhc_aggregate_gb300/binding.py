@@ -58,6 +58,7 @@ EXPORTS = (
     "mhc_post_bwd_path",
     "mhc_status_string",
     "mhc_h_aggregate_last_cuda_error",
+    "mhc_h_aggregate_wait_timeouts",
 )
 
 _lock = threading.Lock()
@@ -131,6 +132,8 @@ def load(path: str | None = None):
         lib.mhc_status_string.restype = ctypes.c_char_p
         lib.mhc_h_aggregate_last_cuda_error.argtypes = []
         lib.mhc_h_aggregate_last_cuda_error.restype = i32
+        lib.mhc_h_aggregate_wait_timeouts.argtypes = []
+        lib.mhc_h_aggregate_wait_timeouts.restype = i64
         if path == _build.LIB_PATH:
             _lib = lib
         return lib
@@ -198,6 +201,13 @@ def agg_sigmoid_bwd_raw(grad_out: int, residual: int, mix: int, alpha: int, b: i
 def sigmoid_param_grad_raw(grad_z: int, mix: int, grad_b: int, grad_alpha: int, T: int, n: int,
                            stream: int = 0) -> int:
     return load().mhc_sigmoid_param_grad(grad_z, mix, grad_b, grad_alpha, T, n, stream)
+
+
+def wait_timeouts() -> int:
+    """1 if a bounded wait of the bulk-copy kernels ran out on the current
+    device since the last call, else 0 (clears it; synchronizes the device);
+    -1 on a CUDA error."""
+    return int(load().mhc_h_aggregate_wait_timeouts())
 
 
 def post_fwd_raw(x: int, y: int, post: int, res: int, out: int, T: int, n: int, H: int, dtype: int,

@@ -15,7 +15,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 4;
+constexpr int kAbiVersion = 5;
 
 thread_local int32_t g_last_cuda_error = 0;
 
@@ -272,7 +272,6 @@ mhc_path_t post_fwd_path(const void* x, const void* y, const float* post, const 
     const Range ins[4] = {range_of(x, TH * 2 * nu), range_of(y, TH * 2),
                           range_of(post, uint64_t(T) * 4 * nu), range_of(res, uint64_t(T) * 4 * nu * nu)};
     if (!disjoint(outs, 1, ins, 4)) return MHC_PATH_NONE;
-    if (H % 16 == 0 && aligned(x, 32) && aligned(y, 32) && aligned(out, 32)) return MHC_PATH_VEC32;
     if (H % 8 == 0 && aligned(x, 16) && aligned(y, 16) && aligned(out, 16)) return MHC_PATH_VEC16;
     return MHC_PATH_ELEMENT;
 }
@@ -309,8 +308,7 @@ mhc_status_t post_fwd(const void* x, const void* y, const float* post, const flo
     if (T == 0) return MHC_OK;
     const mhc_path_t path = post_fwd_path(x, y, post, res, out, T, n, H);
     if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
-    if ((path == MHC_PATH_VEC32 || path == MHC_PATH_VEC16) && uint64_t(H) / 8 > 0x7FFFFFFFull)
-        return MHC_ERR_UNSUPPORTED;
+    if (path == MHC_PATH_VEC16 && uint64_t(H) / 8 > 0x7FFFFFFFull) return MHC_ERR_UNSUPPORTED;
     const mhc::PostFwdCall c{x, y, post, res, out, uint64_t(T), uint64_t(H), int(n), int(path),
                              num_sms(), reinterpret_cast<cudaStream_t>(stream)};
     return finish(mhc::post_fwd(c, dtype == MHC_DTYPE_BF16 ? mhc::kBF16 : mhc::kF16));
@@ -356,6 +354,8 @@ const char* mhc_status_string(mhc_status_t status) {
 }
 
 int32_t mhc_h_aggregate_last_cuda_error(void) { return g_last_cuda_error; }
+
+int64_t mhc_h_aggregate_wait_timeouts(void) { return mhc::take_wait_timeouts(); }
 
 mhc_path_t mhc_h_aggregate_fwd_path(const void* residual, const float* pre, const void* out,
                                     int64_t T, int64_t H) {

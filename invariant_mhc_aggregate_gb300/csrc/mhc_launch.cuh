@@ -84,6 +84,10 @@ struct PostBwdCall {
 
 cudaError_t post_fwd(const PostFwdCall& c, int dtype);
 cudaError_t post_bwd(const PostBwdCall& c, int dtype);
+// 1 if a bounded wait of the bulk-copy kernels ran out on the current device
+// since the last call, else 0 (clears the record; synchronizes the device);
+// -1 on a CUDA error.
+int64_t take_wait_timeouts();
 
 // The coefficient kernels of their own (mhc_launch_coeffs.cu).
 cudaError_t pre_sigmoid(const float* mix, const float* alpha, const float* b, float* pre,
@@ -91,14 +95,15 @@ cudaError_t pre_sigmoid(const float* mix, const float* alpha, const float* b, fl
 cudaError_t sigmoid_param_grad(const float* grad_z, const float* mix, float* grad_b,
                                float* grad_alpha, uint64_t T, int n, bool vec, cudaStream_t stream);
 
-// Launch with programmatic stream serialization (see pdl_enter).
+// Launch with programmatic stream serialization (see pdl_enter) and
+// `smem` bytes of dynamic shared memory.
 template <typename... Params, typename... Args>
-cudaError_t launch(void (*kernel)(Params...), uint32_t grid, uint32_t block, cudaStream_t stream,
-                   Args... args) {
+cudaError_t launch_smem(void (*kernel)(Params...), uint32_t grid, uint32_t block, uint32_t smem,
+                        cudaStream_t stream, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -106,6 +111,12 @@ cudaError_t launch(void (*kernel)(Params...), uint32_t grid, uint32_t block, cud
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch(void (*kernel)(Params...), uint32_t grid, uint32_t block, cudaStream_t stream,
+                   Args... args) {
+    return launch_smem(kernel, grid, block, 0, stream, args...);
 }
 
 inline uint32_t grid_for(uint64_t items, uint32_t per_block, uint64_t cap) {

@@ -35,6 +35,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "mhc_bulk.cuh"
+
 namespace mhc {
 
 // The n*n mixing and n post coefficients of token t, in registers.
@@ -49,13 +51,21 @@ __device__ __forceinline__ void ld_post_coeffs(const float* post, const float* r
     }
 }
 
+// The barrier of the threads that share a token's shared-memory tables: the
+// whole block, or (bulk kernel) its consumer threads.
+struct BlockSync {
+    __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
 // The coefficients of the token a backward block works on.  Up to n = 4 they
 // sit in registers; at n = 8 (72 values, next to 72 lane sums) in shared
 // memory, read where they are used.
 template <int N, bool kShared = (N >= 8)>
 struct PostCoeffs {
     float pk[N], rk[N][N];
-    __device__ __forceinline__ void load(const float* post, const float* res, uint64_t t, float*) {
+    template <class Sync = BlockSync>
+    __device__ __forceinline__ void load(const float* post, const float* res, uint64_t t, float*,
+                                         Sync = Sync()) {
         ld_post_coeffs<N>(post, res, t, pk, rk);
     }
     __device__ __forceinline__ float r(int k, int j) const { return rk[k][j]; }
@@ -67,25 +77,37 @@ struct PostCoeffs<N, true> {
     const float* s;   // rk row-major, then pk
     // Every thread of the block calls this; the previous token's readers have
     // passed the fold's closing barrier.
-    __device__ __forceinline__ void load(const float* post, const float* res, uint64_t t, float* smem) {
+    template <class Sync = BlockSync>
+    __device__ __forceinline__ void load(const float* post, const float* res, uint64_t t, float* smem,
+                                         Sync sync = Sync()) {
         if (threadIdx.x < uint32_t(N * N)) smem[threadIdx.x] = __ldg(res + uint64_t(N) * N * t + threadIdx.x);
         else if (threadIdx.x < uint32_t(N * N + N))
             smem[threadIdx.x] = __ldg(post + uint64_t(N) * t + (threadIdx.x - N * N));
-        __syncthreads();
+        sync();
         s = smem;
     }
     __device__ __forceinline__ float r(int k, int j) const { return s[k * N + j]; }
     __device__ __forceinline__ float p(int k) const { return s[N * N + k]; }
 };
 
-// One output value of stream k from the n input values xs and y.
+// One output value of stream k from the n input values xs and y, given row
+// k of res (rk) and post[t,k] (pk).
 template <int N>
-__device__ __forceinline__ float post_value(const float (&pk)[N], const float (&rk)[N][N], int k,
-                                            const float (&xs)[N], float ys) {
+__device__ __forceinline__ float post_value(const float (&rk)[N], float pk, const float (&xs)[N], float ys) {
     float p[N];
 #pragma unroll
-    for (int j = 0; j < N; ++j) p[j] = __fmul_rn(rk[k][j], xs[j]);
-    return __fadd_rn(tree_sum<N>(p), __fmul_rn(pk[k], ys));
+    for (int j = 0; j < N; ++j) p[j] = __fmul_rn(rk[j], xs[j]);
+    return __fadd_rn(tree_sum<N>(p), __fmul_rn(pk, ys));
+}
+
+// Row k of res and post[t,k] for token t (read-only cache: every thread of a
+// token reads the same values).
+template <int N>
+__device__ __forceinline__ void ld_post_row(const float* post, const float* res, uint64_t t, int k,
+                                            float (&rk)[N], float& pk) {
+    pk = __ldg(post + uint64_t(N) * t + k);
+#pragma unroll
+    for (int j = 0; j < N; ++j) rk[j] = __ldg(res + (uint64_t(N) * t + k) * N + j);
 }
 
 // --------------------------------------------------------------------------
@@ -94,38 +116,54 @@ __device__ __forceinline__ float post_value(const float (&pk)[N], const float (&
 
 constexpr int kPostBlock = 256;
 
-// Vector path: vector i of the [T, V] plane (V = H / (2*NW) per row).
-template <int N, int DT, int NW>
-__global__ void __launch_bounds__(kPostBlock)
+// Vector path: the [T, V] plane of vectors (V = H / (2*NW) per row), block
+// b taking vectors b*BLOCK*U + u*BLOCK + threadIdx (u < U): each thread loads
+// the n x vectors and the y vector of its U positions, then writes their n
+// output vectors.
+template <int N, int DT, int NW, int U, int MIN_BLOCKS>
+__global__ void __launch_bounds__(kPostBlock, MIN_BLOCKS)
 post_fwd_vec_kernel(const Words<NW>* __restrict__ x, const Words<NW>* __restrict__ y,
                     const float* __restrict__ post, const float* __restrict__ res,
                     Words<NW>* __restrict__ out, uint32_t n_vec, uint32_t V, FastDivU32 divV) {
     pdl_enter();
-    const uint32_t i = blockIdx.x * kPostBlock + threadIdx.x;
-    if (i >= n_vec) return;
-    const uint32_t t = fastdiv_u32(i, divV);
-    const uint64_t row0 = uint64_t(N) * t * V + (i - t * V);   // x / out vector of stream 0
-    Words<NW> xv[N];
+    const uint32_t i0 = blockIdx.x * (kPostBlock * U) + threadIdx.x;
+    Words<NW> xv[U][N], yv[U];
+    uint32_t tok[U];
+    uint64_t row0[U];   // x / out vector of stream 0
 #pragma unroll
-    for (int j = 0; j < N; ++j) xv[j] = ld_stream<NW>(x + row0 + uint64_t(j) * V);
-    const Words<NW> yv = ld_stream<NW>(y + i);
-    float pk[N], rk[N][N];
-    ld_post_coeffs<N>(post, res, t, pk, rk);
+    for (int u = 0; u < U; ++u) {
+        const uint32_t i = i0 + uint32_t(u) * kPostBlock;
+        if (i < n_vec) {
+            tok[u] = fastdiv_u32(i, divV);
+            row0[u] = uint64_t(N) * tok[u] * V + (i - tok[u] * V);
 #pragma unroll
-    for (int k = 0; k < N; ++k) {
-        Words<NW> o;
-#pragma unroll
-        for (int e = 0; e < NW; ++e) {
-            float xl[N], xh[N];
-#pragma unroll
-            for (int j = 0; j < N; ++j) {
-                xl[j] = Elem<DT>::lo(xv[j].w[e]);
-                xh[j] = Elem<DT>::hi(xv[j].w[e]);
-            }
-            o.w[e] = Elem<DT>::pack(post_value<N>(pk, rk, k, xl, Elem<DT>::lo(yv.w[e])),
-                                    post_value<N>(pk, rk, k, xh, Elem<DT>::hi(yv.w[e])));
+            for (int j = 0; j < N; ++j) xv[u][j] = ld_stream<NW>(x + row0[u] + uint64_t(j) * V);
+            yv[u] = ld_stream<NW>(y + i);
         }
-        st_stream<NW>(out + row0 + uint64_t(k) * V, o);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint32_t i = i0 + uint32_t(u) * kPostBlock;
+        if (i < n_vec) {
+#pragma unroll
+            for (int k = 0; k < N; ++k) {
+                float rk[N], pk;
+                ld_post_row<N>(post, res, tok[u], k, rk, pk);
+                Words<NW> o;
+#pragma unroll
+                for (int e = 0; e < NW; ++e) {
+                    float xl[N], xh[N];
+#pragma unroll
+                    for (int j = 0; j < N; ++j) {
+                        xl[j] = Elem<DT>::lo(xv[u][j].w[e]);
+                        xh[j] = Elem<DT>::hi(xv[u][j].w[e]);
+                    }
+                    o.w[e] = Elem<DT>::pack(post_value<N>(rk, pk, xl, Elem<DT>::lo(yv[u].w[e])),
+                                            post_value<N>(rk, pk, xh, Elem<DT>::hi(yv[u].w[e])));
+                }
+                st_stream<NW>(out + row0[u] + uint64_t(k) * V, o);
+            }
+        }
     }
 }
 
@@ -139,8 +177,6 @@ post_fwd_element_kernel(const uint16_t* __restrict__ x, const uint16_t* __restri
     pdl_enter();
     const uint64_t base = uint64_t(blockIdx.x) * kNarrowSeg + threadIdx.x;
     for (uint64_t t = blockIdx.y; t < T; t += gridDim.y) {
-        float pk[N], rk[N][N];
-        ld_post_coeffs<N>(post, res, t, pk, rk);
 #pragma unroll 2
         for (int e = 0; e < kNarrowPerThread; ++e) {
             const uint64_t h = base + uint64_t(e) * kNarrowBlock;
@@ -150,8 +186,11 @@ post_fwd_element_kernel(const uint16_t* __restrict__ x, const uint16_t* __restri
                 for (int j = 0; j < N; ++j) xs[j] = Elem<DT>::one(ld_stream2(x + (uint64_t(N) * t + j) * H + h));
                 const float ys = Elem<DT>::one(ld_stream2(y + t * H + h));
 #pragma unroll
-                for (int k = 0; k < N; ++k)
-                    st_stream2(out + (uint64_t(N) * t + k) * H + h, Elem<DT>::cvt(post_value<N>(pk, rk, k, xs, ys)));
+                for (int k = 0; k < N; ++k) {
+                    float rk[N], pk;
+                    ld_post_row<N>(post, res, t, k, rk, pk);
+                    st_stream2(out + (uint64_t(N) * t + k) * H + h, Elem<DT>::cvt(post_value<N>(rk, pk, xs, ys)));
+                }
             }
         }
     }
@@ -161,25 +200,32 @@ post_fwd_element_kernel(const uint16_t* __restrict__ x, const uint16_t* __restri
 // backward
 // --------------------------------------------------------------------------
 
-// The ORDER-256 fold of M = n*n + n lane sums of a 256-thread block (one lane
-// per thread): xor shuffles over each group of 32, the 8 group values
-// through shared memory; grad_res[t,k,j] = value k*n + j, grad_post[t,k] =
-// value n*n + k.
-template <int N>
-__device__ __forceinline__ void post_fold_and_store(float (&acc)[N * N + N], float (*red)[N * N + N],
+// The ORDER-256 fold of M = n*n + n lane sums of a 256-lane block (LPT lanes
+// per thread: lanes LPT*thread + l): xor shuffles over each group of 32 lanes,
+// the 8 group values through shared memory; grad_res[t,k,j] = value k*n + j,
+// grad_post[t,k] = value n*n + k.  All threads of the block call it.
+template <int N, int LPT, class Sync = BlockSync>
+__device__ __forceinline__ void post_fold_and_store(float (&acc)[LPT][N * N + N], float (*red)[N * N + N],
                                                     float* __restrict__ grad_post,
-                                                    float* __restrict__ grad_res, uint64_t t) {
+                                                    float* __restrict__ grad_res, uint64_t t,
+                                                    Sync sync = Sync()) {
     constexpr int M = N * N + N;
+    constexpr int kThreadsPerGroup = 32 / LPT;
 #pragma unroll
     for (int m = 0; m < M; ++m) {
 #pragma unroll
-        for (int s = 16; s >= 1; s >>= 1) acc[m] = __fadd_rn(acc[m], __shfl_xor_sync(0xffffffffu, acc[m], s));
-    }
-    if ((threadIdx.x & 31u) == 0) {
+        for (int s = kThreadsPerGroup / 2; s >= 1; s >>= 1) {
 #pragma unroll
-        for (int m = 0; m < M; ++m) red[threadIdx.x / 32][m] = acc[m];
+            for (int l = 0; l < LPT; ++l)
+                acc[l][m] = __fadd_rn(acc[l][m], __shfl_xor_sync(0xffffffffu, acc[l][m], s));
+        }
+        if (LPT == 2) acc[0][m] = __fadd_rn(acc[0][m], acc[LPT - 1][m]);
     }
-    __syncthreads();
+    if ((threadIdx.x % kThreadsPerGroup) == 0) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) red[threadIdx.x / kThreadsPerGroup][m] = acc[0][m];
+    }
+    sync();
     if (threadIdx.x < uint32_t(M)) {
         const int m = threadIdx.x;
         float w[kGroups];
@@ -193,16 +239,16 @@ __device__ __forceinline__ void post_fold_and_store(float (&acc)[N * N + N], flo
         if (m < N * N) grad_res[uint64_t(N) * N * t + m] = w[0];
         else grad_post[uint64_t(N) * t + (m - N * N)] = w[0];
     }
-    __syncthreads();   // red[] is reused by the next token
+    sync();   // red[] (and the coefficient table) are reused by the next token
 }
 
-// The chunk's grad_x vector of input stream j (j < n) or its grad_y vector
-// (j == n) from the n g vectors: coefficient column j of res, or post.
-template <int N, int DT, class C>
-__device__ __forceinline__ Words<4> post_chunk_grad(const C& cf, const Words<4> (&gv)[N], int j) {
-    Words<4> o;
+// The grad_x vector of input stream j (j < n) or the grad_y vector (j == n)
+// from the n g vectors of one position: coefficient column j of res, or post.
+template <int N, int DT, int NW, class C>
+__device__ __forceinline__ Words<NW> post_chunk_grad(const C& cf, const Words<NW> (&gv)[N], int j) {
+    Words<NW> o;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < NW; ++e) {
         float ql[N], qh[N];
 #pragma unroll
         for (int k = 0; k < N; ++k) {
@@ -215,59 +261,208 @@ __device__ __forceinline__ Words<4> post_chunk_grad(const C& cf, const Words<4> 
     return o;
 }
 
-// One chunk of a token: writes its grad_x and grad_y vectors and adds its
-// partials to the n*n + n lane sums.  Stream by stream, so that only one
-// stream's gradient vector is live at a time.
-template <int N, int DT, class C, class StX, class StY>
-__device__ __forceinline__ void post_chunk(const C& cf, const Words<4> (&gv)[N], const Words<4> (&xv)[N],
-                                           const Words<4>& yv, float (&acc)[N * N + N], StX st_x, StY st_y) {
+// One position (NW/4 chunks) of a token: writes its grad_x and grad_y vectors
+// and adds each chunk's partials to its lane's n*n + n sums.  Stream by
+// stream, so that one gradient vector is live at a time.
+template <int N, int DT, int NW, class C, class StX, class StY>
+__device__ __forceinline__ void post_chunk(const C& cf, const Words<NW> (&gv)[N], const Words<NW> (&xv)[N],
+                                           const Words<NW>& yv, float (&acc)[NW / 4][N * N + N], StX st_x,
+                                           StY st_y) {
 #pragma unroll
     for (int j = 0; j < N; ++j) {
-        st_x(j, post_chunk_grad<N, DT>(cf, gv, j));
+        st_x(j, post_chunk_grad<N, DT, NW>(cf, gv, j));
 #pragma unroll
-        for (int k = 0; k < N; ++k) acc[k * N + j] = __fadd_rn(acc[k * N + j], chunk_partial<DT, 4>(gv[k], xv[j], 0));
+        for (int k = 0; k < N; ++k) {
+#pragma unroll
+            for (int l = 0; l < NW / 4; ++l)
+                acc[l][k * N + j] = __fadd_rn(acc[l][k * N + j], chunk_partial<DT, NW>(gv[k], xv[j], 4 * l));
+        }
     }
-    st_y(post_chunk_grad<N, DT>(cf, gv, N));
+    st_y(post_chunk_grad<N, DT, NW>(cf, gv, N));
 #pragma unroll
-    for (int k = 0; k < N; ++k) acc[N * N + k] = __fadd_rn(acc[N * N + k], chunk_partial<DT, 4>(gv[k], yv, 0));
+    for (int k = 0; k < N; ++k) {
+#pragma unroll
+        for (int l = 0; l < NW / 4; ++l)
+            acc[l][N * N + k] = __fadd_rn(acc[l][N * N + k], chunk_partial<DT, NW>(gv[k], yv, 4 * l));
+    }
 }
 
-// 16-byte path: H % 8 == 0, the 2-byte buffers 16-byte aligned; V = H / 8
-// vectors (= chunks) per row.
-template <int N, int DT>
-__global__ void __launch_bounds__(kLanes)
-post_bwd_vec_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict__ x,
-                    const Words<4>* __restrict__ y, const float* __restrict__ post,
-                    const float* __restrict__ res, Words<4>* __restrict__ grad_x,
-                    Words<4>* __restrict__ grad_y, float* __restrict__ grad_post,
+// Vector path: H % (2*NW) == 0 and the 2-byte buffers aligned to 4*NW
+// bytes; V = H / (2*NW) vectors per row.  One token per block of 256/LPT
+// threads (LPT = NW/4 lanes per thread): thread j takes vectors j, j + B,
+// j + 2B, ... (B threads), i.e. for lane LPT*j + l the chunks
+// (LPT*j + l) + 256m, in increasing order; BATCH vectors of each row are
+// loaded per pass.
+template <int N, int DT, int NW, int BATCH, int MIN_BLOCKS, bool SMEM_COEF>
+__global__ void __launch_bounds__(kLanes / (NW / 4), MIN_BLOCKS)
+post_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict__ x,
+                    const Words<NW>* __restrict__ y, const float* __restrict__ post,
+                    const float* __restrict__ res, Words<NW>* __restrict__ grad_x,
+                    Words<NW>* __restrict__ grad_y, float* __restrict__ grad_post,
                     float* __restrict__ grad_res, uint64_t T, uint32_t V) {
     constexpr int M = N * N + N;
+    constexpr int LPT = NW / 4;
+    constexpr uint32_t B = kLanes / LPT;
     __shared__ float red[kGroups][M];
     __shared__ float coef[M];
     pdl_enter();
     const uint32_t j = threadIdx.x;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        PostCoeffs<N> cf;
+        PostCoeffs<N, SMEM_COEF> cf;
         cf.load(post, res, t, coef);
-        float acc[M];
+        float acc[LPT][M];
 #pragma unroll
-        for (int m = 0; m < M; ++m) acc[m] = 0.0f;
+        for (int l = 0; l < LPT; ++l)
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[l][m] = 0.0f;
         const uint64_t row0 = uint64_t(N) * t * V;
-        for (uint32_t v = j; v < V; v += kLanes) {
-            Words<4> gv[N], xv[N];
+#pragma unroll 1
+        for (uint32_t v0 = j; v0 < V; v0 += B * BATCH) {
+            Words<NW> gv[BATCH][N], xv[BATCH][N], yv[BATCH];
 #pragma unroll
-            for (int k = 0; k < N; ++k) {
-                gv[k] = ld_stream<4>(g + row0 + uint64_t(k) * V + v);
-                xv[k] = ld_stream<4>(x + row0 + uint64_t(k) * V + v);
+            for (int b = 0; b < BATCH; ++b) {
+                const uint32_t v = v0 + uint32_t(b) * B;
+                if (b == 0 || v < V) {
+#pragma unroll
+                    for (int k = 0; k < N; ++k) {
+                        gv[b][k] = ld_stream<NW>(g + row0 + uint64_t(k) * V + v);
+                        xv[b][k] = ld_stream<NW>(x + row0 + uint64_t(k) * V + v);
+                    }
+                    yv[b] = ld_stream<NW>(y + t * V + v);
+                }
             }
-            const Words<4> yv = ld_stream<4>(y + t * V + v);
-            post_chunk<N, DT>(
-                cf, gv, xv, yv, acc,
-                [&](int k, const Words<4>& o) { st_stream<4>(grad_x + row0 + uint64_t(k) * V + v, o); },
-                [&](const Words<4>& o) { st_stream<4>(grad_y + t * V + v, o); });
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const uint32_t v = v0 + uint32_t(b) * B;
+                if (b == 0 || v < V) {
+                    post_chunk<N, DT, NW>(
+                        cf, gv[b], xv[b], yv[b], acc,
+                        [&](int k, const Words<NW>& o) { st_stream<NW>(grad_x + row0 + uint64_t(k) * V + v, o); },
+                        [&](const Words<NW>& o) { st_stream<NW>(grad_y + t * V + v, o); });
+                }
+            }
         }
-        post_fold_and_store<N>(acc, red, grad_post, grad_res, t);
+        post_fold_and_store<N, LPT>(acc, red, grad_post, grad_res, t);
     }
+}
+
+// Bulk-copy path (H % 8 == 0, the 2-byte buffers 16-byte aligned): the
+// token's rows stream through shared memory.  A persistent block of 256
+// consumer threads (ORDER-256 lane j = thread j) and one producer warp walks
+// its tokens t = blockIdx, blockIdx + gridDim, ...; each token in segments of
+// 256 chunks (4 KB of each row).  One producer thread copies a segment's
+// 2n + 1 input row pieces (g, x, y) into a free stage of a STAGES-deep ring
+// with bulk copies that complete on the stage's "full" barrier; each
+// consumer thread then takes chunk j of the segment from shared memory,
+// writes its grad_x and grad_y vectors, adds its partials, and its warp
+// releases the stage on the "empty" barrier.  The loads thus stay in flight
+// without holding registers.  After a token's last segment the consumers
+// fold the lane sums (named barrier 1 over the 256 consumers).
+//
+// A wait that runs out (no copy should ever take that long) sets *timeouts
+// to 1 (a plain store: every writer writes the same value); the thread then
+// stops waiting, the block still runs to its end
+// on whatever the stage holds, and the producer waits (bounded) for the
+// copies it issued before it exits.
+constexpr int kBulkThreads = kLanes + 32;
+
+__host__ __device__ constexpr uint32_t post_bulk_stage_bytes(int n) {
+    return uint32_t(2 * n + 1) * kLanes * 16u;
+}
+
+template <int N, int DT, int STAGES, int MIN_BLOCKS>
+__global__ void __launch_bounds__(kBulkThreads, MIN_BLOCKS)
+post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict__ x,
+                     const Words<4>* __restrict__ y, const float* __restrict__ post,
+                     const float* __restrict__ res, Words<4>* __restrict__ grad_x,
+                     Words<4>* __restrict__ grad_y, float* __restrict__ grad_post,
+                     float* __restrict__ grad_res, uint64_t T, uint32_t V,
+                     unsigned int* __restrict__ timeouts) {
+    constexpr int R = 2 * N + 1;   // staged rows: g (N), x (N), y
+    constexpr int M = N * N + N;
+    extern __shared__ __align__(128) unsigned char stage_mem[];   // STAGES * R * 4 KB
+    __shared__ __align__(8) uint64_t full[STAGES];
+    __shared__ __align__(8) uint64_t empty[STAGES];
+    __shared__ float red[kGroups][M];
+    __shared__ float coef[M];
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kGroups);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    pdl_enter();
+    const uint32_t nseg = (V + kLanes - 1) / kLanes;
+
+    if (threadIdx.x >= kLanes) {
+        // producer warp: one thread issues the copies
+        if (threadIdx.x != kLanes) return;
+        bool ok = true;
+        uint32_t item = 0;
+        for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
+            for (uint32_t s = 0; s < nseg; ++s, ++item) {
+                const uint32_t st = item % STAGES, round = item / STAGES;
+                if (round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1u);
+                const uint32_t c0 = s * kLanes;
+                const uint32_t bytes = (V - c0 < uint32_t(kLanes) ? V - c0 : uint32_t(kLanes)) * 16u;
+                unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N);
+                mbar_arrive_expect_tx(&full[st], bytes * R);
+#pragma unroll
+                for (int k = 0; k < N; ++k) {
+                    bulk_copy_g2s(dst + size_t(k) * kLanes * 16, g + (uint64_t(N) * t + k) * V + c0, bytes, &full[st]);
+                    bulk_copy_g2s(dst + size_t(N + k) * kLanes * 16, x + (uint64_t(N) * t + k) * V + c0, bytes,
+                                  &full[st]);
+                }
+                bulk_copy_g2s(dst + size_t(2 * N) * kLanes * 16, y + t * V + c0, bytes, &full[st]);
+            }
+        }
+        // every copy issued has landed before the block's shared memory goes
+        for (uint32_t i = item > uint32_t(STAGES) ? item - STAGES : 0; i < item; ++i)
+            if (!mbar_wait(&full[i % STAGES], (i / STAGES) & 1u)) ok = false;
+        if (!ok) *timeouts = 1u;
+        return;
+    }
+
+    // consumers
+    const uint32_t j = threadIdx.x;
+    const auto sync = [] { named_sync(1, kLanes); };
+    bool ok = true;
+    uint32_t item = 0;
+    for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        PostCoeffs<N> cf;
+        cf.load(post, res, t, coef, sync);
+        float acc[1][M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc[0][m] = 0.0f;
+#pragma unroll 1
+        for (uint32_t s = 0; s < nseg; ++s, ++item) {
+            const uint32_t st = item % STAGES;
+            if (ok) ok = mbar_wait(&full[st], (item / STAGES) & 1u);
+            const uint32_t c = s * kLanes + j;
+            if (c < V) {
+                const Words<4>* sm =
+                    reinterpret_cast<const Words<4>*>(stage_mem + size_t(st) * post_bulk_stage_bytes(N)) + j;
+                Words<4> gv[N], xv[N];
+#pragma unroll
+                for (int k = 0; k < N; ++k) {
+                    gv[k] = sm[k * kLanes];
+                    xv[k] = sm[(N + k) * kLanes];
+                }
+                const Words<4> yv = sm[2 * N * kLanes];
+                post_chunk<N, DT, 4>(
+                    cf, gv, xv, yv, acc,
+                    [&](int k, const Words<4>& o) { st_stream<4>(grad_x + (uint64_t(N) * t + k) * V + c, o); },
+                    [&](const Words<4>& o) { st_stream<4>(grad_y + t * V + c, o); });
+            }
+            __syncwarp();
+            if ((j & 31u) == 0) mbar_arrive(&empty[st]);
+        }
+        post_fold_and_store<N, 1>(acc, red, grad_post, grad_res, t, sync);
+    }
+    if (!ok) *timeouts = 1u;
 }
 
 // 2-byte path: any H and 2-byte alignment; the same lanes and chunks, the
@@ -302,9 +497,9 @@ post_bwd_element_kernel(const uint16_t* __restrict__ g, const uint16_t* __restri
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
         PostCoeffs<N> cf;
         cf.load(post, res, t, coef);
-        float acc[M];
+        float acc[1][M];
 #pragma unroll
-        for (int m = 0; m < M; ++m) acc[m] = 0.0f;
+        for (int m = 0; m < M; ++m) acc[0][m] = 0.0f;
         const uint64_t row0 = uint64_t(N) * t * H;
         for (uint64_t c = j; c < C; c += kLanes) {
             Words<4> gv[N], xv[N];
@@ -314,12 +509,12 @@ post_bwd_element_kernel(const uint16_t* __restrict__ g, const uint16_t* __restri
                 xv[k] = ld_chunk2(x + row0 + uint64_t(k) * H, 8 * c, H);
             }
             const Words<4> yv = ld_chunk2(y + t * H, 8 * c, H);
-            post_chunk<N, DT>(
+            post_chunk<N, DT, 4>(
                 cf, gv, xv, yv, acc,
                 [&](int k, const Words<4>& o) { st_chunk2(grad_x + row0 + uint64_t(k) * H, 8 * c, H, o); },
                 [&](const Words<4>& o) { st_chunk2(grad_y + t * H, 8 * c, H, o); });
         }
-        post_fold_and_store<N>(acc, red, grad_post, grad_res, t);
+        post_fold_and_store<N, 1>(acc, red, grad_post, grad_res, t);
     }
 }
 

@@ -50,7 +50,7 @@ def test_only_the_c_abi_is_exported():
 
 
 def test_abi_version(lib):
-    assert lib.mhc_h_aggregate_abi_version() == 4
+    assert lib.mhc_h_aggregate_abi_version() == 5
 
 
 def test_status_strings(lib):
@@ -352,12 +352,13 @@ def post_bpath(offs=(0,) * 9, T=4, n=4, H=4096):
 
 
 def test_post_fwd_path_choice(lib):
-    assert post_fpath() == binding.MHC_PATH_VEC32
-    assert post_fpath(p_off=4, r_off=4) == binding.MHC_PATH_VEC32     # coefficients need 4 bytes
+    assert post_fpath() == binding.MHC_PATH_VEC16
+    assert post_fpath(p_off=4, r_off=4) == binding.MHC_PATH_VEC16     # coefficients need 4 bytes
     assert post_fpath(y_off=16) == binding.MHC_PATH_VEC16
     assert post_fpath(o_off=16) == binding.MHC_PATH_VEC16
     assert post_fpath(H=4104) == binding.MHC_PATH_VEC16
     assert post_fpath(x_off=8) == binding.MHC_PATH_ELEMENT
+    assert post_fpath(o_off=8) == binding.MHC_PATH_ELEMENT
     assert post_fpath(H=4100) == binding.MHC_PATH_ELEMENT
     assert post_fpath(H=1279, n=8) == binding.MHC_PATH_ELEMENT
     assert post_fpath(x_off=1) == binding.MHC_PATH_NONE
@@ -384,7 +385,7 @@ def test_post_rejects_overlap(lib):
     assert binding.post_fwd_path_raw(x, y, p, r, x + 64, T, n, H) == binding.MHC_PATH_NONE
     assert binding.post_fwd_path_raw(x, y, p, r, y, T, n, H) == binding.MHC_PATH_NONE
     assert binding.post_fwd_path_raw(x, y, p, o + 256, o, T, n, H) == binding.MHC_PATH_NONE
-    assert binding.post_fwd_path_raw(x, y, p, r, x + T * n * H * 2, T, n, H) == binding.MHC_PATH_VEC32
+    assert binding.post_fwd_path_raw(x, y, p, r, x + T * n * H * 2, T, n, H) == binding.MHC_PATH_VEC16
     bufs = [A + i * GAP for i in range(9)]
     # every output against every other buffer
     for out in range(5, 9):

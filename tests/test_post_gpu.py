@@ -39,8 +39,6 @@ def _ids(v):
 def expected_post_fwd_path(H, offsets):
     """offsets: x, y, post, res, out."""
     a = min(_align_of(offsets[0]), _align_of(offsets[1]), _align_of(offsets[4]))
-    if H % 16 == 0 and a >= 32:
-        return binding.MHC_PATH_VEC32
     if H % 8 == 0 and a >= 16:
         return binding.MHC_PATH_VEC16
     return binding.MHC_PATH_ELEMENT
@@ -87,10 +85,10 @@ def run_post_bwd(g, x, y, post, res, offsets=(0,) * 9):
 # (T, H, offsets of x, y, post, res, out): each forward path, rows spanning
 # several blocks and ragged tails, tokens straddling blocks of the flat grid
 FWD_CASES = [
-    (5, 4096, (0, 0, 0, 0, 0)),        # 32-byte vectors
-    (3, 7168, (0, 0, 4, 4, 0)),        # 32-byte, a block spans two tokens
-    (7, 4104, (0, 0, 0, 0, 0)),        # H % 16 == 8: 16-byte vectors
-    (4, 4096, (16, 0, 0, 0, 0)),       # x 16-byte aligned: 16-byte vectors
+    (5, 4096, (0, 0, 0, 0, 0)),        # 16-byte vectors
+    (3, 7168, (0, 0, 4, 4, 0)),        # a block spans two tokens
+    (7, 4104, (0, 0, 0, 0, 0)),        # H % 16 == 8
+    (4, 4096, (16, 0, 0, 0, 0)),       # x only 16-byte aligned
     (3, 4100, (0, 0, 0, 0, 0)),        # H % 8 != 0: 2-byte path
     (2, 1279, (0, 2, 0, 0, 6)),        # odd H, 2-byte aligned buffers
     (9, 8, (0, 0, 0, 0, 0)),           # one 16-byte vector a row
