@@ -38,6 +38,11 @@ Parity status of each function (what pins it, from the oracle pin tests):
   * post_fwd / post_bwd (mHC post, a reading not on the pages): hand-worked
     tree-order cases, exact-rational emulation, identity and zero special
     cases, integer-valued exact sums for grad_res and grad_post, FP64 bounds.
+  * post_sigmoid_fwd / post_sigmoid_bwd (post coefficients from their own
+    mix, a reading): z = 0 makes post = 0.5 and grad_z = grad_post / 4
+    exactly (exact-rational forward, integer-valued grad_post); the
+    pre-activation and epilogue wiring against numpy binary32 arithmetic on
+    the pinned sigmoid and post.
 """
 
 from __future__ import annotations
@@ -162,6 +167,11 @@ class Oracle:
         lib.oracle_post_fwd.restype = ctypes.c_int
         lib.oracle_post_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i64, i64, i64, ctypes.c_int]
         lib.oracle_post_bwd.restype = ctypes.c_int
+        lib.oracle_post_sigmoid_fwd.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, ctypes.c_int]
+        lib.oracle_post_sigmoid_fwd.restype = ctypes.c_int
+        lib.oracle_post_sigmoid_bwd.argtypes = [p, p, p, p, p, p, p, p, p, p, p, p, i64, i64, i64,
+                                                ctypes.c_int]
+        lib.oracle_post_sigmoid_bwd.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -337,6 +347,35 @@ class Oracle:
             raise ValueError(f"unsupported n={n} or dtype={dtype}")
         return gx, gy, gp, gr
 
+    def post_sigmoid_fwd(self, x, y, mix, alpha, b, res, dtype: str = "bf16") -> np.ndarray:
+        """post_fwd with post = sigmoid(alpha * mix + b); [T,n,H]."""
+        mix, alpha, b = self._coeffs(mix, alpha, b)
+        x, y, _, res, T, n, H = self._post_args(x, y, mix, res)
+        out = np.empty((T, n, H), dtype=np.uint16)
+        if self.lib.oracle_post_sigmoid_fwd(_ptr(x), _ptr(y), _ptr(mix), _ptr(alpha), _ptr(b), _ptr(res),
+                                            _ptr(out), T, n, H, _DTYPES[dtype]) != 0:
+            raise ValueError(f"unsupported n={n} or dtype={dtype}")
+        return out
+
+    def post_sigmoid_bwd(self, g, x, y, mix, alpha, b, res, dtype: str = "bf16"):
+        """(grad_x [T,n,H], grad_y [T,H], grad_z float32 [T,n], grad_mix float32 [T,n],
+        grad_res float32 [T,n,n])."""
+        mix, alpha, b = self._coeffs(mix, alpha, b)
+        x, y, _, res, T, n, H = self._post_args(x, y, mix, res)
+        g = _as(g, np.uint16)
+        if g.shape != (T, n, H):
+            raise ValueError(f"g must be [{T},{n},{H}]")
+        gx = np.empty((T, n, H), dtype=np.uint16)
+        gy = np.empty((T, H), dtype=np.uint16)
+        gz = np.empty((T, n), dtype=np.float32)
+        gm = np.empty((T, n), dtype=np.float32)
+        gr = np.empty((T, n, n), dtype=np.float32)
+        if self.lib.oracle_post_sigmoid_bwd(_ptr(g), _ptr(x), _ptr(y), _ptr(mix), _ptr(alpha), _ptr(b),
+                                            _ptr(res), _ptr(gx), _ptr(gy), _ptr(gz), _ptr(gm), _ptr(gr),
+                                            T, n, H, _DTYPES[dtype]) != 0:
+            raise ValueError(f"unsupported n={n} or dtype={dtype}")
+        return gx, gy, gz, gm, gr
+
     def fwd(self, residual, pre) -> np.ndarray:
         """out[t,h] = bf16((pre0*r0 + pre1*r1) + (pre2*r2 + pre3*r3)); uint16 [T,H]."""
         residual = _as(residual, np.uint16)
@@ -455,3 +494,11 @@ def post_fwd(x, y, post, res, dtype="bf16"):
 
 def post_bwd(g, x, y, post, res, dtype="bf16"):
     return default().post_bwd(g, x, y, post, res, dtype)
+
+
+def post_sigmoid_fwd(x, y, mix, alpha, b, res, dtype="bf16"):
+    return default().post_sigmoid_fwd(x, y, mix, alpha, b, res, dtype)
+
+
+def post_sigmoid_bwd(g, x, y, mix, alpha, b, res, dtype="bf16"):
+    return default().post_sigmoid_bwd(g, x, y, mix, alpha, b, res, dtype)

@@ -525,6 +525,19 @@ int oracle_pre_sigmoid(const float* mix, const float* alpha, const float* b, flo
     return 0;
 }
 
+/* The coefficient-gradient epilogue: for coefficients c = sigmoid(z),
+ * z = RN(RN(alpha * mix) + b[k]), and the gradient grad_c of a loss with
+ * respect to c, grad_z = RN(grad_c * sigmoid'(z)) and
+ * grad_mix = RN(alpha * grad_z), all [T,n]. */
+static void sigmoid_epilogue(const float* grad_c, const float* mix, const float* alpha,
+                             const float* b, float* grad_z, float* grad_mix, int64_t T, int64_t n) {
+    for (int64_t i = 0; i < T * n; ++i) {
+        float z = pre_activation(alpha[0], mix[i], b[i % n]);
+        grad_z[i] = grad_c[i] * oracle_sigmoid32_grad(z);
+        grad_mix[i] = alpha[0] * grad_z[i];
+    }
+}
+
 /* out = aggregate(residual, sigmoid(alpha * mix + b)). */
 int oracle_aggregate_sigmoid_fwd(const uint16_t* residual, const float* mix, const float* alpha,
                                  const float* b, uint16_t* out, int64_t T, int64_t n, int64_t H,
@@ -554,11 +567,7 @@ int oracle_aggregate_sigmoid_bwd(const uint16_t* g, const uint16_t* residual, co
     }
     oracle_pre_sigmoid(mix, alpha, b, pre, T, n);
     int rc = oracle_aggregate_bwd(g, residual, pre, grad_residual, grad_pre, T, n, H, dtype);
-    for (int64_t i = 0; rc == 0 && i < T * n; ++i) {
-        float z = pre_activation(alpha[0], mix[i], b[i % n]);
-        grad_z[i] = grad_pre[i] * oracle_sigmoid32_grad(z);
-        grad_mix[i] = alpha[0] * grad_z[i];
-    }
+    if (rc == 0) sigmoid_epilogue(grad_pre, mix, alpha, b, grad_z, grad_mix, T, n);
     free(pre);
     free(grad_pre);
     return rc;
@@ -689,4 +698,51 @@ int oracle_post_bwd(const uint16_t* g, const uint16_t* x, const uint16_t* y, con
         }
     }
     return 0;
+}
+
+/* ----------------------------------------------------------------------- */
+/* mHC post with its coefficients computed from their own mix               */
+/* ----------------------------------------------------------------------- */
+
+/* "perf: fuse mHC coefficient backward epilogue", Summary, names the post
+ * sigmoid's derivative next to the pre sigmoid's, with grad_mix and the
+ * grad_b / alpha gradients.  Reading used here, as for pre (no other scale
+ * is on the pages):
+ *
+ *   post[t,k] = sigmoid(z[t,k]),  z[t,k] = RN(RN(alpha * mix[t,k]) + b[k])
+ *   out       = oracle_post_fwd(x, y, post, res)
+ *   grad_z    = RN(grad_post * sigmoid'(z)),  grad_mix = RN(alpha * grad_z)
+ *
+ * with grad_post from oracle_post_bwd; grad_b and grad_alpha are then
+ * oracle_sigmoid_param_grad(grad_z, mix). */
+int oracle_post_sigmoid_fwd(const uint16_t* x, const uint16_t* y, const float* mix,
+                            const float* alpha, const float* b, const float* res, uint16_t* out,
+                            int64_t T, int64_t n, int64_t H, int dtype) {
+    if (!valid_streams(n) || (dtype != 0 && dtype != 1)) return -1;
+    float* post = (float*)malloc(sizeof(float) * (size_t)(T * n + 1));
+    if (!post) return -2;
+    oracle_pre_sigmoid(mix, alpha, b, post, T, n);
+    int rc = oracle_post_fwd(x, y, post, res, out, T, n, H, dtype);
+    free(post);
+    return rc;
+}
+
+int oracle_post_sigmoid_bwd(const uint16_t* g, const uint16_t* x, const uint16_t* y, const float* mix,
+                            const float* alpha, const float* b, const float* res, uint16_t* grad_x,
+                            uint16_t* grad_y, float* grad_z, float* grad_mix, float* grad_res,
+                            int64_t T, int64_t n, int64_t H, int dtype) {
+    if (!valid_streams(n) || (dtype != 0 && dtype != 1)) return -1;
+    float* post = (float*)malloc(sizeof(float) * (size_t)(T * n + 1));
+    float* grad_post = (float*)malloc(sizeof(float) * (size_t)(T * n + 1));
+    if (!post || !grad_post) {
+        free(post);
+        free(grad_post);
+        return -2;
+    }
+    oracle_pre_sigmoid(mix, alpha, b, post, T, n);
+    int rc = oracle_post_bwd(g, x, y, post, res, grad_x, grad_y, grad_post, grad_res, T, n, H, dtype);
+    if (rc == 0) sigmoid_epilogue(grad_post, mix, alpha, b, grad_z, grad_mix, T, n);
+    free(post);
+    free(grad_post);
+    return rc;
 }

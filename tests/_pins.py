@@ -1161,3 +1161,80 @@ ALL_CHECKS += [
     check_post_bwd_tree_golden,
     check_post_bwd_order_golden,
 ]
+
+
+# ---------------------------------------------------------------------------
+# mHC post with post = sigmoid(alpha * mix + b)
+# ---------------------------------------------------------------------------
+
+def check_post_sigmoid_fwd_half(o):
+    """mix = 0 and b = 0 give z = 0 and post = 0.5 exactly: the forward is the
+    post with post = 0.5, emulated in exact rationals."""
+    rng = np.random.default_rng(310)
+    for dtype in ("bf16", "f16"):
+        for n in (1, 2, 4, 8):
+            T, H = 2, 7
+            x = random_storage(rng, (T, n, H), dtype, scale=2.0)
+            y = random_storage(rng, (T, H), dtype, scale=2.0)
+            res = rng.random((T, n, n), dtype=np.float32)
+            got = o.post_sigmoid_fwd(x, y, np.zeros((T, n), np.float32), np.float32(1.7),
+                                     np.zeros(n, np.float32), res, dtype)
+            want = _post_exact(x, y, np.full((T, n), 0.5, dtype=np.float32), res, dtype)
+            assert np.array_equal(got, want), (dtype, n)
+
+
+def check_post_sigmoid_bwd_half(o):
+    """z = 0: sigmoid' = 1/4 exactly, so with integer-valued g and y, grad_z is
+    the exact integer sum of g*y / 4, grad_mix = RN(alpha * grad_z); with
+    res = I, grad_x = g; grad_y = cvt(tree of g / 2) and grad_res the exact
+    integer sums."""
+    rng = np.random.default_rng(311)
+    lut = np.array([bf16_bits_of(float(v)) for v in range(-8, 9)], dtype=np.uint16)
+    for n in (1, 2, 4, 8):
+        T, H = 2, 2053
+        gi = rng.integers(-8, 9, size=(T, n, H))
+        xi = rng.integers(-8, 9, size=(T, n, H))
+        yi = rng.integers(-8, 9, size=(T, H))
+        alpha = np.float32(1.3)
+        res = np.broadcast_to(np.eye(n, dtype=np.float32), (T, n, n)).copy()
+        gx, gy, gz, gm, gr = o.post_sigmoid_bwd(lut[gi + 8], lut[xi + 8], lut[yi + 8],
+                                                np.zeros((T, n), np.float32), alpha,
+                                                np.zeros(n, np.float32), res)
+        exact = np.einsum("tkh,th->tk", gi, yi).astype(np.float64) / 4.0
+        assert np.array_equal(gz.astype(np.float64), exact), n
+        assert np.array_equal(f32_bits(gm), f32_bits(alpha * exact.astype(np.float32))), n
+        assert np.array_equal(gr.astype(np.float64), np.einsum("tkh,tjh->tkj", gi, xi).astype(np.float64)), n
+        assert np.array_equal(bf16_widen(gx), bf16_widen(lut[gi + 8])), n
+        # grad_y = sum over k of g / 2: integers / 2, exact in BF16 while |sum| <= 256
+        half_sum = gi.sum(axis=1).astype(np.float64) / 2.0
+        assert np.array_equal(bf16_widen(gy).astype(np.float64), half_sum), n
+
+
+def check_post_sigmoid_wiring(o):
+    """Random mix, alpha, b: the forward and backward are post_fwd / post_bwd at
+    post = sigmoid32(RN(RN(alpha * mix) + b[k])) (pre-activation by numpy
+    binary32 arithmetic), grad_z = RN(grad_post * sigmoid'(z)) and
+    grad_mix = RN(alpha * grad_z)."""
+    rng = np.random.default_rng(312)
+    for dtype, n, T, H in (("bf16", 4, 4, 40), ("f16", 2, 3, 21), ("bf16", 8, 2, 16), ("f16", 1, 5, 9)):
+        g = random_storage(rng, (T, n, H), dtype)
+        x = random_storage(rng, (T, n, H), dtype)
+        y = random_storage(rng, (T, H), dtype)
+        res = rng.random((T, n, n), dtype=np.float32)
+        mix, alpha, b = _coeff_inputs(rng, T, n)
+        z = ((alpha * mix).astype(np.float32) + b[None, :]).astype(np.float32)
+        post, ds = o.sigmoid32(z)
+        assert np.array_equal(o.post_sigmoid_fwd(x, y, mix, alpha, b, res, dtype),
+                              o.post_fwd(x, y, post, res, dtype)), (dtype, n)
+        gx, gy, gz, gm, gr = o.post_sigmoid_bwd(g, x, y, mix, alpha, b, res, dtype)
+        wx, wy, wp, wr = o.post_bwd(g, x, y, post, res, dtype)
+        assert np.array_equal(gx, wx) and np.array_equal(gy, wy) and np.array_equal(gr, wr), (dtype, n)
+        assert np.array_equal(f32_bits(gz), f32_bits((wp * ds).astype(np.float32))), (dtype, n)
+        assert np.array_equal(f32_bits(gm), f32_bits((alpha * gz).astype(np.float32))), (dtype, n)
+
+
+ALL_CHECKS += [
+    check_post_sigmoid_fwd_half,
+    check_post_sigmoid_bwd_half,
+    check_post_sigmoid_wiring,
+]

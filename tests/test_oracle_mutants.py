@@ -119,7 +119,7 @@ MUTANTS = {
     "preact_fma": ("    return scaled + b;", "    return __builtin_fmaf(alpha, mix, b) + 0.0f * scaled;"),
     "preact_bias_first_column": ("pre_activation(alpha[0], mix[t * n + k], b[k])",
                                  "pre_activation(alpha[0], mix[t * n + k], b[0])"),
-    "bwd_grad_z_uses_sigmoid": ("grad_pre[i] * oracle_sigmoid32_grad(z)", "grad_pre[i] * oracle_sigmoid32(z)"),
+    "bwd_grad_z_uses_sigmoid": ("grad_c[i] * oracle_sigmoid32_grad(z)", "grad_c[i] * oracle_sigmoid32(z)"),
     "bwd_grad_mix_unscaled": ("grad_mix[i] = alpha[0] * grad_z[i];", "grad_mix[i] = grad_z[i];"),
     "bwd_bias_index": ("pre_activation(alpha[0], mix[i], b[i % n])", "pre_activation(alpha[0], mix[i], b[i / n % n])"),
     "param_alpha_without_mix": ("p[k] = grad_z[t * n + k] * mix[t * n + k];", "p[k] = grad_z[t * n + k];"),
@@ -142,6 +142,13 @@ MUTANTS = {
                                      "for (int64_t k = 0; k < n; ++k) q[k] = 1.0f * widen("),
     "post_bwd_grad_post_against_x": ("grad_post[t * n + k] = grad_pre_row(g_row, y + t * H, H, dtype);",
                                      "grad_post[t * n + k] = grad_pre_row(g_row, x + (t * n + k) * H, H, dtype);"),
+    # mHC post with post = sigmoid(alpha * mix + b)
+    "post_sigmoid_fwd_mix_as_post": ("int rc = oracle_post_fwd(x, y, post, res, out, T, n, H, dtype);",
+                                     "int rc = oracle_post_fwd(x, y, mix, res, out, T, n, H, dtype);"),
+    "post_sigmoid_bwd_mix_as_post": ("int rc = oracle_post_bwd(g, x, y, post, res, grad_x, grad_y, grad_post,",
+                                     "int rc = oracle_post_bwd(g, x, y, mix, res, grad_x, grad_y, grad_post,"),
+    "post_sigmoid_bwd_outputs_swapped": ("sigmoid_epilogue(grad_post, mix, alpha, b, grad_z, grad_mix, T, n);",
+                                         "sigmoid_epilogue(grad_post, mix, alpha, b, grad_mix, grad_z, T, n);"),
     "post_bwd_grad_res_wrong_row": ("grad_res[(t * n + k) * n + j] = grad_pre_row(g_row, x + (t * n + j) * H, H, dtype);",
                                     "grad_res[(t * n + k) * n + j] = grad_pre_row(g_row, x + (t * n + k) * H, H, dtype);"),
     "hc_grad_pre_wrong_row": ("grad_pre_row(g + t * H, residual + (t * n + k) * H, H, dtype)",
