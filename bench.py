@@ -665,6 +665,29 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
                         "steady": {"us": us_b, "sets": ns, **entry_for(us_b, bb)}})
         del x, y, post, res, g, sets, bsets
         torch.cuda.empty_cache()
+
+    # the mHC post with post = sigmoid(alpha * mix + b) computed in the kernels, n = 4
+    T, H, n = 4096, 7168, 4
+    x, y, _, res, g = post_inputs(T, H, n, "normal", 6, device=dev, with_grad=True)
+    mix, alpha, b = coeff_inputs(T, n, "normal", 7, device=dev)
+    fb = T * (2 * (2 * n + 1) * H + 4 * n + 4 * n * n)
+    bb = T * (2 * (3 * n + 2) * H + 12 * n + 8 * n * n)
+    ns = n_sets(fb) or 2
+    sets = [(g, x, y, mix, res)] + [tuple(t.clone() for t in (g, x, y, mix, res)) for _ in range(ns - 1)]
+    fsets = [(xx, yy, mm, alpha, b, rr, torch.empty_like(xx)) for _, xx, yy, mm, rr in sets]
+    us_f = time_steady(lambda *a: binding.mhc_post_sigmoid_fwd(*a), fsets)
+    del fsets
+    bsets = [(gg, xx, yy, mm, alpha, b, rr, torch.empty_like(xx), torch.empty_like(yy), torch.empty_like(mm),
+              torch.empty_like(mm), torch.empty_like(rr)) for gg, xx, yy, mm, rr in sets]
+    us_b = time_steady(lambda *a: binding.mhc_post_sigmoid_bwd(*a), bsets)
+    results.append({"workload": "post_sigmoid_n4_bf16", "dir": "fwd", "T": T, "H": H, "n": n,
+                    "note": "post = sigmoid(alpha*mix + b) computed in the kernel; bytes T*(18H + 80)",
+                    "steady": {"us": us_f, "sets": ns, **entry_for(us_f, fb)}})
+    results.append({"workload": "post_sigmoid_n4_bf16", "dir": "bwd", "T": T, "H": H, "n": n,
+                    "note": "grad_x, grad_y, grad_res, grad_z, grad_mix; bytes T*(28H + 176)",
+                    "steady": {"us": us_b, "sets": ns, **entry_for(us_b, bb)}})
+    del x, y, res, g, mix, sets, bsets
+    torch.cuda.empty_cache()
     torch.cuda.synchronize()
     return results
 

@@ -305,7 +305,37 @@ MHC_API mhc_status_t mhc_post_bwd(const void* grad_out, const void* x, const voi
                                   float* grad_post, float* grad_res, int64_t T, int32_t n,
                                   int64_t H, mhc_dtype_t dtype, mhc_stream_t stream);
 
-/* Kernel path of the two calls (no launch, no CUDA call). */
+/* The mHC post with its post coefficients computed from their own mix, as
+ * the pre coefficients are for the aggregate ("perf: fuse mHC coefficient
+ * backward epilogue", Summary, names the post sigmoid's derivative beside
+ * the pre one):
+ *
+ *   post[t,k] = sigmoid(z[t,k]),  z[t,k] = RN(RN(alpha * mix[t,k]) + b[k])
+ *   (the library's binary32 sigmoid, as for mhc_pre_sigmoid)
+ *
+ * mhc_post_sigmoid_fwd gives mhc_post_fwd's out at that post.
+ * mhc_post_sigmoid_bwd gives mhc_post_bwd's grad_x, grad_y and grad_res, and
+ * in place of grad_post grad_z[t,k] = RN(grad_post[t,k] * sigmoid'(z[t,k]))
+ * and grad_mix[t,k] = RN(alpha * grad_z[t,k]) (FP32 [T,n]); grad_b and
+ * grad_alpha then come from mhc_sigmoid_param_grad(grad_z, mix).  mix is
+ * FP32 [T,n], alpha one FP32 value, b FP32 [n]; the other arguments and all
+ * rules as for mhc_post_fwd / mhc_post_bwd (mix and grad_z take the places
+ * of post and grad_post in the alignment and overlap rules; grad_mix,
+ * alpha and b must overlap no output). */
+MHC_API mhc_status_t mhc_post_sigmoid_fwd(const void* x, const void* y, const float* mix,
+                                          const float* alpha, const float* b, const float* res,
+                                          void* out, int64_t T, int32_t n, int64_t H,
+                                          mhc_dtype_t dtype, mhc_stream_t stream);
+
+MHC_API mhc_status_t mhc_post_sigmoid_bwd(const void* grad_out, const void* x, const void* y,
+                                          const float* mix, const float* alpha, const float* b,
+                                          const float* res, void* grad_x, void* grad_y,
+                                          float* grad_z, float* grad_mix, float* grad_res,
+                                          int64_t T, int32_t n, int64_t H, mhc_dtype_t dtype,
+                                          mhc_stream_t stream);
+
+/* Kernel path of mhc_post_fwd / mhc_post_bwd (no launch, no CUDA call); the
+ * sigmoid variants take the same path for the same buffers. */
 MHC_API mhc_path_t mhc_post_fwd_path(const void* x, const void* y, const float* post,
                                      const float* res, const void* out, int64_t T, int32_t n,
                                      int64_t H);

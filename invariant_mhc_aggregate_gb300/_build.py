@@ -26,10 +26,10 @@ LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
 SOURCES = [os.path.join(CSRC, f) for f in
            ("mhc_h_aggregate.cu", "mhc_launch_bf16.cu", "mhc_launch_f16.cu",
             "mhc_launch_sigmoid_bf16.cu", "mhc_launch_sigmoid_f16.cu", "mhc_launch_coeffs.cu",
-            "mhc_launch_post.cu")]
+            "mhc_launch_post.cu", "mhc_launch_post_sigmoid.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in
                   ("fastdiv.cuh", "mhc_coeffs.cuh", "mhc_device.cuh", "mhc_shift.cuh", "mhc_post.cuh",
-                   "mhc_launch.cuh")] \
+                   "mhc_bulk.cuh", "mhc_launch.cuh", "mhc_launch_post.cuh")] \
     + [os.path.join(INCLUDE, "mhc_h_aggregate.h")]
 
 ARCH = "sm_103a"
@@ -68,9 +68,10 @@ def source_digest() -> str:
 
 
 KERNEL_FILES = [os.path.join(CSRC, f) for f in
-                ("mhc_device.cuh", "mhc_coeffs.cuh", "mhc_shift.cuh", "mhc_post.cuh", "fastdiv.cuh",
-                 "mhc_launch.cuh", "mhc_launch_bf16.cu", "mhc_launch_f16.cu", "mhc_launch_sigmoid_bf16.cu",
-                 "mhc_launch_sigmoid_f16.cu", "mhc_launch_coeffs.cu", "mhc_launch_post.cu")]
+                ("mhc_device.cuh", "mhc_coeffs.cuh", "mhc_shift.cuh", "mhc_post.cuh", "mhc_bulk.cuh",
+                 "fastdiv.cuh", "mhc_launch.cuh", "mhc_launch_post.cuh", "mhc_launch_bf16.cu",
+                 "mhc_launch_f16.cu", "mhc_launch_sigmoid_bf16.cu", "mhc_launch_sigmoid_f16.cu",
+                 "mhc_launch_coeffs.cu", "mhc_launch_post.cu", "mhc_launch_post_sigmoid.cu")]
 
 
 def _code_only(text: str) -> str:

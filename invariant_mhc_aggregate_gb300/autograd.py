@@ -155,3 +155,63 @@ class MhcPost(torch.autograd.Function):
 def mhc_post(x: torch.Tensor, y: torch.Tensor, post: torch.Tensor, res: torch.Tensor) -> torch.Tensor:
     """Differentiable mHC post (see MhcPost)."""
     return MhcPost.apply(x, y, post, res)
+
+
+class MhcPostSigmoid(torch.autograd.Function):
+    """The mHC post with post = sigmoid(alpha * mix + b) computed inside the
+    kernels ("perf: fuse mHC coefficient backward epilogue", Summary: the post
+    sigmoid's derivative, grad_mix and the grad_b / alpha gradients).  The
+    backward is one fused kernel for grad_x, grad_y, grad_res, grad_z and
+    grad_mix, and one kernel summing grad_b and grad_alpha over tokens in a
+    fixed order."""
+
+    @staticmethod
+    def forward(ctx, x, y, mix, alpha, b, res):
+        if x.dtype not in (torch.bfloat16, torch.float16) or y.dtype != x.dtype:
+            raise TypeError("expects x [...,n,H] and y [...,H] of one type, bf16 or f16")
+        if mix.dtype != torch.float32 or res.dtype != torch.float32:
+            raise TypeError("expects mix [...,n] and res [...,n,n] fp32")
+        if x.dim() < 2:
+            raise ValueError(f"x must be [...,n,H], got {tuple(x.shape)}")
+        lead = x.shape[:-2]
+        n, H = x.shape[-2], x.shape[-1]
+        if y.shape != (*lead, H) or mix.shape != (*lead, n) or res.shape != (*lead, n, n):
+            raise ValueError(f"shape mismatch: x {tuple(x.shape)}, y {tuple(y.shape)}, "
+                             f"mix {tuple(mix.shape)}, res {tuple(res.shape)}")
+        xx = x.reshape(-1, n, H).contiguous()
+        yy = y.reshape(-1, H).contiguous()
+        mm = mix.reshape(-1, n).contiguous()
+        rr = res.reshape(-1, n, n).contiguous()
+        a = alpha.reshape(1).contiguous()
+        bb = b.contiguous()
+        out = binding.post_sigmoid(xx, yy, mm, a, bb, rr)
+        ctx.save_for_backward(xx, yy, mm, a, bb, rr)
+        ctx.lead = lead
+        ctx.alpha_shape = alpha.shape
+        return out.reshape(*lead, n, H)
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        xx, yy, mm, a, bb, rr = ctx.saved_tensors
+        n, H = xx.shape[-2], xx.shape[-1]
+        if grad_out.dtype != xx.dtype:
+            raise TypeError(f"the output gradient must be {xx.dtype}, got {grad_out.dtype}")
+        g = grad_out.reshape(-1, n, H).contiguous()
+        gx, gy, gz, gm, gr = binding.post_sigmoid_backward(g, xx, yy, mm, a, bb, rr)
+        grad_alpha = grad_b = None
+        if ctx.needs_input_grad[3] or ctx.needs_input_grad[4]:
+            grad_b, grad_alpha = binding.sigmoid_param_grad(gz, mm)
+            grad_alpha = grad_alpha.reshape(ctx.alpha_shape)
+        lead = ctx.lead
+        return (gx.reshape(*lead, n, H) if ctx.needs_input_grad[0] else None,
+                gy.reshape(*lead, H) if ctx.needs_input_grad[1] else None,
+                gm.reshape(*lead, n) if ctx.needs_input_grad[2] else None,
+                grad_alpha if ctx.needs_input_grad[3] else None,
+                grad_b if ctx.needs_input_grad[4] else None,
+                gr.reshape(*lead, n, n) if ctx.needs_input_grad[5] else None)
+
+
+def mhc_post_sigmoid(x: torch.Tensor, y: torch.Tensor, mix: torch.Tensor, alpha: torch.Tensor,
+                     b: torch.Tensor, res: torch.Tensor) -> torch.Tensor:
+    """Differentiable mHC post with post = sigmoid(alpha * mix + b) computed in the kernel."""
+    return MhcPostSigmoid.apply(x, y, mix, alpha, b, res)

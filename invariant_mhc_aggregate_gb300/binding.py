@@ -54,6 +54,8 @@ EXPORTS = (
     "mhc_sigmoid_param_grad",
     "mhc_post_fwd",
     "mhc_post_bwd",
+    "mhc_post_sigmoid_fwd",
+    "mhc_post_sigmoid_bwd",
     "mhc_post_fwd_path",
     "mhc_post_bwd_path",
     "mhc_status_string",
@@ -124,6 +126,10 @@ def load(path: str | None = None):
         lib.mhc_post_fwd.restype = i32
         lib.mhc_post_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i64, i32, i64, i32, p]
         lib.mhc_post_bwd.restype = i32
+        lib.mhc_post_sigmoid_fwd.argtypes = [p, p, p, p, p, p, p, i64, i32, i64, i32, p]
+        lib.mhc_post_sigmoid_fwd.restype = i32
+        lib.mhc_post_sigmoid_bwd.argtypes = [p, p, p, p, p, p, p, p, p, p, p, p, i64, i32, i64, i32, p]
+        lib.mhc_post_sigmoid_bwd.restype = i32
         lib.mhc_post_fwd_path.argtypes = [p, p, p, p, p, i64, i32, i64]
         lib.mhc_post_fwd_path.restype = i32
         lib.mhc_post_bwd_path.argtypes = [p, p, p, p, p, p, p, p, p, i64, i32, i64]
@@ -220,6 +226,18 @@ def post_bwd_raw(grad_out: int, x: int, y: int, post: int, res: int, grad_x: int
                  stream: int = 0) -> int:
     return load().mhc_post_bwd(grad_out, x, y, post, res, grad_x, grad_y, grad_post, grad_res,
                                T, n, H, dtype, stream)
+
+
+def post_sigmoid_fwd_raw(x: int, y: int, mix: int, alpha: int, b: int, res: int, out: int, T: int, n: int,
+                         H: int, dtype: int, stream: int = 0) -> int:
+    return load().mhc_post_sigmoid_fwd(x, y, mix, alpha, b, res, out, T, n, H, dtype, stream)
+
+
+def post_sigmoid_bwd_raw(grad_out: int, x: int, y: int, mix: int, alpha: int, b: int, res: int,
+                         grad_x: int, grad_y: int, grad_z: int, grad_mix: int, grad_res: int, T: int,
+                         n: int, H: int, dtype: int, stream: int = 0) -> int:
+    return load().mhc_post_sigmoid_bwd(grad_out, x, y, mix, alpha, b, res, grad_x, grad_y, grad_z,
+                                       grad_mix, grad_res, T, n, H, dtype, stream)
 
 
 def post_fwd_path_raw(x: int, y: int, post: int, res: int, out: int, T: int, n: int, H: int) -> int:
@@ -563,3 +581,64 @@ def post_backward(grad_out: torch.Tensor, x: torch.Tensor, y: torch.Tensor,
     grad_res = torch.empty((T, n, n), dtype=torch.float32, device=x.device)
     mhc_post_bwd(grad_out, x, y, post_coeffs, res, grad_x, grad_y, grad_post, grad_res, stream)
     return grad_x, grad_y, grad_post, grad_res
+
+
+# ---------------------------------------------------------------------------
+# mHC post with post = sigmoid(alpha * mix + b) computed in the kernels
+# ---------------------------------------------------------------------------
+
+def mhc_post_sigmoid_fwd(x: torch.Tensor, y: torch.Tensor, mix: torch.Tensor, alpha: torch.Tensor,
+                         b: torch.Tensor, res: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """out = the mHC post with post = sigmoid(alpha * mix + b), in one kernel."""
+    T, n, H, dt = _post_shapes(x, y, mix, res)
+    _check(out, "out", x.dtype, (T, n, H))
+    _coeff_params(alpha, b, n, x.device)
+    st = post_sigmoid_fwd_raw(x.data_ptr(), y.data_ptr(), mix.data_ptr(), alpha.data_ptr(), b.data_ptr(),
+                              res.data_ptr(), out.data_ptr(), T, n, H, dt, _stream_handle(stream, x.device))
+    if st != MHC_OK:
+        raise MhcError(st, "mhc_post_sigmoid_fwd")
+
+
+def mhc_post_sigmoid_bwd(grad_out: torch.Tensor, x: torch.Tensor, y: torch.Tensor, mix: torch.Tensor,
+                         alpha: torch.Tensor, b: torch.Tensor, res: torch.Tensor, grad_x: torch.Tensor,
+                         grad_y: torch.Tensor, grad_z: torch.Tensor, grad_mix: torch.Tensor,
+                         grad_res: torch.Tensor, stream=None) -> None:
+    """Fused backward: grad_x, grad_y, grad_res, and grad_z = grad_post * sigmoid'(z),
+    grad_mix = alpha * grad_z in the epilogue."""
+    T, n, H, dt = _post_shapes(x, y, mix, res)
+    _check(grad_out, "grad_out", x.dtype, (T, n, H))
+    _check(grad_x, "grad_x", x.dtype, (T, n, H))
+    _check(grad_y, "grad_y", x.dtype, (T, H))
+    _check(grad_z, "grad_z", torch.float32, (T, n))
+    _check(grad_mix, "grad_mix", torch.float32, (T, n))
+    _check(grad_res, "grad_res", torch.float32, (T, n, n))
+    _coeff_params(alpha, b, n, x.device)
+    st = post_sigmoid_bwd_raw(grad_out.data_ptr(), x.data_ptr(), y.data_ptr(), mix.data_ptr(),
+                              alpha.data_ptr(), b.data_ptr(), res.data_ptr(), grad_x.data_ptr(),
+                              grad_y.data_ptr(), grad_z.data_ptr(), grad_mix.data_ptr(), grad_res.data_ptr(),
+                              T, n, H, dt, _stream_handle(stream, x.device))
+    if st != MHC_OK:
+        raise MhcError(st, "mhc_post_sigmoid_bwd")
+
+
+def post_sigmoid(x: torch.Tensor, y: torch.Tensor, mix: torch.Tensor, alpha: torch.Tensor,
+                 b: torch.Tensor, res: torch.Tensor, stream=None) -> torch.Tensor:
+    """Allocate ``out`` [T,n,H] and run the post with post from the mix."""
+    out = torch.empty_like(x)
+    mhc_post_sigmoid_fwd(x, y, mix, alpha, b, res, out, stream)
+    return out
+
+
+def post_sigmoid_backward(grad_out: torch.Tensor, x: torch.Tensor, y: torch.Tensor, mix: torch.Tensor,
+                          alpha: torch.Tensor, b: torch.Tensor, res: torch.Tensor, stream=None):
+    """Allocate and return (grad_x [T,n,H], grad_y [T,H], grad_z [T,n], grad_mix [T,n],
+    grad_res [T,n,n])."""
+    T, n, H = _TnH(x)
+    grad_x = torch.empty_like(x)
+    grad_y = torch.empty((T, H), dtype=x.dtype, device=x.device)
+    grad_z = torch.empty((T, n), dtype=torch.float32, device=x.device)
+    grad_mix = torch.empty((T, n), dtype=torch.float32, device=x.device)
+    grad_res = torch.empty((T, n, n), dtype=torch.float32, device=x.device)
+    mhc_post_sigmoid_bwd(grad_out, x, y, mix, alpha, b, res, grad_x, grad_y, grad_z, grad_mix, grad_res,
+                         stream)
+    return grad_x, grad_y, grad_z, grad_mix, grad_res

@@ -15,7 +15,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 5;
+constexpr int kAbiVersion = 6;
 
 thread_local int32_t g_last_cuda_error = 0;
 
@@ -309,9 +309,10 @@ mhc_status_t post_fwd(const void* x, const void* y, const float* post, const flo
     const mhc_path_t path = post_fwd_path(x, y, post, res, out, T, n, H);
     if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
     if (path == MHC_PATH_VEC16 && uint64_t(H) / 8 > 0x7FFFFFFFull) return MHC_ERR_UNSUPPORTED;
-    const mhc::PostFwdCall c{x, y, post, res, out, uint64_t(T), uint64_t(H), int(n), int(path),
-                             num_sms(), reinterpret_cast<cudaStream_t>(stream)};
-    return finish(mhc::post_fwd(c, dtype == MHC_DTYPE_BF16 ? mhc::kBF16 : mhc::kF16));
+    const mhc::PostFwdCall c{x, y, res, out, uint64_t(T), uint64_t(H), int(n), int(path), num_sms(),
+                             reinterpret_cast<cudaStream_t>(stream)};
+    const mhc::PlainCoeffs k{post, nullptr, false};
+    return finish(mhc::post_fwd(c, k, dtype == MHC_DTYPE_BF16 ? mhc::kBF16 : mhc::kF16));
 }
 
 mhc_status_t post_bwd(const void* g, const void* x, const void* y, const float* post, const float* res,
@@ -325,10 +326,58 @@ mhc_status_t post_bwd(const void* g, const void* x, const void* y, const float* 
         post_bwd_path(g, x, y, post, res, grad_x, grad_y, grad_post, grad_res, T, n, H);
     if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
     if (path == MHC_PATH_VEC16 && uint64_t(H) / 8 > 0x7FFFFFFFull) return MHC_ERR_UNSUPPORTED;
-    const mhc::PostBwdCall c{g, x, y, post, res, grad_x, grad_y, grad_post, grad_res, uint64_t(T),
-                             uint64_t(H), int(n), int(path), num_sms(),
+    const mhc::PostBwdCall c{g, x, y, res, grad_x, grad_y, grad_res, uint64_t(T), uint64_t(H), int(n),
+                             int(path), num_sms(), reinterpret_cast<cudaStream_t>(stream)};
+    const mhc::PlainCoeffs k{post, grad_post, false};
+    return finish(mhc::post_bwd(c, k, dtype == MHC_DTYPE_BF16 ? mhc::kBF16 : mhc::kF16));
+}
+
+// ---- mHC post with post = sigmoid(alpha * mix + b) --------------------------
+
+mhc_status_t post_sigmoid_fwd(const void* x, const void* y, const float* mix, const float* alpha,
+                              const float* b, const float* res, void* out, int64_t T, int64_t n, int64_t H,
+                              int32_t dtype, mhc_stream_t stream) {
+    if (!dtype_ok(dtype)) return MHC_ERR_INVALID_ARG;
+    if (!streams_ok(n)) return MHC_ERR_UNSUPPORTED;
+    if (!sizes_ok(T, n, H)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    // mix stands in for post in the path check (same shape and rules)
+    const mhc_path_t path = post_fwd_path(x, y, mix, res, out, T, n, H);
+    if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
+    const Range ro = range_of(out, uint64_t(T) * 2 * uint64_t(n) * uint64_t(H));
+    if (!params_ok(alpha, b, n, &ro, 1)) return MHC_ERR_INVALID_ARG;
+    if (path == MHC_PATH_VEC16 && uint64_t(H) / 8 > 0x7FFFFFFFull) return MHC_ERR_UNSUPPORTED;
+    const mhc::PostFwdCall c{x, y, res, out, uint64_t(T), uint64_t(H), int(n), int(path), num_sms(),
                              reinterpret_cast<cudaStream_t>(stream)};
-    return finish(mhc::post_bwd(c, dtype == MHC_DTYPE_BF16 ? mhc::kBF16 : mhc::kF16));
+    const mhc::SigmoidCoeffs k{mix, alpha, b, nullptr, nullptr, false};
+    return finish(mhc::post_fwd(c, k, dtype == MHC_DTYPE_BF16 ? mhc::kBF16 : mhc::kF16));
+}
+
+mhc_status_t post_sigmoid_bwd(const void* g, const void* x, const void* y, const float* mix,
+                              const float* alpha, const float* b, const float* res, void* grad_x,
+                              void* grad_y, float* grad_z, float* grad_mix, float* grad_res, int64_t T,
+                              int64_t n, int64_t H, int32_t dtype, mhc_stream_t stream) {
+    if (!dtype_ok(dtype)) return MHC_ERR_INVALID_ARG;
+    if (!streams_ok(n)) return MHC_ERR_UNSUPPORTED;
+    if (!sizes_ok(T, n, H)) return MHC_ERR_INVALID_ARG;
+    if (T == 0) return MHC_OK;
+    // mix and grad_z stand in for post and grad_post in the path check
+    const mhc_path_t path = post_bwd_path(g, x, y, mix, res, grad_x, grad_y, grad_z, grad_res, T, n, H);
+    if (path == MHC_PATH_NONE) return MHC_ERR_INVALID_ARG;
+    if (!grad_mix || !aligned(grad_mix, 4)) return MHC_ERR_INVALID_ARG;
+    const uint64_t TH = uint64_t(T) * uint64_t(H), nu = uint64_t(n);
+    const Range outs[5] = {range_of(grad_x, TH * 2 * nu), range_of(grad_y, TH * 2),
+                           range_of(grad_z, uint64_t(T) * 4 * nu), range_of(grad_res, uint64_t(T) * 4 * nu * nu),
+                           range_of(grad_mix, uint64_t(T) * 4 * nu)};
+    const Range ins[5] = {range_of(g, TH * 2 * nu), range_of(x, TH * 2 * nu), range_of(y, TH * 2),
+                          range_of(mix, uint64_t(T) * 4 * nu), range_of(res, uint64_t(T) * 4 * nu * nu)};
+    if (!disjoint(outs, 5, ins, 5)) return MHC_ERR_INVALID_ARG;
+    if (!params_ok(alpha, b, n, outs, 5)) return MHC_ERR_INVALID_ARG;
+    if (path == MHC_PATH_VEC16 && uint64_t(H) / 8 > 0x7FFFFFFFull) return MHC_ERR_UNSUPPORTED;
+    const mhc::PostBwdCall c{g, x, y, res, grad_x, grad_y, grad_res, uint64_t(T), uint64_t(H), int(n),
+                             int(path), num_sms(), reinterpret_cast<cudaStream_t>(stream)};
+    const mhc::SigmoidCoeffs k{mix, alpha, b, grad_z, grad_mix, false};
+    return finish(mhc::post_bwd(c, k, dtype == MHC_DTYPE_BF16 ? mhc::kBF16 : mhc::kF16));
 }
 
 }  // namespace
@@ -439,6 +488,21 @@ mhc_status_t mhc_post_bwd(const void* grad_out, const void* x, const void* y, co
                           mhc_stream_t stream) {
     return post_bwd(grad_out, x, y, post, res, grad_x, grad_y, grad_post, grad_res, T, n, H,
                     int32_t(dtype), stream);
+}
+
+mhc_status_t mhc_post_sigmoid_fwd(const void* x, const void* y, const float* mix, const float* alpha,
+                                  const float* b, const float* res, void* out, int64_t T, int32_t n,
+                                  int64_t H, mhc_dtype_t dtype, mhc_stream_t stream) {
+    return post_sigmoid_fwd(x, y, mix, alpha, b, res, out, T, n, H, int32_t(dtype), stream);
+}
+
+mhc_status_t mhc_post_sigmoid_bwd(const void* grad_out, const void* x, const void* y, const float* mix,
+                                  const float* alpha, const float* b, const float* res, void* grad_x,
+                                  void* grad_y, float* grad_z, float* grad_mix, float* grad_res,
+                                  int64_t T, int32_t n, int64_t H, mhc_dtype_t dtype,
+                                  mhc_stream_t stream) {
+    return post_sigmoid_bwd(grad_out, x, y, mix, alpha, b, res, grad_x, grad_y, grad_z, grad_mix,
+                            grad_res, T, n, H, int32_t(dtype), stream);
 }
 
 mhc_path_t mhc_post_fwd_path(const void* x, const void* y, const float* post, const float* res,

@@ -51,11 +51,12 @@ cudaError_t fwd_f16(const FwdCall& c, const SigmoidCoeffs& k);
 cudaError_t bwd_bf16(const BwdCall& c, const SigmoidCoeffs& k);
 cudaError_t bwd_f16(const BwdCall& c, const SigmoidCoeffs& k);
 
-// mHC post (mhc_post.cuh, launched from mhc_launch_post.cu).
+// mHC post (mhc_post.cuh, launched from mhc_launch_post.cu and
+// mhc_launch_post_sigmoid.cu); the post coefficients (given, or from the mix)
+// and their gradient travel in the PlainCoeffs / SigmoidCoeffs value.
 struct PostFwdCall {
     const void* x;
     const void* y;
-    const float* post;
     const float* res;
     void* out;
     uint64_t T, H;
@@ -69,11 +70,9 @@ struct PostBwdCall {
     const void* g;
     const void* x;
     const void* y;
-    const float* post;
     const float* res;
     void* grad_x;
     void* grad_y;
-    float* grad_post;
     float* grad_res;
     uint64_t T, H;
     int n;
@@ -82,8 +81,10 @@ struct PostBwdCall {
     cudaStream_t stream;
 };
 
-cudaError_t post_fwd(const PostFwdCall& c, int dtype);
-cudaError_t post_bwd(const PostBwdCall& c, int dtype);
+cudaError_t post_fwd(const PostFwdCall& c, const PlainCoeffs& k, int dtype);
+cudaError_t post_bwd(const PostBwdCall& c, const PlainCoeffs& k, int dtype);
+cudaError_t post_fwd(const PostFwdCall& c, const SigmoidCoeffs& k, int dtype);
+cudaError_t post_bwd(const PostBwdCall& c, const SigmoidCoeffs& k, int dtype);
 // 1 if a bounded wait of the bulk-copy kernels ran out on the current device
 // since the last call, else 0 (clears the record; synchronizes the device);
 // -1 on a CUDA error.

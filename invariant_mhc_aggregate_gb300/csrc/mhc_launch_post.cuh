@@ -1,0 +1,138 @@
+// Launch shapes of the mHC post kernels (mhc_post.cuh), templated on the
+// post coefficient source; instantiated by mhc_launch_post.cu (post given)
+// and mhc_launch_post_sigmoid.cu (post from the mix).
+#pragma once
+
+#include <atomic>
+
+#include "mhc_launch.cuh"
+
+namespace mhc {
+
+// The device address of the flag that the bulk-copy kernels set when a
+// bounded wait runs out (defined in mhc_launch_post.cu), for the current device.
+cudaError_t wait_flag_ptr(unsigned int** p);
+
+namespace post_launch {
+
+constexpr int kMaxDevices = 64;
+
+inline int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+// Raises a kernel's dynamic shared-memory limit, once per device (`done`
+// holds one bit per device for that kernel).
+template <class K>
+cudaError_t allow_smem(K kernel, uint32_t bytes, std::atomic<uint64_t>& done) {
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << dev;
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+// Vector indices are 32-bit: calls of 2^31 vectors or more run as several
+// launches over consecutive token ranges (tokens are independent).
+template <int N, int DT, int NW, int U, int MIN_BLOCKS, class Coeffs>
+cudaError_t fwd_vec(const PostFwdCall& c, const Coeffs& k) {
+    const uint64_t V = c.H / (2 * NW);
+    const uint64_t max_tokens = 0x7FFFFFFFull / V;
+    for (uint64_t t0 = 0; t0 < c.T; t0 += max_tokens) {
+        const uint64_t nt = (c.T - t0 < max_tokens) ? c.T - t0 : max_tokens;
+        const uint32_t n_vec = uint32_t(nt * V);
+        const auto* x = static_cast<const Words<NW>*>(c.x) + uint64_t(N) * t0 * V;
+        const auto* y = static_cast<const Words<NW>*>(c.y) + t0 * V;
+        auto* o = static_cast<Words<NW>*>(c.out) + uint64_t(N) * t0 * V;
+        const cudaError_t e =
+            launch(post_fwd_vec_kernel<N, DT, NW, U, MIN_BLOCKS, Coeffs>, grid_for(n_vec, kPostBlock * U, ~0u),
+                   kPostBlock, c.stream, x, y, k.shifted(uint64_t(N) * t0), c.res + uint64_t(N) * N * t0, o,
+                   n_vec, uint32_t(V), make_fastdiv_u32(uint32_t(V)));
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+// Launch shapes (measured at T = 4096, H = 7168): 16-byte vectors, one per
+// thread, with the register budget of 4 blocks per SM (2 at n = 8, whose
+// inputs alone take 36 registers); 32-byte vectors, more vectors per thread
+// or fewer blocks per SM were slower.
+template <int N, int DT, class Coeffs>
+cudaError_t fwd_n(const PostFwdCall& c, const Coeffs& k) {
+    if (c.path == kPathVec16) return fwd_vec<N, DT, 4, 1, (N >= 8 ? 2 : 4)>(c, k);
+    return launch2d(post_fwd_element_kernel<N, DT, Coeffs>, narrow_grid(c.H, c.T), kNarrowBlock, c.stream,
+                    static_cast<const uint16_t*>(c.x), static_cast<const uint16_t*>(c.y), k, c.res,
+                    static_cast<uint16_t*>(c.out), c.T, c.H);
+}
+
+template <int N, int DT, int NW, int BATCH, int MIN_BLOCKS, bool SMEM_COEF, class Coeffs>
+cudaError_t bwd_vec(const PostBwdCall& c, const Coeffs& k) {
+    const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
+    return launch(post_bwd_vec_kernel<N, DT, NW, BATCH, MIN_BLOCKS, SMEM_COEF, Coeffs>, blocks, kLanes / (NW / 4),
+                  c.stream, static_cast<const Words<NW>*>(c.g), static_cast<const Words<NW>*>(c.x),
+                  static_cast<const Words<NW>*>(c.y), k, c.res, static_cast<Words<NW>*>(c.grad_x),
+                  static_cast<Words<NW>*>(c.grad_y), c.grad_res, c.T, uint32_t(c.H / (2 * NW)));
+}
+
+// Bulk-copy backward: a persistent grid of MIN_BLOCKS blocks per SM, each
+// with a STAGES-deep ring of (2n + 1) x 4 KB stages.
+template <int N, int DT, int STAGES, int MIN_BLOCKS, class Coeffs>
+cudaError_t bwd_bulk(const PostBwdCall& c, const Coeffs& k) {
+    static std::atomic<uint64_t> smem_done{0};
+    constexpr uint32_t smem = STAGES * post_bulk_stage_bytes(N);
+    auto* kernel = post_bwd_bulk_kernel<N, DT, STAGES, MIN_BLOCKS, Coeffs>;
+    cudaError_t e = allow_smem(kernel, smem, smem_done);
+    if (e != cudaSuccess) return e;
+    unsigned int* flag = nullptr;
+    if ((e = wait_flag_ptr(&flag)) != cudaSuccess) return e;
+    const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * MIN_BLOCKS);
+    return launch_smem(kernel, blocks, kBulkThreads, smem, c.stream, static_cast<const Words<4>*>(c.g),
+                       static_cast<const Words<4>*>(c.x), static_cast<const Words<4>*>(c.y), k, c.res,
+                       static_cast<Words<4>*>(c.grad_x), static_cast<Words<4>*>(c.grad_y), c.grad_res, c.T,
+                       uint32_t(c.H / 8), flag);
+}
+
+template <int N, int DT, class Coeffs>
+cudaError_t bwd_n(const PostBwdCall& c, const Coeffs& k) {
+    // 16-byte path: the bulk-copy kernel (2 blocks per SM, a 3-stage ring) up
+    // to n = 4; at n = 8 one 16-byte vector per thread and pass, 1 block per
+    // SM, the coefficients in shared memory
+    if (c.path == kPathVec16) {
+        if constexpr (N >= 8) return bwd_vec<N, DT, 4, 1, 1, true>(c, k);
+        else return bwd_bulk<N, DT, 3, 2>(c, k);
+    }
+    const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
+    return launch(post_bwd_element_kernel<N, DT, Coeffs>, blocks, kLanes, c.stream,
+                  static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.x),
+                  static_cast<const uint16_t*>(c.y), k, c.res, static_cast<uint16_t*>(c.grad_x),
+                  static_cast<uint16_t*>(c.grad_y), c.grad_res, c.T, c.H);
+}
+
+template <class Coeffs>
+cudaError_t fwd(const PostFwdCall& c, const Coeffs& k, int dtype) {
+    const bool bf = dtype == kBF16;
+    switch (c.n) {
+        case 1: return bf ? fwd_n<1, kBF16>(c, k) : fwd_n<1, kF16>(c, k);
+        case 2: return bf ? fwd_n<2, kBF16>(c, k) : fwd_n<2, kF16>(c, k);
+        case 4: return bf ? fwd_n<4, kBF16>(c, k) : fwd_n<4, kF16>(c, k);
+        default: return bf ? fwd_n<8, kBF16>(c, k) : fwd_n<8, kF16>(c, k);
+    }
+}
+
+template <class Coeffs>
+cudaError_t bwd(const PostBwdCall& c, const Coeffs& k, int dtype) {
+    const bool bf = dtype == kBF16;
+    switch (c.n) {
+        case 1: return bf ? bwd_n<1, kBF16>(c, k) : bwd_n<1, kF16>(c, k);
+        case 2: return bf ? bwd_n<2, kBF16>(c, k) : bwd_n<2, kF16>(c, k);
+        case 4: return bf ? bwd_n<4, kBF16>(c, k) : bwd_n<4, kF16>(c, k);
+        default: return bf ? bwd_n<8, kBF16>(c, k) : bwd_n<8, kF16>(c, k);
+    }
+}
+
+}  // namespace post_launch
+}  // namespace mhc

@@ -58,8 +58,9 @@ struct BlockSync {
 };
 
 // The coefficients of the token a backward block works on.  Up to n = 4 they
-// sit in registers; at n = 8 (72 values, next to 72 lane sums) in shared
-// memory, read where they are used.
+// sit in registers (loaded from global memory, or copied from the token
+// table); at n = 8 (72 values, next to 72 lane sums) they stay in the token
+// table in shared memory, read where they are used.
 template <int N, bool kShared = (N >= 8)>
 struct PostCoeffs {
     float pk[N], rk[N][N];
@@ -68,27 +69,75 @@ struct PostCoeffs {
                                          Sync = Sync()) {
         ld_post_coeffs<N>(post, res, t, pk, rk);
     }
+    // ... or from a token table in shared memory (post_fill_table)
+    __device__ __forceinline__ void from_table(const float* tab) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+            pk[k] = tab[N * N + k];
+#pragma unroll
+            for (int j = 0; j < N; ++j) rk[k][j] = tab[k * N + j];
+        }
+    }
     __device__ __forceinline__ float r(int k, int j) const { return rk[k][j]; }
     __device__ __forceinline__ float p(int k) const { return pk[k]; }
 };
 
 template <int N>
 struct PostCoeffs<N, true> {
-    const float* s;   // rk row-major, then pk
-    // Every thread of the block calls this; the previous token's readers have
-    // passed the fold's closing barrier.
-    template <class Sync = BlockSync>
-    __device__ __forceinline__ void load(const float* post, const float* res, uint64_t t, float* smem,
-                                         Sync sync = Sync()) {
-        if (threadIdx.x < uint32_t(N * N)) smem[threadIdx.x] = __ldg(res + uint64_t(N) * N * t + threadIdx.x);
-        else if (threadIdx.x < uint32_t(N * N + N))
-            smem[threadIdx.x] = __ldg(post + uint64_t(N) * t + (threadIdx.x - N * N));
-        sync();
-        s = smem;
-    }
+    const float* s;   // the token table (post_fill_table): res row-major, then post
+    __device__ __forceinline__ void from_table(const float* tab) { s = tab; }
     __device__ __forceinline__ float r(int k, int j) const { return s[k * N + j]; }
     __device__ __forceinline__ float p(int k) const { return s[N * N + k]; }
 };
+
+// Token t's table in shared memory, written by threads j < n*n + n of the
+// group that shares it: res[t] row-major (n*n), post[t] (n), and, when post
+// is computed from the mix (Coeffs::kBlockTable), sigmoid'(z[t]) (n) for the
+// backward's epilogue.  Ends with the group's barrier.
+template <int N>
+constexpr int kPostTable = N * N + 2 * N;
+
+template <int N, class Coeffs, class Sync>
+__device__ __forceinline__ void post_fill_table(const Coeffs& c, const float* __restrict__ res, uint64_t t,
+                                                uint32_t j, float* tab, Sync sync) {
+    if (j < uint32_t(N * N)) {
+        tab[j] = __ldg(res + uint64_t(N) * N * t + j);
+    } else if (j < uint32_t(N * N + N)) {
+        const int k = int(j) - N * N;
+        if constexpr (Coeffs::kBlockTable) {
+            c.pre_and_slope(c.mix_at(uint64_t(N) * t + k), k, tab[j], tab[j + N]);
+        } else {
+            tab[j] = __ldg(c.pre + uint64_t(N) * t + k);
+        }
+    }
+    sync();
+}
+
+// Token t's coefficients into cf: straight from global memory (post given,
+// registers), else through the token table.  Every thread of the group
+// calls it; the previous token's readers have passed the fold's closing
+// barrier.
+template <int N, bool SMEM, class Coeffs, class Sync>
+__device__ __forceinline__ void post_load_token(const Coeffs& c, const float* __restrict__ res, uint64_t t,
+                                                uint32_t j, float* tab, PostCoeffs<N, SMEM>& cf, Sync sync) {
+    if constexpr (Coeffs::kBlockTable || SMEM) {
+        post_fill_table<N>(c, res, t, j, tab, sync);
+        cf.from_table(tab);
+    } else {
+        cf.load(c.pre, res, t, tab, sync);
+    }
+}
+
+// The gradient of post[t,k] (the lane sum w) through the coefficient source:
+// grad_post itself, or grad_z and grad_mix with the slope from the table.
+template <int N, class Coeffs>
+__device__ __forceinline__ void post_store_grad(const Coeffs& c, uint64_t t, int k, float w, const float* tab) {
+    if constexpr (Coeffs::kBlockTable) {
+        c.template store_grad_slope<N>(t, k, w, tab[N * N + N + k]);
+    } else {
+        c.template store_grad<N>(t, k, w);
+    }
+}
 
 // One output value of stream k from the n input values xs and y, given row
 // k of res (rk) and post[t,k] (pk).
@@ -100,12 +149,10 @@ __device__ __forceinline__ float post_value(const float (&rk)[N], float pk, cons
     return __fadd_rn(tree_sum<N>(p), __fmul_rn(pk, ys));
 }
 
-// Row k of res and post[t,k] for token t (read-only cache: every thread of a
-// token reads the same values).
+// Row k of res for token t (read-only cache: every thread of a token reads
+// the same values).
 template <int N>
-__device__ __forceinline__ void ld_post_row(const float* post, const float* res, uint64_t t, int k,
-                                            float (&rk)[N], float& pk) {
-    pk = __ldg(post + uint64_t(N) * t + k);
+__device__ __forceinline__ void ld_res_row(const float* res, uint64_t t, int k, float (&rk)[N]) {
 #pragma unroll
     for (int j = 0; j < N; ++j) rk[j] = __ldg(res + (uint64_t(N) * t + k) * N + j);
 }
@@ -120,13 +167,28 @@ constexpr int kPostBlock = 256;
 // b taking vectors b*BLOCK*U + u*BLOCK + threadIdx (u < U): each thread loads
 // the n x vectors and the y vector of its U positions, then writes their n
 // output vectors.
-template <int N, int DT, int NW, int U, int MIN_BLOCKS>
+//
+// With post computed from the mix (Coeffs::kBlockTable) the block's first
+// threads evaluate the sigmoids of the tokens it touches into shared memory,
+// before any bulk load, and one barrier publishes them.
+template <int N, int DT, int NW, int U, int MIN_BLOCKS, class Coeffs>
 __global__ void __launch_bounds__(kPostBlock, MIN_BLOCKS)
-post_fwd_vec_kernel(const Words<NW>* __restrict__ x, const Words<NW>* __restrict__ y,
-                    const float* __restrict__ post, const float* __restrict__ res,
-                    Words<NW>* __restrict__ out, uint32_t n_vec, uint32_t V, FastDivU32 divV) {
+post_fwd_vec_kernel(const Words<NW>* __restrict__ x, const Words<NW>* __restrict__ y, Coeffs coeffs,
+                    const float* __restrict__ res, Words<NW>* __restrict__ out, uint32_t n_vec, uint32_t V,
+                    FastDivU32 divV) {
+    __shared__ float table[Coeffs::kBlockTable ? (kPostBlock * U + 1) * N : 1];
     pdl_enter();
     const uint32_t i0 = blockIdx.x * (kPostBlock * U) + threadIdx.x;
+    uint32_t t_first = 0;
+    if constexpr (Coeffs::kBlockTable) {
+        const uint32_t first = blockIdx.x * (kPostBlock * U);
+        const uint32_t last = (n_vec - first > uint32_t(kPostBlock * U)) ? first + kPostBlock * U - 1 : n_vec - 1;
+        t_first = fastdiv_u32(first, divV);
+        const uint32_t count = (fastdiv_u32(last, divV) - t_first + 1) * N;
+        for (uint32_t q = threadIdx.x; q < count; q += kPostBlock)
+            table[q] = coeffs.pre_from(coeffs.mix_at(uint64_t(N) * t_first + q), int(q % N));
+        __syncthreads();
+    }
     Words<NW> xv[U][N], yv[U];
     uint32_t tok[U];
     uint64_t row0[U];   // x / out vector of stream 0
@@ -147,8 +209,11 @@ post_fwd_vec_kernel(const Words<NW>* __restrict__ x, const Words<NW>* __restrict
         if (i < n_vec) {
 #pragma unroll
             for (int k = 0; k < N; ++k) {
-                float rk[N], pk;
-                ld_post_row<N>(post, res, tok[u], k, rk, pk);
+                float rk[N];
+                ld_res_row<N>(res, tok[u], k, rk);
+                float pk;
+                if constexpr (Coeffs::kBlockTable) pk = table[(tok[u] - t_first) * N + k];
+                else pk = __ldg(coeffs.pre + uint64_t(N) * tok[u] + k);
                 Words<NW> o;
 #pragma unroll
                 for (int e = 0; e < NW; ++e) {
@@ -168,15 +233,22 @@ post_fwd_vec_kernel(const Words<NW>* __restrict__ x, const Words<NW>* __restrict
 }
 
 // 2-byte path: a 2-D grid of (2048-value row segment, token) blocks,
-// grid-stride over tokens; thread j takes values e*256 + j (e < 8).
-template <int N, int DT>
+// grid-stride over tokens; thread j takes values e*256 + j (e < 8).  With
+// post computed from the mix, the token's n sigmoids go through shared
+// memory (threads 0 .. n-1, one barrier before and after their use).
+template <int N, int DT, class Coeffs>
 __global__ void __launch_bounds__(kNarrowBlock)
-post_fwd_element_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ y,
-                        const float* __restrict__ post, const float* __restrict__ res,
-                        uint16_t* __restrict__ out, uint64_t T, uint64_t H) {
+post_fwd_element_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ y, Coeffs coeffs,
+                        const float* __restrict__ res, uint16_t* __restrict__ out, uint64_t T, uint64_t H) {
+    __shared__ float table[N];
     pdl_enter();
     const uint64_t base = uint64_t(blockIdx.x) * kNarrowSeg + threadIdx.x;
     for (uint64_t t = blockIdx.y; t < T; t += gridDim.y) {
+        if constexpr (Coeffs::kBlockTable) {
+            if (threadIdx.x < uint32_t(N))
+                table[threadIdx.x] = coeffs.pre_from(coeffs.mix_at(uint64_t(N) * t + threadIdx.x), int(threadIdx.x));
+            __syncthreads();
+        }
 #pragma unroll 2
         for (int e = 0; e < kNarrowPerThread; ++e) {
             const uint64_t h = base + uint64_t(e) * kNarrowBlock;
@@ -187,12 +259,16 @@ post_fwd_element_kernel(const uint16_t* __restrict__ x, const uint16_t* __restri
                 const float ys = Elem<DT>::one(ld_stream2(y + t * H + h));
 #pragma unroll
                 for (int k = 0; k < N; ++k) {
-                    float rk[N], pk;
-                    ld_post_row<N>(post, res, t, k, rk, pk);
+                    float rk[N];
+                    ld_res_row<N>(res, t, k, rk);
+                    float pk;
+                    if constexpr (Coeffs::kBlockTable) pk = table[k];
+                    else pk = __ldg(coeffs.pre + uint64_t(N) * t + k);
                     st_stream2(out + (uint64_t(N) * t + k) * H + h, Elem<DT>::cvt(post_value<N>(rk, pk, xs, ys)));
                 }
             }
         }
+        if constexpr (Coeffs::kBlockTable) __syncthreads();   // table[] is rewritten for the next token
     }
 }
 
@@ -203,10 +279,12 @@ post_fwd_element_kernel(const uint16_t* __restrict__ x, const uint16_t* __restri
 // The ORDER-256 fold of M = n*n + n lane sums of a 256-lane block (LPT lanes
 // per thread: lanes LPT*thread + l): xor shuffles over each group of 32 lanes,
 // the 8 group values through shared memory; grad_res[t,k,j] = value k*n + j,
-// grad_post[t,k] = value n*n + k.  All threads of the block call it.
-template <int N, int LPT, class Sync = BlockSync>
+// and value n*n + k, the gradient of post[t,k], goes to the coefficient
+// source (post_store_grad; `tab` is the token table when there is one).  All
+// threads of the block call it.
+template <int N, int LPT, class Coeffs, class Sync = BlockSync>
 __device__ __forceinline__ void post_fold_and_store(float (&acc)[LPT][N * N + N], float (*red)[N * N + N],
-                                                    float* __restrict__ grad_post,
+                                                    const Coeffs& coeffs, const float* tab,
                                                     float* __restrict__ grad_res, uint64_t t,
                                                     Sync sync = Sync()) {
     constexpr int M = N * N + N;
@@ -237,7 +315,7 @@ __device__ __forceinline__ void post_fold_and_store(float (&acc)[LPT][N * N + N]
             for (int i = 0; i < s; ++i) w[i] = __fadd_rn(w[i], w[i + s]);
         }
         if (m < N * N) grad_res[uint64_t(N) * N * t + m] = w[0];
-        else grad_post[uint64_t(N) * t + (m - N * N)] = w[0];
+        else post_store_grad<N>(coeffs, t, m - N * N, w[0], tab);
     }
     sync();   // red[] (and the coefficient table) are reused by the next token
 }
@@ -293,23 +371,22 @@ __device__ __forceinline__ void post_chunk(const C& cf, const Words<NW> (&gv)[N]
 // j + 2B, ... (B threads), i.e. for lane LPT*j + l the chunks
 // (LPT*j + l) + 256m, in increasing order; BATCH vectors of each row are
 // loaded per pass.
-template <int N, int DT, int NW, int BATCH, int MIN_BLOCKS, bool SMEM_COEF>
+template <int N, int DT, int NW, int BATCH, int MIN_BLOCKS, bool SMEM_COEF, class Coeffs>
 __global__ void __launch_bounds__(kLanes / (NW / 4), MIN_BLOCKS)
 post_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict__ x,
-                    const Words<NW>* __restrict__ y, const float* __restrict__ post,
-                    const float* __restrict__ res, Words<NW>* __restrict__ grad_x,
-                    Words<NW>* __restrict__ grad_y, float* __restrict__ grad_post,
+                    const Words<NW>* __restrict__ y, Coeffs coeffs, const float* __restrict__ res,
+                    Words<NW>* __restrict__ grad_x, Words<NW>* __restrict__ grad_y,
                     float* __restrict__ grad_res, uint64_t T, uint32_t V) {
     constexpr int M = N * N + N;
     constexpr int LPT = NW / 4;
     constexpr uint32_t B = kLanes / LPT;
     __shared__ float red[kGroups][M];
-    __shared__ float coef[M];
+    __shared__ float coef[kPostTable<N>];
     pdl_enter();
     const uint32_t j = threadIdx.x;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
         PostCoeffs<N, SMEM_COEF> cf;
-        cf.load(post, res, t, coef);
+        post_load_token<N>(coeffs, res, t, j, coef, cf, BlockSync());
         float acc[LPT][M];
 #pragma unroll
         for (int l = 0; l < LPT; ++l)
@@ -342,7 +419,7 @@ post_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict
                 }
             }
         }
-        post_fold_and_store<N, LPT>(acc, red, grad_post, grad_res, t);
+        post_fold_and_store<N, LPT>(acc, red, coeffs, coef, grad_res, t);
     }
 }
 
@@ -370,12 +447,11 @@ __host__ __device__ constexpr uint32_t post_bulk_stage_bytes(int n) {
     return uint32_t(2 * n + 1) * kLanes * 16u;
 }
 
-template <int N, int DT, int STAGES, int MIN_BLOCKS>
+template <int N, int DT, int STAGES, int MIN_BLOCKS, class Coeffs>
 __global__ void __launch_bounds__(kBulkThreads, MIN_BLOCKS)
 post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict__ x,
-                     const Words<4>* __restrict__ y, const float* __restrict__ post,
-                     const float* __restrict__ res, Words<4>* __restrict__ grad_x,
-                     Words<4>* __restrict__ grad_y, float* __restrict__ grad_post,
+                     const Words<4>* __restrict__ y, Coeffs coeffs, const float* __restrict__ res,
+                     Words<4>* __restrict__ grad_x, Words<4>* __restrict__ grad_y,
                      float* __restrict__ grad_res, uint64_t T, uint32_t V,
                      unsigned int* __restrict__ timeouts) {
     constexpr int R = 2 * N + 1;   // staged rows: g (N), x (N), y
@@ -384,7 +460,7 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
     __shared__ __align__(8) uint64_t full[STAGES];
     __shared__ __align__(8) uint64_t empty[STAGES];
     __shared__ float red[kGroups][M];
-    __shared__ float coef[M];
+    __shared__ float coef[kPostTable<N>];
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
@@ -433,7 +509,7 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
     uint32_t item = 0;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
         PostCoeffs<N> cf;
-        cf.load(post, res, t, coef, sync);
+        post_load_token<N>(coeffs, res, t, j, coef, cf, sync);
         float acc[1][M];
 #pragma unroll
         for (int m = 0; m < M; ++m) acc[0][m] = 0.0f;
@@ -460,7 +536,7 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
             __syncwarp();
             if ((j & 31u) == 0) mbar_arrive(&empty[st]);
         }
-        post_fold_and_store<N, 1>(acc, red, grad_post, grad_res, t, sync);
+        post_fold_and_store<N, 1>(acc, red, coeffs, coef, grad_res, t, sync);
     }
     if (!ok) *timeouts = 1u;
 }
@@ -481,22 +557,21 @@ __device__ __forceinline__ void st_chunk2(uint16_t* row, uint64_t h0, uint64_t H
         if (h0 + i < H) st_stream2(row + h0 + i, uint16_t(v.w[i >> 1] >> (16 * (i & 1))));
 }
 
-template <int N, int DT>
+template <int N, int DT, class Coeffs>
 __global__ void __launch_bounds__(kLanes)
 post_bwd_element_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ x,
-                        const uint16_t* __restrict__ y, const float* __restrict__ post,
-                        const float* __restrict__ res, uint16_t* __restrict__ grad_x,
-                        uint16_t* __restrict__ grad_y, float* __restrict__ grad_post,
+                        const uint16_t* __restrict__ y, Coeffs coeffs, const float* __restrict__ res,
+                        uint16_t* __restrict__ grad_x, uint16_t* __restrict__ grad_y,
                         float* __restrict__ grad_res, uint64_t T, uint64_t H) {
     constexpr int M = N * N + N;
     __shared__ float red[kGroups][M];
-    __shared__ float coef[M];
+    __shared__ float coef[kPostTable<N>];
     pdl_enter();
     const uint32_t j = threadIdx.x;
     const uint64_t C = (H + 7) / 8;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
         PostCoeffs<N> cf;
-        cf.load(post, res, t, coef);
+        post_load_token<N>(coeffs, res, t, j, coef, cf, BlockSync());
         float acc[1][M];
 #pragma unroll
         for (int m = 0; m < M; ++m) acc[0][m] = 0.0f;
@@ -514,7 +589,7 @@ post_bwd_element_kernel(const uint16_t* __restrict__ g, const uint16_t* __restri
                 [&](int k, const Words<4>& o) { st_chunk2(grad_x + row0 + uint64_t(k) * H, 8 * c, H, o); },
                 [&](const Words<4>& o) { st_chunk2(grad_y + t * H, 8 * c, H, o); });
         }
-        post_fold_and_store<N, 1>(acc, red, grad_post, grad_res, t);
+        post_fold_and_store<N, 1>(acc, red, coeffs, coef, grad_res, t);
     }
 }
 

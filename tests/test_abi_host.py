@@ -50,7 +50,7 @@ def test_only_the_c_abi_is_exported():
 
 
 def test_abi_version(lib):
-    assert lib.mhc_h_aggregate_abi_version() == 5
+    assert lib.mhc_h_aggregate_abi_version() == 6
 
 
 def test_status_strings(lib):
@@ -423,3 +423,34 @@ def test_post_invalid_arguments(lib):
     # byte count of an n = 8 x overflows int64
     assert binding.post_fwd_raw(*f, 1 << 31, 8, 1 << 29, bf16) == binding.MHC_ERR_INVALID_ARG
     assert lib.mhc_h_aggregate_last_cuda_error() == 0
+
+
+def test_post_sigmoid_invalid_arguments(lib):
+    bf16 = binding.MHC_DTYPE_BF16
+    x, y, mix, alpha, b, res, out = (A + i * GAP for i in range(7))
+    assert binding.post_sigmoid_fwd_raw(x, y, mix, alpha, b, res, out, 4, 3, 64, bf16) == binding.MHC_ERR_UNSUPPORTED
+    assert binding.post_sigmoid_fwd_raw(x, y, mix, alpha, b, res, out, 4, 4, 64, 5) == binding.MHC_ERR_INVALID_ARG
+    assert binding.post_sigmoid_fwd_raw(0, 0, 0, 0, 0, 0, 0, 0, 4, 64, bf16) == binding.MHC_OK
+    assert binding.post_sigmoid_fwd_raw(x, y, mix, 0, b, res, out, 4, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG
+    assert binding.post_sigmoid_fwd_raw(x, y, mix, alpha, b + 2, res, out, 4, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG
+    assert binding.post_sigmoid_fwd_raw(x, y, mix, out + 64, b, res, out, 4, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG
+    assert binding.post_sigmoid_fwd_raw(x, y, out + 16, alpha, b, res, out, 4, 4, 64, bf16) == binding.MHC_ERR_INVALID_ARG
+    names = ("g", "x", "y", "mix", "alpha", "b", "res", "gx", "gy", "gz", "gm", "gr")
+    base = {nm: A + i * GAP for i, nm in enumerate(names)}
+
+    def call(**kw):
+        a = dict(base, T=4, n=4, H=64, dt=bf16)
+        a.update(kw)
+        return binding.post_sigmoid_bwd_raw(*(a[nm] for nm in names), a["T"], a["n"], a["H"], a["dt"])
+
+    assert call(n=6) == binding.MHC_ERR_UNSUPPORTED
+    assert call(dt=3) == binding.MHC_ERR_INVALID_ARG
+    for nm in names:
+        assert call(**{nm: 0}) == binding.MHC_ERR_INVALID_ARG, nm
+    assert call(gm=base["gm"] + 2) == binding.MHC_ERR_INVALID_ARG
+    for out in ("gx", "gy", "gz", "gm", "gr"):
+        for other in names:
+            if other != out:
+                assert call(**{out: base[other]}) == binding.MHC_ERR_INVALID_ARG, (out, other)
+    assert call(alpha=base["gz"] + 4) == binding.MHC_ERR_INVALID_ARG
+    assert call(b=base["gm"]) == binding.MHC_ERR_INVALID_ARG

@@ -251,3 +251,140 @@ def test_post_calls_capture_in_a_graph():
     e = [binding.post(x, y, post, res)] + list(binding.post_backward(g, x, y, post, res))
     for a, b in zip((out, gx, gy, gp, gr), e):
         assert sha(a) == sha(b)
+
+
+# --------------------------------------------------------------------------
+# post = sigmoid(alpha * mix + b) computed in the kernels
+# --------------------------------------------------------------------------
+
+from invariant_mhc_aggregate_gb300.autograd import mhc_post_sigmoid  # noqa: E402
+from invariant_mhc_aggregate_gb300.inputs import coeff_inputs  # noqa: E402
+
+
+def _scalar_buf(v: torch.Tensor) -> DevBuf:
+    return DevBuf.of(v.reshape(-1).to(torch.float32))
+
+
+def _np_ab(alpha, b):
+    return np.float32(alpha.reshape(-1)[0].item()), f32(b)
+
+
+def run_post_sigmoid_fwd(x, y, mix, alpha, b, res, offsets=(0, 0, 0)):
+    """offsets: x, y, out."""
+    T, n, H = x.shape
+    bx, by, bo = DevBuf.of(x, offsets[0]), DevBuf.of(y, offsets[1]), DevBuf(T * n * H * 2, offsets[2])
+    bm, ba, bb, br = DevBuf.of(mix), _scalar_buf(alpha), _scalar_buf(b), DevBuf.of(res)
+    st = binding.post_sigmoid_fwd_raw(bx.ptr, by.ptr, bm.ptr, ba.ptr, bb.ptr, br.ptr, bo.ptr, T, n, H,
+                                      DTYPE_CODE[x.dtype], stream_handle())
+    assert st == binding.MHC_OK, st
+    torch.cuda.synchronize()
+    assert bo.guards_ok(), "forward wrote outside out"
+    return bo.get(np.uint16, (T, n, H))
+
+
+def run_post_sigmoid_bwd(g, x, y, mix, alpha, b, res, offsets=(0, 0, 0, 0, 0)):
+    """offsets: g, x, y, grad_x, grad_y."""
+    T, n, H = x.shape
+    bg, bx, by = DevBuf.of(g, offsets[0]), DevBuf.of(x, offsets[1]), DevBuf.of(y, offsets[2])
+    bm, ba, bb, br = DevBuf.of(mix), _scalar_buf(alpha), _scalar_buf(b), DevBuf.of(res)
+    outs = [DevBuf(T * n * H * 2, offsets[3]), DevBuf(T * H * 2, offsets[4]), DevBuf(T * n * 4),
+            DevBuf(T * n * 4), DevBuf(T * n * n * 4)]
+    st = binding.post_sigmoid_bwd_raw(bg.ptr, bx.ptr, by.ptr, bm.ptr, ba.ptr, bb.ptr, br.ptr,
+                                      *(o.ptr for o in outs), T, n, H, DTYPE_CODE[x.dtype], stream_handle())
+    assert st == binding.MHC_OK, st
+    torch.cuda.synchronize()
+    assert all(o.guards_ok() for o in outs), "backward wrote outside its outputs"
+    return (outs[0].get(np.uint16, (T, n, H)), outs[1].get(np.uint16, (T, H)), outs[2].get(np.float32, (T, n)),
+            outs[3].get(np.float32, (T, n)), outs[4].get(np.float32, (T, n, n)))
+
+
+SIG_CASES = [
+    (5, 4096, (0, 0, 0)),      # 16-byte path
+    (3, 7168, (0, 0, 0)),      # a forward block spans two tokens
+    (37, 64, (0, 0, 0)),       # 8 vectors a row: a forward block spans 33 tokens
+    (6, 8, (0, 0, 0)),         # one vector a row
+    (3, 4100, (0, 0, 0)),      # 2-byte path
+    (2, 1279, (0, 2, 6)),
+]
+
+
+@pytest.mark.parametrize("recipe", ("normal", "wide"))
+@pytest.mark.parametrize("dtype", DTYPES, ids=_ids)
+@pytest.mark.parametrize("n", NS)
+@pytest.mark.parametrize("T,H,offsets", SIG_CASES)
+def test_post_sigmoid_all_paths(T, H, offsets, n, dtype, recipe):
+    x, y, _, res, g = post_inputs(T, H, n, "normal", 1000 + T + H, dtype=dtype, with_grad=True)
+    mix, alpha, b = coeff_inputs(T, n, recipe, 1001 + T)
+    a_np, b_np = _np_ab(alpha, b)
+    name = DTYPE_NAME[dtype]
+    got = run_post_sigmoid_fwd(x, y, mix, alpha, b, res, offsets)
+    want = oracle.post_sigmoid_fwd(u16(x), u16(y), f32(mix), a_np, b_np, f32(res), name)
+    assert_bytes_equal(got, want, "out")
+    got = run_post_sigmoid_bwd(g, x, y, mix, alpha, b, res, (0,) + tuple(offsets[:2]) + (offsets[2], 0))
+    want = oracle.post_sigmoid_bwd(u16(g), u16(x), u16(y), f32(mix), a_np, b_np, f32(res), name)
+    for a, w, what in zip(got, want, ("grad_x", "grad_y", "grad_z", "grad_mix", "grad_res")):
+        assert_bytes_equal(a, w, what)
+
+
+def test_post_sigmoid_full_size_against_oracle():
+    T, H, n = 4096, 7168, 4
+    x, y, _, res, g = post_inputs(T, H, n, "normal", 6, with_grad=True)
+    mix, alpha, b = coeff_inputs(T, n, "normal", 7)
+    xd, yd, rd, gd, md, ad, bd = (t.cuda() for t in (x, y, res, g, mix, alpha, b))
+    out = binding.post_sigmoid(xd, yd, md, ad, bd, rd)
+    grads = binding.post_sigmoid_backward(gd, xd, yd, md, ad, bd, rd)
+    gb, ga = binding.sigmoid_param_grad(grads[2], md)
+    torch.cuda.synchronize()
+    a_np, b_np = _np_ab(alpha, b)
+    o = oracle.default()
+    assert_bytes_equal(u16(out), o.post_sigmoid_fwd(u16(x), u16(y), f32(mix), a_np, b_np, f32(res)), "out")
+    want = o.post_sigmoid_bwd(u16(g), u16(x), u16(y), f32(mix), a_np, b_np, f32(res))
+    for a, w, what in zip((u16(grads[0]), u16(grads[1]), f32(grads[2]), f32(grads[3]), f32(grads[4])), want,
+                          ("grad_x", "grad_y", "grad_z", "grad_mix", "grad_res")):
+        assert_bytes_equal(a, w, what)
+    wgb, wga = o.sigmoid_param_grad(want[2], f32(mix))
+    assert_bytes_equal(f32(gb), wgb, "grad_b")
+    assert f32(ga).view(np.uint32)[0] == np.float32(wga).view(np.uint32)
+
+
+@pytest.mark.parametrize("n", (1, 4, 8))
+def test_post_sigmoid_batch_split_invariance(n):
+    T, H = 64, 4096
+    x, y, _, res, g = post_inputs(T, H, n, "normal", 1100 + n, with_grad=True)
+    mix, alpha, b = coeff_inputs(T, n, "wide", 1101 + n)
+    xd, yd, rd, gd, md, ad, bd = (t.cuda() for t in (x, y, res, g, mix, alpha, b))
+    full = binding.post_sigmoid(xd, yd, md, ad, bd, rd)
+    fgrads = binding.post_sigmoid_backward(gd, xd, yd, md, ad, bd, rd)
+    for chunk in (1, 7, 64):
+        for t0 in range(0, T, chunk):
+            sl = slice(t0, min(T, t0 + chunk))
+            xs, ys, ms, rs, gs = (t[sl].contiguous() for t in (xd, yd, md, rd, gd))
+            assert sha(binding.post_sigmoid(xs, ys, ms, ad, bd, rs)) == sha(full[sl]), (chunk, t0)
+            for p, f in zip(binding.post_sigmoid_backward(gs, xs, ys, ms, ad, bd, rs), fgrads):
+                assert sha(p) == sha(f[sl]), (chunk, t0)
+
+
+def test_post_sigmoid_autograd_matches_oracle():
+    T, H, n = 2 * 11, 2048, 4
+    x, y, _, res, g = post_inputs(T, H, n, "normal", 1200, with_grad=True)
+    mix, alpha, b = coeff_inputs(T, n, "normal", 1201)
+    xd = x.cuda().reshape(2, 11, n, H).requires_grad_(True)
+    yd = y.cuda().reshape(2, 11, H).requires_grad_(True)
+    md = mix.cuda().reshape(2, 11, n).requires_grad_(True)
+    ad = alpha.reshape(()).cuda().requires_grad_(True)
+    bd = b.cuda().requires_grad_(True)
+    rd = res.cuda().reshape(2, 11, n, n).requires_grad_(True)
+    out = mhc_post_sigmoid(xd, yd, md, ad, bd, rd)
+    out.backward(g.cuda().reshape(2, 11, n, H))
+    a_np, b_np = _np_ab(alpha, b)
+    o = oracle.default()
+    assert_bytes_equal(u16(out.detach().reshape(T, n, H)),
+                       o.post_sigmoid_fwd(u16(x), u16(y), f32(mix), a_np, b_np, f32(res)), "out")
+    wgx, wgy, wgz, wgm, wgr = o.post_sigmoid_bwd(u16(g), u16(x), u16(y), f32(mix), a_np, b_np, f32(res))
+    wgb, wga = o.sigmoid_param_grad(wgz, f32(mix))
+    assert_bytes_equal(u16(xd.grad.reshape(T, n, H)), wgx, "x.grad")
+    assert_bytes_equal(u16(yd.grad.reshape(T, H)), wgy, "y.grad")
+    assert_bytes_equal(f32(md.grad.reshape(T, n)), wgm, "mix.grad")
+    assert_bytes_equal(f32(rd.grad.reshape(T, n, n)), wgr, "res.grad")
+    assert_bytes_equal(f32(bd.grad), wgb, "b.grad")
+    assert ad.grad.shape == () and f32(ad.grad).view(np.uint32) == np.float32(wga).view(np.uint32)
