@@ -69,6 +69,13 @@ struct PostCoeffs {
                                          Sync = Sync()) {
         ld_post_coeffs<N>(post, res, t, pk, rk);
     }
+    // ... or res alone (post set by the caller) ...
+    __device__ __forceinline__ void load_res(const float* res, uint64_t t) {
+#pragma unroll
+        for (int k = 0; k < N; ++k)
+#pragma unroll
+            for (int j = 0; j < N; ++j) rk[k][j] = __ldg(res + (uint64_t(N) * t + k) * N + j);
+    }
     // ... or from a token table in shared memory (post_fill_table)
     __device__ __forceinline__ void from_table(const float* tab) {
 #pragma unroll
@@ -129,11 +136,11 @@ __device__ __forceinline__ void post_load_token(const Coeffs& c, const float* __
 }
 
 // The gradient of post[t,k] (the lane sum w) through the coefficient source:
-// grad_post itself, or grad_z and grad_mix with the slope from the table.
+// grad_post itself, or grad_z and grad_mix with sigmoid'(z[t,k]) = slope[k].
 template <int N, class Coeffs>
-__device__ __forceinline__ void post_store_grad(const Coeffs& c, uint64_t t, int k, float w, const float* tab) {
+__device__ __forceinline__ void post_store_grad(const Coeffs& c, uint64_t t, int k, float w, const float* slope) {
     if constexpr (Coeffs::kBlockTable) {
-        c.template store_grad_slope<N>(t, k, w, tab[N * N + N + k]);
+        c.template store_grad_slope<N>(t, k, w, slope[k]);
     } else {
         c.template store_grad<N>(t, k, w);
     }
@@ -168,9 +175,9 @@ constexpr int kPostBlock = 256;
 // the n x vectors and the y vector of its U positions, then writes their n
 // output vectors.
 //
-// With post computed from the mix (Coeffs::kBlockTable) the block's first
-// threads evaluate the sigmoids of the tokens it touches into shared memory,
-// before any bulk load, and one barrier publishes them.
+// With post computed from the mix (Coeffs::kBlockTable) the sigmoids are
+// evaluated once the thread's own loads are issued: per warp for rows of 32
+// vectors or more, else into a block table published by one barrier.
 template <int N, int DT, int NW, int U, int MIN_BLOCKS, class Coeffs>
 __global__ void __launch_bounds__(kPostBlock, MIN_BLOCKS)
 post_fwd_vec_kernel(const Words<NW>* __restrict__ x, const Words<NW>* __restrict__ y, Coeffs coeffs,
@@ -179,16 +186,6 @@ post_fwd_vec_kernel(const Words<NW>* __restrict__ x, const Words<NW>* __restrict
     __shared__ float table[Coeffs::kBlockTable ? (kPostBlock * U + 1) * N : 1];
     pdl_enter();
     const uint32_t i0 = blockIdx.x * (kPostBlock * U) + threadIdx.x;
-    uint32_t t_first = 0;
-    if constexpr (Coeffs::kBlockTable) {
-        const uint32_t first = blockIdx.x * (kPostBlock * U);
-        const uint32_t last = (n_vec - first > uint32_t(kPostBlock * U)) ? first + kPostBlock * U - 1 : n_vec - 1;
-        t_first = fastdiv_u32(first, divV);
-        const uint32_t count = (fastdiv_u32(last, divV) - t_first + 1) * N;
-        for (uint32_t q = threadIdx.x; q < count; q += kPostBlock)
-            table[q] = coeffs.pre_from(coeffs.mix_at(uint64_t(N) * t_first + q), int(q % N));
-        __syncthreads();
-    }
     Words<NW> xv[U][N], yv[U];
     uint32_t tok[U];
     uint64_t row0[U];   // x / out vector of stream 0
@@ -203,6 +200,39 @@ post_fwd_vec_kernel(const Words<NW>* __restrict__ x, const Words<NW>* __restrict
             yv[u] = ld_stream<NW>(y + i);
         }
     }
+    // post from the mix, evaluated while the loads above are in flight: for
+    // rows of 32 vectors or more (one vector per thread) a warp spans at most
+    // two tokens, whose 2n sigmoids its first lanes evaluate and shuffles
+    // hand out, with no barrier; else the block's table and one barrier.
+    const bool warp_coeffs = (U == 1) && V >= 32;
+    uint32_t t_first = 0;
+    float pkw[N];
+    if constexpr (Coeffs::kBlockTable) {
+        if (warp_coeffs) {
+            const uint32_t lane = threadIdx.x & 31u;
+            const uint32_t wbase = blockIdx.x * kPostBlock + (threadIdx.x & ~31u);
+            uint32_t wt = 0;
+            float mine = 0.0f;
+            if (wbase < n_vec) {
+                wt = fastdiv_u32(wbase, divV);
+                const uint32_t tt = wt + lane / N;
+                if (lane < uint32_t(2 * N) && uint64_t(tt) * V < n_vec)
+                    mine = coeffs.pre_from(coeffs.mix_at(uint64_t(N) * tt + lane % N), int(lane % N));
+            }
+            const uint32_t sel = (i0 < n_vec) ? tok[0] - wt : 0u;
+#pragma unroll
+            for (int k = 0; k < N; ++k) pkw[k] = __shfl_sync(0xffffffffu, mine, int(sel) * N + k);
+        } else {
+            const uint32_t first = blockIdx.x * (kPostBlock * U);
+            const uint32_t last =
+                (n_vec - first > uint32_t(kPostBlock * U)) ? first + kPostBlock * U - 1 : n_vec - 1;
+            t_first = fastdiv_u32(first, divV);
+            const uint32_t count = (fastdiv_u32(last, divV) - t_first + 1) * N;
+            for (uint32_t q = threadIdx.x; q < count; q += kPostBlock)
+                table[q] = coeffs.pre_from(coeffs.mix_at(uint64_t(N) * t_first + q), int(q % N));
+            __syncthreads();
+        }
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const uint32_t i = i0 + uint32_t(u) * kPostBlock;
@@ -212,7 +242,7 @@ post_fwd_vec_kernel(const Words<NW>* __restrict__ x, const Words<NW>* __restrict
                 float rk[N];
                 ld_res_row<N>(res, tok[u], k, rk);
                 float pk;
-                if constexpr (Coeffs::kBlockTable) pk = table[(tok[u] - t_first) * N + k];
+                if constexpr (Coeffs::kBlockTable) pk = warp_coeffs ? pkw[k] : table[(tok[u] - t_first) * N + k];
                 else pk = __ldg(coeffs.pre + uint64_t(N) * tok[u] + k);
                 Words<NW> o;
 #pragma unroll
@@ -280,11 +310,11 @@ post_fwd_element_kernel(const uint16_t* __restrict__ x, const uint16_t* __restri
 // per thread: lanes LPT*thread + l): xor shuffles over each group of 32 lanes,
 // the 8 group values through shared memory; grad_res[t,k,j] = value k*n + j,
 // and value n*n + k, the gradient of post[t,k], goes to the coefficient
-// source (post_store_grad; `tab` is the token table when there is one).  All
-// threads of the block call it.
+// source (post_store_grad; `slope` holds the token's sigmoid' when post comes
+// from the mix).  All threads of the block call it.
 template <int N, int LPT, class Coeffs, class Sync = BlockSync>
 __device__ __forceinline__ void post_fold_and_store(float (&acc)[LPT][N * N + N], float (*red)[N * N + N],
-                                                    const Coeffs& coeffs, const float* tab,
+                                                    const Coeffs& coeffs, const float* slope,
                                                     float* __restrict__ grad_res, uint64_t t,
                                                     Sync sync = Sync()) {
     constexpr int M = N * N + N;
@@ -315,7 +345,7 @@ __device__ __forceinline__ void post_fold_and_store(float (&acc)[LPT][N * N + N]
             for (int i = 0; i < s; ++i) w[i] = __fadd_rn(w[i], w[i + s]);
         }
         if (m < N * N) grad_res[uint64_t(N) * N * t + m] = w[0];
-        else post_store_grad<N>(coeffs, t, m - N * N, w[0], tab);
+        else post_store_grad<N>(coeffs, t, m - N * N, w[0], slope);
     }
     sync();   // red[] (and the coefficient table) are reused by the next token
 }
@@ -419,7 +449,7 @@ post_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict
                 }
             }
         }
-        post_fold_and_store<N, LPT>(acc, red, coeffs, coef, grad_res, t);
+        post_fold_and_store<N, LPT>(acc, red, coeffs, coef + N * N + N, grad_res, t);
     }
 }
 
@@ -447,6 +477,15 @@ __host__ __device__ constexpr uint32_t post_bulk_stage_bytes(int n) {
     return uint32_t(2 * n + 1) * kLanes * 16u;
 }
 
+//
+// With post computed from the mix (Coeffs::kBlockTable), lanes 1 .. n of the
+// producer warp evaluate the next token's sigmoids and slopes into a ring of
+// STAGES + 2 token slots while lane 0 goes on issuing the current token's
+// copies; a warp barrier before the next token's first copies orders them
+// before lane 0's arrival, so the consumers find them published by that
+// segment's barrier and never wait on a sigmoid.  The slot of token i is
+// rewritten for token i + STAGES + 2, after lane 0 has seen a segment of
+// token i + 1 released, that is after the consumers' fold of token i.
 template <int N, int DT, int STAGES, int MIN_BLOCKS, class Coeffs>
 __global__ void __launch_bounds__(kBulkThreads, MIN_BLOCKS)
 post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict__ x,
@@ -454,13 +493,16 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
                      Words<4>* __restrict__ grad_x, Words<4>* __restrict__ grad_y,
                      float* __restrict__ grad_res, uint64_t T, uint32_t V,
                      unsigned int* __restrict__ timeouts) {
+    static_assert(N <= 4, "the bulk-copy kernel keeps its coefficients in registers");
+    constexpr bool kSig = Coeffs::kBlockTable;
     constexpr int R = 2 * N + 1;   // staged rows: g (N), x (N), y
     constexpr int M = N * N + N;
+    constexpr int kSlots = STAGES + 2;
     extern __shared__ __align__(128) unsigned char stage_mem[];   // STAGES * R * 4 KB
     __shared__ __align__(8) uint64_t full[STAGES];
     __shared__ __align__(8) uint64_t empty[STAGES];
     __shared__ float red[kGroups][M];
-    __shared__ float coef[kPostTable<N>];
+    __shared__ float slots[kSig ? kSlots : 1][2 * N];   // post, then sigmoid'
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
@@ -474,27 +516,49 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
     const uint32_t nseg = (V + kLanes - 1) / kLanes;
 
     if (threadIdx.x >= kLanes) {
-        // producer warp: one thread issues the copies
-        if (threadIdx.x != kLanes) return;
+        // producer warp: lane 0 issues the copies (lanes 1 .. n: the sigmoids)
+        const uint32_t lane = threadIdx.x - kLanes;
+        if (!kSig && lane != 0) return;
         bool ok = true;
-        uint32_t item = 0;
-        for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        uint32_t item = 0, tok = 0;
+        // token tok's sigmoids and slopes into its slot (lanes 1 .. n)
+        const auto sigmoids = [&](uint64_t t, uint32_t tok) {
+            if constexpr (kSig) {
+                if (t < T && lane >= 1 && lane <= uint32_t(N)) {
+                    const int k = int(lane) - 1;
+                    float* slot = slots[tok % kSlots];
+                    coeffs.pre_and_slope(coeffs.mix_at(uint64_t(N) * t + k), k, slot[k], slot[N + k]);
+                }
+            }
+        };
+        if constexpr (kSig) sigmoids(blockIdx.x, 0);
+        for (uint64_t t = blockIdx.x; t < T; t += gridDim.x, ++tok) {
             for (uint32_t s = 0; s < nseg; ++s, ++item) {
                 const uint32_t st = item % STAGES, round = item / STAGES;
-                if (round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1u);
-                const uint32_t c0 = s * kLanes;
-                const uint32_t bytes = (V - c0 < uint32_t(kLanes) ? V - c0 : uint32_t(kLanes)) * 16u;
-                unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N);
-                mbar_arrive_expect_tx(&full[st], bytes * R);
+                if (lane == 0 && round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1u);
+                // token tok's slot is written, and (lane 0's wait) the readers of
+                // the slot the next token takes are done, before the first copies
+                if (kSig && s == 0) __syncwarp();
+                if (lane == 0) {
+                    const uint32_t c0 = s * kLanes;
+                    const uint32_t bytes = (V - c0 < uint32_t(kLanes) ? V - c0 : uint32_t(kLanes)) * 16u;
+                    unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N);
+                    mbar_arrive_expect_tx(&full[st], bytes * R);
 #pragma unroll
-                for (int k = 0; k < N; ++k) {
-                    bulk_copy_g2s(dst + size_t(k) * kLanes * 16, g + (uint64_t(N) * t + k) * V + c0, bytes, &full[st]);
-                    bulk_copy_g2s(dst + size_t(N + k) * kLanes * 16, x + (uint64_t(N) * t + k) * V + c0, bytes,
-                                  &full[st]);
+                    for (int k = 0; k < N; ++k) {
+                        bulk_copy_g2s(dst + size_t(k) * kLanes * 16, g + (uint64_t(N) * t + k) * V + c0, bytes,
+                                      &full[st]);
+                        bulk_copy_g2s(dst + size_t(N + k) * kLanes * 16, x + (uint64_t(N) * t + k) * V + c0,
+                                      bytes, &full[st]);
+                    }
+                    bulk_copy_g2s(dst + size_t(2 * N) * kLanes * 16, y + t * V + c0, bytes, &full[st]);
                 }
-                bulk_copy_g2s(dst + size_t(2 * N) * kLanes * 16, y + t * V + c0, bytes, &full[st]);
+                if constexpr (kSig) {
+                    if (s == 0) sigmoids(t + gridDim.x, tok + 1);
+                }
             }
         }
+        if (lane != 0) return;
         // every copy issued has landed before the block's shared memory goes
         for (uint32_t i = item > uint32_t(STAGES) ? item - STAGES : 0; i < item; ++i)
             if (!mbar_wait(&full[i % STAGES], (i / STAGES) & 1u)) ok = false;
@@ -506,10 +570,11 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
     const uint32_t j = threadIdx.x;
     const auto sync = [] { named_sync(1, kLanes); };
     bool ok = true;
-    uint32_t item = 0;
-    for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    uint32_t item = 0, tok = 0;
+    for (uint64_t t = blockIdx.x; t < T; t += gridDim.x, ++tok) {
         PostCoeffs<N> cf;
-        post_load_token<N>(coeffs, res, t, j, coef, cf, sync);
+        if constexpr (kSig) cf.load_res(res, t);
+        else cf.load(coeffs.pre, res, t, nullptr, sync);
         float acc[1][M];
 #pragma unroll
         for (int m = 0; m < M; ++m) acc[0][m] = 0.0f;
@@ -517,6 +582,12 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
         for (uint32_t s = 0; s < nseg; ++s, ++item) {
             const uint32_t st = item % STAGES;
             if (ok) ok = mbar_wait(&full[st], (item / STAGES) & 1u);
+            if constexpr (kSig) {
+                if (s == 0) {
+#pragma unroll
+                    for (int k = 0; k < N; ++k) cf.pk[k] = slots[tok % kSlots][k];
+                }
+            }
             const uint32_t c = s * kLanes + j;
             if (c < V) {
                 const Words<4>* sm =
@@ -536,7 +607,7 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
             __syncwarp();
             if ((j & 31u) == 0) mbar_arrive(&empty[st]);
         }
-        post_fold_and_store<N, 1>(acc, red, coeffs, coef, grad_res, t, sync);
+        post_fold_and_store<N, 1>(acc, red, coeffs, slots[kSig ? tok % kSlots : 0] + N, grad_res, t, sync);
     }
     if (!ok) *timeouts = 1u;
 }
@@ -589,7 +660,7 @@ post_bwd_element_kernel(const uint16_t* __restrict__ g, const uint16_t* __restri
                 [&](int k, const Words<4>& o) { st_chunk2(grad_x + row0 + uint64_t(k) * H, 8 * c, H, o); },
                 [&](const Words<4>& o) { st_chunk2(grad_y + t * H, 8 * c, H, o); });
         }
-        post_fold_and_store<N, 1>(acc, red, coeffs, coef, grad_res, t);
+        post_fold_and_store<N, 1>(acc, red, coeffs, coef + N * N + N, grad_res, t);
     }
 }
 

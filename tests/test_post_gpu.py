@@ -301,6 +301,8 @@ def run_post_sigmoid_bwd(g, x, y, mix, alpha, b, res, offsets=(0, 0, 0, 0, 0)):
 SIG_CASES = [
     (5, 4096, (0, 0, 0)),      # 16-byte path
     (3, 7168, (0, 0, 0)),      # a forward block spans two tokens
+    (9, 320, (0, 0, 0)),       # 40 vectors a row: forward warps straddle tokens, ragged last warp
+    (4, 4104, (0, 0, 0)),      # 513 vectors a row
     (37, 64, (0, 0, 0)),       # 8 vectors a row: a forward block spans 33 tokens
     (6, 8, (0, 0, 0)),         # one vector a row
     (3, 4100, (0, 0, 0)),      # 2-byte path
