@@ -11,6 +11,9 @@ Families (one step = forward then backward):
             mhc_sigmoid_param_grad (pre computed from the mix)
   post      mhc_post_fwd / mhc_post_bwd (the layer output expanded onto the
             n streams)
+  post_sigmoid
+            mhc_post_sigmoid_fwd / mhc_post_sigmoid_bwd, then
+            mhc_sigmoid_param_grad (post computed from the mix)
 
 The buffers are PyTorch allocations (512-byte aligned), so the path follows
 from H: H % 16 == 0 the 32-byte path, H % 8 == 0 the 16-byte path, even H
@@ -67,18 +70,29 @@ def _post(args, dev, dtype) -> None:
              binding.PATH_NAMES[binding.post_bwd_path_raw(*(t.data_ptr() for t in (g, x, y, post, res, gx,
                                                                                   gy, gp, gr)), T, n, H)])
 
-    def step():
-        binding.mhc_post_fwd(x, y, post, res, out)
-        binding.mhc_post_bwd(g, x, y, post, res, gx, gy, gp, gr)
+    if args.family == "post":
+        def step():
+            binding.mhc_post_fwd(x, y, post, res, out)
+            binding.mhc_post_bwd(g, x, y, post, res, gx, gy, gp, gr)
+    else:
+        mix, alpha, b = (t.to(dev) for t in coeff_inputs(T, n, "normal", 7))
+        gm = torch.empty_like(mix)
+        gb = torch.empty((n,), dtype=torch.float32, device=dev)
+        ga = torch.empty((1,), dtype=torch.float32, device=dev)
+
+        def step():
+            binding.mhc_post_sigmoid_fwd(x, y, mix, alpha, b, res, out)
+            binding.mhc_post_sigmoid_bwd(g, x, y, mix, alpha, b, res, gx, gy, gp, gm, gr)
+            binding.mhc_sigmoid_param_grad(gp, mix, gb, ga)
 
     us = _time(step, args.steps)
-    print(f"post T={T} H={H} n={n} {args.dtype} offset={args.offset} paths fwd/bwd={paths[0]}/"
+    print(f"{args.family} T={T} H={H} n={n} {args.dtype} offset={args.offset} paths fwd/bwd={paths[0]}/"
           f"{paths[1]}: {us:.1f} us per step")
 
 
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--family", choices=("plain", "sigmoid", "post"), default="plain")
+    ap.add_argument("--family", choices=("plain", "sigmoid", "post", "post_sigmoid"), default="plain")
     ap.add_argument("--T", type=int, default=4096)
     ap.add_argument("--H", type=int, default=7168)
     ap.add_argument("--n", type=int, default=4)
@@ -92,7 +106,7 @@ def main(argv=None) -> None:
     dev = torch.device("cuda", 0)
     dtype = torch.bfloat16 if args.dtype == "bf16" else torch.float16
     T, H, n = args.T, args.H, args.n
-    if args.family == "post":
+    if args.family in ("post", "post_sigmoid"):
         _post(args, dev, dtype)
         return
     g, res, pre = backward_inputs(T, H, "normal", 4, device=dev, n=n, dtype=dtype)
