@@ -20,15 +20,22 @@
 // Layout: x, g, out, grad_x [T,n,H]; y, grad_y [T,H]; post, grad_post [T,n];
 // res, grad_res [T,n,n] (row k: output stream k, column j: input stream j).
 //
-// Kernels (HBM-bound: the forward moves (4n + 2) H bytes a token, the
-// backward (6n + 4) H):
-//  * forward, vector path: a flat grid over the [T,H] plane in 16- or
-//    32-byte vectors; a thread loads the n x vectors and the y vector of its
-//    position and writes the n output vectors.
-//  * backward, vector path (16-byte): one 256-thread block per token, thread
-//    j = ORDER-256 lane j taking chunks j, j + 256, ...; it writes grad_x and
-//    grad_y for its chunk and adds the chunk partials of the n*n + n sums,
-//    which fold like grad_pre's.
+// The post coefficients come from a coefficient source (mhc_coeffs.cuh):
+// PlainCoeffs reads post and writes grad_post; SigmoidCoeffs computes
+// post = sigmoid(alpha * mix + b) in the kernel and writes grad_z and
+// grad_mix in place of grad_post.
+//
+// Kernels (HBM-bound at n <= 4: the forward moves (4n + 2) H bytes a token,
+// the backward (6n + 4) H):
+//  * forward, 16-byte path: a flat grid over the [T,H] plane, one vector per
+//    thread; a thread loads the n x vectors and the y vector of its position
+//    and writes the n output vectors.
+//  * backward, 16-byte path, n <= 4: the bulk-copy kernel below (rows
+//    streamed through a shared-memory ring, one producer warp, 256 consumer
+//    lanes); n = 8: one 256-thread block per token, thread j = ORDER-256 lane
+//    j taking chunks j, j + 256, ... from global memory.  Either way lane j
+//    writes grad_x and grad_y for its chunks and adds their partials to the
+//    n*n + n sums, which fold like grad_pre's.
 //  * other shapes and alignments: the same arithmetic with 2-byte accesses.
 #pragma once
 

@@ -454,3 +454,17 @@ def test_post_sigmoid_invalid_arguments(lib):
                 assert call(**{out: base[other]}) == binding.MHC_ERR_INVALID_ARG, (out, other)
     assert call(alpha=base["gz"] + 4) == binding.MHC_ERR_INVALID_ARG
     assert call(b=base["gm"]) == binding.MHC_ERR_INVALID_ARG
+
+
+def test_post_vector_index_limit(lib):
+    """Rows of 2^31 16-byte vectors or more are rejected on the vector path
+    (the kernels index vectors of a row in 32 bits); buffers spaced 2^36 apart
+    so that they stay disjoint."""
+    big = 1 << 36
+    bf16 = binding.MHC_DTYPE_BF16
+    H = 1 << 34                       # H / 8 = 2^31 vectors
+    f = [A + i * big for i in range(5)]
+    assert binding.post_fwd_path_raw(*f, 1, 1, H) == binding.MHC_PATH_VEC16
+    assert binding.post_fwd_raw(*f, 1, 1, H, bf16) == binding.MHC_ERR_UNSUPPORTED
+    b = [A + i * big for i in range(9)]
+    assert binding.post_bwd_raw(*b, 1, 1, H, bf16) == binding.MHC_ERR_UNSUPPORTED
