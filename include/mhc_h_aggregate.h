@@ -55,8 +55,11 @@
  * Pointers and ownership.  Every data pointer is a DEVICE pointer (or managed
  * memory) allocated and owned by the caller.  The library allocates nothing,
  * keeps no state between calls except a per-thread copy of the last CUDA
- * error code, and never synchronises: each call enqueues kernels on `stream`
- * (NULL = the legacy default stream) and returns.  Calls are safe from several
+ * error code, the per-device record of bounded waits that ran out
+ * (mhc_h_aggregate_wait_timeouts) and caches of the device addresses and
+ * kernel attributes it needs, and its compute calls never synchronise: each
+ * enqueues kernels on `stream` (NULL = the legacy default stream) and
+ * returns.  Calls are safe from several
  * host threads at once.  Kernels are launched with programmatic stream
  * serialization: they may become resident while the previous kernel in the
  * stream finishes, but touch no memory until it has completed, so stream order
