@@ -90,7 +90,7 @@ cudaError_t bwd_bulk(const PostBwdCall& c, const Coeffs& k) {
     unsigned int* flag = nullptr;
     if ((e = wait_flag_ptr(&flag)) != cudaSuccess) return e;
     const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * MIN_BLOCKS);
-    return launch_smem(kernel, blocks, kBulkThreads, smem, c.stream, static_cast<const Words<4>*>(c.g),
+    return launch_smem(kernel, blocks, post_bulk_threads<Coeffs>(), smem, c.stream, static_cast<const Words<4>*>(c.g),
                        static_cast<const Words<4>*>(c.x), static_cast<const Words<4>*>(c.y), k, c.res,
                        static_cast<Words<4>*>(c.grad_x), static_cast<Words<4>*>(c.grad_y), c.grad_res, c.T,
                        uint32_t(c.H / 8), flag);

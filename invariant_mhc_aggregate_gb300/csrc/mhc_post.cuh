@@ -478,23 +478,28 @@ post_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict
 // stops waiting, the block still runs to its end
 // on whatever the stage holds, and the producer waits (bounded) for the
 // copies it issued before it exits.
-constexpr int kBulkThreads = kLanes + 32;
-
 __host__ __device__ constexpr uint32_t post_bulk_stage_bytes(int n) {
     return uint32_t(2 * n + 1) * kLanes * 16u;
 }
 
 //
-// With post computed from the mix (Coeffs::kBlockTable), lanes 1 .. n of the
-// producer warp evaluate the next token's sigmoids and slopes into a ring of
-// STAGES + 2 token slots while lane 0 goes on issuing the current token's
-// copies; a warp barrier before the next token's first copies orders them
-// before lane 0's arrival, so the consumers find them published by that
-// segment's barrier and never wait on a sigmoid.  The slot of token i is
-// rewritten for token i + STAGES + 2, after lane 0 has seen a segment of
-// token i + 1 released, that is after the consumers' fold of token i.
+// With post computed from the mix (Coeffs::kBlockTable) a helper warp
+// evaluates each token's sigmoids and slopes (lanes 0 .. n-1) into a ring of
+// kPostSlots token slots, ahead of the consumers: slot i % kPostSlots is
+// published by its "ready" barrier (the consumers wait on it before a
+// token's first chunk) and handed back by its "free" barrier (consumer
+// thread 0, after the token's fold), which the helper waits on before
+// writing it again.  Neither the producer nor the consumers evaluate a
+// sigmoid.
+constexpr int kPostSlots = 3;
+
+template <class Coeffs>
+__host__ __device__ constexpr int post_bulk_threads() {
+    return kLanes + 32 + (Coeffs::kBlockTable ? 32 : 0);
+}
+
 template <int N, int DT, int STAGES, int MIN_BLOCKS, class Coeffs>
-__global__ void __launch_bounds__(kBulkThreads, MIN_BLOCKS)
+__global__ void __launch_bounds__(post_bulk_threads<Coeffs>(), MIN_BLOCKS)
 post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict__ x,
                      const Words<4>* __restrict__ y, Coeffs coeffs, const float* __restrict__ res,
                      Words<4>* __restrict__ grad_x, Words<4>* __restrict__ grad_y,
@@ -504,17 +509,24 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
     constexpr bool kSig = Coeffs::kBlockTable;
     constexpr int R = 2 * N + 1;   // staged rows: g (N), x (N), y
     constexpr int M = N * N + N;
-    constexpr int kSlots = STAGES + 2;
+    constexpr int kNS = kSig ? kPostSlots : 1;
     extern __shared__ __align__(128) unsigned char stage_mem[];   // STAGES * R * 4 KB
     __shared__ __align__(8) uint64_t full[STAGES];
     __shared__ __align__(8) uint64_t empty[STAGES];
+    __shared__ __align__(8) uint64_t ready[kNS];
+    __shared__ __align__(8) uint64_t freed[kNS];
     __shared__ float red[kGroups][M];
-    __shared__ float slots[kSig ? kSlots : 1][2 * N];   // post, then sigmoid'
+    __shared__ float slots[kNS][2 * N];   // post, then sigmoid'
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kGroups);
+        }
+#pragma unroll
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(&ready[s], 1);
+            mbar_init(&freed[s], 1);
         }
         mbar_init_fence();
     }
@@ -522,50 +534,50 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
     pdl_enter();
     const uint32_t nseg = (V + kLanes - 1) / kLanes;
 
-    if (threadIdx.x >= kLanes) {
-        // producer warp: lane 0 issues the copies (lanes 1 .. n: the sigmoids)
-        const uint32_t lane = threadIdx.x - kLanes;
-        if (!kSig && lane != 0) return;
-        bool ok = true;
-        uint32_t item = 0, tok = 0;
-        // token tok's sigmoids and slopes into its slot (lanes 1 .. n)
-        const auto sigmoids = [&](uint64_t t, uint32_t tok) {
-            if constexpr (kSig) {
-                if (t < T && lane >= 1 && lane <= uint32_t(N)) {
-                    const int k = int(lane) - 1;
-                    float* slot = slots[tok % kSlots];
-                    coeffs.pre_and_slope(coeffs.mix_at(uint64_t(N) * t + k), k, slot[k], slot[N + k]);
+    if (threadIdx.x >= kLanes + 32) {
+        // helper warp (post from the mix): the block's tokens' sigmoids, in order
+        if constexpr (kSig) {
+            const uint32_t lane = threadIdx.x - (kLanes + 32);
+            bool ok = true;
+            uint32_t tok = 0;
+            for (uint64_t t = blockIdx.x; t < T; t += gridDim.x, ++tok) {
+                const uint32_t sl = tok % kNS;
+                if (tok >= uint32_t(kNS) && lane == 0 && ok) ok = mbar_wait(&freed[sl], (tok / kNS - 1) & 1u);
+                __syncwarp();
+                if (lane < uint32_t(N)) {
+                    coeffs.pre_and_slope(coeffs.mix_at(uint64_t(N) * t + lane), int(lane), slots[sl][lane],
+                                         slots[sl][N + lane]);
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ready[sl]);
             }
-        };
-        if constexpr (kSig) sigmoids(blockIdx.x, 0);
-        for (uint64_t t = blockIdx.x; t < T; t += gridDim.x, ++tok) {
+            if (lane == 0 && !ok) *timeouts = 1u;
+        }
+        return;
+    }
+
+    if (threadIdx.x >= kLanes) {
+        // producer warp: one thread issues the copies
+        if (threadIdx.x != kLanes) return;
+        bool ok = true;
+        uint32_t item = 0;
+        for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
             for (uint32_t s = 0; s < nseg; ++s, ++item) {
                 const uint32_t st = item % STAGES, round = item / STAGES;
-                if (lane == 0 && round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1u);
-                // token tok's slot is written, and (lane 0's wait) the readers of
-                // the slot the next token takes are done, before the first copies
-                if (kSig && s == 0) __syncwarp();
-                if (lane == 0) {
-                    const uint32_t c0 = s * kLanes;
-                    const uint32_t bytes = (V - c0 < uint32_t(kLanes) ? V - c0 : uint32_t(kLanes)) * 16u;
-                    unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N);
-                    mbar_arrive_expect_tx(&full[st], bytes * R);
+                if (round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1u);
+                const uint32_t c0 = s * kLanes;
+                const uint32_t bytes = (V - c0 < uint32_t(kLanes) ? V - c0 : uint32_t(kLanes)) * 16u;
+                unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N);
+                mbar_arrive_expect_tx(&full[st], bytes * R);
 #pragma unroll
-                    for (int k = 0; k < N; ++k) {
-                        bulk_copy_g2s(dst + size_t(k) * kLanes * 16, g + (uint64_t(N) * t + k) * V + c0, bytes,
-                                      &full[st]);
-                        bulk_copy_g2s(dst + size_t(N + k) * kLanes * 16, x + (uint64_t(N) * t + k) * V + c0,
-                                      bytes, &full[st]);
-                    }
-                    bulk_copy_g2s(dst + size_t(2 * N) * kLanes * 16, y + t * V + c0, bytes, &full[st]);
+                for (int k = 0; k < N; ++k) {
+                    bulk_copy_g2s(dst + size_t(k) * kLanes * 16, g + (uint64_t(N) * t + k) * V + c0, bytes, &full[st]);
+                    bulk_copy_g2s(dst + size_t(N + k) * kLanes * 16, x + (uint64_t(N) * t + k) * V + c0, bytes,
+                                  &full[st]);
                 }
-                if constexpr (kSig) {
-                    if (s == 0) sigmoids(t + gridDim.x, tok + 1);
-                }
+                bulk_copy_g2s(dst + size_t(2 * N) * kLanes * 16, y + t * V + c0, bytes, &full[st]);
             }
         }
-        if (lane != 0) return;
         // every copy issued has landed before the block's shared memory goes
         for (uint32_t i = item > uint32_t(STAGES) ? item - STAGES : 0; i < item; ++i)
             if (!mbar_wait(&full[i % STAGES], (i / STAGES) & 1u)) ok = false;
@@ -579,9 +591,16 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
     bool ok = true;
     uint32_t item = 0, tok = 0;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x, ++tok) {
+        const uint32_t sl = tok % kNS;
         PostCoeffs<N> cf;
-        if constexpr (kSig) cf.load_res(res, t);
-        else cf.load(coeffs.pre, res, t, nullptr, sync);
+        if constexpr (kSig) {
+            cf.load_res(res, t);
+            if (ok) ok = mbar_wait(&ready[sl], (tok / kNS) & 1u);
+#pragma unroll
+            for (int k = 0; k < N; ++k) cf.pk[k] = slots[sl][k];
+        } else {
+            cf.load(coeffs.pre, res, t, nullptr, sync);
+        }
         float acc[1][M];
 #pragma unroll
         for (int m = 0; m < M; ++m) acc[0][m] = 0.0f;
@@ -589,12 +608,6 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
         for (uint32_t s = 0; s < nseg; ++s, ++item) {
             const uint32_t st = item % STAGES;
             if (ok) ok = mbar_wait(&full[st], (item / STAGES) & 1u);
-            if constexpr (kSig) {
-                if (s == 0) {
-#pragma unroll
-                    for (int k = 0; k < N; ++k) cf.pk[k] = slots[tok % kSlots][k];
-                }
-            }
             const uint32_t c = s * kLanes + j;
             if (c < V) {
                 const Words<4>* sm =
@@ -614,7 +627,9 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
             __syncwarp();
             if ((j & 31u) == 0) mbar_arrive(&empty[st]);
         }
-        post_fold_and_store<N, 1>(acc, red, coeffs, slots[kSig ? tok % kSlots : 0] + N, grad_res, t, sync);
+        post_fold_and_store<N, 1>(acc, red, coeffs, slots[sl] + N, grad_res, t, sync);
+        // the fold's closing barrier: every consumer is done with the slot
+        if (kSig && j == 0) mbar_arrive(&freed[sl]);
     }
     if (!ok) *timeouts = 1u;
 }
