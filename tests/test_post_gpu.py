@@ -390,3 +390,92 @@ def test_post_sigmoid_autograd_matches_oracle():
     assert_bytes_equal(f32(rd.grad.reshape(T, n, n)), wgr, "res.grad")
     assert_bytes_equal(f32(bd.grad), wgb, "b.grad")
     assert ad.grad.shape == () and f32(ad.grad).view(np.uint32) == np.float32(wga).view(np.uint32)
+
+
+# --------------------------------------------------------------------------
+# fuzzing and concurrency
+# --------------------------------------------------------------------------
+
+def test_post_fuzz_shapes_alignments_sources():
+    rng = np.random.default_rng(2027)
+    for case in range(40):
+        n = int(rng.choice([1, 2, 4, 8]))
+        dtype = torch.bfloat16 if rng.random() < 0.6 else torch.float16
+        H = int(rng.choice([int(rng.integers(1, 300)), 8 * int(rng.integers(1, 1100))]))
+        T = int(rng.integers(1, 24))
+        sig = bool(rng.random() < 0.4)
+        x, y, post, res, g = post_inputs(T, H, n, str(rng.choice(["normal", "ragged"])),
+                                         int(rng.integers(0, 10 ** 6)), dtype=dtype, with_grad=True)
+        name = DTYPE_NAME[dtype]
+        what = f"case {case}: n={n} {name} T={T} H={H} sigmoid={sig}"
+        if sig:
+            mix, alpha, b = coeff_inputs(T, n, str(rng.choice(["normal", "wide"])), int(rng.integers(0, 10 ** 6)))
+            a_np, b_np = _np_ab(alpha, b)
+            fo = tuple(int(rng.choice([0, 2, 8, 16])) for _ in range(3))
+            got = run_post_sigmoid_fwd(x, y, mix, alpha, b, res, fo)
+            assert_bytes_equal(got, oracle.post_sigmoid_fwd(u16(x), u16(y), f32(mix), a_np, b_np, f32(res), name),
+                               "out " + what)
+            bo = tuple(int(rng.choice([0, 2, 8, 16])) for _ in range(5))
+            got = run_post_sigmoid_bwd(g, x, y, mix, alpha, b, res, bo)
+            want = oracle.post_sigmoid_bwd(u16(g), u16(x), u16(y), f32(mix), a_np, b_np, f32(res), name)
+            names = ("grad_x", "grad_y", "grad_z", "grad_mix", "grad_res")
+        else:
+            fo = tuple(int(rng.choice([0, 2, 8, 16])) if i in (0, 1, 4) else int(rng.choice([0, 4, 8]))
+                       for i in range(5))
+            got = run_post_fwd(x, y, post, res, fo)
+            assert_bytes_equal(got, oracle.post_fwd(u16(x), u16(y), f32(post), f32(res), name), "out " + what)
+            bo = tuple(int(rng.choice([0, 2, 8, 16])) if i in (0, 1, 2, 5, 6) else int(rng.choice([0, 4, 8]))
+                       for i in range(9))
+            got = run_post_bwd(g, x, y, post, res, bo)
+            want = oracle.post_bwd(u16(g), u16(x), u16(y), f32(post), f32(res), name)
+            names = ("grad_x", "grad_y", "grad_post", "grad_res")
+        for a, w, nm in zip(got, want, names):
+            assert_bytes_equal(a, w, f"{nm} {what}")
+
+
+def test_post_concurrent_host_threads_on_separate_streams():
+    import threading
+    jobs = []
+    for i in range(6):
+        n = (4, 2, 8)[i % 3]
+        x, y, post, res, g = (t.cuda() for t in post_inputs(96, 4096, n, "normal", 300 + i, with_grad=True))
+        mix, alpha, b = (t.cuda() for t in coeff_inputs(96, n, "normal", 400 + i))
+        jobs.append((x, y, post, res, g, mix, alpha, b, i % 2 == 1))
+    torch.cuda.synchronize()
+
+    def run(job, stream=None):
+        x, y, post, res, g, mix, alpha, b, sig = job
+        if sig:
+            outs = [binding.post_sigmoid(x, y, mix, alpha, b, res, stream)]
+            outs += list(binding.post_sigmoid_backward(g, x, y, mix, alpha, b, res, stream))
+        else:
+            outs = [binding.post(x, y, post, res, stream)] + list(binding.post_backward(g, x, y, post, res, stream))
+        return outs
+
+    refs = []
+    for job in jobs:
+        outs = run(job)
+        torch.cuda.synchronize()
+        refs.append([sha(o) for o in outs])
+    results = [None] * len(jobs)
+    errors = []
+
+    def worker(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(10):
+                    outs = run(jobs[i], s)
+            s.synchronize()
+            results[i] = [sha(o) for o in outs]
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(jobs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    assert results == refs
+    assert binding.wait_timeouts() == 0
