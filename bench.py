@@ -649,7 +649,7 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
 
     # the mHC post (the layer output expanded back onto the n streams), steady state
     from invariant_mhc_aggregate_gb300.inputs import post_inputs
-    for n in (4, 8):
+    for n in (1, 2, 4, 8):
         T, H = 4096, 7168
         x, y, post, res, g = post_inputs(T, H, n, "normal", 6, device=dev, with_grad=True)
         fb = T * (2 * (2 * n + 1) * H + 4 * n + 4 * n * n)
