@@ -479,3 +479,47 @@ def test_post_concurrent_host_threads_on_separate_streams():
     assert not errors, errors
     assert results == refs
     assert binding.wait_timeouts() == 0
+
+
+def test_post_split_launch_beyond_2e31_vectors():
+    """The post forward indexes vectors with 32 bits and splits calls of 2^31
+    vectors or more into launches over consecutive token ranges.  With n = 1,
+    H = 16384 and the 16-byte path, T = 2^20 tokens make exactly 2^31 vectors:
+    the second launch holds the last token (34 GB each for x, y and out).
+    Checked for post given and for post computed from the mix."""
+    T, H, n = 1 << 20, 16384, 1
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev).manual_seed(321)
+    x = torch.empty((T, n, H), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    step = 1 << 28
+    for flat in (x.view(-1), y.view(-1)):
+        for i in range(0, flat.numel(), step):
+            m = min(step, flat.numel() - i)
+            flat[i:i + m] = torch.randn(m, generator=gen, device=dev).to(torch.bfloat16)
+    post = 2 * torch.rand((T, n), generator=gen, device=dev)
+    res = torch.rand((T, n, n), generator=gen, device=dev)
+    out = torch.empty_like(x)
+    assert binding.post_fwd_path_raw(x.data_ptr(), y.data_ptr(), post.data_ptr(), res.data_ptr(),
+                                     out.data_ptr(), T, n, H) == binding.MHC_PATH_VEC16
+    V = H // 8
+    boundary = (2 ** 31 - 1) // V          # first token of the second launch
+    samples = (0, 1, boundary - 1, boundary, T - 1)
+    binding.mhc_post_fwd(x, y, post, res, out)
+    torch.cuda.synchronize()
+    for t in samples:
+        sl = slice(t, t + 1)
+        want = oracle.post_fwd(u16(x[sl]), u16(y[sl]), f32(post[sl]), f32(res[sl]))
+        assert_bytes_equal(u16(out[sl]), want, f"token {t}")
+    mix = torch.randn((T, n), generator=gen, device=dev) * 3
+    alpha = torch.full((1,), 1.25, device=dev)
+    b = torch.full((1,), -0.5, device=dev)
+    binding.mhc_post_sigmoid_fwd(x, y, mix, alpha, b, res, out)
+    torch.cuda.synchronize()
+    for t in samples:
+        sl = slice(t, t + 1)
+        want = oracle.post_sigmoid_fwd(u16(x[sl]), u16(y[sl]), f32(mix[sl]), np.float32(1.25),
+                                       np.float32([-0.5]), f32(res[sl]))
+        assert_bytes_equal(u16(out[sl]), want, f"sigmoid post, token {t}")
+    del x, y, out, post, res, mix
+    torch.cuda.empty_cache()
