@@ -423,10 +423,14 @@ __device__ __forceinline__ float chunk_partial(const Words<NW>& g, const Words<N
 // two lanes.  The 8 group values then fold with strides 4, 2, 1 in shared
 // memory, and grad_pre[t, 0..N-1] goes to the coefficient source (which
 // stores it, or the gradients derived from it).  All threads of the block call it.
+//
+// A block of fewer than 256/LPT threads (`groups` groups of 32 lanes) stands
+// for the full 256 lanes whose higher lanes hold +0: their group values are
+// +0 in the cross-group fold.
 template <int N, int LPT, class Coeffs>
 __device__ __forceinline__ void fold_lanes_and_store(float (&acc)[LPT][N], float (*red)[N],
                                                      const Coeffs& coeffs, uint64_t t,
-                                                     const float* slope) {
+                                                     const float* slope, int groups = kGroups) {
     constexpr int kThreadsPerGroup = 32 / LPT;
 #pragma unroll
     for (int k = 0; k < N; ++k) {
@@ -447,7 +451,7 @@ __device__ __forceinline__ void fold_lanes_and_store(float (&acc)[LPT][N], float
         const int k = threadIdx.x;
         float w[kGroups];
 #pragma unroll
-        for (int i = 0; i < kGroups; ++i) w[i] = red[i][k];
+        for (int i = 0; i < kGroups; ++i) w[i] = (i < groups) ? red[i][k] : 0.0f;
 #pragma unroll
         for (int s = kGroups / 2; s >= 1; s >>= 1) {
 #pragma unroll

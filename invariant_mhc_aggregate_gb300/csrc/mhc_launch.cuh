@@ -292,8 +292,14 @@ cudaError_t bwd_n(const BwdCall& c, const Coeffs& k) {
         case kPathVec32: return bwd_vec32<N, DT>(c, k);
         case kPathVec16: return bwd_vec16<N, DT>(c, k);
         case kPathShift16: {
+            // rows of fewer than 256 chunks: only the warps that hold chunks
+            // (and at least 16n threads for the row-end values)
+            const uint64_t chunks = (c.H + 7) / 8;
+            uint32_t threads = uint32_t(chunks < uint64_t(kLanes) ? (chunks + 31) / 32 * 32 : kLanes);
+            if (threads < uint32_t(16 * N)) threads = uint32_t(16 * N);
+            if (threads < 32u) threads = 32u;
             const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
-            return launch(agg_bwd_shift_kernel<N, DT, Coeffs>, blocks, kLanes, c.stream,
+            return launch(agg_bwd_shift_kernel<N, DT, Coeffs>, blocks, threads, c.stream,
                           static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.residual), k,
                           static_cast<uint16_t*>(c.gres), c.T, c.H);
         }

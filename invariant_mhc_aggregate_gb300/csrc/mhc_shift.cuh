@@ -216,9 +216,11 @@ agg_fwd_shift_kernel(const uint16_t* __restrict__ res, Coeffs coeffs, uint16_t* 
 }
 
 // --------------------------------------------------------------------------
-// backward: one block of 256 threads per token (grid-stride); thread j is
-// ORDER-256 lane j and takes chunks j, j + 256, ... in increasing order, as
-// in every other path.  For chunk c it loads the two aligned vectors of g
+// backward: one block per token (grid-stride); thread j is ORDER-256 lane j
+// and takes chunks j, j + 256, ... in increasing order, as in every other
+// path.  Blocks have 256 threads, or, for rows of fewer than 256 chunks, only
+// the warps that hold chunks (at least 16n threads, for the row-end values):
+// the lanes of the missing warps would hold +0, and the fold counts them so.  For chunk c it loads the two aligned vectors of g
 // and of each residual row that cover values 8c .. 8c+7 and realigns them;
 // g's pair also gives the grad_residual vector c + osh_k of each output row
 // k (at that row's offset).  The fold is the common one.
@@ -342,7 +344,7 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
             if ((s16 < 8) ? (h < head && h < Hi) : (h < Hi))
                 st_stream2(row + h, Elem<DT>::cvt(__fmul_rn(pkk, Elem<DT>::one(ld_stream2(grow + h)))));
         }
-        fold_lanes_and_store<N, 1>(acc, red, coeffs, t, slope);
+        fold_lanes_and_store<N, 1>(acc, red, coeffs, t, slope, int(blockDim.x / 32));
     }
 }
 
