@@ -541,7 +541,7 @@ agg_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict_
                 }
             }
         }
-        fold_lanes_and_store<N, LPT>(acc, red, coeffs, t, slope);
+        fold_lanes_and_store<N, LPT>(acc, red, coeffs, t, slope, int(blockDim.x * LPT / 32));
     }
 }
 

@@ -241,11 +241,14 @@ cudaError_t fwd_dispatch(const FwdCall& c, const Coeffs& k) {
 // backward
 // ---------------------------------------------------------------------------
 
+// Rows of fewer vectors than a block has threads get blocks of only the
+// warps that hold vectors (the fold adds +0 for the missing lane groups).
 template <int N, int DT, int NW, int BATCH, int MIN_BLOCKS, class Coeffs>
 cudaError_t launch_bwd_vec(const BwdCall& c, const Coeffs& k, uint32_t V) {
-    constexpr int kThreads = kLanes / (NW / 4);
+    constexpr uint32_t kThreads = kLanes / (NW / 4);
+    const uint32_t threads = V < kThreads ? (V + 31) / 32 * 32 : kThreads;
     const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
-    return launch(agg_bwd_vec_kernel<N, DT, NW, BATCH, MIN_BLOCKS, Coeffs>, blocks, kThreads, c.stream,
+    return launch(agg_bwd_vec_kernel<N, DT, NW, BATCH, MIN_BLOCKS, Coeffs>, blocks, threads, c.stream,
                   static_cast<const Words<NW>*>(c.g), static_cast<const Words<NW>*>(c.residual), k,
                   static_cast<Words<NW>*>(c.gres), c.T, V);
 }
