@@ -79,21 +79,36 @@ cudaError_t bwd_vec(const PostBwdCall& c, const Coeffs& k) {
 }
 
 // Bulk-copy backward: a persistent grid of MIN_BLOCKS blocks per SM, each
-// with a STAGES-deep ring of (2n + 1) x 4 KB stages.
-template <int N, int DT, int STAGES, int MIN_BLOCKS, class Coeffs>
-cudaError_t bwd_bulk(const PostBwdCall& c, const Coeffs& k) {
+// with a STAGES-deep ring of (2n + 1) x 4 KB stages.  Short rows (NARROW) get
+// blocks of only the consumer warps that hold chunks, stages of that width,
+// and proportionally more blocks per SM.
+template <int N, int DT, int STAGES, int MIN_BLOCKS, class Coeffs, bool NARROW>
+cudaError_t bwd_bulk_launch(const PostBwdCall& c, const Coeffs& k, uint32_t consumers) {
     static std::atomic<uint64_t> smem_done{0};
-    constexpr uint32_t smem = STAGES * post_bulk_stage_bytes(N);
-    auto* kernel = post_bwd_bulk_kernel<N, DT, STAGES, MIN_BLOCKS, Coeffs>;
-    cudaError_t e = allow_smem(kernel, smem, smem_done);
+    constexpr uint32_t kMaxSmem = STAGES * post_bulk_stage_bytes(N);
+    auto* kernel = post_bwd_bulk_kernel<N, DT, STAGES, MIN_BLOCKS, Coeffs, NARROW>;
+    cudaError_t e = allow_smem(kernel, kMaxSmem, smem_done);
     if (e != cudaSuccess) return e;
     unsigned int* flag = nullptr;
     if ((e = wait_flag_ptr(&flag)) != cudaSuccess) return e;
-    const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * MIN_BLOCKS);
-    return launch_smem(kernel, blocks, post_bulk_threads<Coeffs>(), smem, c.stream, static_cast<const Words<4>*>(c.g),
-                       static_cast<const Words<4>*>(c.x), static_cast<const Words<4>*>(c.y), k, c.res,
-                       static_cast<Words<4>*>(c.grad_x), static_cast<Words<4>*>(c.grad_y), c.grad_res, c.T,
-                       uint32_t(c.H / 8), flag);
+    const uint32_t smem = STAGES * post_bulk_stage_bytes(N, consumers);
+    const uint32_t per_sm = MIN_BLOCKS * (uint32_t(kLanes) / consumers);
+    const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * per_sm);
+    return launch_smem(kernel, blocks, post_bulk_threads<Coeffs>(int(consumers)), smem, c.stream,
+                       static_cast<const Words<4>*>(c.g), static_cast<const Words<4>*>(c.x),
+                       static_cast<const Words<4>*>(c.y), k, c.res, static_cast<Words<4>*>(c.grad_x),
+                       static_cast<Words<4>*>(c.grad_y), c.grad_res, c.T, uint32_t(c.H / 8), flag);
+}
+
+// Narrow blocks from rows of at most 128 chunks on, where they let more
+// blocks share an SM (measured at n = 4 and about 2^25 values a call:
+// H = 512 507 -> 266 us, H = 1024 274 -> 193 us; at H = 1536, 192 consumers
+// gained nothing).
+template <int N, int DT, int STAGES, int MIN_BLOCKS, class Coeffs>
+cudaError_t bwd_bulk(const PostBwdCall& c, const Coeffs& k) {
+    const uint64_t V = c.H / 8;
+    if (V > uint64_t(kLanes / 2)) return bwd_bulk_launch<N, DT, STAGES, MIN_BLOCKS, Coeffs, false>(c, k, kLanes);
+    return bwd_bulk_launch<N, DT, STAGES, MIN_BLOCKS, Coeffs, true>(c, k, uint32_t((V + 31) / 32 * 32));
 }
 
 template <int N, int DT, class Coeffs>

@@ -319,11 +319,14 @@ post_fwd_element_kernel(const uint16_t* __restrict__ x, const uint16_t* __restri
 // and value n*n + k, the gradient of post[t,k], goes to the coefficient
 // source (post_store_grad; `slope` holds the token's sigmoid' when post comes
 // from the mix).  All threads of the block call it.
+//
+// `groups`: the lane groups of 32 that have threads; the lanes of the others
+// hold +0 and their group values are +0 in the cross-group fold.
 template <int N, int LPT, class Coeffs, class Sync = BlockSync>
 __device__ __forceinline__ void post_fold_and_store(float (&acc)[LPT][N * N + N], float (*red)[N * N + N],
                                                     const Coeffs& coeffs, const float* slope,
                                                     float* __restrict__ grad_res, uint64_t t,
-                                                    Sync sync = Sync()) {
+                                                    Sync sync = Sync(), int groups = kGroups) {
     constexpr int M = N * N + N;
     constexpr int kThreadsPerGroup = 32 / LPT;
 #pragma unroll
@@ -345,7 +348,7 @@ __device__ __forceinline__ void post_fold_and_store(float (&acc)[LPT][N * N + N]
         const int m = threadIdx.x;
         float w[kGroups];
 #pragma unroll
-        for (int i = 0; i < kGroups; ++i) w[i] = red[i][m];
+        for (int i = 0; i < kGroups; ++i) w[i] = (i < groups) ? red[i][m] : 0.0f;
 #pragma unroll
         for (int s = kGroups / 2; s >= 1; s >>= 1) {
 #pragma unroll
@@ -478,8 +481,10 @@ post_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict
 // stops waiting, the block still runs to its end
 // on whatever the stage holds, and the producer waits (bounded) for the
 // copies it issued before it exits.
-__host__ __device__ constexpr uint32_t post_bulk_stage_bytes(int n) {
-    return uint32_t(2 * n + 1) * kLanes * 16u;
+// A stage holds `width` chunks (16 bytes) of each of the 2n + 1 rows: 256,
+// or for rows of fewer than 256 chunks the block's consumer threads.
+__host__ __device__ constexpr uint32_t post_bulk_stage_bytes(int n, uint32_t width = kLanes) {
+    return uint32_t(2 * n + 1) * width * 16u;
 }
 
 //
@@ -493,12 +498,15 @@ __host__ __device__ constexpr uint32_t post_bulk_stage_bytes(int n) {
 // sigmoid.
 constexpr int kPostSlots = 3;
 
+// Threads of a block with `consumers` consumer threads (256, or for rows of
+// fewer than 256 chunks the warps that hold chunks): then the producer warp,
+// then (post from the mix) the helper warp.
 template <class Coeffs>
-__host__ __device__ constexpr int post_bulk_threads() {
-    return kLanes + 32 + (Coeffs::kBlockTable ? 32 : 0);
+__host__ __device__ constexpr int post_bulk_threads(int consumers = kLanes) {
+    return consumers + 32 + (Coeffs::kBlockTable ? 32 : 0);
 }
 
-template <int N, int DT, int STAGES, int MIN_BLOCKS, class Coeffs>
+template <int N, int DT, int STAGES, int MIN_BLOCKS, class Coeffs, bool NARROW>
 __global__ void __launch_bounds__(post_bulk_threads<Coeffs>(), MIN_BLOCKS)
 post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict__ x,
                      const Words<4>* __restrict__ y, Coeffs coeffs, const float* __restrict__ res,
@@ -517,11 +525,16 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
     __shared__ __align__(8) uint64_t freed[kNS];
     __shared__ float red[kGroups][M];
     __shared__ float slots[kNS][2 * N];   // post, then sigmoid'
+    // consumer threads: 256, or (NARROW: rows of fewer than 256 chunks) a
+    // multiple of 32 set by the launch; a stage row holds `width` chunks (256,
+    // or all of a shorter row's)
+    const uint32_t consumers = NARROW ? blockDim.x - 32u - (kSig ? 32u : 0u) : uint32_t(kLanes);
+    const uint32_t width = consumers;
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kGroups);
+            mbar_init(&empty[s], consumers / 32u);
         }
 #pragma unroll
         for (int s = 0; s < kNS; ++s) {
@@ -534,10 +547,10 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
     pdl_enter();
     const uint32_t nseg = (V + kLanes - 1) / kLanes;
 
-    if (threadIdx.x >= kLanes + 32) {
+    if (threadIdx.x >= consumers + 32u) {
         // helper warp (post from the mix): the block's tokens' sigmoids, in order
         if constexpr (kSig) {
-            const uint32_t lane = threadIdx.x - (kLanes + 32);
+            const uint32_t lane = threadIdx.x - (consumers + 32u);
             bool ok = true;
             uint32_t tok = 0;
             for (uint64_t t = blockIdx.x; t < T; t += gridDim.x, ++tok) {
@@ -556,9 +569,9 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
         return;
     }
 
-    if (threadIdx.x >= kLanes) {
+    if (threadIdx.x >= consumers) {
         // producer warp: one thread issues the copies
-        if (threadIdx.x != kLanes) return;
+        if (threadIdx.x != consumers) return;
         bool ok = true;
         uint32_t item = 0;
         for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
@@ -567,15 +580,15 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
                 if (round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1u);
                 const uint32_t c0 = s * kLanes;
                 const uint32_t bytes = (V - c0 < uint32_t(kLanes) ? V - c0 : uint32_t(kLanes)) * 16u;
-                unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N);
+                unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N, width);
                 mbar_arrive_expect_tx(&full[st], bytes * R);
 #pragma unroll
                 for (int k = 0; k < N; ++k) {
-                    bulk_copy_g2s(dst + size_t(k) * kLanes * 16, g + (uint64_t(N) * t + k) * V + c0, bytes, &full[st]);
-                    bulk_copy_g2s(dst + size_t(N + k) * kLanes * 16, x + (uint64_t(N) * t + k) * V + c0, bytes,
+                    bulk_copy_g2s(dst + size_t(k) * width * 16, g + (uint64_t(N) * t + k) * V + c0, bytes, &full[st]);
+                    bulk_copy_g2s(dst + size_t(N + k) * width * 16, x + (uint64_t(N) * t + k) * V + c0, bytes,
                                   &full[st]);
                 }
-                bulk_copy_g2s(dst + size_t(2 * N) * kLanes * 16, y + t * V + c0, bytes, &full[st]);
+                bulk_copy_g2s(dst + size_t(2 * N) * width * 16, y + t * V + c0, bytes, &full[st]);
             }
         }
         // every copy issued has landed before the block's shared memory goes
@@ -587,7 +600,7 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
 
     // consumers
     const uint32_t j = threadIdx.x;
-    const auto sync = [] { named_sync(1, kLanes); };
+    const auto sync = [consumers] { named_sync(1, consumers); };
     bool ok = true;
     uint32_t item = 0, tok = 0;
     for (uint64_t t = blockIdx.x; t < T; t += gridDim.x, ++tok) {
@@ -611,14 +624,14 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
             const uint32_t c = s * kLanes + j;
             if (c < V) {
                 const Words<4>* sm =
-                    reinterpret_cast<const Words<4>*>(stage_mem + size_t(st) * post_bulk_stage_bytes(N)) + j;
+                    reinterpret_cast<const Words<4>*>(stage_mem + size_t(st) * post_bulk_stage_bytes(N, width)) + j;
                 Words<4> gv[N], xv[N];
 #pragma unroll
                 for (int k = 0; k < N; ++k) {
-                    gv[k] = sm[k * kLanes];
-                    xv[k] = sm[(N + k) * kLanes];
+                    gv[k] = sm[k * width];
+                    xv[k] = sm[(N + k) * width];
                 }
-                const Words<4> yv = sm[2 * N * kLanes];
+                const Words<4> yv = sm[2 * N * width];
                 post_chunk<N, DT, 4>(
                     cf, gv, xv, yv, acc,
                     [&](int k, const Words<4>& o) { st_stream<4>(grad_x + (uint64_t(N) * t + k) * V + c, o); },
@@ -627,7 +640,7 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
             __syncwarp();
             if ((j & 31u) == 0) mbar_arrive(&empty[st]);
         }
-        post_fold_and_store<N, 1>(acc, red, coeffs, slots[sl] + N, grad_res, t, sync);
+        post_fold_and_store<N, 1>(acc, red, coeffs, slots[sl] + N, grad_res, t, sync, int(consumers / 32u));
         // the fold's closing barrier: every consumer is done with the slot
         if (kSig && j == 0) mbar_arrive(&freed[sl]);
     }
