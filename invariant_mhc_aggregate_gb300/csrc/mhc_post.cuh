@@ -313,6 +313,51 @@ post_fwd_element_kernel(const uint16_t* __restrict__ x, const uint16_t* __restri
 // backward
 // --------------------------------------------------------------------------
 
+// One level of a warp reduce-scatter: the lane holds C values (indices
+// base .. base + C - 1, the first `real` of them real, the rest +0 padding)
+// and, with its partner lane ^ S, splits them: the lower lane keeps the first
+// ceil(C/2), the upper one the rest, each adding the partner's copies of the
+// values it keeps.  Every value is summed over exactly the lane pairs of the
+// xor butterfly (lane i with i ^ S), and IEEE addition is commutative bit
+// for bit, so each value's sum is the butterfly's, in fewer shuffles (at
+// n = 4, 21 instead of 100 for 20 values).
+template <int C, int S>
+__device__ __forceinline__ void rs_level(const float (&v)[C], float (&out)[(C + 1) / 2], int& base, int& real,
+                                         uint32_t lane) {
+    constexpr int H = (C + 1) / 2;
+    const bool upper = (lane & uint32_t(S)) != 0u;
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+        const float lo = v[i];
+        const float hi = (H + i < C) ? v[H + i] : 0.0f;
+        const float recv = __shfl_xor_sync(0xffffffffu, upper ? lo : hi, S);
+        out[i] = __fadd_rn(upper ? hi : lo, recv);
+    }
+    if (upper) {
+        base += H;
+        real = real > H ? real - H : 0;
+    } else {
+        real = real < H ? real : H;
+    }
+}
+
+// The warp sums of M values (the xor butterfly over 32 lanes), scattered:
+// each lane writes the values it ends with into row[index].
+template <int M>
+__device__ __forceinline__ void warp_sums_to(const float (&acc)[M], float* row, uint32_t lane) {
+    constexpr int C1 = (M + 1) / 2, C2 = (C1 + 1) / 2, C3 = (C2 + 1) / 2, C4 = (C3 + 1) / 2, C5 = (C4 + 1) / 2;
+    int base = 0, real = M;
+    float a1[C1], a2[C2], a3[C3], a4[C4], a5[C5];
+    rs_level<M, 16>(acc, a1, base, real, lane);
+    rs_level<C1, 8>(a1, a2, base, real, lane);
+    rs_level<C2, 4>(a2, a3, base, real, lane);
+    rs_level<C3, 2>(a3, a4, base, real, lane);
+    rs_level<C4, 1>(a4, a5, base, real, lane);
+#pragma unroll
+    for (int i = 0; i < C5; ++i)
+        if (i < real) row[base + i] = a5[i];
+}
+
 // The ORDER-256 fold of M = n*n + n lane sums of a 256-lane block (LPT lanes
 // per thread: lanes LPT*thread + l): xor shuffles over each group of 32 lanes,
 // the 8 group values through shared memory; grad_res[t,k,j] = value k*n + j,
@@ -329,19 +374,24 @@ __device__ __forceinline__ void post_fold_and_store(float (&acc)[LPT][N * N + N]
                                                     Sync sync = Sync(), int groups = kGroups) {
     constexpr int M = N * N + N;
     constexpr int kThreadsPerGroup = 32 / LPT;
+    if constexpr (LPT == 1) {
+        // one lane per thread: the warp's sums by reduce-scatter
+        warp_sums_to<M>(acc[0], red[threadIdx.x / 32], threadIdx.x & 31u);
+    } else {
 #pragma unroll
-    for (int m = 0; m < M; ++m) {
+        for (int m = 0; m < M; ++m) {
 #pragma unroll
-        for (int s = kThreadsPerGroup / 2; s >= 1; s >>= 1) {
+            for (int s = kThreadsPerGroup / 2; s >= 1; s >>= 1) {
 #pragma unroll
-            for (int l = 0; l < LPT; ++l)
-                acc[l][m] = __fadd_rn(acc[l][m], __shfl_xor_sync(0xffffffffu, acc[l][m], s));
+                for (int l = 0; l < LPT; ++l)
+                    acc[l][m] = __fadd_rn(acc[l][m], __shfl_xor_sync(0xffffffffu, acc[l][m], s));
+            }
+            acc[0][m] = __fadd_rn(acc[0][m], acc[LPT - 1][m]);
         }
-        if (LPT == 2) acc[0][m] = __fadd_rn(acc[0][m], acc[LPT - 1][m]);
-    }
-    if ((threadIdx.x % kThreadsPerGroup) == 0) {
+        if ((threadIdx.x % kThreadsPerGroup) == 0) {
 #pragma unroll
-        for (int m = 0; m < M; ++m) red[threadIdx.x / kThreadsPerGroup][m] = acc[0][m];
+            for (int m = 0; m < M; ++m) red[threadIdx.x / kThreadsPerGroup][m] = acc[0][m];
+        }
     }
     sync();
     if (threadIdx.x < uint32_t(M)) {
