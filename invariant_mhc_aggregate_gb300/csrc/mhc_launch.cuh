@@ -302,7 +302,11 @@ cudaError_t bwd_n(const BwdCall& c, const Coeffs& k) {
             if (threads < uint32_t(16 * N)) threads = uint32_t(16 * N);
             if (threads < 32u) threads = 32u;
             const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
-            return launch(agg_bwd_shift_kernel<N, DT, Coeffs>, blocks, threads, c.stream,
+            if (threads < uint32_t(kLanes))
+                return launch(agg_bwd_shift_kernel<N, DT, Coeffs, true>, blocks, threads, c.stream,
+                              static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.residual), k,
+                              static_cast<uint16_t*>(c.gres), c.T, c.H);
+            return launch(agg_bwd_shift_kernel<N, DT, Coeffs, false>, blocks, threads, c.stream,
                           static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.residual), k,
                           static_cast<uint16_t*>(c.gres), c.T, c.H);
         }

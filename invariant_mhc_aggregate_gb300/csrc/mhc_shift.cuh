@@ -218,9 +218,12 @@ agg_fwd_shift_kernel(const uint16_t* __restrict__ res, Coeffs coeffs, uint16_t* 
 // --------------------------------------------------------------------------
 // backward: one block per token (grid-stride); thread j is ORDER-256 lane j
 // and takes chunks j, j + 256, ... in increasing order, as in every other
-// path.  Blocks have 256 threads, or, for rows of fewer than 256 chunks, only
-// the warps that hold chunks (at least 16n threads, for the row-end values):
-// the lanes of the missing warps would hold +0, and the fold counts them so.  For chunk c it loads the two aligned vectors of g
+// path.  Blocks have 256 threads, or (NARROW), for rows of fewer than 256
+// chunks, only the warps that hold chunks (at least 16n threads, for the
+// row-end values): the lanes of the missing warps would hold +0, and the fold
+// counts them so.  The full-width instance keeps the fold's group count a
+// constant (at n = 4 that is 64 registers rather than 70: four blocks per SM
+// rather than three).  For chunk c it loads the two aligned vectors of g
 // and of each residual row that cover values 8c .. 8c+7 and realigns them;
 // g's pair also gives the grad_residual vector c + osh_k of each output row
 // k (at that row's offset).  The fold is the common one.
@@ -229,7 +232,7 @@ agg_fwd_shift_kernel(const uint16_t* __restrict__ res, Coeffs coeffs, uint16_t* 
 template <int N>
 __host__ __device__ constexpr int shift_bwd_batch() { return N >= 4 ? 1 : 2; }
 
-template <int N, int DT, class Coeffs>
+template <int N, int DT, class Coeffs, bool NARROW>
 __global__ void __launch_bounds__(kLanes)
 agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict__ res,
                      Coeffs coeffs, uint16_t* __restrict__ gres, uint64_t T, uint64_t H) {
@@ -344,7 +347,10 @@ agg_bwd_shift_kernel(const uint16_t* __restrict__ g, const uint16_t* __restrict_
             if ((s16 < 8) ? (h < head && h < Hi) : (h < Hi))
                 st_stream2(row + h, Elem<DT>::cvt(__fmul_rn(pkk, Elem<DT>::one(ld_stream2(grow + h)))));
         }
-        fold_lanes_and_store<N, 1>(acc, red, coeffs, t, slope, int(blockDim.x / 32));
+        if constexpr (NARROW)
+            fold_lanes_and_store<N, 1>(acc, red, coeffs, t, slope, int(blockDim.x / 32));
+        else
+            fold_lanes_and_store<N, 1>(acc, red, coeffs, t, slope);
     }
 }
 
