@@ -111,13 +111,31 @@ cudaError_t bwd_bulk(const PostBwdCall& c, const Coeffs& k) {
     return bwd_bulk_launch<N, DT, STAGES, MIN_BLOCKS, Coeffs, true>(c, k, uint32_t((V + 31) / 32 * 32));
 }
 
+// Split bulk-copy backward (n = 8): one block of 512 consumer threads and a
+// producer warp per SM, a STAGES-deep ring of (2n + 1) x 4 KB stages.
+template <int N, int DT, int STAGES, class Coeffs>
+cudaError_t bwd_split(const PostBwdCall& c, const Coeffs& k) {
+    static std::atomic<uint64_t> smem_done{0};
+    constexpr uint32_t kSmem = STAGES * post_bulk_stage_bytes(N);
+    auto* kernel = post_bwd_split_kernel<N, DT, STAGES, Coeffs>;
+    cudaError_t e = allow_smem(kernel, kSmem, smem_done);
+    if (e != cudaSuccess) return e;
+    unsigned int* flag = nullptr;
+    if ((e = wait_flag_ptr(&flag)) != cudaSuccess) return e;
+    const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms));
+    return launch_smem(kernel, blocks, kSplitConsumers + 32, kSmem, c.stream, static_cast<const Words<4>*>(c.g),
+                       static_cast<const Words<4>*>(c.x), static_cast<const Words<4>*>(c.y), k, c.res,
+                       static_cast<Words<4>*>(c.grad_x), static_cast<Words<4>*>(c.grad_y), c.grad_res, c.T,
+                       uint32_t(c.H / 8), flag);
+}
+
 template <int N, int DT, class Coeffs>
 cudaError_t bwd_n(const PostBwdCall& c, const Coeffs& k) {
     // 16-byte path: the bulk-copy kernel (2 blocks per SM, a 3-stage ring) up
     // to n = 4; at n = 8 one 16-byte vector per thread and pass, 1 block per
     // SM, the coefficients in shared memory
     if (c.path == kPathVec16) {
-        if constexpr (N >= 8) return bwd_vec<N, DT, 4, 1, 1, true>(c, k);
+        if constexpr (N >= 8) return bwd_split<N, DT, 3>(c, k);
         else return bwd_bulk<N, DT, 3, 2>(c, k);
     }
     const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);

@@ -342,9 +342,9 @@ __device__ __forceinline__ void rs_level(const float (&v)[C], float (&out)[(C + 
 }
 
 // The warp sums of M values (the xor butterfly over 32 lanes), scattered:
-// each lane writes the values it ends with into row[index].
-template <int M>
-__device__ __forceinline__ void warp_sums_to(const float (&acc)[M], float* row, uint32_t lane) {
+// each lane hands the values it ends with to put(index, sum) ...
+template <int M, class Put>
+__device__ __forceinline__ void warp_sums_put(const float (&acc)[M], uint32_t lane, Put put) {
     constexpr int C1 = (M + 1) / 2, C2 = (C1 + 1) / 2, C3 = (C2 + 1) / 2, C4 = (C3 + 1) / 2, C5 = (C4 + 1) / 2;
     int base = 0, real = M;
     float a1[C1], a2[C2], a3[C3], a4[C4], a5[C5];
@@ -355,7 +355,39 @@ __device__ __forceinline__ void warp_sums_to(const float (&acc)[M], float* row, 
     rs_level<C4, 1>(a4, a5, base, real, lane);
 #pragma unroll
     for (int i = 0; i < C5; ++i)
-        if (i < real) row[base + i] = a5[i];
+        if (i < real) put(base + i, a5[i]);
+}
+
+// ... or writes them into row[index]
+template <int M>
+__device__ __forceinline__ void warp_sums_to(const float (&acc)[M], float* row, uint32_t lane) {
+    warp_sums_put<M>(acc, lane, [row](int i, float v) { row[i] = v; });
+}
+
+// The cross-group step of the fold below: once the block's group values are
+// in shared memory (group_value(g, m) for g < groups), value m folds over the
+// 8 groups with strides 4, 2, 1 (a missing group counts +0) and is stored.
+// Opens and closes with the group's barrier.
+template <int N, class Coeffs, class Sync, class GroupValue>
+__device__ __forceinline__ void post_fold_groups(GroupValue group_value, const Coeffs& coeffs, const float* slope,
+                                                 float* __restrict__ grad_res, uint64_t t, Sync sync,
+                                                 int groups, uint32_t thread) {
+    constexpr int M = N * N + N;
+    sync();
+    if (thread < uint32_t(M)) {
+        const int m = int(thread);
+        float w[kGroups];
+#pragma unroll
+        for (int i = 0; i < kGroups; ++i) w[i] = (i < groups) ? group_value(i, m) : 0.0f;
+#pragma unroll
+        for (int s = kGroups / 2; s >= 1; s >>= 1) {
+#pragma unroll
+            for (int i = 0; i < s; ++i) w[i] = __fadd_rn(w[i], w[i + s]);
+        }
+        if (m < N * N) grad_res[uint64_t(N) * N * t + m] = w[0];
+        else post_store_grad<N>(coeffs, t, m - N * N, w[0], slope);
+    }
+    sync();   // red[] (and the coefficient table) are reused by the next token
 }
 
 // The ORDER-256 fold of M = n*n + n lane sums of a 256-lane block (LPT lanes
@@ -393,21 +425,8 @@ __device__ __forceinline__ void post_fold_and_store(float (&acc)[LPT][N * N + N]
             for (int m = 0; m < M; ++m) red[threadIdx.x / kThreadsPerGroup][m] = acc[0][m];
         }
     }
-    sync();
-    if (threadIdx.x < uint32_t(M)) {
-        const int m = threadIdx.x;
-        float w[kGroups];
-#pragma unroll
-        for (int i = 0; i < kGroups; ++i) w[i] = (i < groups) ? red[i][m] : 0.0f;
-#pragma unroll
-        for (int s = kGroups / 2; s >= 1; s >>= 1) {
-#pragma unroll
-            for (int i = 0; i < s; ++i) w[i] = __fadd_rn(w[i], w[i + s]);
-        }
-        if (m < N * N) grad_res[uint64_t(N) * N * t + m] = w[0];
-        else post_store_grad<N>(coeffs, t, m - N * N, w[0], slope);
-    }
-    sync();   // red[] (and the coefficient table) are reused by the next token
+    post_fold_groups<N>([red](int i, int m) { return red[i][m]; }, coeffs, slope, grad_res, t, sync, groups,
+                        threadIdx.x);
 }
 
 // The grad_x vector of input stream j (j < n) or the grad_y vector (j == n)
@@ -693,6 +712,250 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
         post_fold_and_store<N, 1>(acc, red, coeffs, slots[sl] + N, grad_res, t, sync, int(consumers / 32u));
         // the fold's closing barrier: every consumer is done with the slot
         if (kSig && j == 0) mbar_arrive(&freed[sl]);
+    }
+    if (!ok) *timeouts = 1u;
+}
+
+// Split bulk-copy path for n = 8 (H % 8 == 0, the 2-byte buffers 16-byte
+// aligned).  A lane's 72 sums do not fit one thread's registers beside its
+// chunk's 17 input vectors, so each ORDER-256 lane is served by two consumer
+// threads that split the chunk's 8 positions: thread half e takes positions
+// 4e .. 4e + 3 (words 2e, 2e + 1 of each 16-byte vector).
+//
+//  * grad_x, grad_y: each thread writes its 8 bytes of every output vector;
+//    the n-term tree is (k < n/2 terms) + (k >= n/2 terms), and a thread
+//    holds the g values of "its" n/2 streams k (4e .. 4e + 3) and of the
+//    other n/2 in separate arrays, so the two subtrees come out in either
+//    order and add commutatively.
+//  * a chunk's partial for stream pair (k, j) is chunk_partial's tree,
+//    (positions 0-3) + (positions 4-7): each thread forms its half for
+//    every k, keeps the sum of k in its own range and sends the other
+//    half to its partner (shfl_xor 1), which adds it to its own.  Thread e
+//    thus keeps the lane sums of grad_res[k][j] and grad_post[k] for
+//    k in 4e .. 4e + 3 (36 values).
+//  * lanes: warps 2q and 2q + 1 hold the lanes of group q with lane bit 0
+//    equal to 0 and 1 (lane 32q + 2i + b in thread 2i + e of warp 2q + b).
+//    The in-group fold's strides 16, 8, 4, 2 are thread strides 16 .. 2
+//    (reduce-scatter), stride 1 adds the two warps' values in shared
+//    memory, then the groups fold with strides 4, 2, 1: ORDER-256's pairs
+//    and order.
+//
+// The rows stream through shared memory as in the bulk kernel above (one
+// producer warp, a STAGES-deep ring of (2n + 1) x 4 KB stages, "full" and
+// "empty" barriers, bounded waits and the same timeout flag).  The token's
+// coefficients sit in a shared table filled by the consumers at the token's
+// start, res transposed (tab[j*n + k] = res[k][j]) so that the n/2 values of
+// a column that a thread multiplies are one 16-byte read; then post, then
+// (post from the mix) sigmoid'.
+constexpr int kSplitConsumers = 2 * kLanes;
+
+template <int N>
+constexpr int kSplitSums = N * N / 2 + N / 2;
+
+// One level of a reduce-scatter over thread strides 16, 8, 4, 2 (thread
+// bit 0, the position half, stays apart).
+template <int M, class Put>
+__device__ __forceinline__ void pair_sums_put(const float (&acc)[M], uint32_t lane, Put put) {
+    constexpr int C1 = (M + 1) / 2, C2 = (C1 + 1) / 2, C3 = (C2 + 1) / 2, C4 = (C3 + 1) / 2;
+    int base = 0, real = M;
+    float a1[C1], a2[C2], a3[C3], a4[C4];
+    rs_level<M, 16>(acc, a1, base, real, lane);
+    rs_level<C1, 8>(a1, a2, base, real, lane);
+    rs_level<C2, 4>(a2, a3, base, real, lane);
+    rs_level<C3, 2>(a3, a4, base, real, lane);
+#pragma unroll
+    for (int i = 0; i < C4; ++i)
+        if (i < real) put(base + i, a4[i]);
+}
+
+// Sum i of position half e is value m of the fold (k*n + j: grad_res;
+// n*n + k: grad_post): i < n*n/2 is k = e n/2 + i / n, j = i % n; the rest
+// grad_post[e n/2 + i - n*n/2].
+template <int N>
+__device__ __forceinline__ int split_sum_index(uint32_t e, int i) {
+    constexpr int NH = N / 2;
+    return i < N * NH ? int(e) * NH * N + i : N * N + int(e) * NH + (i - N * NH);
+}
+
+template <int DT>
+__device__ __forceinline__ void unpack_half(uint2 w, float (&f)[4]) {
+    f[0] = Elem<DT>::lo(w.x);
+    f[1] = Elem<DT>::hi(w.x);
+    f[2] = Elem<DT>::lo(w.y);
+    f[3] = Elem<DT>::hi(w.y);
+}
+
+// chunk_partial's subtree over one position half: (g0 x0 + g1 x1) + (g2 x2 + g3 x3)
+__device__ __forceinline__ float half_partial(const float (&g)[4], const float (&x)[4]) {
+    return __fadd_rn(__fadd_rn(__fmul_rn(g[0], x[0]), __fmul_rn(g[1], x[1])),
+                     __fadd_rn(__fmul_rn(g[2], x[2]), __fmul_rn(g[3], x[3])));
+}
+
+__device__ __forceinline__ void st_stream_half(void* p, uint32_t a, uint32_t b) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" : : "l"(p), "r"(a), "r"(b) : "memory");
+}
+
+// One chunk, position half e: sm = the stage's row 0 at this thread's 8
+// bytes (row r at sm[r * 512]); gx = grad_x row 0 at this thread's 8 bytes
+// (row j at gx[j * rs]); gy likewise for grad_y; `live` = the warp's threads
+// that run it (both threads of each lane).
+template <int N, int DT>
+__device__ __forceinline__ void post_split_chunk(const uint2* sm, uint32_t e, const float* tab,
+                                                 float (&acc)[kSplitSums<N>], uint2* gx, uint64_t rs, uint2* gy,
+                                                 uint32_t live) {
+    constexpr int NH = N / 2;
+    const uint32_t ko = NH * e, kt = NH - ko;   // first stream of this half's k range, of the other's
+    float go[NH][4], gt[NH][4];
+#pragma unroll
+    for (int kk = 0; kk < NH; ++kk) {
+        unpack_half<DT>(sm[(ko + kk) * 2 * kLanes], go[kk]);
+        unpack_half<DT>(sm[(kt + kk) * 2 * kLanes], gt[kk]);
+    }
+#pragma unroll
+    for (int j = 0; j <= N; ++j) {
+        // j < n: input stream j (x row, res column j); j == n: y and post
+        const bool is_y = j == N;
+        float xf[4];
+        unpack_half<DT>(sm[(is_y ? 2 * N : N + j) * 2 * kLanes], xf);
+        float co[NH], ct[NH];
+#pragma unroll
+        for (int kk = 0; kk < NH; kk += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(tab + j * N + ko + kk);
+            const float4 b = *reinterpret_cast<const float4*>(tab + j * N + kt + kk);
+            co[kk] = a.x, co[kk + 1] = a.y, co[kk + 2] = a.z, co[kk + 3] = a.w;
+            ct[kk] = b.x, ct[kk + 1] = b.y, ct[kk + 2] = b.z, ct[kk + 3] = b.w;
+        }
+        float v[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            float qo[NH], qt[NH];
+#pragma unroll
+            for (int kk = 0; kk < NH; ++kk) {
+                qo[kk] = __fmul_rn(co[kk], go[kk][p]);
+                qt[kk] = __fmul_rn(ct[kk], gt[kk][p]);
+            }
+            v[p] = __fadd_rn(tree_sum<NH>(qo), tree_sum<NH>(qt));
+        }
+        const uint32_t w0 = Elem<DT>::pack(v[0], v[1]), w1 = Elem<DT>::pack(v[2], v[3]);
+        st_stream_half(is_y ? gy : gx + uint64_t(j) * rs, w0, w1);
+#pragma unroll
+        for (int kk = 0; kk < NH; ++kk) {
+            const float own = half_partial(go[kk], xf);
+            const float other = __shfl_xor_sync(live, half_partial(gt[kk], xf), 1);
+            const int i = is_y ? N * NH + kk : kk * N + j;
+            acc[i] = __fadd_rn(acc[i], __fadd_rn(own, other));
+        }
+    }
+}
+
+// Token t's table: tab[j*n + k] = res[t,k,j], tab[n*n + k] = post[t,k]
+// (from the mix: computed, and tab[n*n + n + k] = sigmoid').  Consumer
+// threads m < n*n + n write it; ends with the consumers' barrier.
+template <int N, class Coeffs, class Sync>
+__device__ __forceinline__ void split_fill_table(const Coeffs& c, const float* __restrict__ res, uint64_t t,
+                                                 uint32_t m, float* tab, Sync sync) {
+    if (m < uint32_t(N * N)) {
+        tab[(m % N) * N + m / N] = __ldg(res + uint64_t(N) * N * t + m);
+    } else if (m < uint32_t(N * N + N)) {
+        const int k = int(m) - N * N;
+        if constexpr (Coeffs::kBlockTable) {
+            c.pre_and_slope(c.mix_at(uint64_t(N) * t + k), k, tab[m], tab[m + N]);
+        } else {
+            tab[m] = __ldg(c.pre + uint64_t(N) * t + k);
+        }
+    }
+    sync();
+}
+
+template <int N, int DT, int STAGES, class Coeffs>
+__global__ void __launch_bounds__(kSplitConsumers + 32, 1)
+post_bwd_split_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict__ x,
+                      const Words<4>* __restrict__ y, Coeffs coeffs, const float* __restrict__ res,
+                      Words<4>* __restrict__ grad_x, Words<4>* __restrict__ grad_y,
+                      float* __restrict__ grad_res, uint64_t T, uint32_t V, unsigned int* __restrict__ timeouts) {
+    static_assert(N % 8 == 0, "the position halves take n/2 streams, read 4 coefficients at a time");
+    constexpr int R = 2 * N + 1;   // staged rows: g (N), x (N), y
+    constexpr int M = N * N + N;
+    extern __shared__ __align__(128) unsigned char stage_mem[];   // STAGES * R * 4 KB
+    __shared__ __align__(8) uint64_t full[STAGES];
+    __shared__ __align__(8) uint64_t empty[STAGES];
+    __shared__ float red[kSplitConsumers / 32][M];
+    __shared__ __align__(16) float tab[kPostTable<N>];
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kSplitConsumers / 32);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    pdl_enter();
+    const uint32_t nseg = (V + kLanes - 1) / kLanes;
+
+    if (threadIdx.x >= uint32_t(kSplitConsumers)) {
+        // producer warp: one thread issues the copies
+        if (threadIdx.x != uint32_t(kSplitConsumers)) return;
+        bool ok = true;
+        uint32_t item = 0;
+        for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
+            for (uint32_t s = 0; s < nseg; ++s, ++item) {
+                const uint32_t st = item % STAGES, round = item / STAGES;
+                if (round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1u);
+                const uint32_t c0 = s * kLanes;
+                const uint32_t bytes = (V - c0 < uint32_t(kLanes) ? V - c0 : uint32_t(kLanes)) * 16u;
+                unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N);
+                mbar_arrive_expect_tx(&full[st], bytes * R);
+#pragma unroll
+                for (int k = 0; k < N; ++k) {
+                    bulk_copy_g2s(dst + size_t(k) * kLanes * 16, g + (uint64_t(N) * t + k) * V + c0, bytes, &full[st]);
+                    bulk_copy_g2s(dst + size_t(N + k) * kLanes * 16, x + (uint64_t(N) * t + k) * V + c0, bytes,
+                                  &full[st]);
+                }
+                bulk_copy_g2s(dst + size_t(2 * N) * kLanes * 16, y + t * V + c0, bytes, &full[st]);
+            }
+        }
+        // every copy issued has landed before the block's shared memory goes
+        for (uint32_t i = item > uint32_t(STAGES) ? item - STAGES : 0; i < item; ++i)
+            if (!mbar_wait(&full[i % STAGES], (i / STAGES) & 1u)) ok = false;
+        if (!ok) *timeouts = 1u;
+        return;
+    }
+
+    // consumers: warp 2q + b, thread 2i + e holds position half e of lane 32q + 2i + b
+    const uint32_t w = threadIdx.x >> 5, l = threadIdx.x & 31u;
+    const uint32_t e = l & 1u;
+    const uint32_t j = 32u * (w >> 1) + (l & ~1u) + (w & 1u);   // the ORDER-256 lane
+    const auto sync = [] { named_sync(1, kSplitConsumers); };
+    bool ok = true;
+    uint32_t item = 0;
+    for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        split_fill_table<N>(coeffs, res, t, threadIdx.x, tab, sync);
+        float acc[kSplitSums<N>];
+#pragma unroll
+        for (int i = 0; i < kSplitSums<N>; ++i) acc[i] = 0.0f;
+#pragma unroll 1
+        for (uint32_t s = 0; s < nseg; ++s, ++item) {
+            const uint32_t st = item % STAGES;
+            if (ok) ok = mbar_wait(&full[st], (item / STAGES) & 1u);
+            const uint32_t c = s * kLanes + j;
+            // in a row's last segment a warp may hold chunks in only some of
+            // its threads (always both threads of a lane): the partner
+            // exchange runs over those
+            const uint32_t live = __ballot_sync(0xffffffffu, c < V);
+            if (c < V) {
+                const uint2* sm = reinterpret_cast<const uint2*>(stage_mem + size_t(st) * post_bulk_stage_bytes(N)) +
+                                  2 * j + e;
+                uint2* gx = reinterpret_cast<uint2*>(grad_x + uint64_t(N) * t * V + c) + e;
+                uint2* gy = reinterpret_cast<uint2*>(grad_y + t * V + c) + e;
+                post_split_chunk<N, DT>(sm, e, tab, acc, gx, 2ull * V, gy, live);
+            }
+            __syncwarp();
+            if (l == 0) mbar_arrive(&empty[st]);
+        }
+        pair_sums_put<kSplitSums<N>>(acc, l, [&](int i, float v) { red[w][split_sum_index<N>(e, i)] = v; });
+        post_fold_groups<N>([](int q, int m) { return __fadd_rn(red[2 * q][m], red[2 * q + 1][m]); }, coeffs,
+                            tab + N * N + N, grad_res, t, sync, kGroups, threadIdx.x);
     }
     if (!ok) *timeouts = 1u;
 }
