@@ -135,7 +135,7 @@ cudaError_t bwd_n(const PostBwdCall& c, const Coeffs& k) {
     // to n = 4; at n = 8 one 16-byte vector per thread and pass, 1 block per
     // SM, the coefficients in shared memory
     if (c.path == kPathVec16) {
-        if constexpr (N >= 8) return bwd_split<N, DT, 3>(c, k);
+        if constexpr (N >= 8) return bwd_split<N, DT, 2>(c, k);
         else return bwd_bulk<N, DT, 3, 2>(c, k);
     }
     const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);

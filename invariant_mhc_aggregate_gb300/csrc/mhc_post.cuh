@@ -743,10 +743,7 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
 // The rows stream through shared memory as in the bulk kernel above (one
 // producer warp, a STAGES-deep ring of (2n + 1) x 4 KB stages, "full" and
 // "empty" barriers, bounded waits and the same timeout flag).  The token's
-// coefficients sit in a shared table filled by the consumers at the token's
-// start, res transposed (tab[j*n + k] = res[k][j]) so that the n/2 values of
-// a column that a thread multiplies are one 16-byte read; then post, then
-// (post from the mix) sigmoid'.
+// coefficients sit in a shared table (split_prefetch_table).
 constexpr int kSplitConsumers = 2 * kLanes;
 
 template <int N>
@@ -849,19 +846,33 @@ __device__ __forceinline__ void post_split_chunk(const uint2* sm, uint32_t e, co
 }
 
 // Token t's table: tab[j*n + k] = res[t,k,j], tab[n*n + k] = post[t,k]
-// (from the mix: computed, and tab[n*n + n + k] = sigmoid').  Consumer
-// threads m < n*n + n write it; ends with the consumers' barrier.
-template <int N, class Coeffs, class Sync>
-__device__ __forceinline__ void split_fill_table(const Coeffs& c, const float* __restrict__ res, uint64_t t,
-                                                 uint32_t m, float* tab, Sync sync) {
+// (from the mix: computed, and tab[n*n + n + k] = sigmoid').  It is fetched
+// a token ahead: consumer threads m < n*n + n start 4-byte asynchronous
+// copies of their value (the mix value into mix[k] when post comes from the
+// mix) while the block works on the previous token ...
+template <int N, class Coeffs>
+__device__ __forceinline__ void split_prefetch_table(const Coeffs& c, const float* __restrict__ res, uint64_t t,
+                                                     uint32_t m, float* tab, float* mix) {
     if (m < uint32_t(N * N)) {
-        tab[(m % N) * N + m / N] = __ldg(res + uint64_t(N) * N * t + m);
+        cp_async4(&tab[(m % N) * N + m / N], res + uint64_t(N) * N * t + m);
     } else if (m < uint32_t(N * N + N)) {
-        const int k = int(m) - N * N;
-        if constexpr (Coeffs::kBlockTable) {
-            c.pre_and_slope(c.mix_at(uint64_t(N) * t + k), k, tab[m], tab[m + N]);
-        } else {
-            tab[m] = __ldg(c.pre + uint64_t(N) * t + k);
+        const uint32_t k = m - uint32_t(N * N);
+        if constexpr (Coeffs::kBlockTable) cp_async4(&mix[k], c.mix + uint64_t(N) * t + k);
+        else cp_async4(&tab[m], c.pre + uint64_t(N) * t + k);
+    }
+    cp_async_commit();
+}
+
+// ... and complete it at the token's start: each thread waits for its copy,
+// the sigmoids are evaluated (post from the mix), then the consumers' barrier.
+template <int N, class Coeffs, class Sync>
+__device__ __forceinline__ void split_finish_table(const Coeffs& c, uint32_t m, float* tab, const float* mix,
+                                                   Sync sync) {
+    cp_async_wait_all();
+    if constexpr (Coeffs::kBlockTable) {
+        if (m >= uint32_t(N * N) && m < uint32_t(N * N + N)) {
+            const int k = int(m) - N * N;
+            c.pre_and_slope(mix[k], k, tab[m], tab[m + N]);
         }
     }
     sync();
@@ -880,7 +891,8 @@ post_bwd_split_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict
     __shared__ __align__(8) uint64_t full[STAGES];
     __shared__ __align__(8) uint64_t empty[STAGES];
     __shared__ float red[kSplitConsumers / 32][M];
-    __shared__ __align__(16) float tab[kPostTable<N>];
+    __shared__ __align__(16) float tab[2][kPostTable<N>];   // tokens alternate
+    __shared__ float mix[2][N];
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
@@ -928,9 +940,15 @@ post_bwd_split_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict
     const uint32_t j = 32u * (w >> 1) + (l & ~1u) + (w & 1u);   // the ORDER-256 lane
     const auto sync = [] { named_sync(1, kSplitConsumers); };
     bool ok = true;
-    uint32_t item = 0;
-    for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        split_fill_table<N>(coeffs, res, t, threadIdx.x, tab, sync);
+    uint32_t item = 0, tok = 0;
+    if (blockIdx.x < T) split_prefetch_table<N>(coeffs, res, blockIdx.x, threadIdx.x, tab[0], mix[0]);
+    for (uint64_t t = blockIdx.x; t < T; t += gridDim.x, ++tok) {
+        // the previous token's readers of tab[cur ^ 1] are past its fold
+        const uint32_t cur = tok & 1u;
+        split_finish_table<N>(coeffs, threadIdx.x, tab[cur], mix[cur], sync);
+        if (t + gridDim.x < T)
+            split_prefetch_table<N>(coeffs, res, t + gridDim.x, threadIdx.x, tab[cur ^ 1u], mix[cur ^ 1u]);
+        const float* ttab = tab[cur];
         float acc[kSplitSums<N>];
 #pragma unroll
         for (int i = 0; i < kSplitSums<N>; ++i) acc[i] = 0.0f;
@@ -948,14 +966,14 @@ post_bwd_split_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict
                                   2 * j + e;
                 uint2* gx = reinterpret_cast<uint2*>(grad_x + uint64_t(N) * t * V + c) + e;
                 uint2* gy = reinterpret_cast<uint2*>(grad_y + t * V + c) + e;
-                post_split_chunk<N, DT>(sm, e, tab, acc, gx, 2ull * V, gy, live);
+                post_split_chunk<N, DT>(sm, e, ttab, acc, gx, 2ull * V, gy, live);
             }
             __syncwarp();
             if (l == 0) mbar_arrive(&empty[st]);
         }
         pair_sums_put<kSplitSums<N>>(acc, l, [&](int i, float v) { red[w][split_sum_index<N>(e, i)] = v; });
         post_fold_groups<N>([](int q, int m) { return __fadd_rn(red[2 * q][m], red[2 * q + 1][m]); }, coeffs,
-                            tab + N * N + N, grad_res, t, sync, kGroups, threadIdx.x);
+                            ttab + N * N + N, grad_res, t, sync, kGroups, threadIdx.x);
     }
     if (!ok) *timeouts = 1u;
 }
