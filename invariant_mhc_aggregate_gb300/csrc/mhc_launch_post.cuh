@@ -69,15 +69,6 @@ cudaError_t fwd_n(const PostFwdCall& c, const Coeffs& k) {
                     static_cast<uint16_t*>(c.out), c.T, c.H);
 }
 
-template <int N, int DT, int NW, int BATCH, int MIN_BLOCKS, bool SMEM_COEF, class Coeffs>
-cudaError_t bwd_vec(const PostBwdCall& c, const Coeffs& k) {
-    const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
-    return launch(post_bwd_vec_kernel<N, DT, NW, BATCH, MIN_BLOCKS, SMEM_COEF, Coeffs>, blocks, kLanes / (NW / 4),
-                  c.stream, static_cast<const Words<NW>*>(c.g), static_cast<const Words<NW>*>(c.x),
-                  static_cast<const Words<NW>*>(c.y), k, c.res, static_cast<Words<NW>*>(c.grad_x),
-                  static_cast<Words<NW>*>(c.grad_y), c.grad_res, c.T, uint32_t(c.H / (2 * NW)));
-}
-
 // Bulk-copy backward: a persistent grid of MIN_BLOCKS blocks per SM, each
 // with a STAGES-deep ring of (2n + 1) x 4 KB stages.  Short rows (NARROW) get
 // blocks of only the consumer warps that hold chunks, stages of that width,
@@ -132,8 +123,8 @@ cudaError_t bwd_split(const PostBwdCall& c, const Coeffs& k) {
 template <int N, int DT, class Coeffs>
 cudaError_t bwd_n(const PostBwdCall& c, const Coeffs& k) {
     // 16-byte path: the bulk-copy kernel (2 blocks per SM, a 3-stage ring) up
-    // to n = 4; at n = 8 one 16-byte vector per thread and pass, 1 block per
-    // SM, the coefficients in shared memory
+    // to n = 4; at n = 8 the split kernel (two threads per lane, 1 block per
+    // SM, a 2-stage ring)
     if (c.path == kPathVec16) {
         if constexpr (N >= 8) return bwd_split<N, DT, 2>(c, k);
         else return bwd_bulk<N, DT, 3, 2>(c, k);

@@ -32,8 +32,8 @@
 //    and writes the n output vectors.
 //  * backward, 16-byte path, n <= 4: the bulk-copy kernel below (rows
 //    streamed through a shared-memory ring, one producer warp, 256 consumer
-//    lanes); n = 8: one 256-thread block per token, thread j = ORDER-256 lane
-//    j taking chunks j, j + 256, ... from global memory.  Either way lane j
+//    lanes); n = 8: the split kernel (the same ring, each lane served by two
+//    threads that take half of each chunk's positions).  Either way lane j
 //    writes grad_x and grad_y for its chunks and adds their partials to the
 //    n*n + n sums, which fold like grad_pre's.
 //  * other shapes and alignments: the same arithmetic with 2-byte accesses.
@@ -471,64 +471,6 @@ __device__ __forceinline__ void post_chunk(const C& cf, const Words<NW> (&gv)[N]
 #pragma unroll
         for (int l = 0; l < NW / 4; ++l)
             acc[l][N * N + k] = __fadd_rn(acc[l][N * N + k], chunk_partial<DT, NW>(gv[k], yv, 4 * l));
-    }
-}
-
-// Vector path: H % (2*NW) == 0 and the 2-byte buffers aligned to 4*NW
-// bytes; V = H / (2*NW) vectors per row.  One token per block of 256/LPT
-// threads (LPT = NW/4 lanes per thread): thread j takes vectors j, j + B,
-// j + 2B, ... (B threads), i.e. for lane LPT*j + l the chunks
-// (LPT*j + l) + 256m, in increasing order; BATCH vectors of each row are
-// loaded per pass.
-template <int N, int DT, int NW, int BATCH, int MIN_BLOCKS, bool SMEM_COEF, class Coeffs>
-__global__ void __launch_bounds__(kLanes / (NW / 4), MIN_BLOCKS)
-post_bwd_vec_kernel(const Words<NW>* __restrict__ g, const Words<NW>* __restrict__ x,
-                    const Words<NW>* __restrict__ y, Coeffs coeffs, const float* __restrict__ res,
-                    Words<NW>* __restrict__ grad_x, Words<NW>* __restrict__ grad_y,
-                    float* __restrict__ grad_res, uint64_t T, uint32_t V) {
-    constexpr int M = N * N + N;
-    constexpr int LPT = NW / 4;
-    constexpr uint32_t B = kLanes / LPT;
-    __shared__ float red[kGroups][M];
-    __shared__ float coef[kPostTable<N>];
-    pdl_enter();
-    const uint32_t j = threadIdx.x;
-    for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        PostCoeffs<N, SMEM_COEF> cf;
-        post_load_token<N>(coeffs, res, t, j, coef, cf, BlockSync());
-        float acc[LPT][M];
-#pragma unroll
-        for (int l = 0; l < LPT; ++l)
-#pragma unroll
-            for (int m = 0; m < M; ++m) acc[l][m] = 0.0f;
-        const uint64_t row0 = uint64_t(N) * t * V;
-#pragma unroll 1
-        for (uint32_t v0 = j; v0 < V; v0 += B * BATCH) {
-            Words<NW> gv[BATCH][N], xv[BATCH][N], yv[BATCH];
-#pragma unroll
-            for (int b = 0; b < BATCH; ++b) {
-                const uint32_t v = v0 + uint32_t(b) * B;
-                if (b == 0 || v < V) {
-#pragma unroll
-                    for (int k = 0; k < N; ++k) {
-                        gv[b][k] = ld_stream<NW>(g + row0 + uint64_t(k) * V + v);
-                        xv[b][k] = ld_stream<NW>(x + row0 + uint64_t(k) * V + v);
-                    }
-                    yv[b] = ld_stream<NW>(y + t * V + v);
-                }
-            }
-#pragma unroll
-            for (int b = 0; b < BATCH; ++b) {
-                const uint32_t v = v0 + uint32_t(b) * B;
-                if (b == 0 || v < V) {
-                    post_chunk<N, DT, NW>(
-                        cf, gv[b], xv[b], yv[b], acc,
-                        [&](int k, const Words<NW>& o) { st_stream<NW>(grad_x + row0 + uint64_t(k) * V + v, o); },
-                        [&](const Words<NW>& o) { st_stream<NW>(grad_y + t * V + v, o); });
-                }
-            }
-        }
-        post_fold_and_store<N, LPT>(acc, red, coeffs, coef + N * N + N, grad_res, t);
     }
 }
 
