@@ -61,8 +61,32 @@ cudaError_t fwd_vec(const PostFwdCall& c, const Coeffs& k) {
 // thread, with the register budget of 4 blocks per SM (2 at n = 8, whose
 // inputs alone take 36 registers); 32-byte vectors, more vectors per thread
 // or fewer blocks per SM were slower.
+// Split forward (n = 8, rows of at least 128 vectors): 128 positions per
+// block, two threads each.
+template <int N, int DT, int MIN_BLOCKS, class Coeffs>
+cudaError_t fwd_split(const PostFwdCall& c, const Coeffs& k) {
+    const uint64_t V = c.H / 8;
+    const uint64_t max_tokens = 0x7FFFFFFFull / V;
+    for (uint64_t t0 = 0; t0 < c.T; t0 += max_tokens) {
+        const uint64_t nt = (c.T - t0 < max_tokens) ? c.T - t0 : max_tokens;
+        const uint32_t n_vec = uint32_t(nt * V);
+        const auto* x = static_cast<const Words<4>*>(c.x) + uint64_t(N) * t0 * V;
+        const auto* y = static_cast<const Words<4>*>(c.y) + t0 * V;
+        auto* o = static_cast<Words<4>*>(c.out) + uint64_t(N) * t0 * V;
+        const cudaError_t e =
+            launch(post_fwd_split_kernel<N, DT, MIN_BLOCKS, Coeffs>, grid_for(n_vec, kSplitFwdVecs, ~0u), kPostBlock,
+                   c.stream, x, y, k.shifted(uint64_t(N) * t0), c.res + uint64_t(N) * N * t0, o, n_vec, uint32_t(V),
+                   make_fastdiv_u32(uint32_t(V)));
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 template <int N, int DT, class Coeffs>
 cudaError_t fwd_n(const PostFwdCall& c, const Coeffs& k) {
+    if constexpr (N >= 8) {
+        if (c.path == kPathVec16 && c.H / 8 >= uint64_t(kSplitFwdVecs)) return fwd_split<N, DT, 4>(c, k);
+    }
     if (c.path == kPathVec16) return fwd_vec<N, DT, 4, 1, (N >= 8 ? 2 : 4)>(c, k);
     return launch2d(post_fwd_element_kernel<N, DT, Coeffs>, narrow_grid(c.H, c.T), kNarrowBlock, c.stream,
                     static_cast<const uint16_t*>(c.x), static_cast<const uint16_t*>(c.y), k, c.res,

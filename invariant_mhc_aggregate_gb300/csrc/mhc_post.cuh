@@ -269,6 +269,105 @@ post_fwd_vec_kernel(const Words<NW>* __restrict__ x, const Words<NW>* __restrict
     }
 }
 
+// Split forward (n = 8, 16-byte path, rows of at least kSplitFwdVecs
+// vectors): two threads per 16-byte position, thread half e taking its
+// positions 4e .. 4e + 3 (8 bytes of each of the n x vectors and of y), so
+// that a thread's unpacked inputs (4n + 4 values) and one output's
+// coefficients fit in few registers and more blocks share an SM.  A block's
+// 128 positions span at most two tokens, whose coefficients (res row-major,
+// then post, computed when post comes from the mix) the block puts in a
+// shared table while its loads are in flight.  Each output value is
+// post_value's: the n-term tree, then the post term.
+constexpr int kSplitFwdVecs = kPostBlock / 2;
+
+// The 4 values of 8 bytes of a 2-byte row (2 words, low half first).
+template <int DT>
+__device__ __forceinline__ void unpack_half(uint2 w, float (&f)[4]) {
+    f[0] = Elem<DT>::lo(w.x);
+    f[1] = Elem<DT>::hi(w.x);
+    f[2] = Elem<DT>::lo(w.y);
+    f[3] = Elem<DT>::hi(w.y);
+}
+
+// An 8-byte streaming store.
+__device__ __forceinline__ void st_stream_half(void* p, uint32_t a, uint32_t b) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" : : "l"(p), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ uint2 ld_stream_half(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+template <int N, int DT, int MIN_BLOCKS, class Coeffs>
+__global__ void __launch_bounds__(kPostBlock, MIN_BLOCKS)
+post_fwd_split_kernel(const Words<4>* __restrict__ x, const Words<4>* __restrict__ y, Coeffs coeffs,
+                      const float* __restrict__ res, Words<4>* __restrict__ out, uint32_t n_vec, uint32_t V,
+                      FastDivU32 divV) {
+    constexpr int M = N * N + N;
+    __shared__ __align__(16) float tab[2][M];
+    pdl_enter();
+    const uint32_t e = threadIdx.x & 1u;
+    const uint32_t first = blockIdx.x * uint32_t(kSplitFwdVecs);
+    const uint32_t i = first + (threadIdx.x >> 1);
+    const bool mine = i < n_vec;
+    uint32_t tok = 0;
+    uint64_t row0 = 0;   // x / out vector of stream 0
+    float xf[N][4], yf[4];
+    if (mine) {
+        tok = fastdiv_u32(i, divV);
+        row0 = uint64_t(N) * tok * V + (i - tok * V);
+        uint2 xw[N];
+#pragma unroll
+        for (int j = 0; j < N; ++j) xw[j] = ld_stream_half(reinterpret_cast<const uint2*>(x + row0 + uint64_t(j) * V) + e);
+        const uint2 yw = ld_stream_half(reinterpret_cast<const uint2*>(y + i) + e);
+#pragma unroll
+        for (int j = 0; j < N; ++j) unpack_half<DT>(xw[j], xf[j]);
+        unpack_half<DT>(yw, yf);
+    }
+    // the block's tokens' coefficients (V >= 128: at most two tokens)
+    const uint32_t last = (n_vec - first > uint32_t(kSplitFwdVecs)) ? first + kSplitFwdVecs - 1 : n_vec - 1;
+    const uint32_t t_first = fastdiv_u32(first, divV);
+    const uint32_t count = (fastdiv_u32(last, divV) - t_first + 1) * uint32_t(M);
+    for (uint32_t q = threadIdx.x; q < count; q += kPostBlock) {
+        const uint32_t tt = q / uint32_t(M), m = q - tt * uint32_t(M);
+        const uint64_t t = uint64_t(t_first) + tt;
+        float v;
+        if (m < uint32_t(N * N)) {
+            v = __ldg(res + uint64_t(N) * N * t + m);
+        } else {
+            const int k = int(m) - N * N;
+            if constexpr (Coeffs::kBlockTable) v = coeffs.pre_from(coeffs.mix_at(uint64_t(N) * t + k), k);
+            else v = __ldg(coeffs.pre + uint64_t(N) * t + k);
+        }
+        tab[tt][m] = v;
+    }
+    __syncthreads();
+    if (!mine) return;
+    const float* ct = tab[tok - t_first];
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+        float rk[N];
+#pragma unroll
+        for (int j = 0; j < N; j += 4) {
+            const float4 c = *reinterpret_cast<const float4*>(ct + k * N + j);
+            rk[j] = c.x, rk[j + 1] = c.y, rk[j + 2] = c.z, rk[j + 3] = c.w;
+        }
+        const float pk = ct[N * N + k];
+        float o[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            float xs[N];
+#pragma unroll
+            for (int j = 0; j < N; ++j) xs[j] = xf[j][p];
+            o[p] = post_value<N>(rk, pk, xs, yf[p]);
+        }
+        st_stream_half(reinterpret_cast<uint2*>(out + row0 + uint64_t(k) * V) + e, Elem<DT>::pack(o[0], o[1]),
+                       Elem<DT>::pack(o[2], o[3]));
+    }
+}
+
 // 2-byte path: a 2-D grid of (2048-value row segment, token) blocks,
 // grid-stride over tokens; thread j takes values e*256 + j (e < 8).  With
 // post computed from the mix, the token's n sigmoids go through shared
@@ -716,22 +815,10 @@ __device__ __forceinline__ int split_sum_index(uint32_t e, int i) {
     return i < N * NH ? int(e) * NH * N + i : N * N + int(e) * NH + (i - N * NH);
 }
 
-template <int DT>
-__device__ __forceinline__ void unpack_half(uint2 w, float (&f)[4]) {
-    f[0] = Elem<DT>::lo(w.x);
-    f[1] = Elem<DT>::hi(w.x);
-    f[2] = Elem<DT>::lo(w.y);
-    f[3] = Elem<DT>::hi(w.y);
-}
-
 // chunk_partial's subtree over one position half: (g0 x0 + g1 x1) + (g2 x2 + g3 x3)
 __device__ __forceinline__ float half_partial(const float (&g)[4], const float (&x)[4]) {
     return __fadd_rn(__fadd_rn(__fmul_rn(g[0], x[0]), __fmul_rn(g[1], x[1])),
                      __fadd_rn(__fmul_rn(g[2], x[2]), __fmul_rn(g[3], x[3])));
-}
-
-__device__ __forceinline__ void st_stream_half(void* p, uint32_t a, uint32_t b) {
-    asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" : : "l"(p), "r"(a), "r"(b) : "memory");
 }
 
 // One chunk, position half e: sm = the stage's row 0 at this thread's 8
