@@ -94,6 +94,8 @@ FWD_CASES = [
     (9, 8, (0, 0, 0, 0, 0)),           # one 16-byte vector a row
     (3, 1, (0, 0, 0, 0, 0)),           # one value a row
     (1, 2048 + 16, (0, 0, 0, 0, 0)),   # a single token
+    (5, 1024, (0, 0, 0, 0, 0)),        # 128 vectors a row: n = 8's split forward from here on
+    (5, 1016, (0, 0, 0, 0, 0)),        # 127 vectors a row: n = 8's one-thread-per-vector forward
 ]
 
 
@@ -119,6 +121,7 @@ BWD_CASES = [
     (9, 8, (0,) * 9),
     (3, 1, (0,) * 9),
     (1, 2048 * 8 + 8, (0,) * 9),                       # long row: 8+ chunks a lane
+    (3, 8 * (256 + 37), (0,) * 9),                     # last segment ends inside a warp's lanes
 ]
 
 
