@@ -59,8 +59,9 @@ cudaError_t fwd_vec(const PostFwdCall& c, const Coeffs& k) {
 
 // Launch shapes (measured at T = 4096, H = 7168): 16-byte vectors, one per
 // thread, with the register budget of 4 blocks per SM (2 at n = 8, whose
-// inputs alone take 36 registers); 32-byte vectors, more vectors per thread
-// or fewer blocks per SM were slower.
+// inputs alone take 36 registers: used for rows of fewer than 128 vectors,
+// the split forward takes the longer ones); 32-byte vectors, more vectors
+// per thread or fewer blocks per SM were slower.
 // Split forward (n = 8, rows of at least 128 vectors): 128 positions per
 // block, two threads each.
 template <int N, int DT, int MIN_BLOCKS, class Coeffs>

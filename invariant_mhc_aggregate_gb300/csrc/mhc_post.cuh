@@ -29,7 +29,8 @@
 // the backward (6n + 4) H):
 //  * forward, 16-byte path: a flat grid over the [T,H] plane, one vector per
 //    thread; a thread loads the n x vectors and the y vector of its position
-//    and writes the n output vectors.
+//    and writes the n output vectors (n = 8, rows of 128+ vectors: two
+//    threads per position, 4 of its 8 values each).
 //  * backward, 16-byte path, n <= 4: the bulk-copy kernel below (rows
 //    streamed through a shared-memory ring, one producer warp, 256 consumer
 //    lanes); n = 8: the split kernel (the same ring, each lane served by two
@@ -64,10 +65,11 @@ struct BlockSync {
     __device__ __forceinline__ void operator()() const { __syncthreads(); }
 };
 
-// The coefficients of the token a backward block works on.  Up to n = 4 they
-// sit in registers (loaded from global memory, or copied from the token
-// table); at n = 8 (72 values, next to 72 lane sums) they stay in the token
-// table in shared memory, read where they are used.
+// The coefficients of the token a backward block works on (bulk and 2-byte
+// kernels).  Up to n = 4 they sit in registers (loaded from global memory,
+// or copied from the token table); at n = 8 (72 values, next to 72 lane
+// sums) they stay in the token table in shared memory, read where they are
+// used.
 template <int N, bool kShared = (N >= 8)>
 struct PostCoeffs {
     float pk[N], rk[N][N];
