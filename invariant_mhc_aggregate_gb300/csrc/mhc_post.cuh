@@ -792,8 +792,9 @@ constexpr int kSplitConsumers = 2 * kLanes;
 template <int N>
 constexpr int kSplitSums = N * N / 2 + N / 2;
 
-// One level of a reduce-scatter over thread strides 16, 8, 4, 2 (thread
-// bit 0, the position half, stays apart).
+// warp_sums_put's reduce-scatter over thread strides 16, 8, 4, 2 only
+// (thread bit 0, the position half, stays apart): each thread hands the
+// sums it ends with to put(index, sum).
 template <int M, class Put>
 __device__ __forceinline__ void pair_sums_put(const float (&acc)[M], uint32_t lane, Put put) {
     constexpr int C1 = (M + 1) / 2, C2 = (C1 + 1) / 2, C3 = (C2 + 1) / 2, C4 = (C3 + 1) / 2;
@@ -909,6 +910,10 @@ __device__ __forceinline__ void split_finish_table(const Coeffs& c, uint32_t m, 
     sync();
 }
 
+// 16 consumer warps and the producer warp: 17 warps put 5 on one SM
+// sub-partition, which caps a thread at 96 registers and leaves the
+// consumers some spills; with 2 stages (139 KB) the shared-memory carve-out
+// leaves room in L1 for them, with 3 most of their reloads went to L2.
 template <int N, int DT, int STAGES, class Coeffs>
 __global__ void __launch_bounds__(kSplitConsumers + 32, 1)
 post_bwd_split_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict__ x,
