@@ -400,9 +400,10 @@ def e2e_measure(args, torch, binding, g, res, pre, dev, stream, world, dist):
     ho = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     hgr = torch.empty((T, 4, H), dtype=torch.bfloat16).pin_memory()
     hgp = torch.empty((T, 4), dtype=torch.float32).pin_memory()
-    pipe = HostPipeline(4, H, torch.bfloat16, chunk_tokens=min(512, T), slots=3, device=dev)
+    pipe = HostPipeline(4, H, torch.bfloat16, chunk_tokens=min(1024, T), slots=5, device=dev)
     # the first steps on fresh pinned buffers run up to 30% slower (measured:
-    # 2.5 against 1.94 ms a step at T=4096), so warm up for several steps
+    # 2.5 against 1.94 ms a step at T=4096 with 512-token chunks), so warm up
+    # for several steps
     for _ in range(10):
         pipe.step(hr, hp, hg, ho, hgr, hgp)
     pipe.synchronize()
@@ -434,7 +435,7 @@ def e2e_measure(args, torch, binding, g, res, pre, dev, stream, world, dist):
     return {"value": round(value, 1), "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "rounds_ms": [round(r, 4) for r in rounds],
-            "note": ("pinned host buffers; HostPipeline: 512-token chunks, host->device copies, "
+            "note": ("pinned host buffers; HostPipeline: 1024-token chunks in 5 slots, host->device copies, "
                      "kernels and device->host copies overlapped on three streams")}
 
 
