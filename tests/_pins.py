@@ -1238,3 +1238,68 @@ ALL_CHECKS += [
     check_post_sigmoid_bwd_half,
     check_post_sigmoid_wiring,
 ]
+
+
+# --------------------------------------------------------------------------
+# ORDER-256 over h: the oracle's row sums against the recursive builder
+# --------------------------------------------------------------------------
+
+#: row lengths that give lanes no chunk, one chunk or several, with ragged tails
+RECURSIVE_H = tuple(range(1, 17)) + (255, 2047, 2049, 4104, 9001)
+
+
+def _widen(u16, dtype):
+    return bf16_widen(u16) if dtype == "bf16" else f16_widen(u16)
+
+
+def check_gp_recursive_builder(o):
+    """grad_pre equals the recursive ORDER-256 builder evaluated on the exact
+    products g[t,h]*r[t,k,h] (a product of two 8- or 11-bit significands is
+    exact in binary32), bit for bit, on random BF16 and FP16 data.  The
+    builder shares nothing with the oracle's loops, so a different tree shape
+    (another lane count, fold order or chunk tree) fails here on random data."""
+    rng = np.random.default_rng(2563)
+    for dtype in ("bf16", "f16"):
+        for H in RECURSIVE_H:
+            n = 4
+            g = random_storage(rng, (1, H), dtype)
+            r = random_storage(rng, (1, n, H), dtype)
+            pre = np.ones((1, n), np.float32)
+            _, gp = o.aggregate_bwd(g, r, pre, dtype)
+            sums = [gp]
+            if dtype == "bf16":
+                sums.append(o.grad_pre(g, r))       # the pages' op (n = 4, BF16)
+            q = _widen(g, dtype)[0][None, :] * _widen(r, dtype)[0]
+            for k in range(n):
+                want = f32_bits(order256_reference(q[k]))
+                for s in sums:
+                    assert f32_bits(s[0, k]) == want, (dtype, H, k)
+
+
+def check_post_bwd_recursive_builder(o):
+    """The mHC post's grad_post[t,k] = sum_h g[t,k,h]*y[t,h] and grad_res[t,k,j]
+    = sum_h g[t,k,h]*x[t,j,h] equal the recursive ORDER-256 builder on the
+    exact products, bit for bit (n = 2, BF16 and FP16)."""
+    rng = np.random.default_rng(2564)
+    n = 2
+    for dtype in ("bf16", "f16"):
+        for H in RECURSIVE_H:
+            g = random_storage(rng, (1, n, H), dtype)
+            x = random_storage(rng, (1, n, H), dtype)
+            y = random_storage(rng, (1, H), dtype)
+            post = np.ones((1, n), np.float32)
+            res = np.ones((1, n, n), np.float32)
+            _, _, gp, gr = o.post_bwd(g, x, y, post, res, dtype)
+            gw, xw, yw = _widen(g, dtype)[0], _widen(x, dtype)[0], _widen(y, dtype)[0]
+            for k in range(n):
+                assert f32_bits(gp[0, k]) == f32_bits(order256_reference(gw[k] * yw)), \
+                    ("grad_post", dtype, H, k)
+                for j in range(n):
+                    assert f32_bits(gr[0, k, j]) == f32_bits(order256_reference(gw[k] * xw[j])), \
+                        ("grad_res", dtype, H, k, j)
+
+
+ALL_CHECKS += [
+    check_gp_recursive_builder,
+    check_post_bwd_recursive_builder,
+]
