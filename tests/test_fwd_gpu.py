@@ -87,40 +87,7 @@ def test_decode_bit_exact(T, H):
     assert_bytes_equal(got, oracle_fwd(res, pre), f"decode T={T} H={H}")
 
 
-# --- workload fwd_prefill: H=7168, T up to 65536, seed 3
-
-@pytest.mark.parametrize("T", [1024, 4096, 16384])
-def test_prefill_bit_exact_full(T):
-    w = workload("fwd_prefill")
-    res, pre = forward_inputs(T, 7168, w.recipe, w.seed)
-    r_d, p_d = res.cuda(), pre.cuda()
-    out = binding.h_aggregate(r_d, p_d)
-    torch.cuda.synchronize()
-    assert_bytes_equal(u16(out), oracle_fwd(res, pre), f"prefill T={T}")
-
-
-def test_prefill_t65536_sampled_tokens():
-    """The largest workload (3.76 GB residual), drawn on the device and timed in
-    the benchmark in this same launch configuration; the oracle checks a
-    sample of whole tokens, which it computes one by one."""
-    w = workload("fwd_prefill")
-    T, H = 65536, 7168
-    res, pre = forward_inputs(T, H, w.recipe, w.seed, device="cuda")
-    out = binding.h_aggregate(res, pre)
-    torch.cuda.synchronize()
-    rng = np.random.default_rng(5)
-    sample = np.unique(np.concatenate([[0, 1, T // 2, T - 2, T - 1],
-                                       rng.integers(0, T, size=59)]))
-    idx = torch.as_tensor(sample, device="cuda")
-    want = oracle_fwd(res[idx], pre[idx])
-    assert_bytes_equal(u16(out[idx]), want, "T=65536 sampled tokens")
-    # a property at full size: every token equals its own one-token call
-    one = torch.empty((1, H), dtype=torch.bfloat16, device="cuda")
-    for t in sample[:8]:
-        binding.mhc_h_aggregate_fwd(res[t:t + 1], pre[t:t + 1], one)
-        torch.cuda.synchronize()
-        assert torch.equal(one[0].view(torch.int16), out[t].view(torch.int16))
-    del res, out
+# --- workload fwd_prefill: every shape in full, with repeats and splits, in test_configs_gpu.py
 
 
 # --- hand-worked elements through every path

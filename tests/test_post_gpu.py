@@ -171,30 +171,6 @@ def test_post_full_size_against_oracle():
         assert_bytes_equal(a, b, what)
 
 
-def test_post_n8_full_size_sampled_tokens():
-    """n = 8 at T = 4096, H = 7168 (the benchmark's n = 8 shape), one call
-    each way as the benchmark makes it; 40 tokens spread over the batch (the
-    first, the last, both sides of several blocks' token ranges) against the
-    oracle run on those tokens alone (tokens are independent)."""
-    T, H, n = 4096, 7168, 8
-    x, y, post, res, g = post_inputs(T, H, n, "normal", 6, with_grad=True)
-    xd, yd, pd, rd, gd = (t.cuda() for t in (x, y, post, res, g))
-    out = binding.post(xd, yd, pd, rd)
-    gx, gy, gp, gr = binding.post_backward(gd, xd, yd, pd, rd)
-    torch.cuda.synchronize()
-    rng = np.random.default_rng(11)
-    idx = np.unique(np.concatenate([[0, 1, 151, 152, 153, 303, 304, 2047, 2048, T - 2, T - 1],
-                                    rng.choice(T, 29, replace=False)]))
-    sel = torch.from_numpy(idx)
-    o = oracle.default()
-    xs, ys, ps, rs, gs = (t[sel].contiguous() for t in (x, y, post, res, g))
-    assert_bytes_equal(u16(out.cpu()[sel]), o.post_fwd(u16(xs), u16(ys), f32(ps), f32(rs)), "out")
-    want = o.post_bwd(u16(gs), u16(xs), u16(ys), f32(ps), f32(rs))
-    got = (u16(gx.cpu()[sel]), u16(gy.cpu()[sel]), f32(gp.cpu()[sel]), f32(gr.cpu()[sel]))
-    for a, b, what in zip(got, want, ("grad_x", "grad_y", "grad_post", "grad_res")):
-        assert_bytes_equal(a, b, what)
-
-
 @pytest.mark.parametrize("n", (1, 4, 8))
 def test_post_batch_split_invariance(n):
     """Every token's outputs are the same bytes whatever batch it is run in."""
