@@ -66,7 +66,8 @@ def bwd_bytes(T, H):
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=8000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 8000; 3 with --profile-family)")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--T", type=int, default=4096)
@@ -81,6 +82,24 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target length of the CPU oracle baseline sample")
+    prof = ap.add_argument_group(
+        "profiling workload",
+        "--profile-family F runs --steps steps (one warm-up step first) of one call family on "
+        "seeded inputs with nothing else in the process, a fixed workload for ncu -k, and prints "
+        "one plain line with the mean step time instead of the JSON line.  Families (a step is "
+        "the forward then the backward): plain (mhc_aggregate_fwd/bwd), sigmoid "
+        "(mhc_aggregate_sigmoid_fwd/bwd, then mhc_sigmoid_param_grad), post (mhc_post_fwd/bwd), "
+        "post_sigmoid (mhc_post_sigmoid_fwd/bwd, then mhc_sigmoid_param_grad).  Buffers are "
+        "PyTorch allocations, so the path follows from H (H % 16 == 0: 32-byte vectors, "
+        "H % 8 == 0: 16-byte, even H: 4-byte pairs, odd H: realigned 16-byte); --offset 2 moves "
+        "every 2-byte buffer off its allocation's alignment (the realigned path for H >= 64)")
+    prof.add_argument("--profile-family", choices=("plain", "sigmoid", "post", "post_sigmoid"),
+                      default=None)
+    prof.add_argument("--n", type=int, default=4, help="stream count of the profiling workload")
+    prof.add_argument("--dtype", choices=("bf16", "f16"), default="bf16",
+                      help="storage type of the profiling workload")
+    prof.add_argument("--offset", type=int, default=0,
+                      help="byte offset (even) of every 2-byte buffer of the profiling workload")
     return ap.parse_args(argv)
 
 
@@ -379,11 +398,40 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(g, res, pre, T, H, args.cpu_seconds)
 
+    if "sweep" in line:
+        # kept last, so that it stays in the tail of a truncated log
+        line["kernels_at_h7168"] = headline_kernels(line["sweep"])
+
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def headline_kernels(results):
+    """The forward alone at T = 4096, 16384 and 65536 and the backward alone
+    at T = 4096 (H = 7168), from the sweep: steady (back to back, no L2
+    reuse), cold_clean (graph replay after an L2 flush that leaves no dirty
+    lines) and cold_write_flush (the pages' write flush, whose write-back the
+    call pays); microseconds and the fraction of the measured copy peak (m)
+    and of 8 TB/s (n)."""
+    out = {}
+    for e in results:
+        key = (e.get("dir"), e.get("T"), e.get("H"))
+        if e.get("workload") not in ("fwd_prefill", "bwd_t4096_h7168") or key not in (
+                ("fwd", 4096, 7168), ("fwd", 16384, 7168), ("fwd", 65536, 7168), ("bwd", 4096, 7168)):
+            continue
+        d = {}
+        for col, name in (("steady", "steady"), ("cold_clean", "cold_clean"),
+                          ("cold", "cold_write_flush")):
+            if col not in e:
+                continue
+            c = e[col]
+            us = c["us"] if "us" in c else c["us_p20_p50_p80"][1]
+            d[name] = {"us": us, "m": c["frac_of_measured"], "n": c["frac_of_8TBs"]}
+        out[f"{key[0]}_t{key[1]}"] = d
+    return out
 
 
 def e2e_measure(args, torch, binding, g, res, pre, dev, stream, world, dist):
@@ -408,10 +456,10 @@ def e2e_measure(args, torch, binding, g, res, pre, dev, stream, world, dist):
         pipe.step(hr, hp, hg, ho, hgr, hgp)
     pipe.synchronize()
     n = max(5, min(args.steps, 50))
-    # three rounds of n steps, the median round reported: the host link's
-    # rate varies from run to run (1.94 to 2.45 ms a step seen on one box)
+    # five rounds of n steps, the median round reported: the host link's
+    # rate varies from round to round (1.82 to 3.10 ms a step seen on one box)
     rounds = []
-    for _ in range(3):
+    for _ in range(5):
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
@@ -423,7 +471,7 @@ def e2e_measure(args, torch, binding, g, res, pre, dev, stream, world, dist):
         e1.record(pipe.d2h)
         torch.cuda.synchronize()
         rounds.append(e0.elapsed_time(e1) / n)
-    ms = max_over_ranks(sorted(rounds)[1], dist, dev)
+    ms = max_over_ranks(sorted(rounds)[len(rounds) // 2], dist, dev)
     # the host results are the device results of the same inputs
     d_out = binding.h_aggregate(res, pre)
     d_gr, d_gp = binding.h_aggregate_backward(g, res, pre)
@@ -443,9 +491,14 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
     """us/call per (T,H).
 
     "cold": CUDA-graph replay of one call with L2 flushed by a 256 MiB write
-    before each sample (the pages' cold-L2 method; the flush leaves dirty lines
-    that the timed call has to write back); 7 rounds x (10 warm-up + 100
-    samples), p20/p50/p80 of the round medians.
+    before each sample (the pages' cold-L2 method); 7 rounds x (10 warm-up +
+    100 samples), p20/p50/p80 of the round medians.  The write flush leaves
+    up to a whole L2 of dirty lines that the timed call has to write back, so
+    this column charges the flush's own write-back to the call.
+    "cold_clean": the same, with a read of 4x L2 after the write flush and
+    before the start event: the flush's dirty lines are written back during
+    that read, and the timed call starts with an L2 holding only clean lines
+    of an unrelated buffer (none of its inputs, nothing to write back).
     "steady": about 400 calls back to back (a CUDA graph of at least 16
     calls, replayed), rotating over enough buffer sets that no call finds its
     inputs in L2 (at least 3x L2 in total), events only at the two ends;
@@ -457,12 +510,17 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
     stream = torch.cuda.Stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 
-    def time_graph(graph):
+    rflush = torch.ones(4 * l2 // 8, dtype=torch.int64, device=dev)
+    sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def time_graph(graph, clean=False):
         meds = []
         for _ in range(7):
             samples = []
             for i in range(110):
                 flush.zero_()
+                if clean:
+                    torch.sum(rflush, dim=0, out=sink)
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record()
@@ -518,7 +576,8 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
     results.append({"workload": "launch_floor", "dir": "none",
                     "note": "one trivial kernel timed by the cold method (graph replay after a "
                             "256 MiB write flush, CUDA events)",
-                    "cold": {"us_p20_p50_p80": time_graph(floor_graph)}})
+                    "cold": {"us_p20_p50_p80": time_graph(floor_graph)},
+                    "cold_clean": {"us_p20_p50_p80": time_graph(floor_graph, clean=True)}})
     del floor_graph
 
     for name, seed, recipe, shapes in FWD_SWEEP:
@@ -532,8 +591,10 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
                 binding.mhc_h_aggregate_fwd(r, p, o)
             nbytes = fwd_bytes(T, H)
             us = time_graph(graph)
+            us_c = time_graph(graph, clean=True)
             entry = {"workload": name, "dir": "fwd", "T": T, "H": H,
-                     "cold": {"us_p20_p50_p80": us, **entry_for(us[1], nbytes)}}
+                     "cold": {"us_p20_p50_p80": us, **entry_for(us[1], nbytes)},
+                     "cold_clean": {"us_p20_p50_p80": us_c, **entry_for(us_c[1], nbytes)}}
             del graph
             ns = n_sets(nbytes)
             if ns is not None:
@@ -566,8 +627,10 @@ def sweep(torch, binding, forward_inputs, backward_inputs, dev, flush, peak):
                 binding.mhc_h_aggregate_bwd(g, r, p, gr, gp)
             nbytes = bwd_bytes(T, H)
             us = time_graph(graph)
+            us_c = time_graph(graph, clean=True)
             entry = {"workload": name, "dir": "bwd", "T": T, "H": H,
-                     "cold": {"us_p20_p50_p80": us, **entry_for(us[1], nbytes)}}
+                     "cold": {"us_p20_p50_p80": us, **entry_for(us[1], nbytes)},
+                     "cold_clean": {"us_p20_p50_p80": us_c, **entry_for(us_c[1], nbytes)}}
             del graph
             ns = n_sets(nbytes)
             if ns is not None:
@@ -815,9 +878,107 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# profiling workload: one call family, nothing else in the process
+# ---------------------------------------------------------------------------
+
+def _shifted(torch, t, offset: int):
+    """A copy of t placed `offset` bytes past its allocation's alignment."""
+    if offset == 0:
+        return t
+    n = t.numel()
+    buf = torch.empty(n + 256, dtype=t.dtype, device=t.device)
+    e = offset // t.element_size()
+    view = buf[e:e + n].view(t.shape)
+    view.copy_(t)
+    return view
+
+
+def run_profile_family(args):
+    import torch
+    from invariant_mhc_aggregate_gb300 import _build, binding
+    from invariant_mhc_aggregate_gb300.inputs import backward_inputs, coeff_inputs, post_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    if args.offset % 2:
+        raise SystemExit("--offset must be even (2-byte elements)")
+    _build.build()
+    binding.load()
+    dev = torch.device("cuda", 0)
+    dtype = torch.bfloat16 if args.dtype == "bf16" else torch.float16
+    T, H, n, fam = args.T, args.H, args.n, args.profile_family
+    sh = lambda t: _shifted(torch, t, args.offset)  # noqa: E731
+    ptrs = lambda *ts: [t.data_ptr() for t in ts]  # noqa: E731
+    if fam in ("post", "post_sigmoid"):
+        x, y, post, res, g = post_inputs(T, H, n, "normal", 6, device=dev, dtype=dtype, with_grad=True)
+        x, y, g = sh(x), sh(y), sh(g)
+        out, gx, gy = sh(torch.empty_like(x)), sh(torch.empty_like(x)), sh(torch.empty_like(y))
+        gp, gr = torch.empty_like(post), torch.empty_like(res)
+        paths = (binding.post_fwd_path_raw(*ptrs(x, y, post, res, out), T, n, H),
+                 binding.post_bwd_path_raw(*ptrs(g, x, y, post, res, gx, gy, gp, gr), T, n, H))
+        if fam == "post":
+            def step():
+                binding.mhc_post_fwd(x, y, post, res, out)
+                binding.mhc_post_bwd(g, x, y, post, res, gx, gy, gp, gr)
+        else:
+            mix, alpha, b = coeff_inputs(T, n, "normal", 7, device=dev)
+            gm = torch.empty_like(mix)
+            gb = torch.empty((n,), dtype=torch.float32, device=dev)
+            ga = torch.empty((1,), dtype=torch.float32, device=dev)
+
+            def step():
+                binding.mhc_post_sigmoid_fwd(x, y, mix, alpha, b, res, out)
+                binding.mhc_post_sigmoid_bwd(g, x, y, mix, alpha, b, res, gx, gy, gp, gm, gr)
+                binding.mhc_sigmoid_param_grad(gp, mix, gb, ga)
+    else:
+        g, res, pre = backward_inputs(T, H, "normal", 4, device=dev, n=n, dtype=dtype)
+        g, res = sh(g), sh(res)
+        out = sh(torch.empty((T, H), dtype=dtype, device=dev))
+        gres = sh(torch.empty((T, n, H), dtype=dtype, device=dev))
+        if fam == "plain":
+            coef = pre
+            gp = torch.empty((T, n), dtype=torch.float32, device=dev)
+
+            def step():
+                binding.mhc_aggregate_fwd(res, pre, out)
+                binding.mhc_aggregate_bwd(g, res, pre, gres, gp)
+        else:
+            mix, alpha, b = coeff_inputs(T, n, "normal", 5, device=dev)
+            coef = mix
+            gp = torch.empty((T, n), dtype=torch.float32, device=dev)
+            gm = torch.empty_like(gp)
+            gb = torch.empty((n,), dtype=torch.float32, device=dev)
+            ga = torch.empty((1,), dtype=torch.float32, device=dev)
+
+            def step():
+                binding.mhc_aggregate_sigmoid_fwd(res, mix, alpha, b, out)
+                binding.mhc_aggregate_sigmoid_bwd(g, res, mix, alpha, b, gres, gp, gm)
+                binding.mhc_sigmoid_param_grad(gp, mix, gb, ga)
+        paths = (binding.agg_fwd_path_raw(*ptrs(res, coef, out), T, n, H),
+                 binding.agg_bwd_path_raw(*ptrs(g, res, coef, gres, gp), T, n, H))
+    step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / max(args.steps, 1)
+    print(f"{fam} T={T} H={H} n={n} {args.dtype} offset={args.offset} paths fwd/bwd="
+          f"{binding.PATH_NAMES[paths[0]]}/{binding.PATH_NAMES[paths[1]]}: {us:.1f} us per step",
+          flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
-    if args.impl == "reference":
+    if args.steps is None:
+        args.steps = 3 if args.profile_family is not None else 8000
+    if args.profile_family is not None:
+        run_profile_family(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
