@@ -610,6 +610,17 @@ __host__ __device__ constexpr uint32_t post_bulk_stage_bytes(int n, uint32_t wid
 // sigmoid.
 constexpr int kPostSlots = 3;
 
+// The producer's check before it fills stage `st` for the `round`-th time:
+// the consumers have released the stage's previous contents ("empty") and
+// every byte of its previous copies has landed ("full"; the consumers waited
+// for that phase already, so in a normal run this costs one poll).  If
+// either wait runs out, the producer issues no further copy: re-arming a
+// transaction barrier whose previous phase is still open, or writing into a
+// stage that copies are still filling, is never done.
+__device__ __forceinline__ bool stage_reusable(uint64_t* full, uint64_t* empty, uint32_t st, uint32_t round) {
+    return mbar_wait(&empty[st], (round - 1) & 1u) && mbar_wait(&full[st], (round - 1) & 1u);
+}
+
 // Threads of a block with `consumers` consumer threads (256, or for rows of
 // fewer than 256 chunks the warps that hold chunks): then the producer warp,
 // then (post from the mix) the helper warp.
@@ -686,10 +697,13 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
         if (threadIdx.x != consumers) return;
         bool ok = true;
         uint32_t item = 0;
-        for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        for (uint64_t t = blockIdx.x; t < T && ok; t += gridDim.x) {
             for (uint32_t s = 0; s < nseg; ++s, ++item) {
                 const uint32_t st = item % STAGES, round = item / STAGES;
-                if (round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1u);
+                if (round > 0 && !stage_reusable(full, empty, st, round)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t c0 = s * kLanes;
                 const uint32_t bytes = (V - c0 < uint32_t(kLanes) ? V - c0 : uint32_t(kLanes)) * 16u;
                 unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N, width);
@@ -946,10 +960,13 @@ post_bwd_split_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict
         if (threadIdx.x != uint32_t(kSplitConsumers)) return;
         bool ok = true;
         uint32_t item = 0;
-        for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        for (uint64_t t = blockIdx.x; t < T && ok; t += gridDim.x) {
             for (uint32_t s = 0; s < nseg; ++s, ++item) {
                 const uint32_t st = item % STAGES, round = item / STAGES;
-                if (round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1u);
+                if (round > 0 && !stage_reusable(full, empty, st, round)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t c0 = s * kLanes;
                 const uint32_t bytes = (V - c0 < uint32_t(kLanes) ? V - c0 : uint32_t(kLanes)) * 16u;
                 unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N);
