@@ -127,8 +127,9 @@ cudaError_t bwd_bulk(const PostBwdCall& c, const Coeffs& k) {
     return bwd_bulk_launch<N, DT, STAGES, MIN_BLOCKS, Coeffs, true>(c, k, uint32_t((V + 31) / 32 * 32));
 }
 
-// Split bulk-copy backward (n = 8): one block of 512 consumer threads and a
-// producer warp per SM, a STAGES-deep ring of (2n + 1) x 4 KB stages.
+// Split bulk-copy backward (n = 8): one block of 512 consumer threads per SM
+// (no producer warp: the warp that frees a stage last refills it), a
+// STAGES-deep ring of (2n + 1) x 4 KB stages.
 template <int N, int DT, int STAGES, class Coeffs>
 cudaError_t bwd_split(const PostBwdCall& c, const Coeffs& k) {
     static std::atomic<uint64_t> smem_done{0};
@@ -139,7 +140,7 @@ cudaError_t bwd_split(const PostBwdCall& c, const Coeffs& k) {
     unsigned int* flag = nullptr;
     if ((e = wait_flag_ptr(&flag)) != cudaSuccess) return e;
     const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms));
-    return launch_smem(kernel, blocks, kSplitConsumers + 32, kSmem, c.stream, static_cast<const Words<4>*>(c.g),
+    return launch_smem(kernel, blocks, kSplitConsumers, kSmem, c.stream, static_cast<const Words<4>*>(c.g),
                        static_cast<const Words<4>*>(c.x), static_cast<const Words<4>*>(c.y), k, c.res,
                        static_cast<Words<4>*>(c.grad_x), static_cast<Words<4>*>(c.grad_y), c.grad_res, c.T,
                        uint32_t(c.H / 8), flag);

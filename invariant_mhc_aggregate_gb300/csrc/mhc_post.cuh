@@ -44,6 +44,7 @@
 #include <stdint.h>
 
 #include "mhc_bulk.cuh"
+#include "mhc_f32x2.cuh"
 
 namespace mhc {
 
@@ -302,12 +303,19 @@ __device__ __forceinline__ uint2 ld_stream_half(const void* p) {
     return v;
 }
 
+// The block table of the split forward, per token: res[t] row-major (n*n),
+// then post[t,k] twice for each k (a packed pair).
+template <int N>
+constexpr int kSplitFwdTable = N * N + 2 * N;
+
 template <int N, int DT, int MIN_BLOCKS, class Coeffs>
 __global__ void __launch_bounds__(kPostBlock, MIN_BLOCKS)
 post_fwd_split_kernel(const Words<4>* __restrict__ x, const Words<4>* __restrict__ y, Coeffs coeffs,
                       const float* __restrict__ res, Words<4>* __restrict__ out, uint32_t n_vec, uint32_t V,
                       FastDivU32 divV) {
-    constexpr int M = N * N + N;
+    static_assert(N == 8, "the packed split forward is written for n = 8");
+    constexpr int M = kSplitFwdTable<N>;
+    constexpr int JP = N / 2;   // input stream pairs
     __shared__ __align__(16) float tab[2][M];
     pdl_enter();
     const uint32_t e = threadIdx.x & 1u;
@@ -316,7 +324,9 @@ post_fwd_split_kernel(const Words<4>* __restrict__ x, const Words<4>* __restrict
     const bool mine = i < n_vec;
     uint32_t tok = 0;
     uint64_t row0 = 0;   // x / out vector of stream 0
-    float xf[N][4], yf[4];
+    // x paired across input streams, xp[jp][p] = {x[2jp](p), x[2jp+1](p)},
+    // and y at positions (0, 1), (2, 3)
+    F2 xp[JP][4], yp[2];
     if (mine) {
         tok = fastdiv_u32(i, divV);
         row0 = uint64_t(N) * tok * V + (i - tok * V);
@@ -325,8 +335,17 @@ post_fwd_split_kernel(const Words<4>* __restrict__ x, const Words<4>* __restrict
         for (int j = 0; j < N; ++j) xw[j] = ld_stream_half(reinterpret_cast<const uint2*>(x + row0 + uint64_t(j) * V) + e);
         const uint2 yw = ld_stream_half(reinterpret_cast<const uint2*>(y + i) + e);
 #pragma unroll
-        for (int j = 0; j < N; ++j) unpack_half<DT>(xw[j], xf[j]);
+        for (int jp = 0; jp < JP; ++jp) {
+            float a[4], b[4];
+            unpack_half<DT>(xw[2 * jp], a);
+            unpack_half<DT>(xw[2 * jp + 1], b);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) xp[jp][p] = f2(a[p], b[p]);
+        }
+        float yf[4];
         unpack_half<DT>(yw, yf);
+        yp[0] = f2(yf[0], yf[1]);
+        yp[1] = f2(yf[2], yf[3]);
     }
     // the block's tokens' coefficients (V >= 128: at most two tokens)
     const uint32_t last = (n_vec - first > uint32_t(kSplitFwdVecs)) ? first + kSplitFwdVecs - 1 : n_vec - 1;
@@ -339,7 +358,7 @@ post_fwd_split_kernel(const Words<4>* __restrict__ x, const Words<4>* __restrict
         if (m < uint32_t(N * N)) {
             v = __ldg(res + uint64_t(N) * N * t + m);
         } else {
-            const int k = int(m) - N * N;
+            const int k = int(m - N * N) / 2;
             if constexpr (Coeffs::kBlockTable) v = coeffs.pre_from(coeffs.mix_at(uint64_t(N) * t + k), k);
             else v = __ldg(coeffs.pre + uint64_t(N) * t + k);
         }
@@ -350,23 +369,29 @@ post_fwd_split_kernel(const Words<4>* __restrict__ x, const Words<4>* __restrict
     const float* ct = tab[tok - t_first];
 #pragma unroll
     for (int k = 0; k < N; ++k) {
-        float rk[N];
+        // {res[k][2jp], res[k][2jp+1]} and {post[k], post[k]}
+        F2 c[JP];
 #pragma unroll
-        for (int j = 0; j < N; j += 4) {
-            const float4 c = *reinterpret_cast<const float4*>(ct + k * N + j);
-            rk[j] = c.x, rk[j + 1] = c.y, rk[j + 2] = c.z, rk[j + 3] = c.w;
+        for (int jp = 0; jp < JP; jp += 2) {
+            const ulonglong2 r = *reinterpret_cast<const ulonglong2*>(ct + k * N + 2 * jp);
+            c[jp].v = r.x, c[jp + 1].v = r.y;
         }
-        const float pk = ct[N * N + k];
-        float o[4];
+        F2 pk;
+        pk.v = *reinterpret_cast<const uint64_t*>(ct + N * N + 2 * k);
+        // post_value at positions (0, 1) and (2, 3): the tree's first level by
+        // scalar adds of each packed product's halves, its upper levels
+        // packed over the position pair, then the post term added by halves
+        F2 o[2];
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            float xs[N];
+        for (int pp = 0; pp < 2; ++pp) {
+            F2 l1[JP];
 #pragma unroll
-            for (int j = 0; j < N; ++j) xs[j] = xf[j][p];
-            o[p] = post_value<N>(rk, pk, xs, yf[p]);
+            for (int jp = 0; jp < JP; ++jp)
+                l1[jp] = f2(padd_halves(pmul(c[jp], xp[jp][2 * pp])), padd_halves(pmul(c[jp], xp[jp][2 * pp + 1])));
+            o[pp] = sadd2(padd(padd(l1[0], l1[1]), padd(l1[2], l1[3])), pmul(pk, yp[pp]));
         }
-        st_stream_half(reinterpret_cast<uint2*>(out + row0 + uint64_t(k) * V) + e, Elem<DT>::pack(o[0], o[1]),
-                       Elem<DT>::pack(o[2], o[3]));
+        st_stream_half(reinterpret_cast<uint2*>(out + row0 + uint64_t(k) * V) + e,
+                       Elem<DT>::pack(f2_lo(o[0]), f2_hi(o[0])), Elem<DT>::pack(f2_lo(o[1]), f2_hi(o[1])));
     }
 }
 
@@ -832,61 +857,84 @@ __device__ __forceinline__ int split_sum_index(uint32_t e, int i) {
     return i < N * NH ? int(e) * NH * N + i : N * N + int(e) * NH + (i - N * NH);
 }
 
-// chunk_partial's subtree over one position half: (g0 x0 + g1 x1) + (g2 x2 + g3 x3)
-__device__ __forceinline__ float half_partial(const float (&g)[4], const float (&x)[4]) {
-    return __fadd_rn(__fadd_rn(__fmul_rn(g[0], x[0]), __fmul_rn(g[1], x[1])),
-                     __fadd_rn(__fmul_rn(g[2], x[2]), __fmul_rn(g[3], x[3])));
-}
-
-// One chunk, position half e: sm = the stage's row 0 at this thread's 8
-// bytes (row r at sm[r * 512]); gx = grad_x row 0 at this thread's 8 bytes
-// (row j at gx[j * rs]); gy likewise for grad_y; `live` = the warp's threads
-// that run it (both threads of each lane).
+// One chunk, position half e, in packed pairs (mhc_f32x2.cuh).  sm = the
+// stage's row 0 at this thread's 8 bytes (row r at sm[r * 2 * kLanes]);
+// tab = the token table (tab[j*n + k] = res[t,k,j], tab[n*n + k] =
+// post[t,k]); gx = grad_x row 0 at this thread's 8 bytes (row j at
+// gx[j * rs]); gy likewise for grad_y; `live` = the warp's threads that run
+// it (both threads of each lane).
+//
+// The g values are paired across streams: go[i][p] = {g[ko + 2i](p),
+// g[ko + 2i + 1](p)} for this thread's own streams ko = n/2 e ..., gt[i][p]
+// for the other half's, at its 4 positions p.  For each input j (j == n:
+// y with post):
+//  * grad_x / grad_y at positions p, p + 1: each coefficient pair times
+//    each g pair (packed products) summed by halves (scalar adds: the
+//    tree's first level, streams 2i + 2i+1), then the tree's upper levels
+//    on position pairs (packed sums); own subtree + other subtree is the
+//    tree's last add.
+//  * the half partials of every (k, j): the 4 products of a g pair with x
+//    duplicated, (p0 + p1) + (p2 + p3) by scalar then packed adds; the
+//    other half's two pairs go to the partner (shuffle), whose own add
+//    completes chunk_partial's last level; acc[j][i] (own streams
+//    ko + 2i, ko + 2i + 1) adds the chunk's partial (packed).
 template <int N, int DT>
 __device__ __forceinline__ void post_split_chunk(const uint2* sm, uint32_t e, const float* tab,
-                                                 float (&acc)[kSplitSums<N>], uint2* gx, uint64_t rs, uint2* gy,
+                                                 F2 (&acc)[N + 1][N / 4], uint2* gx, uint64_t rs, uint2* gy,
                                                  uint32_t live) {
-    constexpr int NH = N / 2;
-    const uint32_t ko = NH * e, kt = NH - ko;   // first stream of this half's k range, of the other's
-    float go[NH][4], gt[NH][4];
+    static_assert(N == 8, "the packed split chunk is written for n = 8");
+    constexpr int NH = N / 2, KP = NH / 2;   // streams per half, stream pairs per half
+    const uint32_t ko = NH * e, kt = NH - ko;   // first own stream, first of the other half
+    F2 go[KP][4], gt[KP][4];
 #pragma unroll
-    for (int kk = 0; kk < NH; ++kk) {
-        unpack_half<DT>(sm[(ko + kk) * 2 * kLanes], go[kk]);
-        unpack_half<DT>(sm[(kt + kk) * 2 * kLanes], gt[kk]);
+    for (int i = 0; i < KP; ++i) {
+        float a[4], b[4], c[4], d[4];
+        unpack_half<DT>(sm[(ko + 2 * i) * 2 * kLanes], a);
+        unpack_half<DT>(sm[(ko + 2 * i + 1) * 2 * kLanes], b);
+        unpack_half<DT>(sm[(kt + 2 * i) * 2 * kLanes], c);
+        unpack_half<DT>(sm[(kt + 2 * i + 1) * 2 * kLanes], d);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            go[i][p] = f2(a[p], b[p]);
+            gt[i][p] = f2(c[p], d[p]);
+        }
     }
 #pragma unroll
     for (int j = 0; j <= N; ++j) {
-        // j < n: input stream j (x row, res column j); j == n: y and post
         const bool is_y = j == N;
         float xf[4];
         unpack_half<DT>(sm[(is_y ? 2 * N : N + j) * 2 * kLanes], xf);
-        float co[NH], ct[NH];
-#pragma unroll
-        for (int kk = 0; kk < NH; kk += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(tab + j * N + ko + kk);
-            const float4 b = *reinterpret_cast<const float4*>(tab + j * N + kt + kk);
-            co[kk] = a.x, co[kk + 1] = a.y, co[kk + 2] = a.z, co[kk + 3] = a.w;
-            ct[kk] = b.x, ct[kk + 1] = b.y, ct[kk + 2] = b.z, ct[kk + 3] = b.w;
+        F2 co[KP], ct[KP];
+        {
+            const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(tab + j * N + ko);
+            const ulonglong2 b = *reinterpret_cast<const ulonglong2*>(tab + j * N + kt);
+            co[0].v = a.x, co[1].v = a.y, ct[0].v = b.x, ct[1].v = b.y;
         }
-        float v[4];
+        // grad_x (grad_y) at positions (0, 1) and (2, 3)
+        F2 v[2];
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            float qo[NH], qt[NH];
+        for (int pp = 0; pp < 2; ++pp) {
+            F2 lo[KP], lt[KP];
 #pragma unroll
-            for (int kk = 0; kk < NH; ++kk) {
-                qo[kk] = __fmul_rn(co[kk], go[kk][p]);
-                qt[kk] = __fmul_rn(ct[kk], gt[kk][p]);
+            for (int i = 0; i < KP; ++i) {
+                lo[i] = f2(padd_halves(pmul(co[i], go[i][2 * pp])), padd_halves(pmul(co[i], go[i][2 * pp + 1])));
+                lt[i] = f2(padd_halves(pmul(ct[i], gt[i][2 * pp])), padd_halves(pmul(ct[i], gt[i][2 * pp + 1])));
             }
-            v[p] = __fadd_rn(tree_sum<NH>(qo), tree_sum<NH>(qt));
+            v[pp] = padd(padd(lo[0], lo[1]), padd(lt[0], lt[1]));
         }
-        const uint32_t w0 = Elem<DT>::pack(v[0], v[1]), w1 = Elem<DT>::pack(v[2], v[3]);
-        st_stream_half(is_y ? gy : gx + uint64_t(j) * rs, w0, w1);
+        st_stream_half(is_y ? gy : gx + uint64_t(j) * rs, Elem<DT>::pack(f2_lo(v[0]), f2_hi(v[0])),
+                       Elem<DT>::pack(f2_lo(v[1]), f2_hi(v[1])));
+        // half partials of (k, j) for every k
+        F2 xd[4];
 #pragma unroll
-        for (int kk = 0; kk < NH; ++kk) {
-            const float own = half_partial(go[kk], xf);
-            const float other = __shfl_xor_sync(live, half_partial(gt[kk], xf), 1);
-            const int i = is_y ? N * NH + kk : kk * N + j;
-            acc[i] = __fadd_rn(acc[i], __fadd_rn(own, other));
+        for (int p = 0; p < 4; ++p) xd[p] = f2(xf[p], xf[p]);
+#pragma unroll
+        for (int i = 0; i < KP; ++i) {
+            const F2 ho = padd(sadd2(pmul(go[i][0], xd[0]), pmul(go[i][1], xd[1])),
+                               sadd2(pmul(go[i][2], xd[2]), pmul(go[i][3], xd[3])));
+            const F2 ht = padd(sadd2(pmul(gt[i][0], xd[0]), pmul(gt[i][1], xd[1])),
+                               sadd2(pmul(gt[i][2], xd[2]), pmul(gt[i][3], xd[3])));
+            acc[j][i] = padd(acc[j][i], padd(ho, shfl_xor_f2(live, ht, 1)));
         }
     }
 }
@@ -924,70 +972,65 @@ __device__ __forceinline__ void split_finish_table(const Coeffs& c, uint32_t m, 
     sync();
 }
 
-// 16 consumer warps and the producer warp: 17 warps put 5 on one SM
-// sub-partition, which caps a thread at 96 registers and leaves the
-// consumers some spills; with 2 stages (139 KB) the shared-memory carve-out
-// leaves room in L1 for them, with 3 most of their reloads went to L2.
+// The block is the 16 consumer warps alone (512 threads, up to 128 registers
+// a thread): there is no producer warp.  The ring's first STAGES items are
+// issued by thread 0 at the start; afterwards the warp that releases a stage
+// last (a shared-memory counter of releasing warps) refills it with the item
+// STAGES ahead, which is the earliest moment any producer could.  Items are
+// the block's (token, segment) pairs in order.
+template <int N>
+__device__ __forceinline__ void split_issue(uint64_t* full, unsigned char* stage_mem, uint32_t item, uint32_t nseg,
+                                            uint32_t stages, const Words<4>* g, const Words<4>* x, const Words<4>* y,
+                                            uint32_t V) {
+    constexpr int R = 2 * N + 1;   // staged rows: g (N), x (N), y
+    const uint32_t st = item % stages;
+    const uint64_t t = blockIdx.x + uint64_t(item / nseg) * gridDim.x;
+    const uint32_t c0 = (item % nseg) * kLanes;
+    const uint32_t bytes = (V - c0 < uint32_t(kLanes) ? V - c0 : uint32_t(kLanes)) * 16u;
+    unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N);
+    mbar_arrive_expect_tx(&full[st], bytes * R);
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+        bulk_copy_g2s(dst + size_t(k) * kLanes * 16, g + (uint64_t(N) * t + k) * V + c0, bytes, &full[st]);
+        bulk_copy_g2s(dst + size_t(N + k) * kLanes * 16, x + (uint64_t(N) * t + k) * V + c0, bytes, &full[st]);
+    }
+    bulk_copy_g2s(dst + size_t(2 * N) * kLanes * 16, y + t * V + c0, bytes, &full[st]);
+}
+
 template <int N, int DT, int STAGES, class Coeffs>
-__global__ void __launch_bounds__(kSplitConsumers + 32, 1)
+__global__ void __launch_bounds__(kSplitConsumers, 1)
 post_bwd_split_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict__ x,
                       const Words<4>* __restrict__ y, Coeffs coeffs, const float* __restrict__ res,
                       Words<4>* __restrict__ grad_x, Words<4>* __restrict__ grad_y,
                       float* __restrict__ grad_res, uint64_t T, uint32_t V, unsigned int* __restrict__ timeouts) {
     static_assert(N % 8 == 0, "the position halves take n/2 streams, read 4 coefficients at a time");
-    constexpr int R = 2 * N + 1;   // staged rows: g (N), x (N), y
     constexpr int M = N * N + N;
-    extern __shared__ __align__(128) unsigned char stage_mem[];   // STAGES * R * 4 KB
+    constexpr uint32_t kWarps = kSplitConsumers / 32;
+    extern __shared__ __align__(128) unsigned char stage_mem[];   // STAGES * (2n + 1) * 4 KB
     __shared__ __align__(8) uint64_t full[STAGES];
-    __shared__ __align__(8) uint64_t empty[STAGES];
-    __shared__ float red[kSplitConsumers / 32][M];
+    __shared__ uint32_t released[STAGES];
+    __shared__ float red[kWarps][M];
     __shared__ __align__(16) float tab[2][kPostTable<N>];   // tokens alternate
     __shared__ float mix[2][N];
+    const uint32_t nseg = (V + kLanes - 1) / kLanes;
+    const uint64_t tokens = T > blockIdx.x ? (T - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const uint32_t items = uint32_t(tokens * nseg);
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kSplitConsumers / 32);
+            released[s] = 0;
         }
         mbar_init_fence();
     }
     __syncthreads();
     pdl_enter();
-    const uint32_t nseg = (V + kLanes - 1) / kLanes;
-
-    if (threadIdx.x >= uint32_t(kSplitConsumers)) {
-        // producer warp: one thread issues the copies
-        if (threadIdx.x != uint32_t(kSplitConsumers)) return;
-        bool ok = true;
-        uint32_t item = 0;
-        for (uint64_t t = blockIdx.x; t < T && ok; t += gridDim.x) {
-            for (uint32_t s = 0; s < nseg; ++s, ++item) {
-                const uint32_t st = item % STAGES, round = item / STAGES;
-                if (round > 0 && !stage_reusable(full, empty, st, round)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t c0 = s * kLanes;
-                const uint32_t bytes = (V - c0 < uint32_t(kLanes) ? V - c0 : uint32_t(kLanes)) * 16u;
-                unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N);
-                mbar_arrive_expect_tx(&full[st], bytes * R);
-#pragma unroll
-                for (int k = 0; k < N; ++k) {
-                    bulk_copy_g2s(dst + size_t(k) * kLanes * 16, g + (uint64_t(N) * t + k) * V + c0, bytes, &full[st]);
-                    bulk_copy_g2s(dst + size_t(N + k) * kLanes * 16, x + (uint64_t(N) * t + k) * V + c0, bytes,
-                                  &full[st]);
-                }
-                bulk_copy_g2s(dst + size_t(2 * N) * kLanes * 16, y + t * V + c0, bytes, &full[st]);
-            }
-        }
-        // every copy issued has landed before the block's shared memory goes
-        for (uint32_t i = item > uint32_t(STAGES) ? item - STAGES : 0; i < item; ++i)
-            if (!mbar_wait(&full[i % STAGES], (i / STAGES) & 1u)) ok = false;
-        if (!ok) *timeouts = 1u;
-        return;
+    if (threadIdx.x == 0) {
+        for (uint32_t i = 0; i < items && i < uint32_t(STAGES); ++i)
+            split_issue<N>(full, stage_mem, i, nseg, STAGES, g, x, y, V);
     }
 
-    // consumers: warp 2q + b, thread 2i + e holds position half e of lane 32q + 2i + b
+    // warp 2q + b, thread 2i + e holds position half e of lane 32q + 2i + b
     const uint32_t w = threadIdx.x >> 5, l = threadIdx.x & 31u;
     const uint32_t e = l & 1u;
     const uint32_t j = 32u * (w >> 1) + (l & ~1u) + (w & 1u);   // the ORDER-256 lane
@@ -1002,9 +1045,11 @@ post_bwd_split_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict
         if (t + gridDim.x < T)
             split_prefetch_table<N>(coeffs, res, t + gridDim.x, threadIdx.x, tab[cur ^ 1u], mix[cur ^ 1u]);
         const float* ttab = tab[cur];
-        float acc[kSplitSums<N>];
+        F2 acc[N + 1][N / 4];
 #pragma unroll
-        for (int i = 0; i < kSplitSums<N>; ++i) acc[i] = 0.0f;
+        for (int jj = 0; jj <= N; ++jj)
+#pragma unroll
+            for (int i = 0; i < N / 4; ++i) acc[jj][i] = f2(0.0f, 0.0f);
 #pragma unroll 1
         for (uint32_t s = 0; s < nseg; ++s, ++item) {
             const uint32_t st = item % STAGES;
@@ -1021,12 +1066,43 @@ post_bwd_split_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict
                 uint2* gy = reinterpret_cast<uint2*>(grad_y + t * V + c) + e;
                 post_split_chunk<N, DT>(sm, e, ttab, acc, gx, 2ull * V, gy, live);
             }
+            // the warp is done with the stage; the last warp to say so refills
+            // it with the item STAGES ahead, once the stage's copies have all
+            // landed (a wait that ran out stops the refills)
             __syncwarp();
-            if (l == 0) mbar_arrive(&empty[st]);
+            if (l == 0) {
+                __threadfence_block();
+                if (atomicInc(&released[st], kWarps - 1) == kWarps - 1 && item + STAGES < items) {
+                    __threadfence_block();
+                    fence_proxy_async_shared();
+                    if (ok && mbar_wait(&full[st], (item / STAGES) & 1u))
+                        split_issue<N>(full, stage_mem, item + STAGES, nseg, STAGES, g, x, y, V);
+                    else
+                        ok = false;
+                }
+            }
         }
-        pair_sums_put<kSplitSums<N>>(acc, l, [&](int i, float v) { red[w][split_sum_index<N>(e, i)] = v; });
+        // the pairs in split_sum_index's order: own stream ko + c of input j
+        // at c * n + j, grad_post of own stream ko + c at n*n/2 + c
+        float flat[kSplitSums<N>];
+#pragma unroll
+        for (int jj = 0; jj <= N; ++jj)
+#pragma unroll
+            for (int i = 0; i < N / 4; ++i) {
+                const int c0 = 2 * i, c1 = 2 * i + 1;
+                flat[jj < N ? c0 * N + jj : N * N / 2 + c0] = f2_lo(acc[jj][i]);
+                flat[jj < N ? c1 * N + jj : N * N / 2 + c1] = f2_hi(acc[jj][i]);
+            }
+        pair_sums_put<kSplitSums<N>>(flat, l, [&](int i, float v) { red[w][split_sum_index<N>(e, i)] = v; });
         post_fold_groups<N>([](int q, int m) { return __fadd_rn(red[2 * q][m], red[2 * q + 1][m]); }, coeffs,
                             ttab + N * N + N, grad_res, t, sync, kGroups, threadIdx.x);
+    }
+    // every copy issued has landed before the block's shared memory goes (in a
+    // normal run the consumers waited for each already)
+    sync();
+    if (threadIdx.x == 0) {
+        for (uint32_t i = items > uint32_t(STAGES) ? items - STAGES : 0; i < items; ++i)
+            if (!mbar_wait(&full[i % STAGES], (i / STAGES) & 1u)) ok = false;
     }
     if (!ok) *timeouts = 1u;
 }

@@ -529,3 +529,49 @@ def test_post_split_launch_beyond_2e31_vectors():
         assert_bytes_equal(u16(out[sl]), want, f"sigmoid post, token {t}")
     del x, y, out, post, res, mix
     torch.cuda.empty_cache()
+
+
+# --- magnitudes around the exact-product check of the fused first level
+
+# (row kind, row index, scale): whole rows scaled by a power of two; FP16
+# cases stay finite (subnormals and underflow to zero, values up to ~2^15)
+MAGNITUDE_CASES = {
+    torch.bfloat16: (("x", 3, 2.0 ** -40), ("x", 5, 2.0 ** -62), ("y", 0, 2.0 ** -66),
+                     ("g", 2, 2.0 ** -75), ("x", 1, 2.0 ** -130), ("g", 6, 2.0 ** 62),
+                     ("x", 0, 2.0 ** 66), ("y", 0, 2.0 ** 100)),
+    torch.float16: (("x", 3, 2.0 ** -8), ("x", 5, 2.0 ** -14), ("y", 0, 2.0 ** -20),
+                    ("g", 2, 2.0 ** -30), ("x", 1, 2.0 ** 4), ("g", 6, 2.0 ** 8),
+                    ("x", 0, 2.0 ** 12), ("y", 0, 2.0 ** 13)),
+}
+
+
+@pytest.mark.parametrize("n", (4, 8))
+@pytest.mark.parametrize("dtype", DTYPES, ids=_ids)
+def test_post_bwd_magnitude_classes(n, dtype):
+    """Blocks of tokens whose g, x or y rows are scaled far from 1 (BF16: into
+    the subnormal range, around the 2^-63 and 2^64 bounds of the check that
+    lets a chunk take the fused first level, and beyond), plus exact zeros and
+    lone extreme values in one position half: every output against the
+    oracle.  The n = 8 kernel takes the fused or the unfused level chunk by
+    chunk; both must give the oracle's bytes."""
+    cases = MAGNITUDE_CASES[dtype]
+    T, H = 8 * len(cases), 2048
+    x, y, post, res, g = post_inputs(T, H, n, "normal", 21, dtype=dtype, with_grad=True)
+    x, y, g = x.float(), y.float(), g.float()
+    rows = {"x": x, "y": y, "g": g}
+    for b, (kind, r, scale) in enumerate(cases):
+        sl = slice(8 * b, 8 * b + 8)
+        if kind == "y":
+            rows[kind][sl] *= scale
+        else:
+            rows[kind][sl, r % n] *= scale
+    # exact zeros, and lone extremes at single positions of otherwise normal rows
+    x[0, 0, ::5] = 0.0
+    g[1, n - 1, 7] = 2.0 ** -100 if dtype == torch.bfloat16 else 2.0 ** -24
+    x[2, 0, 1029] = 2.0 ** 70 if dtype == torch.bfloat16 else 60000.0
+    y[3, 4] = -(2.0 ** -64) if dtype == torch.bfloat16 else 2.0 ** -20
+    x, y, g = (t.to(dtype) for t in (x, y, g))
+    got = run_post_bwd(g, x, y, post, res)
+    want = oracle.default().post_bwd(u16(g), u16(x), u16(y), f32(post), f32(res), DTYPE_NAME[dtype])
+    for a, w, what in zip(got, want, ("grad_x", "grad_y", "grad_post", "grad_res")):
+        assert_bytes_equal(a, w, f"{what} n={n}")
