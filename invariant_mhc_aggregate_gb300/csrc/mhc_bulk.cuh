@@ -3,7 +3,8 @@
 // inline PTX for sm_103a.
 //
 //  * bulk_copy_g2s: one contiguous copy of `bytes` (a multiple of 16, both
-//    addresses 16-byte aligned) that counts its bytes on barrier `bar`.
+//    addresses 16-byte aligned) that counts its bytes on barrier `bar`;
+//    tensor_copy_4d: one box of a tensor map (several rows at once).
 //  * A stage barrier ("full") is armed by its single producer thread with the
 //    number of bytes the stage's copies deliver (arrive_expect_tx); its phase
 //    completes once every byte has landed.  A release barrier ("empty") counts
@@ -14,6 +15,7 @@
 //    error flag set instead of hanging the GPU.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -85,6 +87,21 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         :
         : "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// A tiled copy global -> shared of the box at element coordinates {c0, c1,
+// c2, c3} of a 4-D tensor map (a __grid_constant__ kernel parameter),
+// counting its bytes on barrier `bar`: the whole box, whose elements past
+// the tensor's end read as zero.  c0 (the innermost coordinate) stays a
+// multiple of 16 bytes' worth of elements; dst is 128-byte aligned.
+__device__ __forceinline__ void tensor_copy_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                               uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];"
+        :
+        : "r"(smem_addr(dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
         : "memory");
 }
 

@@ -1,5 +1,7 @@
 // Launches the mHC post kernels with post given (PlainCoeffs), for both
 // storage types, and owns the bounded-wait flag of the bulk-copy kernels.
+#include <cudaTypedefs.h>
+
 #include "mhc_launch_post.cuh"
 
 namespace mhc {
@@ -24,6 +26,35 @@ cudaError_t wait_flag_ptr(unsigned int** p) {
     }
     *p = q;
     return cudaSuccess;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (the
+// library does not link the driver library itself); resolved once.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::atomic<void*> fn{nullptr};
+    void* p = fn.load(std::memory_order_acquire);
+    if (p == nullptr) {
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn.store(p, std::memory_order_release);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+}
+
+cudaError_t encode_rows_map(CUtensorMap* map, const void* base, uint64_t V, uint32_t rows, uint64_t T) {
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr) return cudaErrorInvalidValue;
+    const cuuint64_t dims[4] = {8, V, rows, T};
+    const cuuint64_t strides[3] = {16, V * 16, uint64_t(rows) * V * 16};   // bytes, dimensions 1..3
+    const cuuint32_t box[4] = {8, kLanes, rows, 1};
+    const cuuint32_t step[4] = {1, 1, 1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides, box,
+                              step, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 cudaError_t post_fwd(const PostFwdCall& c, const PlainCoeffs& k, int dtype) {

@@ -977,36 +977,44 @@ __device__ __forceinline__ void split_finish_table(const Coeffs& c, uint32_t m, 
 // issued by thread 0 at the start; afterwards the warp that releases a stage
 // last (a shared-memory counter of releasing warps) refills it with the item
 // STAGES ahead, which is the earliest moment any producer could.  Items are
-// the block's (token, segment) pairs in order.
+// the block's (token, segment) pairs in order.  A stage is three tiled
+// copies, each a box of 256 chunks of a token's rows: g's n rows, x's n rows
+// and y's row (tensor maps of [T][rows][V chunks][8 values]; the boxes of a
+// row's last segment read zeros past its end).  Three copies a stage, not
+// one a row: the count of copies, not their bytes, set the pace (at
+// T = 4096, H = 7168 with two stages: 17 copies of 4 KB a stage 377 us, 34
+// of 2 KB 443 us; with three: 17 copies 380 us, three tiled copies 366 us).
+// A schedule whose two warp halves swap lane halves every token (so that
+// neither idles in a row's last, half-empty round) needed two tiled copies
+// per input a stage and measured 362 us at H = 7168 but 10-13 us more at
+// H = 2048 .. 6144.
 template <int N>
 __device__ __forceinline__ void split_issue(uint64_t* full, unsigned char* stage_mem, uint32_t item, uint32_t nseg,
-                                            uint32_t stages, const Words<4>* g, const Words<4>* x, const Words<4>* y,
-                                            uint32_t V) {
-    constexpr int R = 2 * N + 1;   // staged rows: g (N), x (N), y
+                                            uint32_t stages, const CUtensorMap* g, const CUtensorMap* x,
+                                            const CUtensorMap* y) {
     const uint32_t st = item % stages;
-    const uint64_t t = blockIdx.x + uint64_t(item / nseg) * gridDim.x;
-    const uint32_t c0 = (item % nseg) * kLanes;
-    const uint32_t bytes = (V - c0 < uint32_t(kLanes) ? V - c0 : uint32_t(kLanes)) * 16u;
+    const int t = int(blockIdx.x + (item / nseg) * gridDim.x);
+    const int c0 = int((item % nseg) * kLanes);
     unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N);
-    mbar_arrive_expect_tx(&full[st], bytes * R);
-#pragma unroll
-    for (int k = 0; k < N; ++k) {
-        bulk_copy_g2s(dst + size_t(k) * kLanes * 16, g + (uint64_t(N) * t + k) * V + c0, bytes, &full[st]);
-        bulk_copy_g2s(dst + size_t(N + k) * kLanes * 16, x + (uint64_t(N) * t + k) * V + c0, bytes, &full[st]);
-    }
-    bulk_copy_g2s(dst + size_t(2 * N) * kLanes * 16, y + t * V + c0, bytes, &full[st]);
+    mbar_arrive_expect_tx(&full[st], post_bulk_stage_bytes(N));
+    tensor_copy_4d(dst, g, 0, c0, 0, t, &full[st]);
+    tensor_copy_4d(dst + size_t(N) * kLanes * 16, x, 0, c0, 0, t, &full[st]);
+    tensor_copy_4d(dst + size_t(2 * N) * kLanes * 16, y, 0, c0, 0, t, &full[st]);
 }
 
 template <int N, int DT, int STAGES, class Coeffs>
 __global__ void __launch_bounds__(kSplitConsumers, 1)
-post_bwd_split_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict__ x,
-                      const Words<4>* __restrict__ y, Coeffs coeffs, const float* __restrict__ res,
+post_bwd_split_kernel(const __grid_constant__ CUtensorMap g, const __grid_constant__ CUtensorMap x,
+                      const __grid_constant__ CUtensorMap y, Coeffs coeffs, const float* __restrict__ res,
                       Words<4>* __restrict__ grad_x, Words<4>* __restrict__ grad_y,
                       float* __restrict__ grad_res, uint64_t T, uint32_t V, unsigned int* __restrict__ timeouts) {
     static_assert(N % 8 == 0, "the position halves take n/2 streams, read 4 coefficients at a time");
     constexpr int M = N * N + N;
     constexpr uint32_t kWarps = kSplitConsumers / 32;
-    extern __shared__ __align__(128) unsigned char stage_mem[];   // STAGES * (2n + 1) * 4 KB
+    extern __shared__ __align__(128) unsigned char smem_raw[];   // STAGES * (2n + 1) * 4 KB + 128
+    // tiled copies land on 128-byte boundaries: the ring starts at the first
+    // one in the dynamic allocation (which has 128 bytes to spare)
+    unsigned char* const stage_mem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
     __shared__ __align__(8) uint64_t full[STAGES];
     __shared__ uint32_t released[STAGES];
     __shared__ float red[kWarps][M];
@@ -1027,7 +1035,7 @@ post_bwd_split_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict
     pdl_enter();
     if (threadIdx.x == 0) {
         for (uint32_t i = 0; i < items && i < uint32_t(STAGES); ++i)
-            split_issue<N>(full, stage_mem, i, nseg, STAGES, g, x, y, V);
+            split_issue<N>(full, stage_mem, i, nseg, STAGES, &g, &x, &y);
     }
 
     // warp 2q + b, thread 2i + e holds position half e of lane 32q + 2i + b
@@ -1076,7 +1084,7 @@ post_bwd_split_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict
                     __threadfence_block();
                     fence_proxy_async_shared();
                     if (ok && mbar_wait(&full[st], (item / STAGES) & 1u))
-                        split_issue<N>(full, stage_mem, item + STAGES, nseg, STAGES, g, x, y, V);
+                        split_issue<N>(full, stage_mem, item + STAGES, nseg, STAGES, &g, &x, &y);
                     else
                         ok = false;
                 }
