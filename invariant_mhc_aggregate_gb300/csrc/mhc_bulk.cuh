@@ -82,6 +82,12 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return false;
 }
 
+// mbar_wait with its first poll inline: where the phase has almost always
+// completed already, no call is made.
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity) {
+    return mbar_try_wait(bar, parity) || mbar_wait(bar, parity);
+}
+
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"

@@ -643,7 +643,7 @@ constexpr int kPostSlots = 3;
 // transaction barrier whose previous phase is still open, or writing into a
 // stage that copies are still filling, is never done.
 __device__ __forceinline__ bool stage_reusable(uint64_t* full, uint64_t* empty, uint32_t st, uint32_t round) {
-    return mbar_wait(&empty[st], (round - 1) & 1u) && mbar_wait(&full[st], (round - 1) & 1u);
+    return mbar_wait(&empty[st], (round - 1) & 1u) && mbar_wait_fast(&full[st], (round - 1) & 1u);
 }
 
 // Threads of a block with `consumers` consumer threads (256, or for rows of
@@ -721,14 +721,12 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
         // producer warp: one thread issues the copies
         if (threadIdx.x != consumers) return;
         bool ok = true;
-        uint32_t item = 0;
-        for (uint64_t t = blockIdx.x; t < T && ok; t += gridDim.x) {
+        uint32_t item = 0, issued = 0;
+        for (uint64_t t = blockIdx.x; t < T; t += gridDim.x) {
             for (uint32_t s = 0; s < nseg; ++s, ++item) {
                 const uint32_t st = item % STAGES, round = item / STAGES;
-                if (round > 0 && !stage_reusable(full, empty, st, round)) {
-                    ok = false;
-                    break;
-                }
+                if (round > 0 && ok) ok = stage_reusable(full, empty, st, round);
+                if (!ok) continue;   // after a wait ran out, no copy is issued
                 const uint32_t c0 = s * kLanes;
                 const uint32_t bytes = (V - c0 < uint32_t(kLanes) ? V - c0 : uint32_t(kLanes)) * 16u;
                 unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N, width);
@@ -740,10 +738,11 @@ post_bwd_bulk_kernel(const Words<4>* __restrict__ g, const Words<4>* __restrict_
                                   &full[st]);
                 }
                 bulk_copy_g2s(dst + size_t(2 * N) * width * 16, y + t * V + c0, bytes, &full[st]);
+                issued = item + 1;
             }
         }
         // every copy issued has landed before the block's shared memory goes
-        for (uint32_t i = item > uint32_t(STAGES) ? item - STAGES : 0; i < item; ++i)
+        for (uint32_t i = issued > uint32_t(STAGES) ? issued - STAGES : 0; i < issued; ++i)
             if (!mbar_wait(&full[i % STAGES], (i / STAGES) & 1u)) ok = false;
         if (!ok) *timeouts = 1u;
         return;
@@ -1083,7 +1082,7 @@ post_bwd_split_kernel(const __grid_constant__ CUtensorMap g, const __grid_consta
                 if (atomicInc(&released[st], kWarps - 1) == kWarps - 1 && item + STAGES < items) {
                     __threadfence_block();
                     fence_proxy_async_shared();
-                    if (ok && mbar_wait(&full[st], (item / STAGES) & 1u))
+                    if (ok && mbar_wait_fast(&full[st], (item / STAGES) & 1u))
                         split_issue<N>(full, stage_mem, item + STAGES, nseg, STAGES, &g, &x, &y);
                     else
                         ok = false;
