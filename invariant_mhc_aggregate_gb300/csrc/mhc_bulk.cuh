@@ -128,6 +128,19 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The counter of warps that have released a stage: returns the count before
+// this arrival and wraps to 0 after `last` (atom.inc), with acquire-release
+// ordering at block scope: the warp's earlier shared-memory reads happen
+// before it, and the arrival that sees `last` sees every earlier one's.
+__device__ __forceinline__ uint32_t release_count(uint32_t* counter, uint32_t last) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.inc.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "r"(smem_addr(counter)), "r"(last)
+                 : "memory");
+    return old;
+}
+
 // Barrier over the first `threads` threads of the block (named barrier `id`,
 // 1..15; id 0 is __syncthreads).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads) {

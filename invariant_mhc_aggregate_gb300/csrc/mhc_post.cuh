@@ -1078,9 +1078,7 @@ post_bwd_split_kernel(const __grid_constant__ CUtensorMap g, const __grid_consta
             // landed (a wait that ran out stops the refills)
             __syncwarp();
             if (l == 0) {
-                __threadfence_block();
-                if (atomicInc(&released[st], kWarps - 1) == kWarps - 1 && item + STAGES < items) {
-                    __threadfence_block();
+                if (release_count(&released[st], kWarps - 1) == kWarps - 1 && item + STAGES < items) {
                     fence_proxy_async_shared();
                     if (ok && mbar_wait_fast(&full[st], (item / STAGES) & 1u))
                         split_issue<N>(full, stage_mem, item + STAGES, nseg, STAGES, &g, &x, &y);

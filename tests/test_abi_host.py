@@ -189,9 +189,11 @@ def test_kernels_use_rn_intrinsics_only():
     # one writer per output element: no device atomics or reductions on any
     # output; the only atomic is the bulk-copy ring's shared-memory counter of
     # warps that released a stage
-    atomics = re.findall(r"\batomic[A-Z]\w*\([^,]*", code)
-    assert atomics == ["atomicInc(&released[st]"]
-    assert not re.search(r"\bred\.|\batom\.", code)
+    assert not re.findall(r"\batomic[A-Z]\w*\(", code)
+    assert not re.search(r"\bred\.", code)
+    atoms = re.findall(r"\batom\.[\w.:]+", code)
+    assert atoms == ["atom.acq_rel.cta.shared::cta.inc.u32"]
+    assert code.count("release_count(") == 2   # its definition and the stage ring's one call
 
 
 def test_fastdiv_exhaustive_sample(tmp_path):
