@@ -6,7 +6,8 @@
 // 366).  Summary: residual [T,4,H] BF16, pre [T,4] FP32, out [T,H] BF16,
 //   out = bf16((pre0*r0 + pre1*r1) + (pre2*r2 + pre3*r3)).
 // Batch invariance: one writer per output, no atomics, FP32 __fmul_rn /
-// __fadd_rn, the fixed (0 + 1) + (2 + 3) tree, BF16 only at the boundaries.
+// __fadd_rn in the fixed (0 + 1) + (2 + 3) tree; inputs widened exactly,
+// one rounding to BF16 per output.
 // The backward answers that page's reviewer request; its formula is the exact
 // derivative of the Summary formula and its grad_pre order (ORDER-256) is
 // defined in mhc_h_aggregate.h.  N = 4 with BF16 storage is the pages' op;

@@ -17,9 +17,10 @@
  *     - Summary: shapes residual [T,4,H] BF16, pre [T,4] FP32, output [T,H]
  *       BF16, and the formula
  *         out = bf16((pre0*r0 + pre1*r1) + (pre2*r2 + pre3*r3)).
- *     - Batch invariance: FP32 round-to-nearest multiplies and adds, the fixed
- *       (0 + 1) + (2 + 3) tree, BF16 conversion only at the input and output
- *       boundaries, the two values of a BF16 pair computed independently.
+ *     - Batch invariance: every multiply and add is one binary32
+ *       round-to-nearest operation in the fixed (0 + 1) + (2 + 3) tree; the
+ *       BF16 inputs are widened exactly, and each output is rounded to BF16
+ *       once; each value of a BF16 pair is computed on its own.
  *     - Reviewer comment: asks for the backward of h_aggregate (gradient
  *       accuracy and gradient invariance).  The page gives no backward
  *       formula; the one used here is the exact derivative of the Summary
