@@ -56,8 +56,9 @@
  * memory) allocated and owned by the caller.  The library allocates nothing,
  * keeps no state between calls except a per-thread copy of the last CUDA
  * error code, the per-device record of bounded waits that ran out
- * (mhc_h_aggregate_wait_timeouts) and caches of the device addresses and
- * kernel attributes it needs, and its compute calls never synchronise: each
+ * (mhc_h_aggregate_wait_timeouts) and caches of the device addresses,
+ * kernel attributes and driver entry point (the tensor-map encoder) it needs,
+ * and its compute calls never synchronise: each
  * enqueues kernels on `stream` (NULL = the legacy default stream) and
  * returns.  Calls are safe from several
  * host threads at once.  Kernels are launched with programmatic stream
