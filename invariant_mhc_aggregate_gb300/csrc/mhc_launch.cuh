@@ -191,6 +191,28 @@ cudaError_t launch2d(void (*kernel)(Params...), dim3 grid, uint32_t block, cudaS
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
 }
 
+// The realigned forward: compile-time window offsets (one kernel per H mod 8)
+// for the pages' operation (n = 4, BF16, pre given), run-time offsets for
+// the others.
+template <int N, int DT, int U, class Coeffs>
+cudaError_t fwd_shift_launch(dim3 grid, uint32_t block, const FwdCall& c, const uint16_t* r, const Coeffs& k,
+                             uint16_t* o) {
+    if constexpr (N == 4 && DT == kBF16 && !Coeffs::kBlockTable) {
+        switch (c.H & 7u) {
+            case 0: return launch2d(agg_fwd_shift_kernel<N, DT, U, 0, Coeffs>, grid, block, c.stream, r, k, o, c.T, c.H);
+            case 1: return launch2d(agg_fwd_shift_kernel<N, DT, U, 1, Coeffs>, grid, block, c.stream, r, k, o, c.T, c.H);
+            case 2: return launch2d(agg_fwd_shift_kernel<N, DT, U, 2, Coeffs>, grid, block, c.stream, r, k, o, c.T, c.H);
+            case 3: return launch2d(agg_fwd_shift_kernel<N, DT, U, 3, Coeffs>, grid, block, c.stream, r, k, o, c.T, c.H);
+            case 4: return launch2d(agg_fwd_shift_kernel<N, DT, U, 4, Coeffs>, grid, block, c.stream, r, k, o, c.T, c.H);
+            case 5: return launch2d(agg_fwd_shift_kernel<N, DT, U, 5, Coeffs>, grid, block, c.stream, r, k, o, c.T, c.H);
+            case 6: return launch2d(agg_fwd_shift_kernel<N, DT, U, 6, Coeffs>, grid, block, c.stream, r, k, o, c.T, c.H);
+            default: return launch2d(agg_fwd_shift_kernel<N, DT, U, 7, Coeffs>, grid, block, c.stream, r, k, o, c.T, c.H);
+        }
+    } else {
+        return launch2d(agg_fwd_shift_kernel<N, DT, U, -1, Coeffs>, grid, block, c.stream, r, k, o, c.T, c.H);
+    }
+}
+
 template <int N, int DT, class Coeffs>
 cudaError_t fwd_n(const FwdCall& c, const Coeffs& k) {
     switch (c.path) {
@@ -209,12 +231,10 @@ cudaError_t fwd_n(const FwdCall& c, const Coeffs& k) {
                 const uint64_t nseg = (vecs + 8 * kRun2 - 1) / (8 * kRun2);
                 const uint64_t per_seg = (vecs + nseg - 1) / nseg;
                 const uint32_t warps = uint32_t((per_seg + kRun2 - 1) / kRun2);
-                return launch2d(agg_fwd_shift_kernel<N, DT, 2, Coeffs>, dim3(uint32_t(nseg), tokens),
-                                32 * warps, c.stream, r, k, o, c.T, c.H);
+                return fwd_shift_launch<N, DT, 2>(dim3(uint32_t(nseg), tokens), 32 * warps, c, r, k, o);
             }
             const uint32_t warps = uint32_t((vecs + kShiftWarpVectors - 1) / kShiftWarpVectors);
-            return launch2d(agg_fwd_shift_kernel<N, DT, 1, Coeffs>, dim3(1, tokens), 32 * warps, c.stream,
-                            r, k, o, c.T, c.H);
+            return fwd_shift_launch<N, DT, 1>(dim3(1, tokens), 32 * warps, c, r, k, o);
         }
         case kPathPair: {
             const uint64_t P = c.H / 2;
