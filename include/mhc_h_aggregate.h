@@ -356,14 +356,16 @@ MHC_API const char* mhc_status_string(mhc_status_t status);
 MHC_API int32_t mhc_h_aggregate_last_cuda_error(void);
 
 /* Kernels that stream their inputs through shared memory with bulk copies
- * (the mHC post backward on its 16-byte path) bound every wait for a copy or
- * for a free stage (1 s of the GPU's global timer), so no wait can hang the
- * GPU.  After a wait runs out the block issues no further copy, waits (again
- * bounded) for the copies it has in flight, and runs to its end.  This
- * returns 1 if a wait ran out on the current device since the previous call,
- * else 0, and clears the record; -1 if a CUDA call fails.  It synchronizes
- * the device.  A return of 1 means that the outputs of every mHC post
- * backward call on the device since the previous call are invalid. */
+ * (the mHC post backward on its 16-byte path, and the aggregate backward on
+ * its realigned path for n = 4, BF16, pre given, rows of at least 2041
+ * values and grad_residual at the residual's 16-byte offset) bound every
+ * wait for a copy or for a free stage (1 s of the GPU's global timer), so no
+ * wait can hang the GPU.  After a wait runs out the block issues no further
+ * copy, waits (again bounded) for the copies it has in flight, and runs to
+ * its end.  This returns 1 if a wait ran out on the current device since the
+ * previous call, else 0, and clears the record; -1 if a CUDA call fails.  It
+ * synchronizes the device.  A return of 1 means that the outputs of every
+ * such call on the device since the previous call are invalid. */
 MHC_API int64_t mhc_h_aggregate_wait_timeouts(void);
 
 #ifdef __cplusplus

@@ -29,7 +29,7 @@ SOURCES = [os.path.join(CSRC, f) for f in
             "mhc_launch_post.cu", "mhc_launch_post_sigmoid.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in
                   ("fastdiv.cuh", "mhc_coeffs.cuh", "mhc_device.cuh", "mhc_shift.cuh", "mhc_post.cuh",
-                   "mhc_bulk.cuh", "mhc_f32x2.cuh", "mhc_launch.cuh", "mhc_launch_post.cuh")] \
+                   "mhc_shift_bulk.cuh", "mhc_bulk.cuh", "mhc_f32x2.cuh", "mhc_launch.cuh", "mhc_launch_post.cuh")] \
     + [os.path.join(INCLUDE, "mhc_h_aggregate.h")]
 
 ARCH = "sm_103a"
@@ -68,7 +68,7 @@ def source_digest() -> str:
 
 
 KERNEL_FILES = [os.path.join(CSRC, f) for f in
-                ("mhc_device.cuh", "mhc_coeffs.cuh", "mhc_shift.cuh", "mhc_post.cuh", "mhc_bulk.cuh",
+                ("mhc_device.cuh", "mhc_coeffs.cuh", "mhc_shift.cuh", "mhc_shift_bulk.cuh", "mhc_post.cuh", "mhc_bulk.cuh",
                  "mhc_f32x2.cuh", "fastdiv.cuh", "mhc_launch.cuh", "mhc_launch_post.cuh", "mhc_launch_bf16.cu",
                  "mhc_launch_f16.cu", "mhc_launch_sigmoid_bf16.cu", "mhc_launch_sigmoid_f16.cu",
                  "mhc_launch_coeffs.cu", "mhc_launch_post.cu", "mhc_launch_post_sigmoid.cu")]

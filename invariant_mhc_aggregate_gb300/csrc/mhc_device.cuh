@@ -427,11 +427,23 @@ __device__ __forceinline__ float chunk_partial(const Words<NW>& g, const Words<N
 //
 // A block of fewer than 256/LPT threads (`groups` groups of 32 lanes) stands
 // for the full 256 lanes whose higher lanes hold +0: their group values are
-// +0 in the cross-group fold.
-template <int N, int LPT, class Coeffs>
+// +0 in the cross-group fold.  `sync` is the barrier over the folding
+// threads (the whole block, or the consumer threads of a block with a
+// producer warp), and `tid` the thread's index among them (threadIdx.x if
+// negative).
+// The barrier of the threads that fold a token's lane sums or share its
+// shared-memory tables: the whole block, or (bulk-copy kernels) its consumer
+// threads.
+struct BlockSync {
+    __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+template <int N, int LPT, class Coeffs, class Sync = BlockSync>
 __device__ __forceinline__ void fold_lanes_and_store(float (&acc)[LPT][N], float (*red)[N],
                                                      const Coeffs& coeffs, uint64_t t,
-                                                     const float* slope, int groups = kGroups) {
+                                                     const float* slope, int groups = kGroups,
+                                                     Sync sync = Sync{}, int tid = -1) {
+    const int x = tid < 0 ? int(threadIdx.x) : tid;   // the thread's index among the folding threads
     constexpr int kThreadsPerGroup = 32 / LPT;
 #pragma unroll
     for (int k = 0; k < N; ++k) {
@@ -443,13 +455,13 @@ __device__ __forceinline__ void fold_lanes_and_store(float (&acc)[LPT][N], float
         }
         if (LPT == 2) acc[0][k] = __fadd_rn(acc[0][k], acc[LPT - 1][k]);
     }
-    if ((threadIdx.x % kThreadsPerGroup) == 0) {
+    if ((x % kThreadsPerGroup) == 0) {
 #pragma unroll
-        for (int k = 0; k < N; ++k) red[threadIdx.x / kThreadsPerGroup][k] = acc[0][k];
+        for (int k = 0; k < N; ++k) red[x / kThreadsPerGroup][k] = acc[0][k];
     }
-    __syncthreads();
-    if (threadIdx.x < N) {
-        const int k = threadIdx.x;
+    sync();
+    if (x < N) {
+        const int k = x;
         float w[kGroups];
 #pragma unroll
         for (int i = 0; i < kGroups; ++i) w[i] = (i < groups) ? red[i][k] : 0.0f;
@@ -464,7 +476,7 @@ __device__ __forceinline__ void fold_lanes_and_store(float (&acc)[LPT][N], float
             coeffs.template store_grad<N>(t, k, w[0]);
         }
     }
-    __syncthreads();  // red[] (and the slope table) are reused by the next token of this block
+    sync();  // red[] (and the slope table) are reused by the next token of this block
 }
 
 // Vector path: H % (2*NW) == 0 and g / residual / grad_residual aligned to
@@ -815,3 +827,4 @@ sigmoid_param_grad_kernel(const float* __restrict__ grad_z, const float* __restr
 
 #include "mhc_shift.cuh"
 #include "mhc_post.cuh"
+#include "mhc_shift_bulk.cuh"

@@ -6,9 +6,36 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "mhc_device.cuh"
 
 namespace mhc {
+
+constexpr int kMaxDevices = 64;
+
+inline int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+// Raises a kernel's dynamic shared-memory limit, once per device (`done`
+// holds one bit per device for that kernel).
+template <class K>
+cudaError_t allow_smem(K kernel, uint32_t bytes, std::atomic<uint64_t>& done) {
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << dev;
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+// The device address of the flag that the bulk-copy kernels set when a
+// bounded wait runs out (defined in mhc_launch_post.cu), for the current device.
+cudaError_t wait_flag_ptr(unsigned int** p);
 
 // Kernel path codes (the values of mhc_path_t).
 constexpr int kPathVec16 = 0;
@@ -309,6 +336,37 @@ cudaError_t bwd_vec16(const BwdCall& c, const Coeffs& k) {
     }
 }
 
+// The realigned backward with bulk copies (mhc_shift_bulk.cuh): persistent
+// blocks of 256 consumers and a producer warp, two per SM (96 registers a
+// thread), each with a ring of 3 stages of 21.1 KB.  Measured at T = 4096,
+// H = 7167: 3 stages 84.7 us, 2 stages 91 us, 4 stages 89 us; one block per
+// SM with 4 or 6 stages (no register cap) 94-97 us.
+template <int N, int DT, class Coeffs>
+cudaError_t bwd_shift_bulk(const BwdCall& c, const Coeffs& k) {
+    constexpr int S = 3, B = 2;
+    constexpr uint32_t kSmem = S * shift_bulk_stage_bytes<N>();
+    void (*kernel)(const uint16_t*, const uint16_t*, Coeffs, uint16_t*, uint64_t, uint64_t, unsigned int*);
+    switch (c.H & 7u) {
+        case 0: kernel = agg_bwd_shift_bulk_kernel<N, DT, 0, S, B, Coeffs>; break;
+        case 1: kernel = agg_bwd_shift_bulk_kernel<N, DT, 1, S, B, Coeffs>; break;
+        case 2: kernel = agg_bwd_shift_bulk_kernel<N, DT, 2, S, B, Coeffs>; break;
+        case 3: kernel = agg_bwd_shift_bulk_kernel<N, DT, 3, S, B, Coeffs>; break;
+        case 4: kernel = agg_bwd_shift_bulk_kernel<N, DT, 4, S, B, Coeffs>; break;
+        case 5: kernel = agg_bwd_shift_bulk_kernel<N, DT, 5, S, B, Coeffs>; break;
+        case 6: kernel = agg_bwd_shift_bulk_kernel<N, DT, 6, S, B, Coeffs>; break;
+        default: kernel = agg_bwd_shift_bulk_kernel<N, DT, 7, S, B, Coeffs>; break;
+    }
+    static std::atomic<uint64_t> smem_done[8];
+    cudaError_t e = allow_smem(kernel, kSmem, smem_done[c.H & 7u]);
+    if (e != cudaSuccess) return e;
+    unsigned int* flag = nullptr;
+    if ((e = wait_flag_ptr(&flag)) != cudaSuccess) return e;
+    const uint32_t blocks = uint32_t(c.T < uint64_t(c.num_sms) * B ? c.T : uint64_t(c.num_sms) * B);
+    return launch_smem(kernel, blocks, uint32_t(kLanes + 32), kSmem, c.stream, static_cast<const uint16_t*>(c.g),
+                       static_cast<const uint16_t*>(c.residual), k, static_cast<uint16_t*>(c.gres), c.T, c.H,
+                       flag);
+}
+
 template <int N, int DT, class Coeffs>
 cudaError_t bwd_n(const BwdCall& c, const Coeffs& k) {
     switch (c.path) {
@@ -322,6 +380,11 @@ cudaError_t bwd_n(const BwdCall& c, const Coeffs& k) {
             if (threads < uint32_t(16 * N)) threads = uint32_t(16 * N);
             if (threads < 32u) threads = 32u;
             const uint32_t blocks = grid_for(c.T, 1, uint64_t(c.num_sms) * 256);
+            if constexpr (N == 4 && DT == kBF16 && !Coeffs::kBlockTable) {
+                const bool same_offset =
+                    ((reinterpret_cast<uintptr_t>(c.gres) - reinterpret_cast<uintptr_t>(c.residual)) & 15u) == 0;
+                if (same_offset && chunks >= uint64_t(kLanes)) return bwd_shift_bulk<N, DT>(c, k);
+            }
             if (threads < uint32_t(kLanes))
                 return launch(agg_bwd_shift_kernel<N, DT, Coeffs, true>, blocks, threads, c.stream,
                               static_cast<const uint16_t*>(c.g), static_cast<const uint16_t*>(c.residual), k,

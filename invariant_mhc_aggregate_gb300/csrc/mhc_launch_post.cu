@@ -11,12 +11,12 @@ namespace {
 // Set to 1 when a bounded wait runs out (see mhc_bulk.cuh); one per device.
 __device__ unsigned int g_wait_timeouts;
 
-std::atomic<unsigned int*> g_flag_ptr[post_launch::kMaxDevices];
+std::atomic<unsigned int*> g_flag_ptr[kMaxDevices];
 
 }  // namespace
 
 cudaError_t wait_flag_ptr(unsigned int** p) {
-    const int dev = post_launch::current_device();
+    const int dev = current_device();
     if (dev < 0) return cudaErrorInvalidDevice;
     unsigned int* q = g_flag_ptr[dev].load(std::memory_order_acquire);
     if (q == nullptr) {

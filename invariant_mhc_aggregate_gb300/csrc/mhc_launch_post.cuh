@@ -9,10 +9,6 @@
 
 namespace mhc {
 
-// The device address of the flag that the bulk-copy kernels set when a
-// bounded wait runs out (defined in mhc_launch_post.cu), for the current device.
-cudaError_t wait_flag_ptr(unsigned int** p);
-
 // A tensor map over T tokens of `rows` rows of V 16-byte chunks of 2-byte
 // values (base 16-byte aligned), boxes of 8 values x 256 chunks x `rows`
 // rows x 1 token, elements past the end read as zero (defined in
@@ -20,27 +16,6 @@ cudaError_t wait_flag_ptr(unsigned int** p);
 cudaError_t encode_rows_map(CUtensorMap* map, const void* base, uint64_t V, uint32_t rows, uint64_t T);
 
 namespace post_launch {
-
-constexpr int kMaxDevices = 64;
-
-inline int current_device() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
-    return dev;
-}
-
-// Raises a kernel's dynamic shared-memory limit, once per device (`done`
-// holds one bit per device for that kernel).
-template <class K>
-cudaError_t allow_smem(K kernel, uint32_t bytes, std::atomic<uint64_t>& done) {
-    const int dev = current_device();
-    if (dev < 0) return cudaErrorInvalidDevice;
-    const uint64_t bit = 1ull << dev;
-    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
-    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
-    return e;
-}
 
 // Vector indices are 32-bit: calls of 2^31 vectors or more run as several
 // launches over consecutive token ranges (tokens are independent).

@@ -60,12 +60,6 @@ __device__ __forceinline__ void ld_post_coeffs(const float* post, const float* r
     }
 }
 
-// The barrier of the threads that share a token's shared-memory tables: the
-// whole block, or (bulk kernel) its consumer threads.
-struct BlockSync {
-    __device__ __forceinline__ void operator()() const { __syncthreads(); }
-};
-
 // The coefficients of the token a backward block works on (bulk and 2-byte
 // kernels).  Up to n = 4 they sit in registers (loaded from global memory,
 // or copied from the token table); at n = 8 (72 values, next to 72 lane

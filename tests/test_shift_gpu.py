@@ -52,6 +52,26 @@ def test_every_phase_backward(H):
         assert_bytes_equal(gp, want_gp, f"grad_pre H={H} offsets={offs}")
 
 
+# rows of at least 256 chunks, every H mod 8
+FIXED_HS = (2041, 2046, 2048, 2050, 2052, 2053, 4099, 7167)
+
+
+@pytest.mark.parametrize("H", FIXED_HS)
+def test_backward_residual_offsets_alike(H):
+    """grad_residual at the residual's 16-byte offset (the compile-time window
+    kernel for n = 4, BF16): every offset of g against every offset of the
+    residual, over tokens whose rows step through the phases."""
+    T, n = 5, 4
+    g, res, pre = backward_inputs(T, H, "ragged", 800 + H, n=n)
+    want_gr, want_gp = oracle.aggregate_bwd(u16(g), u16(res), f32(pre), "bf16")
+    for g_off in range(0, 16, 2):
+        for r_off in range(0, 16, 2):
+            offs = (g_off, r_off, 4, r_off, 8)
+            gr, gp = run_agg_bwd(g, res, pre, offs)
+            assert_bytes_equal(gr, want_gr, f"grad_residual H={H} offsets={offs}")
+            assert_bytes_equal(gp, want_gp, f"grad_pre H={H} offsets={offs}")
+
+
 @pytest.mark.parametrize("dtype", (torch.bfloat16, torch.float16), ids=("bf16", "f16"))
 @pytest.mark.parametrize("n", (1, 2, 8))
 def test_streams_and_dtypes(n, dtype):

@@ -12,7 +12,7 @@ import torch
 
 from _gpu import lib
 from invariant_mhc_aggregate_gb300 import _build, binding
-from invariant_mhc_aggregate_gb300.inputs import post_inputs
+from invariant_mhc_aggregate_gb300.inputs import backward_inputs, post_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -62,4 +62,7 @@ def test_library_counts_no_timeouts_in_normal_runs():
     for n in (1, 2, 4):
         x, y, post, res, g = (t.cuda() for t in post_inputs(300, 7168, n, "normal", 12 + n, with_grad=True))
         binding.post_backward(g, x, y, post, res)
+    # the aggregate backward's bulk-copy kernel (odd H)
+    g, res, pre = (t.cuda() for t in backward_inputs(300, 7167, "normal", 16))
+    binding.aggregate_backward(g, res, pre)
     assert binding.wait_timeouts() == 0
