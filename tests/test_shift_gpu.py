@@ -126,3 +126,25 @@ def test_large_odd_h_against_oracle():
     assert_bytes_equal(u16(sgr), wgr, "sigmoid grad_residual")
     assert_bytes_equal(f32(sgz), wgz, "grad_z")
     assert_bytes_equal(f32(sgm), wgm, "grad_mix")
+
+
+@pytest.mark.parametrize("H", (7167, 7166))
+def test_realigned_backward_t4096_every_token(H):
+    """The realigned backward at the benchmark's size (n = 4, BF16: the
+    bulk-copy kernel, whose blocks each walk about 13 tokens through their
+    ring): every output against the oracle, then 1- and 64-token calls, whose
+    row blocks start and end part-way into 16-byte lines (the edge-token
+    handling at every call)."""
+    from test_configs_gpu import bwd_split, by_token_blocks, same_bytes
+    T = 4096
+    g, res, pre = backward_inputs(T, H, "normal", 900 + H)
+    g_d, r_d, p_d = g.cuda(), res.cuda(), pre.cuda()
+    gr, gp = binding.aggregate_backward(g_d, r_d, p_d)
+    torch.cuda.synchronize()
+    want_gr, want_gp = by_token_blocks(oracle.aggregate_bwd, u16(g), u16(res), f32(pre))
+    assert_bytes_equal(u16(gr), want_gr, f"grad_residual H={H}")
+    assert_bytes_equal(f32(gp), want_gp, f"grad_pre H={H}")
+    for chunk in (1, 64):
+        sgr, sgp = bwd_split(g_d, r_d, p_d, chunk)
+        assert same_bytes(sgr, gr), f"grad_residual differs with {chunk}-token calls (H={H})"
+        assert same_bytes(sgp, gp), f"grad_pre differs with {chunk}-token calls (H={H})"
