@@ -40,10 +40,10 @@ cudaError_t fwd_vec(const PostFwdCall& c, const Coeffs& k) {
 
 // Launch shapes (measured at T = 4096, H = 7168): 16-byte vectors, one per
 // thread, with the register budget of 4 blocks per SM (2 at n = 8, whose
-// inputs alone take 36 registers: used for rows of fewer than 128 vectors,
+// inputs alone take 36 registers: used for rows of fewer than 64 vectors,
 // the split forward takes the longer ones); 32-byte vectors, more vectors
 // per thread or fewer blocks per SM were slower.
-// Split forward (n = 8, rows of at least 128 vectors): 128 positions per
+// Split forward (n = 8, rows of at least 64 vectors): 64 positions per
 // block, two threads each.
 template <int N, int DT, int MIN_BLOCKS, class Coeffs>
 cudaError_t fwd_split(const PostFwdCall& c, const Coeffs& k) {
@@ -56,7 +56,7 @@ cudaError_t fwd_split(const PostFwdCall& c, const Coeffs& k) {
         const auto* y = static_cast<const Words<4>*>(c.y) + t0 * V;
         auto* o = static_cast<Words<4>*>(c.out) + uint64_t(N) * t0 * V;
         const cudaError_t e =
-            launch(post_fwd_split_kernel<N, DT, MIN_BLOCKS, Coeffs>, grid_for(n_vec, kSplitFwdVecs, ~0u), kPostBlock,
+            launch(post_fwd_split_kernel<N, DT, MIN_BLOCKS, Coeffs>, grid_for(n_vec, kSplitFwdVecs, ~0u), kSplitFwdBlock,
                    c.stream, x, y, k.shifted(uint64_t(N) * t0), c.res + uint64_t(N) * N * t0, o, n_vec, uint32_t(V),
                    make_fastdiv_u32(uint32_t(V)));
         if (e != cudaSuccess) return e;
@@ -67,7 +67,7 @@ cudaError_t fwd_split(const PostFwdCall& c, const Coeffs& k) {
 template <int N, int DT, class Coeffs>
 cudaError_t fwd_n(const PostFwdCall& c, const Coeffs& k) {
     if constexpr (N >= 8) {
-        if (c.path == kPathVec16 && c.H / 8 >= uint64_t(kSplitFwdVecs)) return fwd_split<N, DT, 4>(c, k);
+        if (c.path == kPathVec16 && c.H / 8 >= uint64_t(kSplitFwdVecs)) return fwd_split<N, DT, kSplitFwdMinBlocks>(c, k);
     }
     if (c.path == kPathVec16) return fwd_vec<N, DT, 4, 1, (N >= 8 ? 2 : 4)>(c, k);
     return launch2d(post_fwd_element_kernel<N, DT, Coeffs>, narrow_grid(c.H, c.T), kNarrowBlock, c.stream,

@@ -270,12 +270,19 @@ post_fwd_vec_kernel(const Words<NW>* __restrict__ x, const Words<NW>* __restrict
 // vectors): two threads per 16-byte position, thread half e taking its
 // positions 4e .. 4e + 3 (8 bytes of each of the n x vectors and of y), so
 // that a thread's unpacked inputs (4n + 4 values) and one output's
-// coefficients fit in few registers and more blocks share an SM.  A block's
-// 128 positions span at most two tokens, whose coefficients (res row-major,
-// then post, computed when post comes from the mix) the block puts in a
-// shared table while its loads are in flight.  Each output value is
+// coefficients fit in few registers and more blocks share an SM: blocks of
+// 128 threads (64 positions), 8 per SM at 64 registers (256-thread blocks
+// 0.6% slower at T = 4096, H = 7168, 512-thread blocks 12%).  A block's
+// positions span at most two tokens (rows of at least 64 vectors), whose
+// coefficients (res row-major, then post, computed when post comes from the
+// mix) the block puts in a shared table while its loads are in flight: with
+// post given, 4-byte asynchronous copies issued before the x loads, so that
+// no thread waits for a coefficient before issuing them (169.6 -> 167.8 us);
+// with post from the mix, computed after them.  Each output value is
 // post_value's: the n-term tree, then the post term.
-constexpr int kSplitFwdVecs = kPostBlock / 2;
+constexpr int kSplitFwdBlock = 128;
+constexpr int kSplitFwdMinBlocks = 8;
+constexpr int kSplitFwdVecs = kSplitFwdBlock / 2;
 
 // The 4 values of 8 bytes of a 2-byte row (2 words, low half first).
 template <int DT>
@@ -303,7 +310,7 @@ template <int N>
 constexpr int kSplitFwdTable = N * N + 2 * N;
 
 template <int N, int DT, int MIN_BLOCKS, class Coeffs>
-__global__ void __launch_bounds__(kPostBlock, MIN_BLOCKS)
+__global__ void __launch_bounds__(kSplitFwdBlock, MIN_BLOCKS)
 post_fwd_split_kernel(const Words<4>* __restrict__ x, const Words<4>* __restrict__ y, Coeffs coeffs,
                       const float* __restrict__ res, Words<4>* __restrict__ out, uint32_t n_vec, uint32_t V,
                       FastDivU32 divV) {
@@ -316,6 +323,19 @@ post_fwd_split_kernel(const Words<4>* __restrict__ x, const Words<4>* __restrict
     const uint32_t first = blockIdx.x * uint32_t(kSplitFwdVecs);
     const uint32_t i = first + (threadIdx.x >> 1);
     const bool mine = i < n_vec;
+    // the block's tokens' coefficients (V >= kSplitFwdVecs: at most two tokens)
+    const uint32_t last = (n_vec - first > uint32_t(kSplitFwdVecs)) ? first + kSplitFwdVecs - 1 : n_vec - 1;
+    const uint32_t t_first = fastdiv_u32(first, divV);
+    const uint32_t count = (fastdiv_u32(last, divV) - t_first + 1) * uint32_t(M);
+    if constexpr (!Coeffs::kBlockTable) {
+        for (uint32_t q = threadIdx.x; q < count; q += kSplitFwdBlock) {
+            const uint32_t tt = q / uint32_t(M), m = q - tt * uint32_t(M);
+            const uint64_t t = uint64_t(t_first) + tt;
+            if (m < uint32_t(N * N)) cp_async4(&tab[tt][m], res + uint64_t(N) * N * t + m);
+            else cp_async4(&tab[tt][m], coeffs.pre + uint64_t(N) * t + int(m - N * N) / 2);
+        }
+        cp_async_commit();
+    }
     uint32_t tok = 0;
     uint64_t row0 = 0;   // x / out vector of stream 0
     // x paired across input streams, xp[jp][p] = {x[2jp](p), x[2jp+1](p)},
@@ -341,22 +361,17 @@ post_fwd_split_kernel(const Words<4>* __restrict__ x, const Words<4>* __restrict
         yp[0] = f2(yf[0], yf[1]);
         yp[1] = f2(yf[2], yf[3]);
     }
-    // the block's tokens' coefficients (V >= 128: at most two tokens)
-    const uint32_t last = (n_vec - first > uint32_t(kSplitFwdVecs)) ? first + kSplitFwdVecs - 1 : n_vec - 1;
-    const uint32_t t_first = fastdiv_u32(first, divV);
-    const uint32_t count = (fastdiv_u32(last, divV) - t_first + 1) * uint32_t(M);
-    for (uint32_t q = threadIdx.x; q < count; q += kPostBlock) {
-        const uint32_t tt = q / uint32_t(M), m = q - tt * uint32_t(M);
-        const uint64_t t = uint64_t(t_first) + tt;
-        float v;
-        if (m < uint32_t(N * N)) {
-            v = __ldg(res + uint64_t(N) * N * t + m);
-        } else {
-            const int k = int(m - N * N) / 2;
-            if constexpr (Coeffs::kBlockTable) v = coeffs.pre_from(coeffs.mix_at(uint64_t(N) * t + k), k);
-            else v = __ldg(coeffs.pre + uint64_t(N) * t + k);
+    if constexpr (Coeffs::kBlockTable) {
+        // post from the mix: the sigmoids are computed once the loads are issued
+        for (uint32_t q = threadIdx.x; q < count; q += kSplitFwdBlock) {
+            const uint32_t tt = q / uint32_t(M), m = q - tt * uint32_t(M);
+            const uint64_t t = uint64_t(t_first) + tt;
+            tab[tt][m] = (m < uint32_t(N * N)) ? __ldg(res + uint64_t(N) * N * t + m)
+                                               : coeffs.pre_from(coeffs.mix_at(uint64_t(N) * t + (m - N * N) / 2),
+                                                                 int(m - N * N) / 2);
         }
-        tab[tt][m] = v;
+    } else {
+        cp_async_wait_all();
     }
     __syncthreads();
     if (!mine) return;

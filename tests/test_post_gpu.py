@@ -94,8 +94,10 @@ FWD_CASES = [
     (9, 8, (0, 0, 0, 0, 0)),           # one 16-byte vector a row
     (3, 1, (0, 0, 0, 0, 0)),           # one value a row
     (1, 2048 + 16, (0, 0, 0, 0, 0)),   # a single token
-    (5, 1024, (0, 0, 0, 0, 0)),        # 128 vectors a row: n = 8's split forward from here on
-    (5, 1016, (0, 0, 0, 0, 0)),        # 127 vectors a row: n = 8's one-thread-per-vector forward
+    (5, 1024, (0, 0, 0, 0, 0)),        # 128 vectors a row
+    (5, 512, (0, 0, 0, 0, 0)),         # 64 vectors a row: n = 8's split forward from here on
+    (5, 504, (0, 0, 0, 0, 0)),         # 63 vectors a row: n = 8's one-thread-per-vector forward
+    (37, 520, (0, 0, 0, 0, 0)),        # 65 vectors a row: split blocks span two tokens
 ]
 
 
