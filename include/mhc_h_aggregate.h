@@ -115,7 +115,9 @@ typedef enum mhc_path {
     MHC_PATH_SHIFT16 = 4  /* 16-byte loads/stores at each row's own alignment, realigned in
                              registers, for 64 <= H < 2^30 when no vector path applies
                              (the forward leaves even H with 4-byte-aligned buffers to
-                             the PAIR path) */
+                             the PAIR path; the backward for n = 4, BF16, pre given,
+                             H >= 2041 and grad_residual at the residual's 16-byte
+                             offset stages its rows in shared memory with bulk copies) */
 } mhc_path_t;
 
 /* Version of this ABI; changes when a declaration here changes. */
