@@ -44,12 +44,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
 }
 
-cudaError_t encode_rows_map(CUtensorMap* map, const void* base, uint64_t V, uint32_t rows, uint64_t T) {
+cudaError_t encode_rows_map(CUtensorMap* map, const void* base, uint64_t H, uint32_t W, uint32_t rows, uint64_t T) {
     const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-    if (encode == nullptr) return cudaErrorInvalidValue;
-    const cuuint64_t dims[4] = {8, V, rows, T};
-    const cuuint64_t strides[3] = {16, V * 16, uint64_t(rows) * V * 16};   // bytes, dimensions 1..3
-    const cuuint32_t box[4] = {8, kLanes, rows, 1};
+    if (encode == nullptr || W == 0 || H % W != 0) return cudaErrorInvalidValue;
+    const cuuint64_t dims[4] = {W, H / W, rows, T};
+    const cuuint64_t strides[3] = {uint64_t(W) * 2, H * 2, uint64_t(rows) * H * 2};   // bytes, dimensions 1..3
+    const cuuint32_t box[4] = {W, uint32_t(8 * kLanes) / W, rows, 1};
     const cuuint32_t step[4] = {1, 1, 1, 1};
     const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides, box,
                               step, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

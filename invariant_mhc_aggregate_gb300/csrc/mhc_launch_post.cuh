@@ -9,11 +9,24 @@
 
 namespace mhc {
 
-// A tensor map over T tokens of `rows` rows of V 16-byte chunks of 2-byte
-// values (base 16-byte aligned), boxes of 8 values x 256 chunks x `rows`
-// rows x 1 token, elements past the end read as zero (defined in
+// A tensor map over T tokens of `rows` rows of H 2-byte values (base 16-byte
+// aligned) seen as groups of W values (W divides H): boxes of W values x
+// 2048 / W groups x `rows` rows x 1 token, i.e. 2048 consecutive values of
+// each row, elements past the row's end reading as zero (defined in
 // mhc_launch_post.cu; cudaErrorInvalidValue if the driver refuses it).
-cudaError_t encode_rows_map(CUtensorMap* map, const void* base, uint64_t V, uint32_t rows, uint64_t T);
+cudaError_t encode_rows_map(CUtensorMap* map, const void* base, uint64_t H, uint32_t W, uint32_t rows, uint64_t T);
+
+#ifndef MHC_SPLIT_MAX_BOX_ROW
+#define MHC_SPLIT_MAX_BOX_ROW 256
+#endif
+
+// The widest box row (values) that divides H: the copy engine moves a box
+// row by row, so wider rows mean fewer of them for the same bytes.
+inline uint32_t split_box_row(uint64_t H) {
+    uint32_t W = MHC_SPLIT_MAX_BOX_ROW;
+    while (W > 8 && H % W != 0) W /= 2;
+    return W;
+}
 
 namespace post_launch {
 
@@ -124,21 +137,22 @@ cudaError_t bwd_split(const PostBwdCall& c, const Coeffs& k) {
     unsigned int* flag = nullptr;
     if ((e = wait_flag_ptr(&flag)) != cudaSuccess) return e;
     const uint64_t V = c.H / 8;
+    const uint32_t W = split_box_row(c.H);
     constexpr uint64_t kMaxTokens = 0x7FFFFFFFull;
     for (uint64_t t0 = 0; t0 < c.T; t0 += kMaxTokens) {
         const uint64_t nt = (c.T - t0 < kMaxTokens) ? c.T - t0 : kMaxTokens;
         CUtensorMap mg, mx, my;
-        if ((e = encode_rows_map(&mg, static_cast<const uint16_t*>(c.g) + uint64_t(N) * t0 * c.H, V, N, nt)) !=
+        if ((e = encode_rows_map(&mg, static_cast<const uint16_t*>(c.g) + uint64_t(N) * t0 * c.H, c.H, W, N, nt)) !=
                 cudaSuccess ||
-            (e = encode_rows_map(&mx, static_cast<const uint16_t*>(c.x) + uint64_t(N) * t0 * c.H, V, N, nt)) !=
+            (e = encode_rows_map(&mx, static_cast<const uint16_t*>(c.x) + uint64_t(N) * t0 * c.H, c.H, W, N, nt)) !=
                 cudaSuccess ||
-            (e = encode_rows_map(&my, static_cast<const uint16_t*>(c.y) + t0 * c.H, V, 1, nt)) != cudaSuccess)
+            (e = encode_rows_map(&my, static_cast<const uint16_t*>(c.y) + t0 * c.H, c.H, W, 1, nt)) != cudaSuccess)
             return e;
         const uint32_t blocks = grid_for(nt, 1, uint64_t(c.num_sms));
         e = launch_smem(kernel, blocks, kSplitConsumers, kSmem, c.stream, mg, mx, my, k.shifted(uint64_t(N) * t0),
                         c.res + uint64_t(N) * N * t0, static_cast<Words<4>*>(c.grad_x) + uint64_t(N) * t0 * V,
                         static_cast<Words<4>*>(c.grad_y) + t0 * V, c.grad_res + uint64_t(N) * N * t0, nt, uint32_t(V),
-                        flag);
+                        W, flag);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -986,12 +986,18 @@ __device__ __forceinline__ void split_finish_table(const Coeffs& c, uint32_t m, 
 // last (a shared-memory counter of releasing warps) refills it with the item
 // STAGES ahead, which is the earliest moment any producer could.  Items are
 // the block's (token, segment) pairs in order.  A stage is three tiled
-// copies, each a box of 256 chunks of a token's rows: g's n rows, x's n rows
-// and y's row (tensor maps of [T][rows][V chunks][8 values]; the boxes of a
-// row's last segment read zeros past its end).  Three copies a stage, not
-// one a row: the count of copies, not their bytes, set the pace (at
-// T = 4096, H = 7168 with two stages: 17 copies of 4 KB a stage 377 us, 34
-// of 2 KB 443 us; with three: 17 copies 380 us, three tiled copies 366 us).
+// copies, each a box of 2048 consecutive values (256 chunks) of a token's
+// rows: g's n rows, x's n rows and y's row (tensor maps of
+// [T][rows][H / W groups][W values], W the widest of 256, 128, ..., 8 that
+// divides H; the boxes of a row's last segment read zeros past its end).
+// The copy engine set the pace, not the arithmetic: it works through a box
+// row by row, and with 16-byte rows (W = 8) a stage is about 4000 of them
+// (T = 4096, H = 7168: W = 8 366 us, W = 64 or 256 336 us; with W = 8,
+// removing 45% of the FP32 work gained 5 us, and an L2 prefetch of the next
+// items through the same tensor maps doubled the time).  Three copies a
+// stage, not one a row: with linear copies the count set the pace (two
+// stages: 17 copies of 4 KB a stage 377 us, 34 of 2 KB 443 us; three stages:
+// 17 copies 380 us).
 // A schedule whose two warp halves swap lane halves every token (so that
 // neither idles in a row's last, half-empty round) needed two tiled copies
 // per input a stage and measured 362 us at H = 7168 but 10-13 us more at
@@ -999,10 +1005,10 @@ __device__ __forceinline__ void split_finish_table(const Coeffs& c, uint32_t m, 
 template <int N>
 __device__ __forceinline__ void split_issue(uint64_t* full, unsigned char* stage_mem, uint32_t item, uint32_t nseg,
                                             uint32_t stages, const CUtensorMap* g, const CUtensorMap* x,
-                                            const CUtensorMap* y) {
+                                            const CUtensorMap* y, uint32_t W) {
     const uint32_t st = item % stages;
     const int t = int(blockIdx.x + (item / nseg) * gridDim.x);
-    const int c0 = int((item % nseg) * kLanes);
+    const int c0 = int((item % nseg) * (8u * kLanes / W));   // the segment's first group of W values
     unsigned char* dst = stage_mem + size_t(st) * post_bulk_stage_bytes(N);
     mbar_arrive_expect_tx(&full[st], post_bulk_stage_bytes(N));
     tensor_copy_4d(dst, g, 0, c0, 0, t, &full[st]);
@@ -1015,7 +1021,8 @@ __global__ void __launch_bounds__(kSplitConsumers, 1)
 post_bwd_split_kernel(const __grid_constant__ CUtensorMap g, const __grid_constant__ CUtensorMap x,
                       const __grid_constant__ CUtensorMap y, Coeffs coeffs, const float* __restrict__ res,
                       Words<4>* __restrict__ grad_x, Words<4>* __restrict__ grad_y,
-                      float* __restrict__ grad_res, uint64_t T, uint32_t V, unsigned int* __restrict__ timeouts) {
+                      float* __restrict__ grad_res, uint64_t T, uint32_t V, uint32_t W,
+                      unsigned int* __restrict__ timeouts) {
     static_assert(N % 8 == 0, "the position halves take n/2 streams, read 4 coefficients at a time");
     constexpr int M = N * N + N;
     constexpr uint32_t kWarps = kSplitConsumers / 32;
@@ -1043,7 +1050,7 @@ post_bwd_split_kernel(const __grid_constant__ CUtensorMap g, const __grid_consta
     pdl_enter();
     if (threadIdx.x == 0) {
         for (uint32_t i = 0; i < items && i < uint32_t(STAGES); ++i)
-            split_issue<N>(full, stage_mem, i, nseg, STAGES, &g, &x, &y);
+            split_issue<N>(full, stage_mem, i, nseg, STAGES, &g, &x, &y, W);
     }
 
     // warp 2q + b, thread 2i + e holds position half e of lane 32q + 2i + b
@@ -1090,7 +1097,7 @@ post_bwd_split_kernel(const __grid_constant__ CUtensorMap g, const __grid_consta
                 if (release_count(&released[st], kWarps - 1) == kWarps - 1 && item + STAGES < items) {
                     fence_proxy_async_shared();
                     if (ok && mbar_wait_fast(&full[st], (item / STAGES) & 1u))
-                        split_issue<N>(full, stage_mem, item + STAGES, nseg, STAGES, &g, &x, &y);
+                        split_issue<N>(full, stage_mem, item + STAGES, nseg, STAGES, &g, &x, &y, W);
                     else
                         ok = false;
                 }
