@@ -20,14 +20,19 @@
 // second load instruction finds its lines in L1 (or in flight there).
 // Measured at H = 7167: shuffles are faster for the forward (46 against
 // 55 us), paired loads for the backward (87 against 97 us; the shuffle
-// version also needed a 9-warp block and a shared-memory fold).
+// version also needed a 9-warp block and a shared-memory fold).  For the
+// pages' operation (n = 4, BF16, pre given) the forward fixes its window
+// offsets at compile time (42.8 us), and the backward, when grad_residual
+// sits at the residual's 16-byte offset and rows hold at least 256 chunks,
+// is the bulk-copy kernel of mhc_shift_bulk.cuh (84.7 us).
 // Outputs are written with aligned 16-byte stores when the whole vector lies
 // in the row; the at most 7 + 7 values at the row's two ends are computed and
 // stored one by one.  Loads stay inside the buffer (a vector not wholly
 // inside it, only at the buffer's ends, is read value by value), and no store
-// leaves the row.  The data is not staged through shared memory; the only
-// block barriers publish a token's sigmoid coefficients (when pre is computed
-// from the mix) and fold the backward's lane sums, once per token.
+// leaves the row.  These kernels do not stage data through shared memory;
+// the only block barriers publish a token's sigmoid coefficients (when pre
+// is computed from the mix) and fold the backward's lane sums, once per
+// token.
 //
 // The kernels run the same per-element arithmetic, the same per-lane
 // ORDER-256 chunks and the same fold as every other path, so the bytes are
