@@ -124,6 +124,12 @@ BWD_CASES = [
     (3, 1, (0,) * 9),
     (1, 2048 * 8 + 8, (0,) * 9),                       # long row: 8+ chunks a lane
     (3, 8 * (256 + 37), (0,) * 9),                     # last segment ends inside a warp's lanes
+    # n = 8 tensor maps group a row in the widest power of two up to 256
+    # that divides H: 16, 32, 64 and 128 values here (256 and 8 above)
+    (3, 4112, (0,) * 9),
+    (3, 2080, (0,) * 9),
+    (3, 2112, (0,) * 9),
+    (3, 2176, (0,) * 9),
 ]
 
 
